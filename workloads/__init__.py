@@ -1,0 +1,130 @@
+"""Seeded synthetic inputs for exact attention forward.
+
+This module holds no attention arithmetic: it only draws random tensors and
+packs them.  Both the fp64 oracle (test infrastructure) and the CUDA path are
+fed from here, so the two sides always see identical bf16 inputs.
+
+Recipe (the pages only say "i.i.d. N(0,1) from seed 0"; this is the reading
+taken): a CPU ``torch.Generator`` seeded with ``seed`` draws Q, then K, then V
+with ``torch.randn(..., dtype=float32)``; Q is multiplied by ``q_mult``; all
+three are then rounded to bf16 (round-to-nearest-even).  The oracle consumes
+the rounded bf16 values, so input quantisation is not counted as error.
+
+Variable-length batches draw their lengths with
+``torch.randint(lo, hi + 1, (n,))`` from a generator seeded with ``seed``
+("uniform on [lo, hi]", read as inclusive) and pack sequences token-major,
+``[total_tokens, heads, D]``, with int32 prefix offsets ``cu_seqlens``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One attention-forward problem: shapes, mask and input recipe."""
+
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Lq: int
+    Lk: int
+    D: int
+    causal: bool
+    q_mult: float = 1.0
+    seed: int = 0
+    # variable-length batches: per-sequence lengths (Lq/Lk above are unused)
+    seqlens: tuple[int, ...] | None = None
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def varlen(self) -> bool:
+        return self.seqlens is not None
+
+    def flops(self) -> float:
+        """Matrix FLOPs of the forward: 4*Lq*Lk*D per head, halved when causal.
+
+        This is the accounting of the benchmark spec's metric (multiply and add
+        counted separately; the causal half ignores the diagonal's extra half
+        tile).
+        """
+        if self.varlen:
+            total = sum(4.0 * self.Hq * L * L * self.D for L in self.seqlens)
+        else:
+            total = 4.0 * self.B * self.Hq * self.Lq * self.Lk * self.D
+        return total / 2 if self.causal else total
+
+
+def varlen_lengths(n: int = 8, lo: int = 512, hi: int = 8192, seed: int = 0) -> list[int]:
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi + 1, (n,), generator=g).tolist()
+
+
+def _bf16(x: torch.Tensor) -> torch.Tensor:
+    return x.to(torch.bfloat16)
+
+
+def dense_inputs(w: Workload):
+    """Q [B,Hq,Lq,D], K and V [B,Hkv,Lk,D], bf16 on the CPU."""
+    assert not w.varlen
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn((w.B, w.Hq, w.Lq, w.D), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.Hkv, w.Lk, w.D), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.Hkv, w.Lk, w.D), generator=g, dtype=torch.float32)
+    if w.q_mult != 1.0:
+        q = q * w.q_mult
+    return _bf16(q), _bf16(k), _bf16(v)
+
+
+def varlen_inputs(w: Workload):
+    """Packed Q [Tq,Hq,D], K and V [Tk,Hkv,D] (bf16) and int32 cu_seqlens.
+
+    Query and key lengths are equal per sequence (self-attention prefill).
+    """
+    assert w.varlen
+    lens = list(w.seqlens)
+    total = sum(lens)
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn((total, w.Hq, w.D), generator=g, dtype=torch.float32)
+    k = torch.randn((total, w.Hkv, w.D), generator=g, dtype=torch.float32)
+    v = torch.randn((total, w.Hkv, w.D), generator=g, dtype=torch.float32)
+    if w.q_mult != 1.0:
+        q = q * w.q_mult
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    return _bf16(q), _bf16(k), _bf16(v), cu, cu.clone()
+
+
+def random_inputs(shape_q, shape_k, seed: int, q_mult: float = 1.0):
+    """Generic seeded bf16 triple for edge-case tests with arbitrary shapes."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(shape_q, generator=g, dtype=torch.float32) * q_mult
+    k = torch.randn(shape_k, generator=g, dtype=torch.float32)
+    v = torch.randn(shape_k, generator=g, dtype=torch.float32)
+    return _bf16(q), _bf16(k), _bf16(v)
+
+
+_VARLEN_LENS = tuple(varlen_lengths(8, 512, 8192, seed=0))
+
+# The five workloads of the headline benchmark.  Names say what they are.
+WORKLOADS: dict[str, Workload] = {
+    "b1_h1_l128_d64": Workload("b1_h1_l128_d64", 1, 1, 1, 128, 128, 64, False),
+    "b4_h16_l1024_d64": Workload("b4_h16_l1024_d64", 4, 16, 16, 1024, 1024, 64, False),
+    "b4_h16_l1024_d64_causal": Workload("b4_h16_l1024_d64_causal", 4, 16, 16, 1024, 1024, 64, True),
+    "gqa_b2_h32x8_l4096_d128_causal_q3": Workload(
+        "gqa_b2_h32x8_l4096_d128_causal_q3", 2, 32, 8, 4096, 4096, 128, True, q_mult=3.0),
+    "b1_h16_l16384_d128": Workload("b1_h16_l16384_d128", 1, 16, 16, 16384, 16384, 128, False),
+    "b1_h16_l16384_d128_causal": Workload("b1_h16_l16384_d128_causal", 1, 16, 16, 16384, 16384, 128, True),
+    "varlen8_h32x8_d128_causal": Workload(
+        "varlen8_h32x8_d128_causal", 8, 32, 8, 0, 0, 128, True, seqlens=_VARLEN_LENS),
+}
+
+# The configuration the throughput metric is quoted on.
+HEADLINE = "b1_h16_l16384_d128"

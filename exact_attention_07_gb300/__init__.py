@@ -1,0 +1,162 @@
+"""Exact attention forward on GB300 (sm_103a): Python binding of libfa_gb300.
+
+The functions here only marshal arguments (tensor pointers, sizes, the
+current CUDA stream) into the C ABI declared in ``include/fa_gb300.h``; every
+step of the computation runs in the library's CUDA kernels.  There is no CPU
+or eager-PyTorch fallback: if the library is missing or the device is not an
+sm_103 GPU the call raises.
+
+    o, lse = fa_fwd(q, k, v, causal=True)          # q [B,Hq,Lq,D], k/v [B,Hkv,Lk,D]
+    o, lse = fa_fwd_varlen(q, k, v, cu_q, cu_k, max_q, max_k, causal=True)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_check", "fa_status_string", "fa_last_launch_count",
+           "FAError", "library_path", "load_library", "EXPORTED_SYMBOLS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
+_lock = threading.Lock()
+_lib = None
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_check", "fa_status_string", "fa_last_launch_count")
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libfa_gb300.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build the CUDA library first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fa_fwd.restype = i
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+        lib.fa_fwd_varlen.restype = i
+        lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
+        lib.fa_check.restype = i
+        lib.fa_check.argtypes = [vp]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_last_launch_count.restype = i
+        lib.fa_last_launch_count.argtypes = []
+        _lib = lib
+        return lib
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_last_launch_count() -> int:
+    return int(load_library().fa_last_launch_count())
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+           softmax_scale: float | None = None, out: torch.Tensor | None = None,
+           lse: torch.Tensor | None = None, stream=None):
+    """Dense attention forward.  q [B,Hq,Lq,D], k/v [B,Hkv,Lk,D] bf16 CUDA.
+
+    Returns (o [B,Hq,Lq,D] bf16, lse [B,Hq,Lq] fp32).  Asynchronous on the
+    current (or given) stream.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, torch.bfloat16, 4)
+    B, Hq, Lq, D = q.shape
+    Bk, Hkv, Lk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    _check_tensor(out, "out", torch.bfloat16, 4)
+    _check_tensor(lse, "lse", torch.float32, 3)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                        B, Hq, Hkv, Lq, Lk, D, int(bool(causal)), float(softmax_scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd")
+    return out, lse
+
+
+def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                  cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, causal: bool = False,
+                  softmax_scale: float | None = None, out: torch.Tensor | None = None,
+                  lse: torch.Tensor | None = None, stream=None):
+    """Packed variable-length forward.  q [Tq,Hq,D], k/v [Tk,Hkv,D] bf16 CUDA,
+    cu_seqlens_* int32 CUDA [num_seqs+1].  Returns (o [Tq,Hq,D], lse [Hq,Tq])."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, torch.bfloat16, 3)
+    _check_tensor(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check_tensor(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    Tq, Hq, D = q.shape
+    Tk, Hkv, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Dk != D or cu_seqlens_q.numel() != cu_seqlens_k.numel():
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), cu_seqlens_q.numel() - 1,
+                               Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, int(bool(causal)),
+                               float(softmax_scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_varlen")
+    return out, lse
+
+
+def fa_check(stream=None) -> int:
+    """Synchronise the stream and raise if a kernel latched an error."""
+    st = load_library().fa_check(_stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_check")
+    return st

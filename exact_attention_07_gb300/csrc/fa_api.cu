@@ -1,0 +1,338 @@
+// C ABI of the attention library: argument validation, tensor-map encoding,
+// scheduling and launch.  Declarations and contracts: include/fa_gb300.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa_gb300.h"
+#include "fa_launch.h"
+#include "fa_params.h"
+
+namespace fa {
+
+// Device-side error latch: bit 0 = a pipeline wait timed out, bit 1 = invalid
+// variable-length offsets.  g_diag keeps the first failing wait site.
+__device__ int g_err;
+__device__ int g_diag[4];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+// Share of the 126 MB L2 that one scheduling section's K/V may occupy.
+constexpr long long kL2SectionBytes = 48ll << 20;
+
+struct DeviceState {
+    bool ready = false;
+    fa_status_t status = FA_OK;
+    int num_sms = 0;
+    int* err = nullptr;
+    int* diag = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+thread_local int g_last_launches = 0;
+
+fa_status_t device_state(DeviceState** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& s = g_dev[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        if (major != 10 || minor != 3) {
+            s.status = FA_ERR_UNSUPPORTED;  // kernels are built for sm_103a only
+        } else {
+            if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_err) != cudaSuccess ||
+                cudaGetSymbolAddress(reinterpret_cast<void**>(&s.diag), g_diag) != cudaSuccess)
+                return FA_ERR_CUDA;
+            if (!g_encode) {
+                cudaDriverEntryPointQueryResult q;
+                void* fn = nullptr;
+                if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                                     &q) != cudaSuccess ||
+                    q != cudaDriverEntryPointSuccess || !fn)
+                    return FA_ERR_CUDA;
+                g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            }
+        }
+        s.ready = true;
+    }
+    *out = &s;
+    return s.status;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D bf16 tensor map with 128-byte swizzle: box = {64, box1, box2} elements.
+bool encode_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1, uint32_t box2)
+{
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {64, box1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int heads_per_section(int Hkv, long long Lk, int D)
+{
+    const long long kv_bytes = 2ll * Lk * D * 2;  // K and V of one KV head
+    long long hs = kv_bytes > 0 ? kL2SectionBytes / kv_bytes : Hkv;
+    if (hs < 1) hs = 1;
+    if (hs > Hkv) hs = Hkv;
+    return (int)hs;
+}
+
+template <bool VARLEN>
+cudaError_t dispatch(int D, bool causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                     const FwdParams& p, int grid, cudaStream_t st)
+{
+    if (D == 64)
+        return causal ? launch_fwd<64, true, VARLEN>(q, k, v, p, grid, st)
+                      : launch_fwd<64, false, VARLEN>(q, k, v, p, grid, st);
+    return causal ? launch_fwd<128, true, VARLEN>(q, k, v, p, grid, st)
+                  : launch_fwd<128, false, VARLEN>(q, k, v, p, grid, st);
+}
+
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+}  // namespace
+
+// --------------------------------------------------------------- varlen schedule
+
+// One CTA of 1024 threads.  Validates the offsets, orders sequences longest
+// key range first (the longest work tile of a sequence visits ceil(Lk/128)
+// KV tiles; FlashAttention-4 notes, "LPT scheduling", step 4) and writes the
+// exclusive prefix of work tiles in that order.
+//
+// sched layout (int32): [0] total tiles | [1 .. n+1] prefix by schedule rank |
+// [n+2 .. 2n+1] order (rank -> sequence) | [2n+2 .. 3n+1] tiles by sequence.
+constexpr int kSchedThreads = 1024;
+constexpr int kSortMax = 4096;
+
+__global__ void __launch_bounds__(kSchedThreads)
+    fa_varlen_schedule_kernel(const int* __restrict__ cu_q, const int* __restrict__ cu_k, int n, int total_q,
+                              int total_k, int max_q, int max_k, int Hq, int* __restrict__ sched,
+                              int* __restrict__ err)
+{
+    __shared__ int key[kSortMax];
+    __shared__ int part[kSchedThreads];
+    __shared__ int bad;
+    const int tid = threadIdx.x;
+    int* prefix = sched + 1;
+    int* order = sched + 2 + n;
+    int* tiles = sched + 2 + 2 * n;
+    if (tid == 0) bad = (cu_q[0] != 0 || cu_k[0] != 0 || cu_q[n] != total_q || cu_k[n] != total_k) ? 1 : 0;
+    __syncthreads();
+    // per-sequence check; an invalid sequence is scheduled with no work
+    for (int s = tid; s < n; s += kSchedThreads) {
+        const int q0 = cu_q[s], q1 = cu_q[s + 1], k0 = cu_k[s], k1 = cu_k[s + 1];
+        const bool ok = !bad && q0 >= 0 && q1 >= q0 && q1 <= total_q && q1 - q0 <= max_q && k0 >= 0 &&
+                        k1 >= k0 && k1 <= total_k && k1 - k0 <= max_k;
+        if (!ok) atomicOr(err, 2);
+        if (n <= kSortMax) key[s] = (ok && q1 > q0) ? (k1 - k0) : -1;
+        tiles[s] = ok ? Hq * ((q1 - q0 + 255) / 256) : 0;
+    }
+    __syncthreads();
+    for (int s = tid; s < n; s += kSchedThreads) {
+        int rank = s;
+        if (n <= kSortMax) {
+            const int ks = key[s];
+            rank = 0;
+            for (int t = 0; t < n; ++t) {
+                const int kt = key[t];
+                rank += (kt > ks || (kt == ks && t < s)) ? 1 : 0;
+            }
+        }
+        order[rank] = s;
+    }
+    __syncthreads();
+    // exclusive scan of tiles in schedule order: per-thread chunks, then chunk offsets
+    const int chunk = (n + kSchedThreads - 1) / kSchedThreads;
+    const int c0 = min(n, tid * chunk), c1 = min(n, c0 + chunk);
+    int sum = 0;
+    for (int r = c0; r < c1; ++r) sum += tiles[order[r]];
+    part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int i = 0; i < kSchedThreads; ++i) {
+            const int x = part[i];
+            part[i] = acc;
+            acc += x;
+        }
+        sched[0] = acc;
+        prefix[n] = acc;
+    }
+    __syncthreads();
+    int acc = part[tid];
+    for (int r = c0; r < c1; ++r) {
+        prefix[r] = acc;
+        acc += tiles[order[r]];
+    }
+}
+
+cudaError_t launch_varlen_schedule(const int* cu_q, const int* cu_k, int num_seqs, int total_q, int total_k,
+                                   int max_q, int max_k, int Hq, int* sched, int* err, cudaStream_t stream)
+{
+    fa_varlen_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(cu_q, cu_k, num_seqs, total_q, total_k, max_q,
+                                                              max_k, Hq, sched, err);
+    return cudaGetLastError();
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                              int Hkv, int Lq, int Lk, int D, int causal, float softmax_scale,
+                              cudaStream_t stream)
+{
+    g_last_launches = 0;
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !scale_ok(softmax_scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    const long long nmb = (Lq + kRowsPerCta - 1) / kRowsPerCta;
+    const long long tiles = (long long)B * Hq * nmb;
+    if (tiles >= (1ll << 31) || (long long)B * Hq >= (1ll << 31) || (long long)B * Hkv >= (1ll << 31))
+        return FA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    fa_status_t st = device_state(&ds);
+    if (st != FA_OK) return st;
+
+    CUtensorMap mq, mk, mv;
+    const uint64_t row = (uint64_t)D * 2;
+    if (!encode_map(&mq, q, D, Lq, (uint64_t)B * Hq, row, row * Lq, 128, 1) ||
+        !encode_map(&mk, k, D, Lk, (uint64_t)B * Hkv, row, row * Lk, 128, 1) ||
+        !encode_map(&mv, v, D, Lk, (uint64_t)B * Hkv, row, row * Lk, 128, 1))
+        return FA_ERR_CUDA;
+
+    FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lq = Lq;
+    p.Lk = Lk;
+    p.group = Hq / Hkv;
+    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+    p.heads_per_section = heads_per_section(Hkv, Lk, D);
+    p.num_tiles = (int)tiles;
+    p.err = ds->err;
+    p.diag = ds->diag;
+    const int grid = (int)(tiles < ds->num_sms ? tiles : ds->num_sms);
+    if (dispatch<false>(D, causal != 0, mq, mk, mv, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+    g_last_launches = 1;
+    return FA_OK;
+}
+
+extern "C" fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                     const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                                     int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int Hq,
+                                     int Hkv, int D, int causal, float softmax_scale, cudaStream_t stream)
+{
+    g_last_launches = 0;
+    if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || total_q <= 0 || total_k <= 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 || Hq <= 0 ||
+        Hkv <= 0 || D <= 0)
+        return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !scale_ok(softmax_scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+        return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    // upper bound of the work tiles: sum_s ceil(Lq_s / 256) <= total_q / 256 + num_seqs
+    long long ub = (long long)Hq * ((long long)total_q / kRowsPerCta + num_seqs);
+    const long long ub2 = (long long)Hq * num_seqs * ((max_seqlen_q + kRowsPerCta - 1) / kRowsPerCta);
+    if (ub2 < ub) ub = ub2;
+    if ((long long)Hq * ((long long)total_q / kRowsPerCta + num_seqs) >= (1ll << 31) ||
+        (long long)total_q * Hq >= (1ll << 31) * 64ll)
+        return FA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    fa_status_t st = device_state(&ds);
+    if (st != FA_OK) return st;
+
+    CUtensorMap mq, mk, mv;
+    const uint64_t row = (uint64_t)D * 2;
+    if (!encode_map(&mq, q, D, Hq, total_q, row, row * Hq, 1, 128) ||
+        !encode_map(&mk, k, D, Hkv, total_k, row, row * Hkv, 1, 128) ||
+        !encode_map(&mv, v, D, Hkv, total_k, row, row * Hkv, 1, 128))
+        return FA_ERR_CUDA;
+
+    int* sched = nullptr;
+    const size_t ws = sizeof(int) * (2 + 3 * (size_t)num_seqs);
+    if (cudaMallocAsync(reinterpret_cast<void**>(&sched), ws, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                               max_seqlen_k, Hq, sched, ds->err, stream) != cudaSuccess) {
+        cudaFreeAsync(sched, stream);
+        return FA_ERR_CUDA;
+    }
+    FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = Hq / Hkv;
+    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, D);
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.sched = sched;
+    p.num_seqs = num_seqs;
+    p.total_q = total_q;
+    p.err = ds->err;
+    p.diag = ds->diag;
+    const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
+    const cudaError_t e = dispatch<true>(D, causal != 0, mq, mk, mv, p, grid, stream);
+    cudaFreeAsync(sched, stream);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    g_last_launches = 2;
+    return FA_OK;
+}
+
+extern "C" fa_status_t fa_check(cudaStream_t stream)
+{
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+    DeviceState* ds = nullptr;
+    fa_status_t st = device_state(&ds);
+    if (st != FA_OK) return st;
+    int h = 0;
+    if (cudaMemcpyFromSymbol(&h, g_err, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    if (h == 0) return FA_OK;
+    const int zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_err, zero, sizeof(int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_diag, zero, sizeof(zero)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return (h & 1) ? FA_ERR_TIMEOUT : FA_ERR_INVALID_ARG;
+}
+
+extern "C" const char* fa_status_string(fa_status_t s)
+{
+    switch (s) {
+        case FA_OK: return "ok";
+        case FA_ERR_INVALID_ARG: return "invalid argument";
+        case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case FA_ERR_CUDA: return "CUDA error";
+        case FA_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    }
+    return "unknown status";
+}
+
+extern "C" int fa_last_launch_count(void) { return g_last_launches; }

@@ -1,0 +1,3 @@
+// Kernel instances for head dimension 64 (same source as the D = 128 unit).
+#define FA_HEAD_DIM 64
+#include "fa_fwd_d128.cu"

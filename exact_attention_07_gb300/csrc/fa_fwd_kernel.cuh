@@ -1,0 +1,572 @@
+// Exact attention forward for sm_103a (GB300): TMA -> shared-memory ring ->
+// tcgen05 MMAs accumulating in tensor memory, online softmax one thread per
+// query row, persistent CTAs over a longest-first tile order.
+//
+// Method (FlashAttention Cheat Sheet, sec. 4 "The complete FlashAttention
+// flow" and sec. 5 "Why online softmax is globally exact"; FlashAttention
+// from Scratch, sec. 6.3 "Build a small fused forward" and sec. 7.1 "Delay
+// normalization"): a CTA keeps its query rows resident, streams K and V tiles
+// past them, keeps per row a running reference r, a running sum l and an
+// unnormalised accumulator A, and writes O = A / l and LSE = r + ln l once.
+// Scores S and probabilities P live only in tensor memory.
+//
+// Work split inside a CTA (FlashAttention-4 notes, "Forward TMEM pipeline"):
+//   warps 0-3   softmax for Q tile 0 (rows 0..127 of the CTA's 256-row block)
+//   warps 4-7   softmax for Q tile 1 (rows 128..255)
+//   warps 8-11  epilogue: O = A / l -> bf16 -> global, LSE
+//   warp  12    TMA producer: Q tiles and the K/V ring
+//   warp  13    MMA issuer and tensor-memory owner
+//   warps 14-15 idle
+// Register budget per thread after setmaxnreg: softmax 176, epilogue 64,
+// producer/MMA warpgroup 96 (2*128*176 + 128*64 + 128*96 = 65536, the whole
+// register file at the launch's 128 per thread).
+// The two Q tiles ping-pong: while one softmax group turns S into P, the
+// tensor core computes the other tile's S or P.V.
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   [0,128)   S0 (fp32); P0 (bf16 pairs) overwrites its first 64 columns
+//   [128,256) S1 / P1
+//   [256,256+D)     O0 accumulator (fp32)
+//   [256+D,256+2D)  O1 accumulator
+//
+// Base-2 exponentials with log2(e) folded into the scale (FlashAttention from
+// Scratch, sec. 6.3): p = 2^(s * scale * log2e - r).  The reference r only
+// moves when a tile's maximum exceeds it by more than 8 (a factor 256;
+// sec. 11.3 "Derive conditional rescaling correctly"), so O rarely needs a
+// correction; when it does, the softmax thread that owns the row rescales it
+// in tensor memory before releasing P.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "fa_params.h"
+#include "ptx_sm103.cuh"
+
+namespace fa {
+
+template <int D>
+struct FwdSmem {
+    static constexpr int kTileBytes = kBlockN * D * 2;          // one 128 x D bf16 tile
+    static constexpr int kStages = (D == 128) ? 4 : 8;           // K/V ring depth
+    static constexpr int kQOff = 0;                              // Q0, Q1
+    static constexpr int kKVOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    // barrier slots (8 bytes each)
+    static constexpr int kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kStages;
+    static constexpr int kSFull = 4 + 2 * kStages, kPFull = kSFull + 2, kOFull = kSFull + 4,
+                         kOEmpty = kSFull + 6, kStFull = kSFull + 8, kStEmpty = kSFull + 10,
+                         kDrain = kSFull + 12, kNumBars = kSFull + 13;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;      // tmem base, abort flag
+    static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;  // float2 [2][128]
+    static constexpr int kBytes = kStatsOff + 2 * kBlockM * 8;
+    static constexpr int kAlloc = kBytes + 1024;  // slack for 1 KB alignment
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0, kColO = 256;
+};
+
+struct Work {
+    int hq, hkv;
+    int m0;      // first query row of the CTA's 256-row block, within the sequence
+    int lq, lk;  // query / key length of this problem
+    int zq, zk;  // TMA coordinates: dense = head slab (b*H + h), varlen = first token
+    int q0;      // varlen: first query token of the sequence
+    int b;       // dense batch index
+    int nk;      // number of KV tiles this block visits (0: every row is empty)
+};
+
+// Tile order (FlashAttention-4 notes, "LPT scheduling for imbalanced grids"):
+// batches (or sequences, longest first) outermost; KV heads in L2-sized
+// sections; inside a section the 256-row blocks in reverse order when causal
+// (longest work first), then the KV head, then the query heads sharing it.
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ Work decode_tile(const FwdParams& p, int t)
+{
+    Work w;
+    int rem = t, nmb;
+    w.b = 0;
+    w.q0 = 0;
+    int k0 = 0;
+    if constexpr (VARLEN) {
+        const int n = p.num_seqs;
+        const int* prefix = p.sched + 1;
+        const int* order = p.sched + 2 + n;
+        int lo = 0, hi = n - 1;
+        while (lo < hi) {  // largest index whose prefix is <= t
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(prefix + mid) <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        const int s = __ldg(order + lo);
+        rem = t - __ldg(prefix + lo);
+        w.q0 = __ldg(p.cu_q + s);
+        k0 = __ldg(p.cu_k + s);
+        w.lq = __ldg(p.cu_q + s + 1) - w.q0;
+        w.lk = __ldg(p.cu_k + s + 1) - k0;
+        nmb = (w.lq + kRowsPerCta - 1) / kRowsPerCta;
+    } else {
+        w.lq = p.Lq;
+        w.lk = p.Lk;
+        nmb = (p.Lq + kRowsPerCta - 1) / kRowsPerCta;
+        const int per_b = nmb * p.Hq;
+        w.b = t / per_b;
+        rem = t - w.b * per_b;
+    }
+    const int G = p.group, hs = p.heads_per_section;
+    const int sec_tiles = nmb * hs * G;
+    const int sec = rem / sec_tiles;
+    const int rem2 = rem - sec * sec_tiles;
+    const int hs_cur = min(hs, p.Hkv - sec * hs);
+    const int i = rem2 / (hs_cur * G);
+    const int rem3 = rem2 - i * hs_cur * G;
+    w.hkv = sec * hs + rem3 / G;
+    w.hq = w.hkv * G + rem3 % G;
+    const int mb = CAUSAL ? (nmb - 1 - i) : i;
+    w.m0 = mb * kRowsPerCta;
+    if constexpr (VARLEN) {
+        w.zq = w.q0;
+        w.zk = k0;
+    } else {
+        w.zq = w.b * p.Hq + w.hq;
+        w.zk = w.b * p.Hkv + w.hkv;
+    }
+    if (w.lk <= 0) {
+        w.nk = 0;
+    } else if (!CAUSAL) {
+        w.nk = (w.lk + kBlockN - 1) / kBlockN;
+    } else {
+        const int last_row = min(w.m0 + kRowsPerCta - 1, w.lq - 1);
+        const int last_key = min(w.lk - 1, last_row + (w.lk - w.lq));
+        w.nk = last_key < 0 ? 0 : last_key / kBlockN + 1;
+    }
+    return w;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// All 32 lanes wait on the same barrier; the outcome is made warp-uniform so
+// that warp-collective tensor-memory instructions stay aligned.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          const WaitFailure& wf, int site, int tile)
+{
+    const bool ok = mbar_wait(bar, parity, abort_flag, wf, site, tile);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int D, bool CAUSAL, bool VARLEN>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const FwdParams p)
+{
+    using L = FwdSmem<D>;
+    constexpr int kHalves = D / 64;  // 64-column (128-byte) swizzle blocks per row
+    constexpr float kTau = 8.0f;     // rescale threshold, log2 units
+    constexpr float kLn2 = 0.69314718055994530942f;
+
+    // operand tiles need 1 KB alignment of their shared-memory address (the
+    // 128-byte swizzle pattern repeats every 8 rows of 128 bytes)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bar0 = sb + L::kBarOff;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+    float2* stats = reinterpret_cast<float2*>(smem + L::kStatsOff);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const WaitFailure wf{p.err, p.diag};
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(L::kQFull + t), 1);
+            mbar_init(bar(L::kQEmpty + t), 1);
+            mbar_init(bar(L::kSFull + t), 1);
+            mbar_init(bar(L::kPFull + t), kBlockM);
+            mbar_init(bar(L::kOFull + t), 1);
+            mbar_init(bar(L::kOEmpty + t), kBlockM);
+            mbar_init(bar(L::kStFull + t), kBlockM);
+            mbar_init(bar(L::kStEmpty + t), kBlockM);
+        }
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(bar(L::kKVFull + s), 1);
+            mbar_init(bar(L::kKVEmpty + s), 1);
+        }
+        mbar_init(bar(L::kDrain), 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 12 && lane == 0) {
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmV);
+    }
+    if (warp == 13) {
+        tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int num_tiles = VARLEN ? __ldg(p.sched) : p.num_tiles;
+
+    if (warp < 8) {
+        // ============================================================ softmax
+        regs_increase<176>();
+        const int t = warp >> 2;             // Q tile of this group
+        const int row = threadIdx.x & 127;   // query row within the tile == TMEM lane
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t tS = tmem + lane_base + L::kColS + (uint32_t)(t * kBlockN);
+        const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * D);
+        const float sl2 = p.scale_log2;
+        uint32_t s_ph = 0, st_ph = 1;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
+            if (w.nk == 0) continue;
+            const int q_row = w.m0 + t * kBlockM + row;
+            int kv_last = w.lk - 1;  // last key this row may attend
+            if (CAUSAL) kv_last = min(kv_last, q_row + (w.lk - w.lq));
+            float r = -INFINITY, l = 0.f;
+            for (int j = 0; j < w.nk; ++j) {
+                if (!warp_wait(bar(L::kSFull + t), s_ph, abort_flag, wf, 1 + t, tile)) goto done;
+                s_ph ^= 1;
+                tc_fence_after_sync();
+                uint32_t sv[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, sv[c]);
+                tmem_wait_ld();
+                // masking: keys past the row's last allowed key (causal diagonal,
+                // sequence tail) get -inf (FlashAttention from Scratch, sec. 7.3)
+                const int nvalid = kv_last - j * kBlockN + 1;
+                if (__any_sync(0xffffffffu, nvalid < kBlockN)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i >= nvalid) sv[c][i] = __float_as_uint(-INFINITY);
+                }
+                // row maximum of the raw scores
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sv[i >> 1][(i & 1) * 16]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = 32 * c + i;
+                        if ((e & 15) == 0) continue;
+                        mx[e >> 4] = fmaxf(mx[e >> 4], __uint_as_float(sv[c][i]));
+                    }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], mx[i + 4]);
+                const float mrow = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+                // conditional rescale: keep r unless the maximum rose by more than tau
+                const float r_new = (mrow - r > kTau) ? mrow : r;
+                const float alpha = (r_new == r) ? 1.f : ex2_approx(r - r_new);
+                const float r_use = (r_new == -INFINITY) ? 0.f : r_new;
+                l *= alpha;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float e = ex2_approx(fmaf(__uint_as_float(sv[c][i]), sl2, -r_use));
+                        acc[i & 3] += e;
+                        sv[c][i] = __float_as_uint(e);
+                    }
+                l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                // P (bf16 pairs) over the first 64 columns of S
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = 64 * c + 2 * i;
+                        pk[i] = pack_bf16x2(__uint_as_float(sv[e >> 5][e & 31]),
+                                            __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31]));
+                    }
+                    tmem_st32(tS + 32u * c, pk);
+                }
+                // correction of the accumulator when the reference moved (O is idle
+                // here: the previous P.V completed before this S was committed)
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + 32u * c, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(tO + 32u * c, ov);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::kPFull + t));
+                r = r_new;
+            }
+            // hand the row statistics to the epilogue
+            if (!warp_wait(bar(L::kStEmpty + t), st_ph, abort_flag, wf, 3 + t, tile)) goto done;
+            st_ph ^= 1;
+            stats[t * kBlockM + row] = make_float2(l, r);
+            mbar_arrive(bar(L::kStFull + t));
+        }
+    } else if (warp < 12) {
+        // ============================================================ epilogue
+        regs_decrease<64>();
+        const int row = threadIdx.x & 127;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        uint32_t o_ph[2] = {0, 0}, st_ph[2] = {0, 0};
+        __nv_bfloat16* obase = reinterpret_cast<__nv_bfloat16*>(p.o);
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
+            for (int t = 0; t < 2; ++t) {
+                const int q_row = w.m0 + t * kBlockM + row;
+                const bool valid = q_row < w.lq;
+                int64_t orow, lidx;
+                if constexpr (VARLEN) {
+                    orow = ((int64_t)(w.q0 + q_row) * p.Hq + w.hq) * D;
+                    lidx = (int64_t)w.hq * p.total_q + w.q0 + q_row;
+                } else {
+                    lidx = ((int64_t)w.b * p.Hq + w.hq) * p.Lq + q_row;
+                    orow = lidx * D;
+                }
+                uint4* dst = reinterpret_cast<uint4*>(obase + orow);
+                if (w.nk == 0) {  // no key reaches this block: O = 0, LSE = -inf
+                    if (valid) {
+#pragma unroll
+                        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                        p.lse[lidx] = -INFINITY;
+                    }
+                    continue;
+                }
+                if (!warp_wait(bar(L::kOFull + t), o_ph[t], abort_flag, wf, 5 + t, tile)) goto done;
+                o_ph[t] ^= 1;
+                tc_fence_after_sync();
+                if (!warp_wait(bar(L::kStFull + t), st_ph[t], abort_flag, wf, 7 + t, tile)) goto done;
+                st_ph[t] ^= 1;
+                const float2 st = stats[t * kBlockM + row];
+                mbar_arrive(bar(L::kStEmpty + t));
+                const float l = st.x;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * D);
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + 32u * c, ov);
+                    tmem_wait_ld();
+                    if (valid) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv,
+                                                __uint_as_float(ov[2 * i + 1]) * inv);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[4 * c + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                }
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::kOEmpty + t));
+                if (valid) p.lse[lidx] = l > 0.f ? (st.y + __log2f(l)) * kLn2 : -INFINITY;
+            }
+        }
+    } else {
+        regs_decrease<96>();
+        if (warp == 12) {
+            // ============================================================ TMA producer
+            if (lane == 0) {
+                uint32_t q_ph[2] = {1, 1};
+                int stage = 0;
+                uint32_t kv_ph = 1;
+                // last armed phase of each buffer, to wait out copies in flight at exit
+                int q_armed[2] = {-1, -1};
+                int kv_armed[L::kStages];
+                for (int s = 0; s < L::kStages; ++s) kv_armed[s] = -1;
+                auto load_q = [&](const Work& w, int t, int tile) -> bool {
+                    if (!mbar_wait(bar(L::kQEmpty + t), q_ph[t], abort_flag, wf, 9 + t, tile)) return false;
+                    q_ph[t] ^= 1;
+                    mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
+                    q_armed[t] = (int)q_ph[t];  // parity of the phase this copy completes
+                    const uint32_t dst = sb + L::kQOff + (uint32_t)(t * L::kTileBytes);
+                    const int row0 = w.m0 + t * kBlockM;
+#pragma unroll
+                    for (int h = 0; h < kHalves; ++h) {
+                        if constexpr (VARLEN)
+                            tma_load_3d(dst + h * (L::kTileBytes / kHalves), &tmQ, bar(L::kQFull + t), 64 * h,
+                                        w.hq, w.zq + row0);
+                        else
+                            tma_load_3d(dst + h * (L::kTileBytes / kHalves), &tmQ, bar(L::kQFull + t), 64 * h,
+                                        row0, w.zq);
+                    }
+                    return true;
+                };
+                auto load_kv = [&](const CUtensorMap* map, const Work& w, int j, int tile) -> bool {
+                    if (!mbar_wait(bar(L::kKVEmpty + stage), kv_ph, abort_flag, wf, 11, tile)) return false;
+                    mbar_arrive_expect_tx(bar(L::kKVFull + stage), L::kTileBytes);
+                    kv_armed[stage] = (int)(kv_ph ^ 1u);
+                    const uint32_t dst = sb + L::kKVOff + (uint32_t)(stage * L::kTileBytes);
+#pragma unroll
+                    for (int h = 0; h < kHalves; ++h) {
+                        if constexpr (VARLEN)
+                            tma_load_3d(dst + h * (L::kTileBytes / kHalves), map, bar(L::kKVFull + stage),
+                                        64 * h, w.hkv, w.zk + j * kBlockN);
+                        else
+                            tma_load_3d(dst + h * (L::kTileBytes / kHalves), map, bar(L::kKVFull + stage),
+                                        64 * h, j * kBlockN, w.zk);
+                    }
+                    if (++stage == L::kStages) {
+                        stage = 0;
+                        kv_ph ^= 1;
+                    }
+                    return true;
+                };
+                for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                    const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
+                    if (w.nk == 0) continue;
+                    if (!load_q(w, 0, tile)) break;
+                    if (!load_kv(&tmK, w, 0, tile)) break;
+                    if (!load_q(w, 1, tile)) break;
+                    if (!load_kv(&tmV, w, 0, tile)) break;
+                    bool ok = true;
+                    for (int j = 1; j < w.nk && ok; ++j) ok = load_kv(&tmK, w, j, tile) && load_kv(&tmV, w, j, tile);
+                    if (!ok) break;
+                }
+                // every copy this warp started has landed before the CTA retires
+                for (int t = 0; t < 2; ++t)
+                    if (q_armed[t] >= 0) mbar_settle(bar(L::kQFull + t), (uint32_t)q_armed[t], wf, 13);
+                for (int s = 0; s < L::kStages; ++s)
+                    if (kv_armed[s] >= 0) mbar_settle(bar(L::kKVFull + s), (uint32_t)kv_armed[s], wf, 14);
+            }
+            __syncwarp();
+        } else if (warp == 13) {
+            // ============================================================ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false);
+                constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
+                uint32_t q_ph[2] = {0, 0}, p_ph[2] = {0, 0}, oe_ph[2] = {1, 1};
+                int stage = 0;
+                uint32_t kv_ph = 0;
+                bool issued = false;
+                auto next_stage = [&]() -> int {
+                    const int s = stage;
+                    if (++stage == L::kStages) {
+                        stage = 0;
+                        kv_ph ^= 1;
+                    }
+                    return s;
+                };
+                // S_t = Q_t K^T over D in steps of 16 (both operands K-major, 128B swizzle)
+                auto issue_s = [&](int t, int ks) {
+                    const uint32_t qa = sb + L::kQOff + (uint32_t)(t * L::kTileBytes);
+                    const uint32_t ka = sb + L::kKVOff + (uint32_t)(ks * L::kTileBytes);
+#pragma unroll 1
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (uint32_t)((kk >> 2) * (L::kTileBytes / kHalves) + (kk & 3) * 32);
+                        mma_ss(tmem + L::kColS + (uint32_t)(t * kBlockN), smem_desc_sw128(qa + off, 16, 1024),
+                               smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                };
+                // O_t (+)= P_t V: P from tensor memory, V MN-major (rows of D, 128B swizzle)
+                auto issue_pv = [&](int t, int vs, bool acc) {
+                    const uint32_t va = sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes);
+#pragma unroll 1
+                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                        mma_ts(tmem + L::kColO + (uint32_t)(t * D), tmem + L::kColS + (uint32_t)(t * kBlockN + kk * 8),
+                               smem_desc_sw128(va + (uint32_t)(kk * 16 * 128), L::kTileBytes / kHalves, 1024),
+                               kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                    }
+                };
+                for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                    const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
+                    if (w.nk == 0) continue;
+                    const int nk = w.nk;
+                    // prologue: S0(0), S1(0)
+                    if (!mbar_wait(bar(L::kQFull + 0), q_ph[0], abort_flag, wf, 15, tile)) break;
+                    q_ph[0] ^= 1;
+                    int ks = stage;
+                    if (!mbar_wait(bar(L::kKVFull + ks), kv_ph, abort_flag, wf, 17, tile)) break;
+                    next_stage();
+                    tc_fence_after_sync();
+                    issue_s(0, ks);
+                    issued = true;
+                    tc_commit(bar(L::kSFull + 0));
+                    if (nk == 1) tc_commit(bar(L::kQEmpty + 0));
+                    if (!mbar_wait(bar(L::kQFull + 1), q_ph[1], abort_flag, wf, 16, tile)) break;
+                    q_ph[1] ^= 1;
+                    tc_fence_after_sync();
+                    issue_s(1, ks);
+                    tc_commit(bar(L::kSFull + 1));
+                    tc_commit(bar(L::kKVEmpty + ks));
+                    if (nk == 1) tc_commit(bar(L::kQEmpty + 1));
+                    bool ok = true;
+                    for (int j = 0; j < nk && ok; ++j) {
+                        const int vs = stage;
+                        if (!(ok = mbar_wait(bar(L::kKVFull + vs), kv_ph, abort_flag, wf, 18, tile))) break;
+                        next_stage();
+                        // tile 0: P0(j) . V(j), then S0(j+1)
+                        if (j == 0) {
+                            if (!(ok = mbar_wait(bar(L::kOEmpty + 0), oe_ph[0], abort_flag, wf, 19, tile))) break;
+                            oe_ph[0] ^= 1;
+                        }
+                        if (!(ok = mbar_wait(bar(L::kPFull + 0), p_ph[0], abort_flag, wf, 21, tile))) break;
+                        p_ph[0] ^= 1;
+                        tc_fence_after_sync();
+                        issue_pv(0, vs, j > 0);
+                        int kn = -1;
+                        if (j + 1 < nk) {
+                            kn = stage;
+                            if (!(ok = mbar_wait(bar(L::kKVFull + kn), kv_ph, abort_flag, wf, 17, tile))) break;
+                            next_stage();
+                            issue_s(0, kn);
+                            tc_commit(bar(L::kSFull + 0));
+                            if (j + 2 == nk) tc_commit(bar(L::kQEmpty + 0));
+                        } else {
+                            tc_commit(bar(L::kOFull + 0));
+                        }
+                        // tile 1: P1(j) . V(j), then S1(j+1)
+                        if (j == 0) {
+                            if (!(ok = mbar_wait(bar(L::kOEmpty + 1), oe_ph[1], abort_flag, wf, 20, tile))) break;
+                            oe_ph[1] ^= 1;
+                        }
+                        if (!(ok = mbar_wait(bar(L::kPFull + 1), p_ph[1], abort_flag, wf, 22, tile))) break;
+                        p_ph[1] ^= 1;
+                        tc_fence_after_sync();
+                        issue_pv(1, vs, j > 0);
+                        tc_commit(bar(L::kKVEmpty + vs));
+                        if (kn >= 0) {
+                            issue_s(1, kn);
+                            tc_commit(bar(L::kSFull + 1));
+                            tc_commit(bar(L::kKVEmpty + kn));
+                            if (j + 2 == nk) tc_commit(bar(L::kQEmpty + 1));
+                        } else {
+                            tc_commit(bar(L::kOFull + 1));
+                        }
+                    }
+                    if (!ok) break;
+                }
+                // every MMA this thread issued has completed before TMEM is released
+                if (issued) {
+                    tc_commit(bar(L::kDrain));
+                    mbar_settle(bar(L::kDrain), 0, wf, 23);
+                }
+            }
+            __syncwarp();
+        }
+    }
+done:
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 13) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+}  // namespace fa

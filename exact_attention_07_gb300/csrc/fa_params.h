@@ -1,0 +1,34 @@
+// Launch parameters shared by the host launcher and the sm_103a kernels.
+#pragma once
+
+#include <cstdint>
+
+namespace fa {
+
+struct FwdParams {
+    void* o;           // bf16 output
+    float* lse;        // fp32 output, natural log
+    int B, Hq, Hkv;    // batch (dense only), query heads, KV heads
+    int Lq, Lk;        // dense sequence lengths (unused for varlen)
+    int group;         // Hq / Hkv
+    float scale_log2;  // softmax_scale * log2(e)
+    int heads_per_section;  // KV heads per L2-sized scheduling section
+    int num_tiles;          // dense: number of work tiles
+    // variable-length batches
+    const int* cu_q;
+    const int* cu_k;
+    const int* sched;  // [0] tiles, [1..n+1] tile prefix in schedule order, [n+2..2n+1] order
+    int num_seqs;
+    int total_q;
+    // error reporting
+    int* err;
+    int* diag;
+};
+
+// Rows of one Q tile and keys of one KV tile; a CTA owns two Q tiles.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+constexpr int kRowsPerCta = 2 * kBlockM;
+constexpr int kThreads = 512;
+
+}  // namespace fa

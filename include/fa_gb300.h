@@ -1,0 +1,118 @@
+/*
+ * fa_gb300.h -- exact scaled-dot-product attention forward on GB300 (sm_103a).
+ *
+ * Operation (FlashAttention from Scratch, sec. 2 "Begin with one attention
+ * row"; FlashAttention Cheat Sheet, sec. 1 "The whole operation"):
+ *
+ *     O = softmax(Q K^T * softmax_scale + M) V,   LSE_i = ln sum_j exp(s_ij)
+ *
+ * computed tile by tile with the online-softmax recurrence (running maximum,
+ * running sum, unnormalised accumulator; Cheat Sheet sec. 5) so that the
+ * score matrix never reaches device memory.  M is 0 for allowed pairs and
+ * -inf otherwise.  With causal != 0 key j is allowed for query i iff
+ * j <= i + (Lk - Lq): the queries are the last Lq positions of the key
+ * sequence (bottom-right alignment; FlashAttention from Scratch, sec. 5
+ * "Rectangular causal masking is a correctness issue").  A query row with no
+ * allowed key gets O = 0 and LSE = -inf (sec. 4.4 "Handle the empty state
+ * deliberately").  LSE is in natural-log units (sec. 6.3).
+ *
+ * Grouped-query attention: Hq must be a multiple of Hkv and query head h
+ * reads KV head h / (Hq / Hkv) (sec. 9.2 "GQA and MQA change decode
+ * traffic"); K and V are not replicated.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers are DEVICE pointers on the current CUDA device, 16-byte
+ *    aligned, and owned by the caller.  Q, K, V are read only; O and LSE are
+ *    fully overwritten (including fully masked rows and rows of empty
+ *    sequences).  Output buffers must not overlap the inputs.
+ *  - Q, K, V, O are bf16 (raw 16-bit storage, passed as void*); LSE is fp32.
+ *  - Head dimension D must be 64 or 128.
+ *  - The call is asynchronous on `stream` (0 = legacy default stream) and
+ *    never synchronises it.  Errors detected inside a kernel (a pipeline wait
+ *    that exceeded its time limit) are latched on the device and reported by
+ *    the next fa_check().
+ *  - Nothing throws across this interface: every call returns a status.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, Hq % Hkv != 0,
+                               non-finite or non-positive scale, misalignment */
+    FA_ERR_UNSUPPORTED = 2, /* D not in {64, 128}, or no sm_103 device */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or launch failed */
+    FA_ERR_TIMEOUT = 4      /* a kernel pipeline wait hit its time limit */
+} fa_status_t;
+
+/*
+ * Dense batched attention forward.
+ *
+ *   q   [B, Hq,  Lq, D] bf16, contiguous row-major
+ *   k   [B, Hkv, Lk, D] bf16
+ *   v   [B, Hkv, Lk, D] bf16
+ *   o   [B, Hq,  Lq, D] bf16   (output)
+ *   lse [B, Hq,  Lq]    fp32   (output, natural log)
+ *
+ * softmax_scale multiplies Q K^T (1/sqrt(D) is the usual choice, sec. 2
+ * "Why divide by sqrt d?").  Uses no memory beyond its arguments.
+ */
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int Hq, int Hkv, int Lq, int Lk, int D, int causal,
+                   float softmax_scale, cudaStream_t stream);
+
+/*
+ * Variable-length (packed) attention forward: num_seqs independent problems
+ * stored back to back, token-major.
+ *
+ *   q   [total_q, Hq,  D] bf16;  k, v [total_k, Hkv, D] bf16
+ *   o   [total_q, Hq,  D] bf16   (output)
+ *   lse [Hq, total_q]     fp32   (output, natural log)
+ *   cu_seqlens_q, cu_seqlens_k: int32 DEVICE arrays of num_seqs + 1
+ *     non-decreasing prefix offsets starting at 0, ending at total_q / total_k.
+ *     Sequence s owns query tokens [cu_seqlens_q[s], cu_seqlens_q[s+1]) and key
+ *     tokens [cu_seqlens_k[s], cu_seqlens_k[s+1]); the causal mask is relative
+ *     to each sequence (bottom-right alignment per sequence).
+ *   max_seqlen_q, max_seqlen_k: upper bounds on any sequence's length.
+ *
+ * Offsets are read on the device.  Offsets that are not non-decreasing, or a
+ * sequence longer than its max_seqlen bound, latch FA_ERR_INVALID_ARG on the
+ * device (reported by fa_check); such sequences produce no output.
+ * Scheduling first sorts sequences by work, longest first, into a small
+ * scratch buffer that this call obtains with cudaMallocAsync on `stream` and
+ * releases with cudaFreeAsync on the same stream (stream-ordered, no
+ * synchronisation).
+ */
+fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                          int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                          int Hq, int Hkv, int D, int causal, float softmax_scale,
+                          cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device-side error latch
+ * of the current device (FA_ERR_TIMEOUT or FA_ERR_INVALID_ARG from an earlier
+ * launch), or FA_ERR_CUDA if the stream reports an error.
+ */
+fa_status_t fa_check(cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status_t status);
+
+/*
+ * Number of kernels the last successful fa_fwd / fa_fwd_varlen call on this
+ * host thread launched (1 for dense, 2 for varlen: schedule + attention).
+ */
+int fa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

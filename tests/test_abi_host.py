@@ -1,0 +1,83 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/fa_gb300.h declares, and rejects bad arguments before touching the
+device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import exact_attention_07_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_07_gb300 import _build
+    _build.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert set(declared_functions()) == set(fa.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, f"{name} not exported"
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert fa.fa_status_string(code)
+    assert fa.fa_status_string(99) == "unknown status"
+
+
+def _fwd(lib, q=16, k=16, v=16, o=16, lse=16, B=1, Hq=2, Hkv=1, Lq=8, Lk=8, D=64, causal=0, scale=0.125):
+    return lib.fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, causal, scale, None)
+
+
+def test_dense_argument_validation(lib):
+    INV, UNS = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, q=None) == INV
+    assert _fwd(lib, lse=None) == INV
+    assert _fwd(lib, B=0) == INV
+    assert _fwd(lib, Lq=-1) == INV
+    assert _fwd(lib, Lk=0) == INV
+    assert _fwd(lib, Hq=3, Hkv=2) == INV             # Hq % Hkv != 0
+    assert _fwd(lib, scale=0.0) == INV
+    assert _fwd(lib, scale=float("nan")) == INV
+    assert _fwd(lib, scale=float("inf")) == INV
+    assert _fwd(lib, q=24) == INV                    # not 16-byte aligned
+    assert _fwd(lib, D=96) == UNS
+    assert _fwd(lib, D=256) == UNS
+    assert lib.fa_last_launch_count() == 0
+
+
+def test_varlen_argument_validation(lib):
+    INV, UNS = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+
+    def call(cu_q=32, cu_k=32, n=2, tq=10, tk=10, mq=8, mk=8, Hq=2, Hkv=2, D=128, scale=0.1):
+        return lib.fa_fwd_varlen(16, 16, 16, 16, 16, cu_q, cu_k, n, tq, tk, mq, mk, Hq, Hkv, D, 1, scale, None)
+
+    assert call(cu_q=None) == INV
+    assert call(n=0) == INV
+    assert call(tq=0) == INV
+    assert call(mk=0) == INV
+    assert call(Hq=4, Hkv=3) == INV
+    assert call(cu_k=34) == INV                      # int32 offsets must be 4-byte aligned
+    assert call(scale=-1.0) == INV
+    assert call(D=80) == UNS

@@ -1,0 +1,352 @@
+"""Benchmark: exact attention forward (bf16) on GB300, one JSON line.
+
+A step is one fa_fwd call over the whole workload (B=1, Hq=Hkv=16,
+Lq=Lk=16384, D=128, non-causal by default): every stage of the forward
+(tile schedule, TMA loads, S = QK^T, masking, online softmax, P.V, epilogue)
+runs inside it.  The metric is matrix TFLOP/s, 4*B*Hq*Lq*Lk*D per step
+(halved when causal).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own copy of the
+workload (the problem partitions over batch and heads with no exchange), and
+`value` is the total work of all ranks over the slowest rank's time.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (BF16) and fraction of GB300 dense BF16 peak"
+FALLBACK_BF16_TFLOPS = 1900.0
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def aggregate(values_per_rank: list[float], units_per_rank: list[float]) -> tuple[float, float]:
+    """Whole-job throughput: total units of all ranks over the slowest rank's seconds."""
+    t = max(values_per_rank)
+    return sum(units_per_rank) / t if t > 0 else 0.0, t
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    def __init__(self, gpu_index: int, path: str | None = None):
+        self.gpu = gpu_index
+        self.path = path
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+            if self.path:
+                with open(self.path, "w") as f:
+                    f.write(SMI_FIELDS + "\n" + "\n".join(self.lines) + "\n")
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def cpu_oracle_rate(w, inputs, seconds: float, rng_seed: int = 0):
+    """Time the fp64 oracle on sampled output rows for about `seconds`.
+
+    Returns (TFLOP/s, threads, description).  FLOPs per row follow the metric
+    (4*Lk*D, halved on average when causal).
+    """
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(rng_seed)
+    if w.varlen:
+        q, k, v, cq, ck = inputs
+        Tq = q.shape[0]
+        total_rows = w.Hq * Tq
+        per_row = w.flops() / total_rows
+
+        def run(rows):
+            oracle.attention_varlen(q, k, v, cq.numpy(), ck.numpy(), scale=w.scale, causal=w.causal, rows=rows)
+    else:
+        q, k, v = inputs
+        total_rows = w.B * w.Hq * w.Lq
+        per_row = w.flops() / total_rows
+
+        def run(rows):
+            oracle.attention(q, k, v, scale=w.scale, causal=w.causal, rows=rows)
+    threads = oracle.num_cpus()
+    n = max(threads, 16)
+    t0 = time.perf_counter()
+    run(rng.integers(0, total_rows, n))
+    dt = time.perf_counter() - t0
+    n = int(min(total_rows, max(n, n * seconds / max(dt, 1e-6))))
+    rows = rng.integers(0, total_rows, n)
+    t0 = time.perf_counter()
+    run(rows)
+    dt = time.perf_counter() - t0
+    return per_row * n / dt / 1e12, threads, f"{n} random output rows of {total_rows} ({dt:.1f} s)"
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from workloads import dense_inputs, varlen_inputs
+    inputs = varlen_inputs(w) if w.varlen else dense_inputs(w)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    rates = []
+    for i in range(args.warmup + args.steps):
+        r, threads, desc = cpu_oracle_rate(w, inputs, budget, rng_seed=i)
+        if i >= args.warmup:
+            rates.append(r)
+    value = statistics.median(rates)
+    ms = w.flops() / (value * 1e12) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk, "D": w.D,
+                       "causal": w.causal},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"per step: {desc}"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def main(argv=None):
+    args = parse_args(argv)
+    from workloads import HEADLINE, WORKLOADS
+    w = WORKLOADS[args.workload or HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+
+    import exact_attention_07_gb300 as fa
+    from workloads import dense_inputs, varlen_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    stream = torch.cuda.current_stream(dev)
+
+    # inputs resident in HBM (seeded on the CPU, copied once)
+    host_inputs = varlen_inputs(w) if w.varlen else dense_inputs(w)
+    if w.varlen:
+        q, k, v, cq, ck = (t.to(dev) for t in host_inputs)
+        maxl = max(w.seqlens)
+
+        def step(o=None, lse=None, qq=q, kk=k, vv=v):
+            return fa.fa_fwd_varlen(qq, kk, vv, cq, ck, maxl, maxl, causal=w.causal, out=o, lse=lse)
+        out_shape, lse_shape = tuple(q.shape), (w.Hq, q.shape[0])
+    else:
+        q, k, v = (t.to(dev) for t in host_inputs)
+
+        def step(o=None, lse=None, qq=q, kk=k, vv=v):
+            return fa.fa_fwd(qq, kk, vv, causal=w.causal, out=o, lse=lse)
+        out_shape, lse_shape = tuple(q.shape), (w.B, w.Hq, w.Lq)
+    o = torch.empty(out_shape, dtype=torch.float32, device=dev)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    l2_note = ("inputs larger than L2 (Q+K+V+O = %.0f MiB vs 126 MiB L2); no flush" %
+               ((in_bytes + o.numel() * 4) / 2**20))
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        step(o, lse)
+    fa.fa_check()
+    launches_per_step = fa.fa_last_launch_count()
+
+    # ---- device-resident timed region
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clk_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_rank{rank}.csv")
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(dev.index, clk_path) as clocks:
+        barrier()
+        start.record(stream)
+        for _ in range(args.steps):
+            step(o, lse)
+        end.record(stream)
+        barrier()
+    fa.fa_check()
+    secs = start.elapsed_time(end) / 1e3
+    flops_step = w.flops()
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([secs], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        secs_max = float(tt.item())
+    else:
+        secs_max = secs
+    total_units = flops_step * args.steps * world
+    value = total_units / secs_max / 1e12
+    ms_per_step = secs_max / args.steps * 1e3
+
+    # ---- end to end through the public API with host buffers (pinned)
+    e2e = None
+    if not args.no_e2e:
+        pin = [t.pin_memory() for t in host_inputs]
+        h_o = torch.empty(out_shape, dtype=torch.float32).pin_memory()
+        h_l = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
+        d_in = [torch.empty_like(t, device=dev) for t in pin]
+
+        def e2e_step():
+            for d, h in zip(d_in, pin):
+                d.copy_(h, non_blocking=True)
+            if w.varlen:
+                fa.fa_fwd_varlen(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], maxl, maxl, causal=w.causal,
+                                 out=o, lse=lse)
+            else:
+                fa.fa_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse)
+            h_o.copy_(o, non_blocking=True)
+            h_l.copy_(lse, non_blocking=True)
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        s2 = torch.cuda.Event(enable_timing=True)
+        e2_ = torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e2_.record(stream)
+        barrier()
+        fa.fa_check()
+        e2e_secs = s2.elapsed_time(e2_) / 1e3
+        if world > 1:
+            tt = torch.tensor([e2e_secs], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e2e_secs = float(tt.item())
+        h2d = sum(t.numel() * t.element_size() for t in pin)
+        d2h = h_o.numel() * 4 + h_l.numel() * 4
+        e2e = {"value": flops_step * args.e2e_steps * world / e2e_secs / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_secs / args.e2e_steps * 1e3}
+
+    # ---- roofline of the attention kernel (the only kernel of a dense step)
+    peak, peak_sus, peak_kind = measured_peaks()
+    achieved = flops_step / (secs / args.steps) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "peak_kind": f"{peak_kind} burst bf16 GEMM", "frac_of_sustained": achieved / peak_sus,
+                "kernel": "fa_fwd_sm103_kernel<%d,%s,%s>" % (w.D, str(w.causal).lower(), str(w.varlen).lower())}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, desc = cpu_oracle_rate(w, host_inputs, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk,
+                           "D": w.D, "causal": w.causal, "flops_per_step": flops_step,
+                           "parallelism": f"replicas{world}" if world > 1 else "single", "l2": l2_note},
+                "frac_of_peak": value / world / peak,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps,
+                "clocks": clocks.summary()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -97,7 +97,7 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
            lse: torch.Tensor | None = None, stream=None):
     """Dense attention forward.  q [B,Hq,Lq,D], k/v [B,Hkv,Lk,D] bf16 CUDA.
 
-    Returns (o [B,Hq,Lq,D] bf16, lse [B,Hq,Lq] fp32).  Asynchronous on the
+    Returns (o [B,Hq,Lq,D] fp32, lse [B,Hq,Lq] fp32).  Asynchronous on the
     current (or given) stream.
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -107,10 +107,12 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
     if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
-    _check_tensor(out, "out", torch.bfloat16, 4)
+    _check_tensor(out, "out", torch.float32, 4)
+    if tuple(out.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Lq):
+        raise ValueError("out/lse shape mismatch")
     _check_tensor(lse, "lse", torch.float32, 3)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
@@ -128,7 +130,7 @@ def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_
                   softmax_scale: float | None = None, out: torch.Tensor | None = None,
                   lse: torch.Tensor | None = None, stream=None):
     """Packed variable-length forward.  q [Tq,Hq,D], k/v [Tk,Hkv,D] bf16 CUDA,
-    cu_seqlens_* int32 CUDA [num_seqs+1].  Returns (o [Tq,Hq,D], lse [Hq,Tq])."""
+    cu_seqlens_* int32 CUDA [num_seqs+1].  Returns (o [Tq,Hq,D] fp32, lse [Hq,Tq] fp32)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check_tensor(t, n, torch.bfloat16, 3)
     _check_tensor(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
@@ -138,9 +140,13 @@ def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_
     if tuple(v.shape) != tuple(k.shape) or Dk != D or cu_seqlens_q.numel() != cu_seqlens_k.numel():
         raise ValueError("shape mismatch")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    _check_tensor(out, "out", torch.float32, 3)
+    _check_tensor(lse, "lse", torch.float32, 2)
+    if tuple(out.shape) != tuple(q.shape) or tuple(lse.shape) != (Hq, Tq):
+        raise ValueError("out/lse shape mismatch")
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     lib = load_library()

@@ -197,7 +197,7 @@ cudaError_t launch_varlen_schedule(const int* cu_q, const int* cu_k, int num_seq
 
 using namespace fa;
 
-extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq,
                               int Hkv, int Lq, int Lk, int D, int causal, float softmax_scale,
                               cudaStream_t stream)
 {
@@ -243,7 +243,7 @@ extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, void*
     return FA_OK;
 }
 
-extern "C" fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+extern "C" fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse,
                                      const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
                                      int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int Hq,
                                      int Hkv, int D, int causal, float softmax_scale, cudaStream_t stream)

@@ -13,12 +13,12 @@
 // Work split inside a CTA (FlashAttention-4 notes, "Forward TMEM pipeline"):
 //   warps 0-3   softmax for Q tile 0 (rows 0..127 of the CTA's 256-row block)
 //   warps 4-7   softmax for Q tile 1 (rows 128..255)
-//   warps 8-11  epilogue: O = A / l -> bf16 -> global, LSE
+//   warps 8-11  epilogue: O = A / l -> fp32 -> global, LSE
 //   warp  12    TMA producer: Q tiles and the K/V ring
 //   warp  13    MMA issuer and tensor-memory owner
 //   warps 14-15 idle
-// Register budget per thread after setmaxnreg: softmax 176, epilogue 64,
-// producer/MMA warpgroup 96 (2*128*176 + 128*64 + 128*96 = 65536, the whole
+// Register budget per thread after setmaxnreg: softmax 192, epilogue 64,
+// producer/MMA warpgroup 64 (2*128*192 + 128*64 + 128*64 = 65536, the whole
 // register file at the launch's 128 per thread).
 // The two Q tiles ping-pong: while one softmax group turns S into P, the
 // tensor core computes the other tile's S or P.V.
@@ -57,8 +57,8 @@ struct FwdSmem {
                          kOEmpty = kSFull + 6, kStFull = kSFull + 8, kStEmpty = kSFull + 10,
                          kDrain = kSFull + 12, kNumBars = kSFull + 13;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;      // tmem base, abort flag
-    static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;  // float2 [2][128]
-    static constexpr int kBytes = kStatsOff + 2 * kBlockM * 8;
+    static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;  // float4 [2][128]
+    static constexpr int kBytes = kStatsOff + 2 * kBlockM * 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1 KB alignment
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS = 0, kColO = 256;
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-    float2* stats = reinterpret_cast<float2*>(smem + L::kStatsOff);
+    float4* stats = reinterpret_cast<float4*>(smem + L::kStatsOff);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 8) {
         // ============================================================ softmax
-        regs_increase<176>();
+        regs_increase<192>();
         const int t = warp >> 2;             // Q tile of this group
         const int row = threadIdx.x & 127;   // query row within the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q_row = w.m0 + t * kBlockM + row;
             int kv_last = w.lk - 1;  // last key this row may attend
             if (CAUSAL) kv_last = min(kv_last, q_row + (w.lk - w.lq));
-            float r = -INFINITY, l = 0.f;
+            float r = -INFINITY, l = 0.f, l_rnd = 0.f;
             for (int j = 0; j < w.nk; ++j) {
                 if (!warp_wait(bar(L::kSFull + t), s_ph, abort_flag, wf, 1 + t, tile)) goto done;
                 s_ph ^= 1;
@@ -270,27 +270,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float alpha = (r_new == r) ? 1.f : ex2_approx(r - r_new);
                 const float r_use = (r_new == -INFINITY) ? 0.f : r_new;
                 l *= alpha;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float e = ex2_approx(fmaf(__uint_as_float(sv[c][i]), sl2, -r_use));
-                        acc[i & 3] += e;
-                        sv[c][i] = __float_as_uint(e);
-                    }
-                l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
-                // P (bf16 pairs) over the first 64 columns of S
+                // p = 2^(s*scale*log2e - r), rounded to bf16 for the P.V MMA.  Two row
+                // sums: of the rounded p (it normalises O, so numerator and
+                // denominator weight every key identically) and of the fp32 p (it
+                // gives the LSE).
+                l_rnd *= alpha;
+                const uint64_t c2 = f2_pack(sl2, sl2);
+                const uint64_t nr2 = f2_pack(-r_use, -r_use);
+                uint64_t sum_t[2] = {0ull, 0ull}, sum_r[2] = {0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int e = 64 * c + 2 * i;
-                        pk[i] = pack_bf16x2(__uint_as_float(sv[e >> 5][e & 31]),
-                                            __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31]));
+                        const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sv[e >> 5][e & 31]),
+                                                           __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31])),
+                                                   c2, nr2);
+                        float x0, x1;
+                        f2_unpack(x2, x0, x1);
+                        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+                        pk[i] = pack_bf16x2(e0, e1);
+                        sum_t[i & 1] = f2_add(sum_t[i & 1], f2_pack(e0, e1));
+                        sum_r[i & 1] = f2_add(sum_r[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
+                                                                    __uint_as_float(pk[i] & 0xffff0000u)));
                     }
+                    // P (bf16 pairs) over the first 64 columns of S
                     tmem_st32(tS + 32u * c, pk);
+                }
+                {
+                    float a0, a1, b0, b1;
+                    f2_unpack(f2_add(sum_t[0], sum_t[1]), a0, a1);
+                    f2_unpack(f2_add(sum_r[0], sum_r[1]), b0, b1);
+                    l += a0 + a1;
+                    l_rnd += b0 + b1;
                 }
                 // correction of the accumulator when the reference moved (O is idle
                 // here: the previous P.V completed before this S was committed)
@@ -313,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // hand the row statistics to the epilogue
             if (!warp_wait(bar(L::kStEmpty + t), st_ph, abort_flag, wf, 3 + t, tile)) goto done;
             st_ph ^= 1;
-            stats[t * kBlockM + row] = make_float2(l, r);
+            stats[t * kBlockM + row] = make_float4(l_rnd, l, r, 0.f);
             mbar_arrive(bar(L::kStFull + t));
         }
     } else if (warp < 12) {
@@ -322,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = threadIdx.x & 127;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         uint32_t o_ph[2] = {0, 0}, st_ph[2] = {0, 0};
-        __nv_bfloat16* obase = reinterpret_cast<__nv_bfloat16*>(p.o);
+        float* obase = reinterpret_cast<float*>(p.o);
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
             for (int t = 0; t < 2; ++t) {
@@ -340,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (w.nk == 0) {  // no key reaches this block: O = 0, LSE = -inf
                     if (valid) {
 #pragma unroll
-                        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                        for (int i = 0; i < D / 4; ++i) dst[i] = make_uint4(0, 0, 0, 0);
                         p.lse[lidx] = -INFINITY;
                     }
                     continue;
@@ -350,10 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 if (!warp_wait(bar(L::kStFull + t), st_ph[t], abort_flag, wf, 7 + t, tile)) goto done;
                 st_ph[t] ^= 1;
-                const float2 st = stats[t * kBlockM + row];
+                const float4 st = stats[t * kBlockM + row];  // (sum of rounded p, sum of p, r)
                 mbar_arrive(bar(L::kStEmpty + t));
-                const float l = st.x;
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = st.x > 0.f ? 1.f / st.x : 0.f;
+                const float l = st.y;
                 const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * D);
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
@@ -361,23 +374,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tO + 32u * c, ov);
                     tmem_wait_ld();
                     if (valid) {
-                        uint32_t pk[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv,
-                                                __uint_as_float(ov[2 * i + 1]) * inv);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[4 * c + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        for (int i = 0; i < 8; ++i)
+                            dst[8 * c + i] = make_uint4(__float_as_uint(__uint_as_float(ov[4 * i]) * inv),
+                                                        __float_as_uint(__uint_as_float(ov[4 * i + 1]) * inv),
+                                                        __float_as_uint(__uint_as_float(ov[4 * i + 2]) * inv),
+                                                        __float_as_uint(__uint_as_float(ov[4 * i + 3]) * inv));
                     }
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::kOEmpty + t));
-                if (valid) p.lse[lidx] = l > 0.f ? (st.y + __log2f(l)) * kLn2 : -INFINITY;
+                if (valid) p.lse[lidx] = l > 0.f ? (st.z + __log2f(l)) * kLn2 : -INFINITY;
             }
         }
     } else {
-        regs_decrease<96>();
+        regs_decrease<64>();
         if (warp == 12) {
             // ============================================================ TMA producer
             if (lane == 0) {

@@ -6,7 +6,7 @@
 namespace fa {
 
 struct FwdParams {
-    void* o;           // bf16 output
+    float* o;          // fp32 output
     float* lse;        // fp32 output, natural log
     int B, Hq, Hkv;    // batch (dense only), query heads, KV heads
     int Lq, Lk;        // dense sequence lengths (unused for varlen)

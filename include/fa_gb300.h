@@ -25,7 +25,9 @@
  *    aligned, and owned by the caller.  Q, K, V are read only; O and LSE are
  *    fully overwritten (including fully masked rows and rows of empty
  *    sequences).  Output buffers must not overlap the inputs.
- *  - Q, K, V, O are bf16 (raw 16-bit storage, passed as void*); LSE is fp32.
+ *  - Q, K, V are bf16 (raw 16-bit storage, passed as void*).  O and LSE are
+ *    fp32: the kernel accumulates in fp32, and a bf16 O could not honour an
+ *    absolute error of 1e-2 once |O| >= 4 (half a bf16 ulp is 1/64 there).
  *  - Head dimension D must be 64 or 128.
  *  - The call is asynchronous on `stream` (0 = legacy default stream) and
  *    never synchronises it.  Errors detected inside a kernel (a pipeline wait
@@ -57,13 +59,13 @@ typedef enum {
  *   q   [B, Hq,  Lq, D] bf16, contiguous row-major
  *   k   [B, Hkv, Lk, D] bf16
  *   v   [B, Hkv, Lk, D] bf16
- *   o   [B, Hq,  Lq, D] bf16   (output)
+ *   o   [B, Hq,  Lq, D] fp32   (output)
  *   lse [B, Hq,  Lq]    fp32   (output, natural log)
  *
  * softmax_scale multiplies Q K^T (1/sqrt(D) is the usual choice, sec. 2
  * "Why divide by sqrt d?").  Uses no memory beyond its arguments.
  */
-fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
                    int B, int Hq, int Hkv, int Lq, int Lk, int D, int causal,
                    float softmax_scale, cudaStream_t stream);
 
@@ -72,7 +74,7 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
  * stored back to back, token-major.
  *
  *   q   [total_q, Hq,  D] bf16;  k, v [total_k, Hkv, D] bf16
- *   o   [total_q, Hq,  D] bf16   (output)
+ *   o   [total_q, Hq,  D] fp32   (output)
  *   lse [Hq, total_q]     fp32   (output, natural log)
  *   cu_seqlens_q, cu_seqlens_k: int32 DEVICE arrays of num_seqs + 1
  *     non-decreasing prefix offsets starting at 0, ending at total_q / total_k.
@@ -89,7 +91,7 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
  * releases with cudaFreeAsync on the same stream (stream-ordered, no
  * synchronisation).
  */
-fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse,
                           const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
                           int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
                           int Hq, int Hkv, int D, int causal, float softmax_scale,

@@ -30,14 +30,14 @@ def run_dense(q, k, v, causal, scale=None, canary=True):
     """Run fa_fwd with guard bands around O and LSE; check the guards."""
     B, Hq, Lq, D = q.shape
     G = 4096
-    o_buf = torch.full((B * Hq * Lq * D + 2 * G,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    o_buf = torch.full((B * Hq * Lq * D + 2 * G,), float("nan"), dtype=torch.float32, device=DEV)
     l_buf = torch.full((B * Hq * Lq + 2 * G,), 12345.0, dtype=torch.float32, device=DEV)
     o = o_buf[G:G + B * Hq * Lq * D].view(B, Hq, Lq, D)
     lse = l_buf[G:G + B * Hq * Lq].view(B, Hq, Lq)
     fa.fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, softmax_scale=scale, out=o, lse=lse)
     fa.fa_check()
     if canary:
-        assert torch.isnan(o_buf[:G].float()).all() and torch.isnan(o_buf[-G:].float()).all(), "O guard band written"
+        assert torch.isnan(o_buf[:G]).all() and torch.isnan(o_buf[-G:]).all(), "O guard band written"
         assert (l_buf[:G] == 12345.0).all() and (l_buf[-G:] == 12345.0).all(), "LSE guard band written"
     return o.float().cpu().numpy(), lse.cpu().numpy()
 
@@ -91,7 +91,7 @@ def run_varlen(lq, lk, Hq, Hkv, D, causal, seed=5):
     q, k, v = random_inputs((Tq, Hq, D), (Tk, Hkv, D), seed=seed)
     cq = torch.tensor([0] + np.cumsum(lq).tolist(), dtype=torch.int32)
     ck = torch.tensor([0] + np.cumsum(lk).tolist(), dtype=torch.int32)
-    o = torch.full((Tq, Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    o = torch.full((Tq, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
     lse = torch.full((Hq, Tq), 12345.0, dtype=torch.float32, device=DEV)
     fa.fa_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cq.to(DEV), ck.to(DEV), max(lq), max(max(lk), 1),
                      causal=causal, out=o, lse=lse)
@@ -103,14 +103,15 @@ def run_varlen(lq, lk, Hq, Hkv, D, causal, seed=5):
 def test_varlen_small_full_compare(lq, lk, Hq, Hkv, D, causal):
     q, k, v, cq, ck, o, lse = run_varlen(lq, lk, Hq, Hkv, D, causal)
     ref_o, ref_lse = oracle.attention_varlen(q, k, v, cq.numpy(), ck.numpy(), scale=1 / math.sqrt(D), causal=causal)
-    compare(o, lse, ref_o, ref_lse, f"varlen {lq} {lk}")
+    # O is [T, H, D] and LSE [H, T]: compare per head
+    compare(o.transpose(1, 0, 2), lse, ref_o.transpose(1, 0, 2), ref_lse, f"varlen {lq} {lk}")
 
 
 def test_varlen_invalid_offsets_latch_error():
     Hq, D = 2, 64
     q, k, v = random_inputs((300, Hq, D), (300, Hq, D), seed=3)
     bad = torch.tensor([0, 200, 100, 300], dtype=torch.int32, device=DEV)  # decreasing
-    o = torch.zeros((300, Hq, D), dtype=torch.bfloat16, device=DEV)
+    o = torch.zeros((300, Hq, D), dtype=torch.float32, device=DEV)
     lse = torch.zeros((Hq, 300), dtype=torch.float32, device=DEV)
     fa.fa_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), bad, bad, 300, 300, causal=True, out=o, lse=lse)
     with pytest.raises(fa.FAError) as ei:

@@ -126,5 +126,13 @@ WORKLOADS: dict[str, Workload] = {
         "varlen8_h32x8_d128_causal", 8, 32, 8, 0, 0, 128, True, seqlens=_VARLEN_LENS),
 }
 
+# A smaller case of the headline kernel for detailed profiler captures: Q, K,
+# V and O still exceed the 126 MiB L2 (32 + 32 + 32 + 64 MiB), so DRAM
+# counters stay meaningful, while one launch lasts about half a millisecond.
+PROFILE_WORKLOADS: dict[str, Workload] = {
+    "b1_h16_l8192_d128": Workload("b1_h16_l8192_d128", 1, 16, 16, 8192, 8192, 128, False),
+}
+WORKLOADS.update(PROFILE_WORKLOADS)
+
 # The configuration the throughput metric is quoted on.
 HEADLINE = "b1_h16_l16384_d128"

@@ -156,6 +156,49 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
+// MMA issue sequences of one 128 x 128 x D tile product.  The k-loops are
+// fully unrolled so that tcgen05.mma issues back to back (one 128x128x16 MMA
+// per 64 cycles); a rolled loop recomputes operands between MMAs and halves
+// the tensor-pipe rate.  They are kept out of line so that the issuing warp's
+// register budget does not grow with the number of call sites.  A descriptor
+// advanced by a byte offset is the base descriptor plus offset >> 4 (shared
+// addresses stay below 256 KB, so the 14-bit field never carries).
+
+// S_t = Q_t K^T: both operands K-major with 128-byte swizzle, 16 columns of D per MMA.
+template <int D>
+__device__ __noinline__ void mma_qk(uint32_t tmem, uint32_t sb, int t, int ks)
+{
+    using L = FwdSmem<D>;
+    constexpr int kHalves = D / 64;
+    constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false);
+    const uint64_t qd = smem_desc_sw128(sb + L::kQOff + (uint32_t)(t * L::kTileBytes), 16, 1024);
+    const uint64_t kd = smem_desc_sw128(sb + L::kKVOff + (uint32_t)(ks * L::kTileBytes), 16, 1024);
+    const uint32_t d = tmem + L::kColS + (uint32_t)(t * kBlockN);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = (uint64_t)(((kk >> 2) * (L::kTileBytes / kHalves) + (kk & 3) * 32) >> 4);
+        mma_ss(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
+    }
+}
+
+// O_t (+)= P_t V: P (bf16) from tensor memory, V MN-major with 128-byte swizzle,
+// 16 keys per MMA.
+template <int D>
+__device__ __noinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs, bool acc)
+{
+    using L = FwdSmem<D>;
+    constexpr int kHalves = D / 64;
+    constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
+    const uint64_t vd =
+        smem_desc_sw128(sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes), L::kTileBytes / kHalves, 1024);
+    const uint32_t d = tmem + L::kColO + (uint32_t)(t * D);
+    const uint32_t pa = tmem + L::kColS + (uint32_t)(t * kBlockN);
+#pragma unroll
+    for (int kk = 0; kk < kBlockN / 16; ++kk)
+        mma_ts(d, pa + (uint32_t)(kk * 8), vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+               (acc || kk > 0) ? 1u : 0u);
+}
+
 template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -458,8 +501,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == 13) {
             // ============================================================ MMA issuer
             if (lane == 0) {
-                constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false);
-                constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
                 uint32_t q_ph[2] = {0, 0}, p_ph[2] = {0, 0}, oe_ph[2] = {1, 1};
                 int stage = 0;
                 uint32_t kv_ph = 0;
@@ -472,27 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     return s;
                 };
-                // S_t = Q_t K^T over D in steps of 16 (both operands K-major, 128B swizzle)
-                auto issue_s = [&](int t, int ks) {
-                    const uint32_t qa = sb + L::kQOff + (uint32_t)(t * L::kTileBytes);
-                    const uint32_t ka = sb + L::kKVOff + (uint32_t)(ks * L::kTileBytes);
-#pragma unroll 1
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (uint32_t)((kk >> 2) * (L::kTileBytes / kHalves) + (kk & 3) * 32);
-                        mma_ss(tmem + L::kColS + (uint32_t)(t * kBlockN), smem_desc_sw128(qa + off, 16, 1024),
-                               smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-                    }
-                };
-                // O_t (+)= P_t V: P from tensor memory, V MN-major (rows of D, 128B swizzle)
-                auto issue_pv = [&](int t, int vs, bool acc) {
-                    const uint32_t va = sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes);
-#pragma unroll 1
-                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                        mma_ts(tmem + L::kColO + (uint32_t)(t * D), tmem + L::kColS + (uint32_t)(t * kBlockN + kk * 8),
-                               smem_desc_sw128(va + (uint32_t)(kk * 16 * 128), L::kTileBytes / kHalves, 1024),
-                               kIdescPV, (acc || kk > 0) ? 1u : 0u);
-                    }
-                };
+                auto issue_s = [&](int t, int ks) { mma_qk<D>(tmem, sb, t, ks); };
+                auto issue_pv = [&](int t, int vs, bool acc) { mma_pv<D>(tmem, sb, t, vs, acc); };
                 for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                     const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
                     if (w.nk == 0) continue;

@@ -156,17 +156,17 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-// MMA issue sequences of one 128 x 128 x D tile product.  The k-loops are
-// fully unrolled so that tcgen05.mma issues back to back (one 128x128x16 MMA
-// per 64 cycles); a rolled loop recomputes operands between MMAs and halves
-// the tensor-pipe rate.  They are kept out of line so that the issuing warp's
-// register budget does not grow with the number of call sites.  A descriptor
-// advanced by a byte offset is the base descriptor plus offset >> 4 (shared
-// addresses stay below 256 KB, so the 14-bit field never carries).
+// MMA issue sequences of one 128 x 128 x D tile product, executed by the whole
+// (converged) MMA warp with lane 0 issuing.  Operands computed in converged
+// code stay warp-uniform, and the k-loops are fully unrolled, so tcgen05.mma
+// issues back to back (one 128x128x16 MMA per 64 cycles); a rolled loop, or
+// operands computed by a single lane, leave the tensor pipe idle between MMAs.
+// A descriptor advanced by a byte offset is the base descriptor plus
+// offset >> 4 (shared addresses stay below 256 KB, so the field never carries).
 
 // S_t = Q_t K^T: both operands K-major with 128-byte swizzle, 16 columns of D per MMA.
 template <int D>
-__device__ __noinline__ void mma_qk(uint32_t tmem, uint32_t sb, int t, int ks)
+__device__ __forceinline__ void mma_qk(uint32_t tmem, uint32_t sb, int t, int ks, bool leader)
 {
     using L = FwdSmem<D>;
     constexpr int kHalves = D / 64;
@@ -177,14 +177,15 @@ __device__ __noinline__ void mma_qk(uint32_t tmem, uint32_t sb, int t, int ks)
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = (uint64_t)(((kk >> 2) * (L::kTileBytes / kHalves) + (kk & 3) * 32) >> 4);
-        mma_ss(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
+        if (leader) mma_ss(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
+        __syncwarp();
     }
 }
 
 // O_t (+)= P_t V: P (bf16) from tensor memory, V MN-major with 128-byte swizzle,
 // 16 keys per MMA.
 template <int D>
-__device__ __noinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs, bool acc)
+__device__ __forceinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs, bool acc, bool leader)
 {
     using L = FwdSmem<D>;
     constexpr int kHalves = D / 64;
@@ -194,9 +195,12 @@ __device__ __noinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs, b
     const uint32_t d = tmem + L::kColO + (uint32_t)(t * D);
     const uint32_t pa = tmem + L::kColS + (uint32_t)(t * kBlockN);
 #pragma unroll
-    for (int kk = 0; kk < kBlockN / 16; ++kk)
-        mma_ts(d, pa + (uint32_t)(kk * 8), vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
-               (acc || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < kBlockN / 16; ++kk) {
+        if (leader)
+            mma_ts(d, pa + (uint32_t)(kk * 8), vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                   (acc || kk > 0) ? 1u : 0u);
+        __syncwarp();
+    }
 }
 
 template <int D, bool CAUSAL, bool VARLEN>
@@ -500,94 +504,96 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         } else if (warp == 13) {
             // ============================================================ MMA issuer
-            if (lane == 0) {
-                uint32_t q_ph[2] = {0, 0}, p_ph[2] = {0, 0}, oe_ph[2] = {1, 1};
-                int stage = 0;
-                uint32_t kv_ph = 0;
-                bool issued = false;
-                auto next_stage = [&]() -> int {
-                    const int s = stage;
-                    if (++stage == L::kStages) {
-                        stage = 0;
-                        kv_ph ^= 1;
-                    }
-                    return s;
-                };
-                auto issue_s = [&](int t, int ks) { mma_qk<D>(tmem, sb, t, ks); };
-                auto issue_pv = [&](int t, int vs, bool acc) { mma_pv<D>(tmem, sb, t, vs, acc); };
-                for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                    const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
-                    if (w.nk == 0) continue;
-                    const int nk = w.nk;
-                    // prologue: S0(0), S1(0)
-                    if (!mbar_wait(bar(L::kQFull + 0), q_ph[0], abort_flag, wf, 15, tile)) break;
-                    q_ph[0] ^= 1;
-                    int ks = stage;
-                    if (!mbar_wait(bar(L::kKVFull + ks), kv_ph, abort_flag, wf, 17, tile)) break;
+            // The whole warp runs this loop; lane 0 issues every MMA and commit (a
+            // commit tracks the MMAs of the thread that executes it).
+            const bool leader = lane == 0;
+            const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+            uint32_t q_ph[2] = {0, 0}, p_ph[2] = {0, 0}, oe_ph[2] = {1, 1};
+            int stage = 0;
+            uint32_t kv_ph = 0;
+            bool issued = false;
+            auto next_stage = [&]() {
+                if (++stage == L::kStages) {
+                    stage = 0;
+                    kv_ph ^= 1;
+                }
+            };
+            auto commit = [&](int b) {
+                if (leader) tc_commit(bar(b));
+                __syncwarp();
+            };
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
+                if (w.nk == 0) continue;
+                const int nk = w.nk;
+                // prologue: S0(0), S1(0)
+                if (!warp_wait(bar(L::kQFull + 0), q_ph[0], abort_flag, wf, 15, tile)) break;
+                q_ph[0] ^= 1;
+                const int ks = stage;
+                if (!warp_wait(bar(L::kKVFull + ks), kv_ph, abort_flag, wf, 17, tile)) break;
+                next_stage();
+                tc_fence_after_sync();
+                mma_qk<D>(tm, sb, 0, ks, leader);
+                issued = true;
+                commit(L::kSFull + 0);
+                if (nk == 1) commit(L::kQEmpty + 0);
+                if (!warp_wait(bar(L::kQFull + 1), q_ph[1], abort_flag, wf, 16, tile)) break;
+                q_ph[1] ^= 1;
+                tc_fence_after_sync();
+                mma_qk<D>(tm, sb, 1, ks, leader);
+                commit(L::kSFull + 1);
+                commit(L::kKVEmpty + ks);
+                if (nk == 1) commit(L::kQEmpty + 1);
+                bool ok = true;
+                for (int j = 0; j < nk && ok; ++j) {
+                    const int vs = stage;
+                    if (!(ok = warp_wait(bar(L::kKVFull + vs), kv_ph, abort_flag, wf, 18, tile))) break;
                     next_stage();
-                    tc_fence_after_sync();
-                    issue_s(0, ks);
-                    issued = true;
-                    tc_commit(bar(L::kSFull + 0));
-                    if (nk == 1) tc_commit(bar(L::kQEmpty + 0));
-                    if (!mbar_wait(bar(L::kQFull + 1), q_ph[1], abort_flag, wf, 16, tile)) break;
-                    q_ph[1] ^= 1;
-                    tc_fence_after_sync();
-                    issue_s(1, ks);
-                    tc_commit(bar(L::kSFull + 1));
-                    tc_commit(bar(L::kKVEmpty + ks));
-                    if (nk == 1) tc_commit(bar(L::kQEmpty + 1));
-                    bool ok = true;
-                    for (int j = 0; j < nk && ok; ++j) {
-                        const int vs = stage;
-                        if (!(ok = mbar_wait(bar(L::kKVFull + vs), kv_ph, abort_flag, wf, 18, tile))) break;
-                        next_stage();
-                        // tile 0: P0(j) . V(j), then S0(j+1)
-                        if (j == 0) {
-                            if (!(ok = mbar_wait(bar(L::kOEmpty + 0), oe_ph[0], abort_flag, wf, 19, tile))) break;
-                            oe_ph[0] ^= 1;
-                        }
-                        if (!(ok = mbar_wait(bar(L::kPFull + 0), p_ph[0], abort_flag, wf, 21, tile))) break;
-                        p_ph[0] ^= 1;
-                        tc_fence_after_sync();
-                        issue_pv(0, vs, j > 0);
-                        int kn = -1;
-                        if (j + 1 < nk) {
-                            kn = stage;
-                            if (!(ok = mbar_wait(bar(L::kKVFull + kn), kv_ph, abort_flag, wf, 17, tile))) break;
-                            next_stage();
-                            issue_s(0, kn);
-                            tc_commit(bar(L::kSFull + 0));
-                            if (j + 2 == nk) tc_commit(bar(L::kQEmpty + 0));
-                        } else {
-                            tc_commit(bar(L::kOFull + 0));
-                        }
-                        // tile 1: P1(j) . V(j), then S1(j+1)
-                        if (j == 0) {
-                            if (!(ok = mbar_wait(bar(L::kOEmpty + 1), oe_ph[1], abort_flag, wf, 20, tile))) break;
-                            oe_ph[1] ^= 1;
-                        }
-                        if (!(ok = mbar_wait(bar(L::kPFull + 1), p_ph[1], abort_flag, wf, 22, tile))) break;
-                        p_ph[1] ^= 1;
-                        tc_fence_after_sync();
-                        issue_pv(1, vs, j > 0);
-                        tc_commit(bar(L::kKVEmpty + vs));
-                        if (kn >= 0) {
-                            issue_s(1, kn);
-                            tc_commit(bar(L::kSFull + 1));
-                            tc_commit(bar(L::kKVEmpty + kn));
-                            if (j + 2 == nk) tc_commit(bar(L::kQEmpty + 1));
-                        } else {
-                            tc_commit(bar(L::kOFull + 1));
-                        }
+                    // tile 0: P0(j) . V(j), then S0(j+1)
+                    if (j == 0) {
+                        if (!(ok = warp_wait(bar(L::kOEmpty + 0), oe_ph[0], abort_flag, wf, 19, tile))) break;
+                        oe_ph[0] ^= 1;
                     }
-                    if (!ok) break;
+                    if (!(ok = warp_wait(bar(L::kPFull + 0), p_ph[0], abort_flag, wf, 21, tile))) break;
+                    p_ph[0] ^= 1;
+                    tc_fence_after_sync();
+                    mma_pv<D>(tm, sb, 0, vs, j > 0, leader);
+                    int kn = -1;
+                    if (j + 1 < nk) {
+                        kn = stage;
+                        if (!(ok = warp_wait(bar(L::kKVFull + kn), kv_ph, abort_flag, wf, 17, tile))) break;
+                        next_stage();
+                        mma_qk<D>(tm, sb, 0, kn, leader);
+                        commit(L::kSFull + 0);
+                        if (j + 2 == nk) commit(L::kQEmpty + 0);
+                    } else {
+                        commit(L::kOFull + 0);
+                    }
+                    // tile 1: P1(j) . V(j), then S1(j+1)
+                    if (j == 0) {
+                        if (!(ok = warp_wait(bar(L::kOEmpty + 1), oe_ph[1], abort_flag, wf, 20, tile))) break;
+                        oe_ph[1] ^= 1;
+                    }
+                    if (!(ok = warp_wait(bar(L::kPFull + 1), p_ph[1], abort_flag, wf, 22, tile))) break;
+                    p_ph[1] ^= 1;
+                    tc_fence_after_sync();
+                    mma_pv<D>(tm, sb, 1, vs, j > 0, leader);
+                    commit(L::kKVEmpty + vs);
+                    if (kn >= 0) {
+                        mma_qk<D>(tm, sb, 1, kn, leader);
+                        commit(L::kSFull + 1);
+                        commit(L::kKVEmpty + kn);
+                        if (j + 2 == nk) commit(L::kQEmpty + 1);
+                    } else {
+                        commit(L::kOFull + 1);
+                    }
                 }
-                // every MMA this thread issued has completed before TMEM is released
-                if (issued) {
-                    tc_commit(bar(L::kDrain));
-                    mbar_settle(bar(L::kDrain), 0, wf, 23);
-                }
+                if (!ok) break;
+            }
+            // every MMA this warp issued has completed before TMEM is released
+            if (issued) {
+                commit(L::kDrain);
+                mbar_settle(bar(L::kDrain), 0, wf, 23);
             }
             __syncwarp();
         }

@@ -22,8 +22,11 @@ __device__ int g_diag[4];
 namespace {
 
 constexpr int kMaxDevices = 64;
-// Share of the 126 MB L2 that one scheduling section's K/V may occupy.
-constexpr long long kL2SectionBytes = 48ll << 20;
+// K/V bytes of one scheduling section: the whole L2.  Larger sections keep
+// the longest-first order global (what matters most for causal balance);
+// within a section, concurrently running CTAs walk the same few 256-row
+// blocks of every head, so their K/V stays L2-resident anyway.
+constexpr long long kL2SectionBytes = 128ll << 20;
 
 struct DeviceState {
     bool ready = false;

@@ -546,9 +546,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nk == 1) commit(L::kQEmpty + 1);
                 bool ok = true;
                 for (int j = 0; j < nk && ok; ++j) {
+                    // V(j) and K(j+1) are checked before P is awaited, so that P.V and the
+                    // next S issue back to back once P arrives
                     const int vs = stage;
                     if (!(ok = warp_wait(bar(L::kKVFull + vs), kv_ph, abort_flag, wf, 18, tile))) break;
                     next_stage();
+                    int kn = -1;
+                    if (j + 1 < nk) {
+                        kn = stage;
+                        if (!(ok = warp_wait(bar(L::kKVFull + kn), kv_ph, abort_flag, wf, 17, tile))) break;
+                        next_stage();
+                    }
                     // tile 0: P0(j) . V(j), then S0(j+1)
                     if (j == 0) {
                         if (!(ok = warp_wait(bar(L::kOEmpty + 0), oe_ph[0], abort_flag, wf, 19, tile))) break;
@@ -558,11 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p_ph[0] ^= 1;
                     tc_fence_after_sync();
                     mma_pv<D>(tm, sb, 0, vs, j > 0, leader);
-                    int kn = -1;
-                    if (j + 1 < nk) {
-                        kn = stage;
-                        if (!(ok = warp_wait(bar(L::kKVFull + kn), kv_ph, abort_flag, wf, 17, tile))) break;
-                        next_stage();
+                    if (kn >= 0) {
                         mma_qk<D>(tm, sb, 0, kn, leader);
                         commit(L::kSFull + 0);
                         if (j + 2 == nk) commit(L::kQEmpty + 0);

@@ -18,7 +18,7 @@ import threading
 
 import torch
 
-__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_check", "fa_status_string", "fa_last_launch_count",
+__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_check", "fa_status_string", "fa_last_launch_count",
            "FAError", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -27,7 +27,9 @@ _lock = threading.Lock()
 _lib = None
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_check", "fa_status_string", "fa_last_launch_count")
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_check", "fa_status_string",
+                    "fa_last_launch_count")
+NOALLOC_MAX_SEQS = 16384  # FA_NOALLOC_MAX_SEQS in include/fa_gb300.h
 
 
 class FAError(RuntimeError):
@@ -55,6 +57,8 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
         lib.fa_fwd_varlen.restype = i
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
+        lib.fa_fwd_varlen_noalloc.restype = i
+        lib.fa_fwd_varlen_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
         lib.fa_check.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_status_string.restype = ctypes.c_char_p
@@ -157,6 +161,35 @@ def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_
                                float(softmax_scale), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_varlen")
+    return out, lse
+
+
+def fa_fwd_varlen_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                          cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, out: torch.Tensor,
+                          lse: torch.Tensor, causal: bool = False, softmax_scale: float | None = None,
+                          stream=None):
+    """fa_fwd_varlen for callers that must not allocate device memory: the
+    schedule lives in a fixed array inside the library (at most
+    NOALLOC_MAX_SEQS sequences), and the caller provides ``out`` and ``lse``.
+    Calls that can overlap on the GPU share that array and must be ordered."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, torch.bfloat16, 3)
+    _check_tensor(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check_tensor(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    _check_tensor(out, "out", torch.float32, 3)
+    _check_tensor(lse, "lse", torch.float32, 2)
+    Tq, Hq, D = q.shape
+    Tk, Hkv, _ = k.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_varlen_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                       cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), cu_seqlens_q.numel() - 1,
+                                       Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, int(bool(causal)),
+                                       float(softmax_scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_varlen_noalloc")
     return out, lse
 
 

@@ -310,6 +310,97 @@ extern "C" fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v
     return FA_OK;
 }
 
+// ------------------------------------------------------------- allocation-free varlen
+
+// Scratch of fa_fwd_varlen_noalloc: the sequence schedule lives in this
+// fixed device array instead of memory obtained per call.  Every GPU that
+// loads the library holds it until the process exits.
+constexpr int kNoAllocMaxSeqs = FA_NOALLOC_MAX_SEQS;
+__device__ __align__(256) int g_noalloc_sched[2 + 3 * kNoAllocMaxSeqs];
+
+namespace {
+int* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_sched, per device
+
+// Resolves the array's device address on the current device (once per
+// device).  In host code the symbol names a host-side stand-in, so only the
+// address obtained here may be handed to a kernel.
+fa_status_t noalloc_scratch(int** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_sched) != cudaSuccess || !ptr) return FA_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<int*>(ptr);
+    }
+    *out = g_noalloc_ptr[dev];
+    return FA_OK;
+}
+}  // namespace
+
+extern "C" fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, float* o, float* lse,
+                                             const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                                             int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                                             int Hq, int Hkv, int D, int causal, float softmax_scale,
+                                             cudaStream_t stream)
+{
+    g_last_launches = 0;
+    if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || total_q <= 0 || total_k <= 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 || Hq <= 0 ||
+        Hkv <= 0 || D <= 0)
+        return FA_ERR_INVALID_ARG;
+    if (num_seqs > kNoAllocMaxSeqs) return FA_ERR_INVALID_ARG;  // the fixed scratch holds no more
+    if (Hq % Hkv != 0 || !scale_ok(softmax_scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+        return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    long long ub = (long long)Hq * ((long long)total_q / kRowsPerCta + num_seqs);
+    const long long ub2 = (long long)Hq * num_seqs * ((max_seqlen_q + kRowsPerCta - 1) / kRowsPerCta);
+    if (ub2 < ub) ub = ub2;
+    if ((long long)Hq * ((long long)total_q / kRowsPerCta + num_seqs) >= (1ll << 31) ||
+        (long long)total_q * Hq >= (1ll << 31) * 64ll)
+        return FA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    fa_status_t st = device_state(&ds);
+    if (st != FA_OK) return st;
+    int* sched = nullptr;
+    st = noalloc_scratch(&sched);
+    if (st != FA_OK) return st;
+
+    CUtensorMap mq, mk, mv;
+    const uint64_t row = (uint64_t)D * 2;
+    if (!encode_map(&mq, q, D, Hq, total_q, row, row * Hq, 1, 128) ||
+        !encode_map(&mk, k, D, Hkv, total_k, row, row * Hkv, 1, 128) ||
+        !encode_map(&mv, v, D, Hkv, total_k, row, row * Hkv, 1, 128))
+        return FA_ERR_CUDA;
+    // The schedule kernel writes every scratch entry the attention kernel
+    // reads, so nothing left by an earlier call needs clearing.
+    if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                               max_seqlen_k, Hq, sched, ds->err, stream) != cudaSuccess)
+        return FA_ERR_CUDA;
+    FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = Hq / Hkv;
+    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, D);
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.sched = sched;
+    p.num_seqs = num_seqs;
+    p.total_q = total_q;
+    p.err = ds->err;
+    p.diag = ds->diag;
+    const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
+    if (dispatch<true>(D, causal != 0, mq, mk, mv, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+    g_last_launches = 2;
+    return FA_OK;
+}
+
 extern "C" fa_status_t fa_check(cudaStream_t stream)
 {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;

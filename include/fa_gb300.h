@@ -98,6 +98,35 @@ fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, float* o,
                           cudaStream_t stream);
 
 /*
+ * Allocation-free variant of fa_fwd_varlen (no counterpart on the pages: it
+ * changes where the schedule lives, not what is computed).
+ *
+ * fa_fwd_varlen obtains a small schedule buffer with cudaMallocAsync on every
+ * call.  Some callers cannot allow that: code being captured into a CUDA
+ * graph where memory-pool calls are unwanted, processes that hand all device
+ * memory to their own allocator up front, or runtimes that must not allocate
+ * on the hot path.  This entry point takes the same arguments and gives the
+ * same results, but keeps the schedule in a fixed array compiled into the
+ * library (about 192 KiB, resident on every device that loads the library
+ * until the process exits).  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ *  - num_seqs may be at most FA_NOALLOC_MAX_SEQS; larger batches return
+ *    FA_ERR_INVALID_ARG before any device work.
+ *  - The first call on a device resolves the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls on a device share the one array: calls whose kernels can
+ *    overlap on the GPU (different streams without ordering between them)
+ *    race on it.  Order them on one stream, or use fa_fwd_varlen.
+ */
+#define FA_NOALLOC_MAX_SEQS 16384
+fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, float* o, float* lse,
+                                  const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                                  int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                                  int Hq, int Hkv, int D, int causal, float softmax_scale,
+                                  cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device-side error latch
  * of the current device (FA_ERR_TIMEOUT or FA_ERR_INVALID_ARG from an earlier
  * launch), or FA_ERR_CUDA if the stream reports an error.

@@ -66,6 +66,44 @@ def measured_peaks():
         return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+KERNEL_SOURCES = ("exact_attention_07_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_07_gb300/csrc/ptx_sm103.cuh",
+                  "exact_attention_07_gb300/csrc/fa_params.h")
+
+
+def kernel_source_hash(read=None) -> str:
+    """sha256 of the kernel sources with comments and blank space removed, so
+    that only code changes invalidate recorded counters."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        if read is None:
+            with open(os.path.join(ROOT, f)) as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = "\n".join(line.strip() for line in text.splitlines() if line.strip())
+        h.update(text.encode())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    or None when there is none or the kernel changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"fa_fwd_{workload}_traffic.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = dict(line.strip().split(": ", 1) for line in text.splitlines()
+                  if line.strip().startswith(("traffic_bytes_per_launch:", "kernel_source_sha256:")))
+    if fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return int(fields["traffic_bytes_per_launch"])
+
+
 def aggregate(values_per_rank: list[float], units_per_rank: list[float]) -> tuple[float, float]:
     """Whole-job throughput: total units of all ranks over the slowest rank's seconds."""
     t = max(values_per_rank)
@@ -323,7 +361,7 @@ def main(argv=None):
     peak, peak_sus, peak_kind = measured_peaks()
     achieved = flops_step / (secs / args.steps) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                 "peak_kind": f"{peak_kind} burst bf16 GEMM", "frac_of_sustained": achieved / peak_sus,
                 "kernel": "fa_fwd_sm103_kernel<%d,%s,%s>" % (w.D, str(w.causal).lower(), str(w.varlen).lower())}
 

@@ -118,7 +118,7 @@ bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
 
 // One CTA of 1024 threads.  Validates the offsets, orders sequences longest
 // key range first (the longest work tile of a sequence visits ceil(Lk/128)
-// KV tiles; FlashAttention-4 notes, "LPT scheduling", step 4) and writes the
+// KV tiles; FlashAttention-4: Blackwell Attention Kernel Co-Design, "LPT scheduling for imbalanced grids", step 4) and writes the
 // exclusive prefix of work tiles in that order.
 //
 // sched layout (int32): [0] total tiles | [1 .. n+1] prefix by schedule rank |

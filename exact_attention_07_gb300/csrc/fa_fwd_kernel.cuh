@@ -10,7 +10,7 @@
 // unnormalised accumulator A, and writes O = A / l and LSE = r + ln l once.
 // Scores S and probabilities P live only in tensor memory.
 //
-// Work split inside a CTA (FlashAttention-4 notes, "Forward TMEM pipeline"):
+// Work split inside a CTA (FlashAttention-4: Blackwell Attention Kernel Co-Design, "Forward TMEM pipeline"):
 //   warps 0-3   softmax for Q tile 0 (rows 0..127 of the CTA's 256-row block)
 //   warps 4-7   softmax for Q tile 1 (rows 128..255)
 //   warps 8-11  epilogue: O = A / l -> fp32 -> global, LSE
@@ -74,7 +74,7 @@ struct Work {
     int nk;      // number of KV tiles this block visits (0: every row is empty)
 };
 
-// Tile order (FlashAttention-4 notes, "LPT scheduling for imbalanced grids"):
+// Tile order (FlashAttention-4: Blackwell Attention Kernel Co-Design, "LPT scheduling for imbalanced grids"):
 // batches (or sequences, longest first) outermost; KV heads in L2-sized
 // sections; inside a section the 256-row blocks in reverse order when causal
 // (longest work first), then the KV head, then the query heads sharing it.

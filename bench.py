@@ -104,10 +104,22 @@ def profiled_traffic(workload: str):
     return int(fields["traffic_bytes_per_launch"])
 
 
-def aggregate(values_per_rank: list[float], units_per_rank: list[float]) -> tuple[float, float]:
-    """Whole-job throughput: total units of all ranks over the slowest rank's seconds."""
-    t = max(values_per_rank)
-    return sum(units_per_rank) / t if t > 0 else 0.0, t
+def job_rate(secs: float, units: float, world: int, device=None) -> tuple[float, float]:
+    """Whole-job throughput over all ranks: (sum of units) / (max of seconds).
+
+    Every rank passes its own timed seconds and processed units; all ranks get
+    (units per second, slowest rank's seconds).  With one rank it is local.
+    """
+    if world <= 1:
+        return (units / secs if secs > 0 else 0.0), secs
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([secs], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    secs_max, units_all = float(t.item()), float(u.item())
+    return (units_all / secs_max if secs_max > 0 else 0.0), secs_max
 
 
 # ------------------------------------------------------------------ clocks
@@ -306,15 +318,8 @@ def main(argv=None):
     fa.fa_check()
     secs = start.elapsed_time(end) / 1e3
     flops_step = w.flops()
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([secs], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        secs_max = float(tt.item())
-    else:
-        secs_max = secs
-    total_units = flops_step * args.steps * world
-    value = total_units / secs_max / 1e12
+    rate, secs_max = job_rate(secs, flops_step * args.steps, world, dev)
+    value = rate / 1e12
     ms_per_step = secs_max / args.steps * 1e3
 
     # ---- end to end through the public API with host buffers (pinned)
@@ -347,13 +352,10 @@ def main(argv=None):
         barrier()
         fa.fa_check()
         e2e_secs = s2.elapsed_time(e2_) / 1e3
-        if world > 1:
-            tt = torch.tensor([e2e_secs], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e2e_secs = float(tt.item())
+        e2e_rate, e2e_secs = job_rate(e2e_secs, flops_step * args.e2e_steps, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in pin)
         d2h = h_o.numel() * 4 + h_l.numel() * 4
-        e2e = {"value": flops_step * args.e2e_steps * world / e2e_secs / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": e2e_rate / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_secs / args.e2e_steps * 1e3}
 

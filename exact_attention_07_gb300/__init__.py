@@ -28,7 +28,7 @@ _lib = None
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_check", "fa_status_string",
-                    "fa_last_launch_count")
+                    "fa_last_launch_count", "fa_test_inject_fault")
 NOALLOC_MAX_SEQS = 16384  # FA_NOALLOC_MAX_SEQS in include/fa_gb300.h
 
 
@@ -65,6 +65,8 @@ def load_library() -> ctypes.CDLL:
         lib.fa_status_string.argtypes = [i]
         lib.fa_last_launch_count.restype = i
         lib.fa_last_launch_count.argtypes = []
+        lib.fa_test_inject_fault.restype = None
+        lib.fa_test_inject_fault.argtypes = [i]
         _lib = lib
         return lib
 

@@ -40,6 +40,7 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 thread_local int g_last_launches = 0;
+thread_local int g_fault_next = 0;  // test hook, consumed by the next fa_fwd
 
 fa_status_t device_state(DeviceState** out)
 {
@@ -240,6 +241,8 @@ extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, float
     p.num_tiles = (int)tiles;
     p.err = ds->err;
     p.diag = ds->diag;
+    p.fault = g_fault_next;
+    g_fault_next = 0;
     const int grid = (int)(tiles < ds->num_sms ? tiles : ds->num_sms);
     if (dispatch<false>(D, causal != 0, mq, mk, mv, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 1;
@@ -430,3 +433,5 @@ extern "C" const char* fa_status_string(fa_status_t s)
 }
 
 extern "C" int fa_last_launch_count(void) { return g_last_launches; }
+
+extern "C" void fa_test_inject_fault(int kind) { g_fault_next = kind; }

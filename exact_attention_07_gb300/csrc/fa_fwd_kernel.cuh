@@ -174,12 +174,14 @@ __device__ __forceinline__ void mma_qk(uint32_t tmem, uint32_t sb, int t, int ks
     const uint64_t qd = smem_desc_sw128(sb + L::kQOff + (uint32_t)(t * L::kTileBytes), 16, 1024);
     const uint64_t kd = smem_desc_sw128(sb + L::kKVOff + (uint32_t)(ks * L::kTileBytes), 16, 1024);
     const uint32_t d = tmem + L::kColS + (uint32_t)(t * kBlockN);
+    if (leader) {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = (uint64_t)(((kk >> 2) * (L::kTileBytes / kHalves) + (kk & 3) * 32) >> 4);
-        if (leader) mma_ss(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
-        __syncwarp();
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * (L::kTileBytes / kHalves) + (kk & 3) * 32) >> 4);
+            mma_ss(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
+        }
     }
+    __syncwarp();
 }
 
 // O_t (+)= P_t V: P (bf16) from tensor memory, V MN-major with 128-byte swizzle,
@@ -194,13 +196,13 @@ __device__ __forceinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs
         smem_desc_sw128(sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes), L::kTileBytes / kHalves, 1024);
     const uint32_t d = tmem + L::kColO + (uint32_t)(t * D);
     const uint32_t pa = tmem + L::kColS + (uint32_t)(t * kBlockN);
+    if (leader) {
 #pragma unroll
-    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-        if (leader)
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
             mma_ts(d, pa + (uint32_t)(kk * 8), vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
                    (acc || kk > 0) ? 1u : 0u);
-        __syncwarp();
     }
+    __syncwarp();
 }
 
 template <int D, bool CAUSAL, bool VARLEN>
@@ -466,6 +468,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 auto load_kv = [&](const CUtensorMap* map, const Work& w, int j, int tile) -> bool {
                     if (!mbar_wait(bar(L::kKVEmpty + stage), kv_ph, abort_flag, wf, 11, tile)) return false;
+                    if (p.fault == 1 && j == 0 && map == &tmK && tile == (int)blockIdx.x) {
+                        // test hook: this K tile is never armed or loaded, so the wait
+                        // for it runs out and the launch reports a timeout
+                        if (++stage == L::kStages) {
+                            stage = 0;
+                            kv_ph ^= 1;
+                        }
+                        return true;
+                    }
                     mbar_arrive_expect_tx(bar(L::kKVFull + stage), L::kTileBytes);
                     kv_armed[stage] = (int)(kv_ph ^ 1u);
                     const uint32_t dst = sb + L::kKVOff + (uint32_t)(stage * L::kTileBytes);

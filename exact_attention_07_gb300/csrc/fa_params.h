@@ -23,6 +23,7 @@ struct FwdParams {
     // error reporting
     int* err;
     int* diag;
+    int fault;  // test hook: 1 = the producer drops the first K tile of each CTA
 };
 
 // Rows of one Q tile and keys of one KV tile; a CTA owns two Q tiles.

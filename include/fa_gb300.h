@@ -142,6 +142,16 @@ const char* fa_status_string(fa_status_t status);
  */
 int fa_last_launch_count(void);
 
+/*
+ * Test hook (no counterpart on the pages).  kind = 1 makes the next fa_fwd
+ * call on this host thread drop the first K tile load of every CTA: the MMA
+ * warp's bounded wait for it runs out (about 1 s), every role of the kernel
+ * retires, and fa_check then reports FA_ERR_TIMEOUT with the CUDA context
+ * still usable.  kind = 0 clears a pending request.  Results of the faulted
+ * call are undefined.
+ */
+void fa_test_inject_fault(int kind);
+
 #ifdef __cplusplus
 }
 #endif

@@ -169,3 +169,31 @@ def test_benchmark_varlen_workload_sampled():
     l_s = lse[torch.from_numpy(h).to(DEV), torch.from_numpy(t).to(DEV)].cpu().numpy()
     compare(o_s, l_s, ref_o, ref_lse, "varlen benchmark workload")
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+# ------------------------------------------------------------------ failure detection and limits
+
+def test_timed_out_wait_is_reported_and_context_survives():
+    """A wait that never completes (the test hook drops a K tile) ends the
+    launch after its time limit with FA_ERR_TIMEOUT; the next call works."""
+    q, k, v = random_inputs((1, 4, 512, 128), (1, 4, 512, 128), seed=99)
+    lib = fa.load_library()
+    lib.fa_test_inject_fault(1)
+    fa.fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    with pytest.raises(fa.FAError) as ei:
+        fa.fa_check()
+    assert ei.value.status == fa.FA_ERR_TIMEOUT
+    o, lse = run_dense(q, k, v, True)  # same process, same context
+    ref_o, ref_lse = oracle.attention(q, k, v, scale=1 / math.sqrt(128), causal=True)
+    compare(o, lse, ref_o, ref_lse, "after timeout")
+
+
+def test_long_key_range_large_indices():
+    """Lk = 131072 keys (K and V 64 MiB each per head pair): 64-bit indexing
+    and long KV loops; Lq < Lk with bottom-right causal alignment."""
+    B, Hq, Hkv, Lq, Lk, D = 1, 2, 1, 256, 131072, 128
+    q, k, v = random_inputs((B, Hq, Lq, D), (B, Hkv, Lk, D), seed=7)
+    for causal in (False, True):
+        o, lse = run_dense(q, k, v, causal)
+        ref_o, ref_lse = oracle.attention(q, k, v, scale=1 / math.sqrt(D), causal=causal)
+        compare(o, lse, ref_o, ref_lse, f"Lk=131072 causal={causal}")

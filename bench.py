@@ -56,6 +56,17 @@ def dist_env():
     return rank, world, local
 
 
+FALLBACK_HBM_GBS = 6800.0
+
+
+def measured_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -68,15 +79,17 @@ def measured_peaks():
 
 KERNEL_SOURCES = ("exact_attention_07_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_07_gb300/csrc/ptx_sm103.cuh",
                   "exact_attention_07_gb300/csrc/fa_params.h")
+DECODE_SOURCES = ("exact_attention_07_gb300/csrc/fa_decode.cu", "exact_attention_07_gb300/csrc/ptx_sm103.cuh",
+                  "exact_attention_07_gb300/csrc/fa_decode.h")
 
 
-def kernel_source_hash(read=None) -> str:
+def kernel_source_hash(read=None, sources=KERNEL_SOURCES) -> str:
     """sha256 of the kernel sources with comments and blank space removed, so
     that only code changes invalidate recorded counters."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         if read is None:
             with open(os.path.join(ROOT, f)) as fh:
                 text = fh.read()
@@ -89,17 +102,18 @@ def kernel_source_hash(read=None) -> str:
     return h.hexdigest()
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    or None when there is none or the kernel changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"fa_fwd_{workload}_traffic.md")
+def profiled_traffic(workload: str, sources=KERNEL_SOURCES, prefix="fa_fwd"):
+    """DRAM bytes per launch (per step for decode) from the committed ncu
+    summary of this workload, or None when there is none or the kernel changed
+    since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{prefix}_{workload}_traffic.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     fields = dict(line.strip().split(": ", 1) for line in text.splitlines()
                   if line.strip().startswith(("traffic_bytes_per_launch:", "kernel_source_sha256:")))
-    if fields.get("kernel_source_sha256") != kernel_source_hash():
+    if fields.get("kernel_source_sha256") != kernel_source_hash(sources=sources):
         return None
     return int(fields["traffic_bytes_per_launch"])
 
@@ -279,6 +293,14 @@ def main(argv=None):
         def step(o=None, lse=None, qq=q, kk=k, vv=v):
             return fa.fa_fwd_varlen(qq, kk, vv, cq, ck, maxl, maxl, causal=w.causal, out=o, lse=lse)
         out_shape, lse_shape = tuple(q.shape), (w.Hq, q.shape[0])
+    elif w.decode:
+        q, k, v = (t.to(dev) for t in host_inputs)
+        ws_bytes, n_splits = fa.splitkv_workspace(w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+        def step(o=None, lse=None, qq=q, kk=k, vv=v):
+            return fa.fa_fwd_splitkv(qq, kk, vv, causal=w.causal, out=o, lse=lse, workspace=ws)
+        out_shape, lse_shape = tuple(q.shape), (w.B, w.Hq, w.Lq)
     else:
         q, k, v = (t.to(dev) for t in host_inputs)
 
@@ -336,6 +358,8 @@ def main(argv=None):
             if w.varlen:
                 fa.fa_fwd_varlen(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], maxl, maxl, causal=w.causal,
                                  out=o, lse=lse)
+            elif w.decode:
+                fa.fa_fwd_splitkv(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse, workspace=ws)
             else:
                 fa.fa_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse)
             h_o.copy_(o, non_blocking=True)
@@ -361,11 +385,25 @@ def main(argv=None):
 
     # ---- roofline of the attention kernel (the only kernel of a dense step)
     peak, peak_sus, peak_kind = measured_peaks()
-    achieved = flops_step / (secs / args.steps) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(w.name),
-                "peak_kind": f"{peak_kind} burst bf16 GEMM", "frac_of_sustained": achieved / peak_sus,
-                "kernel": "fa_fwd_sm103_kernel<%d,%s,%s>" % (w.D, str(w.causal).lower(), str(w.varlen).lower())}
+    if w.decode:
+        # HBM-bound: the least bytes of a step over the whole step's time
+        # (partial kernel + merge), so the partial kernel alone runs faster
+        # than this figure says
+        hbm, hbm_kind = measured_hbm()
+        achieved = w.hbm_bytes() / (secs / args.steps) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                    "traffic": profiled_traffic(w.name, DECODE_SOURCES, "fa_decode"),
+                    "peak_kind": f"{hbm_kind} HBM copy",
+                    "algorithmic_bytes_per_step": w.hbm_bytes(), "splits": n_splits,
+                    "kernel": "fa_decode_partial_kernel<%d,*> + fa_decode_merge_kernel<%d>" % (w.D, w.D),
+                    "timed": "whole step (both launches)"}
+    else:
+        achieved = flops_step / (secs / args.steps) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                    "peak_kind": f"{peak_kind} burst bf16 GEMM", "frac_of_sustained": achieved / peak_sus,
+                    "kernel": "fa_fwd_sm103_kernel<%d,%s,%s>" % (w.D, str(w.causal).lower(),
+                                                                str(w.varlen).lower())}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

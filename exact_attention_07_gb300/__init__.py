@@ -8,6 +8,7 @@ sm_103 GPU the call raises.
 
     o, lse = fa_fwd(q, k, v, causal=True)          # q [B,Hq,Lq,D], k/v [B,Hkv,Lk,D]
     o, lse = fa_fwd_varlen(q, k, v, cu_q, cu_k, max_q, max_k, causal=True)
+    o, lse = fa_fwd_splitkv(q, k, v, causal=True)    # decode: (Hq/Hkv)*Lq <= 16, long Lk
 """
 from __future__ import annotations
 
@@ -18,7 +19,7 @@ import threading
 
 import torch
 
-__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_check", "fa_status_string", "fa_last_launch_count",
+__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_splitkv", "splitkv_workspace", "fa_check", "fa_status_string", "fa_last_launch_count",
            "FAError", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -27,8 +28,9 @@ _lock = threading.Lock()
 _lib = None
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_check", "fa_status_string",
-                    "fa_last_launch_count", "fa_test_inject_fault")
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
+                    "fa_check", "fa_status_string", "fa_last_launch_count", "fa_test_inject_fault")
+SPLITKV_MAX_ROWS = 16  # (Hq / Hkv) * Lq limit of fa_fwd_splitkv
 NOALLOC_MAX_SEQS = 16384  # FA_NOALLOC_MAX_SEQS in include/fa_gb300.h
 
 
@@ -59,6 +61,11 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
         lib.fa_fwd_varlen_noalloc.restype = i
         lib.fa_fwd_varlen_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
+        lib.fa_fwd_splitkv.restype = i
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_splitkv_workspace.restype = i
+        lib.fa_fwd_splitkv_workspace.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t),
+                                                 ctypes.POINTER(ctypes.c_int)]
         lib.fa_check.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_status_string.restype = ctypes.c_char_p
@@ -192,6 +199,56 @@ def fa_fwd_varlen_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_
                                        float(softmax_scale), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_varlen_noalloc")
+    return out, lse
+
+
+def splitkv_workspace(B: int, Hq: int, Hkv: int, Lq: int, Lk: int, D: int, num_splits: int = 0) -> tuple[int, int]:
+    """(workspace bytes, partitions) fa_fwd_splitkv uses for this shape on the current device."""
+    nbytes, used = ctypes.c_size_t(0), ctypes.c_int(0)
+    st = load_library().fa_fwd_splitkv_workspace(B, Hq, Hkv, Lq, Lk, D, int(num_splits), ctypes.byref(nbytes),
+                                                 ctypes.byref(used))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_splitkv_workspace")
+    return int(nbytes.value), int(used.value)
+
+
+def fa_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                   softmax_scale: float | None = None, num_splits: int = 0, out: torch.Tensor | None = None,
+                   lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """Split-KV (decode) forward.  q [B,Hq,Lq,D], k/v [B,Hkv,Lk,D] bf16 CUDA with
+    (Hq/Hkv)*Lq <= 16.  ``num_splits`` <= 0 lets the library choose.  The
+    partial-result workspace is taken from ``workspace`` (a CUDA uint8 tensor)
+    or allocated here through PyTorch.  Returns (o fp32, lse fp32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, torch.bfloat16, 4)
+    B, Hq, Lq, D = q.shape
+    Bk, Hkv, Lk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    _check_tensor(out, "out", torch.float32, 4)
+    _check_tensor(lse, "lse", torch.float32, 3)
+    if tuple(out.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Lq):
+        raise ValueError("out/lse shape mismatch")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        nbytes, _ = splitkv_workspace(B, Hq, Hkv, Lq, Lk, D, num_splits)
+        if nbytes and (workspace is None or workspace.numel() * workspace.element_size() < nbytes):
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        ws_ptr = workspace.data_ptr() if (nbytes and workspace is not None) else None
+        ws_len = workspace.numel() * workspace.element_size() if ws_ptr else 0
+        st = lib.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                B, Hq, Hkv, Lq, Lk, D, int(bool(causal)), float(softmax_scale), int(num_splits),
+                                ws_ptr, ws_len, _stream_handle(stream))
+        if ws_ptr and isinstance(stream, torch.cuda.Stream):
+            workspace.record_stream(stream)  # keep the block out of reuse until that stream is done
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_splitkv")
     return out, lse
 
 

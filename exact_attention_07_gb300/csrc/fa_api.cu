@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/fa_gb300.h"
+#include "fa_decode.h"
 #include "fa_launch.h"
 #include "fa_params.h"
 
@@ -401,6 +402,147 @@ extern "C" fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const
     const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
     if (dispatch<true>(D, causal != 0, mq, mk, mv, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 2;
+    return FA_OK;
+}
+
+// ------------------------------------------------------------- split-KV decode
+
+namespace {
+
+constexpr int kMaxSplits = 1024;
+
+struct SplitPlan {
+    int R = 0, rpt = 0, num_tiles = 0, splits = 1, tiles_per_split = 0;
+    size_t ws_bytes = 0;
+};
+
+fa_status_t splitkv_validate(int B, int Hq, int Hkv, int Lq, int Lk, int D)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if ((long long)(Hq / Hkv) * Lq > kDecMaxRows) return FA_ERR_UNSUPPORTED;
+    if ((long long)B * Hq * Lq >= (1ll << 31) || (long long)B * Hkv >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+// Partitions of the key range.  The pages leave the count to the workload:
+// more partitions fill more SMs but add partial results and a merge.  The
+// automatic choice minimises a small cost model in units of one 64-key tile
+// per CTA slot: waves of CTAs over the GPU's resident slots times the tiles
+// of one partition (+2 for pipeline fill), plus the merge (a launch and the
+// partial-result bytes spread over the whole GPU).
+void splitkv_plan(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_splits, int num_sms, SplitPlan* pl)
+{
+    pl->R = (Hq / Hkv) * Lq;
+    pl->rpt = decode_rows_per_thread(D, pl->R);
+    pl->num_tiles = (Lk + kDecKeys - 1) / kDecKeys;
+    const int nkt = pl->num_tiles;
+    const long long bh = (long long)B * Hkv;
+    int splits = 1;
+    if (num_splits > 0) {
+        splits = num_splits < nkt ? num_splits : nkt;
+    } else {
+        const long long slots = (long long)num_sms * decode_ctas_per_sm(D, pl->rpt);
+        const double tile_bytes = 2.0 * kDecKeys * D * 2;
+        double best = 1e300;
+        for (int s = 1; s <= nkt && s <= kMaxSplits; ++s) {
+            const int tps = (nkt + s - 1) / s;
+            if ((nkt + tps - 1) / tps != s) continue;  // same partition as a smaller count
+            if (bh * s >= (1ll << 31)) break;
+            const long long waves = (bh * s + slots - 1) / slots;
+            double cost = (double)waves * (tps + 2.0);
+            if (s > 1) cost += 2.0 + (double)bh * s * pl->R * (D + 1) * 8.0 / ((double)slots * tile_bytes);
+            if (cost < best * (1.0 - 1e-9)) {
+                best = cost;
+                splits = s;
+            }
+        }
+    }
+    pl->tiles_per_split = (nkt + splits - 1) / splits;
+    pl->splits = (nkt + pl->tiles_per_split - 1) / pl->tiles_per_split;  // no empty partition
+    pl->ws_bytes = 0;
+    if (pl->splits > 1) {
+        const size_t rows = (size_t)bh * pl->splits * pl->R;
+        pl->ws_bytes = ((rows * D + rows) * sizeof(float) + 255) & ~(size_t)255;
+    }
+}
+
+}  // namespace
+
+extern "C" fa_status_t fa_fwd_splitkv_workspace(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_splits,
+                                                size_t* workspace_bytes, int* splits_used)
+{
+    if (!workspace_bytes) return FA_ERR_INVALID_ARG;
+    fa_status_t st = splitkv_validate(B, Hq, Hkv, Lq, Lk, D);
+    if (st != FA_OK) return st;
+    DeviceState* ds = nullptr;
+    st = device_state(&ds);
+    if (st != FA_OK) return st;
+    SplitPlan pl;
+    splitkv_plan(B, Hq, Hkv, Lq, Lk, D, num_splits, ds->num_sms, &pl);
+    if ((long long)B * Hkv * pl.splits >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    *workspace_bytes = pl.ws_bytes;
+    if (splits_used) *splits_used = pl.splits;
+    return FA_OK;
+}
+
+extern "C" fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                                      int Hq, int Hkv, int Lq, int Lk, int D, int causal, float softmax_scale,
+                                      int num_splits, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream)
+{
+    g_last_launches = 0;
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    fa_status_t st = splitkv_validate(B, Hq, Hkv, Lq, Lk, D);
+    if (st != FA_OK) return st;
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    st = device_state(&ds);
+    if (st != FA_OK) return st;
+    SplitPlan pl;
+    splitkv_plan(B, Hq, Hkv, Lq, Lk, D, num_splits, ds->num_sms, &pl);
+    const long long grid = (long long)B * Hkv * pl.splits;
+    if (pl.rpt == 0 || grid >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    if (pl.ws_bytes > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < pl.ws_bytes))
+        return FA_ERR_INVALID_ARG;
+
+    CUtensorMap mk, mv;
+    const uint64_t row = (uint64_t)D * 2;
+    if (!encode_map(&mk, k, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kDecKeys, 1) ||
+        !encode_map(&mv, v, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kDecKeys, 1))
+        return FA_ERR_CUDA;
+
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.o = o;
+    p.lse = lse;
+    if (pl.splits > 1) {
+        const size_t rows = (size_t)grid * pl.R;
+        p.o_part = static_cast<float*>(workspace);
+        p.l_part = p.o_part + rows * D;
+    }
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lq = Lq;
+    p.Lk = Lk;
+    p.group = Hq / Hkv;
+    p.R = pl.R;
+    p.num_splits = pl.splits;
+    p.tiles_per_split = pl.tiles_per_split;
+    p.num_tiles = pl.num_tiles;
+    p.causal = causal != 0;
+    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+    p.err = ds->err;
+    p.diag = ds->diag;
+    p.fault = g_fault_next;
+    g_fault_next = 0;
+    if (launch_decode_partial(D, pl.rpt, mk, mv, p, (int)grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (pl.splits > 1 && launch_decode_merge(D, p, stream) != cudaSuccess) return FA_ERR_CUDA;
+    g_last_launches = pl.splits > 1 ? 2 : 1;
     return FA_OK;
 }
 

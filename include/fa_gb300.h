@@ -39,6 +39,7 @@
 #define FA_GB300_H
 
 #include <cuda_runtime_api.h>
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -127,6 +128,47 @@ fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, f
                                   cudaStream_t stream);
 
 /*
+ * Split-KV forward for decode (FlashAttention from Scratch, sec. 9.1 "Split
+ * the long dimension that remains"; sec. 4.3 "Merge independently computed
+ * partitions").  Same operation, layouts and causal rule as fa_fwd, for
+ * problems with few query rows per KV head and a long key range: the key
+ * range of every (batch, KV head) is cut into num_splits partitions that run
+ * as independent CTAs, each producing a normalised partial output and its
+ * log-sum-exp, and a second kernel merges the partitions by their softmax
+ * mass.  All (Hq / Hkv) * Lq query rows that share a KV head are served by
+ * one pass over its K and V.
+ *
+ *   q   [B, Hq,  Lq, D] bf16;  k, v [B, Hkv, Lk, D] bf16
+ *   o   [B, Hq,  Lq, D] fp32 (output);  lse [B, Hq, Lq] fp32 (output, natural log)
+ *   (Hq / Hkv) * Lq must be at most 16, else FA_ERR_UNSUPPORTED (use fa_fwd).
+ *   num_splits: partitions of the key range; <= 0 picks a count from the
+ *     shape and the device's SM count; values above ceil(Lk / 64) are reduced
+ *     to it (a partition holds whole 64-key tiles).
+ *   workspace: caller-owned DEVICE memory of at least the size that
+ *     fa_fwd_splitkv_workspace reports for the same shape and num_splits
+ *     (16-byte aligned; may be NULL when that size is 0, i.e. one partition).
+ *     It holds the partial results between the two kernels; no memory is
+ *     allocated by the call.  Calls that overlap on the GPU need separate
+ *     workspaces.
+ *
+ * Launches 1 kernel (one partition) or 2 (partials, then the merge).
+ * Arithmetic is fp32 throughout (bf16 inputs widened exactly).
+ */
+fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, float* o, float* lse,
+                           int B, int Hq, int Hkv, int Lq, int Lk, int D, int causal,
+                           float softmax_scale, int num_splits, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Workspace bytes fa_fwd_splitkv needs for this shape and num_splits on the
+ * CURRENT device (the automatic count depends on its SM count), written to
+ * *workspace_bytes; *splits_used (if not NULL) receives the partition count
+ * the call will use.  Same argument checks as fa_fwd_splitkv.
+ */
+fa_status_t fa_fwd_splitkv_workspace(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_splits,
+                                     size_t* workspace_bytes, int* splits_used);
+
+/*
  * Synchronises `stream`, then returns and clears the device-side error latch
  * of the current device (FA_ERR_TIMEOUT or FA_ERR_INVALID_ARG from an earlier
  * launch), or FA_ERR_CUDA if the stream reports an error.
@@ -137,17 +179,18 @@ fa_status_t fa_check(cudaStream_t stream);
 const char* fa_status_string(fa_status_t status);
 
 /*
- * Number of kernels the last successful fa_fwd / fa_fwd_varlen call on this
- * host thread launched (1 for dense, 2 for varlen: schedule + attention).
+ * Number of kernels the last successful forward call on this host thread
+ * launched (1 for dense, 2 for varlen: schedule + attention; 1 or 2 for
+ * split-KV: partials, then the merge when there is more than one partition).
  */
 int fa_last_launch_count(void);
 
 /*
  * Test hook (no counterpart on the pages).  kind = 1 makes the next fa_fwd
- * call on this host thread drop the first K tile load of every CTA: the MMA
- * warp's bounded wait for it runs out (about 1 s), every role of the kernel
- * retires, and fa_check then reports FA_ERR_TIMEOUT with the CUDA context
- * still usable.  kind = 0 clears a pending request.  Results of the faulted
+ * (or fa_fwd_splitkv) call on this host thread drop the first K tile load
+ * (split-KV: the first K/V tile) of every CTA: the bounded wait for it runs out (about 1 s), every thread of
+ * the kernel retires, and fa_check then reports FA_ERR_TIMEOUT with the CUDA
+ * context still usable.  kind = 0 clears a pending request.  Results of the faulted
  * call are undefined.
  */
 void fa_test_inject_fault(int kind);

@@ -1,6 +1,6 @@
 """Shared helpers of the GPU parity tests: tolerances and comparisons.
 
-Tolerances (bf16 inputs, fp32 accumulation, bf16 O): O max-abs <= 1e-2 and
+Tolerances (bf16 inputs, fp32 accumulation and output): O max-abs <= 1e-2 and
 relative RMS <= 5e-3 against the fp64 oracle; LSE max-abs <= 1e-3 on rows
 with at least one allowed key, and exactly -inf (with O == 0) on rows with
 none.

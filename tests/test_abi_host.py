@@ -81,3 +81,27 @@ def test_varlen_argument_validation(lib):
     assert call(cu_k=34) == INV                      # int32 offsets must be 4-byte aligned
     assert call(scale=-1.0) == INV
     assert call(D=80) == UNS
+
+
+def test_splitkv_argument_validation(lib):
+    INV, UNS = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+
+    def call(q=16, o=16, B=2, Hq=8, Hkv=2, Lq=1, Lk=100, D=128, scale=0.1, splits=0):
+        return lib.fa_fwd_splitkv(q, 16, 16, o, 16, B, Hq, Hkv, Lq, Lk, D, 0, scale, splits, None, 0, None)
+
+    assert call(q=None) == INV
+    assert call(o=None) == INV
+    assert call(B=0) == INV
+    assert call(Lk=0) == INV
+    assert call(Lq=-3) == INV
+    assert call(Hq=6, Hkv=4) == INV
+    assert call(scale=float("nan")) == INV
+    assert call(o=40) == INV                         # misaligned output
+    assert call(D=96) == UNS
+    assert call(Hq=32, Hkv=1) == UNS                 # 32 query rows per KV head
+    assert call(Hq=8, Hkv=2, Lq=5) == UNS            # 4 heads x 5 rows = 20 > 16
+    n = ctypes.c_size_t(0)
+    assert lib.fa_fwd_splitkv_workspace(2, 8, 2, 1, 100, 128, 0, None, None) == INV
+    assert lib.fa_fwd_splitkv_workspace(2, 64, 2, 1, 100, 128, 0, ctypes.byref(n), None) == UNS
+    assert lib.fa_fwd_splitkv_workspace(2, 8, 2, 1, 100, 80, 0, ctypes.byref(n), None) == UNS
+    assert lib.fa_last_launch_count() == 0

@@ -39,6 +39,9 @@ class Workload:
     seed: int = 0
     # variable-length batches: per-sequence lengths (Lq/Lk above are unused)
     seqlens: tuple[int, ...] | None = None
+    # decode-shaped problem (few query rows per KV head, long key range) that
+    # runs through the split-KV forward
+    decode: bool = False
 
     @property
     def scale(self) -> float:
@@ -60,6 +63,13 @@ class Workload:
         else:
             total = 4.0 * self.B * self.Hq * self.Lq * self.Lk * self.D
         return total / 2 if self.causal else total
+
+    def hbm_bytes(self) -> float:
+        """Least device-memory traffic of one forward: Q, K, V read once (bf16),
+        O (fp32) and LSE (fp32) written once."""
+        assert not self.varlen
+        qo = self.B * self.Hq * self.Lq
+        return 2.0 * qo * self.D + 4.0 * self.B * self.Hkv * self.Lk * self.D + 4.0 * qo * self.D + 4.0 * qo
 
 
 def varlen_lengths(n: int = 8, lo: int = 512, hi: int = 8192, seed: int = 0) -> list[int]:
@@ -133,6 +143,17 @@ PROFILE_WORKLOADS: dict[str, Workload] = {
     "b1_h16_l8192_d128": Workload("b1_h16_l8192_d128", 1, 16, 16, 8192, 8192, 128, False),
 }
 WORKLOADS.update(PROFILE_WORKLOADS)
+
+# Decode through the split-KV forward: one new token per sequence, GQA with
+# four query heads per KV head, a 32768-token KV cache per sequence (K and V
+# together 1 GiB, eight times the L2).  Shaped after the single-token GQA
+# decode the pages discuss; no causal flag, since with one query row at the
+# end of the cache every key is visible either way.
+DECODE_WORKLOADS: dict[str, Workload] = {
+    "decode_b8_h32x8_l32768_d128": Workload("decode_b8_h32x8_l32768_d128", 8, 32, 8, 1, 32768, 128, False,
+                                            decode=True),
+}
+WORKLOADS.update(DECODE_WORKLOADS)
 
 # The configuration the throughput metric is quoted on.
 HEADLINE = "b1_h16_l16384_d128"

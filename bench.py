@@ -79,8 +79,8 @@ def measured_peaks():
 
 KERNEL_SOURCES = ("exact_attention_07_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_07_gb300/csrc/ptx_sm103.cuh",
                   "exact_attention_07_gb300/csrc/fa_params.h")
-DECODE_SOURCES = ("exact_attention_07_gb300/csrc/fa_decode.cu", "exact_attention_07_gb300/csrc/ptx_sm103.cuh",
-                  "exact_attention_07_gb300/csrc/fa_decode.h")
+DECODE_SOURCES = ("exact_attention_07_gb300/csrc/fa_decode_tc.cu", "exact_attention_07_gb300/csrc/fa_decode.cu",
+                  "exact_attention_07_gb300/csrc/ptx_sm103.cuh", "exact_attention_07_gb300/csrc/fa_decode.h")
 
 
 def kernel_source_hash(read=None, sources=KERNEL_SOURCES) -> str:
@@ -395,7 +395,8 @@ def main(argv=None):
                     "traffic": profiled_traffic(w.name, DECODE_SOURCES, "fa_decode"),
                     "peak_kind": f"{hbm_kind} HBM copy",
                     "algorithmic_bytes_per_step": w.hbm_bytes(), "splits": n_splits,
-                    "kernel": "fa_decode_partial_kernel<%d,*> + fa_decode_merge_kernel<%d>" % (w.D, w.D),
+                    "kernel": ("fa_decode_tc_kernel" if w.D == 128 and w.Hq // w.Hkv * w.Lq >= 2
+                               else "fa_decode_partial_kernel<%d,*>" % w.D) + " + fa_decode_merge_kernel<%d>" % w.D,
                     "timed": "whole step (both launches)"}
     else:
         achieved = flops_step / (secs / args.steps) / 1e12

@@ -413,6 +413,7 @@ constexpr int kMaxSplits = 1024;
 
 struct SplitPlan {
     int R = 0, rpt = 0, num_tiles = 0, splits = 1, tiles_per_split = 0;
+    bool tensor = false;  // tensor-core partials (128-key tiles) instead of the FP32-pipe kernel
     size_t ws_bytes = 0;
 };
 
@@ -428,23 +429,25 @@ fa_status_t splitkv_validate(int B, int Hq, int Hkv, int Lq, int Lk, int D)
 
 // Partitions of the key range.  The pages leave the count to the workload:
 // more partitions fill more SMs but add partial results and a merge.  The
-// automatic choice minimises a small cost model in units of one 64-key tile
-// per CTA slot: waves of CTAs over the GPU's resident slots times the tiles
-// of one partition (+2 for pipeline fill), plus the merge (a launch and the
+// automatic choice minimises a small cost model in units of one tile per CTA
+// slot: waves of work items over the GPU's resident slots times the tiles of
+// one partition (+2 for pipeline fill), plus the merge (a launch and the
 // partial-result bytes spread over the whole GPU).
 void splitkv_plan(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_splits, int num_sms, SplitPlan* pl)
 {
     pl->R = (Hq / Hkv) * Lq;
+    pl->tensor = D == 128 && pl->R >= 2;
     pl->rpt = decode_rows_per_thread(D, pl->R);
-    pl->num_tiles = (Lk + kDecKeys - 1) / kDecKeys;
+    const int keys = pl->tensor ? kDecTcKeys : kDecKeys;
+    pl->num_tiles = (Lk + keys - 1) / keys;
     const int nkt = pl->num_tiles;
     const long long bh = (long long)B * Hkv;
     int splits = 1;
     if (num_splits > 0) {
         splits = num_splits < nkt ? num_splits : nkt;
     } else {
-        const long long slots = (long long)num_sms * decode_ctas_per_sm(D, pl->rpt);
-        const double tile_bytes = 2.0 * kDecKeys * D * 2;
+        const long long slots = (long long)num_sms * (pl->tensor ? 1 : decode_ctas_per_sm(D, pl->rpt));
+        const double tile_bytes = 2.0 * keys * D * 2;
         double best = 1e300;
         for (int s = 1; s <= nkt && s <= kMaxSplits; ++s) {
             const int tps = (nkt + s - 1) / s;
@@ -509,11 +512,14 @@ extern "C" fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* 
     if (pl.ws_bytes > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < pl.ws_bytes))
         return FA_ERR_INVALID_ARG;
 
-    CUtensorMap mk, mv;
+    CUtensorMap mq, mk, mv;
     const uint64_t row = (uint64_t)D * 2;
-    if (!encode_map(&mk, k, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kDecKeys, 1) ||
-        !encode_map(&mv, v, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kDecKeys, 1))
+    const uint32_t box_keys = pl.tensor ? kDecTcKeys : kDecKeys;
+    if (!encode_map(&mk, k, D, Lk, (uint64_t)B * Hkv, row, row * Lk, box_keys, 1) ||
+        !encode_map(&mv, v, D, Lk, (uint64_t)B * Hkv, row, row * Lk, box_keys, 1))
         return FA_ERR_CUDA;
+    const uint64_t q_rows = (uint64_t)B * Hq * Lq;
+    if (pl.tensor && !encode_map(&mq, q, D, q_rows, 1, row, row * q_rows, kDecMaxRows, 1)) return FA_ERR_CUDA;
 
     DecodeParams p{};
     p.q = static_cast<const uint16_t*>(q);
@@ -540,7 +546,12 @@ extern "C" fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* 
     p.diag = ds->diag;
     p.fault = g_fault_next;
     g_fault_next = 0;
-    if (launch_decode_partial(D, pl.rpt, mk, mv, p, (int)grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (pl.tensor) {
+        const int g = (int)(grid < ds->num_sms ? grid : ds->num_sms);
+        if (launch_decode_tc(mq, mk, mv, p, g, stream) != cudaSuccess) return FA_ERR_CUDA;
+    } else if (launch_decode_partial(D, pl.rpt, mk, mv, p, (int)grid, stream) != cudaSuccess) {
+        return FA_ERR_CUDA;
+    }
     if (pl.splits > 1 && launch_decode_merge(D, p, stream) != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = pl.splits > 1 ? 2 : 1;
     return FA_OK;

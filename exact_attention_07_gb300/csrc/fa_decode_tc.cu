@@ -1,0 +1,530 @@
+// Split-KV decode partials on the fifth-generation tensor cores (sm_103a, D = 128).
+//
+// Grouped-query decode has R = (Hq / Hkv) * Lq query rows per KV head (up to
+// 16 here).  Packing those rows into one work tile fills a matrix
+// instruction's otherwise mostly empty query dimension (FlashAttention from
+// Scratch, sec. 9.2 "GQA changes the reuse opportunity").  Keys take the
+// 128-row side of the MMA and the packed query rows the 16-column side:
+//
+//     S^T [128 keys x 16 rows] = K_tile [128 x D] . Q^T [D x 16]
+//     O^T [D x 16 rows]       += V_tile^T [D x 128] . P^T [128 keys x 16]
+//
+// both accumulating in tensor memory.  The tensor core does the contraction
+// at a small fraction of its rate, so the kernel is bound by streaming K and
+// V from HBM; the FP32-pipe variant (fa_decode.cu) runs out of issue slots
+// first once R reaches 4.
+//
+// Roles (192 threads, one persistent CTA per SM, work items = (batch, KV
+// head, key partition) in a strided order):
+//   warps 0-3  softmax: thread k owns TMEM lane k -- key k of the tile for
+//              S^T, output dimension k for O^T.  Row maxima across the 128
+//              keys go through a transposing warp reduction and a four-warp
+//              exchange in shared memory; P^T is written to shared memory in
+//              the operand layout; O^T is rescaled in place when a row's
+//              reference moves; the epilogue normalises and stores.
+//   warp  4    TMA producer: Q rows of the item, then K and V tiles in a ring.
+//   warp  5    MMA issuer and tensor-memory owner.
+// The online-softmax state follows the dense kernel: base-2 exponentials,
+// a per-row reference r that moves only when a tile maximum exceeds it by
+// more than 8, the bf16-rounded probability sum to normalise O and the fp32
+// sum for the log-sum-exp (FlashAttention from Scratch, sec. 4.2 and sec. 11.3).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "fa_decode.h"
+#include "ptx_sm103.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr int kTcD = 128;              // head dimension of this kernel
+constexpr int kTcKeys = 128;           // keys per tile (the MMA's M)
+constexpr int kTcRows = 16;            // packed query rows (the MMA's N)
+constexpr int kTcSlots = 6;            // K/V ring slots (one tile of K or V each)
+constexpr int kTcThreads = 192;
+constexpr int kSlotBytes = kTcKeys * kTcD * 2;   // 32 KB
+constexpr int kHalfBytes = kSlotBytes / 2;       // one 64-dimension box
+constexpr int kQBytes = kTcRows * kTcD * 2;      // 4 KB: 16 rows, two 64-dimension boxes
+constexpr int kPBytes = kTcRows * kTcKeys * 2;   // 4 KB: P^T, two 64-key swizzle atoms
+
+struct TcSmem {
+    static constexpr int kSlots = 0;
+    static constexpr int kQ = kSlots + kTcSlots * kSlotBytes;  // [2] Q buffers
+    static constexpr int kP = kQ + 2 * kQBytes;                // [2] P^T buffers
+    static constexpr int kRed = kP + 2 * kPBytes;              // float [2][4][16] row maxima
+    static constexpr int kEpi = kRed + 2 * 4 * 16 * 4;         // float [4][32] row sums
+    static constexpr int kBars = kEpi + 4 * 32 * 4;
+    // barrier slots
+    static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kTcSlots;
+    static constexpr int bSFull = 4 + 2 * kTcSlots, bSEmpty = bSFull + 2, bPFull = bSFull + 4,
+                         bPEmpty = bSFull + 6, bOFull = bSFull + 8, bOEmpty = bSFull + 9,
+                         bRed = bSFull + 10, bEpi = bSFull + 12, bDrain = bSFull + 13, kNumBars = bSFull + 14;
+    static constexpr int kMisc = kBars + kNumBars * 8;  // tmem base, abort flag
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kDynamic = kBytes + 1024;
+};
+static_assert(TcSmem::kDynamic <= 232448, "shared memory of one CTA");
+
+// TMEM columns: S^T double buffer, then O^T.
+constexpr uint32_t kColS = 0, kColO = 2 * kTcRows, kTmemCols = 64;
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+// Generic-proxy shared-memory writes become visible to the tensor core's
+// (async proxy) operand reads.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v)
+{
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ bool tc_warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             const WaitFailure& wf, int site, int item)
+{
+    const bool ok = mbar_wait(bar, parity, abort_flag, wf, site, item);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Reduces 16 per-lane values (one per query row) across the warp with a
+// transposing butterfly: each exchange halves the rows a lane carries, so
+// 16 + 8 + 4 + 2 + 1 values cross lanes instead of 16 * 5.  Returns, in
+// every lane, the reduction of row (lane >> 1) over all 32 lanes.
+template <bool MAX>
+__device__ __forceinline__ float transpose_reduce16(const float (&v)[16], int lane)
+{
+    auto op = [](float a, float b) { return MAX ? fmaxf(a, b) : a + b; };
+    float a[8], b[4], c[2];
+    const bool h4 = lane & 16, h3 = lane & 8, h2 = lane & 4, h1 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float send = h4 ? v[i] : v[i + 8], keep = h4 ? v[i + 8] : v[i];
+        a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = h3 ? a[i] : a[i + 4], keep = h3 ? a[i + 4] : a[i];
+        b[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = h2 ? b[i] : b[i + 2], keep = h2 ? b[i + 2] : b[i];
+        c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    }
+    const float send = h1 ? c[0] : c[1], keep = h1 ? c[1] : c[0];
+    float d = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    return op(d, __shfl_xor_sync(0xffffffffu, d, 1));
+}
+
+struct TcItem {
+    int bh, split, t0, n;
+    long long row0;
+};
+
+__device__ __forceinline__ TcItem tc_item(const DecodeParams& p, int it)
+{
+    TcItem w;
+    w.bh = it / p.num_splits;
+    w.split = it - w.bh * p.num_splits;
+    w.t0 = w.split * p.tiles_per_split;
+    w.n = min(p.num_tiles - w.t0, p.tiles_per_split);
+    const int b = w.bh / p.Hkv, hkv = w.bh - b * p.Hkv;
+    w.row0 = ((long long)b * p.Hq + (long long)hkv * p.group) * p.Lq;
+    return w;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const DecodeParams p)
+{
+    using L = TcSmem;
+    constexpr float kTau = 8.0f;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+    float* red = reinterpret_cast<float*>(smem + L::kRed);
+    float* epi = reinterpret_cast<float*>(smem + L::kEpi);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WaitFailure wf{p.err, p.diag};
+    const int num_items = p.B * p.Hkv * p.num_splits;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(L::bQFull + i), 1);
+            mbar_init(bar(L::bQEmpty + i), 1);
+            mbar_init(bar(L::bSFull + i), 1);
+            mbar_init(bar(L::bSEmpty + i), 128);
+            mbar_init(bar(L::bPFull + i), 128);
+            mbar_init(bar(L::bPEmpty + i), 1);
+            mbar_init(bar(L::bRed + i), 128);
+        }
+        for (int s = 0; s < kTcSlots; ++s) {
+            mbar_init(bar(L::bKVFull + s), 1);
+            mbar_init(bar(L::bKVEmpty + s), 1);
+        }
+        mbar_init(bar(L::bOFull), 1);
+        mbar_init(bar(L::bOEmpty), 128);
+        mbar_init(bar(L::bEpi), 128);
+        mbar_init(bar(L::bDrain), 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmV);
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        // ============================================================ softmax
+        const int k = threadIdx.x;  // TMEM lane: key of the tile / output dimension
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int causal_off = p.Lk - p.Lq;
+        // last key each row may see (bottom-right causal alignment, padding at Lk)
+        int lim[kTcRows];
+        int lim_min = p.Lk - 1;
+#pragma unroll
+        for (int r = 0; r < kTcRows; ++r) {
+            lim[r] = p.causal ? min(p.Lk - 1, (r % p.Lq) + causal_off) : p.Lk - 1;
+            if (r < p.R) lim_min = min(lim_min, lim[r]);
+        }
+        uint32_t T = 0;
+        int I = 0;
+        for (int it = blockIdx.x; it < num_items; it += gridDim.x, ++I) {
+            const TcItem w = tc_item(p, it);
+            float ref[kTcRows], lf[kTcRows], lb[kTcRows];
+#pragma unroll
+            for (int r = 0; r < kTcRows; ++r) {
+                ref[r] = -INFINITY;
+                lf[r] = 0.f;
+                lb[r] = 0.f;
+            }
+            for (int t = 0; t < w.n; ++t, ++T) {
+                const uint32_t b = T & 1u, ph = (T >> 1) & 1u;
+                if (!tc_warp_wait(bar(L::bSFull + b), ph, abort_flag, wf, 60, it)) goto done;
+                tc_fence_after_sync();
+                float s[kTcRows];
+                tmem_ld16(lane_base + kColS + b * kTcRows, s);
+                tmem_wait_ld();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::bSEmpty + b));
+                const int key_base = (w.t0 + t) * kTcKeys;
+#pragma unroll
+                for (int r = 0; r < kTcRows; ++r) s[r] *= p.scale_log2;
+                if (key_base + kTcKeys - 1 > lim_min) {  // tile reaches masked keys
+#pragma unroll
+                    for (int r = 0; r < kTcRows; ++r)
+                        if (key_base + k > lim[r]) s[r] = -INFINITY;
+                }
+                // tile maximum of every row over the 128 keys
+                const float wm = transpose_reduce16<true>(s, lane);
+                float* rb = red + b * 64;
+                if ((lane & 1) == 0) rb[warp * 16 + (lane >> 1)] = wm;
+                mbar_arrive(bar(L::bRed + b));
+                if (!tc_warp_wait(bar(L::bRed + b), ph, abort_flag, wf, 61, it)) goto done;
+                float tm_lane = -INFINITY;
+                if (lane < 16)
+                    tm_lane = fmaxf(fmaxf(rb[lane], rb[16 + lane]), fmaxf(rb[32 + lane], rb[48 + lane]));
+                float alpha[kTcRows];
+                bool moved = false;
+#pragma unroll
+                for (int r = 0; r < kTcRows; ++r) {
+                    const float tm = __shfl_sync(0xffffffffu, tm_lane, r);
+                    alpha[r] = 1.f;
+                    if (tm > ref[r] + kTau) {  // also when ref is still -inf and the tile has a key
+                        alpha[r] = ex2_approx(ref[r] - tm);
+                        ref[r] = tm;
+                        moved = true;
+                    }
+                }
+                // probabilities, rounded to bf16 for the MMA; both sums
+                uint32_t pk[kTcRows / 2];
+#pragma unroll
+                for (int r = 0; r < kTcRows; r += 2) {
+                    const float p0 = ref[r] == -INFINITY ? 0.f : ex2_approx(s[r] - ref[r]);
+                    const float p1 = ref[r + 1] == -INFINITY ? 0.f : ex2_approx(s[r + 1] - ref[r + 1]);
+                    __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+                    pk[r / 2] = *reinterpret_cast<uint32_t*>(&h);
+                    lf[r] = fmaf(lf[r], alpha[r], p0);
+                    lf[r + 1] = fmaf(lf[r + 1], alpha[r + 1], p1);
+                    lb[r] = fmaf(lb[r], alpha[r], __uint_as_float(pk[r / 2] << 16));
+                    lb[r + 1] = fmaf(lb[r + 1], alpha[r + 1], __uint_as_float(pk[r / 2] & 0xffff0000u));
+                }
+                // P^T buffer b is free once P.V of tile T - 2 has completed
+                if (!tc_warp_wait(bar(L::bPEmpty + b), ph ^ 1u, abort_flag, wf, 62, it)) goto done;
+                {
+                    const uint32_t pb = sb + L::kP + b * kPBytes + (uint32_t)((k >> 6) * (kPBytes / 2)) +
+                                        (uint32_t)((k & 7) * 2);
+                    const int chunk = (k & 63) >> 3;
+#pragma unroll
+                    for (int r = 0; r < kTcRows; ++r) {
+                        const uint16_t h = (r & 1) ? (uint16_t)(pk[r / 2] >> 16) : (uint16_t)(pk[r / 2] & 0xffffu);
+                        sts16(pb + (uint32_t)(r * 128 + ((chunk ^ (r & 7)) << 4)), h);
+                    }
+                }
+                fence_proxy_async_smem();
+                if (moved && t > 0) {
+                    // O^T holds tiles up to T - 1: wait for that P.V, then rescale in place
+                    const uint32_t bp = (T - 1) & 1u, php = ((T - 1) >> 1) & 1u;
+                    if (!tc_warp_wait(bar(L::bPEmpty + bp), php, abort_flag, wf, 63, it)) goto done;
+                    tc_fence_after_sync();
+                    float o[kTcRows];
+                    tmem_ld16(lane_base + kColO, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int r = 0; r < kTcRows; ++r) o[r] *= alpha[r];
+                    tmem_st16(lane_base + kColO, o);
+                    tmem_wait_st();
+                }
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::bPFull + b));
+            }
+            // ---- epilogue of the item: O = O^T / l_rounded, LSE = r + log2(l)
+            if (!tc_warp_wait(bar(L::bOFull), (uint32_t)(I & 1), abort_flag, wf, 64, it)) goto done;
+            tc_fence_after_sync();
+            float o[kTcRows];
+            tmem_ld16(lane_base + kColO, o);
+            tmem_wait_ld();
+            tc_fence_before_sync();
+            mbar_arrive(bar(L::bOEmpty));
+            {
+                const float sb_w = transpose_reduce16<false>(lb, lane);
+                const float sf_w = transpose_reduce16<false>(lf, lane);
+                if ((lane & 1) == 0) {
+                    epi[warp * 32 + (lane >> 1)] = sb_w;
+                    epi[warp * 32 + 16 + (lane >> 1)] = sf_w;
+                }
+            }
+            mbar_arrive(bar(L::bEpi));
+            if (!tc_warp_wait(bar(L::bEpi), (uint32_t)(I & 1), abort_flag, wf, 65, it)) goto done;
+            const float lsum = epi[lane] + epi[32 + lane] + epi[64 + lane] + epi[96 + lane];  // lane<16: rounded, else fp32
+            const bool single = p.num_splits == 1;
+#pragma unroll
+            for (int r = 0; r < kTcRows; ++r) {
+                const float l_r = __shfl_sync(0xffffffffu, lsum, r);
+                const float lf_r = __shfl_sync(0xffffffffu, lsum, 16 + r);
+                if (r < p.R) {
+                    const float val = l_r > 0.f ? o[r] / l_r : 0.f;
+                    if (single)
+                        p.o[(w.row0 + r) * kTcD + k] = val;
+                    else
+                        p.o_part[((long long)it * p.R + r) * kTcD + k] = val;
+                    if (k == r) {
+                        const float lse2 = lf_r > 0.f ? ref[r] + log2f(lf_r) : -INFINITY;
+                        if (single)
+                            p.lse[w.row0 + r] = lse2 * 0.6931471805599453f;
+                        else
+                            p.l_part[(long long)it * p.R + r] = lse2;
+                    }
+                }
+            }
+        }
+    } else if (warp == 4) {
+        // ============================================================ TMA producer
+        if (lane == 0) {
+            int q_armed[2] = {-1, -1};
+            int kv_armed[kTcSlots];
+            for (int s = 0; s < kTcSlots; ++s) kv_armed[s] = -1;
+            int stage = 0;
+            uint32_t kv_ph = 0;
+            bool drop_first = p.fault == 1;  // test hook: the first K tile never arrives
+            int I = 0;
+            auto load = [&](const CUtensorMap* map, int key0, int bh, int it) -> bool {
+                if (!mbar_wait(bar(L::bKVEmpty + stage), kv_ph ^ 1u, abort_flag, wf, 66, it)) return false;
+                if (drop_first) {
+                    drop_first = false;
+                } else {
+                    mbar_arrive_expect_tx(bar(L::bKVFull + stage), kSlotBytes);
+                    kv_armed[stage] = (int)kv_ph;
+                    const uint32_t dst = sb + L::kSlots + (uint32_t)(stage * kSlotBytes);
+                    tma_load_3d(dst, map, bar(L::bKVFull + stage), 0, key0, bh);
+                    tma_load_3d(dst + kHalfBytes, map, bar(L::bKVFull + stage), 64, key0, bh);
+                }
+                if (++stage == kTcSlots) {
+                    stage = 0;
+                    kv_ph ^= 1u;
+                }
+                return true;
+            };
+            for (int it = blockIdx.x; it < num_items; it += gridDim.x, ++I) {
+                const TcItem w = tc_item(p, it);
+                const int qb = I & 1;
+                const uint32_t qph = (uint32_t)((I >> 1) & 1);
+                if (!mbar_wait(bar(L::bQEmpty + qb), qph ^ 1u, abort_flag, wf, 67, it)) break;
+                mbar_arrive_expect_tx(bar(L::bQFull + qb), kQBytes);
+                q_armed[qb] = (int)qph;
+                const uint32_t qdst = sb + L::kQ + (uint32_t)(qb * kQBytes);
+                tma_load_3d(qdst, &tmQ, bar(L::bQFull + qb), 0, (int)w.row0, 0);
+                tma_load_3d(qdst + kQBytes / 2, &tmQ, bar(L::bQFull + qb), 64, (int)w.row0, 0);
+                bool ok = true;
+                for (int t = 0; t < w.n && ok; ++t) {
+                    const int key0 = (w.t0 + t) * kTcKeys;
+                    ok = load(&tmK, key0, w.bh, it) && load(&tmV, key0, w.bh, it);
+                }
+                if (!ok) break;
+            }
+            // every copy this thread started has landed before the CTA retires
+            for (int i = 0; i < 2; ++i)
+                if (q_armed[i] >= 0) mbar_settle(bar(L::bQFull + i), (uint32_t)q_armed[i], wf, 68);
+            for (int s = 0; s < kTcSlots; ++s)
+                if (kv_armed[s] >= 0) mbar_settle(bar(L::bKVFull + s), (uint32_t)kv_armed[s], wf, 69);
+        }
+        __syncwarp();
+    } else {
+        // ============================================================ MMA issuer (warp 5)
+        const bool leader = lane == 0;
+        const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+        constexpr uint32_t kIdescS = idesc_bf16_f32(kTcKeys, kTcRows, false);
+        constexpr uint32_t kIdescPV = idesc_bf16_f32(kTcD, kTcRows, false) | (1u << 15);  // A (V^T) MN-major
+        int stage = 0;
+        uint32_t kv_ph = 0;
+        uint32_t T = 0;
+        bool issued = false;
+        auto commit = [&](int b) {
+            if (leader) tc_commit(bar(b));
+            __syncwarp();
+        };
+        // O^T (+)= V^T P^T for tile Tp; V in slot vs (phase vph)
+        auto pv = [&](uint32_t Tp, int vs, uint32_t vph, bool first, int I, int it) -> bool {
+            const uint32_t bp = Tp & 1u;
+            if (!tc_warp_wait(bar(L::bKVFull + vs), vph, abort_flag, wf, 70, it)) return false;
+            if (!tc_warp_wait(bar(L::bPFull + bp), (Tp >> 1) & 1u, abort_flag, wf, 71, it)) return false;
+            if (first && !tc_warp_wait(bar(L::bOEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 72, it))
+                return false;
+            tc_fence_after_sync();
+            const uint64_t vd = smem_desc_sw128(sb + L::kSlots + (uint32_t)(vs * kSlotBytes), kHalfBytes, 1024);
+            const uint64_t pd = smem_desc_sw128(sb + L::kP + bp * kPBytes, 16, 1024);
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                    const uint64_t poff = (uint64_t)(((kk >> 2) * (kPBytes / 2) + (kk & 3) * 32) >> 4);
+                    mma_ss(tm + kColO, vd + (uint64_t)((kk * 16 * 128) >> 4), pd + poff, kIdescPV,
+                           (first && kk == 0) ? 0u : 1u);
+                }
+            }
+            __syncwarp();
+            commit(L::bPEmpty + bp);
+            commit(L::bKVEmpty + vs);
+            return true;
+        };
+        int I = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++I) {
+            const TcItem w = tc_item(p, it);
+            const int qb = I & 1;
+            if (!tc_warp_wait(bar(L::bQFull + qb), (uint32_t)((I >> 1) & 1), abort_flag, wf, 73, it)) break;
+            const uint64_t qd = smem_desc_sw128(sb + L::kQ + (uint32_t)(qb * kQBytes), 16, 1024);
+            int vs_prev = 0;
+            uint32_t vph_prev = 0;
+            for (int t = 0; t < w.n; ++t, ++T) {
+                const int ks = stage;
+                if (!(ok = tc_warp_wait(bar(L::bKVFull + ks), kv_ph, abort_flag, wf, 74, it))) break;
+                if (++stage == kTcSlots) {
+                    stage = 0;
+                    kv_ph ^= 1u;
+                }
+                const uint32_t b = T & 1u;
+                if (!(ok = tc_warp_wait(bar(L::bSEmpty + b), ((T >> 1) & 1u) ^ 1u, abort_flag, wf, 75, it))) break;
+                tc_fence_after_sync();
+                const uint64_t kd = smem_desc_sw128(sb + L::kSlots + (uint32_t)(ks * kSlotBytes), 16, 1024);
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < kTcD / 16; ++kk) {
+                        const uint64_t koff = (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+                        const uint64_t qoff = (uint64_t)(((kk >> 2) * (kQBytes / 2) + (kk & 3) * 32) >> 4);
+                        mma_ss(tm + kColS + b * kTcRows, kd + koff, qd + qoff, kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                }
+                __syncwarp();
+                issued = true;
+                commit(L::bSFull + b);
+                commit(L::bKVEmpty + ks);
+                if (t == w.n - 1) commit(L::bQEmpty + qb);
+                if (t > 0 && !(ok = pv(T - 1, vs_prev, vph_prev, t == 1, I, it))) break;
+                vs_prev = stage;  // V of this tile follows its K in the ring
+                vph_prev = kv_ph;
+                if (++stage == kTcSlots) {
+                    stage = 0;
+                    kv_ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (!(ok = pv(T - 1, vs_prev, vph_prev, w.n == 1, I, it))) break;
+            commit(L::bOFull);
+        }
+        // every MMA this warp issued has completed before TMEM is released
+        if (issued) {
+            commit(L::bDrain);
+            mbar_settle(bar(L::bDrain), 0, wf, 76);
+        }
+        __syncwarp();
+    }
+done:
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+cudaError_t launch_decode_tc(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                             const DecodeParams& p, int grid, cudaStream_t stream)
+{
+    const cudaError_t e =
+        cudaFuncSetAttribute(fa_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kDynamic);
+    if (e != cudaSuccess) return e;
+    fa_decode_tc_kernel<<<grid, kTcThreads, TcSmem::kDynamic, stream>>>(q, k, v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -71,13 +71,14 @@ def test_splitkv_full_compare(B, Hq, Hkv, Lq, Lk, D, causal, splits, qm):
     o, lse = run_splitkv(q, k, v, causal, splits)
     _, used = fa.splitkv_workspace(B, Hq, Hkv, Lq, Lk, D, splits)
     assert fa.fa_last_launch_count() == (2 if used > 1 else 1)
-    assert 1 <= used <= math.ceil(Lk / 64)
+    assert 1 <= used <= math.ceil(Lk / 64)  # partitions hold whole tiles (64 or 128 keys)
     ref_o, ref_lse = oracle.attention(q, k, v, scale=1 / math.sqrt(D), causal=causal)
     compare(o, lse, ref_o, ref_lse, f"splitkv {B,Hq,Hkv,Lq,Lk,D,causal,splits,qm}")
-    # P stays in fp32 on this path: far inside the bf16-P tolerance
-    fin = np.isfinite(ref_lse)
-    assert np.abs(o - ref_o).max() <= 1e-3
-    assert np.abs(lse[fin] - ref_lse[fin]).max() <= 1e-4 if fin.any() else True
+    if D == 64 or (Hq // Hkv) * Lq == 1:
+        # the FP32-pipe kernel keeps P in fp32: far inside the bf16-P tolerance
+        fin = np.isfinite(ref_lse)
+        assert np.abs(o - ref_o).max() <= 1e-3
+        assert np.abs(lse[fin] - ref_lse[fin]).max() <= 1e-4 if fin.any() else True
 
 
 def test_partition_count_does_not_change_the_result_beyond_rounding():
@@ -89,8 +90,10 @@ def test_partition_count_does_not_change_the_result_beyond_rounding():
         o, lse = run_splitkv(q, k, v, False, splits)
         compare(o, lse, ref_o, ref_lse, f"splits={splits}")
         outs.append(o)
+    # P is rounded to bf16 against each partition's own running reference, so
+    # partition counts differ by bf16 rounding of P (about 2^-9 relative)
     for o in outs[1:]:
-        assert np.abs(o - outs[0]).max() <= 1e-4
+        assert np.abs(o - outs[0]).max() <= 1e-3
 
 
 def test_custom_scale_and_repeat_calls_identical():
@@ -118,17 +121,18 @@ def test_workspace_too_small_is_rejected():
     assert st == fa.FA_ERR_INVALID_ARG
 
 
-def test_timed_out_wait_is_reported_and_context_survives():
+@pytest.mark.parametrize("Hq,D", [(4, 128), (4, 64)])  # tensor-core and FP32-pipe partial kernels
+def test_timed_out_wait_is_reported_and_context_survives(Hq, D):
     """The test hook drops the first K/V tile of every CTA: the bounded wait
     runs out, the launch retires with FA_ERR_TIMEOUT, the next call works."""
-    q, k, v = random_inputs((1, 4, 1, 128), (1, 1, 1024, 128), seed=4)
+    q, k, v = random_inputs((1, Hq, 1, D), (1, 1, 1024, D), seed=4)
     fa.load_library().fa_test_inject_fault(1)
     fa.fa_fwd_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), num_splits=2)
     with pytest.raises(fa.FAError) as ei:
         fa.fa_check()
     assert ei.value.status == fa.FA_ERR_TIMEOUT
     o, lse = run_splitkv(q, k, v, False, 2)
-    ref_o, ref_lse = oracle.attention(q, k, v, scale=1 / math.sqrt(128), causal=False)
+    ref_o, ref_lse = oracle.attention(q, k, v, scale=1 / math.sqrt(D), causal=False)
     compare(o, lse, ref_o, ref_lse, "after timeout")
 
 

@@ -1,0 +1,122 @@
+"""fp64 oracle for the attention backward pass -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this module.  Nothing here is shared with the CUDA path.
+
+The loss is L = sum(O * dO) for a given upstream gradient dO (so dO is
+dL/dO).  With the scale c, the mask M (0 or -inf) and, per (batch, query
+head) slice, S = c Q K^T + M, P = softmax_rows(S), O = P V, the gradients are
+the plain definitions (FlashAttention from Scratch, sec. 8 "Backward: spend
+arithmetic to save memory"):
+
+    dV = P^T dO
+    dP = dO V^T
+    delta_i = sum_t P_it dP_it = O_i . dO_i
+    dS = P * (dP - delta)          (row-wise delta)
+    dQ = c dS K,    dK = c dS^T Q
+
+Grouped-query attention: the gradient of a KV head is the sum over the query
+heads that read it (sec. 9.2).  Causal masking is bottom-right aligned, as in
+the forward oracle.  Query rows with no allowed key have P = 0 and
+contribute nothing.
+
+:func:`attention_bwd` evaluates these definitions with materialised S and P,
+one block of query rows at a time (numpy matrix products in fp64), and can
+restrict the returned rows of dQ and of dK/dV to samples so that full-size
+problems can be checked.  :func:`blocked_backward` follows the pages' own
+recomputation order instead (reconstruct P from the saved log-sum-exp tile
+by tile and accumulate each gradient from tile products); the tests pin the
+two against each other, against finite differences and against closed forms.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .reference import allowed_mask, scores, softmax_rows
+
+
+def _f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().float().cpu().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def attention_bwd(q, k, v, do, scale: float, causal: bool = False, q_rows=None, k_rows=None,
+                  block: int = 1024):
+    """Gradients (dq, dk, dv) of sum(O * do) for dense [B, H, L, D] inputs.
+
+    q [B, Hq, Lq, D]; k, v [B, Hkv, Lk, D]; do [B, Hq, Lq, D].  With q_rows
+    (flat indices into B*Hq*Lq) dq is returned only for those rows, shape
+    [n, D]; with k_rows (flat indices into B*Hkv*Lk) dk and dv only for those
+    rows.  Without them the full tensors come back in float64.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, Lq, D = q.shape
+    _, Hkv, Lk, _ = k.shape
+    r = Hq // Hkv
+    mask_all = allowed_mask(Lq, Lk, causal, q_start=Lk - Lq, k_start=0)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    want_q = None if q_rows is None else set(int(x) for x in np.asarray(q_rows).ravel())
+    want_kv_heads = None
+    if k_rows is not None:
+        kr = np.asarray(k_rows).ravel()
+        want_kv_heads = set(int(x) for x in kr // Lk)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // r
+            bh = b * Hq + h
+            need_q = want_q is None or any(bh * Lq <= x < (bh + 1) * Lq for x in want_q)
+            need_kv = want_kv_heads is None or (b * Hkv + hk) in want_kv_heads
+            if not (need_q or need_kv):
+                continue
+            K, V = k[b, hk], v[b, hk]
+            for i0 in range(0, Lq, block):
+                i1 = min(Lq, i0 + block)
+                Q, G = q[b, h, i0:i1], do[b, h, i0:i1]
+                s = (Q @ K.T) * scale
+                s = np.where(mask_all[i0:i1], s, -np.inf)
+                p = softmax_rows(s)
+                o = p @ V
+                delta = (o * G).sum(axis=1)
+                dp = G @ V.T
+                ds = p * (dp - delta[:, None])
+                if need_q:
+                    dq[b, h, i0:i1] = scale * (ds @ K)
+                if need_kv:
+                    dk[b, hk] += scale * (ds.T @ Q)
+                    dv[b, hk] += p.T @ G
+    if q_rows is not None:
+        dq = dq.reshape(-1, D)[np.asarray(q_rows).ravel()]
+    if k_rows is not None:
+        idx = np.asarray(k_rows).ravel()
+        dk = dk.reshape(-1, D)[idx]
+        dv = dv.reshape(-1, v.shape[-1])[idx]
+    return dq, dk, dv
+
+
+def blocked_backward(q, k, v, o, lse, do, scale: float, block_q: int = 32, block_k: int = 64,
+                     causal: bool = False, q_start: int = 0, k_start: int = 0):
+    """Backward of one (batch, head) slice in the recomputation order of the
+    pages: delta from the saved output, P rebuilt tile by tile from the saved
+    natural-log LSE, and the gradient tiles accumulated per (query block, key
+    block) pair.  q [Nq, d], k [Nk, d], v [Nk, dv]; positions q_start/k_start
+    give the causal mask (key position <= query position)."""
+    q, k, v, o, lse, do = (_f64(x) for x in (q, k, v, o, lse, do))
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    delta = (o * do).sum(axis=1)
+    # a row with no allowed key has lse = -inf; shifting by 0 keeps exp(-inf) = 0
+    shift = np.where(np.isfinite(lse), lse, 0.0)
+    for i in range(0, q.shape[0], block_q):
+        rows = slice(i, i + block_q)
+        for j in range(0, k.shape[0], block_k):
+            cols = slice(j, j + block_k)
+            s = scores(q[rows], k[cols], scale, causal, q_start + i, k_start + j)
+            p = np.exp(s - shift[rows, None])
+            dp = do[rows] @ v[cols].T
+            ds = p * (dp - delta[rows, None])
+            dq[rows] += scale * (ds @ k[cols])
+            dk[cols] += scale * (ds.T @ q[rows])
+            dv[cols] += p.T @ do[rows]
+    return dq, dk, dv

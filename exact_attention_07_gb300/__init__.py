@@ -9,6 +9,7 @@ sm_103 GPU the call raises.
     o, lse = fa_fwd(q, k, v, causal=True)          # q [B,Hq,Lq,D], k/v [B,Hkv,Lk,D]
     o, lse = fa_fwd_varlen(q, k, v, cu_q, cu_k, max_q, max_k, causal=True)
     o, lse = fa_fwd_splitkv(q, k, v, causal=True)    # decode: (Hq/Hkv)*Lq <= 16, long Lk
+    dq, dk, dv = fa_bwd(q, k, v, o, lse, do, causal=True)
 """
 from __future__ import annotations
 
@@ -19,7 +20,8 @@ import threading
 
 import torch
 
-__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_splitkv", "splitkv_workspace", "fa_check", "fa_status_string", "fa_last_launch_count",
+__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_splitkv", "splitkv_workspace", "fa_bwd",
+           "bwd_workspace", "fa_check", "fa_status_string", "fa_last_launch_count",
            "FAError", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -29,7 +31,7 @@ _lib = None
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
-                    "fa_check", "fa_status_string", "fa_last_launch_count", "fa_test_inject_fault")
+                    "fa_bwd", "fa_bwd_workspace", "fa_check", "fa_status_string", "fa_last_launch_count", "fa_test_inject_fault")
 SPLITKV_MAX_ROWS = 16  # (Hq / Hkv) * Lq limit of fa_fwd_splitkv
 NOALLOC_MAX_SEQS = 16384  # FA_NOALLOC_MAX_SEQS in include/fa_gb300.h
 
@@ -66,6 +68,10 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd_splitkv_workspace.restype = i
         lib.fa_fwd_splitkv_workspace.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t),
                                                  ctypes.POINTER(ctypes.c_int)]
+        lib.fa_bwd.restype = i
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
+        lib.fa_bwd_workspace.restype = i
+        lib.fa_bwd_workspace.argtypes = [i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         lib.fa_check.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_status_string.restype = ctypes.c_char_p
@@ -250,6 +256,55 @@ def fa_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bo
     if st != FA_OK:
         raise FAError(st, "fa_fwd_splitkv")
     return out, lse
+
+
+def bwd_workspace(B: int, Hq: int, Lq: int) -> int:
+    """Workspace bytes fa_bwd needs."""
+    nbytes = ctypes.c_size_t(0)
+    st = load_library().fa_bwd_workspace(B, Hq, Lq, ctypes.byref(nbytes))
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd_workspace")
+    return int(nbytes.value)
+
+
+def fa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+           dout: torch.Tensor, causal: bool = False, softmax_scale: float | None = None,
+           dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
+           workspace: torch.Tensor | None = None, stream=None):
+    """Backward of fa_fwd.  q/dout [B,Hq,Lq,D], k/v [B,Hkv,Lk,D] bf16; o fp32
+    [B,Hq,Lq,D] and lse fp32 [B,Hq,Lq] from fa_fwd.  Returns (dq, dk, dv) fp32."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _check_tensor(t, n, torch.bfloat16, 4)
+    _check_tensor(o, "o", torch.float32, 4)
+    _check_tensor(lse, "lse", torch.float32, 3)
+    B, Hq, Lq, D = q.shape
+    Bk, Hkv, Lk, Dk = k.shape
+    if (tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D or tuple(dout.shape) != tuple(q.shape)
+            or tuple(o.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Lq)):
+        raise ValueError("shape mismatch")
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=torch.float32, device=q.device) if dv is None else dv
+    for t, n, shp in ((dq, "dq", q.shape), (dk, "dk", k.shape), (dv, "dv", k.shape)):
+        _check_tensor(t, n, torch.float32, 4)
+        if tuple(t.shape) != tuple(shp):
+            raise ValueError(f"{n} shape mismatch")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        nbytes = bwd_workspace(B, Hq, Lq)
+        if workspace is None or workspace.numel() * workspace.element_size() < nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        st = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Lq, Lk, D, int(bool(causal)),
+                        float(softmax_scale), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        _stream_handle(stream))
+        if isinstance(stream, torch.cuda.Stream):
+            workspace.record_stream(stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd")
+    return dq, dk, dv
 
 
 def fa_check(stream=None) -> int:

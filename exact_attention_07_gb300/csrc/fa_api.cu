@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/fa_gb300.h"
+#include "fa_bwd.h"
 #include "fa_decode.h"
 #include "fa_launch.h"
 #include "fa_params.h"
@@ -554,6 +555,88 @@ extern "C" fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* 
     }
     if (pl.splits > 1 && launch_decode_merge(D, p, stream) != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = pl.splits > 1 ? 2 : 1;
+    return FA_OK;
+}
+
+// ------------------------------------------------------------- backward
+
+namespace {
+long long bwd_rows_padded(int Lq) { return ((long long)Lq + kBwdTile - 1) / kBwdTile * kBwdTile; }
+}  // namespace
+
+extern "C" fa_status_t fa_bwd_workspace(int B, int Hq, int Lq, size_t* workspace_bytes)
+{
+    if (!workspace_bytes || B <= 0 || Hq <= 0 || Lq <= 0) return FA_ERR_INVALID_ARG;
+    const long long rows = (long long)B * Hq * bwd_rows_padded(Lq);
+    if (rows >= (1ll << 40)) return FA_ERR_INVALID_ARG;
+    *workspace_bytes = (size_t)((2 * rows * (long long)sizeof(float) + 255) & ~255ll);
+    return FA_OK;
+}
+
+extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                              const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq,
+                              int Lk, int D, int causal, float softmax_scale, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream)
+{
+    g_last_launches = 0;
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !scale_ok(softmax_scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+        return FA_ERR_INVALID_ARG;
+    if (D != 128) return FA_ERR_UNSUPPORTED;
+    const long long lq_pad = bwd_rows_padded(Lq);
+    const long long rows = (long long)B * Hq * lq_pad;
+    if (rows >= (1ll << 31) || (long long)B * Hq >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    const long long kv_tiles = ((long long)Lk + kBwdTile - 1) / kBwdTile;
+    const long long items = (long long)B * Hkv * kv_tiles;
+    if (items >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    size_t need = 0;
+    fa_bwd_workspace(B, Hq, Lq, &need);
+    if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    fa_status_t st = device_state(&ds);
+    if (st != FA_OK) return st;
+
+    CUtensorMap mq, mk, mv, mdo;
+    const uint64_t row = (uint64_t)D * 2;
+    if (!encode_map(&mq, q, D, Lq, (uint64_t)B * Hq, row, row * Lq, kBwdTile, 1) ||
+        !encode_map(&mdo, dout, D, Lq, (uint64_t)B * Hq, row, row * Lq, kBwdTile, 1) ||
+        !encode_map(&mk, k, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kBwdTile, 1) ||
+        !encode_map(&mv, v, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kBwdTile, 1))
+        return FA_ERR_CUDA;
+
+    BwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.dout = static_cast<const uint16_t*>(dout);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.delta = static_cast<float*>(workspace);
+    p.lse2 = p.delta + rows;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lq = Lq;
+    p.Lk = Lk;
+    p.Lq_pad = (int)lq_pad;
+    p.group = Hq / Hkv;
+    p.num_kv_tiles = (int)kv_tiles;
+    p.num_q_tiles = (int)(lq_pad / kBwdTile);
+    p.num_items = (int)items;
+    p.scale = softmax_scale;
+    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+    p.causal = causal != 0;
+    p.err = ds->err;
+    p.diag = ds->diag;
+    p.fault = g_fault_next;
+    g_fault_next = 0;
+    if (launch_bwd_pre(D, p, stream) != cudaSuccess) return FA_ERR_CUDA;
+    const int grid = (int)(items < ds->num_sms ? items : ds->num_sms);
+    if (launch_bwd(D, causal != 0, mq, mk, mv, mdo, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+    g_last_launches = 2;
     return FA_OK;
 }
 

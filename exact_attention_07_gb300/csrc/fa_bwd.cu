@@ -1,0 +1,587 @@
+// Attention backward for sm_103a (D = 128): recompute P from the saved
+// log-sum-exp and form the five matrix products of the gradient on the
+// tcgen05 tensor cores (FlashAttention from Scratch, sec. 8 "Backward: spend
+// arithmetic to save memory"; FlashAttention-4: Blackwell Attention Kernel
+// Co-Design, "TMEM backward pipeline").
+//
+// With c the softmax scale, per (batch, query head):
+//   delta_i = O_i . dO_i                       (preprocess kernel)
+//   P^T  = 2^(c log2e K Q^T - lse2)            S^T = K Q^T on the tensor core
+//   dP^T = V dO^T                              tensor core
+//   dV  += P^T dO                              tensor core, P^T from TMEM
+//   dS^T = c P^T * (dP^T - delta)              softmax warps, bf16 to shared memory
+//   dK  += dS^T Q                              tensor core
+//   dQ  += dS K                                tensor core, then fp32 atomics to global
+//
+// Ownership (sec. 8, "A GPU backward must handle competing ownership
+// requirements"): a CTA owns one 128-key tile of one KV head and loops over
+// every query head of its group and every Q tile that can see the keys, so
+// dK and dV are finished in tensor memory without atomics (grouped-query
+// heads add into the same accumulators); dQ needs a reduction over key tiles
+// and is added to global memory with vector fp32 reductions.  Q-tile order is
+// rotated by the key-tile index so that CTAs of the same head do not all add
+// into the same dQ rows at the same time.
+//
+// Tensor memory (512 columns): [0,128) S^T, overwritten by P^T (bf16 pairs);
+// [128,256) dP^T, then the dQ partial of the same step; [256,384) dV;
+// [384,512) dK.  Shared memory: K and V of the tile, a 2-stage ring of
+// (Q, dO) tiles, and one dS^T tile that serves as the K-major A operand of
+// dK and, read the other way, the MN-major A operand of dQ.
+//
+// Roles (320 threads, one persistent CTA per SM):
+//   warps 0-3  thread k owns key k of the tile: P^T and dS^T
+//   warps 4-7  thread q owns query row q: reads the dQ partial out of TMEM
+//              and reduces it into global dQ; at the end of a work item
+//              (thread = key) writes dK and dV
+//   warp  8    TMA producer      warp 9  MMA issuer, TMEM owner
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "fa_bwd.h"
+#include "ptx_sm103.cuh"
+
+namespace fa {
+
+// ------------------------------------------------------------------ preprocess
+
+// One warp per (batch * head, row) of the padded row range: delta = O . dO,
+// lse2 = LSE * log2(e) (+inf where the row saw no key, so that P = 0), and
+// the row of dQ zeroed for the reductions of the main kernel.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p)
+{
+    constexpr int V = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * 8 + warp;  // over B*Hq*Lq_pad
+    if (row >= (long long)p.B * p.Hq * p.Lq_pad) return;
+    const long long bh = row / p.Lq_pad;
+    const int i = (int)(row - bh * p.Lq_pad);
+    float delta = 0.f, l2 = INFINITY;
+    if (i < p.Lq) {
+        const long long r = bh * p.Lq + i;
+        const float* o = p.o + r * D + lane * V;
+        const uint16_t* g = p.dout + r * D + lane * V;
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc = fmaf(o[e], __uint_as_float((uint32_t)g[e] << 16), acc);
+#pragma unroll
+        for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+        delta = acc;
+        const float l = p.lse[r];
+        l2 = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+        float* dq = p.dq + r * D + lane * V;
+#pragma unroll
+        for (int e = 0; e < V; ++e) dq[e] = 0.f;
+    }
+    if (lane == 0) {
+        p.delta[row] = delta;
+        p.lse2[row] = l2;
+    }
+}
+
+namespace {
+
+constexpr int kBwdD = 128;
+constexpr int kBwdThreads = 320;
+constexpr int kTileBytes = kBwdTile * kBwdD * 2;  // 32 KB
+constexpr int kHalf = kTileBytes / 2;             // one 64-column box
+
+struct BwdSmem {
+    static constexpr int kK = 0, kV = kTileBytes;
+    static constexpr int kQ = 2 * kTileBytes;    // [2] Q stages, each followed by its dO tile
+    static constexpr int kStage = 2 * kTileBytes;
+    static constexpr int kDS = kQ + 2 * kStage;  // dS^T [128 keys][128 queries] bf16
+    static constexpr int kBars = kDS + kTileBytes;
+    static constexpr int bKVFull = 0, bKVEmpty = 1, bQFull = 2, bQEmpty = 4, bSFull = 6, bPFull = 7,
+                         bDPFull = 8, bDSFull = 9, bDSEmpty = 10, bDQFull = 11, bDQEmpty = 12,
+                         bDKVFull = 13, bDKVEmpty = 14, bDrain = 15, kNumBars = 16;
+    static constexpr int kMisc = kBars + kNumBars * 8;
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kDynamic = kBytes + 1024;
+};
+static_assert(BwdSmem::kDynamic <= 232448, "shared memory of one CTA");
+
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384, kBwdTmemCols = 512;
+
+__device__ __forceinline__ void bwd_tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void bwd_fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t bwd_pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ bool bwd_warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              const WaitFailure& wf, int site, int item)
+{
+    const bool ok = mbar_wait(bar, parity, abort_flag, wf, site, item);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// One work item: a 128-key tile of one (batch, KV head); its steps run over
+// the query heads of the group (outer) and the Q tiles that can see any key
+// of the tile (inner, rotated by the tile index).
+struct BwdItem {
+    int b, hkv, j;      // batch, KV head, key tile
+    int i_min, nq;      // first Q tile with an allowed pair; Q tiles per head
+    int steps;          // group * (nq - i_min)
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int it)
+{
+    BwdItem w;
+    const int bh_count = p.B * p.Hkv;
+    w.j = it / bh_count;  // longest items (smallest key tile under causal) first
+    const int bh = it - w.j * bh_count;
+    w.b = bh / p.Hkv;
+    w.hkv = bh - w.b * p.Hkv;
+    w.nq = p.num_q_tiles;
+    w.i_min = 0;
+    if (CAUSAL) {
+        // key k is visible from query q iff k <= q + (Lk - Lq): the tile's first
+        // key j*128 needs q >= j*128 - (Lk - Lq)
+        const long long first_q = (long long)w.j * kBwdTile - (p.Lk - p.Lq);
+        w.i_min = first_q > 0 ? (int)(first_q / kBwdTile) : 0;
+        if (w.i_min > w.nq) w.i_min = w.nq;
+    }
+    w.steps = p.group * (w.nq - w.i_min);
+    return w;
+}
+
+// Query head and Q tile of step s of an item.
+__device__ __forceinline__ void bwd_step(const BwdParams& p, const BwdItem& w, int s, int& h, int& i)
+{
+    const int span = w.nq - w.i_min;
+    const int g = s / span;
+    const int r = s - g * span;
+    h = w.hkv * p.group + g;
+    i = w.i_min + (r + w.j) % span;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ main kernel
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                        const BwdParams p)
+{
+    using L = BwdSmem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WaitFailure wf{p.err, p.diag};
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::bKVFull), 1);
+        mbar_init(bar(L::bKVEmpty), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(L::bQFull + i), 1);
+            mbar_init(bar(L::bQEmpty + i), 1);
+        }
+        mbar_init(bar(L::bSFull), 1);
+        mbar_init(bar(L::bPFull), 128);
+        mbar_init(bar(L::bDPFull), 1);
+        mbar_init(bar(L::bDSFull), 128);
+        mbar_init(bar(L::bDSEmpty), 1);
+        mbar_init(bar(L::bDQFull), 1);
+        mbar_init(bar(L::bDQEmpty), 128);
+        mbar_init(bar(L::bDKVFull), 1);
+        mbar_init(bar(L::bDKVEmpty), 128);
+        mbar_init(bar(L::bDrain), 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmV);
+        tma_prefetch_map(&tmDO);
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_slot), kBwdTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        // ============================================================ P^T and dS^T (thread = key)
+        const int k = threadIdx.x;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int off = p.Lk - p.Lq;
+        uint32_t gstep = 0;
+        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
+            const BwdItem w = bwd_item<CAUSAL>(p, it);
+            const int kpos = w.j * kBwdTile + k;
+            const bool key_ok = kpos < p.Lk;
+            for (int s = 0; s < w.steps; ++s, ++gstep) {
+                int h, i;
+                bwd_step(p, w, s, h, i);
+                const int q0 = i * kBwdTile;
+                const long long ws_row = ((long long)w.b * p.Hq + h) * p.Lq_pad + q0;
+                const float4* l2p = reinterpret_cast<const float4*>(p.lse2 + ws_row);
+                const float4* dlp = reinterpret_cast<const float4*>(p.delta + ws_row);
+                const uint32_t ph = gstep & 1u;
+                // pairs above the bottom-right diagonal exist in this tile
+                const bool need_mask = !key_ok || (CAUSAL && q0 < w.j * kBwdTile + kBwdTile - 1 - off);
+                if (!bwd_warp_wait(bar(L::bSFull), ph, abort_flag, wf, 80, it)) goto done;
+                tc_fence_after_sync();
+                uint32_t pk[64];  // P^T row of this key, bf16 pairs of queries (2c, 2c+1)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + kColS + c * 32, r);
+                    float l2[32];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float4 t = __ldg(l2p + c * 8 + u);
+                        l2[4 * u] = t.x;
+                        l2[4 * u + 1] = t.y;
+                        l2[4 * u + 2] = t.z;
+                        l2[4 * u + 3] = t.w;
+                    }
+                    tmem_wait_ld();
+                    uint32_t pc[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), p.scale_log2, -l2[e]));
+                        float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), p.scale_log2, -l2[e + 1]));
+                        if (need_mask) {
+                            const int q = q0 + c * 32 + e;
+                            if (!key_ok || (CAUSAL && kpos > q + off)) p0 = 0.f;
+                            if (!key_ok || (CAUSAL && kpos > q + 1 + off)) p1 = 0.f;
+                        }
+                        pc[e / 2] = bwd_pack_bf16(p0, p1);
+                        pk[c * 16 + e / 2] = pc[e / 2];
+                    }
+                    bwd_tmem_st16(lane_base + kColS + c * 16, pc);
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::bPFull));
+
+                if (!bwd_warp_wait(bar(L::bDPFull), ph, abort_flag, wf, 81, it)) goto done;
+                if (!bwd_warp_wait(bar(L::bDSEmpty), ph ^ 1u, abort_flag, wf, 82, it)) goto done;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + kColDP + c * 32, r);
+                    float dl[32];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float4 t = __ldg(dlp + c * 8 + u);
+                        dl[4 * u] = t.x;
+                        dl[4 * u + 1] = t.y;
+                        dl[4 * u + 2] = t.z;
+                        dl[4 * u + 3] = t.w;
+                    }
+                    tmem_wait_ld();
+                    uint32_t d[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const uint32_t w2 = pk[c * 16 + e / 2];
+                        const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xffff0000u);
+                        const float ds0 = (__uint_as_float(r[e]) - dl[e]) * (p0 * p.scale);
+                        const float ds1 = (__uint_as_float(r[e + 1]) - dl[e + 1]) * (p1 * p.scale);
+                        d[e / 2] = bwd_pack_bf16(ds0, ds1);
+                    }
+                    // dS^T row k, queries 32c .. 32c+31: half c/2, 16-byte chunks 4(c&1) .. +3
+                    const uint32_t row = sb + L::kDS + (uint32_t)((c >> 1) * kHalf + k * 128);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int chunk = (c & 1) * 4 + u;
+                        sts128(row + (uint32_t)((chunk ^ (k & 7)) << 4), d[4 * u], d[4 * u + 1], d[4 * u + 2],
+                               d[4 * u + 3]);
+                    }
+                }
+                bwd_fence_proxy_async();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::bDSFull));
+            }
+        }
+    } else if (warp < 8) {
+        // ============================================================ dQ reduction, dK/dV epilogue
+        const int qi = threadIdx.x - 128;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        uint32_t gstep = 0;
+        int I = 0;
+        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x, ++I) {
+            const BwdItem w = bwd_item<CAUSAL>(p, it);
+            for (int s = 0; s < w.steps; ++s, ++gstep) {
+                int h, i;
+                bwd_step(p, w, s, h, i);
+                if (!bwd_warp_wait(bar(L::bDQFull), gstep & 1u, abort_flag, wf, 83, it)) goto done;
+                tc_fence_after_sync();
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                tmem_ld32(lane_base + kColDP, v0);
+                tmem_ld32(lane_base + kColDP + 32, v1);
+                tmem_ld32(lane_base + kColDP + 64, v2);
+                tmem_ld32(lane_base + kColDP + 96, v3);
+                tmem_wait_ld();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::bDQEmpty));
+                const int q = i * kBwdTile + qi;
+                if (q < p.Lq) {
+                    float* dst = p.dq + (((long long)w.b * p.Hq + h) * p.Lq + q) * kBwdD;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        red_add_v4(dst + 4 * u, __uint_as_float(v0[4 * u]), __uint_as_float(v0[4 * u + 1]),
+                                   __uint_as_float(v0[4 * u + 2]), __uint_as_float(v0[4 * u + 3]));
+                        red_add_v4(dst + 32 + 4 * u, __uint_as_float(v1[4 * u]), __uint_as_float(v1[4 * u + 1]),
+                                   __uint_as_float(v1[4 * u + 2]), __uint_as_float(v1[4 * u + 3]));
+                        red_add_v4(dst + 64 + 4 * u, __uint_as_float(v2[4 * u]), __uint_as_float(v2[4 * u + 1]),
+                                   __uint_as_float(v2[4 * u + 2]), __uint_as_float(v2[4 * u + 3]));
+                        red_add_v4(dst + 96 + 4 * u, __uint_as_float(v3[4 * u]), __uint_as_float(v3[4 * u + 1]),
+                                   __uint_as_float(v3[4 * u + 2]), __uint_as_float(v3[4 * u + 3]));
+                    }
+                }
+            }
+            // dK and dV of the finished key tile (thread = key)
+            if (!bwd_warp_wait(bar(L::bDKVFull), (uint32_t)(I & 1), abort_flag, wf, 84, it)) goto done;
+            tc_fence_after_sync();
+            const int key = w.j * kBwdTile + qi;
+            const long long orow = ((long long)w.b * p.Hkv + w.hkv) * p.Lk + key;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                float* out = (t == 0 ? p.dv : p.dk) + orow * kBwdD;
+                const uint32_t col = t == 0 ? kColDV : kColDK;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + col + c * 32, r);
+                    tmem_wait_ld();
+                    if (key < p.Lk) {
+                        float4* o4 = reinterpret_cast<float4*>(out + c * 32);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            o4[u] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                                __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(bar(L::bDKVEmpty));
+        }
+    } else if (warp == 8) {
+        // ============================================================ TMA producer
+        if (lane == 0) {
+            int q_armed[2] = {-1, -1}, kv_armed = -1;
+            bool drop = p.fault == 1;  // test hook: this CTA's first K/V never arrives
+            uint32_t gstep = 0;
+            int I = 0;
+            for (int it = blockIdx.x; it < p.num_items; it += gridDim.x, ++I) {
+                const BwdItem w = bwd_item<CAUSAL>(p, it);
+                const int bh_kv = w.b * p.Hkv + w.hkv;
+                if (!mbar_wait(bar(L::bKVEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 85, it)) break;
+                if (drop) {
+                    drop = false;
+                } else {
+                    mbar_arrive_expect_tx(bar(L::bKVFull), 2 * kTileBytes);
+                    kv_armed = I & 1;
+                    const int y = w.j * kBwdTile;
+                    tma_load_3d(sb + L::kK, &tmK, bar(L::bKVFull), 0, y, bh_kv);
+                    tma_load_3d(sb + L::kK + kHalf, &tmK, bar(L::bKVFull), 64, y, bh_kv);
+                    tma_load_3d(sb + L::kV, &tmV, bar(L::bKVFull), 0, y, bh_kv);
+                    tma_load_3d(sb + L::kV + kHalf, &tmV, bar(L::bKVFull), 64, y, bh_kv);
+                }
+                bool ok = true;
+                for (int s = 0; s < w.steps; ++s, ++gstep) {
+                    int h, i;
+                    bwd_step(p, w, s, h, i);
+                    const int st = (int)(gstep & 1u);
+                    const uint32_t ph = (gstep >> 1) & 1u;
+                    if (!(ok = mbar_wait(bar(L::bQEmpty + st), ph ^ 1u, abort_flag, wf, 86, it))) break;
+                    mbar_arrive_expect_tx(bar(L::bQFull + st), 2 * kTileBytes);
+                    q_armed[st] = (int)ph;
+                    const uint32_t dst = sb + L::kQ + (uint32_t)(st * L::kStage);
+                    const int y = i * kBwdTile, z = w.b * p.Hq + h;
+                    tma_load_3d(dst, &tmQ, bar(L::bQFull + st), 0, y, z);
+                    tma_load_3d(dst + kHalf, &tmQ, bar(L::bQFull + st), 64, y, z);
+                    tma_load_3d(dst + kTileBytes, &tmDO, bar(L::bQFull + st), 0, y, z);
+                    tma_load_3d(dst + kTileBytes + kHalf, &tmDO, bar(L::bQFull + st), 64, y, z);
+                }
+                if (!ok) break;
+            }
+            // every copy this thread started has landed before the CTA retires
+            if (kv_armed >= 0) mbar_settle(bar(L::bKVFull), (uint32_t)kv_armed, wf, 87);
+            for (int t = 0; t < 2; ++t)
+                if (q_armed[t] >= 0) mbar_settle(bar(L::bQFull + t), (uint32_t)q_armed[t], wf, 88);
+        }
+        __syncwarp();
+    } else {
+        // ============================================================ MMA issuer (warp 9)
+        const bool leader = lane == 0;
+        const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+        constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false);     // A, B K-major
+        constexpr uint32_t kIdBmn = idesc_bf16_f32(128, 128, true);     // B MN-major
+        constexpr uint32_t kIdABmn = kIdBmn | (1u << 15);               // A and B MN-major
+        auto commit = [&](int b) {
+            if (leader) tc_commit(bar(b));
+            __syncwarp();
+        };
+        auto kmaj = [](int kk) -> uint64_t { return (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4); };
+        auto mnmaj = [](int kk) -> uint64_t { return (uint64_t)((kk * 16 * 128) >> 4); };
+        const uint64_t dK_kmaj = smem_desc_sw128(sb + L::kK, 16, 1024);
+        const uint64_t dK_mn = smem_desc_sw128(sb + L::kK, kHalf, 1024);
+        const uint64_t dV_kmaj = smem_desc_sw128(sb + L::kV, 16, 1024);
+        const uint64_t dS_kmaj = smem_desc_sw128(sb + L::kDS, 16, 1024);
+        const uint64_t dS_mn = smem_desc_sw128(sb + L::kDS, kHalf, 1024);
+        // S^T = K Q^T into the S region
+        auto mma_s = [&](int st) {
+            const uint64_t qd = smem_desc_sw128(sb + L::kQ + (uint32_t)(st * L::kStage), 16, 1024);
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) mma_ss(tm + kColS, dK_kmaj + kmaj(kk), qd + kmaj(kk), kIdSS, kk > 0);
+            }
+            __syncwarp();
+        };
+        uint32_t gstep = 0;
+        int I = 0;
+        bool issued = false, ok = true;
+        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x, ++I) {
+            const BwdItem w = bwd_item<CAUSAL>(p, it);
+            if (!(ok = bwd_warp_wait(bar(L::bKVFull), (uint32_t)(I & 1), abort_flag, wf, 89, it))) break;
+            {
+                const int st = (int)(gstep & 1u);
+                if (!(ok = bwd_warp_wait(bar(L::bQFull + st), (gstep >> 1) & 1u, abort_flag, wf, 90, it))) break;
+                tc_fence_after_sync();
+                mma_s(st);
+                issued = true;
+                commit(L::bSFull);
+            }
+            for (int s = 0; s < w.steps; ++s, ++gstep) {
+                const int st = (int)(gstep & 1u);
+                const uint32_t stage = sb + L::kQ + (uint32_t)(st * L::kStage);
+                const uint64_t q_mn = smem_desc_sw128(stage, kHalf, 1024);
+                const uint64_t do_kmaj = smem_desc_sw128(stage + kTileBytes, 16, 1024);
+                const uint64_t do_mn = smem_desc_sw128(stage + kTileBytes, kHalf, 1024);
+                // dP^T = V dO^T; its columns held the previous step's dQ
+                if (!(ok = bwd_warp_wait(bar(L::bDQEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 91, it))) break;
+                tc_fence_after_sync();
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tm + kColDP, dV_kmaj + kmaj(kk), do_kmaj + kmaj(kk), kIdSS, kk > 0);
+                }
+                __syncwarp();
+                commit(L::bDPFull);
+                // dV += P^T dO
+                if (!(ok = bwd_warp_wait(bar(L::bPFull), gstep & 1u, abort_flag, wf, 92, it))) break;
+                if (s == 0 && !(ok = bwd_warp_wait(bar(L::bDKVEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 93, it)))
+                    break;
+                tc_fence_after_sync();
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tm + kColDV, tm + kColS + (uint32_t)(kk * 8), do_mn + mnmaj(kk), kIdBmn,
+                               (s > 0 || kk > 0) ? 1u : 0u);
+                }
+                __syncwarp();
+                // next step's S^T: P^T of this step has been consumed (MMAs run in order)
+                if (s + 1 < w.steps) {
+                    const int st1 = (int)((gstep + 1) & 1u);
+                    if (!(ok = bwd_warp_wait(bar(L::bQFull + st1), ((gstep + 1) >> 1) & 1u, abort_flag, wf, 90, it)))
+                        break;
+                    tc_fence_after_sync();
+                    mma_s(st1);
+                    commit(L::bSFull);
+                }
+                // dK += dS^T Q and dQ = dS K
+                if (!(ok = bwd_warp_wait(bar(L::bDSFull), gstep & 1u, abort_flag, wf, 94, it))) break;
+                tc_fence_after_sync();
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tm + kColDK, dS_kmaj + kmaj(kk), q_mn + mnmaj(kk), kIdBmn, (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tm + kColDP, dS_mn + mnmaj(kk), dK_mn + mnmaj(kk), kIdABmn, kk > 0);
+                }
+                __syncwarp();
+                commit(L::bDQFull);
+                commit(L::bDSEmpty);
+                commit(L::bQEmpty + st);
+            }
+            if (!ok) break;
+            commit(L::bDKVFull);
+            commit(L::bKVEmpty);
+        }
+        if (issued) {
+            commit(L::bDrain);
+            mbar_settle(bar(L::bDrain), 0, wf, 95);
+        }
+        __syncwarp();
+    }
+done:
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kBwdTmemCols);
+    }
+}
+
+cudaError_t launch_bwd_pre(int D, const BwdParams& p, cudaStream_t stream)
+{
+    const long long rows = (long long)p.B * p.Hq * p.Lq_pad;
+    const int grid = (int)((rows + 7) / 8);
+    if (D == 128)
+        fa_bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(p);
+    else
+        fa_bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream)
+{
+    if (D != kBwdD) return cudaErrorInvalidValue;
+    auto kern = causal ? fa_bwd_sm103_kernel<true> : fa_bwd_sm103_kernel<false>;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem::kDynamic);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kBwdThreads, BwdSmem::kDynamic, stream>>>(q, k, v, dout, p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -169,6 +169,38 @@ fa_status_t fa_fwd_splitkv_workspace(int B, int Hq, int Hkv, int Lq, int Lk, int
                                      size_t* workspace_bytes, int* splits_used);
 
 /*
+ * Attention backward (FlashAttention from Scratch, sec. 8 "Backward: spend
+ * arithmetic to save memory").  Given the forward's inputs, its output O and
+ * log-sum-exp LSE (as written by fa_fwd) and the upstream gradient dO, returns
+ * the gradients of sum(O * dO):
+ *
+ *     dV = P^T dO,  dS = P * (dO V^T - rowsum(O * dO)),  dQ = c dS K,  dK = c dS^T Q
+ *
+ * with P rebuilt from Q, K and LSE (never stored) and c = softmax_scale.
+ * Grouped-query heads add into their shared KV head.  Same masking rules as
+ * fa_fwd; rows with LSE = -inf contribute nothing.
+ *
+ *   q [B, Hq, Lq, D], k/v [B, Hkv, Lk, D], dout [B, Hq, Lq, D]: bf16
+ *   o [B, Hq, Lq, D], lse [B, Hq, Lq]: fp32 (fa_fwd's outputs)
+ *   dq [B, Hq, Lq, D], dk/dv [B, Hkv, Lk, D]: fp32 outputs, fully overwritten
+ *   workspace: DEVICE memory of at least fa_bwd_workspace bytes, 16-byte
+ *     aligned, owned by the caller (per-row statistics between the two
+ *     kernels); calls that overlap on the GPU need separate workspaces.
+ *   D must be 128 (FA_ERR_UNSUPPORTED otherwise).
+ *
+ * Launches 2 kernels: a preprocess (rowsum(O * dO), LSE in base 2, dq zeroed)
+ * and the gradient kernel.  dq is accumulated with fp32 atomic additions, so
+ * its low bits may differ between runs; dk and dv are deterministic.
+ */
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                   const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq,
+                   int Lk, int D, int causal, float softmax_scale, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes fa_bwd needs: 8 * B * Hq * (Lq rounded up to 128), written to *workspace_bytes. */
+fa_status_t fa_bwd_workspace(int B, int Hq, int Lq, size_t* workspace_bytes);
+
+/*
  * Synchronises `stream`, then returns and clears the device-side error latch
  * of the current device (FA_ERR_TIMEOUT or FA_ERR_INVALID_ARG from an earlier
  * launch), or FA_ERR_CUDA if the stream reports an error.
@@ -181,14 +213,15 @@ const char* fa_status_string(fa_status_t status);
 /*
  * Number of kernels the last successful forward call on this host thread
  * launched (1 for dense, 2 for varlen: schedule + attention; 1 or 2 for
- * split-KV: partials, then the merge when there is more than one partition).
+ * split-KV: partials, then the merge when there is more than one partition;
+ * 2 for backward).
  */
 int fa_last_launch_count(void);
 
 /*
  * Test hook (no counterpart on the pages).  kind = 1 makes the next fa_fwd
- * (or fa_fwd_splitkv) call on this host thread drop the first K tile load
- * (split-KV: the first K/V tile) of every CTA: the bounded wait for it runs out (about 1 s), every thread of
+ * (or fa_fwd_splitkv or fa_bwd) call on this host thread drop the first K
+ * tile load (split-KV, backward: the first K/V tile) of every CTA: the bounded wait for it runs out (about 1 s), every thread of
  * the kernel retires, and fa_check then reports FA_ERR_TIMEOUT with the CUDA
  * context still usable.  kind = 0 clears a pending request.  Results of the faulted
  * call are undefined.

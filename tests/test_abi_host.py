@@ -105,3 +105,25 @@ def test_splitkv_argument_validation(lib):
     assert lib.fa_fwd_splitkv_workspace(2, 64, 2, 1, 100, 128, 0, ctypes.byref(n), None) == UNS
     assert lib.fa_fwd_splitkv_workspace(2, 8, 2, 1, 100, 80, 0, ctypes.byref(n), None) == UNS
     assert lib.fa_last_launch_count() == 0
+
+
+def test_bwd_argument_validation(lib):
+    INV, UNS = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+
+    def call(q=16, dq=16, ws=16, B=1, Hq=2, Hkv=1, Lq=64, Lk=64, D=128, scale=0.1, wsb=1 << 20):
+        return lib.fa_bwd(q, 16, 16, 16, 16, 16, dq, 16, 16, B, Hq, Hkv, Lq, Lk, D, 1, scale, ws, wsb, None)
+
+    assert call(q=None) == INV
+    assert call(dq=None) == INV
+    assert call(ws=None) == INV
+    assert call(B=0) == INV
+    assert call(Lk=-1) == INV
+    assert call(Hq=3, Hkv=2) == INV
+    assert call(scale=0.0) == INV
+    assert call(dq=20) == INV                        # misaligned
+    assert call(wsb=100) == INV                      # workspace too small
+    assert call(D=64) == UNS
+    n = ctypes.c_size_t(0)
+    assert lib.fa_bwd_workspace(2, 3, 130, ctypes.byref(n)) == fa.FA_OK
+    assert n.value == 2 * 4 * 2 * 3 * 256            # delta and lse2, rows padded to 128
+    assert lib.fa_bwd_workspace(2, 3, 0, ctypes.byref(n)) == INV

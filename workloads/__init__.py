@@ -121,6 +121,13 @@ def random_inputs(shape_q, shape_k, seed: int, q_mult: float = 1.0):
     return _bf16(q), _bf16(k), _bf16(v)
 
 
+def grad_output(shape, seed: int):
+    """Seeded upstream gradient dO for the backward pass: N(0,1) from its own
+    generator (seed + 1000, so it never repeats the Q/K/V stream), bf16."""
+    g = torch.Generator().manual_seed(seed + 1000)
+    return _bf16(torch.randn(shape, generator=g, dtype=torch.float32))
+
+
 _VARLEN_LENS = tuple(varlen_lengths(8, 512, 8192, seed=0))
 
 # The five workloads of the headline benchmark.  Names say what they are.

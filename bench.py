@@ -79,6 +79,8 @@ def measured_peaks():
 
 KERNEL_SOURCES = ("exact_attention_07_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_07_gb300/csrc/ptx_sm103.cuh",
                   "exact_attention_07_gb300/csrc/fa_params.h")
+BWD_SOURCES = ("exact_attention_07_gb300/csrc/fa_bwd.cu", "exact_attention_07_gb300/csrc/ptx_sm103.cuh",
+               "exact_attention_07_gb300/csrc/fa_bwd.h")
 DECODE_SOURCES = ("exact_attention_07_gb300/csrc/fa_decode_tc.cu", "exact_attention_07_gb300/csrc/fa_decode.cu",
                   "exact_attention_07_gb300/csrc/ptx_sm103.cuh", "exact_attention_07_gb300/csrc/fa_decode.h")
 
@@ -204,6 +206,8 @@ def cpu_oracle_rate(w, inputs, seconds: float, rng_seed: int = 0):
 
     import oracle
     rng = np.random.default_rng(rng_seed)
+    if w.bwd:
+        return _cpu_backward_rate(w, inputs, seconds)
     if w.varlen:
         q, k, v, cq, ck = inputs
         Tq = q.shape[0]
@@ -230,6 +234,34 @@ def cpu_oracle_rate(w, inputs, seconds: float, rng_seed: int = 0):
     run(rows)
     dt = time.perf_counter() - t0
     return per_row * n / dt / 1e12, threads, f"{n} random output rows of {total_rows} ({dt:.1f} s)"
+
+
+def _cpu_backward_rate(w, inputs, seconds: float):
+    """Time the fp64 backward oracle on the last n query rows of one head
+    (all keys; with bottom-right causal alignment those rows keep the same
+    masks as in the full problem).  FLOPs: 10 * D per allowed (query, key)
+    pair, the metric's accounting of the five matrix products."""
+    import numpy as np
+
+    import oracle
+    from oracle.backward import attention_bwd
+    from workloads import grad_output
+    q, k, v = inputs
+    do = grad_output(tuple(q.shape), w.seed)
+
+    def run(n):
+        sl = slice(w.Lq - n, w.Lq)
+        t0 = time.perf_counter()
+        attention_bwd(q[:1, :1, sl], k[:1, :1], v[:1, :1], do[:1, :1, sl], w.scale, w.causal)
+        dt = time.perf_counter() - t0
+        rows = np.arange(w.Lq - n, w.Lq)
+        pairs = np.minimum(rows + 1 + (w.Lk - w.Lq), w.Lk).clip(0).sum() if w.causal else n * w.Lk
+        return dt, 10.0 * w.D * float(pairs)
+    n = min(w.Lq, 64)
+    dt, _ = run(n)
+    n = int(min(w.Lq, max(n, n * seconds / max(dt, 1e-6))))
+    dt, fl = run(n)
+    return fl / dt / 1e12, oracle.num_cpus(), f"backward of the last {n} query rows of one head ({dt:.1f} s)"
 
 
 # ------------------------------------------------------------------ reference arm
@@ -293,6 +325,18 @@ def main(argv=None):
         def step(o=None, lse=None, qq=q, kk=k, vv=v):
             return fa.fa_fwd_varlen(qq, kk, vv, cq, ck, maxl, maxl, causal=w.causal, out=o, lse=lse)
         out_shape, lse_shape = tuple(q.shape), (w.Hq, q.shape[0])
+    elif w.bwd:
+        from workloads import grad_output
+        q, k, v = (t.to(dev) for t in host_inputs)
+        do = grad_output(tuple(q.shape), w.seed).to(dev)
+        o_f, lse_f = fa.fa_fwd(q, k, v, causal=w.causal)  # the forward's outputs, computed once
+        dk_b = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        dv_b = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        ws_b = torch.empty(fa.bwd_workspace(w.B, w.Hq, w.Lq), dtype=torch.uint8, device=dev)
+
+        def step(o=None, lse=None, qq=q, kk=k, vv=v):  # o receives dQ
+            return fa.fa_bwd(qq, kk, vv, o_f, lse_f, do, causal=w.causal, dq=o, dk=dk_b, dv=dv_b, workspace=ws_b)
+        out_shape, lse_shape = tuple(q.shape), (w.B, w.Hq, w.Lq)
     elif w.decode:
         q, k, v = (t.to(dev) for t in host_inputs)
         ws_bytes, n_splits = fa.splitkv_workspace(w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D)
@@ -347,9 +391,15 @@ def main(argv=None):
     # ---- end to end through the public API with host buffers (pinned)
     e2e = None
     if not args.no_e2e:
-        pin = [t.pin_memory() for t in host_inputs]
+        e2e_in = list(host_inputs)
+        if w.bwd:  # the backward's own inputs: Q, K, V, dO and the forward's O and LSE
+            e2e_in += [do.cpu(), o_f.cpu(), lse_f.cpu()]
+        pin = [t.pin_memory() for t in e2e_in]
         h_o = torch.empty(out_shape, dtype=torch.float32).pin_memory()
         h_l = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
+        h_extra = []  # dK and dV of the backward
+        if w.bwd:
+            h_extra = [torch.empty(dk_b.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
         d_in = [torch.empty_like(t, device=dev) for t in pin]
 
         def e2e_step():
@@ -360,10 +410,17 @@ def main(argv=None):
                                  out=o, lse=lse)
             elif w.decode:
                 fa.fa_fwd_splitkv(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse, workspace=ws)
+            elif w.bwd:
+                fa.fa_bwd(d_in[0], d_in[1], d_in[2], d_in[4], d_in[5], d_in[3], causal=w.causal, dq=o, dk=dk_b,
+                          dv=dv_b, workspace=ws_b)
             else:
                 fa.fa_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse)
             h_o.copy_(o, non_blocking=True)
-            h_l.copy_(lse, non_blocking=True)
+            if w.bwd:
+                h_extra[0].copy_(dk_b, non_blocking=True)
+                h_extra[1].copy_(dv_b, non_blocking=True)
+            else:
+                h_l.copy_(lse, non_blocking=True)
         for _ in range(3):
             e2e_step()
         barrier()
@@ -378,7 +435,7 @@ def main(argv=None):
         e2e_secs = s2.elapsed_time(e2_) / 1e3
         e2e_rate, e2e_secs = job_rate(e2e_secs, flops_step * args.e2e_steps, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in pin)
-        d2h = h_o.numel() * 4 + h_l.numel() * 4
+        d2h = h_o.numel() * 4 + (sum(t.numel() * 4 for t in h_extra) if w.bwd else h_l.numel() * 4)
         e2e = {"value": e2e_rate / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_secs / args.e2e_steps * 1e3}
@@ -397,6 +454,14 @@ def main(argv=None):
                     "algorithmic_bytes_per_step": w.hbm_bytes(), "splits": n_splits,
                     "kernel": ("fa_decode_tc_kernel" if w.D == 128 and w.Hq // w.Hkv * w.Lq >= 2
                                else "fa_decode_partial_kernel<%d,*>" % w.D) + " + fa_decode_merge_kernel<%d>" % w.D,
+                    "timed": "whole step (both launches)"}
+    elif w.bwd:
+        # both launches of the step (preprocess + gradient kernel) over the step's time
+        achieved = flops_step / (secs / args.steps) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": profiled_traffic(w.name, BWD_SOURCES, "fa_bwd"),
+                    "peak_kind": f"{peak_kind} burst bf16 GEMM", "frac_of_sustained": achieved / peak_sus,
+                    "kernel": "fa_bwd_pre_kernel<%d> + fa_bwd_sm103_kernel<%s>" % (w.D, str(w.causal).lower()),
                     "timed": "whole step (both launches)"}
     else:
         achieved = flops_step / (secs / args.steps) / 1e12

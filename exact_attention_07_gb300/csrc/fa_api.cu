@@ -17,7 +17,8 @@
 namespace fa {
 
 // Device-side error latch: bit 0 = a pipeline wait timed out, bit 1 = invalid
-// variable-length offsets.  g_diag keeps the first failing wait site.
+// variable-length offsets, bit 2 = a kernel found its launch configuration
+// unusable (shared-memory window alignment) and did nothing.  g_diag keeps the first failing wait site.
 __device__ int g_err;
 __device__ int g_diag[4];
 
@@ -653,7 +654,8 @@ extern "C" fa_status_t fa_check(cudaStream_t stream)
     if (cudaMemcpyToSymbol(g_err, zero, sizeof(int)) != cudaSuccess ||
         cudaMemcpyToSymbol(g_diag, zero, sizeof(zero)) != cudaSuccess)
         return FA_ERR_CUDA;
-    return (h & 1) ? FA_ERR_TIMEOUT : FA_ERR_INVALID_ARG;
+    if (h & 1) return FA_ERR_TIMEOUT;
+    return (h & 4) ? FA_ERR_CUDA : FA_ERR_INVALID_ARG;
 }
 
 extern "C" const char* fa_status_string(fa_status_t s)

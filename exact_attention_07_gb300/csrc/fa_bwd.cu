@@ -11,29 +11,36 @@
 //   dV  += P^T dO                              tensor core, P^T from TMEM
 //   dS^T = c P^T * (dP^T - delta)              softmax warps, bf16 to shared memory
 //   dK  += dS^T Q                              tensor core
-//   dQ  += dS K                                tensor core, then fp32 atomics to global
+//   dQ^T = K^T dS^T                            tensor core, then fp32 reductions to global
 //
 // Ownership (sec. 8, "A GPU backward must handle competing ownership
 // requirements"): a CTA owns one 128-key tile of one KV head and loops over
 // every query head of its group and every Q tile that can see the keys, so
 // dK and dV are finished in tensor memory without atomics (grouped-query
 // heads add into the same accumulators); dQ needs a reduction over key tiles
-// and is added to global memory with vector fp32 reductions.  Q-tile order is
-// rotated by the key-tile index so that CTAs of the same head do not all add
-// into the same dQ rows at the same time.
+// and is added to global memory with fp32 reductions.  dQ is formed
+// transposed (dQ^T = K^T dS^T) so that TMEM lanes hold the head dimension and
+// every warp-wide reduction covers 128 contiguous bytes of one dQ row.  Q-tile
+// order is rotated by the key-tile index so that CTAs of the same head do not
+// all add into the same dQ rows at the same time.
 //
 // Tensor memory (512 columns): [0,128) S^T, overwritten by P^T (bf16 pairs);
-// [128,256) dP^T, then the dQ partial of the same step; [256,384) dV;
+// [128,256) dP^T, then the dQ^T partial of the same step; [256,384) dV;
 // [384,512) dK.  Shared memory: K and V of the tile, a 2-stage ring of
 // (Q, dO) tiles, and one dS^T tile that serves as the K-major A operand of
-// dK and, read the other way, the MN-major A operand of dQ.
+// dK and the MN-major B operand of dQ^T.
 //
-// Roles (320 threads, one persistent CTA per SM):
-//   warps 0-3  thread k owns key k of the tile: P^T and dS^T
-//   warps 4-7  thread q owns query row q: reads the dQ partial out of TMEM
-//              and reduces it into global dQ; at the end of a work item
-//              (thread = key) writes dK and dV
-//   warp  8    TMA producer      warp 9  MMA issuer, TMEM owner
+// Roles (448 threads, one persistent CTA per SM):
+//   warps 0-3   thread k owns key k of the tile: P^T into TMEM
+//   warps 4-11  two groups of four warps, one per half of the 128 query
+//               columns; lane t of a group owns TMEM lane t.  Each copies its
+//               half of P^T into registers (so the next S^T may overwrite
+//               it), forms that half of dS^T, then reads that half of the
+//               dQ^T partial (head dimension t) and reduces it into global dQ;
+//               at the end of a work item the groups write dK and dV
+//   warp  12    TMA producer      warp 13  MMA issuer, TMEM owner
+// Splitting P from dS lets P of the next step overlap dS of this one, and
+// halving dS per thread shortens the dS -> dK/dQ -> dP chain that bounds a step.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -86,7 +93,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p)
 namespace {
 
 constexpr int kBwdD = 128;
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 448;
 constexpr int kTileBytes = kBwdTile * kBwdD * 2;  // 32 KB
 constexpr int kHalf = kTileBytes / 2;             // one 64-column box
 
@@ -95,13 +102,16 @@ struct BwdSmem {
     static constexpr int kQ = 2 * kTileBytes;    // [2] Q stages, each followed by its dO tile
     static constexpr int kStage = 2 * kTileBytes;
     static constexpr int kDS = kQ + 2 * kStage;  // dS^T [128 keys][128 queries] bf16
-    static constexpr int kBars = kDS + kTileBytes;
+    static constexpr int kRowStats = kDS + kTileBytes;  // [2 stages] lse2[128], delta[128] (fp32)
+    static constexpr int kBars = kRowStats + 2 * 1024;
     static constexpr int bKVFull = 0, bKVEmpty = 1, bQFull = 2, bQEmpty = 4, bSFull = 6, bPFull = 7,
                          bDPFull = 8, bDSFull = 9, bDSEmpty = 10, bDQFull = 11, bDQEmpty = 12,
-                         bDKVFull = 13, bDKVEmpty = 14, bDrain = 15, kNumBars = 16;
+                         bDKVFull = 13, bDKVEmpty = 14, bDrain = 15, bPRead = 16, kNumBars = 17;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
-    static constexpr int kDynamic = kBytes + 1024;
+    // all the shared memory a CTA may have; the part beyond kBytes absorbs the
+    // alignment of the dynamic window to 1024 bytes (checked at run time)
+    static constexpr int kDynamic = 232448;
 };
 static_assert(BwdSmem::kDynamic <= 232448, "shared memory of one CTA");
 
@@ -128,9 +138,17 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                  : "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d)
+__device__ __forceinline__ void red_add(float* addr, float a)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completion counted on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                  : "memory");
 }
 
@@ -207,6 +225,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const WaitFailure wf{p.err, p.diag};
+    if ((uint32_t)(smem - smem_raw) + L::kBytes > (uint32_t)L::kDynamic) {
+        // the dynamic window is aligned too loosely for the layout: report, touch nothing
+        if (threadIdx.x == 0) atomicOr(p.err, 4);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::bKVFull), 1);
@@ -218,23 +241,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::bSFull), 1);
         mbar_init(bar(L::bPFull), 128);
         mbar_init(bar(L::bDPFull), 1);
-        mbar_init(bar(L::bDSFull), 128);
+        mbar_init(bar(L::bDSFull), 256);
         mbar_init(bar(L::bDSEmpty), 1);
         mbar_init(bar(L::bDQFull), 1);
-        mbar_init(bar(L::bDQEmpty), 128);
+        mbar_init(bar(L::bDQEmpty), 256);
         mbar_init(bar(L::bDKVFull), 1);
-        mbar_init(bar(L::bDKVEmpty), 128);
+        mbar_init(bar(L::bDKVEmpty), 256);
         mbar_init(bar(L::bDrain), 1);
+        mbar_init(bar(L::bPRead), 256);
         *abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == 12 && lane == 0) {
         tma_prefetch_map(&tmQ);
         tma_prefetch_map(&tmK);
         tma_prefetch_map(&tmV);
         tma_prefetch_map(&tmDO);
     }
-    if (warp == 9) {
+    if (warp == 13) {
         tmem_alloc(smem_u32(tmem_slot), kBwdTmemCols);
         tmem_relinquish();
     }
@@ -244,7 +268,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp < 4) {
-        // ============================================================ P^T and dS^T (thread = key)
+        // ============================================================ P^T (thread = key)
         const int k = threadIdx.x;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         const int off = p.Lk - p.Lq;
@@ -257,15 +281,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 int h, i;
                 bwd_step(p, w, s, h, i);
                 const int q0 = i * kBwdTile;
-                const long long ws_row = ((long long)w.b * p.Hq + h) * p.Lq_pad + q0;
-                const float4* l2p = reinterpret_cast<const float4*>(p.lse2 + ws_row);
-                const float4* dlp = reinterpret_cast<const float4*>(p.delta + ws_row);
-                const uint32_t ph = gstep & 1u;
+                // this step's row statistics, staged with its Q and dO tiles
+                const float4* l2p = reinterpret_cast<const float4*>(smem + L::kRowStats + (gstep & 1u) * 1024);
                 // pairs above the bottom-right diagonal exist in this tile
                 const bool need_mask = !key_ok || (CAUSAL && q0 < w.j * kBwdTile + kBwdTile - 1 - off);
-                if (!bwd_warp_wait(bar(L::bSFull), ph, abort_flag, wf, 80, it)) goto done;
+                // the statistics arrive with the stage's Q and dO (observed here
+                // directly, not through the MMA warp)
+                if (!bwd_warp_wait(bar(L::bQFull + (gstep & 1u)), (gstep >> 1) & 1u, abort_flag, wf, 79, it))
+                    goto done;
+                if (!bwd_warp_wait(bar(L::bSFull), gstep & 1u, abort_flag, wf, 80, it)) goto done;
                 tc_fence_after_sync();
-                uint32_t pk[64];  // P^T row of this key, bf16 pairs of queries (2c, 2c+1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t r[32];
@@ -273,7 +298,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     float l2[32];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        const float4 t = __ldg(l2p + c * 8 + u);
+                        const float4 t = l2p[c * 8 + u];
                         l2[4 * u] = t.x;
                         l2[4 * u + 1] = t.y;
                         l2[4 * u + 2] = t.z;
@@ -291,58 +316,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             if (!key_ok || (CAUSAL && kpos > q + 1 + off)) p1 = 0.f;
                         }
                         pc[e / 2] = bwd_pack_bf16(p0, p1);
-                        pk[c * 16 + e / 2] = pc[e / 2];
                     }
                     bwd_tmem_st16(lane_base + kColS + c * 16, pc);
                 }
                 tmem_wait_st();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::bPFull));
-
-                if (!bwd_warp_wait(bar(L::bDPFull), ph, abort_flag, wf, 81, it)) goto done;
-                if (!bwd_warp_wait(bar(L::bDSEmpty), ph ^ 1u, abort_flag, wf, 82, it)) goto done;
-                tc_fence_after_sync();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_base + kColDP + c * 32, r);
-                    float dl[32];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const float4 t = __ldg(dlp + c * 8 + u);
-                        dl[4 * u] = t.x;
-                        dl[4 * u + 1] = t.y;
-                        dl[4 * u + 2] = t.z;
-                        dl[4 * u + 3] = t.w;
-                    }
-                    tmem_wait_ld();
-                    uint32_t d[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const uint32_t w2 = pk[c * 16 + e / 2];
-                        const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xffff0000u);
-                        const float ds0 = (__uint_as_float(r[e]) - dl[e]) * (p0 * p.scale);
-                        const float ds1 = (__uint_as_float(r[e + 1]) - dl[e + 1]) * (p1 * p.scale);
-                        d[e / 2] = bwd_pack_bf16(ds0, ds1);
-                    }
-                    // dS^T row k, queries 32c .. 32c+31: half c/2, 16-byte chunks 4(c&1) .. +3
-                    const uint32_t row = sb + L::kDS + (uint32_t)((c >> 1) * kHalf + k * 128);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int chunk = (c & 1) * 4 + u;
-                        sts128(row + (uint32_t)((chunk ^ (k & 7)) << 4), d[4 * u], d[4 * u + 1], d[4 * u + 2],
-                               d[4 * u + 3]);
-                    }
-                }
-                bwd_fence_proxy_async();
-                tc_fence_before_sync();
-                mbar_arrive(bar(L::bDSFull));
             }
         }
-    } else if (warp < 8) {
-        // ============================================================ dQ reduction, dK/dV epilogue
-        const int qi = threadIdx.x - 128;
-        const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    } else if (warp < 12) {
+        // ============================================================ dS^T, dQ reduction, dK/dV epilogue
+        // Warp w owns TMEM lanes 32 (w % 4) .. +31 and one half of the tile's
+        // 128 query columns: lane t is key t of the tile for P^T and dS^T,
+        // head dimension t for the dQ^T partial, key t again for dK and dV.
+        const int t = 32 * (warp & 3) + lane;
+        const int ch = (warp - 4) >> 2;  // column half: queries 64ch .. 64ch+63
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         uint32_t gstep = 0;
         int I = 0;
         for (int it = blockIdx.x; it < p.num_items; it += gridDim.x, ++I) {
@@ -350,43 +339,93 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 int h, i;
                 bwd_step(p, w, s, h, i);
-                if (!bwd_warp_wait(bar(L::bDQFull), gstep & 1u, abort_flag, wf, 83, it)) goto done;
+                const uint32_t ph = gstep & 1u;
+                // this half of P^T into registers before the next S^T overwrites it
+                if (!bwd_warp_wait(bar(L::bPFull), ph, abort_flag, wf, 81, it)) goto done;
                 tc_fence_after_sync();
-                uint32_t v0[32], v1[32], v2[32], v3[32];
-                tmem_ld32(lane_base + kColDP, v0);
-                tmem_ld32(lane_base + kColDP + 32, v1);
-                tmem_ld32(lane_base + kColDP + 64, v2);
-                tmem_ld32(lane_base + kColDP + 96, v3);
+                uint32_t pk[32];  // bf16 pairs of queries 64ch + (2e, 2e+1)
+                tmem_ld32(lane_base + kColS + 32 * ch, pk);
+                tmem_wait_ld();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::bPRead));
+                // dS^T = c P^T (dP^T - delta) for the half's 64 queries
+                const float4* dlp =
+                    reinterpret_cast<const float4*>(smem + L::kRowStats + (gstep & 1u) * 1024) + 32;
+                if (!bwd_warp_wait(bar(L::bQFull + (gstep & 1u)), (gstep >> 1) & 1u, abort_flag, wf, 78, it))
+                    goto done;
+                if (!bwd_warp_wait(bar(L::bDPFull), ph, abort_flag, wf, 82, it)) goto done;
+                if (!bwd_warp_wait(bar(L::bDSEmpty), ph ^ 1u, abort_flag, wf, 83, it)) goto done;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * ch + cc;  // 32-query chunk of the tile
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + kColDP + c * 32, r);
+                    float dl[32];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float4 v4 = dlp[c * 8 + u];
+                        dl[4 * u] = v4.x;
+                        dl[4 * u + 1] = v4.y;
+                        dl[4 * u + 2] = v4.z;
+                        dl[4 * u + 3] = v4.w;
+                    }
+                    tmem_wait_ld();
+                    uint32_t d[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const uint32_t w2 = pk[cc * 16 + e / 2];
+                        const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xffff0000u);
+                        const float ds0 = (__uint_as_float(r[e]) - dl[e]) * (p0 * p.scale);
+                        const float ds1 = (__uint_as_float(r[e + 1]) - dl[e + 1]) * (p1 * p.scale);
+                        d[e / 2] = bwd_pack_bf16(ds0, ds1);
+                    }
+                    // dS^T row t, queries 32c .. 32c+31: half c/2 (= ch), 16-byte chunks 4(c&1) .. +3
+                    const uint32_t row = sb + L::kDS + (uint32_t)(ch * kHalf + t * 128);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int chunk = (c & 1) * 4 + u;
+                        sts128(row + (uint32_t)((chunk ^ (t & 7)) << 4), d[4 * u], d[4 * u + 1], d[4 * u + 2],
+                               d[4 * u + 3]);
+                    }
+                }
+                bwd_fence_proxy_async();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::bDSFull));
+                // dQ^T partial (lane = head dimension, columns = the half's query
+                // rows) into global dQ: each warp instruction adds 128 contiguous
+                // bytes of one row
+                if (!bwd_warp_wait(bar(L::bDQFull), ph, abort_flag, wf, 84, it)) goto done;
+                tc_fence_after_sync();
+                uint32_t v0[32], v1[32];
+                tmem_ld32(lane_base + kColDP + 64 * ch, v0);
+                tmem_ld32(lane_base + kColDP + 64 * ch + 32, v1);
                 tmem_wait_ld();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::bDQEmpty));
-                const int q = i * kBwdTile + qi;
-                if (q < p.Lq) {
-                    float* dst = p.dq + (((long long)w.b * p.Hq + h) * p.Lq + q) * kBwdD;
+                {
+                    const int qh = i * kBwdTile + 64 * ch;  // first query row of the half
+                    const int nrows = min(64, p.Lq - qh);
+                    float* dst = p.dq + (((long long)w.b * p.Hq + h) * p.Lq + qh) * kBwdD + t;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        red_add_v4(dst + 4 * u, __uint_as_float(v0[4 * u]), __uint_as_float(v0[4 * u + 1]),
-                                   __uint_as_float(v0[4 * u + 2]), __uint_as_float(v0[4 * u + 3]));
-                        red_add_v4(dst + 32 + 4 * u, __uint_as_float(v1[4 * u]), __uint_as_float(v1[4 * u + 1]),
-                                   __uint_as_float(v1[4 * u + 2]), __uint_as_float(v1[4 * u + 3]));
-                        red_add_v4(dst + 64 + 4 * u, __uint_as_float(v2[4 * u]), __uint_as_float(v2[4 * u + 1]),
-                                   __uint_as_float(v2[4 * u + 2]), __uint_as_float(v2[4 * u + 3]));
-                        red_add_v4(dst + 96 + 4 * u, __uint_as_float(v3[4 * u]), __uint_as_float(v3[4 * u + 1]),
-                                   __uint_as_float(v3[4 * u + 2]), __uint_as_float(v3[4 * u + 3]));
+                    for (int c = 0; c < 32; ++c) {
+                        if (c < nrows) red_add(dst + c * kBwdD, __uint_as_float(v0[c]));
+                        if (32 + c < nrows) red_add(dst + (32 + c) * kBwdD, __uint_as_float(v1[c]));
                     }
                 }
             }
-            // dK and dV of the finished key tile (thread = key)
-            if (!bwd_warp_wait(bar(L::bDKVFull), (uint32_t)(I & 1), abort_flag, wf, 84, it)) goto done;
+            // dK and dV of the finished key tile (thread = key t, columns of the half)
+            if (!bwd_warp_wait(bar(L::bDKVFull), (uint32_t)(I & 1), abort_flag, wf, 85, it)) goto done;
             tc_fence_after_sync();
-            const int key = w.j * kBwdTile + qi;
+            const int key = w.j * kBwdTile + t;
             const long long orow = ((long long)w.b * p.Hkv + w.hkv) * p.Lk + key;
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                float* out = (t == 0 ? p.dv : p.dk) + orow * kBwdD;
-                const uint32_t col = t == 0 ? kColDV : kColDK;
+            for (int o = 0; o < 2; ++o) {
+                float* out = (o == 0 ? p.dv : p.dk) + orow * kBwdD;
+                const uint32_t col = o == 0 ? kColDV : kColDK;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * ch + cc;
                     uint32_t r[32];
                     tmem_ld32(lane_base + col + c * 32, r);
                     tmem_wait_ld();
@@ -402,7 +441,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_before_sync();
             mbar_arrive(bar(L::bDKVEmpty));
         }
-    } else if (warp == 8) {
+    } else if (warp == 12) {
         // ============================================================ TMA producer
         if (lane == 0) {
             int q_armed[2] = {-1, -1}, kv_armed = -1;
@@ -431,10 +470,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const int st = (int)(gstep & 1u);
                     const uint32_t ph = (gstep >> 1) & 1u;
                     if (!(ok = mbar_wait(bar(L::bQEmpty + st), ph ^ 1u, abort_flag, wf, 86, it))) break;
-                    mbar_arrive_expect_tx(bar(L::bQFull + st), 2 * kTileBytes);
+                    mbar_arrive_expect_tx(bar(L::bQFull + st), 2 * kTileBytes + 1024);
                     q_armed[st] = (int)ph;
                     const uint32_t dst = sb + L::kQ + (uint32_t)(st * L::kStage);
                     const int y = i * kBwdTile, z = w.b * p.Hq + h;
+                    const long long ws_row = (long long)z * p.Lq_pad + y;
+                    const uint32_t rs = sb + L::kRowStats + (uint32_t)(st * 1024);
+                    bulk_load(rs, p.lse2 + ws_row, 512, bar(L::bQFull + st));
+                    bulk_load(rs + 512, p.delta + ws_row, 512, bar(L::bQFull + st));
                     tma_load_3d(dst, &tmQ, bar(L::bQFull + st), 0, y, z);
                     tma_load_3d(dst + kHalf, &tmQ, bar(L::bQFull + st), 64, y, z);
                     tma_load_3d(dst + kTileBytes, &tmDO, bar(L::bQFull + st), 0, y, z);
@@ -449,7 +492,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         __syncwarp();
     } else {
-        // ============================================================ MMA issuer (warp 9)
+        // ============================================================ MMA issuer (warp 13)
         const bool leader = lane == 0;
         const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
         constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false);     // A, B K-major
@@ -522,6 +565,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const int st1 = (int)((gstep + 1) & 1u);
                     if (!(ok = bwd_warp_wait(bar(L::bQFull + st1), ((gstep + 1) >> 1) & 1u, abort_flag, wf, 90, it)))
                         break;
+                    // the dS warps hold P^T of this step in registers
+                    if (!(ok = bwd_warp_wait(bar(L::bPRead), gstep & 1u, abort_flag, wf, 96, it))) break;
                     tc_fence_after_sync();
                     mma_s(st1);
                     commit(L::bSFull);
@@ -533,9 +578,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ss(tm + kColDK, dS_kmaj + kmaj(kk), q_mn + mnmaj(kk), kIdBmn, (s > 0 || kk > 0) ? 1u : 0u);
+                    // dQ^T = K^T dS^T: lanes = head dimension, so the reduction into
+                    // global dQ is coalesced along each row
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tm + kColDP, dS_mn + mnmaj(kk), dK_mn + mnmaj(kk), kIdABmn, kk > 0);
+                        mma_ss(tm + kColDP, dK_mn + mnmaj(kk), dS_mn + mnmaj(kk), kIdABmn, kk > 0);
                 }
                 __syncwarp();
                 commit(L::bDQFull);
@@ -556,7 +603,7 @@ done:
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kBwdTmemCols);
     }

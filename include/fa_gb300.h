@@ -202,8 +202,9 @@ fa_status_t fa_bwd_workspace(int B, int Hq, int Lq, size_t* workspace_bytes);
 
 /*
  * Synchronises `stream`, then returns and clears the device-side error latch
- * of the current device (FA_ERR_TIMEOUT or FA_ERR_INVALID_ARG from an earlier
- * launch), or FA_ERR_CUDA if the stream reports an error.
+ * of the current device: FA_ERR_TIMEOUT or FA_ERR_INVALID_ARG from an earlier
+ * launch, or FA_ERR_CUDA when a kernel found its launch configuration unusable
+ * and did nothing; FA_ERR_CUDA also if the stream reports an error.
  */
 fa_status_t fa_check(cudaStream_t stream);
 

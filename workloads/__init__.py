@@ -42,6 +42,8 @@ class Workload:
     # decode-shaped problem (few query rows per KV head, long key range) that
     # runs through the split-KV forward
     decode: bool = False
+    # the backward pass (fa_bwd) of this problem instead of the forward
+    bwd: bool = False
 
     @property
     def scale(self) -> float:
@@ -62,6 +64,8 @@ class Workload:
             total = sum(4.0 * self.Hq * L * L * self.D for L in self.seqlens)
         else:
             total = 4.0 * self.B * self.Hq * self.Lq * self.Lk * self.D
+        if self.bwd:  # five matrix products instead of two (S, dP, dV, dQ, dK)
+            total *= 2.5
         return total / 2 if self.causal else total
 
     def hbm_bytes(self) -> float:
@@ -161,6 +165,19 @@ DECODE_WORKLOADS: dict[str, Workload] = {
                                             decode=True),
 }
 WORKLOADS.update(DECODE_WORKLOADS)
+
+# Backward of the long-sequence workloads (same shapes and seeds; dO drawn by
+# grad_output), and a smaller case for profiler captures (Q, K, V, dO, O, dQ,
+# dK, dV total 288 MiB, above the L2).
+BWD_WORKLOADS: dict[str, Workload] = {
+    "bwd_b1_h16_l16384_d128": Workload("bwd_b1_h16_l16384_d128", 1, 16, 16, 16384, 16384, 128, False, bwd=True),
+    "bwd_b1_h16_l16384_d128_causal": Workload("bwd_b1_h16_l16384_d128_causal", 1, 16, 16, 16384, 16384, 128, True,
+                                              bwd=True),
+    "bwd_gqa_b2_h32x8_l4096_d128_causal_q3": Workload(
+        "bwd_gqa_b2_h32x8_l4096_d128_causal_q3", 2, 32, 8, 4096, 4096, 128, True, q_mult=3.0, bwd=True),
+    "bwd_b1_h16_l4096_d128": Workload("bwd_b1_h16_l4096_d128", 1, 16, 16, 4096, 4096, 128, False, bwd=True),
+}
+WORKLOADS.update(BWD_WORKLOADS)
 
 # The configuration the throughput metric is quoted on.
 HEADLINE = "b1_h16_l16384_d128"

@@ -30,17 +30,21 @@
 // (Q, dO) tiles, and one dS^T tile that serves as the K-major A operand of
 // dK and the MN-major B operand of dQ^T.
 //
-// Roles (448 threads, one persistent CTA per SM):
-//   warps 0-3   thread k owns key k of the tile: P^T into TMEM
+// Roles (512 threads, one persistent CTA per SM):
+//   warps 0-3   thread t owns TMEM lane t: reads the dQ^T partial (head
+//               dimension t) out of TMEM and reduces it into global dQ; at
+//               the end of a work item writes dK and dV (key t)
 //   warps 4-11  two groups of four warps, one per half of the 128 query
-//               columns; lane t of a group owns TMEM lane t.  Each copies its
-//               half of P^T into registers (so the next S^T may overwrite
-//               it), forms that half of dS^T, then reads that half of the
-//               dQ^T partial (head dimension t) and reduces it into global dQ;
-//               at the end of a work item the groups write dK and dV
+//               columns; lane t of a group owns key t of the tile.  Each
+//               forms its half of P^T (into TMEM, for dV) and of dS^T (into
+//               shared memory, for dK and dQ), keeping P^T in registers
 //   warp  12    TMA producer      warp 13  MMA issuer, TMEM owner
-// Splitting P from dS lets P of the next step overlap dS of this one, and
-// halving dS per thread shortens the dS -> dK/dQ -> dP chain that bounds a step.
+//   warps 14-15 idle (they complete the last warpgroup for setmaxnreg)
+// Registers after setmaxnreg: warps 0-3 192, warps 4-11 128, warps 12-15 64
+// (128*192 + 256*128 + 128*64 = 65536, the launch's 128 per thread).
+// The dQ reductions (64 KB per step) run on their own warps, overlapped with
+// everything else; halving P and dS per thread shortens the chain
+// dS -> dK/dQ -> dP -> dS that bounds a step.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p)
 namespace {
 
 constexpr int kBwdD = 128;
-constexpr int kBwdThreads = 448;
+constexpr int kBwdThreads = 512;
 constexpr int kTileBytes = kBwdTile * kBwdD * 2;  // 32 KB
 constexpr int kHalf = kTileBytes / 2;             // one 64-column box
 
@@ -106,7 +110,7 @@ struct BwdSmem {
     static constexpr int kBars = kRowStats + 2 * 1024;
     static constexpr int bKVFull = 0, bKVEmpty = 1, bQFull = 2, bQEmpty = 4, bSFull = 6, bPFull = 7,
                          bDPFull = 8, bDSFull = 9, bDSEmpty = 10, bDQFull = 11, bDQEmpty = 12,
-                         bDKVFull = 13, bDKVEmpty = 14, bDrain = 15, bPRead = 16, kNumBars = 17;
+                         bDKVFull = 13, bDKVEmpty = 14, bDrain = 15, kNumBars = 16;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     // all the shared memory a CTA may have; the part beyond kBytes absorbs the
@@ -239,16 +243,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar(L::bQEmpty + i), 1);
         }
         mbar_init(bar(L::bSFull), 1);
-        mbar_init(bar(L::bPFull), 128);
+        mbar_init(bar(L::bPFull), 256);
         mbar_init(bar(L::bDPFull), 1);
         mbar_init(bar(L::bDSFull), 256);
         mbar_init(bar(L::bDSEmpty), 1);
         mbar_init(bar(L::bDQFull), 1);
-        mbar_init(bar(L::bDQEmpty), 256);
+        mbar_init(bar(L::bDQEmpty), 128);
         mbar_init(bar(L::bDKVFull), 1);
-        mbar_init(bar(L::bDKVEmpty), 256);
+        mbar_init(bar(L::bDKVEmpty), 128);
         mbar_init(bar(L::bDrain), 1);
-        mbar_init(bar(L::bPRead), 256);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -268,44 +271,113 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp < 4) {
-        // ============================================================ P^T (thread = key)
-        const int k = threadIdx.x;
+        // ============================================================ dQ reduction, dK/dV epilogue
+        // Thread t owns TMEM lane t: head dimension t of the dQ^T partial (its
+        // 128 columns are the Q tile's rows), key t for dK and dV.
+        regs_increase<192>();
+        const int t = threadIdx.x;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        uint32_t gstep = 0;
+        int I = 0;
+        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x, ++I) {
+            const BwdItem w = bwd_item<CAUSAL>(p, it);
+            for (int s = 0; s < w.steps; ++s, ++gstep) {
+                int h, i;
+                bwd_step(p, w, s, h, i);
+                if (!bwd_warp_wait(bar(L::bDQFull), gstep & 1u, abort_flag, wf, 84, it)) goto done;
+                tc_fence_after_sync();
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                tmem_ld32(lane_base + kColDP, v0);
+                tmem_ld32(lane_base + kColDP + 32, v1);
+                tmem_ld32(lane_base + kColDP + 64, v2);
+                tmem_ld32(lane_base + kColDP + 96, v3);
+                tmem_wait_ld();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::bDQEmpty));
+                // each warp instruction adds 128 contiguous bytes of one dQ row
+                const int q0 = i * kBwdTile;
+                const int nrows = min(kBwdTile, p.Lq - q0);
+                float* dst = p.dq + (((long long)w.b * p.Hq + h) * p.Lq + q0) * kBwdD + t;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    if (c < nrows) red_add(dst + c * kBwdD, __uint_as_float(v0[c]));
+                    if (32 + c < nrows) red_add(dst + (32 + c) * kBwdD, __uint_as_float(v1[c]));
+                    if (64 + c < nrows) red_add(dst + (64 + c) * kBwdD, __uint_as_float(v2[c]));
+                    if (96 + c < nrows) red_add(dst + (96 + c) * kBwdD, __uint_as_float(v3[c]));
+                }
+            }
+            // dK and dV of the finished key tile (thread = key)
+            if (!bwd_warp_wait(bar(L::bDKVFull), (uint32_t)(I & 1), abort_flag, wf, 85, it)) goto done;
+            tc_fence_after_sync();
+            const int key = w.j * kBwdTile + t;
+            const long long orow = ((long long)w.b * p.Hkv + w.hkv) * p.Lk + key;
+#pragma unroll
+            for (int o = 0; o < 2; ++o) {
+                float* out = (o == 0 ? p.dv : p.dk) + orow * kBwdD;
+                const uint32_t col = o == 0 ? kColDV : kColDK;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + col + c * 32, r);
+                    tmem_wait_ld();
+                    if (key < p.Lk) {
+                        float4* o4 = reinterpret_cast<float4*>(out + c * 32);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            o4[u] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                                __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(bar(L::bDKVEmpty));
+        }
+    } else if (warp < 12) {
+        // ============================================================ P^T and dS^T
+        // Two groups of four warps, one per half of the Q tile's 128 columns;
+        // lane t of a group owns TMEM lane t = key t of the tile.  A thread
+        // keeps its half of P^T in registers for dS^T, so the next S^T may
+        // overwrite P^T as soon as P.V has read it.
+        const int t = 32 * (warp & 3) + lane;
+        const int ch = (warp - 4) >> 2;  // column half: queries 64ch .. 64ch+63
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const int off = p.Lk - p.Lq;
         uint32_t gstep = 0;
         for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
             const BwdItem w = bwd_item<CAUSAL>(p, it);
-            const int kpos = w.j * kBwdTile + k;
+            const int kpos = w.j * kBwdTile + t;
             const bool key_ok = kpos < p.Lk;
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 int h, i;
                 bwd_step(p, w, s, h, i);
                 const int q0 = i * kBwdTile;
+                const uint32_t ph = gstep & 1u;
                 // this step's row statistics, staged with its Q and dO tiles
+                // (observed here directly, not through the MMA warp)
                 const float4* l2p = reinterpret_cast<const float4*>(smem + L::kRowStats + (gstep & 1u) * 1024);
+                const float4* dlp = l2p + 32;
                 // pairs above the bottom-right diagonal exist in this tile
                 const bool need_mask = !key_ok || (CAUSAL && q0 < w.j * kBwdTile + kBwdTile - 1 - off);
-                // the statistics arrive with the stage's Q and dO (observed here
-                // directly, not through the MMA warp)
                 if (!bwd_warp_wait(bar(L::bQFull + (gstep & 1u)), (gstep >> 1) & 1u, abort_flag, wf, 79, it))
                     goto done;
-                if (!bwd_warp_wait(bar(L::bSFull), gstep & 1u, abort_flag, wf, 80, it)) goto done;
+                if (!bwd_warp_wait(bar(L::bSFull), ph, abort_flag, wf, 80, it)) goto done;
                 tc_fence_after_sync();
+                uint32_t pk[32];  // bf16 pairs of queries 64ch + (2e, 2e+1)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * ch + cc;  // 32-query chunk of the tile
                     uint32_t r[32];
                     tmem_ld32(lane_base + kColS + c * 32, r);
                     float l2[32];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        const float4 t = l2p[c * 8 + u];
-                        l2[4 * u] = t.x;
-                        l2[4 * u + 1] = t.y;
-                        l2[4 * u + 2] = t.z;
-                        l2[4 * u + 3] = t.w;
+                        const float4 v4 = l2p[c * 8 + u];
+                        l2[4 * u] = v4.x;
+                        l2[4 * u + 1] = v4.y;
+                        l2[4 * u + 2] = v4.z;
+                        l2[4 * u + 3] = v4.w;
                     }
                     tmem_wait_ld();
-                    uint32_t pc[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), p.scale_log2, -l2[e]));
@@ -315,50 +387,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             if (!key_ok || (CAUSAL && kpos > q + off)) p0 = 0.f;
                             if (!key_ok || (CAUSAL && kpos > q + 1 + off)) p1 = 0.f;
                         }
-                        pc[e / 2] = bwd_pack_bf16(p0, p1);
+                        pk[cc * 16 + e / 2] = bwd_pack_bf16(p0, p1);
                     }
-                    bwd_tmem_st16(lane_base + kColS + c * 16, pc);
+                }
+                // the S^T columns of this half were all read above: overwrite
+                // the half's first 32 columns with its P^T (column c = queries 2c, 2c+1)
+                {
+                    uint32_t lo[16], hi[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        lo[e] = pk[e];
+                        hi[e] = pk[16 + e];
+                    }
+                    bwd_tmem_st16(lane_base + kColS + 32 * ch, lo);
+                    bwd_tmem_st16(lane_base + kColS + 32 * ch + 16, hi);
                 }
                 tmem_wait_st();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::bPFull));
-            }
-        }
-    } else if (warp < 12) {
-        // ============================================================ dS^T, dQ reduction, dK/dV epilogue
-        // Warp w owns TMEM lanes 32 (w % 4) .. +31 and one half of the tile's
-        // 128 query columns: lane t is key t of the tile for P^T and dS^T,
-        // head dimension t for the dQ^T partial, key t again for dK and dV.
-        const int t = 32 * (warp & 3) + lane;
-        const int ch = (warp - 4) >> 2;  // column half: queries 64ch .. 64ch+63
-        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        uint32_t gstep = 0;
-        int I = 0;
-        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x, ++I) {
-            const BwdItem w = bwd_item<CAUSAL>(p, it);
-            for (int s = 0; s < w.steps; ++s, ++gstep) {
-                int h, i;
-                bwd_step(p, w, s, h, i);
-                const uint32_t ph = gstep & 1u;
-                // this half of P^T into registers before the next S^T overwrites it
-                if (!bwd_warp_wait(bar(L::bPFull), ph, abort_flag, wf, 81, it)) goto done;
-                tc_fence_after_sync();
-                uint32_t pk[32];  // bf16 pairs of queries 64ch + (2e, 2e+1)
-                tmem_ld32(lane_base + kColS + 32 * ch, pk);
-                tmem_wait_ld();
-                tc_fence_before_sync();
-                mbar_arrive(bar(L::bPRead));
                 // dS^T = c P^T (dP^T - delta) for the half's 64 queries
-                const float4* dlp =
-                    reinterpret_cast<const float4*>(smem + L::kRowStats + (gstep & 1u) * 1024) + 32;
-                if (!bwd_warp_wait(bar(L::bQFull + (gstep & 1u)), (gstep >> 1) & 1u, abort_flag, wf, 78, it))
-                    goto done;
                 if (!bwd_warp_wait(bar(L::bDPFull), ph, abort_flag, wf, 82, it)) goto done;
                 if (!bwd_warp_wait(bar(L::bDSEmpty), ph ^ 1u, abort_flag, wf, 83, it)) goto done;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
-                    const int c = 2 * ch + cc;  // 32-query chunk of the tile
+                    const int c = 2 * ch + cc;
                     uint32_t r[32];
                     tmem_ld32(lane_base + kColDP + c * 32, r);
                     float dl[32];
@@ -380,7 +433,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const float ds1 = (__uint_as_float(r[e + 1]) - dl[e + 1]) * (p1 * p.scale);
                         d[e / 2] = bwd_pack_bf16(ds0, ds1);
                     }
-                    // dS^T row t, queries 32c .. 32c+31: half c/2 (= ch), 16-byte chunks 4(c&1) .. +3
+                    // dS^T row t, queries 32c .. 32c+31: half ch, 16-byte chunks 4(c&1) .. +3
                     const uint32_t row = sb + L::kDS + (uint32_t)(ch * kHalf + t * 128);
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -392,57 +445,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bwd_fence_proxy_async();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::bDSFull));
-                // dQ^T partial (lane = head dimension, columns = the half's query
-                // rows) into global dQ: each warp instruction adds 128 contiguous
-                // bytes of one row
-                if (!bwd_warp_wait(bar(L::bDQFull), ph, abort_flag, wf, 84, it)) goto done;
-                tc_fence_after_sync();
-                uint32_t v0[32], v1[32];
-                tmem_ld32(lane_base + kColDP + 64 * ch, v0);
-                tmem_ld32(lane_base + kColDP + 64 * ch + 32, v1);
-                tmem_wait_ld();
-                tc_fence_before_sync();
-                mbar_arrive(bar(L::bDQEmpty));
-                {
-                    const int qh = i * kBwdTile + 64 * ch;  // first query row of the half
-                    const int nrows = min(64, p.Lq - qh);
-                    float* dst = p.dq + (((long long)w.b * p.Hq + h) * p.Lq + qh) * kBwdD + t;
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        if (c < nrows) red_add(dst + c * kBwdD, __uint_as_float(v0[c]));
-                        if (32 + c < nrows) red_add(dst + (32 + c) * kBwdD, __uint_as_float(v1[c]));
-                    }
-                }
             }
-            // dK and dV of the finished key tile (thread = key t, columns of the half)
-            if (!bwd_warp_wait(bar(L::bDKVFull), (uint32_t)(I & 1), abort_flag, wf, 85, it)) goto done;
-            tc_fence_after_sync();
-            const int key = w.j * kBwdTile + t;
-            const long long orow = ((long long)w.b * p.Hkv + w.hkv) * p.Lk + key;
-#pragma unroll
-            for (int o = 0; o < 2; ++o) {
-                float* out = (o == 0 ? p.dv : p.dk) + orow * kBwdD;
-                const uint32_t col = o == 0 ? kColDV : kColDK;
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c = 2 * ch + cc;
-                    uint32_t r[32];
-                    tmem_ld32(lane_base + col + c * 32, r);
-                    tmem_wait_ld();
-                    if (key < p.Lk) {
-                        float4* o4 = reinterpret_cast<float4*>(out + c * 32);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            o4[u] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                                                __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
-                    }
-                }
-            }
-            tc_fence_before_sync();
-            mbar_arrive(bar(L::bDKVEmpty));
         }
     } else if (warp == 12) {
         // ============================================================ TMA producer
+        regs_decrease<64>();
         if (lane == 0) {
             int q_armed[2] = {-1, -1}, kv_armed = -1;
             bool drop = p.fault == 1;  // test hook: this CTA's first K/V never arrives
@@ -491,8 +498,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (q_armed[t] >= 0) mbar_settle(bar(L::bQFull + t), (uint32_t)q_armed[t], wf, 88);
         }
         __syncwarp();
-    } else {
+    } else if (warp == 13) {
         // ============================================================ MMA issuer (warp 13)
+        regs_decrease<64>();
         const bool leader = lane == 0;
         const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
         constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false);     // A, B K-major
@@ -565,8 +573,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const int st1 = (int)((gstep + 1) & 1u);
                     if (!(ok = bwd_warp_wait(bar(L::bQFull + st1), ((gstep + 1) >> 1) & 1u, abort_flag, wf, 90, it)))
                         break;
-                    // the dS warps hold P^T of this step in registers
-                    if (!(ok = bwd_warp_wait(bar(L::bPRead), gstep & 1u, abort_flag, wf, 96, it))) break;
                     tc_fence_after_sync();
                     mma_s(st1);
                     commit(L::bSFull);
@@ -598,6 +604,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_settle(bar(L::bDrain), 0, wf, 95);
         }
         __syncwarp();
+    } else {
+        regs_decrease<64>();  // warps 14-15 only complete the last warpgroup
     }
 done:
     __syncwarp();

@@ -26,9 +26,11 @@
 //
 // Tensor memory (512 columns): [0,128) S^T, overwritten by P^T (bf16 pairs);
 // [128,256) dP^T, then the dQ^T partial of the same step; [256,384) dV;
-// [384,512) dK.  Shared memory: K and V of the tile, a 2-stage ring of
-// (Q, dO) tiles, and one dS^T tile that serves as the K-major A operand of
-// dK and the MN-major B operand of dQ^T.
+// [384,512) dK.  Shared memory: K and V of the tile; a 3-stage ring of Q
+// tiles (each with its lse2 row), because S^T of the next step is issued
+// before the current step's dK has released its Q; one dO stage, released by
+// P.V halfway through a step; a 2-stage ring of delta rows; and one dS^T tile
+// that serves as the K-major A operand of dK and the MN-major B operand of dQ^T.
 //
 // Roles (512 threads, one persistent CTA per SM):
 //   warps 0-3   thread t owns TMEM lane t: reads the dQ^T partial (head
@@ -103,14 +105,17 @@ constexpr int kHalf = kTileBytes / 2;             // one 64-column box
 
 struct BwdSmem {
     static constexpr int kK = 0, kV = kTileBytes;
-    static constexpr int kQ = 2 * kTileBytes;    // [2] Q stages, each followed by its dO tile
-    static constexpr int kStage = 2 * kTileBytes;
-    static constexpr int kDS = kQ + 2 * kStage;  // dS^T [128 keys][128 queries] bf16
-    static constexpr int kRowStats = kDS + kTileBytes;  // [2 stages] lse2[128], delta[128] (fp32)
-    static constexpr int kBars = kRowStats + 2 * 1024;
-    static constexpr int bKVFull = 0, bKVEmpty = 1, bQFull = 2, bQEmpty = 4, bSFull = 6, bPFull = 7,
-                         bDPFull = 8, bDSFull = 9, bDSEmpty = 10, bDQFull = 11, bDQEmpty = 12,
-                         bDKVFull = 13, bDKVEmpty = 14, bDrain = 15, kNumBars = 16;
+    static constexpr int kQStages = 3;
+    static constexpr int kQ = 2 * kTileBytes;                  // [3] Q tiles
+    static constexpr int kDO = kQ + kQStages * kTileBytes;     // dO tile (one stage: free after P.V)
+    static constexpr int kDS = kDO + kTileBytes;               // dS^T [128 keys][128 queries] bf16
+    static constexpr int kL2 = kDS + kTileBytes;               // [3] lse2 rows (fp32 x 128), with Q
+    static constexpr int kDL = kL2 + kQStages * 512;           // [2] delta rows (fp32 x 128)
+    static constexpr int kBars = kDL + 2 * 512;
+    static constexpr int bKVFull = 0, bKVEmpty = 1, bQFull = 2, bQEmpty = 5, bDOFull = 8, bDOEmpty = 9,
+                         bDLFull = 10, bDLEmpty = 12, bSFull = 14, bPFull = 15, bDPFull = 16, bDSFull = 17,
+                         bDSEmpty = 18, bDQFull = 19, bDQEmpty = 20, bDKVFull = 21, bDKVEmpty = 22, bDrain = 23,
+                         kNumBars = 24;
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     // all the shared memory a CTA may have; the part beyond kBytes absorbs the
@@ -238,9 +243,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(L::bKVFull), 1);
         mbar_init(bar(L::bKVEmpty), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < L::kQStages; ++i) {
             mbar_init(bar(L::bQFull + i), 1);
             mbar_init(bar(L::bQEmpty + i), 1);
+        }
+        mbar_init(bar(L::bDOFull), 1);
+        mbar_init(bar(L::bDOEmpty), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(L::bDLFull + i), 1);
+            mbar_init(bar(L::bDLEmpty + i), 256);
         }
         mbar_init(bar(L::bSFull), 1);
         mbar_init(bar(L::bPFull), 256);
@@ -279,7 +290,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         uint32_t gstep = 0;
         int I = 0;
-        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x, ++I) {
+        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
             const BwdItem w = bwd_item<CAUSAL>(p, it);
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 int h, i;
@@ -331,6 +342,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tc_fence_before_sync();
             mbar_arrive(bar(L::bDKVEmpty));
+            ++I;
         }
     } else if (warp < 12) {
         // ============================================================ P^T and dS^T
@@ -352,14 +364,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bwd_step(p, w, s, h, i);
                 const int q0 = i * kBwdTile;
                 const uint32_t ph = gstep & 1u;
-                // this step's row statistics, staged with its Q and dO tiles
-                // (observed here directly, not through the MMA warp)
-                const float4* l2p = reinterpret_cast<const float4*>(smem + L::kRowStats + (gstep & 1u) * 1024);
-                const float4* dlp = l2p + 32;
+                // this step's row statistics: lse2 staged with its Q tile, delta in
+                // a ring of its own (both observed here directly, not through the
+                // MMA warp)
+                const uint32_t qs = gstep % L::kQStages, qph = (gstep / L::kQStages) & 1u;
+                const uint32_t ds = gstep & 1u, dph = (gstep >> 1) & 1u;
+                const float4* l2p = reinterpret_cast<const float4*>(smem + L::kL2 + qs * 512);
+                const float4* dlp = reinterpret_cast<const float4*>(smem + L::kDL + ds * 512);
                 // pairs above the bottom-right diagonal exist in this tile
                 const bool need_mask = !key_ok || (CAUSAL && q0 < w.j * kBwdTile + kBwdTile - 1 - off);
-                if (!bwd_warp_wait(bar(L::bQFull + (gstep & 1u)), (gstep >> 1) & 1u, abort_flag, wf, 79, it))
-                    goto done;
+                if (!bwd_warp_wait(bar(L::bQFull + qs), qph, abort_flag, wf, 79, it)) goto done;
                 if (!bwd_warp_wait(bar(L::bSFull), ph, abort_flag, wf, 80, it)) goto done;
                 tc_fence_after_sync();
                 uint32_t pk[32];  // bf16 pairs of queries 64ch + (2e, 2e+1)
@@ -406,6 +420,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::bPFull));
                 // dS^T = c P^T (dP^T - delta) for the half's 64 queries
+                if (!bwd_warp_wait(bar(L::bDLFull + ds), dph, abort_flag, wf, 77, it)) goto done;
                 if (!bwd_warp_wait(bar(L::bDPFull), ph, abort_flag, wf, 82, it)) goto done;
                 if (!bwd_warp_wait(bar(L::bDSEmpty), ph ^ 1u, abort_flag, wf, 83, it)) goto done;
                 tc_fence_after_sync();
@@ -445,17 +460,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bwd_fence_proxy_async();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::bDSFull));
+                mbar_arrive(bar(L::bDLEmpty + ds));
             }
         }
     } else if (warp == 12) {
         // ============================================================ TMA producer
         regs_decrease<64>();
         if (lane == 0) {
-            int q_armed[2] = {-1, -1}, kv_armed = -1;
+            int q_armed[L::kQStages] = {-1, -1, -1}, dl_armed[2] = {-1, -1}, do_armed = -1, kv_armed = -1;
             bool drop = p.fault == 1;  // test hook: this CTA's first K/V never arrives
             uint32_t gstep = 0;
             int I = 0;
-            for (int it = blockIdx.x; it < p.num_items; it += gridDim.x, ++I) {
+            for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
                 const BwdItem w = bwd_item<CAUSAL>(p, it);
                 const int bh_kv = w.b * p.Hkv + w.hkv;
                 if (!mbar_wait(bar(L::bKVEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 85, it)) break;
@@ -474,28 +490,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int s = 0; s < w.steps; ++s, ++gstep) {
                     int h, i;
                     bwd_step(p, w, s, h, i);
-                    const int st = (int)(gstep & 1u);
-                    const uint32_t ph = (gstep >> 1) & 1u;
-                    if (!(ok = mbar_wait(bar(L::bQEmpty + st), ph ^ 1u, abort_flag, wf, 86, it))) break;
-                    mbar_arrive_expect_tx(bar(L::bQFull + st), 2 * kTileBytes + 1024);
-                    q_armed[st] = (int)ph;
-                    const uint32_t dst = sb + L::kQ + (uint32_t)(st * L::kStage);
                     const int y = i * kBwdTile, z = w.b * p.Hq + h;
                     const long long ws_row = (long long)z * p.Lq_pad + y;
-                    const uint32_t rs = sb + L::kRowStats + (uint32_t)(st * 1024);
-                    bulk_load(rs, p.lse2 + ws_row, 512, bar(L::bQFull + st));
-                    bulk_load(rs + 512, p.delta + ws_row, 512, bar(L::bQFull + st));
-                    tma_load_3d(dst, &tmQ, bar(L::bQFull + st), 0, y, z);
-                    tma_load_3d(dst + kHalf, &tmQ, bar(L::bQFull + st), 64, y, z);
-                    tma_load_3d(dst + kTileBytes, &tmDO, bar(L::bQFull + st), 0, y, z);
-                    tma_load_3d(dst + kTileBytes + kHalf, &tmDO, bar(L::bQFull + st), 64, y, z);
+                    // Q and its lse2 row (3-stage ring: freed after dK)
+                    const uint32_t qs = gstep % L::kQStages, qph = (gstep / L::kQStages) & 1u;
+                    if (!(ok = mbar_wait(bar(L::bQEmpty + qs), qph ^ 1u, abort_flag, wf, 86, it))) break;
+                    mbar_arrive_expect_tx(bar(L::bQFull + qs), kTileBytes + 512);
+                    q_armed[qs] = (int)qph;
+                    const uint32_t qdst = sb + L::kQ + qs * kTileBytes;
+                    tma_load_3d(qdst, &tmQ, bar(L::bQFull + qs), 0, y, z);
+                    tma_load_3d(qdst + kHalf, &tmQ, bar(L::bQFull + qs), 64, y, z);
+                    bulk_load(sb + L::kL2 + qs * 512, p.lse2 + ws_row, 512, bar(L::bQFull + qs));
+                    // delta row (2-stage ring: freed by the dS warps)
+                    const uint32_t ds = gstep & 1u, dph = (gstep >> 1) & 1u;
+                    if (!(ok = mbar_wait(bar(L::bDLEmpty + ds), dph ^ 1u, abort_flag, wf, 87, it))) break;
+                    mbar_arrive_expect_tx(bar(L::bDLFull + ds), 512);
+                    dl_armed[ds] = (int)dph;
+                    bulk_load(sb + L::kDL + ds * 512, p.delta + ws_row, 512, bar(L::bDLFull + ds));
+                    // dO (one stage: freed after P.V)
+                    if (!(ok = mbar_wait(bar(L::bDOEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 88, it))) break;
+                    mbar_arrive_expect_tx(bar(L::bDOFull), kTileBytes);
+                    do_armed = (int)(gstep & 1u);
+                    tma_load_3d(sb + L::kDO, &tmDO, bar(L::bDOFull), 0, y, z);
+                    tma_load_3d(sb + L::kDO + kHalf, &tmDO, bar(L::bDOFull), 64, y, z);
                 }
                 if (!ok) break;
+                ++I;
             }
             // every copy this thread started has landed before the CTA retires
-            if (kv_armed >= 0) mbar_settle(bar(L::bKVFull), (uint32_t)kv_armed, wf, 87);
+            if (kv_armed >= 0) mbar_settle(bar(L::bKVFull), (uint32_t)kv_armed, wf, 97);
+            for (int t = 0; t < L::kQStages; ++t)
+                if (q_armed[t] >= 0) mbar_settle(bar(L::bQFull + t), (uint32_t)q_armed[t], wf, 98);
             for (int t = 0; t < 2; ++t)
-                if (q_armed[t] >= 0) mbar_settle(bar(L::bQFull + t), (uint32_t)q_armed[t], wf, 88);
+                if (dl_armed[t] >= 0) mbar_settle(bar(L::bDLFull + t), (uint32_t)dl_armed[t], wf, 99);
+            if (do_armed >= 0) mbar_settle(bar(L::bDOFull), (uint32_t)do_armed, wf, 100);
         }
         __syncwarp();
     } else if (warp == 13) {
@@ -518,8 +546,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t dS_kmaj = smem_desc_sw128(sb + L::kDS, 16, 1024);
         const uint64_t dS_mn = smem_desc_sw128(sb + L::kDS, kHalf, 1024);
         // S^T = K Q^T into the S region
-        auto mma_s = [&](int st) {
-            const uint64_t qd = smem_desc_sw128(sb + L::kQ + (uint32_t)(st * L::kStage), 16, 1024);
+        const uint64_t dO_kmaj = smem_desc_sw128(sb + L::kDO, 16, 1024);
+        const uint64_t dO_mn = smem_desc_sw128(sb + L::kDO, kHalf, 1024);
+        auto mma_s = [&](uint32_t qs) {
+            const uint64_t qd = smem_desc_sw128(sb + L::kQ + qs * kTileBytes, 16, 1024);
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) mma_ss(tm + kColS, dK_kmaj + kmaj(kk), qd + kmaj(kk), kIdSS, kk > 0);
@@ -529,30 +559,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t gstep = 0;
         int I = 0;
         bool issued = false, ok = true;
-        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x, ++I) {
+        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
             const BwdItem w = bwd_item<CAUSAL>(p, it);
             if (!(ok = bwd_warp_wait(bar(L::bKVFull), (uint32_t)(I & 1), abort_flag, wf, 89, it))) break;
             {
-                const int st = (int)(gstep & 1u);
-                if (!(ok = bwd_warp_wait(bar(L::bQFull + st), (gstep >> 1) & 1u, abort_flag, wf, 90, it))) break;
+                const uint32_t qs = gstep % L::kQStages, qph = (gstep / L::kQStages) & 1u;
+                if (!(ok = bwd_warp_wait(bar(L::bQFull + qs), qph, abort_flag, wf, 90, it))) break;
                 tc_fence_after_sync();
-                mma_s(st);
+                mma_s(qs);
                 issued = true;
                 commit(L::bSFull);
             }
             for (int s = 0; s < w.steps; ++s, ++gstep) {
-                const int st = (int)(gstep & 1u);
-                const uint32_t stage = sb + L::kQ + (uint32_t)(st * L::kStage);
-                const uint64_t q_mn = smem_desc_sw128(stage, kHalf, 1024);
-                const uint64_t do_kmaj = smem_desc_sw128(stage + kTileBytes, 16, 1024);
-                const uint64_t do_mn = smem_desc_sw128(stage + kTileBytes, kHalf, 1024);
+                const uint32_t qs = gstep % L::kQStages;
+                const uint64_t q_mn = smem_desc_sw128(sb + L::kQ + qs * kTileBytes, kHalf, 1024);
                 // dP^T = V dO^T; its columns held the previous step's dQ
                 if (!(ok = bwd_warp_wait(bar(L::bDQEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 91, it))) break;
+                if (!(ok = bwd_warp_wait(bar(L::bDOFull), gstep & 1u, abort_flag, wf, 101, it))) break;
                 tc_fence_after_sync();
                 if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tm + kColDP, dV_kmaj + kmaj(kk), do_kmaj + kmaj(kk), kIdSS, kk > 0);
+                        mma_ss(tm + kColDP, dV_kmaj + kmaj(kk), dO_kmaj + kmaj(kk), kIdSS, kk > 0);
                 }
                 __syncwarp();
                 commit(L::bDPFull);
@@ -564,17 +592,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tm + kColDV, tm + kColS + (uint32_t)(kk * 8), do_mn + mnmaj(kk), kIdBmn,
+                        mma_ts(tm + kColDV, tm + kColS + (uint32_t)(kk * 8), dO_mn + mnmaj(kk), kIdBmn,
                                (s > 0 || kk > 0) ? 1u : 0u);
                 }
                 __syncwarp();
+                commit(L::bDOEmpty);  // dO's last reader
                 // next step's S^T: P^T of this step has been consumed (MMAs run in order)
                 if (s + 1 < w.steps) {
-                    const int st1 = (int)((gstep + 1) & 1u);
-                    if (!(ok = bwd_warp_wait(bar(L::bQFull + st1), ((gstep + 1) >> 1) & 1u, abort_flag, wf, 90, it)))
-                        break;
+                    const uint32_t q1 = (gstep + 1) % L::kQStages, ph1 = ((gstep + 1) / L::kQStages) & 1u;
+                    if (!(ok = bwd_warp_wait(bar(L::bQFull + q1), ph1, abort_flag, wf, 90, it))) break;
                     tc_fence_after_sync();
-                    mma_s(st1);
+                    mma_s(q1);
                     commit(L::bSFull);
                 }
                 // dK += dS^T Q and dQ = dS K
@@ -593,11 +621,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __syncwarp();
                 commit(L::bDQFull);
                 commit(L::bDSEmpty);
-                commit(L::bQEmpty + st);
+                commit(L::bQEmpty + qs);  // Q's last reader is dK
             }
             if (!ok) break;
             commit(L::bDKVFull);
             commit(L::bKVEmpty);
+            ++I;
         }
         if (issued) {
             commit(L::bDrain);

@@ -354,8 +354,13 @@ def main(argv=None):
     o = torch.empty(out_shape, dtype=torch.float32, device=dev)
     lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
-    l2_note = ("inputs larger than L2 (Q+K+V+O = %.0f MiB vs 126 MiB L2); no flush" %
-               ((in_bytes + o.numel() * 4) / 2**20))
+    if w.bwd:  # Q, K, V, dO, O, LSE in; dQ, dK, dV out
+        in_bytes += do.numel() * 2 + o_f.numel() * 4 + dk_b.numel() * 8
+        l2_note = ("operands larger than L2 (Q+K+V+dO+O+dQ+dK+dV = %.0f MiB vs 126 MiB L2); no flush" %
+                   ((in_bytes + o.numel() * 4) / 2**20))
+    else:
+        l2_note = ("inputs larger than L2 (Q+K+V+O = %.0f MiB vs 126 MiB L2); no flush" %
+                   ((in_bytes + o.numel() * 4) / 2**20))
 
     def barrier():
         torch.cuda.synchronize(dev)

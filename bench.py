@@ -208,6 +208,8 @@ def cpu_oracle_rate(w, inputs, seconds: float, rng_seed: int = 0):
     rng = np.random.default_rng(rng_seed)
     if w.bwd:
         return _cpu_backward_rate(w, inputs, seconds)
+    if w.window is not None:
+        return _cpu_variant_rate(w, inputs, seconds)
     if w.varlen:
         q, k, v, cq, ck = inputs
         Tq = q.shape[0]
@@ -262,6 +264,31 @@ def _cpu_backward_rate(w, inputs, seconds: float):
     n = int(min(w.Lq, max(n, n * seconds / max(dt, 1e-6))))
     dt, fl = run(n)
     return fl / dt / 1e12, oracle.num_cpus(), f"backward of the last {n} query rows of one head ({dt:.1f} s)"
+
+
+def _cpu_variant_rate(w, inputs, seconds: float):
+    """Time the fp64 variant oracle on the last n query rows of one head (whole
+    1024-row blocks of the oracle); FLOPs: 4 * D per allowed pair."""
+    import numpy as np
+
+    import oracle
+    from oracle.variants import attention_variant
+    q, k, v = inputs
+
+    def run(n):
+        rows = np.arange(w.Lq - n, w.Lq)
+        t0 = time.perf_counter()
+        attention_variant(q[:1, :1], k[:1, :1], v[:1, :1], w.scale, w.window, rows=rows)
+        dt = time.perf_counter() - t0
+        c = rows + (w.Lk - w.Lq)
+        lo = np.maximum(0, c - w.window[0]) if w.window[0] >= 0 else np.zeros_like(c)
+        hi = np.minimum(w.Lk - 1, c + w.window[1]) if w.window[1] >= 0 else np.full_like(c, w.Lk - 1)
+        return dt, 4.0 * w.D * float(np.maximum(hi - lo + 1, 0).sum())
+    n = 1024
+    dt, _ = run(n)
+    n = int(min(w.Lq, max(1024, (n * seconds / max(dt, 1e-6)) // 1024 * 1024)))
+    dt, fl = run(n)
+    return fl / dt / 1e12, oracle.num_cpus(), f"last {n} query rows of one head ({dt:.1f} s)"
 
 
 # ------------------------------------------------------------------ reference arm
@@ -336,6 +363,12 @@ def main(argv=None):
 
         def step(o=None, lse=None, qq=q, kk=k, vv=v):  # o receives dQ
             return fa.fa_bwd(qq, kk, vv, o_f, lse_f, do, causal=w.causal, dq=o, dk=dk_b, dv=dv_b, workspace=ws_b)
+        out_shape, lse_shape = tuple(q.shape), (w.B, w.Hq, w.Lq)
+    elif w.window is not None:
+        q, k, v = (t.to(dev) for t in host_inputs)
+
+        def step(o=None, lse=None, qq=q, kk=k, vv=v):
+            return fa.fa_fwd_variant(qq, kk, vv, window=w.window, out=o, lse=lse)
         out_shape, lse_shape = tuple(q.shape), (w.B, w.Hq, w.Lq)
     elif w.decode:
         q, k, v = (t.to(dev) for t in host_inputs)
@@ -418,6 +451,8 @@ def main(argv=None):
             elif w.bwd:
                 fa.fa_bwd(d_in[0], d_in[1], d_in[2], d_in[4], d_in[5], d_in[3], causal=w.causal, dq=o, dk=dk_b,
                           dv=dv_b, workspace=ws_b)
+            elif w.window is not None:
+                fa.fa_fwd_variant(d_in[0], d_in[1], d_in[2], window=w.window, out=o, lse=lse)
             else:
                 fa.fa_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse)
             h_o.copy_(o, non_blocking=True)
@@ -473,8 +508,9 @@ def main(argv=None):
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                     "peak_kind": f"{peak_kind} burst bf16 GEMM", "frac_of_sustained": achieved / peak_sus,
-                    "kernel": "fa_fwd_sm103_kernel<%d,%s,%s>" % (w.D, str(w.causal).lower(),
-                                                                str(w.varlen).lower())}
+                    "kernel": "fa_fwd_sm103_kernel<%d,%s,%s,%d>" % (w.D, str(w.causal).lower(),
+                                                                   str(w.varlen).lower(),
+                                                                   1 if w.window is not None else 0)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

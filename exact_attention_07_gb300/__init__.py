@@ -10,6 +10,7 @@ sm_103 GPU the call raises.
     o, lse = fa_fwd_varlen(q, k, v, cu_q, cu_k, max_q, max_k, causal=True)
     o, lse = fa_fwd_splitkv(q, k, v, causal=True)    # decode: (Hq/Hkv)*Lq <= 16, long Lk
     dq, dk, dv = fa_bwd(q, k, v, o, lse, do, causal=True)
+    o, lse = fa_fwd_variant(q, k, v, window=(4095, 0), softcap=0.0, alibi_slopes=None)
 """
 from __future__ import annotations
 
@@ -20,7 +21,8 @@ import threading
 
 import torch
 
-__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_splitkv", "splitkv_workspace", "fa_bwd",
+__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
+           "fa_fwd_splitkv", "splitkv_workspace", "fa_bwd",
            "bwd_workspace", "fa_check", "fa_status_string", "fa_last_launch_count",
            "FAError", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
@@ -30,10 +32,16 @@ _lock = threading.Lock()
 _lib = None
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
-                    "fa_bwd", "fa_bwd_workspace", "fa_check", "fa_status_string", "fa_last_launch_count", "fa_test_inject_fault")
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
+                    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace", "fa_bwd", "fa_bwd_workspace", "fa_check", "fa_status_string", "fa_last_launch_count", "fa_test_inject_fault")
 SPLITKV_MAX_ROWS = 16  # (Hq / Hkv) * Lq limit of fa_fwd_splitkv
 NOALLOC_MAX_SEQS = 16384  # FA_NOALLOC_MAX_SEQS in include/fa_gb300.h
+
+
+class _Variant(ctypes.Structure):
+    # struct fa_variant in include/fa_gb300.h
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int), ("softcap", ctypes.c_float),
+                ("alibi_slopes", ctypes.c_void_p)]
 
 
 class FAError(RuntimeError):
@@ -68,6 +76,11 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd_splitkv_workspace.restype = i
         lib.fa_fwd_splitkv_workspace.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t),
                                                  ctypes.POINTER(ctypes.c_int)]
+        vr = ctypes.POINTER(_Variant)
+        lib.fa_fwd_variant.restype = i
+        lib.fa_fwd_variant.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vr, f, vp]
+        lib.fa_fwd_varlen_variant.restype = i
+        lib.fa_fwd_varlen_variant.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vr, f, vp]
         lib.fa_bwd.restype = i
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
         lib.fa_bwd_workspace.restype = i
@@ -205,6 +218,75 @@ def fa_fwd_varlen_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_
                                        float(softmax_scale), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_varlen_noalloc")
+    return out, lse
+
+
+def _variant(window, softcap, alibi_slopes, Hq: int, device):
+    if alibi_slopes is not None:
+        _check_tensor(alibi_slopes, "alibi_slopes", torch.float32, 1)
+        if alibi_slopes.numel() != Hq or alibi_slopes.device != device:
+            raise ValueError("alibi_slopes must be a float32 tensor of Hq elements on the inputs' device")
+    wl, wr = window
+    return _Variant(int(wl), int(wr), float(softcap), alibi_slopes.data_ptr() if alibi_slopes is not None else None)
+
+
+def fa_fwd_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window=(-1, -1), softcap: float = 0.0,
+                   alibi_slopes: torch.Tensor | None = None, softmax_scale: float | None = None,
+                   out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """Dense forward with a key window (left, right) around each query's
+    bottom-right-aligned position (-1 = unlimited), soft-capping of the
+    scaled scores, or ALiBi slopes per query head.  D = 128."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, torch.bfloat16, 4)
+    B, Hq, Lq, D = q.shape
+    Bk, Hkv, Lk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError("shape mismatch")
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out is None else out
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensor(out, "out", torch.float32, 4)
+    _check_tensor(lse, "lse", torch.float32, 3)
+    if tuple(out.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Lq):
+        raise ValueError("out/lse shape mismatch")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    var = _variant(window, softcap, alibi_slopes, Hq, q.device)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_variant(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq,
+                                Hkv, Lq, Lk, D, ctypes.byref(var), float(softmax_scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_variant")
+    return out, lse
+
+
+def fa_fwd_varlen_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                          cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, window=(-1, -1),
+                          softcap: float = 0.0, alibi_slopes: torch.Tensor | None = None,
+                          softmax_scale: float | None = None, out: torch.Tensor | None = None,
+                          lse: torch.Tensor | None = None, stream=None):
+    """Packed forward with a variant; windows and distances are per sequence."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, torch.bfloat16, 3)
+    _check_tensor(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check_tensor(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    Tq, Hq, D = q.shape
+    Tk, Hkv, _ = k.shape
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out is None else out
+    lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensor(out, "out", torch.float32, 3)
+    _check_tensor(lse, "lse", torch.float32, 2)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    var = _variant(window, softcap, alibi_slopes, Hq, q.device)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_varlen_variant(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                       cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), cu_seqlens_q.numel() - 1,
+                                       Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, ctypes.byref(var),
+                                       float(softmax_scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_varlen_variant")
     return out, lse
 
 

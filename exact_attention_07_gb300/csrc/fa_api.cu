@@ -104,6 +104,35 @@ int heads_per_section(int Hkv, long long Lk, int D)
 }
 
 template <bool VARLEN>
+cudaError_t dispatch_variant(int var, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                             const FwdParams& p, int grid, cudaStream_t st)
+{
+    if (var == kVarSoftcap) return launch_fwd<128, false, VARLEN, kVarSoftcap>(q, k, v, p, grid, st);
+    if (var == kVarAlibi) return launch_fwd<128, false, VARLEN, kVarAlibi>(q, k, v, p, grid, st);
+    return launch_fwd<128, false, VARLEN, kVarWindow>(q, k, v, p, grid, st);
+}
+
+// Validates a variant description and fills the kernel parameters; returns
+// the variant kind (kVar*) or a negative fa_status_t.
+int prepare_variant(const fa_variant_t* var, int D, float scale, FwdParams* p)
+{
+    if (!var) return -(int)FA_ERR_INVALID_ARG;
+    if (!std::isfinite(var->softcap) || var->softcap < 0.f) return -(int)FA_ERR_INVALID_ARG;
+    if (var->alibi_slopes && (reinterpret_cast<uintptr_t>(var->alibi_slopes) & 3u)) return -(int)FA_ERR_INVALID_ARG;
+    if (D != 128) return -(int)FA_ERR_UNSUPPORTED;
+    if (var->softcap > 0.f && var->alibi_slopes) return -(int)FA_ERR_UNSUPPORTED;
+    p->win_left = var->window_left < 0 ? -1 : var->window_left;
+    p->win_right = var->window_right < 0 ? -1 : var->window_right;
+    p->alibi = var->alibi_slopes;
+    if (var->softcap > 0.f) {
+        p->cap_in = scale / var->softcap;
+        p->cap_out = (float)((double)var->softcap * 1.4426950408889634);
+        return kVarSoftcap;
+    }
+    return var->alibi_slopes ? kVarAlibi : kVarWindow;
+}
+
+template <bool VARLEN>
 cudaError_t dispatch(int D, bool causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                      const FwdParams& p, int grid, cudaStream_t st)
 {
@@ -204,9 +233,10 @@ cudaError_t launch_varlen_schedule(const int* cu_q, const int* cu_k, int num_seq
 
 using namespace fa;
 
-extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq,
-                              int Hkv, int Lq, int Lk, int D, int causal, float softmax_scale,
-                              cudaStream_t stream)
+namespace {
+fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq, int Hkv,
+                      int Lq, int Lk, int D, int causal, const fa_variant_t* variant, float softmax_scale,
+                      cudaStream_t stream)
 {
     g_last_launches = 0;
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
@@ -219,6 +249,12 @@ extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, float
     const long long tiles = (long long)B * Hq * nmb;
     if (tiles >= (1ll << 31) || (long long)B * Hq >= (1ll << 31) || (long long)B * Hkv >= (1ll << 31))
         return FA_ERR_INVALID_ARG;
+    FwdParams p{};
+    int var = kVarNone;
+    if (variant) {
+        var = prepare_variant(variant, D, softmax_scale, &p);
+        if (var < 0) return (fa_status_t)(-var);
+    }
     DeviceState* ds = nullptr;
     fa_status_t st = device_state(&ds);
     if (st != FA_OK) return st;
@@ -230,7 +266,6 @@ extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, float
         !encode_map(&mv, v, D, Lk, (uint64_t)B * Hkv, row, row * Lk, 128, 1))
         return FA_ERR_CUDA;
 
-    FwdParams p{};
     p.o = o;
     p.lse = lse;
     p.B = B;
@@ -247,15 +282,34 @@ extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, float
     p.fault = g_fault_next;
     g_fault_next = 0;
     const int grid = (int)(tiles < ds->num_sms ? tiles : ds->num_sms);
-    if (dispatch<false>(D, causal != 0, mq, mk, mv, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+    const cudaError_t e = variant ? dispatch_variant<false>(var, mq, mk, mv, p, grid, stream)
+                                  : dispatch<false>(D, causal != 0, mq, mk, mv, p, grid, stream);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 1;
     return FA_OK;
 }
+}  // namespace
 
-extern "C" fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse,
-                                     const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
-                                     int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int Hq,
-                                     int Hkv, int D, int causal, float softmax_scale, cudaStream_t stream)
+extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq,
+                              int Hkv, int Lq, int Lk, int D, int causal, float softmax_scale,
+                              cudaStream_t stream)
+{
+    return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, causal, nullptr, softmax_scale, stream);
+}
+
+extern "C" fa_status_t fa_fwd_variant(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                                      int Hq, int Hkv, int Lq, int Lk, int D, const fa_variant_t* variant,
+                                      float softmax_scale, cudaStream_t stream)
+{
+    if (!variant) return FA_ERR_INVALID_ARG;
+    return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, 0, variant, softmax_scale, stream);
+}
+
+namespace {
+fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse, const int* cu_seqlens_q,
+                       const int* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
+                       int max_seqlen_k, int Hq, int Hkv, int D, int causal, const fa_variant_t* variant,
+                       float softmax_scale, cudaStream_t stream)
 {
     g_last_launches = 0;
     if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
@@ -274,6 +328,12 @@ extern "C" fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v
     if ((long long)Hq * ((long long)total_q / kRowsPerCta + num_seqs) >= (1ll << 31) ||
         (long long)total_q * Hq >= (1ll << 31) * 64ll)
         return FA_ERR_INVALID_ARG;
+    FwdParams p{};
+    int var = kVarNone;
+    if (variant) {
+        var = prepare_variant(variant, D, softmax_scale, &p);
+        if (var < 0) return (fa_status_t)(-var);
+    }
     DeviceState* ds = nullptr;
     fa_status_t st = device_state(&ds);
     if (st != FA_OK) return st;
@@ -293,7 +353,6 @@ extern "C" fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v
         cudaFreeAsync(sched, stream);
         return FA_ERR_CUDA;
     }
-    FwdParams p{};
     p.o = o;
     p.lse = lse;
     p.Hq = Hq;
@@ -309,11 +368,33 @@ extern "C" fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v
     p.err = ds->err;
     p.diag = ds->diag;
     const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
-    const cudaError_t e = dispatch<true>(D, causal != 0, mq, mk, mv, p, grid, stream);
+    const cudaError_t e = variant ? dispatch_variant<true>(var, mq, mk, mv, p, grid, stream)
+                                  : dispatch<true>(D, causal != 0, mq, mk, mv, p, grid, stream);
     cudaFreeAsync(sched, stream);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 2;
     return FA_OK;
+}
+}  // namespace
+
+extern "C" fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse,
+                                     const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                                     int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int Hq,
+                                     int Hkv, int D, int causal, float softmax_scale, cudaStream_t stream)
+{
+    return fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                      max_seqlen_k, Hq, Hkv, D, causal, nullptr, softmax_scale, stream);
+}
+
+extern "C" fa_status_t fa_fwd_varlen_variant(const void* q, const void* k, const void* v, float* o, float* lse,
+                                             const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                                             int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                                             int Hq, int Hkv, int D, const fa_variant_t* variant,
+                                             float softmax_scale, cudaStream_t stream)
+{
+    if (!variant) return FA_ERR_INVALID_ARG;
+    return fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                      max_seqlen_k, Hq, Hkv, D, 0, variant, softmax_scale, stream);
 }
 
 // ------------------------------------------------------------- allocation-free varlen

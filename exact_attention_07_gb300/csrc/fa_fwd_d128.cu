@@ -4,11 +4,11 @@
 
 namespace fa {
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, int VAR>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const FwdParams& p, int grid, cudaStream_t stream)
 {
-    auto kern = fa_fwd_sm103_kernel<D, CAUSAL, VARLEN>;
+    auto kern = fa_fwd_sm103_kernel<D, CAUSAL, VARLEN, VAR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          FwdSmem<D>::kAlloc);
     if (e != cudaSuccess) return e;
@@ -16,16 +16,26 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
     return cudaGetLastError();
 }
 
-#define FA_INSTANCE(D, C, V)                                                                        \
-    template cudaError_t launch_fwd<D, C, V>(const CUtensorMap&, const CUtensorMap&,              \
-                                             const CUtensorMap&, const FwdParams&, int, cudaStream_t);
+#define FA_INSTANCE(D, C, V, VAR)                                                                        \
+    template cudaError_t launch_fwd<D, C, V, VAR>(const CUtensorMap&, const CUtensorMap&,              \
+                                                  const CUtensorMap&, const FwdParams&, int, cudaStream_t);
 
+#ifndef FA_VARIANTS
 #ifndef FA_HEAD_DIM
 #define FA_HEAD_DIM 128
 #endif
-FA_INSTANCE(FA_HEAD_DIM, false, false)
-FA_INSTANCE(FA_HEAD_DIM, true, false)
-FA_INSTANCE(FA_HEAD_DIM, false, true)
-FA_INSTANCE(FA_HEAD_DIM, true, true)
+FA_INSTANCE(FA_HEAD_DIM, false, false, kVarNone)
+FA_INSTANCE(FA_HEAD_DIM, true, false, kVarNone)
+FA_INSTANCE(FA_HEAD_DIM, false, true, kVarNone)
+FA_INSTANCE(FA_HEAD_DIM, true, true, kVarNone)
+#else
+// score variants: D = 128, dense and packed
+FA_INSTANCE(128, false, false, kVarWindow)
+FA_INSTANCE(128, false, true, kVarWindow)
+FA_INSTANCE(128, false, false, kVarSoftcap)
+FA_INSTANCE(128, false, true, kVarSoftcap)
+FA_INSTANCE(128, false, false, kVarAlibi)
+FA_INSTANCE(128, false, true, kVarAlibi)
+#endif
 
 }  // namespace fa

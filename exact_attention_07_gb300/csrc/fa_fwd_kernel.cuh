@@ -72,13 +72,14 @@ struct Work {
     int q0;      // varlen: first query token of the sequence
     int b;       // dense batch index
     int nk;      // number of KV tiles this block visits (0: every row is empty)
+    int kf;      // first KV tile it visits (key windows skip the tiles before it)
 };
 
 // Tile order (FlashAttention-4: Blackwell Attention Kernel Co-Design, "LPT scheduling for imbalanced grids"):
 // batches (or sequences, longest first) outermost; KV heads in L2-sized
 // sections; inside a section the 256-row blocks in reverse order when causal
 // (longest work first), then the KV head, then the query heads sharing it.
-template <bool CAUSAL, bool VARLEN>
+template <bool CAUSAL, bool VARLEN, int VAR>
 __device__ __forceinline__ Work decode_tile(const FwdParams& p, int t)
 {
     Work w;
@@ -129,8 +130,21 @@ __device__ __forceinline__ Work decode_tile(const FwdParams& p, int t)
         w.zq = w.b * p.Hq + w.hq;
         w.zk = w.b * p.Hkv + w.hkv;
     }
+    w.kf = 0;
     if (w.lk <= 0) {
         w.nk = 0;
+    } else if (VAR != kVarNone) {
+        // key window [c - left, c + right] around each row's aligned position c
+        const int off = w.lk - w.lq;
+        const int last_row = min(w.m0 + kRowsPerCta - 1, w.lq - 1);
+        const int lo = p.win_left >= 0 ? max(0, w.m0 + off - p.win_left) : 0;
+        const int hi = p.win_right >= 0 ? min(w.lk - 1, last_row + off + p.win_right) : w.lk - 1;
+        if (hi < lo) {
+            w.nk = 0;
+        } else {
+            w.kf = lo / kBlockN;
+            w.nk = hi / kBlockN - w.kf + 1;
+        }
     } else if (!CAUSAL) {
         w.nk = (w.lk + kBlockN - 1) / kBlockN;
     } else {
@@ -139,6 +153,13 @@ __device__ __forceinline__ Work decode_tile(const FwdParams& p, int t)
         w.nk = last_key < 0 ? 0 : last_key / kBlockN + 1;
     }
     return w;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -205,7 +226,7 @@ __device__ __forceinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs
     __syncwarp();
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, int VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const FwdParams p)
@@ -275,11 +296,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = p.scale_log2;
         uint32_t s_ph = 0, st_ph = 1;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
+            const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, tile);
             if (w.nk == 0) continue;
             const int q_row = w.m0 + t * kBlockM + row;
             int kv_last = w.lk - 1;  // last key this row may attend
-            if (CAUSAL) kv_last = min(kv_last, q_row + (w.lk - w.lq));
+            int kv_first = 0;        // first key this row may attend
+            const int c_row = q_row + (w.lk - w.lq);  // the row's aligned position among the keys
+            if (CAUSAL) kv_last = min(kv_last, c_row);
+            if constexpr (VAR != kVarNone) {
+                if (p.win_right >= 0) kv_last = min(kv_last, c_row + p.win_right);
+                if (p.win_left >= 0) kv_first = max(0, c_row - p.win_left);
+            }
+            float alibi_l2 = 0.f;  // ALiBi slope of this head, log2 units
+            if constexpr (VAR == kVarAlibi) alibi_l2 = __ldg(p.alibi + w.hq) * 1.4426950408889634f;
+            // score multiplier inside the exponent: the score modifiers already
+            // produce log2-unit scores
+            const float smul = VAR >= kVarSoftcap ? 1.f : sl2;
             float r = -INFINITY, l = 0.f, l_rnd = 0.f;
             for (int j = 0; j < w.nk; ++j) {
                 if (!warp_wait(bar(L::kSFull + t), s_ph, abort_flag, wf, 1 + t, tile)) goto done;
@@ -289,15 +321,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, sv[c]);
                 tmem_wait_ld();
-                // masking: keys past the row's last allowed key (causal diagonal,
-                // sequence tail) get -inf (FlashAttention from Scratch, sec. 7.3)
-                const int nvalid = kv_last - j * kBlockN + 1;
-                if (__any_sync(0xffffffffu, nvalid < kBlockN)) {
+                const int key0 = (j + w.kf) * kBlockN;
+                // score modifiers (FlashAttention from Scratch, sec. 12), in log2 units
+                if constexpr (VAR == kVarSoftcap) {
+                    // cap * tanh(s * scale / cap), tanh(u) = 1 - 2 / (1 + e^(2u))
+                    const float k2 = p.cap_in * (2.f * 1.4426950408889634f);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float e2u = ex2_approx(__uint_as_float(sv[c][i]) * k2);
+                            const float th = fmaf(-2.f, rcp_approx(1.f + e2u), 1.f);
+                            sv[c][i] = __float_as_uint(th * p.cap_out);
+                        }
+                } else if constexpr (VAR == kVarAlibi) {
+                    // s * scale - slope * |c - key|
+                    const float cf = (float)(c_row - key0);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (32 * c + i >= nvalid) sv[c][i] = __float_as_uint(-INFINITY);
+                            sv[c][i] = __float_as_uint(fmaf(-alibi_l2, fabsf(cf - (float)(32 * c + i)),
+                                                            __uint_as_float(sv[c][i]) * sl2));
+                }
+                // masking: keys outside [kv_first, kv_last] (causal diagonal, key
+                // window, sequence tail) get -inf (FlashAttention from Scratch, sec. 7.3)
+                const int nvalid = kv_last - key0 + 1;
+                const int nskip = kv_first - key0;
+                if (__any_sync(0xffffffffu, nvalid < kBlockN || nskip > 0)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i >= nvalid || 32 * c + i < nskip) sv[c][i] = __float_as_uint(-INFINITY);
                 }
                 // row maximum of the raw scores
                 float mx[8];
@@ -313,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], mx[i + 4]);
-                const float mrow = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+                const float mrow = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * smul;
                 // conditional rescale: keep r unless the maximum rose by more than tau
                 const float r_new = (mrow - r > kTau) ? mrow : r;
                 const float alpha = (r_new == r) ? 1.f : ex2_approx(r - r_new);
@@ -324,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // denominator weight every key identically) and of the fp32 p (it
                 // gives the LSE).
                 l_rnd *= alpha;
-                const uint64_t c2 = f2_pack(sl2, sl2);
+                const uint64_t c2 = f2_pack(smul, smul);
                 const uint64_t nr2 = f2_pack(-r_use, -r_use);
                 uint64_t sum_t[2] = {0ull, 0ull}, sum_r[2] = {0ull, 0ull};
 #pragma unroll
@@ -386,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o_ph[2] = {0, 0}, st_ph[2] = {0, 0};
         float* obase = reinterpret_cast<float*>(p.o);
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
+            const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, tile);
             for (int t = 0; t < 2; ++t) {
                 const int q_row = w.m0 + t * kBlockM + row;
                 const bool valid = q_row < w.lq;
@@ -484,10 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < kHalves; ++h) {
                         if constexpr (VARLEN)
                             tma_load_3d(dst + h * (L::kTileBytes / kHalves), map, bar(L::kKVFull + stage),
-                                        64 * h, w.hkv, w.zk + j * kBlockN);
+                                        64 * h, w.hkv, w.zk + (j + w.kf) * kBlockN);
                         else
                             tma_load_3d(dst + h * (L::kTileBytes / kHalves), map, bar(L::kKVFull + stage),
-                                        64 * h, j * kBlockN, w.zk);
+                                        64 * h, (j + w.kf) * kBlockN, w.zk);
                     }
                     if (++stage == L::kStages) {
                         stage = 0;
@@ -496,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return true;
                 };
                 for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                    const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
+                    const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, tile);
                     if (w.nk == 0) continue;
                     if (!load_q(w, 0, tile)) break;
                     if (!load_kv(&tmK, w, 0, tile)) break;
@@ -534,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             };
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                const Work w = decode_tile<CAUSAL, VARLEN>(p, tile);
+                const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, tile);
                 if (w.nk == 0) continue;
                 const int nk = w.nk;
                 // prologue: S0(0), S1(0)

@@ -1,0 +1,4 @@
+// Kernel instances of the score variants (key window, soft-capping, ALiBi),
+// head dimension 128 (same source as the D = 128 unit).
+#define FA_VARIANTS 1
+#include "fa_fwd_d128.cu"

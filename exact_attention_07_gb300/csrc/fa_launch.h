@@ -12,7 +12,7 @@ namespace fa {
 // Dynamic shared memory the attention kernel needs for head dimension D.
 int fwd_smem_bytes(int D);
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, int VAR = kVarNone>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const FwdParams& p, int grid, cudaStream_t stream);
 

@@ -20,6 +20,11 @@ struct FwdParams {
     const int* sched;  // [0] tiles, [1..n+1] tile prefix in schedule order, [n+2..2n+1] order
     int num_seqs;
     int total_q;
+    // programmable variants (kernels instantiated with VAR > 0)
+    int win_left, win_right;  // key window around the query's aligned position; < 0 = unlimited
+    float cap_in;             // soft-capping: scale / cap
+    float cap_out;            // soft-capping: cap * log2(e)
+    const float* alibi;       // ALiBi: per query head slope (natural-log units)
     // error reporting
     int* err;
     int* diag;
@@ -31,5 +36,9 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 constexpr int kRowsPerCta = 2 * kBlockM;
 constexpr int kThreads = 512;
+
+// Score variants of the forward kernel (FlashAttention from Scratch, sec. 12):
+// 0 = plain, 1 = key window, 2 = key window + soft-capping, 3 = key window + ALiBi.
+enum : int { kVarNone = 0, kVarWindow = 1, kVarSoftcap = 2, kVarAlibi = 3 };
 
 }  // namespace fa

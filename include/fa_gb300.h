@@ -128,6 +128,44 @@ fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, f
                                   cudaStream_t stream);
 
 /*
+ * Programmable variants of the forward (FlashAttention from Scratch, sec. 12
+ * "Programmable attention: FlexAttention meets FA4"): which query-key pairs
+ * may attend, and a modification of the score before the softmax.
+ *
+ *   window_left, window_right: key j may attend query i iff
+ *       c_i - window_left <= j <= c_i + window_right,  c_i = i + (Lk - Lq)
+ *     (c_i is the query's position in the key sequence, bottom-right
+ *     aligned as for the causal mask; per sequence for packed batches).
+ *     A negative bound is unlimited: (-1, -1) is full attention, (-1, 0) the
+ *     causal mask, (w - 1, 0) a causal sliding window of width w.  KV tiles
+ *     outside every row's window are skipped.
+ *   softcap > 0: the scaled score s becomes softcap * tanh(s / softcap).
+ *   alibi_slopes: DEVICE fp32 [Hq] (or NULL); the score of query head h
+ *     becomes s - alibi_slopes[h] * |c_i - j|.
+ *   Order: scale, then the score modifier, then the window.  softcap and
+ *   alibi_slopes cannot be combined (FA_ERR_UNSUPPORTED); D must be 128.
+ *   LSE is the log-sum-exp of the modified scores.
+ */
+typedef struct fa_variant {
+    int window_left;
+    int window_right;
+    float softcap;
+    const float* alibi_slopes;
+} fa_variant_t;
+
+/* fa_fwd with a variant (same layouts; `variant` is a HOST pointer). */
+fa_status_t fa_fwd_variant(const void* q, const void* k, const void* v, float* o, float* lse,
+                           int B, int Hq, int Hkv, int Lq, int Lk, int D, const fa_variant_t* variant,
+                           float softmax_scale, cudaStream_t stream);
+
+/* fa_fwd_varlen with a variant (windows and ALiBi distances per sequence). */
+fa_status_t fa_fwd_varlen_variant(const void* q, const void* k, const void* v, float* o, float* lse,
+                                  const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                                  int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                                  int Hq, int Hkv, int D, const fa_variant_t* variant,
+                                  float softmax_scale, cudaStream_t stream);
+
+/*
  * Split-KV forward for decode (FlashAttention from Scratch, sec. 9.1 "Split
  * the long dimension that remains"; sec. 4.3 "Merge independently computed
  * partitions").  Same operation, layouts and causal rule as fa_fwd, for

@@ -127,3 +127,20 @@ def test_bwd_argument_validation(lib):
     assert lib.fa_bwd_workspace(2, 3, 130, ctypes.byref(n)) == fa.FA_OK
     assert n.value == 2 * 4 * 2 * 3 * 256            # delta and lse2, rows padded to 128
     assert lib.fa_bwd_workspace(2, 3, 0, ctypes.byref(n)) == INV
+
+
+def test_variant_argument_validation(lib):
+    INV, UNS = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+    from exact_attention_07_gb300 import _Variant
+
+    def call(var, D=128):
+        return lib.fa_fwd_variant(16, 16, 16, 16, 16, 1, 2, 1, 64, 64, D, var, 0.1, None)
+
+    assert call(None) == INV
+    assert call(ctypes.byref(_Variant(-1, 0, float("nan"), None))) == INV
+    assert call(ctypes.byref(_Variant(-1, 0, -1.0, None))) == INV
+    assert call(ctypes.byref(_Variant(-1, 0, 0.0, 18))) == INV        # misaligned slopes
+    assert call(ctypes.byref(_Variant(-1, 0, 0.0, None)), D=64) == UNS
+    assert call(ctypes.byref(_Variant(-1, 0, 5.0, 16))) == UNS        # soft-capping with ALiBi
+    assert lib.fa_fwd_varlen_variant(16, 16, 16, 16, 16, 32, 32, 1, 10, 10, 8, 8, 2, 2, 128, None, 0.1,
+                                     None) == INV

@@ -44,6 +44,9 @@ class Workload:
     decode: bool = False
     # the backward pass (fa_bwd) of this problem instead of the forward
     bwd: bool = False
+    # key window (left, right) around each query's aligned position, run
+    # through the variant forward (-1 = unlimited)
+    window: tuple[int, int] | None = None
 
     @property
     def scale(self) -> float:
@@ -64,6 +67,13 @@ class Workload:
             total = sum(4.0 * self.Hq * L * L * self.D for L in self.seqlens)
         else:
             total = 4.0 * self.B * self.Hq * self.Lq * self.Lk * self.D
+        if self.window is not None:  # count only the pairs the window allows
+            import numpy as np
+            c = np.arange(self.Lq, dtype=np.int64) + (self.Lk - self.Lq)
+            lo = np.maximum(0, c - self.window[0]) if self.window[0] >= 0 else np.zeros_like(c)
+            hi = np.minimum(self.Lk - 1, c + self.window[1]) if self.window[1] >= 0 else np.full_like(c, self.Lk - 1)
+            pairs = float(np.maximum(hi - lo + 1, 0).sum())
+            return 4.0 * self.B * self.Hq * pairs * self.D
         if self.bwd:  # five matrix products instead of two (S, dP, dV, dQ, dK)
             total *= 2.5
         return total / 2 if self.causal else total
@@ -178,6 +188,15 @@ BWD_WORKLOADS: dict[str, Workload] = {
     "bwd_b1_h16_l4096_d128": Workload("bwd_b1_h16_l4096_d128", 1, 16, 16, 4096, 4096, 128, False, bwd=True),
 }
 WORKLOADS.update(BWD_WORKLOADS)
+
+# Causal sliding window of width 4096 over the long-sequence shape (the
+# variant forward skips KV tiles outside every row's window; FLOPs count the
+# allowed pairs only).
+VARIANT_WORKLOADS: dict[str, Workload] = {
+    "swa4096_b1_h16_l16384_d128": Workload("swa4096_b1_h16_l16384_d128", 1, 16, 16, 16384, 16384, 128, False,
+                                           window=(4095, 0)),
+}
+WORKLOADS.update(VARIANT_WORKLOADS)
 
 # The configuration the throughput metric is quoted on.
 HEADLINE = "b1_h16_l16384_d128"

@@ -364,6 +364,15 @@ def main(argv=None):
         def step(o=None, lse=None, qq=q, kk=k, vv=v):  # o receives dQ
             return fa.fa_bwd(qq, kk, vv, o_f, lse_f, do, causal=w.causal, dq=o, dk=dk_b, dv=dv_b, workspace=ws_b)
         out_shape, lse_shape = tuple(q.shape), (w.B, w.Hq, w.Lq)
+    elif w.fp8:
+        from workloads import fp8_signs
+        q, k, v = (t.to(dev) for t in host_inputs)
+        signs_d = torch.from_numpy(fp8_signs(w.D, w.seed)).float().to(dev)
+        prep = fa.fp8_prepare(q, k, v, signs_d)  # inputs prepared once, as a KV cache would be
+
+        def step(o=None, lse=None):
+            return fa.fa_fwd_fp8(prep, w.B, w.Hq, w.Hkv, w.Lq, w.Lk, causal=w.causal, out=o, lse=lse)
+        out_shape, lse_shape = tuple(q.shape), (w.B, w.Hq, w.Lq)
     elif w.window is not None:
         q, k, v = (t.to(dev) for t in host_inputs)
 
@@ -453,6 +462,9 @@ def main(argv=None):
                           dv=dv_b, workspace=ws_b)
             elif w.window is not None:
                 fa.fa_fwd_variant(d_in[0], d_in[1], d_in[2], window=w.window, out=o, lse=lse)
+            elif w.fp8:  # bf16 inputs from the host, prepared and attended on the device
+                fa.fp8_prepare(d_in[0], d_in[1], d_in[2], signs_d, prepared=prep)
+                fa.fa_fwd_fp8(prep, w.B, w.Hq, w.Hkv, w.Lq, w.Lk, causal=w.causal, out=o, lse=lse)
             else:
                 fa.fa_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse)
             h_o.copy_(o, non_blocking=True)
@@ -495,6 +507,16 @@ def main(argv=None):
                     "kernel": ("fa_decode_tc_kernel" if w.D == 128 and w.Hq // w.Hkv * w.Lq >= 2
                                else "fa_decode_partial_kernel<%d,*>" % w.D) + " + fa_decode_merge_kernel<%d>" % w.D,
                     "timed": "whole step (both launches)"}
+    elif w.fp8:
+        # e4m3 tensor-core peak: the measured bf16 GEMM peak times the nominal
+        # fp8/bf16 ratio (4.5 / 2.25 dense PFLOP/s)
+        achieved = flops_step / (secs / args.steps) / 1e12
+        peak8 = peak * 2.0
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak8, "unit": "TFLOP/s",
+                    "frac": achieved / peak8, "traffic": None,
+                    "peak_kind": f"{peak_kind} burst bf16 GEMM x 2 (nominal e4m3/bf16 ratio)",
+                    "frac_of_bf16_peak": achieved / peak,
+                    "kernel": "fa_fwd_sm103_kernel<128,%s,false,4>" % str(w.causal).lower()}
     elif w.bwd:
         # both launches of the step (preprocess + gradient kernel) over the step's time
         achieved = flops_step / (secs / args.steps) / 1e12
@@ -520,7 +542,7 @@ def main(argv=None):
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "vs_baseline": None, "dtype": "e4m3" if w.fp8 else "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk,
                            "D": w.D, "causal": w.causal, "flops_per_step": flops_step,
                            "parallelism": f"replicas{world}" if world > 1 else "single", "l2": l2_note},

@@ -22,7 +22,7 @@ import threading
 import torch
 
 __all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
-           "fa_fwd_splitkv", "splitkv_workspace", "fa_bwd",
+           "fa_fwd_splitkv", "fp8_prepare", "fa_fwd_fp8", "fp8_sections", "splitkv_workspace", "fa_bwd",
            "bwd_workspace", "fa_check", "fa_status_string", "fa_last_launch_count",
            "FAError", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
@@ -33,7 +33,9 @@ _lib = None
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
-                    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace", "fa_bwd", "fa_bwd_workspace", "fa_check", "fa_status_string", "fa_last_launch_count", "fa_test_inject_fault")
+                    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace", "fa_bwd", "fa_bwd_workspace", "fa_fp8_workspace",
+                    "fa_fp8_prepare", "fa_fwd_fp8", "fa_check", "fa_status_string", "fa_last_launch_count",
+                    "fa_test_inject_fault")
 SPLITKV_MAX_ROWS = 16  # (Hq / Hkv) * Lq limit of fa_fwd_splitkv
 NOALLOC_MAX_SEQS = 16384  # FA_NOALLOC_MAX_SEQS in include/fa_gb300.h
 
@@ -81,6 +83,12 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd_variant.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vr, f, vp]
         lib.fa_fwd_varlen_variant.restype = i
         lib.fa_fwd_varlen_variant.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vr, f, vp]
+        lib.fa_fp8_workspace.restype = i
+        lib.fa_fp8_workspace.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_fp8_prepare.restype = i
+        lib.fa_fp8_prepare.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_fp8.restype = i
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
         lib.fa_bwd.restype = i
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
         lib.fa_bwd_workspace.restype = i
@@ -287,6 +295,67 @@ def fa_fwd_varlen_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_
                                        float(softmax_scale), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_varlen_variant")
+    return out, lse
+
+
+def fp8_sections(B: int, Hq: int, Hkv: int, Lq: int, Lk: int) -> dict:
+    """Byte offsets and shapes of the sections of a prepared FP8 buffer (the
+    layout documented with fa_fp8_prepare in include/fa_gb300.h)."""
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    nq, nk = (Lq + 127) // 128, (Lk + 127) // 128
+    lk_pad = nk * 128
+    sec, off = {}, 0
+    for name, nbytes, shape in (("qc", B * Hq * Lq * 128, (B, Hq, Lq, 128)), ("kc", B * Hkv * Lk * 128, (B, Hkv, Lk, 128)),
+                                ("vt", B * Hkv * 128 * lk_pad, (B, Hkv, 128, lk_pad)), ("sq", B * Hq * nq * 4, (B, Hq, nq)),
+                                ("sk", B * Hkv * nk * 4, (B, Hkv, nk)), ("sv", B * Hkv * 4, (B, Hkv)),
+                                ("vmax", B * Hkv * 4, (B, Hkv))):
+        sec[name] = (off, nbytes, shape)
+        off = up(off + nbytes)
+    sec["total"] = off
+    return sec
+
+
+def fp8_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, signs: torch.Tensor,
+                prepared: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Rotate and quantise bf16 q [B,Hq,Lq,128], k/v [B,Hkv,Lk,128] for
+    fa_fwd_fp8; signs: fp32 CUDA [128] of +-1.  Returns the prepared buffer
+    (a CUDA uint8 tensor)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, torch.bfloat16, 4)
+    _check_tensor(signs, "signs", torch.float32, 1)
+    B, Hq, Lq, D = q.shape
+    _, Hkv, Lk, _ = k.shape
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    st = lib.fa_fp8_workspace(B, Hq, Hkv, Lq, Lk, D, ctypes.byref(n))
+    if st != FA_OK:
+        raise FAError(st, "fa_fp8_workspace")
+    if prepared is None or prepared.numel() < n.value:
+        prepared = torch.empty(n.value, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib.fa_fp8_prepare(q.data_ptr(), k.data_ptr(), v.data_ptr(), signs.data_ptr(), B, Hq, Hkv, Lq, Lk, D,
+                                prepared.data_ptr(), prepared.numel(), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fp8_prepare")
+    return prepared
+
+
+def fa_fwd_fp8(prepared: torch.Tensor, B: int, Hq: int, Hkv: int, Lq: int, Lk: int, causal: bool = False,
+               softmax_scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+               D: int = 128, stream=None):
+    """Attention of a buffer made by fp8_prepare.  Returns (o fp32 [B,Hq,Lq,D], lse fp32 [B,Hq,Lq])."""
+    out = torch.empty((B, Hq, Lq, D), dtype=torch.float32, device=prepared.device) if out is None else out
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=prepared.device) if lse is None else lse
+    _check_tensor(out, "out", torch.float32, 4)
+    _check_tensor(lse, "lse", torch.float32, 3)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    with torch.cuda.device(prepared.device):
+        st = lib.fa_fwd_fp8(prepared.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Lq, Lk, D,
+                            int(bool(causal)), float(softmax_scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_fp8")
     return out, lse
 
 

@@ -11,6 +11,7 @@
 #include "../../include/fa_gb300.h"
 #include "fa_bwd.h"
 #include "fa_decode.h"
+#include "fa_fp8.h"
 #include "fa_launch.h"
 #include "fa_params.h"
 
@@ -719,6 +720,166 @@ extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const
     const int grid = (int)(items < ds->num_sms ? items : ds->num_sms);
     if (launch_bwd(D, causal != 0, mq, mk, mv, mdo, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 2;
+    return FA_OK;
+}
+
+// ------------------------------------------------------------- FP8 forward
+
+namespace {
+
+// Sections of a prepared FP8 buffer, each 256-byte aligned.
+struct Fp8Layout {
+    size_t qc, kc, vt, sq, sk, sv, vmax, total;
+    int nq, nk, lk_pad;
+};
+
+bool fp8_layout(int B, int Hq, int Hkv, int Lq, int Lk, Fp8Layout* l)
+{
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    l->nq = (Lq + kFp8Tile - 1) / kFp8Tile;
+    l->nk = (Lk + kFp8Tile - 1) / kFp8Tile;
+    l->lk_pad = l->nk * kFp8Tile;
+    size_t off = 0;
+    l->qc = off; off = up(off + (size_t)B * Hq * Lq * 128);
+    l->kc = off; off = up(off + (size_t)B * Hkv * Lk * 128);
+    l->vt = off; off = up(off + (size_t)B * Hkv * 128 * l->lk_pad);
+    l->sq = off; off = up(off + (size_t)B * Hq * l->nq * 4);
+    l->sk = off; off = up(off + (size_t)B * Hkv * l->nk * 4);
+    l->sv = off; off = up(off + (size_t)B * Hkv * 4);
+    l->vmax = off; off = up(off + (size_t)B * Hkv * 4);
+    l->total = off;
+    return true;
+}
+
+fa_status_t fp8_validate(int B, int Hq, int Hkv, int Lq, int Lk, int D)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (D != 128) return FA_ERR_UNSUPPORTED;
+    if ((long long)B * Hq * Lq >= (1ll << 31) || (long long)B * Hkv * (Lk + kFp8Tile) >= (1ll << 31))
+        return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+// 3-D e4m3 (byte) tensor map, 128-byte swizzle, box = {128, box1, 1}.
+bool encode_map_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+                   uint64_t stride2, uint32_t box1)
+{
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1, stride2};
+    const cuuint32_t box[3] = {128, box1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" fa_status_t fa_fp8_workspace(int B, int Hq, int Hkv, int Lq, int Lk, int D, size_t* bytes)
+{
+    if (!bytes) return FA_ERR_INVALID_ARG;
+    const fa_status_t st = fp8_validate(B, Hq, Hkv, Lq, Lk, D);
+    if (st != FA_OK) return st;
+    Fp8Layout l;
+    fp8_layout(B, Hq, Hkv, Lq, Lk, &l);
+    *bytes = l.total;
+    return FA_OK;
+}
+
+extern "C" fa_status_t fa_fp8_prepare(const void* q, const void* k, const void* v, const float* signs, int B,
+                                      int Hq, int Hkv, int Lq, int Lk, int D, void* prepared,
+                                      size_t prepared_bytes, cudaStream_t stream)
+{
+    g_last_launches = 0;
+    if (!q || !k || !v || !signs || !prepared) return FA_ERR_INVALID_ARG;
+    fa_status_t st = fp8_validate(B, Hq, Hkv, Lq, Lk, D);
+    if (st != FA_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(prepared) ||
+        (reinterpret_cast<uintptr_t>(signs) & 3u))
+        return FA_ERR_INVALID_ARG;
+    Fp8Layout l;
+    fp8_layout(B, Hq, Hkv, Lq, Lk, &l);
+    if (prepared_bytes < l.total) return FA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    st = device_state(&ds);
+    if (st != FA_OK) return st;
+    uint8_t* base = static_cast<uint8_t*>(prepared);
+    Fp8PrepParams p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.k = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.signs = signs;
+    p.qc = base + l.qc;
+    p.kc = base + l.kc;
+    p.vt = base + l.vt;
+    p.sq = reinterpret_cast<float*>(base + l.sq);
+    p.sk = reinterpret_cast<float*>(base + l.sk);
+    p.sv = reinterpret_cast<float*>(base + l.sv);
+    p.vmax = reinterpret_cast<unsigned*>(base + l.vmax);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lq = Lq;
+    p.Lk = Lk;
+    p.Lk_pad = l.lk_pad;
+    p.nq = l.nq;
+    p.nk = l.nk;
+    if (cudaMemsetAsync(p.vmax, 0, (size_t)B * Hkv * 4, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_fp8_prepare(p, stream) != cudaSuccess) return FA_ERR_CUDA;
+    g_last_launches = 3;
+    return FA_OK;
+}
+
+extern "C" fa_status_t fa_fwd_fp8(const void* prepared, float* o, float* lse, int B, int Hq, int Hkv, int Lq,
+                                  int Lk, int D, int causal, float softmax_scale, cudaStream_t stream)
+{
+    g_last_launches = 0;
+    if (!prepared || !o || !lse) return FA_ERR_INVALID_ARG;
+    fa_status_t st = fp8_validate(B, Hq, Hkv, Lq, Lk, D);
+    if (st != FA_OK) return st;
+    if (!scale_ok(softmax_scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(prepared) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+    const long long nmb = (Lq + kRowsPerCta - 1) / kRowsPerCta;
+    const long long tiles = (long long)B * Hq * nmb;
+    if (tiles >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    st = device_state(&ds);
+    if (st != FA_OK) return st;
+    Fp8Layout l;
+    fp8_layout(B, Hq, Hkv, Lq, Lk, &l);
+    const uint8_t* base = static_cast<const uint8_t*>(prepared);
+    CUtensorMap mq, mk, mv;
+    if (!encode_map_u8(&mq, base + l.qc, 128, Lq, (uint64_t)B * Hq, 128, 128ull * Lq, 128) ||
+        !encode_map_u8(&mk, base + l.kc, 128, Lk, (uint64_t)B * Hkv, 128, 128ull * Lk, 128) ||
+        !encode_map_u8(&mv, base + l.vt, l.lk_pad, 128, (uint64_t)B * Hkv, l.lk_pad, 128ull * l.lk_pad, 128))
+        return FA_ERR_CUDA;
+    FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lq = Lq;
+    p.Lk = Lk;
+    p.group = Hq / Hkv;
+    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+    p.heads_per_section = heads_per_section(Hkv, Lk, D / 2);  // e4m3 K/V: half the bytes of bf16
+    p.num_tiles = (int)tiles;
+    p.fp8_sq = reinterpret_cast<const float*>(base + l.sq);
+    p.fp8_sk = reinterpret_cast<const float*>(base + l.sk);
+    p.fp8_sv = reinterpret_cast<const float*>(base + l.sv);
+    p.fp8_nq = l.nq;
+    p.fp8_nk = l.nk;
+    p.err = ds->err;
+    p.diag = ds->diag;
+    p.fault = g_fault_next;
+    g_fault_next = 0;
+    const int grid = (int)(tiles < ds->num_sms ? tiles : ds->num_sms);
+    const cudaError_t e = causal ? launch_fwd<128, true, false, kVarFp8>(mq, mk, mv, p, grid, stream)
+                                 : launch_fwd<128, false, false, kVarFp8>(mq, mk, mv, p, grid, stream);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    g_last_launches = 1;
     return FA_OK;
 }
 

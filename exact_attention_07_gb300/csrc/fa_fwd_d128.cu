@@ -10,9 +10,9 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 {
     auto kern = fa_fwd_sm103_kernel<D, CAUSAL, VARLEN, VAR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FwdSmem<D>::kAlloc);
+                                         FwdSmem<D, VAR>::kAlloc);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, FwdSmem<D>::kAlloc, stream>>>(q, k, v, p);
+    kern<<<grid, kThreads, FwdSmem<D, VAR>::kAlloc, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 
@@ -20,7 +20,11 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
     template cudaError_t launch_fwd<D, C, V, VAR>(const CUtensorMap&, const CUtensorMap&,              \
                                                   const CUtensorMap&, const FwdParams&, int, cudaStream_t);
 
-#ifndef FA_VARIANTS
+#if defined(FA_FP8)
+// e4m3 inputs: D = 128, dense
+FA_INSTANCE(128, false, false, kVarFp8)
+FA_INSTANCE(128, true, false, kVarFp8)
+#elif !defined(FA_VARIANTS)
 #ifndef FA_HEAD_DIM
 #define FA_HEAD_DIM 128
 #endif

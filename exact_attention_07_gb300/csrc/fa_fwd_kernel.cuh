@@ -38,19 +38,23 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "fa_params.h"
 #include "ptx_sm103.cuh"
 
 namespace fa {
 
-template <int D>
+template <int D, int VAR = kVarNone>
 struct FwdSmem {
-    static constexpr int kTileBytes = kBlockN * D * 2;          // one 128 x D bf16 tile
-    static constexpr int kStages = (D == 128) ? 4 : 8;           // K/V ring depth
-    static constexpr int kQOff = 0;                              // Q0, Q1
+    static constexpr bool kFp8 = VAR == kVarFp8;
+    static constexpr int kTileBytes = kBlockN * D * (kFp8 ? 1 : 2);  // one 128 x D tile
+    static constexpr int kHalves = kTileBytes / (kBlockN * 128);     // 128-byte swizzle blocks per row
+    static constexpr int kStages = kTileBytes == 32768 ? 4 : 8;      // K/V ring depth
+    static constexpr int kQOff = 0;                                  // Q0, Q1
     static constexpr int kKVOff = 2 * kTileBytes;
-    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kPOff = kKVOff + kStages * kTileBytes;      // FP8: P0, P1 (e4m3, A of P.V)
+    static constexpr int kBarOff = kPOff + (kFp8 ? 2 * kTileBytes : 0);
     // barrier slots (8 bytes each)
     static constexpr int kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kStages;
     static constexpr int kSFull = 4 + 2 * kStages, kPFull = kSFull + 2, kOFull = kSFull + 4,
@@ -133,7 +137,7 @@ __device__ __forceinline__ Work decode_tile(const FwdParams& p, int t)
     w.kf = 0;
     if (w.lk <= 0) {
         w.nk = 0;
-    } else if (VAR != kVarNone) {
+    } else if (var_window(VAR)) {
         // key window [c - left, c + right] around each row's aligned position c
         const int off = w.lk - w.lq;
         const int last_row = min(w.m0 + kRowsPerCta - 1, w.lq - 1);
@@ -153,6 +157,32 @@ __device__ __forceinline__ Work decode_tile(const FwdParams& p, int t)
         w.nk = last_key < 0 ? 0 : last_key / kBlockN + 1;
     }
     return w;
+}
+
+// Two fp32 values to two e4m3 codes (round to nearest even, saturating), `lo`
+// in the low byte; and back to fp32.
+__device__ __forceinline__ uint16_t e4m3x2_pack(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float2 e4m3x2_unpack(uint16_t v)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    return __half22float2(*reinterpret_cast<__half2*>(&h2));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ float rcp_approx(float x)
@@ -185,43 +215,76 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // A descriptor advanced by a byte offset is the base descriptor plus
 // offset >> 4 (shared addresses stay below 256 KB, so the field never carries).
 
-// S_t = Q_t K^T: both operands K-major with 128-byte swizzle, 16 columns of D per MMA.
-template <int D>
+// MMA with both operands e4m3 in shared memory (kind::f8f6f4, 32 elements of K).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor, kind::f8f6f4 with e4m3 A/B (format code 0), fp32 D,
+// both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
+{
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// S_t = Q_t K^T: both operands K-major with 128-byte swizzle, 32 bytes of the
+// row (16 bf16 or 32 e4m3 elements) per MMA.
+template <int D, int VAR>
 __device__ __forceinline__ void mma_qk(uint32_t tmem, uint32_t sb, int t, int ks, bool leader)
 {
-    using L = FwdSmem<D>;
-    constexpr int kHalves = D / 64;
-    constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false);
+    using L = FwdSmem<D, VAR>;
+    constexpr int kSteps = L::kTileBytes / kBlockN / 32;
     const uint64_t qd = smem_desc_sw128(sb + L::kQOff + (uint32_t)(t * L::kTileBytes), 16, 1024);
     const uint64_t kd = smem_desc_sw128(sb + L::kKVOff + (uint32_t)(ks * L::kTileBytes), 16, 1024);
     const uint32_t d = tmem + L::kColS + (uint32_t)(t * kBlockN);
     if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = (uint64_t)(((kk >> 2) * (L::kTileBytes / kHalves) + (kk & 3) * 32) >> 4);
-            mma_ss(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kSteps; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * (L::kTileBytes / L::kHalves) + (kk & 3) * 32) >> 4);
+            if constexpr (L::kFp8)
+                mma_ss_f8(d, qd + off, kd + off, idesc_e4m3_f32(kBlockM, kBlockN), kk > 0 ? 1u : 0u);
+            else
+                mma_ss(d, qd + off, kd + off, idesc_bf16_f32(kBlockM, kBlockN, false), kk > 0 ? 1u : 0u);
         }
     }
     __syncwarp();
 }
 
-// O_t (+)= P_t V: P (bf16) from tensor memory, V MN-major with 128-byte swizzle,
-// 16 keys per MMA.
-template <int D>
+// O_t (+)= P_t V.  bf16: P from tensor memory, V MN-major with 128-byte
+// swizzle, 16 keys per MMA.  e4m3: P from shared memory (K-major) and V^T
+// (K-major, [d][key]), 32 keys per MMA.
+template <int D, int VAR>
 __device__ __forceinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs, bool acc, bool leader)
 {
-    using L = FwdSmem<D>;
-    constexpr int kHalves = D / 64;
-    constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
-    const uint64_t vd =
-        smem_desc_sw128(sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes), L::kTileBytes / kHalves, 1024);
+    using L = FwdSmem<D, VAR>;
     const uint32_t d = tmem + L::kColO + (uint32_t)(t * D);
-    const uint32_t pa = tmem + L::kColS + (uint32_t)(t * kBlockN);
-    if (leader) {
+    if constexpr (L::kFp8) {
+        const uint64_t pd = smem_desc_sw128(sb + L::kPOff + (uint32_t)(t * L::kTileBytes), 16, 1024);
+        const uint64_t vd = smem_desc_sw128(sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes), 16, 1024);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-            mma_ts(d, pa + (uint32_t)(kk * 8), vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
-                   (acc || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBlockN / 32; ++kk)
+                mma_ss_f8(d, pd + (uint64_t)((kk * 32) >> 4), vd + (uint64_t)((kk * 32) >> 4),
+                          idesc_e4m3_f32(kBlockM, D), (acc || kk > 0) ? 1u : 0u);
+        }
+    } else {
+        constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
+        const uint64_t vd = smem_desc_sw128(sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes),
+                                            L::kTileBytes / L::kHalves, 1024);
+        const uint32_t pa = tmem + L::kColS + (uint32_t)(t * kBlockN);
+        if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < kBlockN / 16; ++kk)
+                mma_ts(d, pa + (uint32_t)(kk * 8), vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                       (acc || kk > 0) ? 1u : 0u);
+        }
     }
     __syncwarp();
 }
@@ -231,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const FwdParams p)
 {
-    using L = FwdSmem<D>;
-    constexpr int kHalves = D / 64;  // 64-column (128-byte) swizzle blocks per row
+    using L = FwdSmem<D, VAR>;
+    constexpr int kHalves = L::kHalves;  // 128-byte swizzle blocks per row
     constexpr float kTau = 8.0f;     // rescale threshold, log2 units
     constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -303,15 +366,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             int kv_first = 0;        // first key this row may attend
             const int c_row = q_row + (w.lk - w.lq);  // the row's aligned position among the keys
             if (CAUSAL) kv_last = min(kv_last, c_row);
-            if constexpr (VAR != kVarNone) {
+            if constexpr (var_window(VAR)) {
                 if (p.win_right >= 0) kv_last = min(kv_last, c_row + p.win_right);
                 if (p.win_left >= 0) kv_first = max(0, c_row - p.win_left);
             }
             float alibi_l2 = 0.f;  // ALiBi slope of this head, log2 units
             if constexpr (VAR == kVarAlibi) alibi_l2 = __ldg(p.alibi + w.hq) * 1.4426950408889634f;
             // score multiplier inside the exponent: the score modifiers already
-            // produce log2-unit scores
-            const float smul = VAR >= kVarSoftcap ? 1.f : sl2;
+            // produce log2-unit scores; e4m3 scores carry the tiles' scales
+            constexpr bool kLog2Mod = VAR == kVarSoftcap || VAR == kVarAlibi;
+            float smul = kLog2Mod ? 1.f : sl2;
+            const float* fp8_sk = nullptr;
+            if constexpr (VAR == kVarFp8) {
+                smul = sl2 * __ldg(p.fp8_sq + ((long long)w.b * p.Hq + w.hq) * p.fp8_nq + (w.m0 + t * kBlockM) / kBlockM);
+                fp8_sk = p.fp8_sk + ((long long)w.b * p.Hkv + w.hkv) * p.fp8_nk + w.kf;
+            }
+            const float smul_q = smul;
             float r = -INFINITY, l = 0.f, l_rnd = 0.f;
             for (int j = 0; j < w.nk; ++j) {
                 if (!warp_wait(bar(L::kSFull + t), s_ph, abort_flag, wf, 1 + t, tile)) goto done;
@@ -322,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, sv[c]);
                 tmem_wait_ld();
                 const int key0 = (j + w.kf) * kBlockN;
+                if constexpr (VAR == kVarFp8) smul = smul_q * __ldg(fp8_sk + j);
                 // score modifiers (FlashAttention from Scratch, sec. 12), in log2 units
                 if constexpr (VAR == kVarSoftcap) {
                     // cap * tanh(s * scale / cap), tanh(u) = 1 - 2 / (1 + e^(2u))
@@ -395,14 +466,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float x0, x1;
                         f2_unpack(x2, x0, x1);
                         const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-                        pk[i] = pack_bf16x2(e0, e1);
                         sum_t[i & 1] = f2_add(sum_t[i & 1], f2_pack(e0, e1));
-                        sum_r[i & 1] = f2_add(sum_r[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
-                                                                    __uint_as_float(pk[i] & 0xffff0000u)));
+                        if constexpr (VAR == kVarFp8) {
+                            const uint16_t h = e4m3x2_pack(e0, e1);
+                            const float2 rf = e4m3x2_unpack(h);
+                            sum_r[i & 1] = f2_add(sum_r[i & 1], f2_pack(rf.x, rf.y));
+                            if (i & 1)
+                                pk[i >> 1] |= (uint32_t)h << 16;
+                            else
+                                pk[i >> 1] = h;
+                        } else {
+                            pk[i] = pack_bf16x2(e0, e1);
+                            sum_r[i & 1] = f2_add(sum_r[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
+                                                                        __uint_as_float(pk[i] & 0xffff0000u)));
+                        }
                     }
-                    // P (bf16 pairs) over the first 64 columns of S
-                    tmem_st32(tS + 32u * c, pk);
+                    if constexpr (VAR == kVarFp8) {
+                        // P (e4m3, keys 64c .. 64c+63 = 16-byte chunks 4c .. 4c+3 of the
+                        // row) into the P tile, 128-byte swizzle, for the SS P.V MMA
+                        const uint32_t prow = sb + L::kPOff + (uint32_t)(t * L::kTileBytes + row * 128);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            st_shared_v4(prow + (uint32_t)(((4 * c + u) ^ (row & 7)) << 4), pk[4 * u], pk[4 * u + 1],
+                                         pk[4 * u + 2], pk[4 * u + 3]);
+                    } else {
+                        // P (bf16 pairs) over the first 64 columns of S
+                        tmem_st32(tS + 32u * c, pk);
+                    }
                 }
+                if constexpr (VAR == kVarFp8) fence_proxy_async_shared();  // P visible to the tensor core
                 {
                     float a0, a1, b0, b1;
                     f2_unpack(f2_add(sum_t[0], sum_t[1]), a0, a1);
@@ -470,7 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st_ph[t] ^= 1;
                 const float4 st = stats[t * kBlockM + row];  // (sum of rounded p, sum of p, r)
                 mbar_arrive(bar(L::kStEmpty + t));
-                const float inv = st.x > 0.f ? 1.f / st.x : 0.f;
+                float inv = st.x > 0.f ? 1.f / st.x : 0.f;
+                if constexpr (VAR == kVarFp8) inv *= __ldg(p.fp8_sv + (long long)w.b * p.Hkv + w.hkv);
                 const float l = st.y;
                 const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * D);
 #pragma unroll 1
@@ -536,14 +629,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(bar(L::kKVFull + stage), L::kTileBytes);
                     kv_armed[stage] = (int)(kv_ph ^ 1u);
                     const uint32_t dst = sb + L::kKVOff + (uint32_t)(stage * L::kTileBytes);
+                    if (L::kFp8 && map == &tmV) {
+                        // e4m3 V is stored transposed, [d][key]: the tile is keys
+                        // (j+kf)*128 .. +127 of all 128 rows d
+                        tma_load_3d(dst, map, bar(L::kKVFull + stage), (j + w.kf) * kBlockN, 0, w.zk);
+                    } else {
 #pragma unroll
-                    for (int h = 0; h < kHalves; ++h) {
-                        if constexpr (VARLEN)
-                            tma_load_3d(dst + h * (L::kTileBytes / kHalves), map, bar(L::kKVFull + stage),
-                                        64 * h, w.hkv, w.zk + (j + w.kf) * kBlockN);
-                        else
-                            tma_load_3d(dst + h * (L::kTileBytes / kHalves), map, bar(L::kKVFull + stage),
-                                        64 * h, (j + w.kf) * kBlockN, w.zk);
+                        for (int h = 0; h < kHalves; ++h) {
+                            if constexpr (VARLEN)
+                                tma_load_3d(dst + h * (L::kTileBytes / kHalves), map, bar(L::kKVFull + stage),
+                                            64 * h, w.hkv, w.zk + (j + w.kf) * kBlockN);
+                            else
+                                tma_load_3d(dst + h * (L::kTileBytes / kHalves), map, bar(L::kKVFull + stage),
+                                            64 * h, (j + w.kf) * kBlockN, w.zk);
+                        }
                     }
                     if (++stage == L::kStages) {
                         stage = 0;
@@ -600,14 +699,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!warp_wait(bar(L::kKVFull + ks), kv_ph, abort_flag, wf, 17, tile)) break;
                 next_stage();
                 tc_fence_after_sync();
-                mma_qk<D>(tm, sb, 0, ks, leader);
+                mma_qk<D, VAR>(tm, sb, 0, ks, leader);
                 issued = true;
                 commit(L::kSFull + 0);
                 if (nk == 1) commit(L::kQEmpty + 0);
                 if (!warp_wait(bar(L::kQFull + 1), q_ph[1], abort_flag, wf, 16, tile)) break;
                 q_ph[1] ^= 1;
                 tc_fence_after_sync();
-                mma_qk<D>(tm, sb, 1, ks, leader);
+                mma_qk<D, VAR>(tm, sb, 1, ks, leader);
                 commit(L::kSFull + 1);
                 commit(L::kKVEmpty + ks);
                 if (nk == 1) commit(L::kQEmpty + 1);
@@ -632,9 +731,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = warp_wait(bar(L::kPFull + 0), p_ph[0], abort_flag, wf, 21, tile))) break;
                     p_ph[0] ^= 1;
                     tc_fence_after_sync();
-                    mma_pv<D>(tm, sb, 0, vs, j > 0, leader);
+                    mma_pv<D, VAR>(tm, sb, 0, vs, j > 0, leader);
                     if (kn >= 0) {
-                        mma_qk<D>(tm, sb, 0, kn, leader);
+                        mma_qk<D, VAR>(tm, sb, 0, kn, leader);
                         commit(L::kSFull + 0);
                         if (j + 2 == nk) commit(L::kQEmpty + 0);
                     } else {
@@ -648,10 +747,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = warp_wait(bar(L::kPFull + 1), p_ph[1], abort_flag, wf, 22, tile))) break;
                     p_ph[1] ^= 1;
                     tc_fence_after_sync();
-                    mma_pv<D>(tm, sb, 1, vs, j > 0, leader);
+                    mma_pv<D, VAR>(tm, sb, 1, vs, j > 0, leader);
                     commit(L::kKVEmpty + vs);
                     if (kn >= 0) {
-                        mma_qk<D>(tm, sb, 1, kn, leader);
+                        mma_qk<D, VAR>(tm, sb, 1, kn, leader);
                         commit(L::kSFull + 1);
                         commit(L::kKVEmpty + kn);
                         if (j + 2 == nk) commit(L::kQEmpty + 1);

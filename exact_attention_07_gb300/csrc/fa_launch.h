@@ -9,8 +9,6 @@
 
 namespace fa {
 
-// Dynamic shared memory the attention kernel needs for head dimension D.
-int fwd_smem_bytes(int D);
 
 template <int D, bool CAUSAL, bool VARLEN, int VAR = kVarNone>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,

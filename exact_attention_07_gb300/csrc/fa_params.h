@@ -25,6 +25,11 @@ struct FwdParams {
     float cap_in;             // soft-capping: scale / cap
     float cap_out;            // soft-capping: cap * log2(e)
     const float* alibi;       // ALiBi: per query head slope (natural-log units)
+    // FP8 forward (VAR = kVarFp8): dequantisation scales of the e4m3 inputs
+    const float* fp8_sq;      // [B*Hq][fp8_nq] per 128-row Q tile
+    const float* fp8_sk;      // [B*Hkv][fp8_nk] per 128-key K tile
+    const float* fp8_sv;      // [B*Hkv] per V slice
+    int fp8_nq, fp8_nk;
     // error reporting
     int* err;
     int* diag;
@@ -37,8 +42,10 @@ constexpr int kBlockN = 128;
 constexpr int kRowsPerCta = 2 * kBlockM;
 constexpr int kThreads = 512;
 
-// Score variants of the forward kernel (FlashAttention from Scratch, sec. 12):
-// 0 = plain, 1 = key window, 2 = key window + soft-capping, 3 = key window + ALiBi.
-enum : int { kVarNone = 0, kVarWindow = 1, kVarSoftcap = 2, kVarAlibi = 3 };
+// Variants of the forward kernel: 0 = plain, 1 = key window, 2 = key window +
+// soft-capping, 3 = key window + ALiBi (FlashAttention from Scratch, sec. 12),
+// 4 = e4m3 inputs with per-tile scales (sec. 10.3).
+enum : int { kVarNone = 0, kVarWindow = 1, kVarSoftcap = 2, kVarAlibi = 3, kVarFp8 = 4 };
+constexpr bool var_window(int v) { return v == kVarWindow || v == kVarSoftcap || v == kVarAlibi; }
 
 }  // namespace fa

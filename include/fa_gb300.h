@@ -166,6 +166,39 @@ fa_status_t fa_fwd_varlen_variant(const void* q, const void* k, const void* v, f
                                   float softmax_scale, cudaStream_t stream);
 
 /*
+ * FP8 forward (FlashAttention from Scratch, sec. 10.3 "Treat FP8 as a second
+ * lesson"; FlashAttention 1-4, FA3 item 3 "FP8 with block quantization and
+ * incoherent processing").  Two steps:
+ *
+ * fa_fp8_prepare: rotates Q and K by the same orthogonal matrix
+ *   M = diag(signs) H / sqrt(128) (H the Sylvester Hadamard matrix, applied as
+ *   a fast Walsh-Hadamard transform; (QM)(KM)^T = QK^T), then quantises each
+ *   128-row tile of every (batch, head) slice of QM and KM to e4m3 with scale
+ *   amax(tile) / 448.  V gets one scale per (batch, KV head) slice and is
+ *   stored transposed.  q, k, v: bf16 DEVICE, layouts as fa_fwd; signs: DEVICE
+ *   fp32 [128], each +1 or -1 (the caller draws them).  `prepared`: caller-owned
+ *   DEVICE buffer of fa_fp8_workspace bytes, 16-byte aligned.  3 kernels and a
+ *   memset on `stream`.
+ *
+ * fa_fwd_fp8: attention of the prepared inputs: S = (QM)(KM)^T from e4m3
+ *   operands on the tensor cores (kind::f8f6f4), fp32 online softmax, P
+ *   rounded to e4m3 for P.V, O = (P.V) * scale_v / sum(P) in fp32.  Same
+ *   output layouts, causal rule and empty-row convention as fa_fwd.  1 kernel.
+ *
+ * D must be 128 (FA_ERR_UNSUPPORTED otherwise).  The prepared buffer holds,
+ * each section 256-byte aligned: Q codes [B*Hq][Lq][128], K codes
+ * [B*Hkv][Lk][128], V codes [B*Hkv][128][Lk rounded up to 128], Q tile scales
+ * [B*Hq][ceil(Lq/128)], K tile scales [B*Hkv][ceil(Lk/128)], V scales
+ * [B*Hkv] (fp32), and 4 bytes per V slice of scratch.
+ */
+fa_status_t fa_fp8_workspace(int B, int Hq, int Hkv, int Lq, int Lk, int D, size_t* bytes);
+fa_status_t fa_fp8_prepare(const void* q, const void* k, const void* v, const float* signs,
+                           int B, int Hq, int Hkv, int Lq, int Lk, int D, void* prepared,
+                           size_t prepared_bytes, cudaStream_t stream);
+fa_status_t fa_fwd_fp8(const void* prepared, float* o, float* lse, int B, int Hq, int Hkv,
+                       int Lq, int Lk, int D, int causal, float softmax_scale, cudaStream_t stream);
+
+/*
  * Split-KV forward for decode (FlashAttention from Scratch, sec. 9.1 "Split
  * the long dimension that remains"; sec. 4.3 "Merge independently computed
  * partitions").  Same operation, layouts and causal rule as fa_fwd, for
@@ -259,7 +292,7 @@ int fa_last_launch_count(void);
 
 /*
  * Test hook (no counterpart on the pages).  kind = 1 makes the next fa_fwd
- * (or fa_fwd_splitkv or fa_bwd) call on this host thread drop the first K
+ * (or fa_fwd_splitkv, fa_bwd or fa_fwd_fp8) call on this host thread drop the first K
  * tile load (split-KV, backward: the first K/V tile) of every CTA: the bounded wait for it runs out (about 1 s), every thread of
  * the kernel retires, and fa_check then reports FA_ERR_TIMEOUT with the CUDA
  * context still usable.  kind = 0 clears a pending request.  Results of the faulted

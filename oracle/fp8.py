@@ -58,7 +58,8 @@ def rotation(signs) -> np.ndarray:
 
 def round_e4m3(x) -> np.ndarray:
     """Round to the nearest e4m3 value (ties to even) through PyTorch's
-    float8_e4m3fn conversion; |x| must not exceed 448."""
+    float8_e4m3fn conversion, after rounding to fp32 as the device does;
+    |x| must not exceed 448."""
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
     return t.to(torch.float8_e4m3fn).to(torch.float32).numpy().astype(np.float64)
 

@@ -144,3 +144,18 @@ def test_variant_argument_validation(lib):
     assert call(ctypes.byref(_Variant(-1, 0, 5.0, 16))) == UNS        # soft-capping with ALiBi
     assert lib.fa_fwd_varlen_variant(16, 16, 16, 16, 16, 32, 32, 1, 10, 10, 8, 8, 2, 2, 128, None, 0.1,
                                      None) == INV
+
+
+def test_fp8_argument_validation(lib):
+    INV, UNS = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+    n = ctypes.c_size_t(0)
+    assert lib.fa_fp8_workspace(1, 2, 1, 300, 200, 128, ctypes.byref(n)) == fa.FA_OK
+    sec = fa.fp8_sections(1, 2, 1, 300, 200)
+    assert n.value == sec["total"]
+    assert sec["vt"][2] == (1, 1, 128, 256)                       # keys padded to a multiple of 128
+    assert lib.fa_fp8_workspace(1, 2, 1, 300, 200, 64, ctypes.byref(n)) == UNS
+    assert lib.fa_fp8_workspace(1, 3, 2, 300, 200, 128, ctypes.byref(n)) == INV
+    assert lib.fa_fp8_prepare(16, 16, 16, 16, 1, 2, 1, 64, 64, 128, 16, 10, None) == INV   # buffer too small
+    assert lib.fa_fp8_prepare(16, 16, 16, 18, 1, 2, 1, 64, 64, 128, 16, 1 << 20, None) == INV  # signs misaligned
+    assert lib.fa_fwd_fp8(None, 16, 16, 1, 2, 1, 64, 64, 128, 0, 0.1, None) == INV
+    assert lib.fa_fwd_fp8(16, 16, 16, 1, 2, 1, 64, 64, 128, 0, -0.1, None) == INV

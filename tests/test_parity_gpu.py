@@ -130,7 +130,8 @@ def _dense_workload(name):
     return w, q, k, v, o, lse
 
 
-@pytest.mark.parametrize("name", [n for n, w in WORKLOADS.items() if not w.varlen])
+@pytest.mark.parametrize("name", [n for n, w in WORKLOADS.items()
+                                  if not (w.varlen or w.bwd or w.fp8 or w.window is not None)])
 def test_benchmark_workload_sampled(name):
     w, q, k, v, o, lse = _dense_workload(name)
     rows_per_slab = w.Lq

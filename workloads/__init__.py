@@ -47,6 +47,8 @@ class Workload:
     # key window (left, right) around each query's aligned position, run
     # through the variant forward (-1 = unlimited)
     window: tuple[int, int] | None = None
+    # the FP8 forward (e4m3 inputs after the Hadamard rotation)
+    fp8: bool = False
 
     @property
     def scale(self) -> float:
@@ -142,6 +144,14 @@ def grad_output(shape, seed: int):
     return _bf16(torch.randn(shape, generator=g, dtype=torch.float32))
 
 
+def fp8_signs(d: int, seed: int):
+    """The random +-1 signs of the FP8 rotation diag(signs) H / sqrt(d): a
+    seeded draw, passed to both the kernel and the oracle (float64 array)."""
+    import numpy as np
+    g = torch.Generator().manual_seed(seed + 2000)
+    return np.where(torch.rand(d, generator=g).numpy() < 0.5, -1.0, 1.0)
+
+
 _VARLEN_LENS = tuple(varlen_lengths(8, 512, 8192, seed=0))
 
 # The five workloads of the headline benchmark.  Names say what they are.
@@ -197,6 +207,12 @@ VARIANT_WORKLOADS: dict[str, Workload] = {
                                            window=(4095, 0)),
 }
 WORKLOADS.update(VARIANT_WORKLOADS)
+
+# The long-sequence shape through the FP8 forward (inputs prepared once).
+FP8_WORKLOADS: dict[str, Workload] = {
+    "fp8_b1_h16_l16384_d128": Workload("fp8_b1_h16_l16384_d128", 1, 16, 16, 16384, 16384, 128, False, fp8=True),
+}
+WORKLOADS.update(FP8_WORKLOADS)
 
 # The configuration the throughput metric is quoted on.
 HEADLINE = "b1_h16_l16384_d128"

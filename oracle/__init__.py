@@ -51,7 +51,7 @@ def _load():
             lib.oracle_attention_rows.argtypes = [
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, i64p, i64p, i64p,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_num_cpus.restype = ctypes.c_int
             _lib = lib
@@ -78,7 +78,7 @@ def _strides4(a: np.ndarray):
     return (ctypes.c_int64 * 3)(*(s // 4 for s in a.strides[:3]))
 
 
-def _run(qf, kf, vf, qs, ks, vs, B, Hq, Hkv, Lq, Lk, D, causal, scale, rows, nthreads):
+def _run(qf, kf, vf, qs, ks, vs, B, Hq, Hkv, Lq, Lk, D, Dv, causal, scale, rows, nthreads):
     lib = _load()
     if rows is None:
         n = B * Hq * Lq
@@ -87,12 +87,12 @@ def _run(qf, kf, vf, qs, ks, vs, B, Hq, Hkv, Lq, Lk, D, causal, scale, rows, nth
         rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         n = rows.size
         rows_ptr = rows.ctypes.data
-    o = np.empty((n, D), dtype=np.float64)
+    o = np.empty((n, Dv), dtype=np.float64)
     lse = np.empty((n,), dtype=np.float64)
     if n == 0:
         return o, lse
     rc = lib.oracle_attention_rows(qf.ctypes.data, kf.ctypes.data, vf.ctypes.data, qs, ks, vs,
-                                   B, Hq, Hkv, Lq, Lk, D, int(bool(causal)), float(scale),
+                                   B, Hq, Hkv, Lq, Lk, D, Dv, int(bool(causal)), float(scale),
                                    rows_ptr, n, o.ctypes.data, lse.ctypes.data, int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attention_rows failed with code {rc}")
@@ -100,41 +100,46 @@ def _run(qf, kf, vf, qs, ks, vs, B, Hq, Hkv, Lq, Lk, D, causal, scale, rows, nth
 
 
 def attention(q, k, v, scale: float, causal: bool = False, rows=None, nthreads: int = 0):
-    """Dense oracle.  q [B,Hq,Lq,D], k/v [B,Hkv,Lk,D] (bf16 or fp32).
+    """Dense oracle.  q [B,Hq,Lq,D], k [B,Hkv,Lk,D], v [B,Hkv,Lk,Dv] (bf16 or
+    fp32); Dv may differ from D.
 
-    Returns (o, lse) in fp64: o [B,Hq,Lq,D] and lse [B,Hq,Lq] when ``rows`` is
-    None, else o [n, D] and lse [n] for the flat row ids
+    Returns (o, lse) in fp64: o [B,Hq,Lq,Dv] and lse [B,Hq,Lq] when ``rows`` is
+    None, else o [n, Dv] and lse [n] for the flat row ids
     ``(b*Hq + h)*Lq + i`` in ``rows``.
     """
     qf, kf, vf = _as_f32(q), _as_f32(k), _as_f32(v)
     B, Hq, Lq, D = qf.shape
-    _, Hkv, Lk, _ = kf.shape
+    _, Hkv, Lk, Dk = kf.shape
+    Dv = vf.shape[3]
+    if Dk != D or vf.shape[:3] != kf.shape[:3]:
+        raise ValueError("shape mismatch between q, k and v")
     o, lse = _run(qf, kf, vf, _strides4(qf), _strides4(kf), _strides4(vf),
-                  B, Hq, Hkv, Lq, Lk, D, causal, scale, rows, nthreads)
+                  B, Hq, Hkv, Lq, Lk, D, Dv, causal, scale, rows, nthreads)
     if rows is None:
-        return o.reshape(B, Hq, Lq, D), lse.reshape(B, Hq, Lq)
+        return o.reshape(B, Hq, Lq, Dv), lse.reshape(B, Hq, Lq)
     return o, lse
 
 
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = False,
                      rows=None, nthreads: int = 0):
-    """Packed oracle.  q [Tq,Hq,D], k/v [Tk,Hkv,D]; sequence s spans tokens
+    """Packed oracle.  q [Tq,Hq,D], k [Tk,Hkv,D], v [Tk,Hkv,Dv]; sequence s spans tokens
     cu_seqlens[s]:cu_seqlens[s+1].  Causal masks are local to each sequence.
 
-    Returns o [Tq,Hq,D] and lse [Hq,Tq] (fp64) when ``rows`` is None, else
-    o [n,D] and lse [n] for flat ids ``h*Tq + t`` in ``rows``.
+    Returns o [Tq,Hq,Dv] and lse [Hq,Tq] (fp64) when ``rows`` is None, else
+    o [n,Dv] and lse [n] for flat ids ``h*Tq + t`` in ``rows``.
     """
     qf, kf, vf = _as_f32(q), _as_f32(k), _as_f32(v)
     Tq, Hq, D = qf.shape
     Hkv = kf.shape[1]
+    Dv = vf.shape[2]
     cq = [int(x) for x in np.asarray(cu_seqlens_q).tolist()]
     ck = [int(x) for x in np.asarray(cu_seqlens_k).tolist()]
     if rows is None:
-        o = np.zeros((Tq, Hq, D), dtype=np.float64)
+        o = np.zeros((Tq, Hq, Dv), dtype=np.float64)
         lse = np.full((Hq, Tq), -np.inf, dtype=np.float64)
     else:
         rows = np.asarray(rows, dtype=np.int64)
-        o = np.zeros((rows.size, D), dtype=np.float64)
+        o = np.zeros((rows.size, Dv), dtype=np.float64)
         lse = np.full((rows.size,), -np.inf, dtype=np.float64)
     for s in range(len(cq) - 1):
         q0, q1, k0, k1 = cq[s], cq[s + 1], ck[s], ck[s + 1]
@@ -149,9 +154,9 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
         vs = (ctypes.c_int64 * 3)(0, vf.strides[1] // 4, vf.strides[0] // 4)
         qv, kv, vv = qf[q0:q1], kf[k0:k1], vf[k0:k1]
         if rows is None:
-            os_, ls_ = _run(qv, kv, vv, qs, ks, vs, 1, Hq, Hkv, Lq, Lk, D, causal, scale,
+            os_, ls_ = _run(qv, kv, vv, qs, ks, vs, 1, Hq, Hkv, Lq, Lk, D, Dv, causal, scale,
                             None, nthreads)
-            o[q0:q1] = os_.reshape(Hq, Lq, D).transpose(1, 0, 2)
+            o[q0:q1] = os_.reshape(Hq, Lq, Dv).transpose(1, 0, 2)
             lse[:, q0:q1] = ls_.reshape(Hq, Lq)
         else:
             h = rows // Tq
@@ -160,7 +165,7 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
             if sel.size == 0:
                 continue
             local = h[sel] * Lq + (t[sel] - q0)
-            os_, ls_ = _run(qv, kv, vv, qs, ks, vs, 1, Hq, Hkv, Lq, Lk, D, causal, scale,
+            os_, ls_ = _run(qv, kv, vv, qs, ks, vs, 1, Hq, Hkv, Lq, Lk, D, Dv, causal, scale,
                             local, nthreads)
             o[sel] = os_
             lse[sel] = ls_

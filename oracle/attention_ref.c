@@ -25,6 +25,10 @@
  * GQA: query head h reads KV head h / (Hq / Hkv)
  * (sec. 9.2 "GQA and MQA change decode traffic").
  *
+ * Queries and keys have D elements per row, values and outputs Dv; the two
+ * differ in the (192, 128) case of the FlashAttention-4 benchmarks
+ * (FlashAttention-4: Blackwell Attention Kernel Co-Design, "How we know").
+ *
  * Inputs are fp32 arrays holding exact bf16 values; every product and sum is
  * done in double.  Element (b, h, i, d) of a tensor X lives at
  * X + b*xs[0] + h*xs[1] + i*xs[2] + d, so the same routine reads the dense
@@ -40,12 +44,12 @@
 typedef struct {
     const float *q, *k, *v;
     int64_t qs[3], ks[3], vs[3];
-    int B, Hq, Hkv, Lq, Lk, D;
+    int B, Hq, Hkv, Lq, Lk, D, Dv;
     int causal;
     double scale;
     const int64_t *rows; /* flat row ids (b*Hq + h)*Lq + i, or NULL = all */
     int64_t nrows;
-    double *o;   /* nrows x D */
+    double *o;   /* nrows x Dv */
     double *lse; /* nrows */
     int64_t begin, end;
     int status;
@@ -79,7 +83,7 @@ static void one_row(const job_t *J, int64_t flat, double *S, double *P, double *
     for (int64_t j = 0; j < J->Lk; ++j)
         if (S[j] > m) m = S[j];
     if (m == -INFINITY) { /* every key masked */
-        for (int d = 0; d < J->D; ++d) o[d] = 0.0;
+        for (int d = 0; d < J->Dv; ++d) o[d] = 0.0;
         *lse = -INFINITY;
         return;
     }
@@ -91,11 +95,11 @@ static void one_row(const job_t *J, int64_t flat, double *S, double *P, double *
     }
     for (int64_t j = 0; j < J->Lk; ++j) P[j] /= l;
     /* o = P V */
-    for (int d = 0; d < J->D; ++d) o[d] = 0.0;
+    for (int d = 0; d < J->Dv; ++d) o[d] = 0.0;
     for (int64_t j = 0; j < J->Lk; ++j) {
         if (P[j] == 0.0) continue; /* masked key: its term is exactly zero */
         const float *vrow = vb + j * J->vs[2];
-        for (int d = 0; d < J->D; ++d) o[d] += P[j] * (double)vrow[d];
+        for (int d = 0; d < J->Dv; ++d) o[d] += P[j] * (double)vrow[d];
     }
     *lse = m + log(l);
 }
@@ -113,7 +117,7 @@ static void *worker(void *arg)
     }
     for (int64_t r = J->begin; r < J->end; ++r) {
         const int64_t flat = J->rows ? J->rows[r] : r;
-        one_row(J, flat, S, P, J->o + r * J->D, J->lse + r);
+        one_row(J, flat, S, P, J->o + r * J->Dv, J->lse + r);
     }
     free(S);
     free(P);
@@ -128,17 +132,17 @@ int oracle_num_cpus(void)
 
 /*
  * Computes nrows output rows (all B*Hq*Lq rows when rows == NULL) into
- * o[nrows][D] and lse[nrows].  Returns 0 on success, nonzero on bad
+ * o[nrows][Dv] and lse[nrows].  Returns 0 on success, nonzero on bad
  * arguments or allocation failure.  nthreads <= 0 uses every online CPU.
  */
 int oracle_attention_rows(const float *q, const float *k, const float *v,
                           const int64_t *q_strides, const int64_t *k_strides,
                           const int64_t *v_strides, int B, int Hq, int Hkv, int Lq,
-                          int Lk, int D, int causal, double scale, const int64_t *rows,
+                          int Lk, int D, int Dv, int causal, double scale, const int64_t *rows,
                           int64_t nrows, double *o, double *lse, int nthreads)
 {
     if (!q || !k || !v || !o || !lse || B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 ||
-        Lk <= 0 || D <= 0 || Hq % Hkv != 0)
+        Lk <= 0 || D <= 0 || Dv <= 0 || Hq % Hkv != 0)
         return 2;
     if (!rows) nrows = (int64_t)B * Hq * Lq;
     if (nrows <= 0) return 0;
@@ -159,6 +163,7 @@ int oracle_attention_rows(const float *q, const float *k, const float *v,
     base.Lq = Lq;
     base.Lk = Lk;
     base.D = D;
+    base.Dv = Dv;
     base.causal = causal;
     base.scale = scale;
     base.rows = rows;

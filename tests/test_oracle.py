@@ -182,8 +182,9 @@ def brute_force_mp(q, k, v, scale, causal, dps=40):
     mpmath.mp.dps = dps
     B, Hq, Lq, D = q.shape
     _, Hkv, Lk, _ = k.shape
+    Dv = v.shape[3]
     r = Hq // Hkv
-    O = np.zeros((B, Hq, Lq, D))
+    O = np.zeros((B, Hq, Lq, Dv))
     L = np.zeros((B, Hq, Lq))
     for b in range(B):
         for h in range(Hq):
@@ -200,7 +201,7 @@ def brute_force_mp(q, k, v, scale, causal, dps=40):
                     L[b, h, i] = -np.inf
                     continue
                 z = mpmath.fsum(mpmath.e ** s for _, s in w)
-                for d in range(D):
+                for d in range(Dv):
                     O[b, h, i, d] = float(mpmath.fsum(mpmath.e ** s * mpmath.mpf(float(v[b, hk, j, d]))
                                                       for j, s in w) / z)
                 L[b, h, i] = float(mpmath.log(z))
@@ -222,6 +223,29 @@ def test_c_oracle_against_mpmath_brute_force(Lq, Lk, causal):
     assert np.all(lse[~fin] == -np.inf) and np.all(o[~fin] == 0.0)
     if causal and Lq > Lk:
         assert (~fin).sum() == B * Hq * (Lq - Lk)  # rows i < Lq - Lk see no key
+
+
+@pytest.mark.parametrize("D,Dv,causal", [(3, 5, False), (6, 2, True)])
+def test_c_oracle_value_width_against_mpmath(D, Dv, causal):
+    # values (and outputs) with Dv elements per row while queries and keys
+    # have D, as in the (192, 128) head-dimension case
+    B, Hq, Hkv, Lq, Lk = 1, 4, 2, 6, 9
+    q, k, v = random_inputs((B, Hq, Lq, D), (B, Hkv, Lk, D), seed=31 + D, shape_v=(B, Hkv, Lk, Dv))
+    o, lse = oracle.attention(q, k, v, scale=0.6, causal=causal)
+    assert o.shape == (B, Hq, Lq, Dv)
+    O, L = brute_force_mp(q.float().numpy(), k.float().numpy(), v.float().numpy(), 0.6, causal)
+    assert np.max(np.abs(o - O)) < 1e-13 and np.max(np.abs(lse - L)) < 1e-13
+
+
+def test_value_columns_are_independent():
+    # every output column uses only its own value column, and the normaliser
+    # does not involve V at all: splitting V by columns splits O exactly and
+    # leaves the LSE unchanged
+    q, k, v = random_inputs((2, 4, 21, 12), (2, 2, 30, 12), seed=4, shape_v=(2, 2, 30, 8))
+    o, lse = oracle.attention(q, k, v, scale=0.3, causal=True)
+    for a, b in ((0, 3), (3, 8)):
+        o2, lse2 = oracle.attention(q, k, v[..., a:b].contiguous(), scale=0.3, causal=True)
+        assert np.array_equal(o2, o[..., a:b]) and np.array_equal(lse2, lse)
 
 
 # ------------------------------------------------------------------ reductions

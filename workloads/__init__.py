@@ -128,12 +128,13 @@ def varlen_inputs(w: Workload):
     return _bf16(q), _bf16(k), _bf16(v), cu, cu.clone()
 
 
-def random_inputs(shape_q, shape_k, seed: int, q_mult: float = 1.0):
-    """Generic seeded bf16 triple for edge-case tests with arbitrary shapes."""
+def random_inputs(shape_q, shape_k, seed: int, q_mult: float = 1.0, shape_v=None):
+    """Generic seeded bf16 triple for edge-case tests with arbitrary shapes;
+    V has shape ``shape_v`` (default: the shape of K)."""
     g = torch.Generator().manual_seed(seed)
     q = torch.randn(shape_q, generator=g, dtype=torch.float32) * q_mult
     k = torch.randn(shape_k, generator=g, dtype=torch.float32)
-    v = torch.randn(shape_k, generator=g, dtype=torch.float32)
+    v = torch.randn(shape_k if shape_v is None else shape_v, generator=g, dtype=torch.float32)
     return _bf16(q), _bf16(k), _bf16(v)
 
 

@@ -312,7 +312,7 @@ def run_reference(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk, "D": w.D,
-                       "causal": w.causal},
+                       "Dv": w.Dv, "causal": w.causal},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": f"per step: {desc}"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -387,6 +387,12 @@ def main(argv=None):
         def step(o=None, lse=None, qq=q, kk=k, vv=v):
             return fa.fa_fwd_splitkv(qq, kk, vv, causal=w.causal, out=o, lse=lse, workspace=ws)
         out_shape, lse_shape = tuple(q.shape), (w.B, w.Hq, w.Lq)
+    elif w.Dv != w.D:
+        q, k, v = (t.to(dev) for t in host_inputs)
+
+        def step(o=None, lse=None, qq=q, kk=k, vv=v):
+            return fa.fa_fwd_hdim(qq, kk, vv, causal=w.causal, out=o, lse=lse)
+        out_shape, lse_shape = (w.B, w.Hq, w.Lq, w.Dv), (w.B, w.Hq, w.Lq)
     else:
         q, k, v = (t.to(dev) for t in host_inputs)
 
@@ -465,6 +471,8 @@ def main(argv=None):
             elif w.fp8:  # bf16 inputs from the host, prepared and attended on the device
                 fa.fp8_prepare(d_in[0], d_in[1], d_in[2], signs_d, prepared=prep)
                 fa.fa_fwd_fp8(prep, w.B, w.Hq, w.Hkv, w.Lq, w.Lk, causal=w.causal, out=o, lse=lse)
+            elif w.Dv != w.D:
+                fa.fa_fwd_hdim(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse)
             else:
                 fa.fa_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse)
             h_o.copy_(o, non_blocking=True)
@@ -530,9 +538,9 @@ def main(argv=None):
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                     "peak_kind": f"{peak_kind} burst bf16 GEMM", "frac_of_sustained": achieved / peak_sus,
-                    "kernel": "fa_fwd_sm103_kernel<%d,%s,%s,%d>" % (w.D, str(w.causal).lower(),
-                                                                   str(w.varlen).lower(),
-                                                                   1 if w.window is not None else 0)}
+                    "kernel": "fa_fwd_sm103_kernel<%d,%s,%s,%d,%d>" % (w.D, str(w.causal).lower(),
+                                                                      str(w.varlen).lower(),
+                                                                      1 if w.window is not None else 0, w.Dv)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -544,7 +552,7 @@ def main(argv=None):
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "e4m3" if w.fp8 else "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk,
-                           "D": w.D, "causal": w.causal, "flops_per_step": flops_step,
+                           "D": w.D, "Dv": w.Dv, "causal": w.causal, "flops_per_step": flops_step,
                            "parallelism": f"replicas{world}" if world > 1 else "single", "l2": l2_note},
                 "frac_of_peak": value / world / peak,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

@@ -21,7 +21,7 @@ import threading
 
 import torch
 
-__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
+__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_hdim", "fa_fwd_varlen_hdim", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
            "fa_fwd_splitkv", "fp8_prepare", "fa_fwd_fp8", "fp8_sections", "splitkv_workspace", "fa_bwd",
            "bwd_workspace", "fa_check", "fa_status_string", "fa_last_launch_count",
            "FAError", "library_path", "load_library", "EXPORTED_SYMBOLS"]
@@ -32,7 +32,7 @@ _lock = threading.Lock()
 _lib = None
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_hdim", "fa_fwd_varlen_hdim", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
                     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace", "fa_bwd", "fa_bwd_workspace", "fa_fp8_workspace",
                     "fa_fp8_prepare", "fa_fwd_fp8", "fa_check", "fa_status_string", "fa_last_launch_count",
                     "fa_test_inject_fault")
@@ -71,6 +71,10 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
         lib.fa_fwd_varlen.restype = i
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
+        lib.fa_fwd_hdim.restype = i
+        lib.fa_fwd_hdim.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
+        lib.fa_fwd_varlen_hdim.restype = i
+        lib.fa_fwd_varlen_hdim.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, i, f, vp]
         lib.fa_fwd_varlen_noalloc.restype = i
         lib.fa_fwd_varlen_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
         lib.fa_fwd_splitkv.restype = i
@@ -197,6 +201,79 @@ def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_
                                float(softmax_scale), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_varlen")
+    return out, lse
+
+
+def fa_fwd_hdim(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                softmax_scale: float | None = None, out: torch.Tensor | None = None,
+                lse: torch.Tensor | None = None, stream=None):
+    """Dense forward whose value head dimension Dv may differ from the
+    query/key one D.  q [B,Hq,Lq,D], k [B,Hkv,Lk,D], v [B,Hkv,Lk,Dv] bf16 CUDA;
+    (D, Dv) in {(64, 64), (128, 128), (192, 128)}.
+
+    Returns (o [B,Hq,Lq,Dv] fp32, lse [B,Hq,Lq] fp32).  The default scale is
+    1/sqrt(D).
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, torch.bfloat16, 4)
+    B, Hq, Lq, D = q.shape
+    Bk, Hkv, Lk, Dk = k.shape
+    Dv = v.shape[3]
+    if tuple(v.shape[:3]) != tuple(k.shape[:3]) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if out is None:
+        out = torch.empty((B, Hq, Lq, Dv), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    _check_tensor(out, "out", torch.float32, 4)
+    _check_tensor(lse, "lse", torch.float32, 3)
+    if tuple(out.shape) != (B, Hq, Lq, Dv) or tuple(lse.shape) != (B, Hq, Lq):
+        raise ValueError("out/lse shape mismatch")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_hdim(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                             B, Hq, Hkv, Lq, Lk, D, Dv, int(bool(causal)), float(softmax_scale),
+                             _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_hdim")
+    return out, lse
+
+
+def fa_fwd_varlen_hdim(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                       cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, causal: bool = False,
+                       softmax_scale: float | None = None, out: torch.Tensor | None = None,
+                       lse: torch.Tensor | None = None, stream=None):
+    """Packed forward with value head dimension Dv: q [Tq,Hq,D], k [Tk,Hkv,D],
+    v [Tk,Hkv,Dv] bf16 CUDA.  Returns (o [Tq,Hq,Dv] fp32, lse [Hq,Tq] fp32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, torch.bfloat16, 3)
+    _check_tensor(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check_tensor(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    Tq, Hq, D = q.shape
+    Tk, Hkv, Dk = k.shape
+    Dv = v.shape[2]
+    if tuple(v.shape[:2]) != (Tk, Hkv) or Dk != D or cu_seqlens_q.numel() != cu_seqlens_k.numel():
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((Tq, Hq, Dv), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    _check_tensor(out, "out", torch.float32, 3)
+    _check_tensor(lse, "lse", torch.float32, 2)
+    if tuple(out.shape) != (Tq, Hq, Dv) or tuple(lse.shape) != (Hq, Tq):
+        raise ValueError("out/lse shape mismatch")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_varlen_hdim(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                    cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), cu_seqlens_q.numel() - 1,
+                                    Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, Dv,
+                                    int(bool(causal)), float(softmax_scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_varlen_hdim")
     return out, lse
 
 

@@ -95,9 +95,10 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int heads_per_section(int Hkv, long long Lk, int D)
+// D_kv = the K and V elements of one key (D + Dv)
+int heads_per_section(int Hkv, long long Lk, int D_kv)
 {
-    const long long kv_bytes = 2ll * Lk * D * 2;  // K and V of one KV head
+    const long long kv_bytes = Lk * D_kv * 2;  // K and V of one KV head
     long long hs = kv_bytes > 0 ? kL2SectionBytes / kv_bytes : Hkv;
     if (hs < 1) hs = 1;
     if (hs > Hkv) hs = Hkv;
@@ -133,10 +134,14 @@ int prepare_variant(const fa_variant_t* var, int D, float scale, FwdParams* p)
     return var->alibi_slopes ? kVarAlibi : kVarWindow;
 }
 
+// (D, Dv) must satisfy hdim_supported()
 template <bool VARLEN>
 cudaError_t dispatch(int D, bool causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                      const FwdParams& p, int grid, cudaStream_t st)
 {
+    if (D == 192)
+        return causal ? launch_fwd<192, true, VARLEN, kVarNone, 128>(q, k, v, p, grid, st)
+                      : launch_fwd<192, false, VARLEN, kVarNone, 128>(q, k, v, p, grid, st);
     if (D == 64)
         return causal ? launch_fwd<64, true, VARLEN>(q, k, v, p, grid, st)
                       : launch_fwd<64, false, VARLEN>(q, k, v, p, grid, st);
@@ -145,6 +150,9 @@ cudaError_t dispatch(int D, bool causal, const CUtensorMap& q, const CUtensorMap
 }
 
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+// Head dimensions with a kernel: (64, 64), (128, 128) and (192, 128).
+bool hdim_supported(int D, int Dv) { return (D == Dv && (D == 64 || D == 128)) || (D == 192 && Dv == 128); }
 
 }  // namespace
 
@@ -236,16 +244,16 @@ using namespace fa;
 
 namespace {
 fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq, int Hkv,
-                      int Lq, int Lk, int D, int causal, const fa_variant_t* variant, float softmax_scale,
+                      int Lq, int Lk, int D, int Dv, int causal, const fa_variant_t* variant, float softmax_scale,
                       cudaStream_t stream)
 {
     g_last_launches = 0;
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || D <= 0 || Dv <= 0) return FA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0 || !scale_ok(softmax_scale)) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!hdim_supported(D, Dv)) return FA_ERR_UNSUPPORTED;
     const long long nmb = (Lq + kRowsPerCta - 1) / kRowsPerCta;
     const long long tiles = (long long)B * Hq * nmb;
     if (tiles >= (1ll << 31) || (long long)B * Hq >= (1ll << 31) || (long long)B * Hkv >= (1ll << 31))
@@ -261,10 +269,10 @@ fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, flo
     if (st != FA_OK) return st;
 
     CUtensorMap mq, mk, mv;
-    const uint64_t row = (uint64_t)D * 2;
+    const uint64_t row = (uint64_t)D * 2, vrow = (uint64_t)Dv * 2;
     if (!encode_map(&mq, q, D, Lq, (uint64_t)B * Hq, row, row * Lq, 128, 1) ||
         !encode_map(&mk, k, D, Lk, (uint64_t)B * Hkv, row, row * Lk, 128, 1) ||
-        !encode_map(&mv, v, D, Lk, (uint64_t)B * Hkv, row, row * Lk, 128, 1))
+        !encode_map(&mv, v, Dv, Lk, (uint64_t)B * Hkv, vrow, vrow * Lk, 128, 1))
         return FA_ERR_CUDA;
 
     p.o = o;
@@ -276,7 +284,7 @@ fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, flo
     p.Lk = Lk;
     p.group = Hq / Hkv;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
-    p.heads_per_section = heads_per_section(Hkv, Lk, D);
+    p.heads_per_section = heads_per_section(Hkv, Lk, D + Dv);
     p.num_tiles = (int)tiles;
     p.err = ds->err;
     p.diag = ds->diag;
@@ -295,7 +303,14 @@ extern "C" fa_status_t fa_fwd(const void* q, const void* k, const void* v, float
                               int Hkv, int Lq, int Lk, int D, int causal, float softmax_scale,
                               cudaStream_t stream)
 {
-    return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, causal, nullptr, softmax_scale, stream);
+    return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, D, causal, nullptr, softmax_scale, stream);
+}
+
+extern "C" fa_status_t fa_fwd_hdim(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                                   int Hq, int Hkv, int Lq, int Lk, int D, int Dv, int causal,
+                                   float softmax_scale, cudaStream_t stream)
+{
+    return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, Dv, causal, nullptr, softmax_scale, stream);
 }
 
 extern "C" fa_status_t fa_fwd_variant(const void* q, const void* k, const void* v, float* o, float* lse, int B,
@@ -303,25 +318,25 @@ extern "C" fa_status_t fa_fwd_variant(const void* q, const void* k, const void* 
                                       float softmax_scale, cudaStream_t stream)
 {
     if (!variant) return FA_ERR_INVALID_ARG;
-    return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, 0, variant, softmax_scale, stream);
+    return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, D, 0, variant, softmax_scale, stream);
 }
 
 namespace {
 fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse, const int* cu_seqlens_q,
                        const int* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
-                       int max_seqlen_k, int Hq, int Hkv, int D, int causal, const fa_variant_t* variant,
+                       int max_seqlen_k, int Hq, int Hkv, int D, int Dv, int causal, const fa_variant_t* variant,
                        float softmax_scale, cudaStream_t stream)
 {
     g_last_launches = 0;
     if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
     if (num_seqs <= 0 || total_q <= 0 || total_k <= 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 || Hq <= 0 ||
-        Hkv <= 0 || D <= 0)
+        Hkv <= 0 || D <= 0 || Dv <= 0)
         return FA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0 || !scale_ok(softmax_scale)) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
         (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
         return FA_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!hdim_supported(D, Dv)) return FA_ERR_UNSUPPORTED;
     // upper bound of the work tiles: sum_s ceil(Lq_s / 256) <= total_q / 256 + num_seqs
     long long ub = (long long)Hq * ((long long)total_q / kRowsPerCta + num_seqs);
     const long long ub2 = (long long)Hq * num_seqs * ((max_seqlen_q + kRowsPerCta - 1) / kRowsPerCta);
@@ -340,10 +355,10 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
     if (st != FA_OK) return st;
 
     CUtensorMap mq, mk, mv;
-    const uint64_t row = (uint64_t)D * 2;
+    const uint64_t row = (uint64_t)D * 2, vrow = (uint64_t)Dv * 2;
     if (!encode_map(&mq, q, D, Hq, total_q, row, row * Hq, 1, 128) ||
         !encode_map(&mk, k, D, Hkv, total_k, row, row * Hkv, 1, 128) ||
-        !encode_map(&mv, v, D, Hkv, total_k, row, row * Hkv, 1, 128))
+        !encode_map(&mv, v, Dv, Hkv, total_k, vrow, vrow * Hkv, 1, 128))
         return FA_ERR_CUDA;
 
     int* sched = nullptr;
@@ -360,7 +375,7 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
     p.Hkv = Hkv;
     p.group = Hq / Hkv;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
-    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, D);
+    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, D + Dv);
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
     p.sched = sched;
@@ -384,7 +399,17 @@ extern "C" fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v
                                      int Hkv, int D, int causal, float softmax_scale, cudaStream_t stream)
 {
     return fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
-                      max_seqlen_k, Hq, Hkv, D, causal, nullptr, softmax_scale, stream);
+                      max_seqlen_k, Hq, Hkv, D, D, causal, nullptr, softmax_scale, stream);
+}
+
+extern "C" fa_status_t fa_fwd_varlen_hdim(const void* q, const void* k, const void* v, float* o, float* lse,
+                                          const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                                          int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int Hq,
+                                          int Hkv, int D, int Dv, int causal, float softmax_scale,
+                                          cudaStream_t stream)
+{
+    return fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                      max_seqlen_k, Hq, Hkv, D, Dv, causal, nullptr, softmax_scale, stream);
 }
 
 extern "C" fa_status_t fa_fwd_varlen_variant(const void* q, const void* k, const void* v, float* o, float* lse,
@@ -395,7 +420,7 @@ extern "C" fa_status_t fa_fwd_varlen_variant(const void* q, const void* k, const
 {
     if (!variant) return FA_ERR_INVALID_ARG;
     return fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
-                      max_seqlen_k, Hq, Hkv, D, 0, variant, softmax_scale, stream);
+                      max_seqlen_k, Hq, Hkv, D, D, 0, variant, softmax_scale, stream);
 }
 
 // ------------------------------------------------------------- allocation-free varlen
@@ -475,7 +500,7 @@ extern "C" fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const
     p.Hkv = Hkv;
     p.group = Hq / Hkv;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
-    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, D);
+    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, 2 * D);
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
     p.sched = sched;

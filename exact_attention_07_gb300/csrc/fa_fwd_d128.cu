@@ -4,23 +4,30 @@
 
 namespace fa {
 
-template <int D, bool CAUSAL, bool VARLEN, int VAR>
+template <int D, bool CAUSAL, bool VARLEN, int VAR, int DV>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const FwdParams& p, int grid, cudaStream_t stream)
 {
-    auto kern = fa_fwd_sm103_kernel<D, CAUSAL, VARLEN, VAR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FwdSmem<D, VAR>::kAlloc);
+    auto kern = fa_fwd_sm103_kernel<D, CAUSAL, VARLEN, VAR, DV>;
+    constexpr int kSmem = FwdSmem<D, VAR, DV>::kAlloc;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, FwdSmem<D, VAR>::kAlloc, stream>>>(q, k, v, p);
+    kern<<<grid, kThreads, kSmem, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 
-#define FA_INSTANCE(D, C, V, VAR)                                                                        \
-    template cudaError_t launch_fwd<D, C, V, VAR>(const CUtensorMap&, const CUtensorMap&,              \
-                                                  const CUtensorMap&, const FwdParams&, int, cudaStream_t);
+#define FA_INSTANCE_DV(D, C, V, VAR, DV)                                                                 \
+    template cudaError_t launch_fwd<D, C, V, VAR, DV>(const CUtensorMap&, const CUtensorMap&,          \
+                                                      const CUtensorMap&, const FwdParams&, int, cudaStream_t);
+#define FA_INSTANCE(D, C, V, VAR) FA_INSTANCE_DV(D, C, V, VAR, D)
 
-#if defined(FA_FP8)
+#if defined(FA_D192)
+// query/key head dimension 192, value head dimension 128
+FA_INSTANCE_DV(192, false, false, kVarNone, 128)
+FA_INSTANCE_DV(192, true, false, kVarNone, 128)
+FA_INSTANCE_DV(192, false, true, kVarNone, 128)
+FA_INSTANCE_DV(192, true, true, kVarNone, 128)
+#elif defined(FA_FP8)
 // e4m3 inputs: D = 128, dense
 FA_INSTANCE(128, false, false, kVarFp8)
 FA_INSTANCE(128, true, false, kVarFp8)

@@ -26,8 +26,8 @@
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [0,128)   S0 (fp32); P0 (bf16 pairs) overwrites its first 64 columns
 //   [128,256) S1 / P1
-//   [256,256+D)     O0 accumulator (fp32)
-//   [256+D,256+2D)  O1 accumulator
+//   [256,256+DV)       O0 accumulator (fp32), DV = value head dimension
+//   [256+DV,256+2DV)   O1 accumulator
 //
 // Base-2 exponentials with log2(e) folded into the scale (FlashAttention from
 // Scratch, sec. 6.3): p = 2^(s * scale * log2e - r).  The reference r only
@@ -45,25 +45,43 @@
 
 namespace fa {
 
-template <int D, int VAR = kVarNone>
+// Shared-memory layout.  D = query/key head dimension, DV = value head
+// dimension (DV < D in the (192, 128) case).  The K/V ring holds V tiles and
+// the first DV columns of K tiles; when D > DV the remaining K columns go
+// through a second, smaller ring.
+template <int D, int VAR = kVarNone, int DV = D>
 struct FwdSmem {
     static constexpr bool kFp8 = VAR == kVarFp8;
-    static constexpr int kTileBytes = kBlockN * D * (kFp8 ? 1 : 2);  // one 128 x D tile
-    static constexpr int kHalves = kTileBytes / (kBlockN * 128);     // 128-byte swizzle blocks per row
-    static constexpr int kStages = kTileBytes == 32768 ? 4 : 8;      // K/V ring depth
-    static constexpr int kQOff = 0;                                  // Q0, Q1
-    static constexpr int kKVOff = 2 * kTileBytes;
-    static constexpr int kPOff = kKVOff + kStages * kTileBytes;      // FP8: P0, P1 (e4m3, A of P.V)
+    static constexpr int kElem = kFp8 ? 1 : 2;                      // bytes per element
+    static constexpr int kBlk = kBlockN * 128;                      // 128 rows of one 128-byte swizzle block
+    static constexpr int kQBytes = kBlockM * D * kElem;             // one Q tile
+    static constexpr int kTileBytes = kBlockN * DV * kElem;         // one ring stage
+    static constexpr int kTailBytes = kBlockN * (D - DV) * kElem;   // one stage of the K-tail ring
+    static constexpr bool kTail = kTailBytes > 0;
+    static constexpr int kHalvesQ = kQBytes / kBlk;                 // swizzle blocks per Q row
+    static constexpr int kHalves = kTileBytes / kBlk;               // swizzle blocks per ring-stage row
+    static constexpr int kTailHalves = kTailBytes / kBlk;
+    static constexpr int kStages = kTail ? 3 : (kTileBytes == 32768 ? 4 : 8);  // K/V ring depth
+    static constexpr int kTailStages = kTail ? 2 : 0;
+    static constexpr int kQOff = 0;                                 // Q0, Q1
+    static constexpr int kKVOff = 2 * kQBytes;
+    static constexpr int kTailOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kPOff = kTailOff + kTailStages * kTailBytes;  // FP8: P0, P1 (e4m3, A of P.V)
     static constexpr int kBarOff = kPOff + (kFp8 ? 2 * kTileBytes : 0);
     // barrier slots (8 bytes each)
     static constexpr int kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kStages;
-    static constexpr int kSFull = 4 + 2 * kStages, kPFull = kSFull + 2, kOFull = kSFull + 4,
+    static constexpr int kTFull = 4 + 2 * kStages, kTEmpty = kTFull + kTailStages;
+    static constexpr int kSFull = kTFull + 2 * kTailStages, kPFull = kSFull + 2, kOFull = kSFull + 4,
                          kOEmpty = kSFull + 6, kStFull = kSFull + 8, kStEmpty = kSFull + 10,
                          kDrain = kSFull + 12, kNumBars = kSFull + 13;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;      // tmem base, abort flag
-    static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;  // float4 [2][128]
-    static constexpr int kBytes = kStatsOff + 2 * kBlockM * 16;
-    static constexpr int kAlloc = kBytes + 1024;  // slack for 1 KB alignment
+    static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;  // float2 [2][128]
+    static constexpr int kBytes = kStatsOff + 2 * kBlockM * 8;
+    // 1 KB of slack for aligning the window where it fits; otherwise the kernel
+    // checks the alignment at run time
+    static constexpr int kMaxDynamic = 232448;
+    static constexpr int kAlloc = kBytes + 1024 <= kMaxDynamic ? kBytes + 1024 : kMaxDynamic;
+    static_assert(kBytes <= kMaxDynamic, "shared-memory layout exceeds the per-CTA limit");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS = 0, kColO = 256;
 };
@@ -235,23 +253,29 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
 }
 
 // S_t = Q_t K^T: both operands K-major with 128-byte swizzle, 32 bytes of the
-// row (16 bf16 or 32 e4m3 elements) per MMA.
-template <int D, int VAR>
-__device__ __forceinline__ void mma_qk(uint32_t tmem, uint32_t sb, int t, int ks, bool leader)
+// row (16 bf16 or 32 e4m3 elements) per MMA.  K's first DV columns sit in
+// ring stage ks, the rest (D > DV) in tail stage ts.
+template <int D, int VAR, int DV>
+__device__ __forceinline__ void mma_qk(uint32_t tmem, uint32_t sb, int t, int ks, int ts, bool leader)
 {
-    using L = FwdSmem<D, VAR>;
-    constexpr int kSteps = L::kTileBytes / kBlockN / 32;
-    const uint64_t qd = smem_desc_sw128(sb + L::kQOff + (uint32_t)(t * L::kTileBytes), 16, 1024);
+    using L = FwdSmem<D, VAR, DV>;
+    constexpr int kSteps = L::kQBytes / kBlockM / 32;
+    constexpr int kMainSteps = L::kTileBytes / kBlockN / 32;
+    const uint64_t qd = smem_desc_sw128(sb + L::kQOff + (uint32_t)(t * L::kQBytes), 16, 1024);
     const uint64_t kd = smem_desc_sw128(sb + L::kKVOff + (uint32_t)(ks * L::kTileBytes), 16, 1024);
+    const uint64_t td =
+        L::kTail ? smem_desc_sw128(sb + L::kTailOff + (uint32_t)(ts * L::kTailBytes), 16, 1024) : 0ull;
     const uint32_t d = tmem + L::kColS + (uint32_t)(t * kBlockN);
     if (leader) {
 #pragma unroll
         for (int kk = 0; kk < kSteps; ++kk) {
-            const uint64_t off = (uint64_t)(((kk >> 2) * (L::kTileBytes / L::kHalves) + (kk & 3) * 32) >> 4);
+            const uint64_t qoff = (uint64_t)(((kk >> 2) * L::kBlk + (kk & 3) * 32) >> 4);
+            const int k2 = kk < kMainSteps ? kk : kk - kMainSteps;
+            const uint64_t kdesc = (kk < kMainSteps ? kd : td) + (uint64_t)(((k2 >> 2) * L::kBlk + (k2 & 3) * 32) >> 4);
             if constexpr (L::kFp8)
-                mma_ss_f8(d, qd + off, kd + off, idesc_e4m3_f32(kBlockM, kBlockN), kk > 0 ? 1u : 0u);
+                mma_ss_f8(d, qd + qoff, kdesc, idesc_e4m3_f32(kBlockM, kBlockN), kk > 0 ? 1u : 0u);
             else
-                mma_ss(d, qd + off, kd + off, idesc_bf16_f32(kBlockM, kBlockN, false), kk > 0 ? 1u : 0u);
+                mma_ss(d, qd + qoff, kdesc, idesc_bf16_f32(kBlockM, kBlockN, false), kk > 0 ? 1u : 0u);
         }
     }
     __syncwarp();
@@ -260,11 +284,11 @@ __device__ __forceinline__ void mma_qk(uint32_t tmem, uint32_t sb, int t, int ks
 // O_t (+)= P_t V.  bf16: P from tensor memory, V MN-major with 128-byte
 // swizzle, 16 keys per MMA.  e4m3: P from shared memory (K-major) and V^T
 // (K-major, [d][key]), 32 keys per MMA.
-template <int D, int VAR>
+template <int D, int VAR, int DV>
 __device__ __forceinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs, bool acc, bool leader)
 {
-    using L = FwdSmem<D, VAR>;
-    const uint32_t d = tmem + L::kColO + (uint32_t)(t * D);
+    using L = FwdSmem<D, VAR, DV>;
+    const uint32_t d = tmem + L::kColO + (uint32_t)(t * DV);
     if constexpr (L::kFp8) {
         const uint64_t pd = smem_desc_sw128(sb + L::kPOff + (uint32_t)(t * L::kTileBytes), 16, 1024);
         const uint64_t vd = smem_desc_sw128(sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes), 16, 1024);
@@ -272,12 +296,11 @@ __device__ __forceinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs
 #pragma unroll
             for (int kk = 0; kk < kBlockN / 32; ++kk)
                 mma_ss_f8(d, pd + (uint64_t)((kk * 32) >> 4), vd + (uint64_t)((kk * 32) >> 4),
-                          idesc_e4m3_f32(kBlockM, D), (acc || kk > 0) ? 1u : 0u);
+                          idesc_e4m3_f32(kBlockM, DV), (acc || kk > 0) ? 1u : 0u);
         }
     } else {
-        constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
-        const uint64_t vd = smem_desc_sw128(sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes),
-                                            L::kTileBytes / L::kHalves, 1024);
+        constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, DV, true);
+        const uint64_t vd = smem_desc_sw128(sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes), L::kBlk, 1024);
         const uint32_t pa = tmem + L::kColS + (uint32_t)(t * kBlockN);
         if (leader) {
 #pragma unroll
@@ -289,13 +312,12 @@ __device__ __forceinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs
     __syncwarp();
 }
 
-template <int D, bool CAUSAL, bool VARLEN, int VAR>
+template <int D, bool CAUSAL, bool VARLEN, int VAR, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const FwdParams p)
 {
-    using L = FwdSmem<D, VAR>;
-    constexpr int kHalves = L::kHalves;  // 128-byte swizzle blocks per row
+    using L = FwdSmem<D, VAR, DV>;
     constexpr float kTau = 8.0f;     // rescale threshold, log2 units
     constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -308,11 +330,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-    float4* stats = reinterpret_cast<float4*>(smem + L::kStatsOff);
+    float2* stats = reinterpret_cast<float2*>(smem + L::kStatsOff);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const WaitFailure wf{p.err, p.diag};
+    if ((uint32_t)(smem - smem_raw) + L::kBytes > (uint32_t)L::kAlloc) {
+        // the dynamic window is aligned too loosely for the layout: report, touch nothing
+        if (threadIdx.x == 0) atomicOr(p.err, 4);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -328,6 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(bar(L::kKVFull + s), 1);
             mbar_init(bar(L::kKVEmpty + s), 1);
+        }
+        for (int s = 0; s < L::kTailStages; ++s) {
+            mbar_init(bar(L::kTFull + s), 1);
+            mbar_init(bar(L::kTEmpty + s), 1);
         }
         mbar_init(bar(L::kDrain), 1);
         *abort_flag = 0;
@@ -355,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = threadIdx.x & 127;   // query row within the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t tS = tmem + lane_base + L::kColS + (uint32_t)(t * kBlockN);
-        const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * D);
+        const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * DV);
         const float sl2 = p.scale_log2;
         uint32_t s_ph = 0, st_ph = 1;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -388,8 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_ph ^= 1;
                 tc_fence_after_sync();
                 uint32_t sv[4][32];
+                // the tensor-memory load also returns each chunk's maximum when the
+                // raw score order is the order the row maximum needs
+                constexpr bool kHwMax = VAR == kVarNone || VAR == kVarWindow || VAR == kVarFp8;
+                float hmx[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, sv[c]);
+                for (int c = 0; c < 4; ++c) {
+                    if constexpr (kHwMax)
+                        tmem_ld32_max(tS + 32u * c, sv[c], hmx[c]);
+                    else
+                        tmem_ld32(tS + 32u * c, sv[c]);
+                }
                 tmem_wait_ld();
                 const int key0 = (j + w.kf) * kBlockN;
                 if constexpr (VAR == kVarFp8) smul = smul_q * __ldg(fp8_sk + j);
@@ -419,28 +459,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // window, sequence tail) get -inf (FlashAttention from Scratch, sec. 7.3)
                 const int nvalid = kv_last - key0 + 1;
                 const int nskip = kv_first - key0;
-                if (__any_sync(0xffffffffu, nvalid < kBlockN || nskip > 0)) {
+                const bool masked = __any_sync(0xffffffffu, nvalid < kBlockN || nskip > 0);
+                if (masked) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             if (32 * c + i >= nvalid || 32 * c + i < nskip) sv[c][i] = __float_as_uint(-INFINITY);
                 }
-                // row maximum of the raw scores
-                float mx[8];
+                // row maximum of the scores: from the loads, unless masking or a
+                // score modifier changed the values
+                float mraw;
+                if (kHwMax && !masked) {
+                    mraw = fmaxf(fmaxf(hmx[0], hmx[1]), fmaxf(hmx[2], hmx[3]));
+                } else {
+                    float mx[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sv[i >> 1][(i & 1) * 16]);
+                    for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sv[i >> 1][(i & 1) * 16]);
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int e = 32 * c + i;
-                        if ((e & 15) == 0) continue;
-                        mx[e >> 4] = fmaxf(mx[e >> 4], __uint_as_float(sv[c][i]));
-                    }
+                        for (int i = 0; i < 32; ++i) {
+                            const int e = 32 * c + i;
+                            if ((e & 15) == 0) continue;
+                            mx[e >> 4] = fmaxf(mx[e >> 4], __uint_as_float(sv[c][i]));
+                        }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], mx[i + 4]);
-                const float mrow = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * smul;
+                    for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], mx[i + 4]);
+                    mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                }
+                const float mrow = mraw * smul;
                 // conditional rescale: keep r unless the maximum rose by more than tau
                 const float r_new = (mrow - r > kTau) ? mrow : r;
                 const float alpha = (r_new == r) ? 1.f : ex2_approx(r - r_new);
@@ -506,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // here: the previous P.V completed before this S was committed)
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < DV / 32; ++c) {
                         uint32_t ov[32];
                         tmem_ld32(tO + 32u * c, ov);
                         tmem_wait_ld();
@@ -523,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // hand the row statistics to the epilogue
             if (!warp_wait(bar(L::kStEmpty + t), st_ph, abort_flag, wf, 3 + t, tile)) goto done;
             st_ph ^= 1;
-            stats[t * kBlockM + row] = make_float4(l_rnd, l, r, 0.f);
+            // (sum of rounded p, base-2 log of the row's normaliser)
+            stats[t * kBlockM + row] = make_float2(l_rnd, l > 0.f ? r + __log2f(l) : -INFINITY);
             mbar_arrive(bar(L::kStFull + t));
         }
     } else if (warp < 12) {
@@ -540,17 +589,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = q_row < w.lq;
                 int64_t orow, lidx;
                 if constexpr (VARLEN) {
-                    orow = ((int64_t)(w.q0 + q_row) * p.Hq + w.hq) * D;
+                    orow = ((int64_t)(w.q0 + q_row) * p.Hq + w.hq) * DV;
                     lidx = (int64_t)w.hq * p.total_q + w.q0 + q_row;
                 } else {
                     lidx = ((int64_t)w.b * p.Hq + w.hq) * p.Lq + q_row;
-                    orow = lidx * D;
+                    orow = lidx * DV;
                 }
                 uint4* dst = reinterpret_cast<uint4*>(obase + orow);
                 if (w.nk == 0) {  // no key reaches this block: O = 0, LSE = -inf
                     if (valid) {
 #pragma unroll
-                        for (int i = 0; i < D / 4; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                        for (int i = 0; i < DV / 4; ++i) dst[i] = make_uint4(0, 0, 0, 0);
                         p.lse[lidx] = -INFINITY;
                     }
                     continue;
@@ -560,14 +609,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 if (!warp_wait(bar(L::kStFull + t), st_ph[t], abort_flag, wf, 7 + t, tile)) goto done;
                 st_ph[t] ^= 1;
-                const float4 st = stats[t * kBlockM + row];  // (sum of rounded p, sum of p, r)
+                const float2 st = stats[t * kBlockM + row];  // (sum of rounded p, log2 normaliser)
                 mbar_arrive(bar(L::kStEmpty + t));
                 float inv = st.x > 0.f ? 1.f / st.x : 0.f;
                 if constexpr (VAR == kVarFp8) inv *= __ldg(p.fp8_sv + (long long)w.b * p.Hkv + w.hkv);
-                const float l = st.y;
-                const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * D);
+                const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * DV);
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < DV / 32; ++c) {
                     uint32_t ov[32];
                     tmem_ld32(tO + 32u * c, ov);
                     tmem_wait_ld();
@@ -582,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::kOEmpty + t));
-                if (valid) p.lse[lidx] = l > 0.f ? (st.z + __log2f(l)) * kLn2 : -INFINITY;
+                if (valid) p.lse[lidx] = st.y * kLn2;
             }
         }
     } else {
@@ -591,27 +639,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ============================================================ TMA producer
             if (lane == 0) {
                 uint32_t q_ph[2] = {1, 1};
-                int stage = 0;
-                uint32_t kv_ph = 1;
+                int stage = 0, tstage = 0;
+                uint32_t kv_ph = 1, t_ph = 1;
                 // last armed phase of each buffer, to wait out copies in flight at exit
                 int q_armed[2] = {-1, -1};
                 int kv_armed[L::kStages];
+                int t_armed[L::kTailStages > 0 ? L::kTailStages : 1];
                 for (int s = 0; s < L::kStages; ++s) kv_armed[s] = -1;
+                for (int s = 0; s < L::kTailStages; ++s) t_armed[s] = -1;
                 auto load_q = [&](const Work& w, int t, int tile) -> bool {
                     if (!mbar_wait(bar(L::kQEmpty + t), q_ph[t], abort_flag, wf, 9 + t, tile)) return false;
                     q_ph[t] ^= 1;
-                    mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
+                    mbar_arrive_expect_tx(bar(L::kQFull + t), L::kQBytes);
                     q_armed[t] = (int)q_ph[t];  // parity of the phase this copy completes
-                    const uint32_t dst = sb + L::kQOff + (uint32_t)(t * L::kTileBytes);
+                    const uint32_t dst = sb + L::kQOff + (uint32_t)(t * L::kQBytes);
                     const int row0 = w.m0 + t * kBlockM;
 #pragma unroll
-                    for (int h = 0; h < kHalves; ++h) {
+                    for (int h = 0; h < L::kHalvesQ; ++h) {
                         if constexpr (VARLEN)
-                            tma_load_3d(dst + h * (L::kTileBytes / kHalves), &tmQ, bar(L::kQFull + t), 64 * h,
-                                        w.hq, w.zq + row0);
+                            tma_load_3d(dst + h * L::kBlk, &tmQ, bar(L::kQFull + t), 64 * h, w.hq, w.zq + row0);
                         else
-                            tma_load_3d(dst + h * (L::kTileBytes / kHalves), &tmQ, bar(L::kQFull + t), 64 * h,
-                                        row0, w.zq);
+                            tma_load_3d(dst + h * L::kBlk, &tmQ, bar(L::kQFull + t), 64 * h, row0, w.zq);
                     }
                     return true;
                 };
@@ -635,18 +683,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(dst, map, bar(L::kKVFull + stage), (j + w.kf) * kBlockN, 0, w.zk);
                     } else {
 #pragma unroll
-                        for (int h = 0; h < kHalves; ++h) {
+                        for (int h = 0; h < L::kHalves; ++h) {
                             if constexpr (VARLEN)
-                                tma_load_3d(dst + h * (L::kTileBytes / kHalves), map, bar(L::kKVFull + stage),
-                                            64 * h, w.hkv, w.zk + (j + w.kf) * kBlockN);
+                                tma_load_3d(dst + h * L::kBlk, map, bar(L::kKVFull + stage), 64 * h, w.hkv,
+                                            w.zk + (j + w.kf) * kBlockN);
                             else
-                                tma_load_3d(dst + h * (L::kTileBytes / kHalves), map, bar(L::kKVFull + stage),
-                                            64 * h, (j + w.kf) * kBlockN, w.zk);
+                                tma_load_3d(dst + h * L::kBlk, map, bar(L::kKVFull + stage), 64 * h,
+                                            (j + w.kf) * kBlockN, w.zk);
                         }
                     }
                     if (++stage == L::kStages) {
                         stage = 0;
                         kv_ph ^= 1;
+                    }
+                    if (L::kTail && map == &tmK) {
+                        // K columns DV .. D-1 into the tail ring
+                        if (!mbar_wait(bar(L::kTEmpty + tstage), t_ph, abort_flag, wf, 24, tile)) return false;
+                        mbar_arrive_expect_tx(bar(L::kTFull + tstage), L::kTailBytes);
+                        t_armed[tstage] = (int)(t_ph ^ 1u);
+                        const uint32_t tdst = sb + L::kTailOff + (uint32_t)(tstage * L::kTailBytes);
+#pragma unroll
+                        for (int h = 0; h < L::kTailHalves; ++h) {
+                            if constexpr (VARLEN)
+                                tma_load_3d(tdst + h * L::kBlk, map, bar(L::kTFull + tstage), 64 * (L::kHalves + h),
+                                            w.hkv, w.zk + (j + w.kf) * kBlockN);
+                            else
+                                tma_load_3d(tdst + h * L::kBlk, map, bar(L::kTFull + tstage), 64 * (L::kHalves + h),
+                                            (j + w.kf) * kBlockN, w.zk);
+                        }
+                        if (++tstage == L::kTailStages) {
+                            tstage = 0;
+                            t_ph ^= 1;
+                        }
                     }
                     return true;
                 };
@@ -666,6 +734,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (q_armed[t] >= 0) mbar_settle(bar(L::kQFull + t), (uint32_t)q_armed[t], wf, 13);
                 for (int s = 0; s < L::kStages; ++s)
                     if (kv_armed[s] >= 0) mbar_settle(bar(L::kKVFull + s), (uint32_t)kv_armed[s], wf, 14);
+                for (int s = 0; s < L::kTailStages; ++s)
+                    if (t_armed[s] >= 0) mbar_settle(bar(L::kTFull + s), (uint32_t)t_armed[s], wf, 26);
             }
             __syncwarp();
         } else if (warp == 13) {
@@ -675,8 +745,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool leader = lane == 0;
             const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
             uint32_t q_ph[2] = {0, 0}, p_ph[2] = {0, 0}, oe_ph[2] = {1, 1};
-            int stage = 0;
-            uint32_t kv_ph = 0;
+            int stage = 0, tstage = 0;
+            uint32_t kv_ph = 0, t_ph = 0;
             bool issued = false;
             auto next_stage = [&]() {
                 if (++stage == L::kStages) {
@@ -688,6 +758,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (leader) tc_commit(bar(b));
                 __syncwarp();
             };
+            // the tail stage of the K tile just taken from the ring (D > DV only)
+            auto take_tail = [&](int tile, int& ts) -> bool {
+                ts = 0;
+                if constexpr (L::kTail) {
+                    ts = tstage;
+                    if (!warp_wait(bar(L::kTFull + ts), t_ph, abort_flag, wf, 25, tile)) return false;
+                    if (++tstage == L::kTailStages) {
+                        tstage = 0;
+                        t_ph ^= 1;
+                    }
+                }
+                return true;
+            };
+            auto release_tail = [&](int ts) {
+                if constexpr (L::kTail) commit(L::kTEmpty + ts);
+            };
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                 const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, tile);
                 if (w.nk == 0) continue;
@@ -698,17 +784,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ks = stage;
                 if (!warp_wait(bar(L::kKVFull + ks), kv_ph, abort_flag, wf, 17, tile)) break;
                 next_stage();
+                int ts;
+                if (!take_tail(tile, ts)) break;
                 tc_fence_after_sync();
-                mma_qk<D, VAR>(tm, sb, 0, ks, leader);
+                mma_qk<D, VAR, DV>(tm, sb, 0, ks, ts, leader);
                 issued = true;
                 commit(L::kSFull + 0);
                 if (nk == 1) commit(L::kQEmpty + 0);
                 if (!warp_wait(bar(L::kQFull + 1), q_ph[1], abort_flag, wf, 16, tile)) break;
                 q_ph[1] ^= 1;
                 tc_fence_after_sync();
-                mma_qk<D, VAR>(tm, sb, 1, ks, leader);
+                mma_qk<D, VAR, DV>(tm, sb, 1, ks, ts, leader);
                 commit(L::kSFull + 1);
                 commit(L::kKVEmpty + ks);
+                release_tail(ts);
                 if (nk == 1) commit(L::kQEmpty + 1);
                 bool ok = true;
                 for (int j = 0; j < nk && ok; ++j) {
@@ -717,11 +806,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int vs = stage;
                     if (!(ok = warp_wait(bar(L::kKVFull + vs), kv_ph, abort_flag, wf, 18, tile))) break;
                     next_stage();
-                    int kn = -1;
+                    int kn = -1, tn = 0;
                     if (j + 1 < nk) {
                         kn = stage;
                         if (!(ok = warp_wait(bar(L::kKVFull + kn), kv_ph, abort_flag, wf, 17, tile))) break;
                         next_stage();
+                        if (!(ok = take_tail(tile, tn))) break;
                     }
                     // tile 0: P0(j) . V(j), then S0(j+1)
                     if (j == 0) {
@@ -731,9 +821,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = warp_wait(bar(L::kPFull + 0), p_ph[0], abort_flag, wf, 21, tile))) break;
                     p_ph[0] ^= 1;
                     tc_fence_after_sync();
-                    mma_pv<D, VAR>(tm, sb, 0, vs, j > 0, leader);
+                    mma_pv<D, VAR, DV>(tm, sb, 0, vs, j > 0, leader);
                     if (kn >= 0) {
-                        mma_qk<D, VAR>(tm, sb, 0, kn, leader);
+                        mma_qk<D, VAR, DV>(tm, sb, 0, kn, tn, leader);
                         commit(L::kSFull + 0);
                         if (j + 2 == nk) commit(L::kQEmpty + 0);
                     } else {
@@ -747,12 +837,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = warp_wait(bar(L::kPFull + 1), p_ph[1], abort_flag, wf, 22, tile))) break;
                     p_ph[1] ^= 1;
                     tc_fence_after_sync();
-                    mma_pv<D, VAR>(tm, sb, 1, vs, j > 0, leader);
+                    mma_pv<D, VAR, DV>(tm, sb, 1, vs, j > 0, leader);
                     commit(L::kKVEmpty + vs);
                     if (kn >= 0) {
-                        mma_qk<D, VAR>(tm, sb, 1, kn, leader);
+                        mma_qk<D, VAR, DV>(tm, sb, 1, kn, tn, leader);
                         commit(L::kSFull + 1);
                         commit(L::kKVEmpty + kn);
+                        release_tail(tn);
                         if (j + 2 == nk) commit(L::kQEmpty + 1);
                     } else {
                         commit(L::kOFull + 1);

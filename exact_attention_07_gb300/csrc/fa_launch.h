@@ -10,7 +10,8 @@
 namespace fa {
 
 
-template <int D, bool CAUSAL, bool VARLEN, int VAR = kVarNone>
+// D = query/key head dimension, DV = value head dimension.
+template <int D, bool CAUSAL, bool VARLEN, int VAR = kVarNone, int DV = D>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const FwdParams& p, int grid, cudaStream_t stream);
 

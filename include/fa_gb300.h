@@ -153,6 +153,31 @@ typedef struct fa_variant {
     const float* alibi_slopes;
 } fa_variant_t;
 
+/*
+ * Forward with a value head dimension that differs from the query/key one
+ * (FlashAttention-4: Blackwell Attention Kernel Co-Design, "How we know": the
+ * (192, 128) case of its benchmarks, as in DeepSeek-V3-style attention).
+ *
+ *   q [B, Hq, Lq, D], k [B, Hkv, Lk, D], v [B, Hkv, Lk, Dv] bf16 (DEVICE)
+ *   o [B, Hq, Lq, Dv] fp32, lse [B, Hq, Lq] fp32 (DEVICE, outputs)
+ *
+ * O = softmax(scale * Q K^T + M) V; everything else (causal rule, GQA,
+ * empty rows, errors, ownership) as fa_fwd.  Supported (D, Dv): (64, 64),
+ * (128, 128) and (192, 128); other pairs return FA_ERR_UNSUPPORTED.
+ * fa_fwd(..., D, ...) is fa_fwd_hdim(..., D, D, ...).  1 kernel.
+ */
+fa_status_t fa_fwd_hdim(const void* q, const void* k, const void* v, float* o, float* lse,
+                        int B, int Hq, int Hkv, int Lq, int Lk, int D, int Dv, int causal,
+                        float softmax_scale, cudaStream_t stream);
+
+/* fa_fwd_varlen with value head dimension Dv: q, k [total, H, D], v [total_k, Hkv, Dv],
+ * o [total_q, Hq, Dv]; same (D, Dv) pairs as fa_fwd_hdim.  2 kernels. */
+fa_status_t fa_fwd_varlen_hdim(const void* q, const void* k, const void* v, float* o, float* lse,
+                               const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                               int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                               int Hq, int Hkv, int D, int Dv, int causal, float softmax_scale,
+                               cudaStream_t stream);
+
 /* fa_fwd with a variant (same layouts; `variant` is a HOST pointer). */
 fa_status_t fa_fwd_variant(const void* q, const void* k, const void* v, float* o, float* lse,
                            int B, int Hq, int Hkv, int Lq, int Lk, int D, const fa_variant_t* variant,

@@ -159,3 +159,25 @@ def test_fp8_argument_validation(lib):
     assert lib.fa_fp8_prepare(16, 16, 16, 18, 1, 2, 1, 64, 64, 128, 16, 1 << 20, None) == INV  # signs misaligned
     assert lib.fa_fwd_fp8(None, 16, 16, 1, 2, 1, 64, 64, 128, 0, 0.1, None) == INV
     assert lib.fa_fwd_fp8(16, 16, 16, 1, 2, 1, 64, 64, 128, 0, -0.1, None) == INV
+
+
+def test_hdim_argument_validation(lib):
+    INV, UNS = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+
+    def call(D=192, Dv=128, v=16, B=1, scale=0.1):
+        return lib.fa_fwd_hdim(16, 16, v, 16, 16, B, 2, 1, 64, 64, D, Dv, 1, scale, None)
+
+    assert call(v=None) == INV
+    assert call(Dv=0) == INV
+    assert call(B=0) == INV
+    assert call(scale=float("inf")) == INV
+    for D, Dv in ((192, 192), (128, 64), (64, 128), (256, 128), (192, 64), (160, 128)):
+        assert call(D=D, Dv=Dv) == UNS, (D, Dv)
+
+    def vcall(D=192, Dv=128, n=2):
+        return lib.fa_fwd_varlen_hdim(16, 16, 16, 16, 16, 32, 32, n, 10, 10, 8, 8, 2, 2, D, Dv, 1, 0.1, None)
+
+    assert vcall(n=0) == INV
+    assert vcall(Dv=-1) == INV
+    assert vcall(D=128, Dv=192) == UNS
+    assert lib.fa_last_launch_count() == 0

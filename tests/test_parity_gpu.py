@@ -125,7 +125,10 @@ def test_varlen_invalid_offsets_latch_error():
 def _dense_workload(name):
     w = WORKLOADS[name]
     q, k, v = dense_inputs(w)
-    o, lse = fa.fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=w.causal)
+    if w.Dv != w.D:
+        o, lse = fa.fa_fwd_hdim(q.to(DEV), k.to(DEV), v.to(DEV), causal=w.causal)
+    else:
+        o, lse = fa.fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=w.causal)
     fa.fa_check()
     return w, q, k, v, o, lse
 
@@ -140,7 +143,7 @@ def test_benchmark_workload_sampled(name):
     slabs = [0, w.B * w.Hq - 1, (w.B * w.Hq) // 2]
     rows = np.arange(n_total) if n_total <= 4096 else sample_rows(n_total, rows_per_slab, slabs, rng)
     ref_o, ref_lse = oracle.attention(q, k, v, scale=w.scale, causal=w.causal, rows=rows)
-    o_s = o.float().reshape(-1, w.D)[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    o_s = o.float().reshape(-1, w.Dv)[torch.from_numpy(rows).to(DEV)].cpu().numpy()
     l_s = lse.reshape(-1)[torch.from_numpy(rows).to(DEV)].cpu().numpy()
     compare(o_s, l_s, ref_o, ref_lse, name)
     # properties that hold for every row at any size

@@ -49,6 +49,12 @@ class Workload:
     window: tuple[int, int] | None = None
     # the FP8 forward (e4m3 inputs after the Hadamard rotation)
     fp8: bool = False
+    # value head dimension when it differs from the query/key one D
+    dv: int | None = None
+
+    @property
+    def Dv(self) -> int:
+        return self.D if self.dv is None else self.dv
 
     @property
     def scale(self) -> float:
@@ -59,23 +65,24 @@ class Workload:
         return self.seqlens is not None
 
     def flops(self) -> float:
-        """Matrix FLOPs of the forward: 4*Lq*Lk*D per head, halved when causal.
+        """Matrix FLOPs of the forward: 2*Lq*Lk*(D + Dv) per head (4*Lq*Lk*D
+        when Dv = D), halved when causal.
 
-        This is the accounting of the benchmark spec's metric (multiply and add
-        counted separately; the causal half ignores the diagonal's extra half
-        tile).
+        Multiply and add are counted separately; the causal half ignores the
+        diagonal's extra half tile.
         """
+        dd = 2.0 * (self.D + self.Dv)
         if self.varlen:
-            total = sum(4.0 * self.Hq * L * L * self.D for L in self.seqlens)
+            total = sum(dd * self.Hq * L * L for L in self.seqlens)
         else:
-            total = 4.0 * self.B * self.Hq * self.Lq * self.Lk * self.D
+            total = dd * self.B * self.Hq * self.Lq * self.Lk
         if self.window is not None:  # count only the pairs the window allows
             import numpy as np
             c = np.arange(self.Lq, dtype=np.int64) + (self.Lk - self.Lq)
             lo = np.maximum(0, c - self.window[0]) if self.window[0] >= 0 else np.zeros_like(c)
             hi = np.minimum(self.Lk - 1, c + self.window[1]) if self.window[1] >= 0 else np.full_like(c, self.Lk - 1)
             pairs = float(np.maximum(hi - lo + 1, 0).sum())
-            return 4.0 * self.B * self.Hq * pairs * self.D
+            return dd * self.B * self.Hq * pairs
         if self.bwd:  # five matrix products instead of two (S, dP, dV, dQ, dK)
             total *= 2.5
         return total / 2 if self.causal else total
@@ -85,7 +92,8 @@ class Workload:
         O (fp32) and LSE (fp32) written once."""
         assert not self.varlen
         qo = self.B * self.Hq * self.Lq
-        return 2.0 * qo * self.D + 4.0 * self.B * self.Hkv * self.Lk * self.D + 4.0 * qo * self.D + 4.0 * qo
+        return (2.0 * qo * self.D + 2.0 * self.B * self.Hkv * self.Lk * (self.D + self.Dv) + 4.0 * qo * self.Dv
+                + 4.0 * qo)
 
 
 def varlen_lengths(n: int = 8, lo: int = 512, hi: int = 8192, seed: int = 0) -> list[int]:
@@ -98,12 +106,12 @@ def _bf16(x: torch.Tensor) -> torch.Tensor:
 
 
 def dense_inputs(w: Workload):
-    """Q [B,Hq,Lq,D], K and V [B,Hkv,Lk,D], bf16 on the CPU."""
+    """Q [B,Hq,Lq,D], K [B,Hkv,Lk,D] and V [B,Hkv,Lk,Dv], bf16 on the CPU."""
     assert not w.varlen
     g = torch.Generator().manual_seed(w.seed)
     q = torch.randn((w.B, w.Hq, w.Lq, w.D), generator=g, dtype=torch.float32)
     k = torch.randn((w.B, w.Hkv, w.Lk, w.D), generator=g, dtype=torch.float32)
-    v = torch.randn((w.B, w.Hkv, w.Lk, w.D), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.Hkv, w.Lk, w.Dv), generator=g, dtype=torch.float32)
     if w.q_mult != 1.0:
         q = q * w.q_mult
     return _bf16(q), _bf16(k), _bf16(v)
@@ -214,6 +222,14 @@ FP8_WORKLOADS: dict[str, Workload] = {
     "fp8_b1_h16_l16384_d128": Workload("fp8_b1_h16_l16384_d128", 1, 16, 16, 16384, 16384, 128, False, fp8=True),
 }
 WORKLOADS.update(FP8_WORKLOADS)
+
+# Query/key head dimension 192 with value head dimension 128 (the asymmetric
+# case of the FlashAttention-4 benchmarks) on the long-sequence shape.
+HDIM_WORKLOADS: dict[str, Workload] = {
+    "d192_b1_h16_l16384": Workload("d192_b1_h16_l16384", 1, 16, 16, 16384, 16384, 192, False, dv=128),
+    "d192_b1_h16_l16384_causal": Workload("d192_b1_h16_l16384_causal", 1, 16, 16, 16384, 16384, 192, True, dv=128),
+}
+WORKLOADS.update(HDIM_WORKLOADS)
 
 # The configuration the throughput metric is quoted on.
 HEADLINE = "b1_h16_l16384_d128"

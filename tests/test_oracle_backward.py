@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.backward import attention_bwd, blocked_backward
+from oracle.backward import attention_bwd, attention_bwd_varlen, blocked_backward
 from oracle.reference import dense_attention
 
 
@@ -181,3 +181,43 @@ def test_sampled_rows_equal_full_result():
     np.testing.assert_allclose(dq, full[0].reshape(-1, D)[qr], atol=1e-12)
     np.testing.assert_allclose(dk, full[1].reshape(-1, D)[kr], atol=1e-12)
     np.testing.assert_allclose(dv, full[2].reshape(-1, D)[kr], atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_matches_autograd_per_sequence(causal):
+    # packed sequences with Lq != Lk, an empty query sequence and an empty key
+    # sequence; each sequence is checked against PyTorch autograd through a
+    # dense softmax of that sequence alone (bottom-right causal alignment)
+    lq, lk = [5, 0, 9, 3, 7], [8, 4, 9, 0, 2]
+    Hq, Hkv, D = 4, 2, 6
+    cq = np.concatenate([[0], np.cumsum(lq)])
+    ck = np.concatenate([[0], np.cumsum(lk)])
+    q = _rand((cq[-1], Hq, D), 1)
+    k = _rand((ck[-1], Hkv, D), 2)
+    v = _rand((ck[-1], Hkv, D), 3)
+    do = _rand((cq[-1], Hq, D), 4)
+    scale = 0.4
+    dq, dk, dv = attention_bwd_varlen(q, k, v, do, cq, ck, scale, causal)
+    r = Hq // Hkv
+    for s in range(len(lq)):
+        q0, q1, k0, k1 = cq[s], cq[s + 1], ck[s], ck[s + 1]
+        if q1 == q0 or k1 == k0:
+            # no pairs: the sequence's gradients stay zero
+            assert np.all(dq[q0:q1] == 0) and np.all(dk[k0:k1] == 0) and np.all(dv[k0:k1] == 0)
+            continue
+        Q = torch.tensor(q[q0:q1].transpose(1, 0, 2), requires_grad=True)
+        K = torch.tensor(k[k0:k1].transpose(1, 0, 2), requires_grad=True)
+        V = torch.tensor(v[k0:k1].transpose(1, 0, 2), requires_grad=True)
+        G = torch.tensor(do[q0:q1].transpose(1, 0, 2))
+        Lq_, Lk_ = q1 - q0, k1 - k0
+        S = scale * Q @ K.repeat_interleave(r, 0).transpose(1, 2)
+        if causal:
+            allowed = torch.arange(Lk_)[None, :] <= torch.arange(Lq_)[:, None] + (Lk_ - Lq_)
+            S = S.masked_fill(~allowed, float("-inf"))
+        P = torch.softmax(S, dim=-1)
+        P = torch.nan_to_num(P, nan=0.0)  # rows without an allowed key
+        O = P @ V.repeat_interleave(r, 0)
+        (O * G).sum().backward()
+        assert np.allclose(dq[q0:q1], Q.grad.numpy().transpose(1, 0, 2), atol=1e-12)
+        assert np.allclose(dk[k0:k1], K.grad.numpy().transpose(1, 0, 2), atol=1e-12)
+        assert np.allclose(dv[k0:k1], V.grad.numpy().transpose(1, 0, 2), atol=1e-12)

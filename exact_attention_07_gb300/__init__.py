@@ -23,7 +23,7 @@ import torch
 
 __all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_hdim", "fa_fwd_varlen_hdim", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
            "fa_fwd_splitkv", "fp8_prepare", "fa_fwd_fp8", "fp8_sections", "splitkv_workspace", "fa_bwd",
-           "bwd_workspace", "fa_check", "fa_status_string", "fa_last_launch_count",
+           "bwd_workspace", "fa_bwd_varlen", "bwd_varlen_workspace", "fa_check", "fa_status_string", "fa_last_launch_count",
            "FAError", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +33,8 @@ _lib = None
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_hdim", "fa_fwd_varlen_hdim", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
-                    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace", "fa_bwd", "fa_bwd_workspace", "fa_fp8_workspace",
+                    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace", "fa_bwd", "fa_bwd_workspace", "fa_bwd_varlen",
+                    "fa_bwd_varlen_workspace", "fa_fp8_workspace",
                     "fa_fp8_prepare", "fa_fwd_fp8", "fa_check", "fa_status_string", "fa_last_launch_count",
                     "fa_test_inject_fault")
 SPLITKV_MAX_ROWS = 16  # (Hq / Hkv) * Lq limit of fa_fwd_splitkv
@@ -97,6 +98,11 @@ def load_library() -> ctypes.CDLL:
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
         lib.fa_bwd_workspace.restype = i
         lib.fa_bwd_workspace.argtypes = [i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_bwd_varlen.restype = i
+        lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp,
+                                      ctypes.c_size_t, vp]
+        lib.fa_bwd_varlen_workspace.restype = i
+        lib.fa_bwd_varlen_workspace.argtypes = [i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         lib.fa_check.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_status_string.restype = ctypes.c_char_p
@@ -532,6 +538,62 @@ def fa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, l
             workspace.record_stream(stream)
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def bwd_varlen_workspace(num_seqs: int, total_q: int, Hq: int) -> int:
+    """Workspace bytes fa_bwd_varlen needs."""
+    nbytes = ctypes.c_size_t(0)
+    st = load_library().fa_bwd_varlen_workspace(num_seqs, total_q, Hq, ctypes.byref(nbytes))
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd_varlen_workspace")
+    return int(nbytes.value)
+
+
+def fa_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+                  dout: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int,
+                  max_seqlen_k: int, causal: bool = False, softmax_scale: float | None = None,
+                  dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, stream=None):
+    """Backward of fa_fwd_varlen.  q/dout [Tq,Hq,D], k/v [Tk,Hkv,D] bf16; o fp32
+    [Tq,Hq,D] and lse fp32 [Hq,Tq] from fa_fwd_varlen; cu_seqlens_* int32 CUDA.
+    Returns (dq, dk, dv) fp32 in the layouts of q, k and v."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _check_tensor(t, n, torch.bfloat16, 3)
+    _check_tensor(o, "o", torch.float32, 3)
+    _check_tensor(lse, "lse", torch.float32, 2)
+    _check_tensor(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check_tensor(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    Tq, Hq, D = q.shape
+    Tk, Hkv, Dk = k.shape
+    if (tuple(v.shape) != tuple(k.shape) or Dk != D or tuple(dout.shape) != tuple(q.shape)
+            or tuple(o.shape) != tuple(q.shape) or tuple(lse.shape) != (Hq, Tq)
+            or cu_seqlens_q.numel() != cu_seqlens_k.numel()):
+        raise ValueError("shape mismatch")
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=torch.float32, device=q.device) if dv is None else dv
+    for t, n, shp in ((dq, "dq", q.shape), (dk, "dk", k.shape), (dv, "dv", k.shape)):
+        _check_tensor(t, n, torch.float32, 3)
+        if tuple(t.shape) != tuple(shp):
+            raise ValueError(f"{n} shape mismatch")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    n_seqs = cu_seqlens_q.numel() - 1
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        nbytes = bwd_varlen_workspace(n_seqs, Tq, Hq)
+        if workspace is None or workspace.numel() * workspace.element_size() < nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        st = lib.fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens_q.data_ptr(),
+                               cu_seqlens_k.data_ptr(), n_seqs, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq,
+                               Hkv, D, int(bool(causal)), float(softmax_scale), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        if isinstance(stream, torch.cuda.Stream):
+            workspace.record_stream(stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd_varlen")
     return dq, dk, dv
 
 

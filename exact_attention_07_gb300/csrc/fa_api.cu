@@ -158,19 +158,28 @@ bool hdim_supported(int D, int Dv) { return (D == Dv && (D == 64 || D == 128)) |
 
 // --------------------------------------------------------------- varlen schedule
 
-// One CTA of 1024 threads.  Validates the offsets, orders sequences longest
-// key range first (the longest work tile of a sequence visits ceil(Lk/128)
-// KV tiles; FlashAttention-4: Blackwell Attention Kernel Co-Design, "LPT scheduling for imbalanced grids", step 4) and writes the
-// exclusive prefix of work tiles in that order.
+// One CTA of 1024 threads.  Validates the offsets, orders sequences by the
+// length of their longest work tile, longest first (FlashAttention-4:
+// Blackwell Attention Kernel Co-Design, "LPT scheduling for imbalanced
+// grids", step 4), and writes the exclusive prefix of work tiles in that
+// order.
+//   forward  (bwd = 0): a tile is 256 query rows of one query head and visits
+//            ceil(Lk/128) KV tiles: tiles = Hq * ceil(Lq/256), sorted by Lk.
+//   backward (bwd = 1): an item is 128 keys of one KV head and visits the Q
+//            tiles of the group: items = Hkv * ceil(Lk/128) when Lq > 0,
+//            sorted by Lq; also the sequences' row offsets in a workspace
+//            where each sequence's rows are padded to a multiple of 128.
 //
 // sched layout (int32): [0] total tiles | [1 .. n+1] prefix by schedule rank |
-// [n+2 .. 2n+1] order (rank -> sequence) | [2n+2 .. 3n+1] tiles by sequence.
+// [n+2 .. 2n+1] order (rank -> sequence) | [2n+2 .. 3n+1] tiles by sequence |
+// backward only: [3n+2 .. 4n+2] padded row offset of each sequence (original
+// order, n+1 entries).
 constexpr int kSchedThreads = 1024;
 constexpr int kSortMax = 4096;
 
 __global__ void __launch_bounds__(kSchedThreads)
     fa_varlen_schedule_kernel(const int* __restrict__ cu_q, const int* __restrict__ cu_k, int n, int total_q,
-                              int total_k, int max_q, int max_k, int Hq, int* __restrict__ sched,
+                              int total_k, int max_q, int max_k, int heads, int bwd, int* __restrict__ sched,
                               int* __restrict__ err)
 {
     __shared__ int key[kSortMax];
@@ -188,8 +197,13 @@ __global__ void __launch_bounds__(kSchedThreads)
         const bool ok = !bad && q0 >= 0 && q1 >= q0 && q1 <= total_q && q1 - q0 <= max_q && k0 >= 0 &&
                         k1 >= k0 && k1 <= total_k && k1 - k0 <= max_k;
         if (!ok) atomicOr(err, 2);
-        if (n <= kSortMax) key[s] = (ok && q1 > q0) ? (k1 - k0) : -1;
-        tiles[s] = ok ? Hq * ((q1 - q0 + 255) / 256) : 0;
+        if (bwd) {
+            if (n <= kSortMax) key[s] = (ok && q1 > q0 && k1 > k0) ? (q1 - q0) : -1;
+            tiles[s] = (ok && q1 > q0) ? heads * ((k1 - k0 + 127) / 128) : 0;
+        } else {
+            if (n <= kSortMax) key[s] = (ok && q1 > q0) ? (k1 - k0) : -1;
+            tiles[s] = ok ? heads * ((q1 - q0 + 255) / 256) : 0;
+        }
     }
     __syncthreads();
     for (int s = tid; s < n; s += kSchedThreads) {
@@ -228,13 +242,37 @@ __global__ void __launch_bounds__(kSchedThreads)
         prefix[r] = acc;
         acc += tiles[order[r]];
     }
+    if (!bwd) return;
+    // padded row offsets in the original sequence order (valid sequences only)
+    __syncthreads();
+    int padded = 0;
+    for (int s = c0; s < c1; ++s) padded += tiles[s] > 0 ? (cu_q[s + 1] - cu_q[s] + 127) / 128 * 128 : 0;
+    part[tid] = padded;
+    __syncthreads();
+    if (tid == 0) {
+        int a = 0;
+        for (int i = 0; i < kSchedThreads; ++i) {
+            const int x = part[i];
+            part[i] = a;
+            a += x;
+        }
+        sched[3 * n + 2 + n] = a;
+    }
+    __syncthreads();
+    int* pad = sched + 3 * n + 2;
+    int a = part[tid];
+    for (int s = c0; s < c1; ++s) {
+        pad[s] = a;
+        a += tiles[s] > 0 ? (cu_q[s + 1] - cu_q[s] + 127) / 128 * 128 : 0;
+    }
 }
 
 cudaError_t launch_varlen_schedule(const int* cu_q, const int* cu_k, int num_seqs, int total_q, int total_k,
-                                   int max_q, int max_k, int Hq, int* sched, int* err, cudaStream_t stream)
+                                   int max_q, int max_k, int heads, int bwd, int* sched, int* err,
+                                   cudaStream_t stream)
 {
     fa_varlen_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(cu_q, cu_k, num_seqs, total_q, total_k, max_q,
-                                                              max_k, Hq, sched, err);
+                                                              max_k, heads, bwd, sched, err);
     return cudaGetLastError();
 }
 
@@ -365,7 +403,7 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
     const size_t ws = sizeof(int) * (2 + 3 * (size_t)num_seqs);
     if (cudaMallocAsync(reinterpret_cast<void**>(&sched), ws, stream) != cudaSuccess) return FA_ERR_CUDA;
     if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
-                               max_seqlen_k, Hq, sched, ds->err, stream) != cudaSuccess) {
+                               max_seqlen_k, Hq, 0, sched, ds->err, stream) != cudaSuccess) {
         cudaFreeAsync(sched, stream);
         return FA_ERR_CUDA;
     }
@@ -491,7 +529,7 @@ extern "C" fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const
     // The schedule kernel writes every scratch entry the attention kernel
     // reads, so nothing left by an earlier call needs clearing.
     if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
-                               max_seqlen_k, Hq, sched, ds->err, stream) != cudaSuccess)
+                               max_seqlen_k, Hq, 0, sched, ds->err, stream) != cudaSuccess)
         return FA_ERR_CUDA;
     FwdParams p{};
     p.o = o;
@@ -741,10 +779,118 @@ extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const
     p.diag = ds->diag;
     p.fault = g_fault_next;
     g_fault_next = 0;
-    if (launch_bwd_pre(D, p, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_bwd_pre(D, false, p, stream) != cudaSuccess) return FA_ERR_CUDA;
     const int grid = (int)(items < ds->num_sms ? items : ds->num_sms);
-    if (launch_bwd(D, causal != 0, mq, mk, mv, mdo, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_bwd(D, causal != 0, false, mq, mk, mv, mdo, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 2;
+    return FA_OK;
+}
+
+// ------------------------------------------------------------- packed backward
+
+namespace {
+// Workspace of fa_bwd_varlen: delta and lse2 as [Hq][rows], every sequence's
+// rows padded to a multiple of 128 (rows = an upper bound of the padded total),
+// then the schedule (4 * num_seqs + 3 ints).
+struct BwdVarlenLayout {
+    long long rows = 0;
+    size_t sched_off = 0, bytes = 0;
+};
+
+bool bwd_varlen_layout(int num_seqs, int total_q, int Hq, BwdVarlenLayout* l)
+{
+    if (num_seqs <= 0 || total_q <= 0 || Hq <= 0) return false;
+    l->rows = ((long long)total_q + 127) / 128 * 128 + 128ll * num_seqs;
+    const long long floats = 2ll * Hq * l->rows;
+    if (floats >= (1ll << 40)) return false;
+    l->sched_off = (size_t)((floats * 4 + 255) & ~255ll);
+    l->bytes = (l->sched_off + sizeof(int) * (4 * (size_t)num_seqs + 3) + 255) & ~(size_t)255;
+    return true;
+}
+}  // namespace
+
+extern "C" fa_status_t fa_bwd_varlen_workspace(int num_seqs, int total_q, int Hq, size_t* workspace_bytes)
+{
+    BwdVarlenLayout l;
+    if (!workspace_bytes || !bwd_varlen_layout(num_seqs, total_q, Hq, &l)) return FA_ERR_INVALID_ARG;
+    *workspace_bytes = l.bytes;
+    return FA_OK;
+}
+
+extern "C" fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                                     const void* dout, float* dq, float* dk, float* dv, const int* cu_seqlens_q,
+                                     const int* cu_seqlens_k, int num_seqs, int total_q, int total_k,
+                                     int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D, int causal,
+                                     float softmax_scale, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream)
+{
+    g_last_launches = 0;
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace || !cu_seqlens_q ||
+        !cu_seqlens_k)
+        return FA_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || total_q <= 0 || total_k <= 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 || Hq <= 0 ||
+        Hkv <= 0 || D <= 0)
+        return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !scale_ok(softmax_scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+        return FA_ERR_INVALID_ARG;
+    if (D != 128) return FA_ERR_UNSUPPORTED;
+    BwdVarlenLayout lay;
+    if (!bwd_varlen_layout(num_seqs, total_q, Hq, &lay) || workspace_bytes < lay.bytes) return FA_ERR_INVALID_ARG;
+    // upper bound of the work items: sum_s ceil(Lk_s / 128) <= total_k / 128 + num_seqs
+    const long long ub = (long long)Hkv * ((long long)total_k / kBwdTile + num_seqs);
+    if (ub >= (1ll << 31) || lay.rows >= (1ll << 31) || (long long)total_q * Hq >= (1ll << 31) * 8ll ||
+        (long long)total_k * Hkv >= (1ll << 31) * 8ll)
+        return FA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    fa_status_t st = device_state(&ds);
+    if (st != FA_OK) return st;
+
+    CUtensorMap mq, mk, mv, mdo;
+    const uint64_t row = (uint64_t)D * 2;
+    if (!encode_map(&mq, q, D, Hq, total_q, row, row * Hq, 1, kBwdTile) ||
+        !encode_map(&mdo, dout, D, Hq, total_q, row, row * Hq, 1, kBwdTile) ||
+        !encode_map(&mk, k, D, Hkv, total_k, row, row * Hkv, 1, kBwdTile) ||
+        !encode_map(&mv, v, D, Hkv, total_k, row, row * Hkv, 1, kBwdTile))
+        return FA_ERR_CUDA;
+
+    int* sched = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + lay.sched_off);
+    if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                               max_seqlen_k, Hkv, 1, sched, ds->err, stream) != cudaSuccess)
+        return FA_ERR_CUDA;
+    BwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.dout = static_cast<const uint16_t*>(dout);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.delta = static_cast<float*>(workspace);
+    p.lse2 = p.delta + (long long)Hq * lay.rows;
+    p.B = 1;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lq_pad = (int)lay.rows;
+    p.group = Hq / Hkv;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.sched = sched;
+    p.num_seqs = num_seqs;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.scale = softmax_scale;
+    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+    p.causal = causal != 0;
+    p.err = ds->err;
+    p.diag = ds->diag;
+    p.fault = g_fault_next;
+    g_fault_next = 0;
+    if (launch_bwd_pre(D, true, p, stream) != cudaSuccess) return FA_ERR_CUDA;
+    const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
+    if (launch_bwd(D, causal != 0, true, mq, mk, mv, mdo, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+    g_last_launches = 3;
     return FA_OK;
 }
 

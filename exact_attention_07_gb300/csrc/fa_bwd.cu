@@ -96,6 +96,80 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p)
     }
 }
 
+// Largest s in [0, n) with a[s] <= x (a non-decreasing, a[0] <= x).
+__device__ __forceinline__ int bwd_upper_index(const int* a, int n, int x)
+{
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a + mid) <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Packed batches, one warp per row, in three ranges of blocks:
+//   [0, nb1)        query token rows (token, head): dQ row zeroed;
+//   [nb1, nb2)      padded workspace rows (head, padded row): delta and lse2
+//                   of the sequence's row, or 0 / +inf on padding rows;
+//   [nb2, gridDim)  key token rows (token, KV head) of sequences without
+//                   work items (no query rows, or invalid offsets): dK and
+//                   dV rows zeroed, since no item writes them.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_varlen_kernel(const BwdParams p, int nb1, int nb2)
+{
+    constexpr int V = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = p.num_seqs;
+    if ((int)blockIdx.x < nb1) {
+        const long long row = (long long)blockIdx.x * 8 + warp;  // token * Hq + head
+        if (row >= (long long)p.total_q * p.Hq) return;
+        float* dq = p.dq + row * D + lane * V;
+#pragma unroll
+        for (int e = 0; e < V; ++e) dq[e] = 0.f;
+    } else if ((int)blockIdx.x < nb2) {
+        const long long row = (long long)(blockIdx.x - nb1) * 8 + warp;  // head * Lq_pad + padded row
+        if (row >= (long long)p.Hq * p.Lq_pad) return;
+        const int h = (int)(row / p.Lq_pad);
+        const int r = (int)(row - (long long)h * p.Lq_pad);
+        const int* pad = p.sched + 3 * n + 2;
+        const int s = bwd_upper_index(pad, n, r);
+        const int i = r - __ldg(pad + s);
+        const int q0 = __ldg(p.cu_q + s), lq = __ldg(p.cu_q + s + 1) - q0;
+        float delta = 0.f, l2 = INFINITY;
+        if (r < __ldg(pad + n) && i < lq) {
+            const long long t = (long long)(q0 + i) * p.Hq + h;
+            const float* o = p.o + t * D + lane * V;
+            const uint16_t* g = p.dout + t * D + lane * V;
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc = fmaf(o[e], __uint_as_float((uint32_t)g[e] << 16), acc);
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+            delta = acc;
+            const float l = p.lse[(long long)h * p.total_q + q0 + i];
+            l2 = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+        }
+        if (lane == 0) {
+            p.delta[row] = delta;
+            p.lse2[row] = l2;
+        }
+    } else {
+        const long long row = (long long)(blockIdx.x - nb2) * 8 + warp;  // key token * Hkv + KV head
+        if (row >= (long long)p.total_k * p.Hkv) return;
+        const int tok = (int)(row / p.Hkv);
+        const int s = bwd_upper_index(p.cu_k, n, tok);
+        if (__ldg(p.sched + 2 + 2 * n + s) > 0) return;  // the sequence's items write these rows
+        float* dk = p.dk + row * D + lane * V;
+        float* dv = p.dv + row * D + lane * V;
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            dk[e] = 0.f;
+            dv[e] = 0.f;
+        }
+    }
+}
+
 namespace {
 
 constexpr int kBwdD = 128;
@@ -181,23 +255,47 @@ struct BwdItem {
     int b, hkv, j;      // batch, KV head, key tile
     int i_min, nq;      // first Q tile with an allowed pair; Q tiles per head
     int steps;          // group * (nq - i_min)
+    int lq, lk;         // query / key length of this problem
+    int q0, k0;         // packed batches: first query / key token of the sequence
+    int ws0;            // packed batches: the sequence's padded workspace row offset
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int it)
 {
     BwdItem w;
-    const int bh_count = p.B * p.Hkv;
-    w.j = it / bh_count;  // longest items (smallest key tile under causal) first
-    const int bh = it - w.j * bh_count;
-    w.b = bh / p.Hkv;
-    w.hkv = bh - w.b * p.Hkv;
-    w.nq = p.num_q_tiles;
+    if constexpr (VARLEN) {
+        // sequences longest query range first; inside one, key tiles in
+        // order (longest items first under causal), KV heads innermost
+        const int n = p.num_seqs;
+        const int lo = bwd_upper_index(p.sched + 1, n, it);
+        const int s = __ldg(p.sched + 2 + n + lo);
+        const int rem = it - __ldg(p.sched + 1 + lo);
+        w.q0 = __ldg(p.cu_q + s);
+        w.lq = __ldg(p.cu_q + s + 1) - w.q0;
+        w.k0 = __ldg(p.cu_k + s);
+        w.lk = __ldg(p.cu_k + s + 1) - w.k0;
+        w.ws0 = __ldg(p.sched + 3 * n + 2 + s);
+        w.j = rem / p.Hkv;
+        w.hkv = rem - w.j * p.Hkv;
+        w.b = 0;
+        w.nq = (w.lq + kBwdTile - 1) / kBwdTile;
+    } else {
+        const int bh_count = p.B * p.Hkv;
+        w.j = it / bh_count;  // longest items (smallest key tile under causal) first
+        const int bh = it - w.j * bh_count;
+        w.b = bh / p.Hkv;
+        w.hkv = bh - w.b * p.Hkv;
+        w.nq = p.num_q_tiles;
+        w.lq = p.Lq;
+        w.lk = p.Lk;
+        w.q0 = w.k0 = w.ws0 = 0;
+    }
     w.i_min = 0;
     if (CAUSAL) {
         // key k is visible from query q iff k <= q + (Lk - Lq): the tile's first
         // key j*128 needs q >= j*128 - (Lk - Lq)
-        const long long first_q = (long long)w.j * kBwdTile - (p.Lk - p.Lq);
+        const long long first_q = (long long)w.j * kBwdTile - (w.lk - w.lq);
         w.i_min = first_q > 0 ? (int)(first_q / kBwdTile) : 0;
         if (w.i_min > w.nq) w.i_min = w.nq;
     }
@@ -230,7 +328,7 @@ __device__ __forceinline__ void bwd_step(const BwdParams& p, const BwdItem& w, i
 
 // ------------------------------------------------------------------ main kernel
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -291,6 +389,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    const int num_items = VARLEN ? __ldg(p.sched) : p.num_items;
 
     if (warp < 4) {
         // ============================================================ dQ reduction, dK/dV epilogue
@@ -301,8 +400,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         uint32_t gstep = 0;
         int I = 0;
-        for (int k = 0, it = bwd_cta_item<CAUSAL>(0); it < p.num_items; it = bwd_cta_item<CAUSAL>(++k)) {
-            const BwdItem w = bwd_item<CAUSAL>(p, it);
+        for (int k = 0, it = bwd_cta_item<CAUSAL || VARLEN>(0); it < num_items; it = bwd_cta_item<CAUSAL || VARLEN>(++k)) {
+            const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 int h, i;
                 bwd_step(p, w, s, h, i);
@@ -318,21 +417,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive(bar(L::bDQEmpty));
                 // each warp instruction adds 128 contiguous bytes of one dQ row
                 const int q0 = i * kBwdTile;
-                const int nrows = min(kBwdTile, p.Lq - q0);
-                float* dst = p.dq + (((long long)w.b * p.Hq + h) * p.Lq + q0) * kBwdD + t;
+                const int nrows = min(kBwdTile, w.lq - q0);
+                // dQ rows: dense [B, Hq, Lq, D], packed [Tq, Hq, D]
+                const long long rs = VARLEN ? (long long)p.Hq * kBwdD : kBwdD;
+                float* dst = p.dq + t +
+                             (VARLEN ? ((long long)(w.q0 + q0) * p.Hq + h) * kBwdD
+                                     : (((long long)w.b * p.Hq + h) * p.Lq + q0) * kBwdD);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    if (c < nrows) red_add(dst + c * kBwdD, __uint_as_float(v0[c]));
-                    if (32 + c < nrows) red_add(dst + (32 + c) * kBwdD, __uint_as_float(v1[c]));
-                    if (64 + c < nrows) red_add(dst + (64 + c) * kBwdD, __uint_as_float(v2[c]));
-                    if (96 + c < nrows) red_add(dst + (96 + c) * kBwdD, __uint_as_float(v3[c]));
+                    if (c < nrows) red_add(dst + c * rs, __uint_as_float(v0[c]));
+                    if (32 + c < nrows) red_add(dst + (32 + c) * rs, __uint_as_float(v1[c]));
+                    if (64 + c < nrows) red_add(dst + (64 + c) * rs, __uint_as_float(v2[c]));
+                    if (96 + c < nrows) red_add(dst + (96 + c) * rs, __uint_as_float(v3[c]));
                 }
             }
             // dK and dV of the finished key tile (thread = key)
             if (!bwd_warp_wait(bar(L::bDKVFull), (uint32_t)(I & 1), abort_flag, wf, 85, it)) goto done;
             tc_fence_after_sync();
             const int key = w.j * kBwdTile + t;
-            const long long orow = ((long long)w.b * p.Hkv + w.hkv) * p.Lk + key;
+            const long long orow = VARLEN ? (long long)(w.k0 + key) * p.Hkv + w.hkv
+                                          : ((long long)w.b * p.Hkv + w.hkv) * p.Lk + key;
 #pragma unroll
             for (int o = 0; o < 2; ++o) {
                 float* out = (o == 0 ? p.dv : p.dk) + orow * kBwdD;
@@ -342,7 +446,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     uint32_t r[32];
                     tmem_ld32(lane_base + col + c * 32, r);
                     tmem_wait_ld();
-                    if (key < p.Lk) {
+                    if (key < w.lk) {
                         float4* o4 = reinterpret_cast<float4*>(out + c * 32);
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
@@ -364,12 +468,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int t = 32 * (warp & 3) + lane;
         const int ch = (warp - 4) >> 2;  // column half: queries 64ch .. 64ch+63
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const int off = p.Lk - p.Lq;
         uint32_t gstep = 0;
-        for (int k = 0, it = bwd_cta_item<CAUSAL>(0); it < p.num_items; it = bwd_cta_item<CAUSAL>(++k)) {
-            const BwdItem w = bwd_item<CAUSAL>(p, it);
+        for (int k = 0, it = bwd_cta_item<CAUSAL || VARLEN>(0); it < num_items; it = bwd_cta_item<CAUSAL || VARLEN>(++k)) {
+            const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
             const int kpos = w.j * kBwdTile + t;
-            const bool key_ok = kpos < p.Lk;
+            const bool key_ok = kpos < w.lk;
+            const int off = w.lk - w.lq;
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 int h, i;
                 bwd_step(p, w, s, h, i);
@@ -482,35 +586,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             bool drop = p.fault == 1;  // test hook: this CTA's first K/V never arrives
             uint32_t gstep = 0;
             int I = 0;
-            for (int k = 0, it = bwd_cta_item<CAUSAL>(0); it < p.num_items; it = bwd_cta_item<CAUSAL>(++k)) {
-                const BwdItem w = bwd_item<CAUSAL>(p, it);
+            for (int k = 0, it = bwd_cta_item<CAUSAL || VARLEN>(0); it < num_items; it = bwd_cta_item<CAUSAL || VARLEN>(++k)) {
+                const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
                 const int bh_kv = w.b * p.Hkv + w.hkv;
+                // TMA coordinates: dense (x, row, head slab), packed (x, head, token)
+                auto ld_kv = [&](uint32_t dst, const CUtensorMap* map, int x) {
+                    if constexpr (VARLEN)
+                        tma_load_3d(dst, map, bar(L::bKVFull), x, w.hkv, w.k0 + w.j * kBwdTile);
+                    else
+                        tma_load_3d(dst, map, bar(L::bKVFull), x, w.j * kBwdTile, bh_kv);
+                };
                 if (!mbar_wait(bar(L::bKVEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 85, it)) break;
                 if (drop) {
                     drop = false;
                 } else {
                     mbar_arrive_expect_tx(bar(L::bKVFull), 2 * kTileBytes);
                     kv_armed = I & 1;
-                    const int y = w.j * kBwdTile;
-                    tma_load_3d(sb + L::kK, &tmK, bar(L::bKVFull), 0, y, bh_kv);
-                    tma_load_3d(sb + L::kK + kHalf, &tmK, bar(L::bKVFull), 64, y, bh_kv);
-                    tma_load_3d(sb + L::kV, &tmV, bar(L::bKVFull), 0, y, bh_kv);
-                    tma_load_3d(sb + L::kV + kHalf, &tmV, bar(L::bKVFull), 64, y, bh_kv);
+                    ld_kv(sb + L::kK, &tmK, 0);
+                    ld_kv(sb + L::kK + kHalf, &tmK, 64);
+                    ld_kv(sb + L::kV, &tmV, 0);
+                    ld_kv(sb + L::kV + kHalf, &tmV, 64);
                 }
                 bool ok = true;
                 for (int s = 0; s < w.steps; ++s, ++gstep) {
                     int h, i;
                     bwd_step(p, w, s, h, i);
                     const int y = i * kBwdTile, z = w.b * p.Hq + h;
-                    const long long ws_row = (long long)z * p.Lq_pad + y;
+                    const long long ws_row = VARLEN ? (long long)h * p.Lq_pad + w.ws0 + y : (long long)z * p.Lq_pad + y;
+                    // Q/dO coordinates: dense (x, row, head slab), packed (x, head, token)
+                    const int c1 = VARLEN ? h : y, c2 = VARLEN ? w.q0 + y : z;
                     // Q and its lse2 row (3-stage ring: freed after dK)
                     const uint32_t qs = gstep % L::kQStages, qph = (gstep / L::kQStages) & 1u;
                     if (!(ok = mbar_wait(bar(L::bQEmpty + qs), qph ^ 1u, abort_flag, wf, 86, it))) break;
                     mbar_arrive_expect_tx(bar(L::bQFull + qs), kTileBytes + 512);
                     q_armed[qs] = (int)qph;
                     const uint32_t qdst = sb + L::kQ + qs * kTileBytes;
-                    tma_load_3d(qdst, &tmQ, bar(L::bQFull + qs), 0, y, z);
-                    tma_load_3d(qdst + kHalf, &tmQ, bar(L::bQFull + qs), 64, y, z);
+                    tma_load_3d(qdst, &tmQ, bar(L::bQFull + qs), 0, c1, c2);
+                    tma_load_3d(qdst + kHalf, &tmQ, bar(L::bQFull + qs), 64, c1, c2);
                     bulk_load(sb + L::kL2 + qs * 512, p.lse2 + ws_row, 512, bar(L::bQFull + qs));
                     // delta row (2-stage ring: freed by the dS warps)
                     const uint32_t ds = gstep & 1u, dph = (gstep >> 1) & 1u;
@@ -522,8 +634,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (!(ok = mbar_wait(bar(L::bDOEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 88, it))) break;
                     mbar_arrive_expect_tx(bar(L::bDOFull), kTileBytes);
                     do_armed = (int)(gstep & 1u);
-                    tma_load_3d(sb + L::kDO, &tmDO, bar(L::bDOFull), 0, y, z);
-                    tma_load_3d(sb + L::kDO + kHalf, &tmDO, bar(L::bDOFull), 64, y, z);
+                    tma_load_3d(sb + L::kDO, &tmDO, bar(L::bDOFull), 0, c1, c2);
+                    tma_load_3d(sb + L::kDO + kHalf, &tmDO, bar(L::bDOFull), 64, c1, c2);
                 }
                 if (!ok) break;
                 ++I;
@@ -570,8 +682,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t gstep = 0;
         int I = 0;
         bool issued = false, ok = true;
-        for (int k = 0, it = bwd_cta_item<CAUSAL>(0); it < p.num_items && ok; it = bwd_cta_item<CAUSAL>(++k)) {
-            const BwdItem w = bwd_item<CAUSAL>(p, it);
+        for (int k = 0, it = bwd_cta_item<CAUSAL || VARLEN>(0); it < num_items && ok; it = bwd_cta_item<CAUSAL || VARLEN>(++k)) {
+            const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
             if (!(ok = bwd_warp_wait(bar(L::bKVFull), (uint32_t)(I & 1), abort_flag, wf, 89, it))) break;
             {
                 const uint32_t qs = gstep % L::kQStages, qph = (gstep / L::kQStages) & 1u;
@@ -657,8 +769,19 @@ done:
     }
 }
 
-cudaError_t launch_bwd_pre(int D, const BwdParams& p, cudaStream_t stream)
+cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t stream)
 {
+    if (varlen) {
+        const long long r1 = (long long)p.total_q * p.Hq, r2 = (long long)p.Hq * p.Lq_pad,
+                        r3 = (long long)p.total_k * p.Hkv;
+        const long long nb1 = (r1 + 7) / 8, nb2 = nb1 + (r2 + 7) / 8, nb = nb2 + (r3 + 7) / 8;
+        if (nb >= (1ll << 31)) return cudaErrorInvalidValue;
+        if (D == 128)
+            fa_bwd_pre_varlen_kernel<128><<<(int)nb, 256, 0, stream>>>(p, (int)nb1, (int)nb2);
+        else
+            fa_bwd_pre_varlen_kernel<64><<<(int)nb, 256, 0, stream>>>(p, (int)nb1, (int)nb2);
+        return cudaGetLastError();
+    }
     const long long rows = (long long)p.B * p.Hq * p.Lq_pad;
     const int grid = (int)((rows + 7) / 8);
     if (D == 128)
@@ -668,11 +791,13 @@ cudaError_t launch_bwd_pre(int D, const BwdParams& p, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream)
+cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
+                       const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
+                       cudaStream_t stream)
 {
     if (D != kBwdD) return cudaErrorInvalidValue;
-    auto kern = causal ? fa_bwd_sm103_kernel<true> : fa_bwd_sm103_kernel<false>;
+    auto kern = varlen ? (causal ? fa_bwd_sm103_kernel<true, true> : fa_bwd_sm103_kernel<false, true>)
+                       : (causal ? fa_bwd_sm103_kernel<true, false> : fa_bwd_sm103_kernel<false, false>);
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem::kDynamic);
     if (e != cudaSuccess) return e;
     kern<<<grid, kBwdThreads, BwdSmem::kDynamic, stream>>>(q, k, v, dout, p);

@@ -10,19 +10,29 @@ namespace fa {
 
 constexpr int kBwdTile = 128;  // keys per KV tile = query rows per Q tile
 
+// Dense layouts are [B, H, L, D]; packed (varlen) ones [T, H, D] with LSE
+// [Hq, Tq], as in the forward.
 struct BwdParams {
     // preprocess inputs
-    const float* o;         // [B, Hq, Lq, D] forward output
-    const float* lse;       // [B, Hq, Lq] natural log
-    const uint16_t* dout;   // bf16 [B, Hq, Lq, D]
+    const float* o;         // forward output (fp32)
+    const float* lse;       // forward LSE, natural log
+    const uint16_t* dout;   // bf16, layout of Q
     // outputs (fp32)
-    float* dq;              // [B, Hq, Lq, D]  zeroed by the preprocess kernel, then accumulated
-    float* dk;              // [B, Hkv, Lk, D]
-    float* dv;              // [B, Hkv, Lk, D]
-    // workspace, [B * Hq][Lq_pad] each
+    float* dq;              // layout of Q; zeroed by the preprocess kernel, then accumulated
+    float* dk;              // layout of K
+    float* dv;              // layout of V
+    // workspace, [B * Hq][Lq_pad] each (varlen: [Hq][Lq_pad], every sequence's
+    // rows padded to a multiple of 128, starting at its padded row offset)
     float* delta;           // rowsum(O * dO); 0 on padding rows
     float* lse2;            // LSE * log2(e); +inf on rows without keys and on padding rows
     int B, Hq, Hkv, Lq, Lk, Lq_pad, group;
+    // packed batches: sequence offsets (int32, device) and the schedule built
+    // by the varlen schedule kernel (item prefix, order, items by sequence,
+    // padded row offsets)
+    const int* cu_q;
+    const int* cu_k;
+    const int* sched;
+    int num_seqs, total_q, total_k;
     int num_kv_tiles;       // ceil(Lk / 128)
     int num_q_tiles;        // ceil(Lq / 128)
     int num_items;          // B * Hkv * num_kv_tiles
@@ -34,8 +44,9 @@ struct BwdParams {
     int fault;              // test hook: 1 = skip the first K/V load of every CTA
 };
 
-cudaError_t launch_bwd_pre(int D, const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
+                       const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
+                       cudaStream_t stream);
 
 }  // namespace fa

@@ -297,6 +297,36 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const float* o, 
 fa_status_t fa_bwd_workspace(int B, int Hq, int Lq, size_t* workspace_bytes);
 
 /*
+ * Backward of a packed (variable-length) batch: the gradients of fa_fwd_varlen,
+ * each sequence an independent problem with its own bottom-right causal
+ * alignment.
+ *
+ *   q, dout [total_q, Hq, D], k, v [total_k, Hkv, D]: bf16
+ *   o [total_q, Hq, D], lse [Hq, total_q]: fp32 (fa_fwd_varlen's outputs)
+ *   dq [total_q, Hq, D], dk/dv [total_k, Hkv, D]: fp32 outputs, fully
+ *     overwritten (zero for sequences without keys / without query rows)
+ *   cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k: as fa_fwd_varlen
+ *     (invalid offsets latch FA_ERR_INVALID_ARG on the device, read by fa_check)
+ *   workspace: DEVICE memory of at least fa_bwd_varlen_workspace bytes,
+ *     16-byte aligned, owned by the caller (row statistics and the schedule);
+ *     calls that overlap on the GPU need separate workspaces.
+ *   D must be 128 (FA_ERR_UNSUPPORTED otherwise).
+ *
+ * Launches 3 kernels: the schedule (sequences longest query range first), the
+ * preprocess and the gradient kernel.  No device memory is allocated.
+ */
+fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                          const void* dout, float* dq, float* dk, float* dv, const int* cu_seqlens_q,
+                          const int* cu_seqlens_k, int num_seqs, int total_q, int total_k,
+                          int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D, int causal,
+                          float softmax_scale, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+/* Workspace bytes fa_bwd_varlen needs for num_seqs sequences of total_q query
+ * tokens and Hq query heads, written to *workspace_bytes. */
+fa_status_t fa_bwd_varlen_workspace(int num_seqs, int total_q, int Hq, size_t* workspace_bytes);
+
+/*
  * Synchronises `stream`, then returns and clears the device-side error latch
  * of the current device: FA_ERR_TIMEOUT or FA_ERR_INVALID_ARG from an earlier
  * launch, or FA_ERR_CUDA when a kernel found its launch configuration unusable

@@ -181,3 +181,27 @@ def test_hdim_argument_validation(lib):
     assert vcall(Dv=-1) == INV
     assert vcall(D=128, Dv=192) == UNS
     assert lib.fa_last_launch_count() == 0
+
+
+def test_bwd_varlen_argument_validation(lib):
+    INV, UNS = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+
+    def call(cu_q=32, dq=16, ws=16, n=2, tq=10, tk=10, mq=8, mk=8, Hq=2, Hkv=1, D=128, scale=0.1, wsb=1 << 20):
+        return lib.fa_bwd_varlen(16, 16, 16, 16, 16, 16, dq, 16, 16, cu_q, 32, n, tq, tk, mq, mk, Hq, Hkv, D, 1,
+                                 scale, ws, wsb, None)
+
+    assert call(cu_q=None) == INV
+    assert call(dq=None) == INV
+    assert call(ws=None) == INV
+    assert call(n=0) == INV
+    assert call(tk=0) == INV
+    assert call(Hq=3, Hkv=2) == INV
+    assert call(cu_q=34) == INV                      # int32 offsets must be 4-byte aligned
+    assert call(wsb=64) == INV                       # workspace too small
+    assert call(D=64) == UNS
+    n = ctypes.c_size_t(0)
+    assert lib.fa_bwd_varlen_workspace(3, 1000, 4, ctypes.byref(n)) == fa.FA_OK
+    rows = (1000 + 127) // 128 * 128 + 128 * 3       # each sequence padded to 128 rows
+    assert n.value >= 2 * 4 * rows * 4 + 4 * (4 * 3 + 3)
+    assert lib.fa_bwd_varlen_workspace(0, 1000, 4, ctypes.byref(n)) == INV
+    assert lib.fa_last_launch_count() == 0

@@ -109,3 +109,56 @@ def test_bwd_timed_out_wait_is_reported_and_context_survives():
     assert ei.value.status == fa.FA_ERR_TIMEOUT
     got = run_bwd(q, k, v, do, False)
     compare_grads(got, attention_bwd(q, k, v, do, 1 / math.sqrt(128), False), "after timeout")
+
+
+# ------------------------------------------------------------------ packed batches
+
+VARLEN_CASES = [
+    # query lengths, key lengths, Hq, Hkv, causal
+    ([1, 127, 128, 129, 300, 5], [1, 127, 128, 129, 300, 5], 4, 2, True),
+    ([1, 127, 128, 129, 300, 5], [1, 127, 128, 129, 300, 5], 4, 2, False),
+    ([50, 700, 3, 256], [90, 650, 3, 300], 4, 4, True),      # Lq != Lk per sequence
+    ([200, 0, 100, 64], [200, 40, 0, 64], 2, 1, True),       # no query rows / no keys
+    ([513, 7, 1024], [513, 7, 1024], 8, 2, False),
+]
+
+
+@pytest.mark.parametrize("lq,lk,Hq,Hkv,causal", VARLEN_CASES)
+def test_bwd_varlen_full_compare(lq, lk, Hq, Hkv, causal):
+    from oracle.backward import attention_bwd_varlen
+    D = 128
+    Tq, Tk = sum(lq), sum(lk)
+    seed = Tq + 3 * Tk + Hq
+    q, k, v = random_inputs((Tq, Hq, D), (Tk, Hkv, D), seed=seed)
+    do = grad_output((Tq, Hq, D), seed)
+    cq = torch.tensor([0] + np.cumsum(lq).tolist(), dtype=torch.int32, device=DEV)
+    ck = torch.tensor([0] + np.cumsum(lk).tolist(), dtype=torch.int32, device=DEV)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = fa.fa_fwd_varlen(qd, kd, vd, cq, ck, max(lq), max(max(lk), 1), causal=causal)
+    # outputs start as NaN: every element must be written
+    dq = torch.full((Tq, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    dk = torch.full((Tk, Hkv, D), float("nan"), dtype=torch.float32, device=DEV)
+    dv = torch.full((Tk, Hkv, D), float("nan"), dtype=torch.float32, device=DEV)
+    fa.fa_bwd_varlen(qd, kd, vd, o, lse, dod, cq, ck, max(lq), max(max(lk), 1), causal=causal,
+                     dq=dq, dk=dk, dv=dv)
+    fa.fa_check()
+    assert fa.fa_last_launch_count() == 3
+    ref = attention_bwd_varlen(q, k, v, do, cq.cpu().numpy(), ck.cpu().numpy(), 1 / math.sqrt(D), causal)
+    compare_grads((dq.cpu().numpy(), dk.cpu().numpy(), dv.cpu().numpy()), ref, f"varlen bwd {lq} {lk}")
+
+
+def test_bwd_varlen_single_sequence_equals_dense():
+    # one packed sequence is the dense problem with B = 1 (layouts transposed)
+    Hq, Hkv, L, D = 4, 2, 333, 128
+    q, k, v = random_inputs((1, Hq, L, D), (1, Hkv, L, D), seed=21)
+    do = grad_output((1, Hq, L, D), 21)
+    a = run_bwd(q, k, v, do, True)
+    pk = [t[0].permute(1, 0, 2).contiguous().to(DEV) for t in (q, k, v, do)]
+    cu = torch.tensor([0, L], dtype=torch.int32, device=DEV)
+    o, lse = fa.fa_fwd_varlen(pk[0], pk[1], pk[2], cu, cu, L, L, causal=True)
+    dq, dk, dv = fa.fa_bwd_varlen(pk[0], pk[1], pk[2], o, lse, pk[3], cu, cu, L, L, causal=True)
+    fa.fa_check()
+    # dK and dV have the same summation order in both layouts: bit-identical
+    assert np.array_equal(dk.cpu().numpy(), a[1][0].transpose(1, 0, 2))
+    assert np.array_equal(dv.cpu().numpy(), a[2][0].transpose(1, 0, 2))
+    assert np.abs(dq.cpu().numpy() - a[0][0].transpose(1, 0, 2)).max() <= 1e-4 * np.abs(a[0]).max()

@@ -248,22 +248,32 @@ def _cpu_backward_rate(w, inputs, seconds: float):
     import oracle
     from oracle.backward import attention_bwd
     from workloads import grad_output
-    q, k, v = inputs
-    do = grad_output(tuple(q.shape), w.seed)
+    if w.varlen:
+        # the first sequence of the packed batch, as a dense [1, H, L, D] problem
+        q, k, v, cq, ck = inputs
+        do = grad_output(tuple(q.shape), w.seed)
+        q0, q1, k0, k1 = int(cq[0]), int(cq[1]), int(ck[0]), int(ck[1])
+        q, do = (t[q0:q1].permute(1, 0, 2)[None] for t in (q, do))
+        k, v = (t[k0:k1].permute(1, 0, 2)[None] for t in (k, v))
+        Lq, Lk, what = q1 - q0, k1 - k0, "the first sequence, "
+    else:
+        q, k, v = inputs
+        do = grad_output(tuple(q.shape), w.seed)
+        Lq, Lk, what = w.Lq, w.Lk, ""
 
     def run(n):
-        sl = slice(w.Lq - n, w.Lq)
+        sl = slice(Lq - n, Lq)
         t0 = time.perf_counter()
         attention_bwd(q[:1, :1, sl], k[:1, :1], v[:1, :1], do[:1, :1, sl], w.scale, w.causal)
         dt = time.perf_counter() - t0
-        rows = np.arange(w.Lq - n, w.Lq)
-        pairs = np.minimum(rows + 1 + (w.Lk - w.Lq), w.Lk).clip(0).sum() if w.causal else n * w.Lk
+        rows = np.arange(Lq - n, Lq)
+        pairs = np.minimum(rows + 1 + (Lk - Lq), Lk).clip(0).sum() if w.causal else n * Lk
         return dt, 10.0 * w.D * float(pairs)
-    n = min(w.Lq, 64)
+    n = min(Lq, 64)
     dt, _ = run(n)
-    n = int(min(w.Lq, max(n, n * seconds / max(dt, 1e-6))))
+    n = int(min(Lq, max(n, n * seconds / max(dt, 1e-6))))
     dt, fl = run(n)
-    return fl / dt / 1e12, oracle.num_cpus(), f"backward of the last {n} query rows of one head ({dt:.1f} s)"
+    return fl / dt / 1e12, oracle.num_cpus(), f"backward of {what}the last {n} query rows of one head ({dt:.1f} s)"
 
 
 def _cpu_variant_rate(w, inputs, seconds: float):
@@ -345,7 +355,22 @@ def main(argv=None):
 
     # inputs resident in HBM (seeded on the CPU, copied once)
     host_inputs = varlen_inputs(w) if w.varlen else dense_inputs(w)
-    if w.varlen:
+    if w.varlen and w.bwd:
+        from workloads import grad_output
+        q, k, v, cq, ck = (t.to(dev) for t in host_inputs)
+        maxl = max(w.seqlens)
+        do = grad_output(tuple(q.shape), w.seed).to(dev)
+        o_f, lse_f = fa.fa_fwd_varlen(q, k, v, cq, ck, maxl, maxl, causal=w.causal)  # computed once
+        dk_b = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        dv_b = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        ws_b = torch.empty(fa.bwd_varlen_workspace(len(w.seqlens), q.shape[0], w.Hq), dtype=torch.uint8,
+                           device=dev)
+
+        def step(o=None, lse=None, qq=q, kk=k, vv=v):  # o receives dQ
+            return fa.fa_bwd_varlen(qq, kk, vv, o_f, lse_f, do, cq, ck, maxl, maxl, causal=w.causal, dq=o,
+                                    dk=dk_b, dv=dv_b, workspace=ws_b)
+        out_shape, lse_shape = tuple(q.shape), (w.Hq, q.shape[0])
+    elif w.varlen:
         q, k, v, cq, ck = (t.to(dev) for t in host_inputs)
         maxl = max(w.seqlens)
 
@@ -445,7 +470,7 @@ def main(argv=None):
     e2e = None
     if not args.no_e2e:
         e2e_in = list(host_inputs)
-        if w.bwd:  # the backward's own inputs: Q, K, V, dO and the forward's O and LSE
+        if w.bwd:  # the backward's own inputs: Q, K, V (cu_seqlens), dO and the forward's O and LSE
             e2e_in += [do.cpu(), o_f.cpu(), lse_f.cpu()]
         pin = [t.pin_memory() for t in e2e_in]
         h_o = torch.empty(out_shape, dtype=torch.float32).pin_memory()
@@ -458,7 +483,10 @@ def main(argv=None):
         def e2e_step():
             for d, h in zip(d_in, pin):
                 d.copy_(h, non_blocking=True)
-            if w.varlen:
+            if w.varlen and w.bwd:  # Q, K, V, cu_q, cu_k, dO, O, LSE
+                fa.fa_bwd_varlen(d_in[0], d_in[1], d_in[2], d_in[6], d_in[7], d_in[5], d_in[3], d_in[4], maxl, maxl,
+                                 causal=w.causal, dq=o, dk=dk_b, dv=dv_b, workspace=ws_b)
+            elif w.varlen:
                 fa.fa_fwd_varlen(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], maxl, maxl, causal=w.causal,
                                  out=o, lse=lse)
             elif w.decode:
@@ -531,8 +559,10 @@ def main(argv=None):
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": profiled_traffic(w.name, BWD_SOURCES, "fa_bwd"),
                     "peak_kind": f"{peak_kind} burst bf16 GEMM", "frac_of_sustained": achieved / peak_sus,
-                    "kernel": "fa_bwd_pre_kernel<%d> + fa_bwd_sm103_kernel<%s>" % (w.D, str(w.causal).lower()),
-                    "timed": "whole step (both launches)"}
+                    "kernel": ("fa_varlen_schedule_kernel + fa_bwd_pre_varlen_kernel<%d> + fa_bwd_sm103_kernel<%s,true>"
+                               if w.varlen else "fa_bwd_pre_kernel<%d> + fa_bwd_sm103_kernel<%s,false>")
+                              % (w.D, str(w.causal).lower()),
+                    "timed": "whole step (all launches)"}
     else:
         achieved = flops_step / (secs / args.steps) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

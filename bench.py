@@ -549,7 +549,7 @@ def main(argv=None):
         achieved = flops_step / (secs / args.steps) / 1e12
         peak8 = peak * 2.0
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak8, "unit": "TFLOP/s",
-                    "frac": achieved / peak8, "traffic": None,
+                    "frac": achieved / peak8, "traffic": profiled_traffic(w.name),
                     "peak_kind": f"{peak_kind} burst bf16 GEMM x 2 (nominal e4m3/bf16 ratio)",
                     "frac_of_bf16_peak": achieved / peak,
                     "kernel": "fa_fwd_sm103_kernel<128,%s,false,4>" % str(w.causal).lower()}

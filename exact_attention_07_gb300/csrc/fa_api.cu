@@ -708,6 +708,23 @@ extern "C" fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* 
 
 namespace {
 long long bwd_rows_padded(int Lq) { return ((long long)Lq + kBwdTile - 1) / kBwdTile * kBwdTile; }
+
+// (batch, KV head) slabs per scheduling section of the backward: the dQ
+// (fp32), Q and dO (bf16) of a section's query heads, 1 KB per query row at
+// D = 128, should fit in half of the L2.  Sections break the longest-first
+// order of the item list, so they are used only when every CTA gets many
+// items (measured: with about 3 items per CTA, a causal GQA problem lost a
+// quarter of its speed to imbalance).
+int bwd_heads_per_section(int slabs, int group, long long Lq, long long items, int num_sms)
+{
+    constexpr long long kBudget = 64ll << 20;
+    if (items < 8ll * num_sms) return slabs;
+    const long long per = (long long)group * Lq * 1024;
+    long long hs = per > 0 ? kBudget / per : slabs;
+    if (hs < 1) hs = 1;
+    if (hs > slabs) hs = slabs;
+    return (int)hs;
+}
 }  // namespace
 
 extern "C" fa_status_t fa_bwd_workspace(int B, int Hq, int Lq, size_t* workspace_bytes)
@@ -772,6 +789,7 @@ extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const
     p.num_kv_tiles = (int)kv_tiles;
     p.num_q_tiles = (int)(lq_pad / kBwdTile);
     p.num_items = (int)items;
+    p.heads_per_section = bwd_heads_per_section(B * Hkv, Hq / Hkv, Lq, items, ds->num_sms);
     p.scale = softmax_scale;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
     p.causal = causal != 0;
@@ -880,6 +898,7 @@ extern "C" fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v
     p.num_seqs = num_seqs;
     p.total_q = total_q;
     p.total_k = total_k;
+    p.heads_per_section = bwd_heads_per_section(Hkv, Hq / Hkv, max_seqlen_q, ub, ds->num_sms);
     p.scale = softmax_scale;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
     p.causal = causal != 0;

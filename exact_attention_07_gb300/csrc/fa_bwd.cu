@@ -260,13 +260,26 @@ struct BwdItem {
     int ws0;            // packed batches: the sequence's padded workspace row offset
 };
 
+// Item r of `slabs` (batch, KV head) slabs of nk key tiles each, in sections
+// of hs slabs: section outer, key tile next (longest items first under
+// causal), slab innermost.  The items in flight then reduce into the dQ of
+// one section's heads only, which stays in L2 between the key tiles.
+__device__ __forceinline__ void bwd_section_order(int r, int slabs, int nk, int hs, int& j, int& slab)
+{
+    const int sec = r / (hs * nk);
+    const int rem = r - sec * hs * nk;
+    const int cur = min(hs, slabs - sec * hs);
+    j = rem / cur;
+    slab = sec * hs + (rem - j * cur);
+}
+
 template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int it)
 {
     BwdItem w;
     if constexpr (VARLEN) {
-        // sequences longest query range first; inside one, key tiles in
-        // order (longest items first under causal), KV heads innermost
+        // sequences longest query range first; inside one, KV heads in
+        // sections, key tiles in order
         const int n = p.num_seqs;
         const int lo = bwd_upper_index(p.sched + 1, n, it);
         const int s = __ldg(p.sched + 2 + n + lo);
@@ -276,14 +289,12 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int it)
         w.k0 = __ldg(p.cu_k + s);
         w.lk = __ldg(p.cu_k + s + 1) - w.k0;
         w.ws0 = __ldg(p.sched + 3 * n + 2 + s);
-        w.j = rem / p.Hkv;
-        w.hkv = rem - w.j * p.Hkv;
+        bwd_section_order(rem, p.Hkv, (w.lk + kBwdTile - 1) / kBwdTile, p.heads_per_section, w.j, w.hkv);
         w.b = 0;
         w.nq = (w.lq + kBwdTile - 1) / kBwdTile;
     } else {
-        const int bh_count = p.B * p.Hkv;
-        w.j = it / bh_count;  // longest items (smallest key tile under causal) first
-        const int bh = it - w.j * bh_count;
+        int bh;
+        bwd_section_order(it, p.B * p.Hkv, p.num_kv_tiles, p.heads_per_section, w.j, bh);
         w.b = bh / p.Hkv;
         w.hkv = bh - w.b * p.Hkv;
         w.nq = p.num_q_tiles;

@@ -36,6 +36,7 @@ struct BwdParams {
     int num_kv_tiles;       // ceil(Lk / 128)
     int num_q_tiles;        // ceil(Lq / 128)
     int num_items;          // B * Hkv * num_kv_tiles
+    int heads_per_section;  // (batch, KV head) slabs whose items are interleaved (L2-sized dQ working set)
     float scale;            // softmax_scale (multiplies dS)
     float scale_log2;       // softmax_scale * log2(e)
     int causal;

@@ -401,6 +401,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const int num_items = VARLEN ? __ldg(p.sched) : p.num_items;
+    constexpr bool kAlt = CAUSAL || VARLEN;  // items of unequal length: alternate the rounds
 
     if (warp < 4) {
         // ============================================================ dQ reduction, dK/dV epilogue
@@ -411,7 +412,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         uint32_t gstep = 0;
         int I = 0;
-        for (int k = 0, it = bwd_cta_item<CAUSAL || VARLEN>(0); it < num_items; it = bwd_cta_item<CAUSAL || VARLEN>(++k)) {
+        for (int k = 0, it = bwd_cta_item<kAlt>(0); it < num_items; it = bwd_cta_item<kAlt>(++k)) {
             const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 int h, i;
@@ -480,7 +481,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int ch = (warp - 4) >> 2;  // column half: queries 64ch .. 64ch+63
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         uint32_t gstep = 0;
-        for (int k = 0, it = bwd_cta_item<CAUSAL || VARLEN>(0); it < num_items; it = bwd_cta_item<CAUSAL || VARLEN>(++k)) {
+        for (int k = 0, it = bwd_cta_item<kAlt>(0); it < num_items; it = bwd_cta_item<kAlt>(++k)) {
             const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
             const int kpos = w.j * kBwdTile + t;
             const bool key_ok = kpos < w.lk;
@@ -597,7 +598,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             bool drop = p.fault == 1;  // test hook: this CTA's first K/V never arrives
             uint32_t gstep = 0;
             int I = 0;
-            for (int k = 0, it = bwd_cta_item<CAUSAL || VARLEN>(0); it < num_items; it = bwd_cta_item<CAUSAL || VARLEN>(++k)) {
+            for (int k = 0, it = bwd_cta_item<kAlt>(0); it < num_items; it = bwd_cta_item<kAlt>(++k)) {
                 const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
                 const int bh_kv = w.b * p.Hkv + w.hkv;
                 // TMA coordinates: dense (x, row, head slab), packed (x, head, token)
@@ -693,7 +694,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t gstep = 0;
         int I = 0;
         bool issued = false, ok = true;
-        for (int k = 0, it = bwd_cta_item<CAUSAL || VARLEN>(0); it < num_items && ok; it = bwd_cta_item<CAUSAL || VARLEN>(++k)) {
+        for (int k = 0, it = bwd_cta_item<kAlt>(0); it < num_items && ok; it = bwd_cta_item<kAlt>(++k)) {
             const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
             if (!(ok = bwd_warp_wait(bar(L::bKVFull), (uint32_t)(I & 1), abort_flag, wf, 89, it))) break;
             {

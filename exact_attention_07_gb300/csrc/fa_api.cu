@@ -710,16 +710,16 @@ namespace {
 long long bwd_rows_padded(int Lq) { return ((long long)Lq + kBwdTile - 1) / kBwdTile * kBwdTile; }
 
 // (batch, KV head) slabs per scheduling section of the backward: the dQ
-// (fp32), Q and dO (bf16) of a section's query heads, 1 KB per query row at
-// D = 128, should fit in half of the L2.  Sections break the longest-first
+// (fp32), Q and dO (bf16) of a section's query heads, 8 * D bytes per query
+// row, should fit in half of the L2.  Sections break the longest-first
 // order of the item list, so they are used only when every CTA gets many
 // items (measured: with about 3 items per CTA, a causal GQA problem lost a
 // quarter of its speed to imbalance).
-int bwd_heads_per_section(int slabs, int group, long long Lq, long long items, int num_sms)
+int bwd_heads_per_section(int slabs, int group, long long Lq, int D, long long items, int num_sms)
 {
     constexpr long long kBudget = 64ll << 20;
     if (items < 8ll * num_sms) return slabs;
-    const long long per = (long long)group * Lq * 1024;
+    const long long per = (long long)group * Lq * 8 * D;
     long long hs = per > 0 ? kBudget / per : slabs;
     if (hs < 1) hs = 1;
     if (hs > slabs) hs = slabs;
@@ -748,7 +748,7 @@ extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
         return FA_ERR_INVALID_ARG;
-    if (D != 128) return FA_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
     const long long lq_pad = bwd_rows_padded(Lq);
     const long long rows = (long long)B * Hq * lq_pad;
     if (rows >= (1ll << 31) || (long long)B * Hq >= (1ll << 31)) return FA_ERR_INVALID_ARG;
@@ -789,7 +789,7 @@ extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const
     p.num_kv_tiles = (int)kv_tiles;
     p.num_q_tiles = (int)(lq_pad / kBwdTile);
     p.num_items = (int)items;
-    p.heads_per_section = bwd_heads_per_section(B * Hkv, Hq / Hkv, Lq, items, ds->num_sms);
+    p.heads_per_section = bwd_heads_per_section(B * Hkv, Hq / Hkv, Lq, D, items, ds->num_sms);
     p.scale = softmax_scale;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
     p.causal = causal != 0;
@@ -854,7 +854,7 @@ extern "C" fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
         (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
         return FA_ERR_INVALID_ARG;
-    if (D != 128) return FA_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
     BwdVarlenLayout lay;
     if (!bwd_varlen_layout(num_seqs, total_q, Hq, &lay) || workspace_bytes < lay.bytes) return FA_ERR_INVALID_ARG;
     // upper bound of the work items: sum_s ceil(Lk_s / 128) <= total_k / 128 + num_seqs
@@ -898,7 +898,7 @@ extern "C" fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v
     p.num_seqs = num_seqs;
     p.total_q = total_q;
     p.total_k = total_k;
-    p.heads_per_section = bwd_heads_per_section(Hkv, Hq / Hkv, max_seqlen_q, ub, ds->num_sms);
+    p.heads_per_section = bwd_heads_per_section(Hkv, Hq / Hkv, max_seqlen_q, D, ub, ds->num_sms);
     p.scale = softmax_scale;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
     p.causal = causal != 0;

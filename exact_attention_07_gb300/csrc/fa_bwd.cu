@@ -172,18 +172,21 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_varlen_kernel(const BwdParams 
 
 namespace {
 
-constexpr int kBwdD = 128;
 constexpr int kBwdThreads = 512;
-constexpr int kTileBytes = kBwdTile * kBwdD * 2;  // 32 KB
-constexpr int kHalf = kTileBytes / 2;             // one 64-column box
+constexpr int kBox = kBwdTile * 64 * 2;  // one 64-column box of 128 rows (16 KB), a 128-byte swizzle block
 
+// Shared memory and tensor memory of the gradient kernel for head dimension D.
+template <int D>
 struct BwdSmem {
-    static constexpr int kK = 0, kV = kTileBytes;
+    static constexpr int kTile = kBwdTile * D * 2;             // one 128-row tile of Q, K, V or dO
+    static constexpr int kBoxes = kTile / kBox;                // 64-column boxes per tile
+    static constexpr int kDSBytes = kBwdTile * kBwdTile * 2;   // dS^T [128 keys][128 queries] bf16
+    static constexpr int kK = 0, kV = kTile;
     static constexpr int kQStages = 3;
-    static constexpr int kQ = 2 * kTileBytes;                  // [3] Q tiles
-    static constexpr int kDO = kQ + kQStages * kTileBytes;     // dO tile (one stage: free after P.V)
-    static constexpr int kDS = kDO + kTileBytes;               // dS^T [128 keys][128 queries] bf16
-    static constexpr int kL2 = kDS + kTileBytes;               // [3] lse2 rows (fp32 x 128), with Q
+    static constexpr int kQ = 2 * kTile;                       // [3] Q tiles
+    static constexpr int kDO = kQ + kQStages * kTile;          // dO tile (one stage: free after P.V)
+    static constexpr int kDS = kDO + kTile;                    // dS^T
+    static constexpr int kL2 = kDS + kDSBytes;                 // [3] lse2 rows (fp32 x 128), with Q
     static constexpr int kDL = kL2 + kQStages * 512;           // [2] delta rows (fp32 x 128)
     static constexpr int kBars = kDL + 2 * 512;
     static constexpr int bKVFull = 0, bKVEmpty = 1, bQFull = 2, bQEmpty = 5, bDOFull = 8, bDOEmpty = 9,
@@ -195,10 +198,15 @@ struct BwdSmem {
     // all the shared memory a CTA may have; the part beyond kBytes absorbs the
     // alignment of the dynamic window to 1024 bytes (checked at run time)
     static constexpr int kDynamic = 232448;
+    static_assert(kBytes <= kDynamic, "shared memory of one CTA");
+    // Tensor memory columns: S^T (then P^T), dP^T, dV, dK.  D = 128: dQ^T
+    // (lanes = head dimension) reuses the dP^T columns; D = 64: dQ (lanes =
+    // query rows, 64 columns) has columns of its own.
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    static constexpr uint32_t kColDQ = D == 128 ? kColDP : 256 + 2 * D;
 };
-static_assert(BwdSmem::kDynamic <= 232448, "shared memory of one CTA");
 
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384, kBwdTmemCols = 512;
+constexpr uint32_t kBwdTmemCols = 512;
 
 __device__ __forceinline__ void bwd_tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
 {
@@ -224,6 +232,13 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 __device__ __forceinline__ void red_add(float* addr, float a)
 {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
+
+// Four consecutive fp32 reductions in one request (16-byte aligned address).
+__device__ __forceinline__ void red_add4(float* addr, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
 }
 
 // Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
@@ -339,13 +354,16 @@ __device__ __forceinline__ void bwd_step(const BwdParams& p, const BwdItem& w, i
 
 // ------------------------------------------------------------------ main kernel
 
-template <bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                         const BwdParams p)
 {
-    using L = BwdSmem;
+    using L = BwdSmem<D>;
+    constexpr uint32_t kColS = L::kColS, kColDP = L::kColDP, kColDV = L::kColDV, kColDK = L::kColDK,
+                       kColDQ = L::kColDQ;
+    constexpr int kHalf = kBox;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
@@ -405,8 +423,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp < 4) {
         // ============================================================ dQ reduction, dK/dV epilogue
-        // Thread t owns TMEM lane t: head dimension t of the dQ^T partial (its
-        // 128 columns are the Q tile's rows), key t for dK and dV.
+        // Thread t owns TMEM lane t.  D = 128: head dimension t of the dQ^T
+        // partial (its 128 columns are the Q tile's rows); D = 64: query row t
+        // of the dQ partial (64 columns).  Key t for dK and dV.
         regs_increase<192>();
         const int t = threadIdx.x;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
@@ -419,28 +438,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bwd_step(p, w, s, h, i);
                 if (!bwd_warp_wait(bar(L::bDQFull), gstep & 1u, abort_flag, wf, 84, it)) goto done;
                 tc_fence_after_sync();
-                uint32_t v0[32], v1[32], v2[32], v3[32];
-                tmem_ld32(lane_base + kColDP, v0);
-                tmem_ld32(lane_base + kColDP + 32, v1);
-                tmem_ld32(lane_base + kColDP + 64, v2);
-                tmem_ld32(lane_base + kColDP + 96, v3);
-                tmem_wait_ld();
-                tc_fence_before_sync();
-                mbar_arrive(bar(L::bDQEmpty));
-                // each warp instruction adds 128 contiguous bytes of one dQ row
                 const int q0 = i * kBwdTile;
                 const int nrows = min(kBwdTile, w.lq - q0);
                 // dQ rows: dense [B, Hq, Lq, D], packed [Tq, Hq, D]
-                const long long rs = VARLEN ? (long long)p.Hq * kBwdD : kBwdD;
-                float* dst = p.dq + t +
-                             (VARLEN ? ((long long)(w.q0 + q0) * p.Hq + h) * kBwdD
-                                     : (((long long)w.b * p.Hq + h) * p.Lq + q0) * kBwdD);
+                const long long rs = VARLEN ? (long long)p.Hq * D : D;
+                float* dst = p.dq + (VARLEN ? ((long long)(w.q0 + q0) * p.Hq + h) * D
+                                            : (((long long)w.b * p.Hq + h) * p.Lq + q0) * D);
+                if constexpr (D == 128) {
+                    uint32_t v0[32], v1[32], v2[32], v3[32];
+                    tmem_ld32(lane_base + kColDQ, v0);
+                    tmem_ld32(lane_base + kColDQ + 32, v1);
+                    tmem_ld32(lane_base + kColDQ + 64, v2);
+                    tmem_ld32(lane_base + kColDQ + 96, v3);
+                    tmem_wait_ld();
+                    tc_fence_before_sync();
+                    mbar_arrive(bar(L::bDQEmpty));
+                    // each warp instruction adds 128 contiguous bytes of one dQ row
+                    dst += t;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    if (c < nrows) red_add(dst + c * rs, __uint_as_float(v0[c]));
-                    if (32 + c < nrows) red_add(dst + (32 + c) * rs, __uint_as_float(v1[c]));
-                    if (64 + c < nrows) red_add(dst + (64 + c) * rs, __uint_as_float(v2[c]));
-                    if (96 + c < nrows) red_add(dst + (96 + c) * rs, __uint_as_float(v3[c]));
+                    for (int c = 0; c < 32; ++c) {
+                        if (c < nrows) red_add(dst + c * rs, __uint_as_float(v0[c]));
+                        if (32 + c < nrows) red_add(dst + (32 + c) * rs, __uint_as_float(v1[c]));
+                        if (64 + c < nrows) red_add(dst + (64 + c) * rs, __uint_as_float(v2[c]));
+                        if (96 + c < nrows) red_add(dst + (96 + c) * rs, __uint_as_float(v3[c]));
+                    }
+                } else {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(lane_base + kColDQ, v0);
+                    tmem_ld32(lane_base + kColDQ + 32, v1);
+                    tmem_wait_ld();
+                    tc_fence_before_sync();
+                    mbar_arrive(bar(L::bDQEmpty));
+                    // thread t adds query row t: 16-byte vector reductions
+                    if (t < nrows) {
+                        float* row = dst + t * rs;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            red_add4(row + 4 * c, __uint_as_float(v0[4 * c]), __uint_as_float(v0[4 * c + 1]),
+                                     __uint_as_float(v0[4 * c + 2]), __uint_as_float(v0[4 * c + 3]));
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            red_add4(row + 32 + 4 * c, __uint_as_float(v1[4 * c]), __uint_as_float(v1[4 * c + 1]),
+                                     __uint_as_float(v1[4 * c + 2]), __uint_as_float(v1[4 * c + 3]));
+                    }
                 }
             }
             // dK and dV of the finished key tile (thread = key)
@@ -451,10 +491,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                           : ((long long)w.b * p.Hkv + w.hkv) * p.Lk + key;
 #pragma unroll
             for (int o = 0; o < 2; ++o) {
-                float* out = (o == 0 ? p.dv : p.dk) + orow * kBwdD;
+                float* out = (o == 0 ? p.dv : p.dk) + orow * D;
                 const uint32_t col = o == 0 ? kColDV : kColDK;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(lane_base + col + c * 32, r);
                     tmem_wait_ld();
@@ -612,12 +652,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (drop) {
                     drop = false;
                 } else {
-                    mbar_arrive_expect_tx(bar(L::bKVFull), 2 * kTileBytes);
+                    mbar_arrive_expect_tx(bar(L::bKVFull), 2 * L::kTile);
                     kv_armed = I & 1;
-                    ld_kv(sb + L::kK, &tmK, 0);
-                    ld_kv(sb + L::kK + kHalf, &tmK, 64);
-                    ld_kv(sb + L::kV, &tmV, 0);
-                    ld_kv(sb + L::kV + kHalf, &tmV, 64);
+#pragma unroll
+                    for (int bx = 0; bx < L::kBoxes; ++bx) {
+                        ld_kv(sb + L::kK + bx * kBox, &tmK, 64 * bx);
+                        ld_kv(sb + L::kV + bx * kBox, &tmV, 64 * bx);
+                    }
                 }
                 bool ok = true;
                 for (int s = 0; s < w.steps; ++s, ++gstep) {
@@ -630,11 +671,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // Q and its lse2 row (3-stage ring: freed after dK)
                     const uint32_t qs = gstep % L::kQStages, qph = (gstep / L::kQStages) & 1u;
                     if (!(ok = mbar_wait(bar(L::bQEmpty + qs), qph ^ 1u, abort_flag, wf, 86, it))) break;
-                    mbar_arrive_expect_tx(bar(L::bQFull + qs), kTileBytes + 512);
+                    mbar_arrive_expect_tx(bar(L::bQFull + qs), L::kTile + 512);
                     q_armed[qs] = (int)qph;
-                    const uint32_t qdst = sb + L::kQ + qs * kTileBytes;
-                    tma_load_3d(qdst, &tmQ, bar(L::bQFull + qs), 0, c1, c2);
-                    tma_load_3d(qdst + kHalf, &tmQ, bar(L::bQFull + qs), 64, c1, c2);
+                    const uint32_t qdst = sb + L::kQ + qs * L::kTile;
+#pragma unroll
+                    for (int bx = 0; bx < L::kBoxes; ++bx)
+                        tma_load_3d(qdst + bx * kBox, &tmQ, bar(L::bQFull + qs), 64 * bx, c1, c2);
                     bulk_load(sb + L::kL2 + qs * 512, p.lse2 + ws_row, 512, bar(L::bQFull + qs));
                     // delta row (2-stage ring: freed by the dS warps)
                     const uint32_t ds = gstep & 1u, dph = (gstep >> 1) & 1u;
@@ -644,10 +686,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     bulk_load(sb + L::kDL + ds * 512, p.delta + ws_row, 512, bar(L::bDLFull + ds));
                     // dO (one stage: freed after P.V)
                     if (!(ok = mbar_wait(bar(L::bDOEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 88, it))) break;
-                    mbar_arrive_expect_tx(bar(L::bDOFull), kTileBytes);
+                    mbar_arrive_expect_tx(bar(L::bDOFull), L::kTile);
                     do_armed = (int)(gstep & 1u);
-                    tma_load_3d(sb + L::kDO, &tmDO, bar(L::bDOFull), 0, c1, c2);
-                    tma_load_3d(sb + L::kDO + kHalf, &tmDO, bar(L::bDOFull), 64, c1, c2);
+#pragma unroll
+                    for (int bx = 0; bx < L::kBoxes; ++bx)
+                        tma_load_3d(sb + L::kDO + bx * kBox, &tmDO, bar(L::bDOFull), 64 * bx, c1, c2);
                 }
                 if (!ok) break;
                 ++I;
@@ -666,9 +709,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         regs_decrease<64>();
         const bool leader = lane == 0;
         const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
-        constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false);     // A, B K-major
-        constexpr uint32_t kIdBmn = idesc_bf16_f32(128, 128, true);     // B MN-major
-        constexpr uint32_t kIdABmn = kIdBmn | (1u << 15);               // A and B MN-major
+        constexpr int kKD = D / 16;                                      // MMAs over the head dimension
+        constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false);     // S^T, dP^T: A, B K-major
+        constexpr uint32_t kIdBmn = idesc_bf16_f32(128, D, true);       // dV, dK: B MN-major, N = D
+        // dQ^T (D = 128: M = head dimension, N = queries) or dQ (D = 64: M =
+        // queries, N = head dimension); A and B MN-major
+        constexpr uint32_t kIdDQ = idesc_bf16_f32(128, D == 128 ? 128 : D, true) | (1u << 15);
         auto commit = [&](int b) {
             if (leader) tc_commit(bar(b));
             __syncwarp();
@@ -684,10 +730,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t dO_kmaj = smem_desc_sw128(sb + L::kDO, 16, 1024);
         const uint64_t dO_mn = smem_desc_sw128(sb + L::kDO, kHalf, 1024);
         auto mma_s = [&](uint32_t qs) {
-            const uint64_t qd = smem_desc_sw128(sb + L::kQ + qs * kTileBytes, 16, 1024);
+            const uint64_t qd = smem_desc_sw128(sb + L::kQ + qs * L::kTile, 16, 1024);
             if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) mma_ss(tm + kColS, dK_kmaj + kmaj(kk), qd + kmaj(kk), kIdSS, kk > 0);
+                for (int kk = 0; kk < kKD; ++kk)
+                    mma_ss(tm + kColS, dK_kmaj + kmaj(kk), qd + kmaj(kk), kIdSS, kk > 0);
             }
             __syncwarp();
         };
@@ -707,14 +754,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 const uint32_t qs = gstep % L::kQStages;
-                const uint64_t q_mn = smem_desc_sw128(sb + L::kQ + qs * kTileBytes, kHalf, 1024);
+                const uint64_t q_mn = smem_desc_sw128(sb + L::kQ + qs * L::kTile, kHalf, 1024);
                 // dP^T = V dO^T; its columns held the previous step's dQ
                 if (!(ok = bwd_warp_wait(bar(L::bDQEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 91, it))) break;
                 if (!(ok = bwd_warp_wait(bar(L::bDOFull), gstep & 1u, abort_flag, wf, 101, it))) break;
                 tc_fence_after_sync();
                 if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
+                    for (int kk = 0; kk < kKD; ++kk)
                         mma_ss(tm + kColDP, dV_kmaj + kmaj(kk), dO_kmaj + kmaj(kk), kIdSS, kk > 0);
                 }
                 __syncwarp();
@@ -747,11 +794,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ss(tm + kColDK, dS_kmaj + kmaj(kk), q_mn + mnmaj(kk), kIdBmn, (s > 0 || kk > 0) ? 1u : 0u);
-                    // dQ^T = K^T dS^T: lanes = head dimension, so the reduction into
-                    // global dQ is coalesced along each row
+                    // D = 128: dQ^T = K^T dS^T, lanes = head dimension, so the reduction
+                    // into global dQ is coalesced along each row.  D = 64: dQ = dS K
+                    // (an M = 64 accumulator would use another lane layout)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tm + kColDP, dK_mn + mnmaj(kk), dS_mn + mnmaj(kk), kIdABmn, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        if constexpr (D == 128)
+                            mma_ss(tm + kColDQ, dK_mn + mnmaj(kk), dS_mn + mnmaj(kk), kIdDQ, kk > 0);
+                        else
+                            mma_ss(tm + kColDQ, dS_mn + mnmaj(kk), dK_mn + mnmaj(kk), kIdDQ, kk > 0);
+                    }
                 }
                 __syncwarp();
                 commit(L::bDQFull);
@@ -803,17 +855,39 @@ cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t 
     return cudaGetLastError();
 }
 
+namespace {
+template <int D, bool CAUSAL, bool VARLEN>
+cudaError_t launch_bwd_kernel(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                              const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream)
+{
+    auto kern = fa_bwd_sm103_kernel<D, CAUSAL, VARLEN>;
+    constexpr int kSmem = BwdSmem<D>::kDynamic;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kBwdThreads, kSmem, stream>>>(q, k, v, dout, p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_dim(bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
+                           const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
+                           cudaStream_t stream)
+{
+    if (varlen)
+        return causal ? launch_bwd_kernel<D, true, true>(q, k, v, dout, p, grid, stream)
+                      : launch_bwd_kernel<D, false, true>(q, k, v, dout, p, grid, stream);
+    return causal ? launch_bwd_kernel<D, true, false>(q, k, v, dout, p, grid, stream)
+                  : launch_bwd_kernel<D, false, false>(q, k, v, dout, p, grid, stream);
+}
+}  // namespace
+
 cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
                        cudaStream_t stream)
 {
-    if (D != kBwdD) return cudaErrorInvalidValue;
-    auto kern = varlen ? (causal ? fa_bwd_sm103_kernel<true, true> : fa_bwd_sm103_kernel<false, true>)
-                       : (causal ? fa_bwd_sm103_kernel<true, false> : fa_bwd_sm103_kernel<false, false>);
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem::kDynamic);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kBwdThreads, BwdSmem::kDynamic, stream>>>(q, k, v, dout, p);
-    return cudaGetLastError();
+    if (D == 128) return launch_bwd_dim<128>(causal, varlen, q, k, v, dout, p, grid, stream);
+    if (D == 64) return launch_bwd_dim<64>(causal, varlen, q, k, v, dout, p, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

@@ -122,7 +122,8 @@ def test_bwd_argument_validation(lib):
     assert call(scale=0.0) == INV
     assert call(dq=20) == INV                        # misaligned
     assert call(wsb=100) == INV                      # workspace too small
-    assert call(D=64) == UNS
+    assert call(D=96) == UNS
+    assert call(D=256) == UNS
     n = ctypes.c_size_t(0)
     assert lib.fa_bwd_workspace(2, 3, 130, ctypes.byref(n)) == fa.FA_OK
     assert n.value == 2 * 4 * 2 * 3 * 256            # delta and lse2, rows padded to 128
@@ -198,7 +199,7 @@ def test_bwd_varlen_argument_validation(lib):
     assert call(Hq=3, Hkv=2) == INV
     assert call(cu_q=34) == INV                      # int32 offsets must be 4-byte aligned
     assert call(wsb=64) == INV                       # workspace too small
-    assert call(D=64) == UNS
+    assert call(D=80) == UNS
     n = ctypes.c_size_t(0)
     assert lib.fa_bwd_varlen_workspace(3, 1000, 4, ctypes.byref(n)) == fa.FA_OK
     rows = (1000 + 127) // 128 * 128 + 128 * 3       # each sequence padded to 128 rows

@@ -74,8 +74,28 @@ CASES = [
 
 @pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,causal,qm", CASES)
 def test_bwd_full_compare(B, Hq, Hkv, Lq, Lk, causal, qm):
-    D = 128
-    seed = B * 7 + Hq + Lq + 3 * Lk
+    _bwd_case(B, Hq, Hkv, Lq, Lk, causal, qm, 128)
+
+
+CASES_D64 = [
+    # head dimension 64: dQ formed untransposed (lanes = query rows)
+    (1, 2, 2, 256, 256, False, 1.0),
+    (2, 4, 2, 300, 300, True, 1.0),
+    (1, 2, 1, 200, 520, True, 1.0),
+    (1, 2, 1, 520, 200, True, 1.0),
+    (1, 8, 2, 513, 513, True, 3.0),
+    (1, 1, 1, 1, 1, False, 1.0),
+    (4, 4, 4, 1024, 1024, True, 1.0),   # the D = 64 forward workload's shape
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,causal,qm", CASES_D64)
+def test_bwd_d64_full_compare(B, Hq, Hkv, Lq, Lk, causal, qm):
+    _bwd_case(B, Hq, Hkv, Lq, Lk, causal, qm, 64)
+
+
+def _bwd_case(B, Hq, Hkv, Lq, Lk, causal, qm, D):
+    seed = B * 7 + Hq + Lq + 3 * Lk + D
     q, k, v = random_inputs((B, Hq, Lq, D), (B, Hkv, Lk, D), seed=seed, q_mult=qm)
     do = grad_output((B, Hq, Lq, D), seed)
     got = run_bwd(q, k, v, do, causal)
@@ -123,10 +143,10 @@ VARLEN_CASES = [
 ]
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("lq,lk,Hq,Hkv,causal", VARLEN_CASES)
-def test_bwd_varlen_full_compare(lq, lk, Hq, Hkv, causal):
+def test_bwd_varlen_full_compare(lq, lk, Hq, Hkv, causal, D):
     from oracle.backward import attention_bwd_varlen
-    D = 128
     Tq, Tk = sum(lq), sum(lk)
     seed = Tq + 3 * Tk + Hq
     q, k, v = random_inputs((Tq, Hq, D), (Tk, Hkv, D), seed=seed)

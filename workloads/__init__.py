@@ -205,6 +205,8 @@ BWD_WORKLOADS: dict[str, Workload] = {
     "bwd_gqa_b2_h32x8_l4096_d128_causal_q3": Workload(
         "bwd_gqa_b2_h32x8_l4096_d128_causal_q3", 2, 32, 8, 4096, 4096, 128, True, q_mult=3.0, bwd=True),
     "bwd_b1_h16_l4096_d128": Workload("bwd_b1_h16_l4096_d128", 1, 16, 16, 4096, 4096, 128, False, bwd=True),
+    # the D = 64 forward workload's shape through the backward
+    "bwd_b4_h16_l1024_d64": Workload("bwd_b4_h16_l1024_d64", 4, 16, 16, 1024, 1024, 64, False, bwd=True),
     # the packed forward workload's batch through the packed backward
     "bwd_varlen8_h32x8_d128_causal": Workload(
         "bwd_varlen8_h32x8_d128_causal", 8, 32, 8, 0, 0, 128, True, seqlens=_VARLEN_LENS, bwd=True),

@@ -120,3 +120,63 @@ def attention_variant_varlen(q, k, v, cu_q, cu_k, scale: float, window=(-1, -1),
         o[a:b] = os_[0].transpose(1, 0, 2)
         lse[:, a:b] = ls_[0]
     return o, lse
+
+
+def attention_variant_bwd(q, k, v, do, scale: float, window=(-1, -1), softcap: float = 0.0, alibi_slopes=None,
+                          block: int = 1024):
+    """Gradients (dq, dk, dv) of sum(O * do) for the variant forward above,
+    dense [B, H, L, D] inputs.  With S the scaled scores and S' the modified
+    ones (FlashAttention from Scratch, sec. 8 and sec. 12):
+        P = softmax(S' masked), dV = P^T dO, dP = dO V^T,
+        dS' = P * (dP - rowsum(P * dP)),
+        dS = dS' * dS'/dS   (soft-capping: 1 - tanh(S / cap)^2; ALiBi and
+                             windows: 1, the bias and the mask do not depend on S),
+        dQ = scale dS K,  dK = scale dS^T Q."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    r = Hq // Hkv
+    slopes = np.zeros(Hq) if alibi_slopes is None else _f64(alibi_slopes).reshape(Hq)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            K, V = k[b, h // r], v[b, h // r]
+            for i0 in range(0, Lq, block):
+                i1 = min(Lq, i0 + block)
+                Q, G = q[b, h, i0:i1], do[b, h, i0:i1]
+                s = variant_scores(Q, K, scale, window, softcap, slopes[h], Lq, Lk, i0)
+                m = s.max(axis=1, keepdims=True)
+                p = np.exp(s - np.where(np.isfinite(m), m, 0.0))
+                ell = p.sum(axis=1, keepdims=True)
+                p = np.where(ell > 0, p / np.where(ell > 0, ell, 1.0), 0.0)
+                dp = G @ V.T
+                ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+                if softcap > 0:
+                    th = np.tanh((Q @ K.T) * scale / softcap)
+                    ds = ds * (1.0 - th * th)
+                dq[b, h, i0:i1] = scale * (ds @ K)
+                dk[b, h // r] += scale * (ds.T @ Q)
+                dv[b, h // r] += p.T @ G
+    return dq, dk, dv
+
+
+def attention_variant_bwd_varlen(q, k, v, do, cu_q, cu_k, scale: float, window=(-1, -1), softcap: float = 0.0,
+                                 alibi_slopes=None):
+    """Packed [T, H, D] version of :func:`attention_variant_bwd`: every
+    sequence is an independent problem; returns (dq, dk, dv) in the packed
+    layouts."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    cu_q, cu_k = np.asarray(cu_q), np.asarray(cu_k)
+    for s_ in range(len(cu_q) - 1):
+        a, b = int(cu_q[s_]), int(cu_q[s_ + 1])
+        c, d = int(cu_k[s_]), int(cu_k[s_ + 1])
+        if b == a or d == c:
+            continue
+        sl = lambda t, x, y: t[x:y].transpose(1, 0, 2)[None]
+        g = attention_variant_bwd(sl(q, a, b), sl(k, c, d), sl(v, c, d), sl(do, a, b), scale, window, softcap,
+                                  alibi_slopes)
+        dq[a:b] = g[0][0].transpose(1, 0, 2)
+        dk[c:d] = g[1][0].transpose(1, 0, 2)
+        dv[c:d] = g[2][0].transpose(1, 0, 2)
+    return dq, dk, dv

@@ -135,3 +135,65 @@ def test_rows_and_varlen_agree_with_dense():
     for b in range(2):
         np.testing.assert_allclose(ov[33 * b:33 * (b + 1)].transpose(1, 0, 2), full[0][b], atol=1e-14)
         np.testing.assert_allclose(lv[:, 33 * b:33 * (b + 1)], full[1][b], atol=1e-14)
+
+
+# ------------------------------------------------------------------ backward
+
+def _torch_variant_grads(q, k, v, do, scale, window, softcap, slopes):
+    """PyTorch autograd through an independently written variant forward."""
+    Q = torch.tensor(q, requires_grad=True)
+    K = torch.tensor(k, requires_grad=True)
+    V = torch.tensor(v, requires_grad=True)
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    r = Hq // Hkv
+    Kr, Vr = K.repeat_interleave(r, 1), V.repeat_interleave(r, 1)
+    S = scale * Q @ Kr.transpose(-1, -2)
+    if softcap > 0:
+        S = softcap * torch.tanh(S / softcap)
+    pos = torch.arange(Lq)[:, None] + (Lk - Lq)
+    key = torch.arange(Lk)[None, :]
+    if slopes is not None:
+        S = S - torch.tensor(slopes)[None, :, None, None] * (pos - key).abs()
+    ok = torch.ones(Lq, Lk, dtype=torch.bool)
+    if window[0] >= 0:
+        ok &= key >= pos - window[0]
+    if window[1] >= 0:
+        ok &= key <= pos + window[1]
+    P = torch.nan_to_num(torch.softmax(S.masked_fill(~ok, float("-inf")), dim=-1), nan=0.0)
+    (P @ Vr * torch.tensor(do)).sum().backward()
+    return Q.grad.numpy(), K.grad.numpy(), V.grad.numpy()
+
+
+@pytest.mark.parametrize("window,softcap,alibi", [((5, 0), 0.0, False), ((3, 4), 0.0, False), ((-1, -1), 2.0, False),
+                                                 ((6, 0), 1.5, False), ((-1, -1), 0.0, True), ((4, 2), 0.0, True)])
+@pytest.mark.parametrize("Lq,Lk", [(13, 13), (9, 17), (17, 9)])
+def test_variant_backward_matches_autograd(window, softcap, alibi, Lq, Lk):
+    from oracle.variants import attention_variant_bwd
+    rng = np.random.default_rng(Lq * 7 + Lk)
+    B, Hq, Hkv, D = 1, 4, 2, 8
+    q = rng.standard_normal((B, Hq, Lq, D))
+    k = rng.standard_normal((B, Hkv, Lk, D))
+    v = rng.standard_normal((B, Hkv, Lk, D))
+    do = rng.standard_normal((B, Hq, Lq, D))
+    slopes = np.array([0.5, 0.25, 0.125, 0.0625]) if alibi else None
+    got = attention_variant_bwd(q, k, v, do, 0.4, window, softcap, slopes, block=5)
+    ref = _torch_variant_grads(q, k, v, do, 0.4, window, softcap, slopes)
+    for g, e, n in zip(got, ref, "qkv"):
+        np.testing.assert_allclose(g, e, atol=1e-11, rtol=1e-9, err_msg=n)
+
+
+def test_variant_backward_varlen_equals_dense_per_sequence():
+    from oracle.variants import attention_variant_bwd, attention_variant_bwd_varlen
+    rng = np.random.default_rng(3)
+    lq, lk, H, D = [7, 0, 12], [9, 5, 12], 2, 8
+    cq, ck = np.concatenate([[0], np.cumsum(lq)]), np.concatenate([[0], np.cumsum(lk)])
+    q, do = rng.standard_normal((cq[-1], H, D)), rng.standard_normal((cq[-1], H, D))
+    k, v = rng.standard_normal((ck[-1], H, D)), rng.standard_normal((ck[-1], H, D))
+    dq, dk, dv = attention_variant_bwd_varlen(q, k, v, do, cq, ck, 0.3, (4, 1), 3.0)
+    for s in (0, 2):
+        sl = lambda t, c, i: t[c[i]:c[i + 1]].transpose(1, 0, 2)[None]
+        g = attention_variant_bwd(sl(q, cq, s), sl(k, ck, s), sl(v, ck, s), sl(do, cq, s), 0.3, (4, 1), 3.0)
+        assert np.array_equal(dq[cq[s]:cq[s + 1]], g[0][0].transpose(1, 0, 2))
+        assert np.array_equal(dk[ck[s]:ck[s + 1]], g[1][0].transpose(1, 0, 2))
+    assert np.all(dk[ck[1]:ck[2]] == 0) and np.all(dv[ck[1]:ck[2]] == 0)  # no query rows

@@ -23,7 +23,7 @@ import torch
 
 __all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_hdim", "fa_fwd_varlen_hdim", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
            "fa_fwd_splitkv", "fp8_prepare", "fa_fwd_fp8", "fp8_sections", "splitkv_workspace", "fa_bwd",
-           "bwd_workspace", "fa_bwd_varlen", "bwd_varlen_workspace", "fa_check", "fa_status_string", "fa_last_launch_count",
+           "bwd_workspace", "fa_bwd_varlen", "bwd_varlen_workspace", "fa_bwd_variant", "fa_bwd_varlen_variant", "fa_check", "fa_status_string", "fa_last_launch_count",
            "FAError", "library_path", "load_library", "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -34,7 +34,7 @@ _lib = None
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_hdim", "fa_fwd_varlen_hdim", "fa_fwd_varlen_noalloc", "fa_fwd_variant", "fa_fwd_varlen_variant",
                     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace", "fa_bwd", "fa_bwd_workspace", "fa_bwd_varlen",
-                    "fa_bwd_varlen_workspace", "fa_fp8_workspace",
+                    "fa_bwd_varlen_workspace", "fa_bwd_variant", "fa_bwd_varlen_variant", "fa_fp8_workspace",
                     "fa_fp8_prepare", "fa_fwd_fp8", "fa_check", "fa_status_string", "fa_last_launch_count",
                     "fa_test_inject_fault")
 SPLITKV_MAX_ROWS = 16  # (Hq / Hkv) * Lq limit of fa_fwd_splitkv
@@ -101,6 +101,12 @@ def load_library() -> ctypes.CDLL:
         lib.fa_bwd_varlen.restype = i
         lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp,
                                       ctypes.c_size_t, vp]
+        lib.fa_bwd_variant.restype = i
+        lib.fa_bwd_variant.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vr, f, vp, ctypes.c_size_t,
+                                       vp]
+        lib.fa_bwd_varlen_variant.restype = i
+        lib.fa_bwd_varlen_variant.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vr,
+                                              f, vp, ctypes.c_size_t, vp]
         lib.fa_bwd_varlen_workspace.restype = i
         lib.fa_bwd_varlen_workspace.argtypes = [i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         lib.fa_check.restype = i
@@ -501,10 +507,20 @@ def bwd_workspace(B: int, Hq: int, Lq: int) -> int:
     return int(nbytes.value)
 
 
+def fa_bwd_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+                   dout: torch.Tensor, window=(-1, -1), alibi_slopes: torch.Tensor | None = None,
+                   softmax_scale: float | None = None, dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
+                   dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """Backward of fa_fwd_variant for key windows and ALiBi (D = 128); o and lse
+    from fa_fwd_variant with the same variant."""
+    var = _variant(window, 0.0, alibi_slopes, q.shape[1], q.device)
+    return fa_bwd(q, k, v, o, lse, dout, False, softmax_scale, dq, dk, dv, workspace, stream, variant=var)
+
+
 def fa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
            dout: torch.Tensor, causal: bool = False, softmax_scale: float | None = None,
            dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
-           workspace: torch.Tensor | None = None, stream=None):
+           workspace: torch.Tensor | None = None, stream=None, variant=None):
     """Backward of fa_fwd.  q/dout [B,Hq,Lq,D], k/v [B,Hkv,Lk,D] bf16; o fp32
     [B,Hq,Lq,D] and lse fp32 [B,Hq,Lq] from fa_fwd.  Returns (dq, dk, dv) fp32."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
@@ -530,14 +546,18 @@ def fa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, l
         nbytes = bwd_workspace(B, Hq, Lq)
         if workspace is None or workspace.numel() * workspace.element_size() < nbytes:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-        st = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
-                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Lq, Lk, D, int(bool(causal)),
-                        float(softmax_scale), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                        _stream_handle(stream))
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Lq, Lk, D)
+        tail = (float(softmax_scale), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                _stream_handle(stream))
+        if variant is None:
+            st, name = lib.fa_bwd(*args, int(bool(causal)), *tail), "fa_bwd"
+        else:
+            st, name = lib.fa_bwd_variant(*args, ctypes.byref(variant), *tail), "fa_bwd_variant"
         if isinstance(stream, torch.cuda.Stream):
             workspace.record_stream(stream)
     if st != FA_OK:
-        raise FAError(st, "fa_bwd")
+        raise FAError(st, name)
     return dq, dk, dv
 
 
@@ -550,11 +570,23 @@ def bwd_varlen_workspace(num_seqs: int, total_q: int, Hq: int) -> int:
     return int(nbytes.value)
 
 
+def fa_bwd_varlen_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+                          dout: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                          max_seqlen_q: int, max_seqlen_k: int, window=(-1, -1),
+                          alibi_slopes: torch.Tensor | None = None, softmax_scale: float | None = None,
+                          dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
+                          dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """Backward of fa_fwd_varlen_variant for key windows and ALiBi (D = 128)."""
+    var = _variant(window, 0.0, alibi_slopes, q.shape[1], q.device)
+    return fa_bwd_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, False,
+                         softmax_scale, dq, dk, dv, workspace, stream, variant=var)
+
+
 def fa_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
                   dout: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int,
                   max_seqlen_k: int, causal: bool = False, softmax_scale: float | None = None,
                   dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
-                  workspace: torch.Tensor | None = None, stream=None):
+                  workspace: torch.Tensor | None = None, stream=None, variant=None):
     """Backward of fa_fwd_varlen.  q/dout [Tq,Hq,D], k/v [Tk,Hkv,D] bf16; o fp32
     [Tq,Hq,D] and lse fp32 [Hq,Tq] from fa_fwd_varlen; cu_seqlens_* int32 CUDA.
     Returns (dq, dk, dv) fp32 in the layouts of q, k and v."""
@@ -585,15 +617,19 @@ def fa_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Te
         nbytes = bwd_varlen_workspace(n_seqs, Tq, Hq)
         if workspace is None or workspace.numel() * workspace.element_size() < nbytes:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-        st = lib.fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                               dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens_q.data_ptr(),
-                               cu_seqlens_k.data_ptr(), n_seqs, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq,
-                               Hkv, D, int(bool(causal)), float(softmax_scale), workspace.data_ptr(),
-                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                n_seqs, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D)
+        tail = (float(softmax_scale), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                _stream_handle(stream))
+        if variant is None:
+            st, name = lib.fa_bwd_varlen(*args, int(bool(causal)), *tail), "fa_bwd_varlen"
+        else:
+            st, name = lib.fa_bwd_varlen_variant(*args, ctypes.byref(variant), *tail), "fa_bwd_varlen_variant"
         if isinstance(stream, torch.cuda.Stream):
             workspace.record_stream(stream)
     if st != FA_OK:
-        raise FAError(st, "fa_bwd_varlen")
+        raise FAError(st, name)
     return dq, dk, dv
 
 

@@ -736,10 +736,26 @@ extern "C" fa_status_t fa_bwd_workspace(int B, int Hq, int Lq, size_t* workspace
     return FA_OK;
 }
 
-extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse,
-                              const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq,
-                              int Lk, int D, int causal, float softmax_scale, void* workspace,
-                              size_t workspace_bytes, cudaStream_t stream)
+namespace {
+// Validates a backward variant (windows and ALiBi; soft-capping has no
+// backward kernel) and fills the parameters; returns the variant kind or a
+// negative fa_status_t.
+int prepare_bwd_variant(const fa_variant_t* var, int D, BwdParams* p)
+{
+    if (!var) return -(int)FA_ERR_INVALID_ARG;
+    if (!std::isfinite(var->softcap) || var->softcap < 0.f) return -(int)FA_ERR_INVALID_ARG;
+    if (var->alibi_slopes && (reinterpret_cast<uintptr_t>(var->alibi_slopes) & 3u)) return -(int)FA_ERR_INVALID_ARG;
+    if (D != 128 || var->softcap > 0.f) return -(int)FA_ERR_UNSUPPORTED;
+    p->win_left = var->window_left < 0 ? -1 : var->window_left;
+    p->win_right = var->window_right < 0 ? -1 : var->window_right;
+    p->alibi = var->alibi_slopes;
+    return var->alibi_slopes ? kVarAlibi : kVarWindow;
+}
+
+fa_status_t bwd_dense(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                      const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq, int Lk,
+                      int D, int causal, const fa_variant_t* variant, float softmax_scale, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream)
 {
     g_last_launches = 0;
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
@@ -758,6 +774,12 @@ extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const
     size_t need = 0;
     fa_bwd_workspace(B, Hq, Lq, &need);
     if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+    BwdParams p{};
+    int var = kVarNone;
+    if (variant) {
+        var = prepare_bwd_variant(variant, D, &p);
+        if (var < 0) return (fa_status_t)(-var);
+    }
     DeviceState* ds = nullptr;
     fa_status_t st = device_state(&ds);
     if (st != FA_OK) return st;
@@ -770,7 +792,6 @@ extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const
         !encode_map(&mv, v, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kBwdTile, 1))
         return FA_ERR_CUDA;
 
-    BwdParams p{};
     p.o = o;
     p.lse = lse;
     p.dout = static_cast<const uint16_t*>(dout);
@@ -799,9 +820,32 @@ extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const
     g_fault_next = 0;
     if (launch_bwd_pre(D, false, p, stream) != cudaSuccess) return FA_ERR_CUDA;
     const int grid = (int)(items < ds->num_sms ? items : ds->num_sms);
-    if (launch_bwd(D, causal != 0, false, mq, mk, mv, mdo, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+    const cudaError_t e = variant ? launch_bwd_variant(var, false, mq, mk, mv, mdo, p, grid, stream)
+                                  : launch_bwd(D, causal != 0, false, mq, mk, mv, mdo, p, grid, stream);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 2;
     return FA_OK;
+}
+}  // namespace
+
+extern "C" fa_status_t fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                              const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq,
+                              int Lk, int D, int causal, float softmax_scale, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream)
+{
+    return bwd_dense(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, causal, nullptr, softmax_scale,
+                     workspace, workspace_bytes, stream);
+}
+
+extern "C" fa_status_t fa_bwd_variant(const void* q, const void* k, const void* v, const float* o,
+                                      const float* lse, const void* dout, float* dq, float* dk, float* dv, int B,
+                                      int Hq, int Hkv, int Lq, int Lk, int D, const fa_variant_t* variant,
+                                      float softmax_scale, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream)
+{
+    if (!variant) return FA_ERR_INVALID_ARG;
+    return bwd_dense(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, 0, variant, softmax_scale,
+                     workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------- packed backward
@@ -835,12 +879,12 @@ extern "C" fa_status_t fa_bwd_varlen_workspace(int num_seqs, int total_q, int Hq
     return FA_OK;
 }
 
-extern "C" fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v, const float* o, const float* lse,
-                                     const void* dout, float* dq, float* dk, float* dv, const int* cu_seqlens_q,
-                                     const int* cu_seqlens_k, int num_seqs, int total_q, int total_k,
-                                     int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D, int causal,
-                                     float softmax_scale, void* workspace, size_t workspace_bytes,
-                                     cudaStream_t stream)
+namespace {
+fa_status_t bwd_varlen(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                       const void* dout, float* dq, float* dk, float* dv, const int* cu_seqlens_q,
+                       const int* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
+                       int max_seqlen_k, int Hq, int Hkv, int D, int causal, const fa_variant_t* variant,
+                       float softmax_scale, void* workspace, size_t workspace_bytes, cudaStream_t stream)
 {
     g_last_launches = 0;
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace || !cu_seqlens_q ||
@@ -862,6 +906,12 @@ extern "C" fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v
     if (ub >= (1ll << 31) || lay.rows >= (1ll << 31) || (long long)total_q * Hq >= (1ll << 31) * 8ll ||
         (long long)total_k * Hkv >= (1ll << 31) * 8ll)
         return FA_ERR_INVALID_ARG;
+    BwdParams p{};
+    int var = kVarNone;
+    if (variant) {
+        var = prepare_bwd_variant(variant, D, &p);
+        if (var < 0) return (fa_status_t)(-var);
+    }
     DeviceState* ds = nullptr;
     fa_status_t st = device_state(&ds);
     if (st != FA_OK) return st;
@@ -878,7 +928,6 @@ extern "C" fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v
     if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
                                max_seqlen_k, Hkv, 1, sched, ds->err, stream) != cudaSuccess)
         return FA_ERR_CUDA;
-    BwdParams p{};
     p.o = o;
     p.lse = lse;
     p.dout = static_cast<const uint16_t*>(dout);
@@ -908,9 +957,37 @@ extern "C" fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v
     g_fault_next = 0;
     if (launch_bwd_pre(D, true, p, stream) != cudaSuccess) return FA_ERR_CUDA;
     const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
-    if (launch_bwd(D, causal != 0, true, mq, mk, mv, mdo, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+    const cudaError_t e = variant ? launch_bwd_variant(var, true, mq, mk, mv, mdo, p, grid, stream)
+                                  : launch_bwd(D, causal != 0, true, mq, mk, mv, mdo, p, grid, stream);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 3;
     return FA_OK;
+}
+}  // namespace
+
+extern "C" fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                                     const void* dout, float* dq, float* dk, float* dv, const int* cu_seqlens_q,
+                                     const int* cu_seqlens_k, int num_seqs, int total_q, int total_k,
+                                     int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D, int causal,
+                                     float softmax_scale, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream)
+{
+    return bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
+                      max_seqlen_q, max_seqlen_k, Hq, Hkv, D, causal, nullptr, softmax_scale, workspace,
+                      workspace_bytes, stream);
+}
+
+extern "C" fa_status_t fa_bwd_varlen_variant(const void* q, const void* k, const void* v, const float* o,
+                                             const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                                             const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                                             int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int Hq,
+                                             int Hkv, int D, const fa_variant_t* variant, float softmax_scale,
+                                             void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    if (!variant) return FA_ERR_INVALID_ARG;
+    return bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
+                      max_seqlen_q, max_seqlen_k, Hq, Hkv, D, 0, variant, softmax_scale, workspace, workspace_bytes,
+                      stream);
 }
 
 // ------------------------------------------------------------- FP8 forward

@@ -269,6 +269,7 @@ __device__ __forceinline__ bool bwd_warp_wait(uint32_t bar, uint32_t parity, vol
 struct BwdItem {
     int b, hkv, j;      // batch, KV head, key tile
     int i_min, nq;      // first Q tile with an allowed pair; Q tiles per head
+    int i_max;          // last Q tile with an allowed pair
     int steps;          // group * (nq - i_min)
     int lq, lk;         // query / key length of this problem
     int q0, k0;         // packed batches: first query / key token of the sequence
@@ -288,7 +289,7 @@ __device__ __forceinline__ void bwd_section_order(int r, int slabs, int nk, int 
     slab = sec * hs + (rem - j * cur);
 }
 
-template <bool CAUSAL, bool VARLEN>
+template <bool CAUSAL, bool VARLEN, int VAR>
 __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int it)
 {
     BwdItem w;
@@ -325,7 +326,20 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int it)
         w.i_min = first_q > 0 ? (int)(first_q / kBwdTile) : 0;
         if (w.i_min > w.nq) w.i_min = w.nq;
     }
-    w.steps = p.group * (w.nq - w.i_min);
+    w.i_max = w.nq - 1;
+    if (var_window(VAR)) {
+        // queries q that see a key of the tile: c_q - left <= key <= c_q + right
+        // for some key of [j*128, j*128+127], with c_q = q + (Lk - Lq)
+        const long long off = w.lk - w.lq, k0 = (long long)w.j * kBwdTile;
+        auto floor_div = [](long long x) { return x >= 0 ? x / kBwdTile : -((-x + kBwdTile - 1) / kBwdTile); };
+        long long lo = 0, hi = w.nq - 1;
+        if (p.win_right >= 0) lo = max(lo, floor_div(k0 - p.win_right - off));
+        if (p.win_left >= 0) hi = min(hi, floor_div(k0 + kBwdTile - 1 + p.win_left - off));
+        if (hi < lo) hi = lo = min(lo, (long long)w.nq - 1);  // no pair: one fully masked step gives dK = dV = 0
+        w.i_min = (int)lo;
+        w.i_max = (int)hi;
+    }
+    w.steps = p.group * (w.i_max - w.i_min + 1);
     return w;
 }
 
@@ -343,7 +357,7 @@ __device__ __forceinline__ int bwd_cta_item(int k)
 // Query head and Q tile of step s of an item.
 __device__ __forceinline__ void bwd_step(const BwdParams& p, const BwdItem& w, int s, int& h, int& i)
 {
-    const int span = w.nq - w.i_min;
+    const int span = w.i_max - w.i_min + 1;
     const int g = s / span;
     const int r = s - g * span;
     h = w.hkv * p.group + g;
@@ -354,7 +368,7 @@ __device__ __forceinline__ void bwd_step(const BwdParams& p, const BwdItem& w, i
 
 // ------------------------------------------------------------------ main kernel
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, int VAR = kVarNone>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -419,7 +433,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const int num_items = VARLEN ? __ldg(p.sched) : p.num_items;
-    constexpr bool kAlt = CAUSAL || VARLEN;  // items of unequal length: alternate the rounds
+    constexpr bool kAlt = CAUSAL || VARLEN || VAR != kVarNone;  // items of unequal length: alternate the rounds
 
     if (warp < 4) {
         // ============================================================ dQ reduction, dK/dV epilogue
@@ -432,7 +446,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t gstep = 0;
         int I = 0;
         for (int k = 0, it = bwd_cta_item<kAlt>(0); it < num_items; it = bwd_cta_item<kAlt>(++k)) {
-            const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
+            const BwdItem w = bwd_item<CAUSAL, VARLEN, VAR>(p, it);
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 int h, i;
                 bwd_step(p, w, s, h, i);
@@ -522,10 +536,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         uint32_t gstep = 0;
         for (int k = 0, it = bwd_cta_item<kAlt>(0); it < num_items; it = bwd_cta_item<kAlt>(++k)) {
-            const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
+            const BwdItem w = bwd_item<CAUSAL, VARLEN, VAR>(p, it);
             const int kpos = w.j * kBwdTile + t;
             const bool key_ok = kpos < w.lk;
             const int off = w.lk - w.lq;
+            float alibi_l2 = 0.f;  // ALiBi slope of the step's query head, log2 units
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 int h, i;
                 bwd_step(p, w, s, h, i);
@@ -538,8 +553,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t ds = gstep & 1u, dph = (gstep >> 1) & 1u;
                 const float4* l2p = reinterpret_cast<const float4*>(smem + L::kL2 + qs * 512);
                 const float4* dlp = reinterpret_cast<const float4*>(smem + L::kDL + ds * 512);
-                // pairs above the bottom-right diagonal exist in this tile
-                const bool need_mask = !key_ok || (CAUSAL && q0 < w.j * kBwdTile + kBwdTile - 1 - off);
+                // pairs above the bottom-right diagonal (or outside the key window)
+                // exist in this tile for this thread's key
+                bool need_mask = !key_ok || (CAUSAL && q0 < w.j * kBwdTile + kBwdTile - 1 - off);
+                if constexpr (var_window(VAR)) {
+                    if (p.win_left >= 0 && kpos < q0 + kBwdTile - 1 + off - p.win_left) need_mask = true;
+                    if (p.win_right >= 0 && kpos > q0 + off + p.win_right) need_mask = true;
+                }
+                if constexpr (VAR == kVarAlibi) alibi_l2 = __ldg(p.alibi + h) * 1.4426950408889634f;
                 if (!bwd_warp_wait(bar(L::bQFull + qs), qph, abort_flag, wf, 79, it)) goto done;
                 if (!bwd_warp_wait(bar(L::bSFull), ph, abort_flag, wf, 80, it)) goto done;
                 tc_fence_after_sync();
@@ -561,12 +582,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), p.scale_log2, -l2[e]));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), p.scale_log2, -l2[e + 1]));
+                        float b0 = -l2[e], b1 = -l2[e + 1];
+                        if constexpr (VAR == kVarAlibi) {
+                            // s * scale - slope * |c_q - key|, in log2 units
+                            const float d0 = (float)(q0 + c * 32 + e + off - kpos);
+                            b0 = fmaf(-alibi_l2, fabsf(d0), b0);
+                            b1 = fmaf(-alibi_l2, fabsf(d0 + 1.f), b1);
+                        }
+                        float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), p.scale_log2, b0));
+                        float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), p.scale_log2, b1));
                         if (need_mask) {
                             const int q = q0 + c * 32 + e;
                             if (!key_ok || (CAUSAL && kpos > q + off)) p0 = 0.f;
                             if (!key_ok || (CAUSAL && kpos > q + 1 + off)) p1 = 0.f;
+                            if constexpr (var_window(VAR)) {
+                                if (p.win_left >= 0 && kpos < q + off - p.win_left) p0 = 0.f;
+                                if (p.win_left >= 0 && kpos < q + 1 + off - p.win_left) p1 = 0.f;
+                                if (p.win_right >= 0 && kpos > q + off + p.win_right) p0 = 0.f;
+                                if (p.win_right >= 0 && kpos > q + 1 + off + p.win_right) p1 = 0.f;
+                            }
                         }
                         pk[cc * 16 + e / 2] = bwd_pack_bf16(p0, p1);
                     }
@@ -639,7 +673,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t gstep = 0;
             int I = 0;
             for (int k = 0, it = bwd_cta_item<kAlt>(0); it < num_items; it = bwd_cta_item<kAlt>(++k)) {
-                const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
+                const BwdItem w = bwd_item<CAUSAL, VARLEN, VAR>(p, it);
                 const int bh_kv = w.b * p.Hkv + w.hkv;
                 // TMA coordinates: dense (x, row, head slab), packed (x, head, token)
                 auto ld_kv = [&](uint32_t dst, const CUtensorMap* map, int x) {
@@ -742,7 +776,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int I = 0;
         bool issued = false, ok = true;
         for (int k = 0, it = bwd_cta_item<kAlt>(0); it < num_items && ok; it = bwd_cta_item<kAlt>(++k)) {
-            const BwdItem w = bwd_item<CAUSAL, VARLEN>(p, it);
+            const BwdItem w = bwd_item<CAUSAL, VARLEN, VAR>(p, it);
             if (!(ok = bwd_warp_wait(bar(L::bKVFull), (uint32_t)(I & 1), abort_flag, wf, 89, it))) break;
             {
                 const uint32_t qs = gstep % L::kQStages, qph = (gstep / L::kQStages) & 1u;
@@ -833,6 +867,7 @@ done:
     }
 }
 
+#if !defined(FA_BWD_VARIANTS)
 cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t stream)
 {
     if (varlen) {
@@ -854,13 +889,14 @@ cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t 
         fa_bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
+#endif
 
 namespace {
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, int VAR = kVarNone>
 cudaError_t launch_bwd_kernel(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                               const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream)
 {
-    auto kern = fa_bwd_sm103_kernel<D, CAUSAL, VARLEN>;
+    auto kern = fa_bwd_sm103_kernel<D, CAUSAL, VARLEN, VAR>;
     constexpr int kSmem = BwdSmem<D>::kDynamic;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
@@ -881,6 +917,7 @@ cudaError_t launch_bwd_dim(bool causal, bool varlen, const CUtensorMap& q, const
 }
 }  // namespace
 
+#if !defined(FA_BWD_VARIANTS)
 cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
                        cudaStream_t stream)
@@ -889,5 +926,19 @@ cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, co
     if (D == 64) return launch_bwd_dim<64>(causal, varlen, q, k, v, dout, p, grid, stream);
     return cudaErrorInvalidValue;
 }
+#else
+cudaError_t launch_bwd_variant(int var, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
+                               const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
+                               cudaStream_t stream)
+{
+    if (var == kVarAlibi)
+        return varlen ? launch_bwd_kernel<128, false, true, kVarAlibi>(q, k, v, dout, p, grid, stream)
+                      : launch_bwd_kernel<128, false, false, kVarAlibi>(q, k, v, dout, p, grid, stream);
+    if (var == kVarWindow)
+        return varlen ? launch_bwd_kernel<128, false, true, kVarWindow>(q, k, v, dout, p, grid, stream)
+                      : launch_bwd_kernel<128, false, false, kVarWindow>(q, k, v, dout, p, grid, stream);
+    return cudaErrorInvalidValue;
+}
+#endif
 
 }  // namespace fa

@@ -6,6 +6,8 @@
 
 #include <cstdint>
 
+#include "fa_params.h"
+
 namespace fa {
 
 constexpr int kBwdTile = 128;  // keys per KV tile = query rows per Q tile
@@ -37,6 +39,11 @@ struct BwdParams {
     int num_q_tiles;        // ceil(Lq / 128)
     int num_items;          // B * Hkv * num_kv_tiles
     int heads_per_section;  // (batch, KV head) slabs whose items are interleaved (L2-sized dQ working set)
+    // variants (kernels instantiated with VAR > 0): key window around each
+    // query's aligned position (< 0 = unlimited) and ALiBi slopes per query
+    // head (natural-log units)
+    int win_left, win_right;
+    const float* alibi;
     float scale;            // softmax_scale (multiplies dS)
     float scale_log2;       // softmax_scale * log2(e)
     int causal;
@@ -49,5 +56,10 @@ cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t 
 cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
                        cudaStream_t stream);
+// Variants (var = kVarWindow or kVarAlibi, D = 128, no separate causal flag:
+// a causal window is (-1, 0)).
+cudaError_t launch_bwd_variant(int var, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
+                               const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
+                               cudaStream_t stream);
 
 }  // namespace fa

@@ -327,6 +327,26 @@ fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v, const flo
 fa_status_t fa_bwd_varlen_workspace(int num_seqs, int total_q, int Hq, size_t* workspace_bytes);
 
 /*
+ * Backward of fa_fwd_variant / fa_fwd_varlen_variant for key windows and ALiBi
+ * (FlashAttention from Scratch, sec. 12): the same modified scores and masks
+ * as the forward (pass the forward's O and LSE), with dS = P * (dP - delta)
+ * unchanged, because neither the bias nor the mask depends on the score.
+ * Layouts, workspace and launches as fa_bwd / fa_bwd_varlen; `variant` is a
+ * HOST pointer.  D must be 128, and soft-capping (softcap > 0) has no
+ * backward kernel: both return FA_ERR_UNSUPPORTED.
+ */
+fa_status_t fa_bwd_variant(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                           const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq,
+                           int Lk, int D, const fa_variant_t* variant, float softmax_scale, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+fa_status_t fa_bwd_varlen_variant(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                                  const void* dout, float* dq, float* dk, float* dv, const int* cu_seqlens_q,
+                                  const int* cu_seqlens_k, int num_seqs, int total_q, int total_k,
+                                  int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
+                                  const fa_variant_t* variant, float softmax_scale, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device-side error latch
  * of the current device: FA_ERR_TIMEOUT or FA_ERR_INVALID_ARG from an earlier
  * launch, or FA_ERR_CUDA when a kernel found its launch configuration unusable

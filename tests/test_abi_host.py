@@ -206,3 +206,20 @@ def test_bwd_varlen_argument_validation(lib):
     assert n.value >= 2 * 4 * rows * 4 + 4 * (4 * 3 + 3)
     assert lib.fa_bwd_varlen_workspace(0, 1000, 4, ctypes.byref(n)) == INV
     assert lib.fa_last_launch_count() == 0
+
+
+def test_bwd_variant_argument_validation(lib):
+    INV, UNS = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+    from exact_attention_07_gb300 import _Variant
+
+    def call(var, D=128):
+        return lib.fa_bwd_variant(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 2, 1, 64, 64, D, var, 0.1, 16, 1 << 20, None)
+
+    assert call(None) == INV
+    assert call(ctypes.byref(_Variant(-1, 0, float("nan"), None))) == INV
+    assert call(ctypes.byref(_Variant(-1, 0, 0.0, 18))) == INV        # misaligned slopes
+    assert call(ctypes.byref(_Variant(-1, 0, 0.0, None)), D=64) == UNS
+    assert call(ctypes.byref(_Variant(-1, 0, 5.0, None))) == UNS      # soft-capping: no backward kernel
+    assert lib.fa_bwd_varlen_variant(16, 16, 16, 16, 16, 16, 16, 16, 16, 32, 32, 1, 10, 10, 8, 8, 2, 2, 128, None,
+                                     0.1, 16, 1 << 20, None) == INV
+    assert lib.fa_last_launch_count() == 0

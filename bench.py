@@ -381,12 +381,18 @@ def main(argv=None):
         from workloads import grad_output
         q, k, v = (t.to(dev) for t in host_inputs)
         do = grad_output(tuple(q.shape), w.seed).to(dev)
-        o_f, lse_f = fa.fa_fwd(q, k, v, causal=w.causal)  # the forward's outputs, computed once
+        if w.window is not None:  # the forward's outputs, computed once
+            o_f, lse_f = fa.fa_fwd_variant(q, k, v, window=w.window)
+        else:
+            o_f, lse_f = fa.fa_fwd(q, k, v, causal=w.causal)
         dk_b = torch.empty(k.shape, dtype=torch.float32, device=dev)
         dv_b = torch.empty(k.shape, dtype=torch.float32, device=dev)
         ws_b = torch.empty(fa.bwd_workspace(w.B, w.Hq, w.Lq), dtype=torch.uint8, device=dev)
 
         def step(o=None, lse=None, qq=q, kk=k, vv=v):  # o receives dQ
+            if w.window is not None:
+                return fa.fa_bwd_variant(qq, kk, vv, o_f, lse_f, do, window=w.window, dq=o, dk=dk_b, dv=dv_b,
+                                         workspace=ws_b)
             return fa.fa_bwd(qq, kk, vv, o_f, lse_f, do, causal=w.causal, dq=o, dk=dk_b, dv=dv_b, workspace=ws_b)
         out_shape, lse_shape = tuple(q.shape), (w.B, w.Hq, w.Lq)
     elif w.fp8:
@@ -491,6 +497,9 @@ def main(argv=None):
                                  out=o, lse=lse)
             elif w.decode:
                 fa.fa_fwd_splitkv(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse, workspace=ws)
+            elif w.bwd and w.window is not None:
+                fa.fa_bwd_variant(d_in[0], d_in[1], d_in[2], d_in[4], d_in[5], d_in[3], window=w.window, dq=o,
+                                  dk=dk_b, dv=dv_b, workspace=ws_b)
             elif w.bwd:
                 fa.fa_bwd(d_in[0], d_in[1], d_in[2], d_in[4], d_in[5], d_in[3], causal=w.causal, dq=o, dk=dk_b,
                           dv=dv_b, workspace=ws_b)

@@ -82,7 +82,7 @@ class Workload:
             lo = np.maximum(0, c - self.window[0]) if self.window[0] >= 0 else np.zeros_like(c)
             hi = np.minimum(self.Lk - 1, c + self.window[1]) if self.window[1] >= 0 else np.full_like(c, self.Lk - 1)
             pairs = float(np.maximum(hi - lo + 1, 0).sum())
-            return dd * self.B * self.Hq * pairs
+            return dd * self.B * self.Hq * pairs * (2.5 if self.bwd else 1.0)
         if self.bwd:  # five matrix products instead of two (S, dP, dV, dQ, dK)
             total *= 2.5
         return total / 2 if self.causal else total
@@ -205,6 +205,9 @@ BWD_WORKLOADS: dict[str, Workload] = {
     "bwd_gqa_b2_h32x8_l4096_d128_causal_q3": Workload(
         "bwd_gqa_b2_h32x8_l4096_d128_causal_q3", 2, 32, 8, 4096, 4096, 128, True, q_mult=3.0, bwd=True),
     "bwd_b1_h16_l4096_d128": Workload("bwd_b1_h16_l4096_d128", 1, 16, 16, 4096, 4096, 128, False, bwd=True),
+    # the sliding-window forward workload through the variant backward
+    "bwd_swa4096_b1_h16_l16384_d128": Workload("bwd_swa4096_b1_h16_l16384_d128", 1, 16, 16, 16384, 16384, 128,
+                                               False, window=(4095, 0), bwd=True),
     # the D = 64 forward workload's shape through the backward
     "bwd_b4_h16_l1024_d64": Workload("bwd_b4_h16_l1024_d64", 4, 16, 16, 1024, 1024, 64, False, bwd=True),
     # the packed forward workload's batch through the packed backward

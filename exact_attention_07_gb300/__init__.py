@@ -508,12 +508,13 @@ def bwd_workspace(B: int, Hq: int, Lq: int) -> int:
 
 
 def fa_bwd_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
-                   dout: torch.Tensor, window=(-1, -1), alibi_slopes: torch.Tensor | None = None,
-                   softmax_scale: float | None = None, dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
-                   dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
-    """Backward of fa_fwd_variant for key windows and ALiBi (D = 128); o and lse
-    from fa_fwd_variant with the same variant."""
-    var = _variant(window, 0.0, alibi_slopes, q.shape[1], q.device)
+                   dout: torch.Tensor, window=(-1, -1), softcap: float = 0.0,
+                   alibi_slopes: torch.Tensor | None = None, softmax_scale: float | None = None,
+                   dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None, stream=None):
+    """Backward of fa_fwd_variant for key windows, soft-capping and ALiBi
+    (D = 128); o and lse from fa_fwd_variant with the same variant."""
+    var = _variant(window, softcap, alibi_slopes, q.shape[1], q.device)
     return fa_bwd(q, k, v, o, lse, dout, False, softmax_scale, dq, dk, dv, workspace, stream, variant=var)
 
 
@@ -572,12 +573,13 @@ def bwd_varlen_workspace(num_seqs: int, total_q: int, Hq: int) -> int:
 
 def fa_bwd_varlen_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
                           dout: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
-                          max_seqlen_q: int, max_seqlen_k: int, window=(-1, -1),
+                          max_seqlen_q: int, max_seqlen_k: int, window=(-1, -1), softcap: float = 0.0,
                           alibi_slopes: torch.Tensor | None = None, softmax_scale: float | None = None,
                           dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
                           dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
-    """Backward of fa_fwd_varlen_variant for key windows and ALiBi (D = 128)."""
-    var = _variant(window, 0.0, alibi_slopes, q.shape[1], q.device)
+    """Backward of fa_fwd_varlen_variant for key windows, soft-capping and
+    ALiBi (D = 128)."""
+    var = _variant(window, softcap, alibi_slopes, q.shape[1], q.device)
     return fa_bwd_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, False,
                          softmax_scale, dq, dk, dv, workspace, stream, variant=var)
 

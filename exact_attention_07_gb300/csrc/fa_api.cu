@@ -737,18 +737,24 @@ extern "C" fa_status_t fa_bwd_workspace(int B, int Hq, int Lq, size_t* workspace
 }
 
 namespace {
-// Validates a backward variant (windows and ALiBi; soft-capping has no
-// backward kernel) and fills the parameters; returns the variant kind or a
-// negative fa_status_t.
-int prepare_bwd_variant(const fa_variant_t* var, int D, BwdParams* p)
+// Validates a backward variant (windows, soft-capping, ALiBi; soft-capping
+// and ALiBi together are unsupported, as in the forward) and fills the
+// parameters; returns the variant kind or a negative fa_status_t.
+int prepare_bwd_variant(const fa_variant_t* var, int D, float scale, BwdParams* p)
 {
     if (!var) return -(int)FA_ERR_INVALID_ARG;
     if (!std::isfinite(var->softcap) || var->softcap < 0.f) return -(int)FA_ERR_INVALID_ARG;
     if (var->alibi_slopes && (reinterpret_cast<uintptr_t>(var->alibi_slopes) & 3u)) return -(int)FA_ERR_INVALID_ARG;
-    if (D != 128 || var->softcap > 0.f) return -(int)FA_ERR_UNSUPPORTED;
+    if (D != 128) return -(int)FA_ERR_UNSUPPORTED;
+    if (var->softcap > 0.f && var->alibi_slopes) return -(int)FA_ERR_UNSUPPORTED;
     p->win_left = var->window_left < 0 ? -1 : var->window_left;
     p->win_right = var->window_right < 0 ? -1 : var->window_right;
     p->alibi = var->alibi_slopes;
+    if (var->softcap > 0.f) {
+        p->cap_in2 = (float)(2.0 * 1.4426950408889634 * (double)scale / (double)var->softcap);
+        p->cap_out = (float)((double)var->softcap * 1.4426950408889634);
+        return kVarSoftcap;
+    }
     return var->alibi_slopes ? kVarAlibi : kVarWindow;
 }
 
@@ -777,7 +783,7 @@ fa_status_t bwd_dense(const void* q, const void* k, const void* v, const float* 
     BwdParams p{};
     int var = kVarNone;
     if (variant) {
-        var = prepare_bwd_variant(variant, D, &p);
+        var = prepare_bwd_variant(variant, D, softmax_scale, &p);
         if (var < 0) return (fa_status_t)(-var);
     }
     DeviceState* ds = nullptr;
@@ -909,7 +915,7 @@ fa_status_t bwd_varlen(const void* q, const void* k, const void* v, const float*
     BwdParams p{};
     int var = kVarNone;
     if (variant) {
-        var = prepare_bwd_variant(variant, D, &p);
+        var = prepare_bwd_variant(variant, D, softmax_scale, &p);
         if (var < 0) return (fa_status_t)(-var);
     }
     DeviceState* ds = nullptr;

@@ -250,6 +250,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  : "memory");
 }
 
+__device__ __forceinline__ float bwd_rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t bwd_pack_bf16(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -564,7 +571,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!bwd_warp_wait(bar(L::bQFull + qs), qph, abort_flag, wf, 79, it)) goto done;
                 if (!bwd_warp_wait(bar(L::bSFull), ph, abort_flag, wf, 80, it)) goto done;
                 tc_fence_after_sync();
-                uint32_t pk[32];  // bf16 pairs of queries 64ch + (2e, 2e+1)
+                // bf16 pairs of queries 64ch + (2e, 2e+1): P, or with soft-capping
+                // P * (1 - tanh^2), the factor dS needs
+                uint32_t pk[32];
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c = 2 * ch + cc;  // 32-query chunk of the tile
@@ -580,6 +589,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         l2[4 * u + 3] = v4.w;
                     }
                     tmem_wait_ld();
+                    uint32_t pt[16];  // soft-capping: this chunk's P for TMEM
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float b0 = -l2[e], b1 = -l2[e + 1];
@@ -589,8 +599,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             b0 = fmaf(-alibi_l2, fabsf(d0), b0);
                             b1 = fmaf(-alibi_l2, fabsf(d0 + 1.f), b1);
                         }
-                        float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), p.scale_log2, b0));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), p.scale_log2, b1));
+                        float p0, p1, g0 = 1.f, g1 = 1.f;
+                        if constexpr (VAR == kVarSoftcap) {
+                            // t = cap tanh(s scale / cap) with tanh(u) = 1 - 2 rho,
+                            // rho = 1 / (1 + e^(2u)); dt/ds = 1 - tanh^2 = 4 rho (1 - rho)
+                            const float rho0 = bwd_rcp_approx(1.f + ex2_approx(__uint_as_float(r[e]) * p.cap_in2));
+                            const float rho1 =
+                                bwd_rcp_approx(1.f + ex2_approx(__uint_as_float(r[e + 1]) * p.cap_in2));
+                            p0 = ex2_approx(fmaf(fmaf(-2.f, rho0, 1.f), p.cap_out, b0));
+                            p1 = ex2_approx(fmaf(fmaf(-2.f, rho1, 1.f), p.cap_out, b1));
+                            g0 = 4.f * rho0 * (1.f - rho0);
+                            g1 = 4.f * rho1 * (1.f - rho1);
+                        } else {
+                            p0 = ex2_approx(fmaf(__uint_as_float(r[e]), p.scale_log2, b0));
+                            p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), p.scale_log2, b1));
+                        }
                         if (need_mask) {
                             const int q = q0 + c * 32 + e;
                             if (!key_ok || (CAUSAL && kpos > q + off)) p0 = 0.f;
@@ -602,20 +625,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 if (p.win_right >= 0 && kpos > q + 1 + off + p.win_right) p1 = 0.f;
                             }
                         }
-                        pk[cc * 16 + e / 2] = bwd_pack_bf16(p0, p1);
+                        if constexpr (VAR == kVarSoftcap) {
+                            pt[e / 2] = bwd_pack_bf16(p0, p1);
+                            pk[cc * 16 + e / 2] = bwd_pack_bf16(p0 * g0, p1 * g1);
+                        } else {
+                            pk[cc * 16 + e / 2] = bwd_pack_bf16(p0, p1);
+                        }
                     }
+                    // P^T of this half goes to the first 32 of its own 64 S^T
+                    // columns (column 64ch + c holds queries 64ch + 2c, 2c + 1), which
+                    // this thread has read; the other half's columns may still be
+                    // being read by its warps
+                    if constexpr (VAR == kVarSoftcap) bwd_tmem_st16(lane_base + kColS + 64 * ch + 16 * cc, pt);
                 }
-                // the S^T columns of this half were all read above: overwrite
-                // the half's first 32 columns with its P^T (column c = queries 2c, 2c+1)
-                {
+                if constexpr (VAR != kVarSoftcap) {
                     uint32_t lo[16], hi[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         lo[e] = pk[e];
                         hi[e] = pk[16 + e];
                     }
-                    bwd_tmem_st16(lane_base + kColS + 32 * ch, lo);
-                    bwd_tmem_st16(lane_base + kColS + 32 * ch + 16, hi);
+                    bwd_tmem_st16(lane_base + kColS + 64 * ch, lo);
+                    bwd_tmem_st16(lane_base + kColS + 64 * ch + 16, hi);
                 }
                 tmem_wait_st();
                 tc_fence_before_sync();
@@ -808,7 +839,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tm + kColDV, tm + kColS + (uint32_t)(kk * 8), dO_mn + mnmaj(kk), kIdBmn,
+                        mma_ts(tm + kColDV, tm + kColS + (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)), dO_mn + mnmaj(kk),
+                               kIdBmn,
                                (s > 0 || kk > 0) ? 1u : 0u);
                 }
                 __syncwarp();
@@ -937,6 +969,9 @@ cudaError_t launch_bwd_variant(int var, bool varlen, const CUtensorMap& q, const
     if (var == kVarWindow)
         return varlen ? launch_bwd_kernel<128, false, true, kVarWindow>(q, k, v, dout, p, grid, stream)
                       : launch_bwd_kernel<128, false, false, kVarWindow>(q, k, v, dout, p, grid, stream);
+    if (var == kVarSoftcap)
+        return varlen ? launch_bwd_kernel<128, false, true, kVarSoftcap>(q, k, v, dout, p, grid, stream)
+                      : launch_bwd_kernel<128, false, false, kVarSoftcap>(q, k, v, dout, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 #endif

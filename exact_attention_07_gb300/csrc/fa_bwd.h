@@ -44,6 +44,8 @@ struct BwdParams {
     // head (natural-log units)
     int win_left, win_right;
     const float* alibi;
+    // soft-capping (VAR = kVarSoftcap): 2 log2(e) scale / cap and cap log2(e)
+    float cap_in2, cap_out;
     float scale;            // softmax_scale (multiplies dS)
     float scale_log2;       // softmax_scale * log2(e)
     int causal;
@@ -56,8 +58,8 @@ cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t 
 cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
                        cudaStream_t stream);
-// Variants (var = kVarWindow or kVarAlibi, D = 128, no separate causal flag:
-// a causal window is (-1, 0)).
+// Variants (var = kVarWindow, kVarSoftcap or kVarAlibi, D = 128, no separate
+// causal flag: a causal window is (-1, 0)).
 cudaError_t launch_bwd_variant(int var, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
                                const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
                                cudaStream_t stream);

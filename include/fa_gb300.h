@@ -327,13 +327,15 @@ fa_status_t fa_bwd_varlen(const void* q, const void* k, const void* v, const flo
 fa_status_t fa_bwd_varlen_workspace(int num_seqs, int total_q, int Hq, size_t* workspace_bytes);
 
 /*
- * Backward of fa_fwd_variant / fa_fwd_varlen_variant for key windows and ALiBi
- * (FlashAttention from Scratch, sec. 12): the same modified scores and masks
- * as the forward (pass the forward's O and LSE), with dS = P * (dP - delta)
- * unchanged, because neither the bias nor the mask depends on the score.
+ * Backward of fa_fwd_variant / fa_fwd_varlen_variant for key windows,
+ * soft-capping and ALiBi (FlashAttention from Scratch, sec. 12): the same
+ * modified scores t and masks as the forward (pass the forward's O and LSE).
+ * The gradient with respect to t is P * (dP - delta); the ALiBi bias and the
+ * masks do not depend on the raw score s, so that is dS, while soft-capping
+ * (t = cap * tanh(s / cap)) multiplies it by dt/ds = 1 - tanh^2(s / cap).
  * Layouts, workspace and launches as fa_bwd / fa_bwd_varlen; `variant` is a
- * HOST pointer.  D must be 128, and soft-capping (softcap > 0) has no
- * backward kernel: both return FA_ERR_UNSUPPORTED.
+ * HOST pointer.  D must be 128, and soft-capping with ALiBi is unsupported,
+ * as in the forward: both return FA_ERR_UNSUPPORTED.
  */
 fa_status_t fa_bwd_variant(const void* q, const void* k, const void* v, const float* o, const float* lse,
                            const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq,

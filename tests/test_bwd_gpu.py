@@ -184,39 +184,43 @@ def test_bwd_varlen_single_sequence_equals_dense():
     assert np.abs(dq.cpu().numpy() - a[0][0].transpose(1, 0, 2)).max() <= 1e-4 * np.abs(a[0]).max()
 
 
-# ------------------------------------------------------------------ variants (windows, ALiBi)
+# ------------------------------------------------------------------ variants (windows, soft-capping, ALiBi)
 
 BWD_VARIANT_CASES = [
-    # B, Hq, Hkv, Lq, Lk, window, alibi
-    (1, 2, 2, 384, 384, (127, 0), False),     # causal window of width 128
-    (1, 2, 1, 513, 513, (300, 0), False),     # window edge inside tiles, GQA
-    (1, 2, 2, 300, 700, (200, 50), False),    # two-sided, Lq < Lk
-    (1, 2, 2, 700, 300, (64, 64), False),     # Lq > Lk: rows without keys
-    (1, 2, 2, 256, 256, (-1, 0), False),      # plain causal as a window
-    (2, 4, 2, 333, 333, (-1, -1), True),      # ALiBi, full
-    (1, 4, 4, 400, 400, (255, 0), True),      # ALiBi inside a causal window
+    # B, Hq, Hkv, Lq, Lk, window, cap, alibi, Q multiplier
+    (1, 2, 2, 384, 384, (127, 0), 0.0, False, 1.0),     # causal window of width 128
+    (1, 2, 1, 513, 513, (300, 0), 0.0, False, 1.0),     # window edge inside tiles, GQA
+    (1, 2, 2, 300, 700, (200, 50), 0.0, False, 1.0),    # two-sided, Lq < Lk
+    (1, 2, 2, 700, 300, (64, 64), 0.0, False, 1.0),     # Lq > Lk: rows without keys
+    (1, 2, 2, 256, 256, (-1, 0), 0.0, False, 1.0),      # plain causal as a window
+    (2, 4, 2, 333, 333, (-1, -1), 0.0, True, 1.0),      # ALiBi, full
+    (1, 4, 4, 400, 400, (255, 0), 0.0, True, 1.0),      # ALiBi inside a causal window
+    (1, 2, 2, 384, 384, (-1, -1), 5.0, False, 4.0),     # soft cap 5, scores ~ N(0, 16): tanh saturates
+    (1, 4, 2, 333, 517, (-1, 0), 30.0, False, 6.0),     # soft cap 30, causal, GQA, ragged, Lq < Lk
+    (2, 2, 2, 300, 300, (100, 20), 2.0, False, 3.0),    # soft cap 2 inside a two-sided window
 ]
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,window,alibi", BWD_VARIANT_CASES)
-def test_bwd_variant_full_compare(B, Hq, Hkv, Lq, Lk, window, alibi):
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,window,cap,alibi,qm", BWD_VARIANT_CASES)
+def test_bwd_variant_full_compare(B, Hq, Hkv, Lq, Lk, window, cap, alibi, qm):
     from oracle.variants import attention_variant_bwd
     D = 128
-    seed = Lq + 2 * Lk + Hq + (7 if alibi else 0)
-    q, k, v = random_inputs((B, Hq, Lq, D), (B, Hkv, Lk, D), seed=seed)
+    seed = Lq + 2 * Lk + Hq + (7 if alibi else 0) + int(cap)
+    q, k, v = random_inputs((B, Hq, Lq, D), (B, Hkv, Lk, D), seed=seed, q_mult=qm)
     do = grad_output((B, Hq, Lq, D), seed)
     slopes = torch.tensor([2.0 ** (-(h + 1)) for h in range(Hq)], dtype=torch.float32) if alibi else None
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
     sd = slopes.to(DEV) if alibi else None
-    o, lse = fa.fa_fwd_variant(qd, kd, vd, window=window, alibi_slopes=sd)
+    o, lse = fa.fa_fwd_variant(qd, kd, vd, window=window, softcap=cap, alibi_slopes=sd)
     dq = torch.full(q.shape, float("nan"), dtype=torch.float32, device=DEV)
     dk = torch.full(k.shape, float("nan"), dtype=torch.float32, device=DEV)
     dv = torch.full(k.shape, float("nan"), dtype=torch.float32, device=DEV)
-    fa.fa_bwd_variant(qd, kd, vd, o, lse, dod, window=window, alibi_slopes=sd, dq=dq, dk=dk, dv=dv)
+    fa.fa_bwd_variant(qd, kd, vd, o, lse, dod, window=window, softcap=cap, alibi_slopes=sd, dq=dq, dk=dk, dv=dv)
     fa.fa_check()
-    ref = attention_variant_bwd(q, k, v, do, 1 / math.sqrt(D), window, 0.0,
+    ref = attention_variant_bwd(q, k, v, do, 1 / math.sqrt(D), window, cap,
                                 slopes.numpy() if alibi else None)
-    compare_grads((dq.cpu().numpy(), dk.cpu().numpy(), dv.cpu().numpy()), ref, f"bwd variant {window} {alibi}")
+    compare_grads((dq.cpu().numpy(), dk.cpu().numpy(), dv.cpu().numpy()), ref,
+                  f"bwd variant {window} cap {cap} alibi {alibi}")
 
 
 def test_bwd_causal_window_equals_causal():
@@ -232,18 +236,20 @@ def test_bwd_causal_window_equals_causal():
     assert np.abs(b[0].cpu().numpy() - a[0]).max() <= 1e-4 * np.abs(a[0]).max()
 
 
-def test_bwd_varlen_variant_full_compare():
+@pytest.mark.parametrize("window,cap,qm", [((100, 0), 0.0, 1.0), ((-1, 0), 8.0, 4.0)])
+def test_bwd_varlen_variant_full_compare(window, cap, qm):
     from oracle.variants import attention_variant_bwd_varlen
     lq, lk, Hq, Hkv, D = [200, 5, 400, 129], [260, 5, 400, 129], 4, 2, 128
-    window = (100, 0)
     Tq, Tk = sum(lq), sum(lk)
-    q, k, v = random_inputs((Tq, Hq, D), (Tk, Hkv, D), seed=61)
+    q, k, v = random_inputs((Tq, Hq, D), (Tk, Hkv, D), seed=61, q_mult=qm)
     do = grad_output((Tq, Hq, D), 61)
     cq = torch.tensor([0] + np.cumsum(lq).tolist(), dtype=torch.int32, device=DEV)
     ck = torch.tensor([0] + np.cumsum(lk).tolist(), dtype=torch.int32, device=DEV)
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
-    o, lse = fa.fa_fwd_varlen_variant(qd, kd, vd, cq, ck, max(lq), max(lk), window=window)
-    dq, dk, dv = fa.fa_bwd_varlen_variant(qd, kd, vd, o, lse, dod, cq, ck, max(lq), max(lk), window=window)
+    o, lse = fa.fa_fwd_varlen_variant(qd, kd, vd, cq, ck, max(lq), max(lk), window=window, softcap=cap)
+    dq, dk, dv = fa.fa_bwd_varlen_variant(qd, kd, vd, o, lse, dod, cq, ck, max(lq), max(lk), window=window,
+                                          softcap=cap)
     fa.fa_check()
-    ref = attention_variant_bwd_varlen(q, k, v, do, cq.cpu().numpy(), ck.cpu().numpy(), 1 / math.sqrt(D), window)
-    compare_grads((dq.cpu().numpy(), dk.cpu().numpy(), dv.cpu().numpy()), ref, "varlen bwd window")
+    ref = attention_variant_bwd_varlen(q, k, v, do, cq.cpu().numpy(), ck.cpu().numpy(), 1 / math.sqrt(D), window,
+                                       cap)
+    compare_grads((dq.cpu().numpy(), dk.cpu().numpy(), dv.cpu().numpy()), ref, f"varlen bwd window cap {cap}")

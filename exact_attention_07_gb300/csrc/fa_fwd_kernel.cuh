@@ -239,6 +239,27 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
+// Three barrier phases tested by back-to-back try_waits of one thread (all
+// lanes execute it, so the warp stays converged): the three shared-memory
+// round trips overlap.  True when all three phases have completed.
+__device__ __forceinline__ bool mbar_try_wait3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2,
+                                               uint32_t p2)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred q0, q1, q2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+        "and.pred q0, q0, q1;\n\t"
+        "and.pred q0, q0, q2;\n\t"
+        "selp.u32 %0, 1, 0, q0;\n\t}\n"
+        : "=r"(ok)
+        : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+        : "memory");
+    return ok != 0;
+}
+
 // MMA issue sequences of one 128 x 128 x D tile product, executed by the whole
 // (converged) MMA warp with lane 0 issuing.  Operands computed in converged
 // code stay warp-uniform, and the k-loops are fully unrolled, so tcgen05.mma
@@ -829,24 +850,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nk == 1) commit(L::kQEmpty + 1);
                 bool ok = true;
                 for (int j = 0; j < nk && ok; ++j) {
-                    // V(j) and K(j+1) are checked before P is awaited, so that P.V and the
-                    // next S issue back to back once P arrives
+                    // V(j), K(j+1) and P0(j): in the steady state all three have
+                    // completed when the warp gets here, and one combined test costs one
+                    // shared-memory round trip; otherwise they are awaited one by one
                     const int vs = stage;
-                    if (!(ok = warp_wait(bar(L::kKVFull + vs), kv_ph, abort_flag, wf, 18, tile))) break;
+                    const uint32_t vph = kv_ph;
                     next_stage();
                     int kn = -1, tn = 0;
+                    uint32_t kph = vph;
                     if (j + 1 < nk) {
                         kn = stage;
-                        if (!(ok = warp_wait(bar(L::kKVFull + kn), kv_ph, abort_flag, wf, 17, tile))) break;
+                        kph = kv_ph;
                         next_stage();
-                        if (!(ok = take_tail(tile, tn))) break;
                     }
+                    const bool all3 = j > 0 &&
+                        __all_sync(0xffffffffu, mbar_try_wait3(bar(L::kKVFull + vs), vph,
+                                                               bar(L::kKVFull + (kn >= 0 ? kn : vs)), kph,
+                                                               bar(L::kPFull + 0), p_ph[0]));
+                    if (!all3) {
+                        if (!(ok = warp_wait(bar(L::kKVFull + vs), vph, abort_flag, wf, 18, tile))) break;
+                        if (kn >= 0 && !(ok = warp_wait(bar(L::kKVFull + kn), kph, abort_flag, wf, 17, tile))) break;
+                    }
+                    if (kn >= 0 && !(ok = take_tail(tile, tn))) break;
                     // tile 0: P0(j) . V(j), then S0(j+1)
                     if (j == 0) {
                         if (!(ok = warp_wait(bar(L::kOEmpty + 0), oe_ph[0], abort_flag, wf, 19, tile))) break;
                         oe_ph[0] ^= 1;
                     }
-                    if (!(ok = warp_wait(bar(L::kPFull + 0), p_ph[0], abort_flag, wf, 21, tile))) break;
+                    if (!all3 && !(ok = warp_wait(bar(L::kPFull + 0), p_ph[0], abort_flag, wf, 21, tile))) break;
                     p_ph[0] ^= 1;
                     tc_fence_after_sync();
                     mma_pv<D, VAR, DV>(tm, sb, 0, vs, j > 0, leader);

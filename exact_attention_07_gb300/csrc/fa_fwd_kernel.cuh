@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using L = FwdSmem<D, VAR, DV>;
     constexpr bool kAlternate = CAUSAL || VARLEN || var_window(VAR);  // tiles of unequal length
+    constexpr bool kSoftmaxFreesKV = !L::kTail && !L::kFp8;  // who frees K/V ring stages (see the softmax role)
     constexpr float kTau = 8.0f;     // rescale threshold, log2 units
     constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -425,6 +426,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * DV);
         const float sl2 = p.scale_log2;
         uint32_t s_ph = 0, st_ph = 1;
+        // K/V ring slots taken before the current work tile (K(0), V(0), K(1), ...)
+        uint32_t kv_seq = 0;
+        // The first thread of the tile-1 group frees the K/V stages (a commit
+        // costs the MMA warp about 100 cycles of tensor-pipe idle time): S1(j)
+        // complete means every MMA issued before it has completed -- S0(j),
+        // P0(j-1).V(j-1) and P1(j-1).V(j-1) -- so K(j) and V(j-1) are no longer
+        // read.  (The MMA warp frees the last V of a work tile.)  A three-stage
+        // ring (D > DV) cannot wait that long for V(j-1), and with e4m3 operands
+        // the softmax, not the MMA warp, bounds the step: in both the MMA warp
+        // commits every release as soon as the MMAs reading the stage are issued.
+        const bool kv_releaser = kSoftmaxFreesKV && t == 1 && row == 0;
         for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
             const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, tile);
             if (w.nk == 0) continue;
@@ -455,6 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < w.nk; ++j) {
                 if (!warp_wait(bar(L::kSFull + t), s_ph, abort_flag, wf, 1 + t, tile)) goto done;
                 s_ph ^= 1;
+                if (kv_releaser) {
+                    mbar_arrive(bar(L::kKVEmpty + (int)((kv_seq + 2u * (uint32_t)j) % (uint32_t)L::kStages)));
+                    if (j > 0)
+                        mbar_arrive(bar(L::kKVEmpty + (int)((kv_seq + 2u * (uint32_t)j - 1u) % (uint32_t)L::kStages)));
+                }
                 tc_fence_after_sync();
                 uint32_t sv[4][32];
                 // the tensor-memory load also returns each chunk's maximum when the
@@ -616,6 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(L::kPFull + t));
                 r = r_new;
             }
+            kv_seq += 2u * (uint32_t)w.nk;
             // hand the row statistics to the epilogue
             if (!warp_wait(bar(L::kStEmpty + t), st_ph, abort_flag, wf, 3 + t, tile)) goto done;
             st_ph ^= 1;
@@ -845,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 mma_qk<D, VAR, DV>(tm, sb, 1, ks, ts, leader);
                 commit(L::kSFull + 1);
-                commit(L::kKVEmpty + ks);
+                if constexpr (!kSoftmaxFreesKV) commit(L::kKVEmpty + ks);
                 release_tail(ts);
                 if (nk == 1) commit(L::kQEmpty + 1);
                 bool ok = true;
@@ -897,15 +915,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p_ph[1] ^= 1;
                     tc_fence_after_sync();
                     mma_pv<D, VAR, DV>(tm, sb, 1, vs, j > 0, leader);
-                    commit(L::kKVEmpty + vs);
+                    if constexpr (!kSoftmaxFreesKV) commit(L::kKVEmpty + vs);
                     if (kn >= 0) {
                         mma_qk<D, VAR, DV>(tm, sb, 1, kn, tn, leader);
                         commit(L::kSFull + 1);
-                        commit(L::kKVEmpty + kn);
+                        if constexpr (!kSoftmaxFreesKV) commit(L::kKVEmpty + kn);
                         release_tail(tn);
                         if (j + 2 == nk) commit(L::kQEmpty + 1);
                     } else {
                         commit(L::kOFull + 1);
+                        if constexpr (kSoftmaxFreesKV) commit(L::kKVEmpty + vs);  // the work tile's last V
                     }
                 }
                 if (!ok) break;

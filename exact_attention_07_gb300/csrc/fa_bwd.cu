@@ -263,6 +263,27 @@ __device__ __forceinline__ uint32_t bwd_pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Three barrier phases tested by back-to-back try_waits of one thread (all
+// lanes execute it, so the warp stays converged): the shared-memory round
+// trips overlap.  True when all three phases have completed.
+__device__ __forceinline__ bool bwd_try_wait3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2,
+                                              uint32_t p2)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred q0, q1, q2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+        "and.pred q0, q0, q1;\n\t"
+        "and.pred q0, q0, q2;\n\t"
+        "selp.u32 %0, 1, 0, q0;\n\t}\n"
+        : "=r"(ok)
+        : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool bwd_warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                               const WaitFailure& wf, int site, int item)
 {
@@ -459,6 +480,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bwd_step(p, w, s, h, i);
                 if (!bwd_warp_wait(bar(L::bDQFull), gstep & 1u, abort_flag, wf, 84, it)) goto done;
                 tc_fence_after_sync();
+                // dK and dQ have completed: their operands dS^T and Q(step) are free.
+                // Released here rather than by MMA-warp commits, each of which holds
+                // the MMA warp for about 100 cycles with the tensor pipe idle.
+                if (t == 0) {
+                    mbar_arrive(bar(L::bDSEmpty));
+                    mbar_arrive(bar(L::bQEmpty + (int)(gstep % L::kQStages)));
+                }
                 const int q0 = i * kBwdTile;
                 const int nrows = min(kBwdTile, w.lq - q0);
                 // dQ rows: dense [B, Hq, Lq, D], packed [Tq, Hq, D]
@@ -820,9 +848,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 const uint32_t qs = gstep % L::kQStages;
                 const uint64_t q_mn = smem_desc_sw128(sb + L::kQ + qs * L::kTile, kHalf, 1024);
-                // dP^T = V dO^T; its columns held the previous step's dQ
-                if (!(ok = bwd_warp_wait(bar(L::bDQEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 91, it))) break;
-                if (!(ok = bwd_warp_wait(bar(L::bDOFull), gstep & 1u, abort_flag, wf, 101, it))) break;
+                // dP^T = V dO^T; its columns held the previous step's dQ.  The waits of
+                // the MMA warp are tested together first (one shared-memory round trip
+                // when, as usual, the phases have completed), then one by one.
+                const bool ready1 = __all_sync(0xffffffffu, bwd_try_wait3(bar(L::bDQEmpty), (gstep & 1u) ^ 1u,
+                                                                          bar(L::bDOFull), gstep & 1u,
+                                                                          bar(L::bDOFull), gstep & 1u));
+                if (!ready1) {
+                    if (!(ok = bwd_warp_wait(bar(L::bDQEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 91, it))) break;
+                    if (!(ok = bwd_warp_wait(bar(L::bDOFull), gstep & 1u, abort_flag, wf, 101, it))) break;
+                }
                 tc_fence_after_sync();
                 if (leader) {
 #pragma unroll
@@ -831,10 +866,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 __syncwarp();
                 commit(L::bDPFull);
-                // dV += P^T dO
-                if (!(ok = bwd_warp_wait(bar(L::bPFull), gstep & 1u, abort_flag, wf, 92, it))) break;
-                if (s == 0 && !(ok = bwd_warp_wait(bar(L::bDKVEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 93, it)))
-                    break;
+                // dV += P^T dO (P^T; at an item's first step the dK/dV accumulators;
+                // and the next step's Q, tested with them)
+                const bool has_next = s + 1 < w.steps;
+                const uint32_t q1 = (gstep + 1) % L::kQStages, ph1 = ((gstep + 1) / L::kQStages) & 1u;
+                const uint32_t bp = bar(L::bPFull), pp = gstep & 1u;
+                const bool ready2 = __all_sync(
+                    0xffffffffu,
+                    bwd_try_wait3(bp, pp, s == 0 ? bar(L::bDKVEmpty) : bp, s == 0 ? ((uint32_t)(I & 1) ^ 1u) : pp,
+                                  has_next ? bar(L::bQFull + q1) : bp, has_next ? ph1 : pp));
+                if (!ready2) {
+                    if (!(ok = bwd_warp_wait(bp, pp, abort_flag, wf, 92, it))) break;
+                    if (s == 0 &&
+                        !(ok = bwd_warp_wait(bar(L::bDKVEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 93, it)))
+                        break;
+                }
                 tc_fence_after_sync();
                 if (leader) {
 #pragma unroll
@@ -846,10 +892,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __syncwarp();
                 commit(L::bDOEmpty);  // dO's last reader
                 // next step's S^T: P^T of this step has been consumed (MMAs run in order)
-                if (s + 1 < w.steps) {
-                    const uint32_t q1 = (gstep + 1) % L::kQStages, ph1 = ((gstep + 1) / L::kQStages) & 1u;
-                    if (!(ok = bwd_warp_wait(bar(L::bQFull + q1), ph1, abort_flag, wf, 90, it))) break;
-                    tc_fence_after_sync();
+                if (has_next) {
+                    if (!ready2) {
+                        if (!(ok = bwd_warp_wait(bar(L::bQFull + q1), ph1, abort_flag, wf, 90, it))) break;
+                        tc_fence_after_sync();
+                    }
                     mma_s(q1);
                     commit(L::bSFull);
                 }
@@ -872,9 +919,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                 }
                 __syncwarp();
-                commit(L::bDQFull);
-                commit(L::bDSEmpty);
-                commit(L::bQEmpty + qs);  // Q's last reader is dK
+                commit(L::bDQFull);  // the dQ warps then free dS^T and Q (stage qs)
             }
             if (!ok) break;
             commit(L::bDKVFull);

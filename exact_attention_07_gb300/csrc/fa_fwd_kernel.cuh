@@ -76,7 +76,14 @@ struct FwdSmem {
                          kDrain = kSFull + 12, kNumBars = kSFull + 13;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;      // tmem base, abort flag
     static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;  // float2 [2][128]
-    static constexpr int kBytes = kStatsOff + 2 * kBlockM * 8;
+    // epilogue staging: per epilogue warp one 32 x 32 fp32 block, rows padded
+    // to 36 floats (conflict-free 16-byte accesses by row and by column group);
+    // left out where shared memory has no room for it (D > DV) and for e4m3
+    // inputs (the epilogue's 64 registers then spill; measured slower)
+    static constexpr int kEpiRowBytes = 36 * 4, kEpiWarpBytes = 32 * kEpiRowBytes;
+    static constexpr bool kEpiStaged = !kTail && !kFp8;
+    static constexpr int kEpiOff = kStatsOff + 2 * kBlockM * 8;
+    static constexpr int kBytes = kEpiOff + (kEpiStaged ? 4 * kEpiWarpBytes : 0);
     // 1 KB of slack for aligning the window where it fits; otherwise the kernel
     // checks the alignment at run time
     static constexpr int kMaxDynamic = 232448;
@@ -210,6 +217,14 @@ __device__ __forceinline__ float2 e4m3x2_unpack(uint16_t v)
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void fence_proxy_async_shared()
@@ -681,18 +696,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float inv = st.x > 0.f ? 1.f / st.x : 0.f;
                 if constexpr (VAR == kVarFp8) inv *= __ldg(p.fp8_sv + (long long)w.b * p.Hkv + w.hkv);
                 const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * DV);
+                if constexpr (L::kEpiStaged) {
+                    // Each 32 x 32 block of the warp's rows goes through shared memory:
+                    // a thread writes its own row, then every store instruction writes
+                    // four whole 128-byte row segments (a thread per row would touch
+                    // 32 scattered sectors per instruction).
+                    const uint32_t stage = sb + L::kEpiOff + (uint32_t)((warp & 3) * L::kEpiWarpBytes);
+                    const int rsub = lane >> 3, cq = lane & 7;  // row within a group of four, 16-byte column
+                    const int wrow0 = w.m0 + t * kBlockM + 32 * (warp & 3);
+                    const int64_t rstride = VARLEN ? (int64_t)p.Hq * DV : (int64_t)DV;
+                    float* wbase = obase + (VARLEN ? ((int64_t)(w.q0 + wrow0) * p.Hq + w.hq) * DV
+                                                   : (((int64_t)w.b * p.Hq + w.hq) * p.Lq + wrow0) * DV);
 #pragma unroll 1
-                for (int c = 0; c < DV / 32; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld32(tO + 32u * c, ov);
-                    tmem_wait_ld();
-                    if (valid) {
+                    for (int c = 0; c < DV / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + 32u * c, ov);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[8 * c + i] = make_uint4(__float_as_uint(__uint_as_float(ov[4 * i]) * inv),
-                                                        __float_as_uint(__uint_as_float(ov[4 * i + 1]) * inv),
-                                                        __float_as_uint(__uint_as_float(ov[4 * i + 2]) * inv),
-                                                        __float_as_uint(__uint_as_float(ov[4 * i + 3]) * inv));
+                        for (int u = 0; u < 8; ++u)
+                            st_shared_v4(stage + (uint32_t)(lane * L::kEpiRowBytes + 16 * u),
+                                         __float_as_uint(__uint_as_float(ov[4 * u]) * inv),
+                                         __float_as_uint(__uint_as_float(ov[4 * u + 1]) * inv),
+                                         __float_as_uint(__uint_as_float(ov[4 * u + 2]) * inv),
+                                         __float_as_uint(__uint_as_float(ov[4 * u + 3]) * inv));
+                        __syncwarp();
+#pragma unroll
+                        for (int k4 = 0; k4 < 8; ++k4) {
+                            const int r = 4 * k4 + rsub;
+                            const uint4 v = ld_shared_v4(stage + (uint32_t)(r * L::kEpiRowBytes + 16 * cq));
+                            if (wrow0 + r < w.lq)
+                                *reinterpret_cast<uint4*>(wbase + r * rstride + 32 * c + 4 * cq) = v;
+                        }
+                        __syncwarp();
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < DV / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + 32u * c, ov);
+                        tmem_wait_ld();
+                        if (valid) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                dst[8 * c + i] = make_uint4(__float_as_uint(__uint_as_float(ov[4 * i]) * inv),
+                                                            __float_as_uint(__uint_as_float(ov[4 * i + 1]) * inv),
+                                                            __float_as_uint(__uint_as_float(ov[4 * i + 2]) * inv),
+                                                            __float_as_uint(__uint_as_float(ov[4 * i + 3]) * inv));
+                        }
                     }
                 }
                 tc_fence_before_sync();

@@ -507,58 +507,113 @@ def main(argv=None):
         h_extra = []  # dK and dV of the backward
         if w.bwd:
             h_extra = [torch.empty(dk_b.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
-        d_in = [torch.empty_like(t, device=dev) for t in pin]
+        # Two slots of device inputs and outputs, so that a step's copies can
+        # overlap the neighbouring steps' kernels: step i's host->device copy runs
+        # on one copy stream, its kernels on the compute stream, its
+        # device->host read on another copy stream.  Every step still moves all
+        # of its inputs and outputs.
+        slots = 2
+        d_ins = [[torch.empty_like(t, device=dev) for t in pin] for _ in range(slots)]
+        if w.bwd:
+            d_outs = [(torch.empty_like(o), torch.empty_like(dk_b), torch.empty_like(dv_b)) for _ in range(slots)]
+        else:
+            d_outs = [(torch.empty_like(o), torch.empty_like(lse)) for _ in range(slots)]
 
-        def e2e_step():
-            for d, h in zip(d_in, pin):
-                d.copy_(h, non_blocking=True)
+        def call(d_in, outs):
+            """One step of the public API on device buffers (on the current stream)."""
+            if w.bwd:
+                dq_o, dk_o, dv_o = outs
+            else:
+                o_o, l_o = outs
             if w.varlen and w.bwd:  # Q, K, V, cu_q, cu_k, dO, O, LSE
                 fa.fa_bwd_varlen(d_in[0], d_in[1], d_in[2], d_in[6], d_in[7], d_in[5], d_in[3], d_in[4], maxl, maxl,
-                                 causal=w.causal, dq=o, dk=dk_b, dv=dv_b, workspace=ws_b)
+                                 causal=w.causal, dq=dq_o, dk=dk_o, dv=dv_o, workspace=ws_b)
             elif w.varlen:
                 fa.fa_fwd_varlen(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], maxl, maxl, causal=w.causal,
-                                 out=o, lse=lse)
+                                 out=o_o, lse=l_o)
             elif w.decode:
-                fa.fa_fwd_splitkv(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse, workspace=ws)
+                fa.fa_fwd_splitkv(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o_o, lse=l_o, workspace=ws)
             elif w.bwd and w.window is not None:
-                fa.fa_bwd_variant(d_in[0], d_in[1], d_in[2], d_in[4], d_in[5], d_in[3], window=w.window, dq=o,
-                                  dk=dk_b, dv=dv_b, workspace=ws_b)
+                fa.fa_bwd_variant(d_in[0], d_in[1], d_in[2], d_in[4], d_in[5], d_in[3], window=w.window, dq=dq_o,
+                                  dk=dk_o, dv=dv_o, workspace=ws_b)
             elif w.bwd:
-                fa.fa_bwd(d_in[0], d_in[1], d_in[2], d_in[4], d_in[5], d_in[3], causal=w.causal, dq=o, dk=dk_b,
-                          dv=dv_b, workspace=ws_b)
+                fa.fa_bwd(d_in[0], d_in[1], d_in[2], d_in[4], d_in[5], d_in[3], causal=w.causal, dq=dq_o, dk=dk_o,
+                          dv=dv_o, workspace=ws_b)
             elif w.window is not None:
-                fa.fa_fwd_variant(d_in[0], d_in[1], d_in[2], window=w.window, out=o, lse=lse)
+                fa.fa_fwd_variant(d_in[0], d_in[1], d_in[2], window=w.window, out=o_o, lse=l_o)
             elif w.fp8:  # bf16 inputs from the host, prepared and attended on the device
                 fa.fp8_prepare(d_in[0], d_in[1], d_in[2], signs_d, prepared=prep)
-                fa.fa_fwd_fp8(prep, w.B, w.Hq, w.Hkv, w.Lq, w.Lk, causal=w.causal, out=o, lse=lse)
+                fa.fa_fwd_fp8(prep, w.B, w.Hq, w.Hkv, w.Lq, w.Lk, causal=w.causal, out=o_o, lse=l_o)
             elif w.Dv != w.D:
-                fa.fa_fwd_hdim(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse)
+                fa.fa_fwd_hdim(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o_o, lse=l_o)
             else:
-                fa.fa_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o, lse=lse)
-            h_o.copy_(o, non_blocking=True)
+                fa.fa_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, out=o_o, lse=l_o)
+
+        def read_back(outs):
+            h_o.copy_(outs[0], non_blocking=True)
             if w.bwd:
-                h_extra[0].copy_(dk_b, non_blocking=True)
-                h_extra[1].copy_(dv_b, non_blocking=True)
+                h_extra[0].copy_(outs[1], non_blocking=True)
+                h_extra[1].copy_(outs[2], non_blocking=True)
             else:
-                h_l.copy_(lse, non_blocking=True)
-        for _ in range(3):
-            e2e_step()
-        barrier()
-        s2 = torch.cuda.Event(enable_timing=True)
-        e2_ = torch.cuda.Event(enable_timing=True)
-        s2.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e2_.record(stream)
-        barrier()
-        fa.fa_check()
-        e2e_secs = s2.elapsed_time(e2_) / 1e3
+                h_l.copy_(outs[1], non_blocking=True)
+
+        def serial_step():
+            for d, h in zip(d_ins[0], pin):
+                d.copy_(h, non_blocking=True)
+            call(d_ins[0], d_outs[0])
+            read_back(d_outs[0])
+
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(slots)]
+        ev_k = [torch.cuda.Event() for _ in range(slots)]
+        ev_out = [torch.cuda.Event() for _ in range(slots)]
+
+        def pipelined_step(i):
+            sl = i % slots
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_k[sl])  # the kernels two steps back are done with these inputs
+                for d, h in zip(d_ins[sl], pin):
+                    d.copy_(h, non_blocking=True)
+                ev_in[sl].record(s_in)
+            stream.wait_event(ev_in[sl])
+            stream.wait_event(ev_out[sl])  # the read-back two steps back is done with these outputs
+            call(d_ins[sl], d_outs[sl])
+            ev_k[sl].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_k[sl])
+                read_back(d_outs[sl])
+                ev_out[sl].record(s_out)
+
+        def timed(run, n):
+            barrier()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for i in range(n):
+                run(i)
+            for e in ev_out:
+                stream.wait_event(e)
+            t1.record(stream)
+            barrier()
+            fa.fa_check()
+            return t0.elapsed_time(t1) / 1e3
+
+        for i in range(3):
+            serial_step()
+        ser_secs = timed(lambda i: serial_step(), args.e2e_steps)
+        for i in range(3):
+            pipelined_step(i)
+        e2e_secs = timed(pipelined_step, args.e2e_steps)
         e2e_rate, e2e_secs = job_rate(e2e_secs, flops_step * args.e2e_steps, world, dev)
+        ser_rate, ser_secs = job_rate(ser_secs, flops_step * args.e2e_steps, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in pin)
         d2h = h_o.numel() * 4 + (sum(t.numel() * 4 for t in h_extra) if w.bwd else h_l.numel() * 4)
         e2e = {"value": e2e_rate / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_secs / args.e2e_steps * 1e3}
+               "ms_per_step": e2e_secs / args.e2e_steps * 1e3,
+               "pipelined": "2 slots: step i's host->device copy and step i-1's read-back overlap other steps' "
+                            "kernels on their own streams",
+               "serial": {"value": ser_rate / 1e12, "ms_per_step": ser_secs / args.e2e_steps * 1e3,
+                          "note": "copy in, compute, read back, one step at a time on one stream"}}
 
     # ---- roofline of the attention kernel (the only kernel of a dense step)
     peak, peak_sus, peak_kind = measured_peaks()

@@ -95,6 +95,20 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D fp32 tensor map without swizzle: box = {box0, box1, box2} elements
+// (the backward's dQ reduce-adds).
+bool encode_map_f32(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1, uint32_t box2)
+{
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {box0, box1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // D_kv = the K and V elements of one key (D + Dv)
 int heads_per_section(int Hkv, long long Lk, int D_kv)
 {
@@ -797,6 +811,9 @@ fa_status_t bwd_dense(const void* q, const void* k, const void* v, const float* 
         !encode_map(&mk, k, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kBwdTile, 1) ||
         !encode_map(&mv, v, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kBwdTile, 1))
         return FA_ERR_CUDA;
+    CUtensorMap mdq;  // dQ reduce-adds: [64 rows][32 columns] fp32 boxes
+    if (!encode_map_f32(&mdq, dq, D, Lq, (uint64_t)B * Hq, (uint64_t)D * 4, (uint64_t)D * 4 * Lq, 32, 64, 1))
+        return FA_ERR_CUDA;
 
     p.o = o;
     p.lse = lse;
@@ -826,8 +843,8 @@ fa_status_t bwd_dense(const void* q, const void* k, const void* v, const float* 
     g_fault_next = 0;
     if (launch_bwd_pre(D, false, p, stream) != cudaSuccess) return FA_ERR_CUDA;
     const int grid = (int)(items < ds->num_sms ? items : ds->num_sms);
-    const cudaError_t e = variant ? launch_bwd_variant(var, false, mq, mk, mv, mdo, p, grid, stream)
-                                  : launch_bwd(D, causal != 0, false, mq, mk, mv, mdo, p, grid, stream);
+    const cudaError_t e = variant ? launch_bwd_variant(var, false, mq, mk, mv, mdo, mdq, p, grid, stream)
+                                  : launch_bwd(D, causal != 0, false, mq, mk, mv, mdo, mdq, p, grid, stream);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 2;
     return FA_OK;
@@ -929,6 +946,9 @@ fa_status_t bwd_varlen(const void* q, const void* k, const void* v, const float*
         !encode_map(&mk, k, D, Hkv, total_k, row, row * Hkv, 1, kBwdTile) ||
         !encode_map(&mv, v, D, Hkv, total_k, row, row * Hkv, 1, kBwdTile))
         return FA_ERR_CUDA;
+    CUtensorMap mdq;  // dQ reduce-adds: [64 tokens][1 head][32 columns] fp32 boxes
+    if (!encode_map_f32(&mdq, dq, D, Hq, total_q, (uint64_t)D * 4, (uint64_t)D * 4 * Hq, 32, 1, 64))
+        return FA_ERR_CUDA;
 
     int* sched = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + lay.sched_off);
     if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
@@ -963,8 +983,8 @@ fa_status_t bwd_varlen(const void* q, const void* k, const void* v, const float*
     g_fault_next = 0;
     if (launch_bwd_pre(D, true, p, stream) != cudaSuccess) return FA_ERR_CUDA;
     const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
-    const cudaError_t e = variant ? launch_bwd_variant(var, true, mq, mk, mv, mdo, p, grid, stream)
-                                  : launch_bwd(D, causal != 0, true, mq, mk, mv, mdo, p, grid, stream);
+    const cudaError_t e = variant ? launch_bwd_variant(var, true, mq, mk, mv, mdo, mdq, p, grid, stream)
+                                  : launch_bwd(D, causal != 0, true, mq, mk, mv, mdo, mdq, p, grid, stream);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 3;
     return FA_OK;

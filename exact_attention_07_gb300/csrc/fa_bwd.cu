@@ -250,6 +250,23 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  : "memory");
 }
 
+// TMA reduce-add of one 3-D fp32 box from shared memory into global memory
+// (a bulk group of the issuing thread), and the waits on such groups.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ float bwd_rcp_approx(float x)
 {
     float y;
@@ -400,7 +417,7 @@ template <int D, bool CAUSAL, bool VARLEN, int VAR = kVarNone>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                        const BwdParams p)
+                        const __grid_constant__ CUtensorMap tmDQ, const BwdParams p)
 {
     using L = BwdSmem<D>;
     constexpr uint32_t kColS = L::kColS, kColDP = L::kColDP, kColDV = L::kColDV, kColDK = L::kColDK,
@@ -425,7 +442,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::bKVEmpty), 1);
         for (int i = 0; i < L::kQStages; ++i) {
             mbar_init(bar(L::bQFull + i), 1);
-            mbar_init(bar(L::bQEmpty + i), 1);
+            mbar_init(bar(L::bQEmpty + i), D == 128 ? 4 : 1);  // D = 128: each dQ warp, after its staging
         }
         mbar_init(bar(L::bDOFull), 1);
         mbar_init(bar(L::bDOEmpty), 1);
@@ -451,6 +468,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_prefetch_map(&tmK);
         tma_prefetch_map(&tmV);
         tma_prefetch_map(&tmDO);
+        if (D == 128) tma_prefetch_map(&tmDQ);
     }
     if (warp == 13) {
         tmem_alloc(smem_u32(tmem_slot), kBwdTmemCols);
@@ -485,7 +503,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // the MMA warp for about 100 cycles with the tensor pipe idle.
                 if (t == 0) {
                     mbar_arrive(bar(L::bDSEmpty));
-                    mbar_arrive(bar(L::bQEmpty + (int)(gstep % L::kQStages)));
+                    if constexpr (D != 128) mbar_arrive(bar(L::bQEmpty + (int)(gstep % L::kQStages)));
                 }
                 const int q0 = i * kBwdTile;
                 const int nrows = min(kBwdTile, w.lq - q0);
@@ -502,15 +520,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tmem_wait_ld();
                     tc_fence_before_sync();
                     mbar_arrive(bar(L::bDQEmpty));
-                    // each warp instruction adds 128 contiguous bytes of one dQ row
-                    dst += t;
+                    // The partial goes out through this step's Q stage, free now that
+                    // dK has read it (the next Q load into it is 1.5 steps away), by
+                    // TMA reduce-adds: two instructions per warp instead of 128
+                    // warp-wide red.global.add, which would hold the SM's memory pipeline
+                    // for thousands of cycles and delay the next dS^T stores.  Warp w
+                    // stages head-dimension columns 32w..32w+31 of 64 rows at a time as
+                    // a [64][32] fp32 box.  Rows past Lq are clipped by the tensor map;
+                    // rows of a packed batch past the sequence's end hold exact zeros
+                    // (P = 0 there), which leave the next sequence's dQ unchanged.
+                    const int lane = t & 31;
+                    const uint32_t stg = sb + L::kQ + (gstep % L::kQStages) * L::kTile + (uint32_t)(warp * 8192);
+                    const int x = 32 * warp;
+                    const int y0 = VARLEN ? h : q0;
+                    const int z0 = VARLEN ? w.q0 + q0 : w.b * p.Hq + h;
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        if (c < nrows) red_add(dst + c * rs, __uint_as_float(v0[c]));
-                        if (32 + c < nrows) red_add(dst + (32 + c) * rs, __uint_as_float(v1[c]));
-                        if (64 + c < nrows) red_add(dst + (64 + c) * rs, __uint_as_float(v2[c]));
-                        if (96 + c < nrows) red_add(dst + (96 + c) * rs, __uint_as_float(v3[c]));
+                    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            sts32(stg + (uint32_t)((c * 32 + lane) * 4), hf == 0 ? v0[c] : v2[c]);
+                            sts32(stg + (uint32_t)(((32 + c) * 32 + lane) * 4), hf == 0 ? v1[c] : v3[c]);
+                        }
+                        bwd_fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (VARLEN)
+                                tma_reduce_add_3d(&tmDQ, stg, x, y0, z0 + 64 * hf);
+                            else
+                                tma_reduce_add_3d(&tmDQ, stg, x, y0 + 64 * hf, z0);
+                            bulk_commit_group();
+                            bulk_wait_read_all();  // the box has been read: the stage may be rewritten
+                        }
+                        __syncwarp();
                     }
+                    if (lane == 0) mbar_arrive(bar(L::bQEmpty + (int)(gstep % L::kQStages)));
+                    (void)dst;
+                    (void)nrows;
+                    (void)rs;
                 } else {
                     uint32_t v0[32], v1[32];
                     tmem_ld32(lane_base + kColDQ, v0);
@@ -971,52 +1017,53 @@ cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t 
 namespace {
 template <int D, bool CAUSAL, bool VARLEN, int VAR = kVarNone>
 cudaError_t launch_bwd_kernel(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                              const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream)
+                              const CUtensorMap& dout, const CUtensorMap& dq, const BwdParams& p, int grid,
+                              cudaStream_t stream)
 {
     auto kern = fa_bwd_sm103_kernel<D, CAUSAL, VARLEN, VAR>;
     constexpr int kSmem = BwdSmem<D>::kDynamic;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kBwdThreads, kSmem, stream>>>(q, k, v, dout, p);
+    kern<<<grid, kBwdThreads, kSmem, stream>>>(q, k, v, dout, dq, p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_bwd_dim(bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
-                           const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
-                           cudaStream_t stream)
+                           const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq, const BwdParams& p,
+                           int grid, cudaStream_t stream)
 {
     if (varlen)
-        return causal ? launch_bwd_kernel<D, true, true>(q, k, v, dout, p, grid, stream)
-                      : launch_bwd_kernel<D, false, true>(q, k, v, dout, p, grid, stream);
-    return causal ? launch_bwd_kernel<D, true, false>(q, k, v, dout, p, grid, stream)
-                  : launch_bwd_kernel<D, false, false>(q, k, v, dout, p, grid, stream);
+        return causal ? launch_bwd_kernel<D, true, true>(q, k, v, dout, dq, p, grid, stream)
+                      : launch_bwd_kernel<D, false, true>(q, k, v, dout, dq, p, grid, stream);
+    return causal ? launch_bwd_kernel<D, true, false>(q, k, v, dout, dq, p, grid, stream)
+                  : launch_bwd_kernel<D, false, false>(q, k, v, dout, dq, p, grid, stream);
 }
 }  // namespace
 
 #if !defined(FA_BWD_VARIANTS)
 cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
-                       const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
-                       cudaStream_t stream)
+                       const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq, const BwdParams& p,
+                       int grid, cudaStream_t stream)
 {
-    if (D == 128) return launch_bwd_dim<128>(causal, varlen, q, k, v, dout, p, grid, stream);
-    if (D == 64) return launch_bwd_dim<64>(causal, varlen, q, k, v, dout, p, grid, stream);
+    if (D == 128) return launch_bwd_dim<128>(causal, varlen, q, k, v, dout, dq, p, grid, stream);
+    if (D == 64) return launch_bwd_dim<64>(causal, varlen, q, k, v, dout, dq, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 #else
 cudaError_t launch_bwd_variant(int var, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
-                               const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
-                               cudaStream_t stream)
+                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq,
+                               const BwdParams& p, int grid, cudaStream_t stream)
 {
     if (var == kVarAlibi)
-        return varlen ? launch_bwd_kernel<128, false, true, kVarAlibi>(q, k, v, dout, p, grid, stream)
-                      : launch_bwd_kernel<128, false, false, kVarAlibi>(q, k, v, dout, p, grid, stream);
+        return varlen ? launch_bwd_kernel<128, false, true, kVarAlibi>(q, k, v, dout, dq, p, grid, stream)
+                      : launch_bwd_kernel<128, false, false, kVarAlibi>(q, k, v, dout, dq, p, grid, stream);
     if (var == kVarWindow)
-        return varlen ? launch_bwd_kernel<128, false, true, kVarWindow>(q, k, v, dout, p, grid, stream)
-                      : launch_bwd_kernel<128, false, false, kVarWindow>(q, k, v, dout, p, grid, stream);
+        return varlen ? launch_bwd_kernel<128, false, true, kVarWindow>(q, k, v, dout, dq, p, grid, stream)
+                      : launch_bwd_kernel<128, false, false, kVarWindow>(q, k, v, dout, dq, p, grid, stream);
     if (var == kVarSoftcap)
-        return varlen ? launch_bwd_kernel<128, false, true, kVarSoftcap>(q, k, v, dout, p, grid, stream)
-                      : launch_bwd_kernel<128, false, false, kVarSoftcap>(q, k, v, dout, p, grid, stream);
+        return varlen ? launch_bwd_kernel<128, false, true, kVarSoftcap>(q, k, v, dout, dq, p, grid, stream)
+                      : launch_bwd_kernel<128, false, false, kVarSoftcap>(q, k, v, dout, dq, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 #endif

@@ -55,13 +55,15 @@ struct BwdParams {
 };
 
 cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t stream);
+// dq: fp32 tensor map of dQ, box {32, 64, 1} (dense) or {32, 1, 64} (packed);
+// used at D = 128.
 cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
-                       const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
-                       cudaStream_t stream);
+                       const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq, const BwdParams& p,
+                       int grid, cudaStream_t stream);
 // Variants (var = kVarWindow, kVarSoftcap or kVarAlibi, D = 128, no separate
 // causal flag: a causal window is (-1, 0)).
 cudaError_t launch_bwd_variant(int var, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
-                               const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p, int grid,
-                               cudaStream_t stream);
+                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq,
+                               const BwdParams& p, int grid, cudaStream_t stream);
 
 }  // namespace fa

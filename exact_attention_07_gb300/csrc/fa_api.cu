@@ -95,8 +95,9 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D fp32 tensor map without swizzle: box = {box0, box1, box2} elements
-// (the backward's dQ reduce-adds).
+// 3-D fp32 tensor map with 128-byte swizzle (box0 = 32 elements = one
+// swizzle row): box = {box0, box1, box2} elements (the backward's dQ
+// reduce-adds).
 bool encode_map_f32(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                     uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1, uint32_t box2)
 {
@@ -105,7 +106,7 @@ bool encode_map_f32(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, 
     const cuuint32_t box[3] = {box0, box1, box2};
     const cuuint32_t estr[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -811,8 +812,8 @@ fa_status_t bwd_dense(const void* q, const void* k, const void* v, const float* 
         !encode_map(&mk, k, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kBwdTile, 1) ||
         !encode_map(&mv, v, D, Lk, (uint64_t)B * Hkv, row, row * Lk, kBwdTile, 1))
         return FA_ERR_CUDA;
-    CUtensorMap mdq;  // dQ reduce-adds: [64 rows][32 columns] fp32 boxes
-    if (!encode_map_f32(&mdq, dq, D, Lq, (uint64_t)B * Hq, (uint64_t)D * 4, (uint64_t)D * 4 * Lq, 32, 64, 1))
+    CUtensorMap mdq;  // dQ reduce-adds: [32 rows][32 columns] fp32 boxes
+    if (!encode_map_f32(&mdq, dq, D, Lq, (uint64_t)B * Hq, (uint64_t)D * 4, (uint64_t)D * 4 * Lq, 32, 32, 1))
         return FA_ERR_CUDA;
 
     p.o = o;
@@ -946,8 +947,8 @@ fa_status_t bwd_varlen(const void* q, const void* k, const void* v, const float*
         !encode_map(&mk, k, D, Hkv, total_k, row, row * Hkv, 1, kBwdTile) ||
         !encode_map(&mv, v, D, Hkv, total_k, row, row * Hkv, 1, kBwdTile))
         return FA_ERR_CUDA;
-    CUtensorMap mdq;  // dQ reduce-adds: [64 tokens][1 head][32 columns] fp32 boxes
-    if (!encode_map_f32(&mdq, dq, D, Hq, total_q, (uint64_t)D * 4, (uint64_t)D * 4 * Hq, 32, 1, 64))
+    CUtensorMap mdq;  // dQ reduce-adds: [32 tokens][1 head][32 columns] fp32 boxes
+    if (!encode_map_f32(&mdq, dq, D, Hq, total_q, (uint64_t)D * 4, (uint64_t)D * 4 * Hq, 32, 1, 32))
         return FA_ERR_CUDA;
 
     int* sched = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + lay.sched_off);

@@ -199,9 +199,9 @@ struct BwdSmem {
     // alignment of the dynamic window to 1024 bytes (checked at run time)
     static constexpr int kDynamic = 232448;
     static_assert(kBytes <= kDynamic, "shared memory of one CTA");
-    // Tensor memory columns: S^T (then P^T), dP^T, dV, dK.  D = 128: dQ^T
-    // (lanes = head dimension) reuses the dP^T columns; D = 64: dQ (lanes =
-    // query rows, 64 columns) has columns of its own.
+    // Tensor memory columns: S^T (then P^T), dP^T, dV, dK.  dQ (lanes = query
+    // rows, D columns) reuses the dP^T columns at D = 128 and has columns of its
+    // own at D = 64.
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
     static constexpr uint32_t kColDQ = D == 128 ? kColDP : 256 + 2 * D;
 };
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 float* dst = p.dq + (VARLEN ? ((long long)(w.q0 + q0) * p.Hq + h) * D
                                             : (((long long)w.b * p.Hq + h) * p.Lq + q0) * D);
                 if constexpr (D == 128) {
-                    uint32_t v0[32], v1[32], v2[32], v3[32];
+                    uint32_t v0[32], v1[32], v2[32], v3[32];  // query row t: head dimension 0..127
                     tmem_ld32(lane_base + kColDQ, v0);
                     tmem_ld32(lane_base + kColDQ + 32, v1);
                     tmem_ld32(lane_base + kColDQ + 64, v2);
@@ -522,34 +522,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mbar_arrive(bar(L::bDQEmpty));
                     // The partial goes out through this step's Q stage, free now that
                     // dK has read it (the next Q load into it is 1.5 steps away), by
-                    // TMA reduce-adds: two instructions per warp instead of 128
-                    // warp-wide red.global.add, which would hold the SM's memory pipeline
-                    // for thousands of cycles and delay the next dS^T stores.  Warp w
-                    // stages head-dimension columns 32w..32w+31 of 64 rows at a time as
-                    // a [64][32] fp32 box.  Rows past Lq are clipped by the tensor map;
-                    // rows of a packed batch past the sequence's end hold exact zeros
-                    // (P = 0 there), which leave the next sequence's dQ unchanged.
+                    // TMA reduce-adds instead of warp-wide red.global.add, which would
+                    // hold the SM's memory pipeline for thousands of cycles and delay
+                    // the next dS^T stores.  Warp w stages its 32 rows as [32][32] fp32
+                    // boxes with the 128-byte swizzle (each thread stores its own row,
+                    // 16 bytes at a time, without bank conflicts), two boxes per round.
+                    // Rows past Lq are clipped by the tensor map; rows of a packed batch
+                    // past the sequence's end hold exact zeros (P = 0 there), which
+                    // leave the next sequence's dQ unchanged.
                     const int lane = t & 31;
                     const uint32_t stg = sb + L::kQ + (gstep % L::kQStages) * L::kTile + (uint32_t)(warp * 8192);
-                    const int x = 32 * warp;
-                    const int y0 = VARLEN ? h : q0;
-                    const int z0 = VARLEN ? w.q0 + q0 : w.b * p.Hq + h;
+                    const int y0 = VARLEN ? h : q0 + 32 * warp;
+                    const int z0 = VARLEN ? w.q0 + q0 + 32 * warp : w.b * p.Hq + h;
+                    const uint32_t row = stg + (uint32_t)(lane * 128);
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
+                    for (int rd = 0; rd < 2; ++rd) {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            sts32(stg + (uint32_t)((c * 32 + lane) * 4), hf == 0 ? v0[c] : v2[c]);
-                            sts32(stg + (uint32_t)(((32 + c) * 32 + lane) * 4), hf == 0 ? v1[c] : v3[c]);
+                        for (int bx = 0; bx < 2; ++bx) {
+                            const uint32_t* v = rd == 0 ? (bx == 0 ? v0 : v1) : (bx == 0 ? v2 : v3);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                sts128(row + (uint32_t)(bx * 4096 + ((c ^ (lane & 7)) << 4)), v[4 * c], v[4 * c + 1],
+                                       v[4 * c + 2], v[4 * c + 3]);
                         }
                         bwd_fence_proxy_async();
                         __syncwarp();
                         if (lane == 0) {
-                            if (VARLEN)
-                                tma_reduce_add_3d(&tmDQ, stg, x, y0, z0 + 64 * hf);
-                            else
-                                tma_reduce_add_3d(&tmDQ, stg, x, y0 + 64 * hf, z0);
+#pragma unroll
+                            for (int bx = 0; bx < 2; ++bx)
+                                tma_reduce_add_3d(&tmDQ, stg + (uint32_t)(bx * 4096), 64 * rd + 32 * bx, y0, z0);
                             bulk_commit_group();
-                            bulk_wait_read_all();  // the box has been read: the stage may be rewritten
+                            bulk_wait_read_all();  // the boxes have been read: the stage may be rewritten
                         }
                         __syncwarp();
                     }
@@ -851,9 +854,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         constexpr int kKD = D / 16;                                      // MMAs over the head dimension
         constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false);     // S^T, dP^T: A, B K-major
         constexpr uint32_t kIdBmn = idesc_bf16_f32(128, D, true);       // dV, dK: B MN-major, N = D
-        // dQ^T (D = 128: M = head dimension, N = queries) or dQ (D = 64: M =
-        // queries, N = head dimension); A and B MN-major
-        constexpr uint32_t kIdDQ = idesc_bf16_f32(128, D == 128 ? 128 : D, true) | (1u << 15);
+        // dQ (M = queries, N = head dimension); A and B MN-major
+        constexpr uint32_t kIdDQ = idesc_bf16_f32(128, D, true) | (1u << 15);
         auto commit = [&](int b) {
             if (leader) tc_commit(bar(b));
             __syncwarp();
@@ -953,16 +955,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ss(tm + kColDK, dS_kmaj + kmaj(kk), q_mn + mnmaj(kk), kIdBmn, (s > 0 || kk > 0) ? 1u : 0u);
-                    // D = 128: dQ^T = K^T dS^T, lanes = head dimension, so the reduction
-                    // into global dQ is coalesced along each row.  D = 64: dQ = dS K
-                    // (an M = 64 accumulator would use another lane layout)
+                    // dQ = dS K with the query rows on the TMEM lanes (A = dS and B = K
+                    // both MN-major), so that each dQ thread holds one row
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        if constexpr (D == 128)
-                            mma_ss(tm + kColDQ, dK_mn + mnmaj(kk), dS_mn + mnmaj(kk), kIdDQ, kk > 0);
-                        else
-                            mma_ss(tm + kColDQ, dS_mn + mnmaj(kk), dK_mn + mnmaj(kk), kIdDQ, kk > 0);
-                    }
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tm + kColDQ, dS_mn + mnmaj(kk), dK_mn + mnmaj(kk), kIdDQ, kk > 0);
                 }
                 __syncwarp();
                 commit(L::bDQFull);  // the dQ warps then free dS^T and Q (stage qs)

@@ -55,7 +55,8 @@ struct BwdParams {
 };
 
 cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t stream);
-// dq: fp32 tensor map of dQ, box {32, 64, 1} (dense) or {32, 1, 64} (packed);
+// dq: fp32 tensor map of dQ with 128-byte swizzle, box {32, 32, 1} (dense) or
+// {32, 1, 32} (packed);
 // used at D = 128.
 cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq, const BwdParams& p,

@@ -229,18 +229,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                  : "memory");
 }
 
-__device__ __forceinline__ void red_add(float* addr, float a)
-{
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
-}
-
-// Four consecutive fp32 reductions in one request (16-byte aligned address).
-__device__ __forceinline__ void red_add4(float* addr, float a, float b, float c, float d)
-{
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
 // Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
 // completion counted on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
@@ -442,7 +430,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::bKVEmpty), 1);
         for (int i = 0; i < L::kQStages; ++i) {
             mbar_init(bar(L::bQFull + i), 1);
-            mbar_init(bar(L::bQEmpty + i), D == 128 ? 4 : 1);  // D = 128: each dQ warp, after its staging
+            mbar_init(bar(L::bQEmpty + i), 4);  // each dQ warp, once its staged dQ boxes have been read
         }
         mbar_init(bar(L::bDOFull), 1);
         mbar_init(bar(L::bDOEmpty), 1);
@@ -468,7 +456,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_prefetch_map(&tmK);
         tma_prefetch_map(&tmV);
         tma_prefetch_map(&tmDO);
-        if (D == 128) tma_prefetch_map(&tmDQ);
+        tma_prefetch_map(&tmDQ);
     }
     if (warp == 13) {
         tmem_alloc(smem_u32(tmem_slot), kBwdTmemCols);
@@ -501,16 +489,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // dK and dQ have completed: their operands dS^T and Q(step) are free.
                 // Released here rather than by MMA-warp commits, each of which holds
                 // the MMA warp for about 100 cycles with the tensor pipe idle.
-                if (t == 0) {
-                    mbar_arrive(bar(L::bDSEmpty));
-                    if constexpr (D != 128) mbar_arrive(bar(L::bQEmpty + (int)(gstep % L::kQStages)));
-                }
-                const int q0 = i * kBwdTile;
-                const int nrows = min(kBwdTile, w.lq - q0);
-                // dQ rows: dense [B, Hq, Lq, D], packed [Tq, Hq, D]
-                const long long rs = VARLEN ? (long long)p.Hq * D : D;
-                float* dst = p.dq + (VARLEN ? ((long long)(w.q0 + q0) * p.Hq + h) * D
-                                            : (((long long)w.b * p.Hq + h) * p.Lq + q0) * D);
+                if (t == 0) mbar_arrive(bar(L::bDSEmpty));
+                const int q0 = i * kBwdTile;  // dQ rows: dense [B, Hq, Lq, D], packed [Tq, Hq, D]
                 if constexpr (D == 128) {
                     uint32_t v0[32], v1[32], v2[32], v3[32];  // query row t: head dimension 0..127
                     tmem_ld32(lane_base + kColDQ, v0);
@@ -557,28 +537,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         __syncwarp();
                     }
                     if (lane == 0) mbar_arrive(bar(L::bQEmpty + (int)(gstep % L::kQStages)));
-                    (void)dst;
-                    (void)nrows;
-                    (void)rs;
                 } else {
-                    uint32_t v0[32], v1[32];
+                    uint32_t v0[32], v1[32];  // query row t: head dimension 0..63
                     tmem_ld32(lane_base + kColDQ, v0);
                     tmem_ld32(lane_base + kColDQ + 32, v1);
                     tmem_wait_ld();
                     tc_fence_before_sync();
                     mbar_arrive(bar(L::bDQEmpty));
-                    // thread t adds query row t: 16-byte vector reductions
-                    if (t < nrows) {
-                        float* row = dst + t * rs;
+                    // as at D = 128, through this step's (16 KB) Q stage: one [32][32]
+                    // box per warp and round, two rounds
+                    const int lane = t & 31;
+                    const uint32_t stg = sb + L::kQ + (gstep % L::kQStages) * L::kTile + (uint32_t)(warp * 4096);
+                    const int y0 = VARLEN ? h : q0 + 32 * warp;
+                    const int z0 = VARLEN ? w.q0 + q0 + 32 * warp : w.b * p.Hq + h;
+                    const uint32_t row = stg + (uint32_t)(lane * 128);
+#pragma unroll
+                    for (int rd = 0; rd < 2; ++rd) {
+                        const uint32_t* v = rd == 0 ? v0 : v1;
 #pragma unroll
                         for (int c = 0; c < 8; ++c)
-                            red_add4(row + 4 * c, __uint_as_float(v0[4 * c]), __uint_as_float(v0[4 * c + 1]),
-                                     __uint_as_float(v0[4 * c + 2]), __uint_as_float(v0[4 * c + 3]));
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            red_add4(row + 32 + 4 * c, __uint_as_float(v1[4 * c]), __uint_as_float(v1[4 * c + 1]),
-                                     __uint_as_float(v1[4 * c + 2]), __uint_as_float(v1[4 * c + 3]));
+                            sts128(row + (uint32_t)((c ^ (lane & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                                   v[4 * c + 3]);
+                        bwd_fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_reduce_add_3d(&tmDQ, stg, 32 * rd, y0, z0);
+                            bulk_commit_group();
+                            bulk_wait_read_all();
+                        }
+                        __syncwarp();
                     }
+                    if (lane == 0) mbar_arrive(bar(L::bQEmpty + (int)(gstep % L::kQStages)));
                 }
             }
             // dK and dV of the finished key tile (thread = key)

@@ -36,6 +36,7 @@ SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.act
 
 
 L2_MIB = 126  # L2 of one GB300 as the runtime reports it
+NOMINAL_BF16_TFLOPS = 2250.0  # dense BF16 tensor peak of one GB300, nominal
 
 
 def parse_args(argv=None):
@@ -659,6 +660,21 @@ def main(argv=None):
                                                                       str(w.varlen).lower(),
                                                                       1 if w.window is not None else 0, w.Dv)}
 
+    # Two more denominators for the tensor-bound kernels: the nominal dense BF16
+    # peak of one GB300 (2.25 PFLOP/s: NVIDIA's 36 PFLOP/s for eight GPUs is
+    # quoted with 2:4 sparsity) and the clock-derived ceiling, SMs x 8192
+    # dense BF16 FLOP per clock and SM x the median SM clock of the timed run.
+    clk = clocks.summary()
+    if roofline.get("bound") == "tensor":
+        nominal = NOMINAL_BF16_TFLOPS * (2.0 if w.fp8 else 1.0)
+        roofline["nominal_peak"] = nominal
+        roofline["frac_of_nominal"] = roofline["achieved"] / nominal
+        if clk.get("sm_mhz"):
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            ceiling = sms * 8192 * (2 if w.fp8 else 1) * clk["sm_mhz"] * 1e6 / 1e12
+            roofline["clock_ceiling"] = ceiling
+            roofline["frac_of_clock_ceiling"] = roofline["achieved"] / ceiling
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, threads, desc = cpu_oracle_rate(w, host_inputs, args.cpu_seconds)
@@ -674,7 +690,7 @@ def main(argv=None):
                 "frac_of_peak": value / world / peak,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps,
-                "clocks": clocks.summary()}
+                "clocks": clk}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -491,6 +491,24 @@ def main(argv=None):
         secs = start.elapsed_time(end) / 1e3
     else:
         secs = sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+
+    # A shorter second pass with one event pair per step gives the median and
+    # the minimum step time next to the whole-loop mean above (which is the
+    # reported value).
+    n_dist = min(args.steps, 50)
+    evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dist)]
+    barrier()
+    for e0, e1 in evd:
+        if flush_buf is not None:
+            flush_buf.zero_()
+        e0.record(stream)
+        step(o, lse)
+        e1.record(stream)
+    barrier()
+    fa.fa_check()
+    step_ms = sorted(e0.elapsed_time(e1) for e0, e1 in evd)
+    step_stats = {"median": statistics.median(step_ms), "min": step_ms[0], "n": n_dist,
+                  "note": "one event pair per step, after the timed loop"}
     flops_step = w.flops()
     rate, secs_max = job_rate(secs, flops_step * args.steps, world, dev)
     value = rate / 1e12
@@ -684,6 +702,7 @@ def main(argv=None):
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "e4m3" if w.fp8 else "bf16", "data": "synthetic",
+                "step_ms": step_stats,
                 "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk,
                            "D": w.D, "Dv": w.Dv, "causal": w.causal, "flops_per_step": flops_step,
                            "parallelism": f"replicas{world}" if world > 1 else "single", "l2": l2_note},

@@ -1,4 +1,4 @@
-// Attention backward for sm_103a (D = 128): recompute P from the saved
+// Attention backward for sm_103a (D = 64 and 128): recompute P from the saved
 // log-sum-exp and form the five matrix products of the gradient on the
 // tcgen05 tensor cores (FlashAttention from Scratch, sec. 8 "Backward: spend
 // arithmetic to save memory"; FlashAttention-4: Blackwell Attention Kernel
@@ -11,31 +11,32 @@
 //   dV  += P^T dO                              tensor core, P^T from TMEM
 //   dS^T = c P^T * (dP^T - delta)              softmax warps, bf16 to shared memory
 //   dK  += dS^T Q                              tensor core
-//   dQ^T = K^T dS^T                            tensor core, then fp32 reductions to global
+//   dQ   = dS K                                tensor core, then TMA reduce-adds to global
 //
 // Ownership (sec. 8, "A GPU backward must handle competing ownership
 // requirements"): a CTA owns one 128-key tile of one KV head and loops over
 // every query head of its group and every Q tile that can see the keys, so
 // dK and dV are finished in tensor memory without atomics (grouped-query
-// heads add into the same accumulators); dQ needs a reduction over key tiles
-// and is added to global memory with fp32 reductions.  dQ is formed
-// transposed (dQ^T = K^T dS^T) so that TMEM lanes hold the head dimension and
-// every warp-wide reduction covers 128 contiguous bytes of one dQ row.  Q-tile
-// order is rotated by the key-tile index so that CTAs of the same head do not
-// all add into the same dQ rows at the same time.
+// heads add into the same accumulators); dQ needs a reduction over key tiles.
+// Each step's dQ partial (query rows on the TMEM lanes) is staged in the Q
+// stage that dK has just released and added to global memory by TMA fp32
+// reduce-adds, which keep the reductions off the SM's memory pipeline.
+// Q-tile order is rotated by the key-tile index so that CTAs of the same head
+// do not all add into the same dQ rows at the same time.
 //
 // Tensor memory (512 columns): [0,128) S^T, overwritten by P^T (bf16 pairs);
-// [128,256) dP^T, then the dQ^T partial of the same step; [256,384) dV;
+// [128,256) dP^T, then the dQ partial of the same step; [256,384) dV;
 // [384,512) dK.  Shared memory: K and V of the tile; a 3-stage ring of Q
 // tiles (each with its lse2 row), because S^T of the next step is issued
 // before the current step's dK has released its Q; one dO stage, released by
 // P.V halfway through a step; a 2-stage ring of delta rows; and one dS^T tile
-// that serves as the K-major A operand of dK and the MN-major B operand of dQ^T.
+// that serves as the K-major A operand of dK and the MN-major A operand of dQ.
 //
 // Roles (512 threads, one persistent CTA per SM):
-//   warps 0-3   thread t owns TMEM lane t: reads the dQ^T partial (head
-//               dimension t) out of TMEM and reduces it into global dQ; at
-//               the end of a work item writes dK and dV (key t)
+//   warps 0-3   thread t owns TMEM lane t: reads query row t of the dQ
+//               partial out of TMEM, stages it and sends it with TMA
+//               reduce-adds into global dQ; at the end of a work item writes
+//               dK and dV (key t)
 //   warps 4-11  two groups of four warps, one per half of the 128 query
 //               columns; lane t of a group owns key t of the tile.  Each
 //               forms its half of P^T (into TMEM, for dV) and of dS^T (into
@@ -46,7 +47,7 @@
 // (128*192 + 256*128 + 128*64 = 65536, the launch's 128 per thread).
 // The dQ reductions (64 KB per step) run on their own warps, overlapped with
 // everything else; halving P and dS per thread shortens the chain
-// dS -> dK/dQ -> dP -> dS that bounds a step.
+// dS -> dK/dQ -> dQ read-out -> dP -> dS that bounds a step.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -63,7 +64,7 @@ namespace fa {
 
 // One warp per (batch * head, row) of the padded row range: delta = O . dO,
 // lse2 = LSE * log2(e) (+inf where the row saw no key, so that P = 0), and
-// the row of dQ zeroed for the reductions of the main kernel.
+// the row of dQ zeroed for the reduce-adds of the main kernel.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p)
 {
@@ -471,9 +472,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp < 4) {
         // ============================================================ dQ reduction, dK/dV epilogue
-        // Thread t owns TMEM lane t.  D = 128: head dimension t of the dQ^T
-        // partial (its 128 columns are the Q tile's rows); D = 64: query row t
-        // of the dQ partial (64 columns).  Key t for dK and dV.
+        // Thread t owns TMEM lane t: query row t of the dQ partial (D
+        // columns), key t for dK and dV.
         regs_increase<192>();
         const int t = threadIdx.x;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);

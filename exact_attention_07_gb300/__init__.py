@@ -332,7 +332,7 @@ def fa_fwd_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window=(-1
                    out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
     """Dense forward with a key window (left, right) around each query's
     bottom-right-aligned position (-1 = unlimited), soft-capping of the
-    scaled scores, or ALiBi slopes per query head.  D = 128."""
+    scaled scores, or ALiBi slopes per query head.  D = 64 or 128."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check_tensor(t, n, torch.bfloat16, 4)
     B, Hq, Lq, D = q.shape
@@ -513,7 +513,7 @@ def fa_bwd_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.T
                    dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
                    workspace: torch.Tensor | None = None, stream=None):
     """Backward of fa_fwd_variant for key windows, soft-capping and ALiBi
-    (D = 128); o and lse from fa_fwd_variant with the same variant."""
+    (D = 64 or 128); o and lse from fa_fwd_variant with the same variant."""
     var = _variant(window, softcap, alibi_slopes, q.shape[1], q.device)
     return fa_bwd(q, k, v, o, lse, dout, False, softmax_scale, dq, dk, dv, workspace, stream, variant=var)
 
@@ -578,7 +578,7 @@ def fa_bwd_varlen_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: 
                           dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
                           dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
     """Backward of fa_fwd_varlen_variant for key windows, soft-capping and
-    ALiBi (D = 128)."""
+    ALiBi (D = 64 or 128)."""
     var = _variant(window, softcap, alibi_slopes, q.shape[1], q.device)
     return fa_bwd_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, False,
                          softmax_scale, dq, dk, dv, workspace, stream, variant=var)

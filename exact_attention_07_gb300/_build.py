@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa_gb300.so")
-SOURCES = ["fa_api.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_decode.cu", "fa_decode_tc.cu", "fa_bwd.cu", "fa_fwd_var.cu", "fa_fwd_fp8.cu", "fa_fp8.cu", "fa_fwd_d192.cu", "fa_bwd_var.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_decode.cu", "fa_decode_tc.cu", "fa_bwd.cu", "fa_fwd_var.cu", "fa_fwd_fp8.cu", "fa_fp8.cu", "fa_fwd_d192.cu", "fa_bwd_var.cu", "fa_fwd_var64.cu", "fa_bwd_var64.cu"]
 HEADERS = ["fa_fwd_kernel.cuh", "ptx_sm103.cuh", "fa_params.h", "fa_launch.h", "fa_decode.h", "fa_bwd.h", "fa_fp8.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -120,13 +120,22 @@ int heads_per_section(int Hkv, long long Lk, int D_kv)
     return (int)hs;
 }
 
+template <int D, bool VARLEN>
+cudaError_t dispatch_variant_dim(int var, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                 const FwdParams& p, int grid, cudaStream_t st)
+{
+    if (var == kVarSoftcap) return launch_fwd<D, false, VARLEN, kVarSoftcap>(q, k, v, p, grid, st);
+    if (var == kVarAlibi) return launch_fwd<D, false, VARLEN, kVarAlibi>(q, k, v, p, grid, st);
+    return launch_fwd<D, false, VARLEN, kVarWindow>(q, k, v, p, grid, st);
+}
+
+// D = 64 or 128 (checked by prepare_variant)
 template <bool VARLEN>
-cudaError_t dispatch_variant(int var, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t dispatch_variant(int D, int var, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                              const FwdParams& p, int grid, cudaStream_t st)
 {
-    if (var == kVarSoftcap) return launch_fwd<128, false, VARLEN, kVarSoftcap>(q, k, v, p, grid, st);
-    if (var == kVarAlibi) return launch_fwd<128, false, VARLEN, kVarAlibi>(q, k, v, p, grid, st);
-    return launch_fwd<128, false, VARLEN, kVarWindow>(q, k, v, p, grid, st);
+    return D == 64 ? dispatch_variant_dim<64, VARLEN>(var, q, k, v, p, grid, st)
+                   : dispatch_variant_dim<128, VARLEN>(var, q, k, v, p, grid, st);
 }
 
 // Validates a variant description and fills the kernel parameters; returns
@@ -136,7 +145,7 @@ int prepare_variant(const fa_variant_t* var, int D, float scale, FwdParams* p)
     if (!var) return -(int)FA_ERR_INVALID_ARG;
     if (!std::isfinite(var->softcap) || var->softcap < 0.f) return -(int)FA_ERR_INVALID_ARG;
     if (var->alibi_slopes && (reinterpret_cast<uintptr_t>(var->alibi_slopes) & 3u)) return -(int)FA_ERR_INVALID_ARG;
-    if (D != 128) return -(int)FA_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return -(int)FA_ERR_UNSUPPORTED;
     if (var->softcap > 0.f && var->alibi_slopes) return -(int)FA_ERR_UNSUPPORTED;
     p->win_left = var->window_left < 0 ? -1 : var->window_left;
     p->win_right = var->window_right < 0 ? -1 : var->window_right;
@@ -344,7 +353,7 @@ fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, flo
     p.fault = g_fault_next;
     g_fault_next = 0;
     const int grid = (int)(tiles < ds->num_sms ? tiles : ds->num_sms);
-    const cudaError_t e = variant ? dispatch_variant<false>(var, mq, mk, mv, p, grid, stream)
+    const cudaError_t e = variant ? dispatch_variant<false>(D, var, mq, mk, mv, p, grid, stream)
                                   : dispatch<false>(D, causal != 0, mq, mk, mv, p, grid, stream);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 1;
@@ -437,7 +446,7 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
     p.err = ds->err;
     p.diag = ds->diag;
     const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
-    const cudaError_t e = variant ? dispatch_variant<true>(var, mq, mk, mv, p, grid, stream)
+    const cudaError_t e = variant ? dispatch_variant<true>(D, var, mq, mk, mv, p, grid, stream)
                                   : dispatch<true>(D, causal != 0, mq, mk, mv, p, grid, stream);
     cudaFreeAsync(sched, stream);
     if (e != cudaSuccess) return FA_ERR_CUDA;
@@ -760,7 +769,7 @@ int prepare_bwd_variant(const fa_variant_t* var, int D, float scale, BwdParams* 
     if (!var) return -(int)FA_ERR_INVALID_ARG;
     if (!std::isfinite(var->softcap) || var->softcap < 0.f) return -(int)FA_ERR_INVALID_ARG;
     if (var->alibi_slopes && (reinterpret_cast<uintptr_t>(var->alibi_slopes) & 3u)) return -(int)FA_ERR_INVALID_ARG;
-    if (D != 128) return -(int)FA_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return -(int)FA_ERR_UNSUPPORTED;
     if (var->softcap > 0.f && var->alibi_slopes) return -(int)FA_ERR_UNSUPPORTED;
     p->win_left = var->window_left < 0 ? -1 : var->window_left;
     p->win_right = var->window_right < 0 ? -1 : var->window_right;
@@ -844,7 +853,7 @@ fa_status_t bwd_dense(const void* q, const void* k, const void* v, const float* 
     g_fault_next = 0;
     if (launch_bwd_pre(D, false, p, stream) != cudaSuccess) return FA_ERR_CUDA;
     const int grid = (int)(items < ds->num_sms ? items : ds->num_sms);
-    const cudaError_t e = variant ? launch_bwd_variant(var, false, mq, mk, mv, mdo, mdq, p, grid, stream)
+    const cudaError_t e = variant ? launch_bwd_variant(D, var, false, mq, mk, mv, mdo, mdq, p, grid, stream)
                                   : launch_bwd(D, causal != 0, false, mq, mk, mv, mdo, mdq, p, grid, stream);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 2;
@@ -984,7 +993,7 @@ fa_status_t bwd_varlen(const void* q, const void* k, const void* v, const float*
     g_fault_next = 0;
     if (launch_bwd_pre(D, true, p, stream) != cudaSuccess) return FA_ERR_CUDA;
     const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
-    const cudaError_t e = variant ? launch_bwd_variant(var, true, mq, mk, mv, mdo, mdq, p, grid, stream)
+    const cudaError_t e = variant ? launch_bwd_variant(D, var, true, mq, mk, mv, mdo, mdq, p, grid, stream)
                                   : launch_bwd(D, causal != 0, true, mq, mk, mv, mdo, mdq, p, grid, stream);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     g_last_launches = 3;

@@ -1037,19 +1037,28 @@ cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, co
     return cudaErrorInvalidValue;
 }
 #else
-cudaError_t launch_bwd_variant(int var, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
-                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq,
-                               const BwdParams& p, int grid, cudaStream_t stream)
+#ifndef FA_BWD_HEAD_DIM
+#define FA_BWD_HEAD_DIM 128
+#endif
+#if FA_BWD_HEAD_DIM == 64
+#define FA_BWD_VARIANT_FN launch_bwd_variant_d64
+#else
+#define FA_BWD_VARIANT_FN launch_bwd_variant_d128
+#endif
+cudaError_t FA_BWD_VARIANT_FN(int var, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
+                              const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq,
+                              const BwdParams& p, int grid, cudaStream_t stream)
 {
+    constexpr int D = FA_BWD_HEAD_DIM;
     if (var == kVarAlibi)
-        return varlen ? launch_bwd_kernel<128, false, true, kVarAlibi>(q, k, v, dout, dq, p, grid, stream)
-                      : launch_bwd_kernel<128, false, false, kVarAlibi>(q, k, v, dout, dq, p, grid, stream);
+        return varlen ? launch_bwd_kernel<D, false, true, kVarAlibi>(q, k, v, dout, dq, p, grid, stream)
+                      : launch_bwd_kernel<D, false, false, kVarAlibi>(q, k, v, dout, dq, p, grid, stream);
     if (var == kVarWindow)
-        return varlen ? launch_bwd_kernel<128, false, true, kVarWindow>(q, k, v, dout, dq, p, grid, stream)
-                      : launch_bwd_kernel<128, false, false, kVarWindow>(q, k, v, dout, dq, p, grid, stream);
+        return varlen ? launch_bwd_kernel<D, false, true, kVarWindow>(q, k, v, dout, dq, p, grid, stream)
+                      : launch_bwd_kernel<D, false, false, kVarWindow>(q, k, v, dout, dq, p, grid, stream);
     if (var == kVarSoftcap)
-        return varlen ? launch_bwd_kernel<128, false, true, kVarSoftcap>(q, k, v, dout, dq, p, grid, stream)
-                      : launch_bwd_kernel<128, false, false, kVarSoftcap>(q, k, v, dout, dq, p, grid, stream);
+        return varlen ? launch_bwd_kernel<D, false, true, kVarSoftcap>(q, k, v, dout, dq, p, grid, stream)
+                      : launch_bwd_kernel<D, false, false, kVarSoftcap>(q, k, v, dout, dq, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 #endif

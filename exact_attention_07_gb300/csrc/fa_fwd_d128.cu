@@ -31,22 +31,24 @@ FA_INSTANCE_DV(192, true, true, kVarNone, 128)
 // e4m3 inputs: D = 128, dense
 FA_INSTANCE(128, false, false, kVarFp8)
 FA_INSTANCE(128, true, false, kVarFp8)
-#elif !defined(FA_VARIANTS)
+#else
 #ifndef FA_HEAD_DIM
 #define FA_HEAD_DIM 128
 #endif
+#if !defined(FA_VARIANTS)
 FA_INSTANCE(FA_HEAD_DIM, false, false, kVarNone)
 FA_INSTANCE(FA_HEAD_DIM, true, false, kVarNone)
 FA_INSTANCE(FA_HEAD_DIM, false, true, kVarNone)
 FA_INSTANCE(FA_HEAD_DIM, true, true, kVarNone)
 #else
-// score variants: D = 128, dense and packed
-FA_INSTANCE(128, false, false, kVarWindow)
-FA_INSTANCE(128, false, true, kVarWindow)
-FA_INSTANCE(128, false, false, kVarSoftcap)
-FA_INSTANCE(128, false, true, kVarSoftcap)
-FA_INSTANCE(128, false, false, kVarAlibi)
-FA_INSTANCE(128, false, true, kVarAlibi)
+// score variants, dense and packed
+FA_INSTANCE(FA_HEAD_DIM, false, false, kVarWindow)
+FA_INSTANCE(FA_HEAD_DIM, false, true, kVarWindow)
+FA_INSTANCE(FA_HEAD_DIM, false, false, kVarSoftcap)
+FA_INSTANCE(FA_HEAD_DIM, false, true, kVarSoftcap)
+FA_INSTANCE(FA_HEAD_DIM, false, false, kVarAlibi)
+FA_INSTANCE(FA_HEAD_DIM, false, true, kVarAlibi)
+#endif
 #endif
 
 }  // namespace fa

@@ -143,7 +143,7 @@ fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, f
  *   alibi_slopes: DEVICE fp32 [Hq] (or NULL); the score of query head h
  *     becomes s - alibi_slopes[h] * |c_i - j|.
  *   Order: scale, then the score modifier, then the window.  softcap and
- *   alibi_slopes cannot be combined (FA_ERR_UNSUPPORTED); D must be 128.
+ *   alibi_slopes cannot be combined (FA_ERR_UNSUPPORTED); D must be 64 or 128.
  *   LSE is the log-sum-exp of the modified scores.
  */
 typedef struct fa_variant {
@@ -282,11 +282,12 @@ fa_status_t fa_fwd_splitkv_workspace(int B, int Hq, int Hkv, int Lq, int Lk, int
  *   workspace: DEVICE memory of at least fa_bwd_workspace bytes, 16-byte
  *     aligned, owned by the caller (per-row statistics between the two
  *     kernels); calls that overlap on the GPU need separate workspaces.
- *   D must be 128 (FA_ERR_UNSUPPORTED otherwise).
+ *   D must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
  *
  * Launches 2 kernels: a preprocess (rowsum(O * dO), LSE in base 2, dq zeroed)
- * and the gradient kernel.  dq is accumulated with fp32 atomic additions, so
- * its low bits may differ between runs; dk and dv are deterministic.
+ * and the gradient kernel.  dq is accumulated by fp32 reduce-adds (the TMA's
+ * atomic additions) from several CTAs in no fixed order, so its low bits may
+ * differ between runs; dk and dv are deterministic.
  */
 fa_status_t fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse,
                    const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq,
@@ -310,7 +311,7 @@ fa_status_t fa_bwd_workspace(int B, int Hq, int Lq, size_t* workspace_bytes);
  *   workspace: DEVICE memory of at least fa_bwd_varlen_workspace bytes,
  *     16-byte aligned, owned by the caller (row statistics and the schedule);
  *     calls that overlap on the GPU need separate workspaces.
- *   D must be 128 (FA_ERR_UNSUPPORTED otherwise).
+ *   D must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
  *
  * Launches 3 kernels: the schedule (sequences longest query range first), the
  * preprocess and the gradient kernel.  No device memory is allocated.
@@ -334,8 +335,8 @@ fa_status_t fa_bwd_varlen_workspace(int num_seqs, int total_q, int Hq, size_t* w
  * masks do not depend on the raw score s, so that is dS, while soft-capping
  * (t = cap * tanh(s / cap)) multiplies it by dt/ds = 1 - tanh^2(s / cap).
  * Layouts, workspace and launches as fa_bwd / fa_bwd_varlen; `variant` is a
- * HOST pointer.  D must be 128, and soft-capping with ALiBi is unsupported,
- * as in the forward: both return FA_ERR_UNSUPPORTED.
+ * HOST pointer.  D must be 64 or 128, and soft-capping with ALiBi is
+ * unsupported, as in the forward: both return FA_ERR_UNSUPPORTED.
  */
 fa_status_t fa_bwd_variant(const void* q, const void* k, const void* v, const float* o, const float* lse,
                            const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq,

@@ -201,10 +201,17 @@ BWD_VARIANT_CASES = [
 ]
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,window,cap,alibi,qm", BWD_VARIANT_CASES)
-def test_bwd_variant_full_compare(B, Hq, Hkv, Lq, Lk, window, cap, alibi, qm):
+BWD_VARIANT_CASES_D64 = [
+    (1, 2, 1, 513, 513, (300, 0), 0.0, False, 1.0),     # window edge inside tiles, GQA
+    (1, 4, 2, 333, 517, (-1, 0), 30.0, False, 6.0),     # soft cap 30, causal, GQA, ragged, Lq < Lk
+    (1, 4, 4, 400, 400, (255, 0), 0.0, True, 1.0),      # ALiBi inside a causal window
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,window,cap,alibi,qm,D",
+                         [c + (128,) for c in BWD_VARIANT_CASES] + [c + (64,) for c in BWD_VARIANT_CASES_D64])
+def test_bwd_variant_full_compare(B, Hq, Hkv, Lq, Lk, window, cap, alibi, qm, D):
     from oracle.variants import attention_variant_bwd
-    D = 128
     seed = Lq + 2 * Lk + Hq + (7 if alibi else 0) + int(cap)
     q, k, v = random_inputs((B, Hq, Lq, D), (B, Hkv, Lk, D), seed=seed, q_mult=qm)
     do = grad_output((B, Hq, Lq, D), seed)
@@ -236,10 +243,11 @@ def test_bwd_causal_window_equals_causal():
     assert np.abs(b[0].cpu().numpy() - a[0]).max() <= 1e-4 * np.abs(a[0]).max()
 
 
-@pytest.mark.parametrize("window,cap,qm", [((100, 0), 0.0, 1.0), ((-1, 0), 8.0, 4.0)])
-def test_bwd_varlen_variant_full_compare(window, cap, qm):
+@pytest.mark.parametrize("window,cap,qm,D", [((100, 0), 0.0, 1.0, 128), ((-1, 0), 8.0, 4.0, 128),
+                                             ((100, 0), 0.0, 1.0, 64)])
+def test_bwd_varlen_variant_full_compare(window, cap, qm, D):
     from oracle.variants import attention_variant_bwd_varlen
-    lq, lk, Hq, Hkv, D = [200, 5, 400, 129], [260, 5, 400, 129], 4, 2, 128
+    lq, lk, Hq, Hkv = [200, 5, 400, 129], [260, 5, 400, 129], 4, 2
     Tq, Tk = sum(lq), sum(lk)
     q, k, v = random_inputs((Tq, Hq, D), (Tk, Hkv, D), seed=61, q_mult=qm)
     do = grad_output((Tq, Hq, D), 61)

@@ -44,9 +44,17 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,window,cap,use_alibi,qm", CASES)
-def test_variant_full_compare(B, Hq, Hkv, Lq, Lk, window, cap, use_alibi, qm):
-    D = 128
+CASES_D64 = [
+    (1, 2, 2, 700, 700, (127, 0), 0.0, False, 1.0),      # causal sliding window of width 128
+    (1, 2, 1, 300, 900, (64, 64), 0.0, False, 1.0),      # two-sided window, Lq < Lk
+    (1, 4, 2, 777, 777, (-1, 0), 5.0, False, 4.0),       # tight cap, causal, GQA
+    (2, 8, 2, 529, 529, (255, 0), 0.0, True, 1.0),       # ALiBi with a causal window, GQA
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,window,cap,use_alibi,qm,D",
+                         [c + (128,) for c in CASES] + [c + (64,) for c in CASES_D64])
+def test_variant_full_compare(B, Hq, Hkv, Lq, Lk, window, cap, use_alibi, qm, D):
     q, k, v = random_inputs((B, Hq, Lq, D), (B, Hkv, Lk, D), seed=Lq + Lk + Hq, q_mult=qm)
     slopes = alibi(Hq) if use_alibi else None
     o, lse = fa.fa_fwd_variant(q.to(DEV), k.to(DEV), v.to(DEV), window=window, softcap=cap,
@@ -56,17 +64,19 @@ def test_variant_full_compare(B, Hq, Hkv, Lq, Lk, window, cap, use_alibi, qm):
     compare(o.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_lse, f"variant {window} cap={cap} alibi={use_alibi}")
 
 
-def test_causal_window_equals_plain_causal_kernel():
-    q, k, v = random_inputs((1, 4, 1000, 128), (1, 4, 1000, 128), seed=3)
+@pytest.mark.parametrize("D", [64, 128])
+def test_causal_window_equals_plain_causal_kernel(D):
+    q, k, v = random_inputs((1, 4, 1000, D), (1, 4, 1000, D), seed=3)
     a = fa.fa_fwd_variant(q.to(DEV), k.to(DEV), v.to(DEV), window=(-1, 0))
     b = fa.fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
     fa.fa_check()
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_varlen_variant():
+@pytest.mark.parametrize("D", [64, 128])
+def test_varlen_variant(D):
     lens_q, lens_k = [300, 1, 700, 129], [300, 50, 700, 400]
-    Hq, Hkv, D = 4, 2, 128
+    Hq, Hkv = 4, 2
     q, k, v = random_inputs((sum(lens_q), Hq, D), (sum(lens_k), Hkv, D), seed=11)
     cq = torch.tensor([0] + np.cumsum(lens_q).tolist(), dtype=torch.int32)
     ck = torch.tensor([0] + np.cumsum(lens_k).tolist(), dtype=torch.int32)

@@ -30,7 +30,13 @@ constexpr int kMaxDevices = 64;
 // the longest-first order global (what matters most for causal balance);
 // within a section, concurrently running CTAs walk the same few 256-row
 // blocks of every head, so their K/V stays L2-resident anyway.
+// K/V bytes per scheduling section of KV heads.  Work tiles of unequal
+// length (causal, key windows, packed batches) need the whole-L2 section so
+// that the longest-first order can balance them; equal tiles measured faster
+// with sections a quarter of the L2, whose K/V stays in it (fewer re-reads
+// from HBM).
 constexpr long long kL2SectionBytes = 128ll << 20;
+constexpr long long kL2SectionBytesEqualTiles = 32ll << 20;
 
 struct DeviceState {
     bool ready = false;
@@ -110,11 +116,12 @@ bool encode_map_f32(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, 
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// D_kv = the K and V elements of one key (D + Dv)
-int heads_per_section(int Hkv, long long Lk, int D_kv)
+// D_kv = the K and V bytes of one key / 2 (D + Dv for bf16)
+int heads_per_section(int Hkv, long long Lk, int D_kv, bool equal_tiles)
 {
     const long long kv_bytes = Lk * D_kv * 2;  // K and V of one KV head
-    long long hs = kv_bytes > 0 ? kL2SectionBytes / kv_bytes : Hkv;
+    const long long budget = equal_tiles ? kL2SectionBytesEqualTiles : kL2SectionBytes;
+    long long hs = kv_bytes > 0 ? budget / kv_bytes : Hkv;
     if (hs < 1) hs = 1;
     if (hs > Hkv) hs = Hkv;
     return (int)hs;
@@ -346,7 +353,7 @@ fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, flo
     p.Lk = Lk;
     p.group = Hq / Hkv;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
-    p.heads_per_section = heads_per_section(Hkv, Lk, D + Dv);
+    p.heads_per_section = heads_per_section(Hkv, Lk, D + Dv, !causal && var == kVarNone);
     p.num_tiles = (int)tiles;
     p.err = ds->err;
     p.diag = ds->diag;
@@ -437,7 +444,7 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
     p.Hkv = Hkv;
     p.group = Hq / Hkv;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
-    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, D + Dv);
+    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, D + Dv, false);
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
     p.sched = sched;
@@ -562,7 +569,7 @@ extern "C" fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const
     p.Hkv = Hkv;
     p.group = Hq / Hkv;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
-    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, 2 * D);
+    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, 2 * D, false);
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
     p.sched = sched;
@@ -1167,7 +1174,7 @@ extern "C" fa_status_t fa_fwd_fp8(const void* prepared, float* o, float* lse, in
     p.Lk = Lk;
     p.group = Hq / Hkv;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
-    p.heads_per_section = heads_per_section(Hkv, Lk, D / 2);  // e4m3 K/V: half the bytes of bf16
+    p.heads_per_section = heads_per_section(Hkv, Lk, D / 2, !causal);  // e4m3 K/V: half the bytes of bf16
     p.num_tiles = (int)tiles;
     p.fp8_sq = reinterpret_cast<const float*>(base + l.sq);
     p.fp8_sk = reinterpret_cast<const float*>(base + l.sk);

@@ -116,14 +116,30 @@ bool encode_map_f32(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, 
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// D_kv = the K and V bytes of one key / 2 (D + Dv for bf16)
-int heads_per_section(int Hkv, long long Lk, int D_kv, bool equal_tiles)
+// Dense batches: the (batch, head) slabs of Q, K, V, O and LSE are contiguous,
+// so B batches of Hq query heads over Hkv KV heads are one batch of B*Hq query
+// heads over B*Hkv KV heads (query head b*Hq + h reads KV head
+// (b*Hq + h) / (Hq/Hkv) = b*Hkv + h/(Hq/Hkv)), and the kernel's longest-first
+// tile order then spans the whole batch instead of restarting at each batch
+// (a causal B = 2 list was 12 % out of balance over 152 CTAs).  ALiBi keeps the
+// batch: its slopes are indexed by the query head within the batch.
+void set_batch_heads(FwdParams* p, int B, int Hq, int Hkv, bool fold)
 {
-    const long long kv_bytes = Lk * D_kv * 2;  // K and V of one KV head
+    p->B = fold ? 1 : B;
+    p->Hq = fold ? B * Hq : Hq;
+    p->Hkv = fold ? B * Hkv : Hkv;
+}
+
+// KV slabs per scheduling section.  slabs = the KV heads of one batch (all
+// (batch, KV head) slabs when the batch is folded into the heads) or of one
+// packed sequence; D_kv = the K and V bytes of one key / 2 (D + Dv for bf16).
+int heads_per_section(int slabs, long long Lk, int D_kv, bool equal_tiles)
+{
+    const long long kv_bytes = Lk * D_kv * 2;  // K and V of one slab
     const long long budget = equal_tiles ? kL2SectionBytesEqualTiles : kL2SectionBytes;
-    long long hs = kv_bytes > 0 ? budget / kv_bytes : Hkv;
+    long long hs = kv_bytes > 0 ? budget / kv_bytes : slabs;
     if (hs < 1) hs = 1;
-    if (hs > Hkv) hs = Hkv;
+    if (hs > slabs) hs = slabs;
     return (int)hs;
 }
 
@@ -346,14 +362,12 @@ fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, flo
 
     p.o = o;
     p.lse = lse;
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
+    set_batch_heads(&p, B, Hq, Hkv, var != kVarAlibi);
     p.Lq = Lq;
     p.Lk = Lk;
     p.group = Hq / Hkv;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
-    p.heads_per_section = heads_per_section(Hkv, Lk, D + Dv, !causal && var == kVarNone);
+    p.heads_per_section = heads_per_section(p.Hkv, Lk, D + Dv, !causal && var == kVarNone);
     p.num_tiles = (int)tiles;
     p.err = ds->err;
     p.diag = ds->diag;
@@ -1167,14 +1181,12 @@ extern "C" fa_status_t fa_fwd_fp8(const void* prepared, float* o, float* lse, in
     FwdParams p{};
     p.o = o;
     p.lse = lse;
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
+    set_batch_heads(&p, B, Hq, Hkv, true);  // the scales are indexed by (batch, head) slab
     p.Lq = Lq;
     p.Lk = Lk;
     p.group = Hq / Hkv;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
-    p.heads_per_section = heads_per_section(Hkv, Lk, D / 2, !causal);  // e4m3 K/V: half the bytes of bf16
+    p.heads_per_section = heads_per_section(p.Hkv, Lk, D / 2, !causal);  // e4m3 K/V: half the bytes of bf16
     p.num_tiles = (int)tiles;
     p.fp8_sq = reinterpret_cast<const float*>(base + l.sq);
     p.fp8_sk = reinterpret_cast<const float*>(base + l.sk);

@@ -369,6 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using L = FwdSmem<D, VAR, DV>;
     constexpr bool kAlternate = CAUSAL || VARLEN || var_window(VAR);  // tiles of unequal length
+    // Registers per thread after the split: 192 for the eight softmax warps,
+    // kEpiRegs for the four epilogue warps and kCtlRegs for the producer, MMA
+    // and two idle warps, 8 * 192 + 4 * (kEpiRegs + kCtlRegs) = 16 * 128, the
+    // launch's own count.  With D >= 128, a packed batch's epilogue spilled
+    // at 64 registers (addresses through the sequence offsets); 80 of them
+    // measured 1.293 -> 1.256 ms on the 8-sequence causal workload.  The dense
+    // kernels measured best with the even split.
+    constexpr int kEpiRegs = (VARLEN && D >= 128) ? 80 : 64;
+    constexpr int kCtlRegs = 128 - kEpiRegs;
     constexpr bool kSoftmaxFreesKV = !L::kTail && !L::kFp8;  // who frees K/V ring stages (see the softmax role)
     constexpr float kTau = 8.0f;     // rescale threshold, log2 units
     constexpr float kLn2 = 0.69314718055994530942f;
@@ -659,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 12) {
         // ============================================================ epilogue
-        regs_decrease<64>();
+        regs_decrease<kEpiRegs>();
         const int row = threadIdx.x & 127;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         uint32_t o_ph[2] = {0, 0}, st_ph[2] = {0, 0};
@@ -751,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        regs_decrease<64>();
+        regs_decrease<kCtlRegs>();
         if (warp == 12) {
             // ============================================================ TMA producer
             if (lane == 0) {

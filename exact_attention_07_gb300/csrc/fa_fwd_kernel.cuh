@@ -369,15 +369,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using L = FwdSmem<D, VAR, DV>;
     constexpr bool kAlternate = CAUSAL || VARLEN || var_window(VAR);  // tiles of unequal length
-    // Registers per thread after the split: 192 for the eight softmax warps,
-    // kEpiRegs for the four epilogue warps and kCtlRegs for the producer, MMA
-    // and two idle warps, 8 * 192 + 4 * (kEpiRegs + kCtlRegs) = 16 * 128, the
-    // launch's own count.  With D >= 128, a packed batch's epilogue spilled
-    // at 64 registers (addresses through the sequence offsets); 80 of them
-    // measured 1.293 -> 1.256 ms on the 8-sequence causal workload.  The dense
-    // kernels measured best with the even split.
-    constexpr int kEpiRegs = (VARLEN && D >= 128) ? 80 : 64;
-    constexpr int kCtlRegs = 128 - kEpiRegs;
+    // Registers per thread after the split: kSmRegs for the eight softmax
+    // warps, kEpiRegs for the four epilogue warps and kCtlRegs for the
+    // producer, MMA and two idle warps, 8 * kSmRegs + 4 * (kEpiRegs + kCtlRegs)
+    // = 16 * 128, the launch's own count.  Measured per kernel (ptxas spills
+    // move between the roles with the split): with D >= 128 a packed batch's
+    // epilogue spilled at 64 (addresses through the sequence offsets), and
+    // 192 / 80 / 48 took the 8-sequence causal workload from 1.293 to
+    // 1.256 ms; the plain dense D = 128 kernel ran 1 % faster at
+    // 184 / 80 / 64; the causal dense kernel ran best at 192 / 64 / 64 (3 %
+    // slower with either of the others).
+    constexpr bool kPlainDense = !CAUSAL && !VARLEN && VAR == kVarNone && D == 128 && DV == 128;
+    constexpr int kSmRegs = kPlainDense ? 184 : 192;
+    constexpr int kEpiRegs = (kPlainDense || (VARLEN && D >= 128)) ? 80 : 64;
+    constexpr int kCtlRegs = 512 - 2 * kSmRegs - kEpiRegs;
+    static_assert(kCtlRegs >= 40 && kSmRegs % 8 == 0 && kEpiRegs % 8 == 0 && kCtlRegs % 8 == 0,
+                  "setmaxnreg split must fill the launch's 16 x 128 registers per lane");
     constexpr bool kSoftmaxFreesKV = !L::kTail && !L::kFp8;  // who frees K/V ring stages (see the softmax role)
     constexpr float kTau = 8.0f;     // rescale threshold, log2 units
     constexpr float kLn2 = 0.69314718055994530942f;
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 8) {
         // ============================================================ softmax
-        regs_increase<192>();
+        regs_increase<kSmRegs>();
         const int t = warp >> 2;             // Q tile of this group
         const int row = threadIdx.x & 127;   // query row within the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;

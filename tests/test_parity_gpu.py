@@ -78,6 +78,33 @@ def test_custom_scale_and_repeat_calls_identical():
     compare(o1, l1, ref_o, ref_lse, "scale 0.05")
 
 
+@pytest.mark.parametrize("mode", ["plain", "causal", "window", "alibi"])
+def test_batch_equals_one_batch_at_a_time(mode):
+    """A dense batch is launched as one list of (batch, head) slabs, each of
+    its work tiles computed by one CTA with no cross-tile arithmetic, so every
+    batch entry must come out bit-identical to a call on that entry alone;
+    GQA (r = 4) checks that query head h of batch b reads KV head
+    b * Hkv + h / r.  ALiBi slopes are per query head of one batch entry."""
+    B, Hq, Hkv, L, D = 3, 8, 2, 700, 128
+    q, k, v = random_inputs((B, Hq, L, D), (B, Hkv, L, D), seed=91)
+    qd, kd, vd = (x.to(DEV) for x in (q, k, v))
+    slopes = torch.tensor([2.0 ** (-(i + 1)) for i in range(Hq)], dtype=torch.float32, device=DEV)
+
+    def call(a, b, c):
+        if mode in ("plain", "causal"):
+            return fa.fa_fwd(a, b, c, causal=mode == "causal")
+        if mode == "window":
+            return fa.fa_fwd_variant(a, b, c, window=(300, 0))
+        return fa.fa_fwd_variant(a, b, c, alibi_slopes=slopes)
+
+    o, lse = call(qd, kd, vd)
+    fa.fa_check()
+    for b in range(B):
+        ob, lb = call(qd[b:b + 1].contiguous(), kd[b:b + 1].contiguous(), vd[b:b + 1].contiguous())
+        fa.fa_check()
+        assert torch.equal(o[b:b + 1], ob) and torch.equal(lse[b:b + 1], lb), f"{mode}: batch entry {b}"
+
+
 VARLEN_CASES = [
     ([1, 127, 128, 129, 300, 5], [1, 127, 128, 129, 300, 5], 4, 2, 128, True),
     ([1, 127, 128, 129, 300, 5], [1, 127, 128, 129, 300, 5], 4, 2, 64, False),

@@ -17,9 +17,10 @@
 //   warp  12    TMA producer: Q tiles and the K/V ring
 //   warp  13    MMA issuer and tensor-memory owner
 //   warps 14-15 idle
-// Register budget per thread after setmaxnreg: softmax 192, epilogue 64,
-// producer/MMA warpgroup 64 (2*128*192 + 128*64 + 128*64 = 65536, the whole
-// register file at the launch's 128 per thread).
+// Register budget per thread after setmaxnreg, the whole register file at the
+// launch's 128 per thread: softmax 192, epilogue 64, producer/MMA warpgroup 64
+// (2*128*192 + 128*64 + 128*64 = 65536); a few kernels shift it (kSmRegs,
+// kEpiRegs, kCtlRegs in the kernel body).
 // The two Q tiles ping-pong: while one softmax group turns S into P, the
 // tensor core computes the other tile's S or P.V.
 //
@@ -108,6 +109,8 @@ struct Work {
 // batches (or sequences, longest first) outermost; KV heads in L2-sized
 // sections; inside a section the 256-row blocks in reverse order when causal
 // (longest work first), then the KV head, then the query heads sharing it.
+// The host launches a dense batch as B = 1 with B*Hq query heads over B*Hkv
+// KV heads (ALiBi excepted), so one longest-first list covers all of it.
 template <bool CAUSAL, bool VARLEN, int VAR>
 __device__ __forceinline__ Work decode_tile(const FwdParams& p, int t)
 {

@@ -465,8 +465,10 @@ def main(argv=None):
     launches_per_step = fa.fa_last_launch_count()
 
     # ---- device-resident timed region
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clk_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_rank{rank}.csv")
+    # raw clock samples of the timed region (the JSON line carries their summary)
+    out_dir = os.environ.get("FA_BENCH_OUT_DIR", os.path.join(ROOT, "bench_out"))
+    os.makedirs(out_dir, exist_ok=True)
+    clk_path = os.path.join(out_dir, f"bench_clocks_rank{rank}.csv")
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier()

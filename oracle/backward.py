@@ -5,7 +5,7 @@ leg may import this module.  Nothing here is shared with the CUDA path.
 
 The loss is L = sum(O * dO) for a given upstream gradient dO (so dO is
 dL/dO).  With the scale c, the mask M (0 or -inf) and, per (batch, query
-head) slice, S = c Q K^T + M, P = softmax_rows(S), O = P V, the gradients are
+head) slice, S = c Q K^T + M, P = row softmax of S, O = P V, the gradients are
 the plain definitions (FlashAttention from Scratch, sec. 8 "Backward: spend
 arithmetic to save memory"):
 
@@ -23,16 +23,19 @@ contribute nothing.
 :func:`attention_bwd` evaluates these definitions with materialised S and P,
 one block of query rows at a time (numpy matrix products in fp64), and can
 restrict the returned rows of dQ and of dK/dV to samples so that full-size
-problems can be checked.  :func:`blocked_backward` follows the pages' own
-recomputation order instead (reconstruct P from the saved log-sum-exp tile
-by tile and accumulate each gradient from tile products); the tests pin the
-two against each other, against finite differences and against closed forms.
+problems can be checked.  :func:`recomputed_backward` is a second model in
+the recomputation style the pages describe (P rebuilt from the saved
+natural-log normaliser instead of being kept, delta from the saved output),
+organised the way a key-parallel GPU backward is: each key block owns its
+dK and dV rows and sweeps every query block, while dQ collects partial
+products from every key block.  The tests pin the two against each other,
+against finite differences and against closed forms.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from .reference import allowed_mask, scores, softmax_rows
+from .reference import allowed, exp_shifted, positions, probabilities, score_matrix
 
 
 def _f64(x) -> np.ndarray:
@@ -54,7 +57,7 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool = False, q_rows=None, 
     B, Hq, Lq, D = q.shape
     _, Hkv, Lk, _ = k.shape
     r = Hq // Hkv
-    mask_all = allowed_mask(Lq, Lk, causal, q_start=Lk - Lq, k_start=0)
+    mask_all = allowed(positions(Lq, Lk - Lq), positions(Lk), causal)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
@@ -77,7 +80,7 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool = False, q_rows=None, 
                 Q, G = q[b, h, i0:i1], do[b, h, i0:i1]
                 s = (Q @ K.T) * scale
                 s = np.where(mask_all[i0:i1], s, -np.inf)
-                p = softmax_rows(s)
+                p = probabilities(s)
                 o = p @ V
                 delta = (o * G).sum(axis=1)
                 dp = G @ V.T
@@ -96,30 +99,39 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool = False, q_rows=None, 
     return dq, dk, dv
 
 
-def blocked_backward(q, k, v, o, lse, do, scale: float, block_q: int = 32, block_k: int = 64,
-                     causal: bool = False, q_start: int = 0, k_start: int = 0):
-    """Backward of one (batch, head) slice in the recomputation order of the
-    pages: delta from the saved output, P rebuilt tile by tile from the saved
-    natural-log LSE, and the gradient tiles accumulated per (query block, key
-    block) pair.  q [Nq, d], k [Nk, d], v [Nk, dv]; positions q_start/k_start
-    give the causal mask (key position <= query position)."""
+def recomputed_backward(q, k, v, o, lse, do, scale: float, causal: bool = False, qpos=None,
+                        kpos=None, query_blocks=None, key_blocks=None):
+    """Gradients (dq, dk, dv) of sum(O * do) for one (batch, head) slice,
+    from the saved forward results o [n, dv] and lse [n] (natural log).
+
+    q [n, d], k [m, d], v [m, dv]; ``qpos``/``kpos`` are token positions
+    for the causal mask (key position <= query position).  ``query_blocks``
+    and ``key_blocks`` are (start, stop) ranges; each key block is finished
+    (its dK, dV rows written) before the next one starts.
+    """
     q, k, v, o, lse, do = (_f64(x) for x in (q, k, v, o, lse, do))
-    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    delta = (o * do).sum(axis=1)
-    # a row with no allowed key has lse = -inf; shifting by 0 keeps exp(-inf) = 0
-    shift = np.where(np.isfinite(lse), lse, 0.0)
-    for i in range(0, q.shape[0], block_q):
-        rows = slice(i, i + block_q)
-        for j in range(0, k.shape[0], block_k):
-            cols = slice(j, j + block_k)
-            s = scores(q[rows], k[cols], scale, causal, q_start + i, k_start + j)
-            p = np.exp(s - shift[rows, None])
-            dp = do[rows] @ v[cols].T
-            ds = p * (dp - delta[rows, None])
-            dq[rows] += scale * (ds @ k[cols])
-            dk[cols] += scale * (ds.T @ q[rows])
-            dv[cols] += p.T @ do[rows]
-    return dq, dk, dv
+    n, m = q.shape[0], k.shape[0]
+    qpos = positions(n) if qpos is None else np.asarray(qpos)
+    kpos = positions(m) if kpos is None else np.asarray(kpos)
+    query_blocks = [(0, n)] if query_blocks is None else list(query_blocks)
+    key_blocks = [(0, m)] if key_blocks is None else list(key_blocks)
+    # delta_i = sum_t P_it dP_it equals the row dot product of O and dO
+    delta = np.einsum("id,id->i", o, do)
+    dq_sum = np.zeros_like(q)
+    dk, dv = np.zeros_like(k), np.zeros_like(v)
+    for c0, c1 in key_blocks:
+        kb, vb = k[c0:c1], v[c0:c1]
+        dk_sum = np.zeros_like(kb)
+        for r0, r1 in query_blocks:
+            s = score_matrix(q[r0:r1], kb, scale, qpos[r0:r1], kpos[c0:c1], causal)
+            # P_ij = exp(s_ij - lse_i); masked pairs (and rows with no key) give 0
+            p = exp_shifted(s, lse[r0:r1, None])
+            ds = p * (do[r0:r1] @ vb.T - delta[r0:r1, None])
+            dv[c0:c1] += p.T @ do[r0:r1]
+            dk_sum += ds.T @ q[r0:r1]
+            dq_sum[r0:r1] += ds @ kb
+        dk[c0:c1] = scale * dk_sum
+    return scale * dq_sum, dk, dv
 
 
 def attention_bwd_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = False):

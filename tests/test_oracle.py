@@ -50,20 +50,20 @@ def test_three_scores_dense(golden):
     q, k, v = scalar_problem(g["scores"], g["values"])
     o, lse = c_oracle_1head(q, k, v, scale=1.0)
     assert printed(o[0, 0], g["output"], g["output_decimals"])
-    o2, _ = R.dense_attention(q, k, v, scale=1.0)
+    o2 = R.definition(q, k, v, scale=1.0).o
     assert printed(o2[0, 0], g["output"], g["output_decimals"])
     # LSE is the natural-log normaliser of the row: exp(lse) sums the weights
     assert math.isclose(math.exp(float(lse[0])), sum(math.exp(s) for s in g["scores"]), rel_tol=1e-14)
 
 
-def test_three_scores_streaming(golden):
+def test_three_scores_online(golden):
     g = golden["three_scores"]
     q, k, v = scalar_problem(g["scores"], g["values"])
-    trace = []
-    o, _ = R.streaming_attention(q, k, v, scale=1.0, block_q=1, block_k=2, trace=trace)
+    hist = []
+    o, _ = R.online(q, k, v, scale=1.0, key_blocks=R.blocks(3, 2), history=hist)
     assert printed(o[0, 0], g["output"], g["output_decimals"])
     # the maximum rises from 2 to 3 on the second tile: alpha = e^(2-3)
-    (m1, _, _), (m2, _, _) = trace
+    m1, m2 = hist[0].top, hist[1].top
     assert float(m1[0]) == 2.0 and float(m2[0]) == 3.0
     assert math.isclose(math.exp(float(m1[0] - m2[0])), math.exp(-1.0), rel_tol=0, abs_tol=0)
 
@@ -72,9 +72,9 @@ def test_two_tile_example_intermediates(golden):
     g = golden["two_tiles"]
     dec = g["decimals"]
     q, k, v = scalar_problem(g["scores"], g["values"])
-    trace = []
-    o, _ = R.streaming_attention(q, k, v, scale=1.0, block_q=1, block_k=g["tile_size"], trace=trace)
-    (m1, l1, A1), (m2, l2, A2) = trace
+    hist = []
+    o, _ = R.online(q, k, v, scale=1.0, key_blocks=R.blocks(len(k), g["tile_size"]), history=hist)
+    (m1, l1, A1), (m2, l2, A2) = ((h.top, h.mass, h.acc) for h in hist)
     assert float(m1[0]) == g["m1"] and float(m2[0]) == g["m2"]
     assert printed(l1[0], g["l1"], dec["l1"])
     assert printed(A1[0, 0], g["A1"], dec["A1"])
@@ -94,19 +94,18 @@ def test_conditional_rescale_keeps_reference(golden):
     tau = c["tau_log2"] * math.log(2.0)  # 8 in base 2 is 8 ln 2 in natural units
     assert math.isclose(math.exp(tau), c["factor"], rel_tol=1e-12)
     q, k, v = scalar_problem(g2["scores"], g2["values"])
-    trace = []
-    o_lazy, lse_lazy = R.streaming_attention(q, k, v, scale=1.0, block_q=1, block_k=2, tau=tau,
-                                             trace=trace)
-    o_eager, lse_eager = R.streaming_attention(q, k, v, scale=1.0, block_q=1, block_k=2)
+    hist = []
+    o_lazy, lse_lazy = R.online(q, k, v, scale=1.0, key_blocks=R.blocks(4, 2), tau=tau, history=hist)
+    o_eager, lse_eager = R.online(q, k, v, scale=1.0, key_blocks=R.blocks(4, 2))
     # max 2 -> 3 is within the threshold: the reference stays at 2
-    assert float(trace[1][0][0]) == 2.0
+    assert float(hist[1].top[0]) == 2.0
     assert abs(float(o_lazy[0, 0] - o_eager[0, 0])) < 1e-12
     assert abs(float(lse_lazy[0] - lse_eager[0])) < 1e-12
     # a jump larger than the threshold does move the reference
     q, k, v = scalar_problem([0.0, 1.0, 20.0, 3.0], [1.0, 2.0, 3.0, 4.0])
-    trace = []
-    R.streaming_attention(q, k, v, scale=1.0, block_q=1, block_k=2, tau=tau, trace=trace)
-    assert float(trace[0][0][0]) == 1.0 and float(trace[1][0][0]) == 20.0
+    hist = []
+    R.online(q, k, v, scale=1.0, key_blocks=R.blocks(4, 2), tau=tau, history=hist)
+    assert float(hist[0].top[0]) == 1.0 and float(hist[1].top[0]) == 20.0
 
 
 # ---------------------------------------------------------------------- invariants
@@ -169,7 +168,7 @@ def test_probability_rows_sum_to_one():
     k = rng.standard_normal((13, 8)) * 3
     v = rng.standard_normal((13, 8))
     for causal in (False, True):
-        _, _, p = R.dense_attention(q, k, v, causal=causal, q_start=4, return_p=True)
+        p = R.definition(q, k, v, causal=causal, qpos=R.positions(9, 4)).p
         assert np.all(p >= 0)
         assert np.max(np.abs(p.sum(axis=1) - 1.0)) < 1e-15 * 16
 
@@ -301,21 +300,22 @@ def test_sampled_rows_match_full_evaluation():
 
 # ----------------------------------------------- tiling, order and partitions (recurrence)
 
-def test_streaming_matches_dense_on_the_pages_case():
+def test_online_matches_definition_on_the_pages_case():
     # 5 queries that are the final positions of a 13-token cache, blocks 3 / 4
     rng = np.random.default_rng(7)
     q = rng.standard_normal((5, 16))
     k = rng.standard_normal((13, 16))
     v = rng.standard_normal((13, 8))
-    ref, ref_lse = R.dense_attention(q, k, v, causal=True, q_start=8)
-    out, lse = R.streaming_attention(q, k, v, block_q=3, block_k=4, causal=True, q_start=8)
+    ref, ref_lse = R.definition(q, k, v, causal=True, qpos=R.positions(5, 8))[2:]
+    out, lse = R.online(q, k, v, causal=True, qpos=R.positions(5, 8), query_blocks=R.blocks(5, 3),
+                        key_blocks=R.blocks(13, 4))
     assert np.max(np.abs(out - ref)) < 1e-10 and np.max(np.abs(lse - ref_lse)) < 1e-10
     # the C oracle (bottom-right alignment, Lq=5, Lk=13) is the same problem
     oc, lc = c_oracle_1head(q.astype(np.float32).tolist(), k.astype(np.float32).tolist(),
                             np.pad(v, ((0, 0), (0, 8))).astype(np.float32).tolist(),
                             scale=1 / 4.0, causal=True)
-    rq, rl = R.dense_attention(q.astype(np.float32), k.astype(np.float32),
-                               v.astype(np.float32), causal=True, q_start=8)
+    rq, rl = R.definition(q.astype(np.float32), k.astype(np.float32),
+                          v.astype(np.float32), causal=True, qpos=R.positions(5, 8))[2:]
     assert np.max(np.abs(oc[:, :8] - rq)) < 1e-12 and np.max(np.abs(lc - rl)) < 1e-12
 
 
@@ -327,15 +327,15 @@ def test_tile_size_and_order_independence(block_q, block_k):
     q = rng.standard_normal((nq, 8)) * 20  # sharp softmax (scores x 20)
     k = rng.standard_normal((nk, 8))
     v = rng.standard_normal((nk, 8))
-    ref, ref_lse = R.dense_attention(q, k, v, causal=True, q_start=nk - nq)
-    ntiles = (nk + block_k - 1) // block_k
-    order = list(range(ntiles))
-    random.Random(block_q + block_k).shuffle(order)
-    for kv_order in (None, order):
+    qpos = R.positions(nq, nk - nq)
+    ref, ref_lse = R.definition(q, k, v, causal=True, qpos=qpos)[2:]
+    in_order = R.blocks(nk, block_k)
+    shuffled = list(in_order)
+    random.Random(block_q + block_k).shuffle(shuffled)
+    for key_blocks in (in_order, shuffled):
         for tau in (None, 0.0, 8 * math.log(2.0)):
-            with np.errstate(invalid="ignore"):
-                out, lse = R.streaming_attention(q, k, v, block_q=block_q, block_k=block_k, causal=True,
-                                                 q_start=nk - nq, tau=tau, kv_order=kv_order)
+            out, lse = R.online(q, k, v, causal=True, qpos=qpos, query_blocks=R.blocks(nq, block_q),
+                                key_blocks=key_blocks, tau=tau)
             assert np.max(np.abs(out - ref)) < 1e-10
             assert np.max(np.abs(lse - ref_lse)) < 1e-10
 
@@ -346,9 +346,9 @@ def test_fully_masked_rows_are_zero_with_minus_inf_lse():
     k = rng.standard_normal((9, 8))
     v = rng.standard_normal((9, 8))
     # q_start = -2: the first two query rows precede every key
-    with np.errstate(invalid="ignore"):
-        out, lse = R.streaming_attention(q, k, v, block_q=4, block_k=4, causal=True, q_start=-2)
-    ref, ref_lse = R.dense_attention(q, k, v, causal=True, q_start=-2)
+    out, lse = R.online(q, k, v, causal=True, qpos=R.positions(6, -2), query_blocks=R.blocks(6, 4),
+                        key_blocks=R.blocks(9, 4))
+    ref, ref_lse = R.definition(q, k, v, causal=True, qpos=R.positions(6, -2))[2:]
     assert np.all(out[:2] == 0) and np.all(lse[:2] == -np.inf)
     assert np.max(np.abs(out[2:] - ref[2:])) < 1e-10
     assert np.array_equal(ref_lse[:2], lse[:2])
@@ -361,17 +361,17 @@ def test_partition_merge_in_two_orders():
     v = rng.standard_normal((30, 8))
     sc = 1 / math.sqrt(8)
     parts = [(0, 11), (11, 12), (12, 30)]
-    st = [R.partition_state(q, k[a:b], v[a:b], sc) for a, b in parts]
-    ref, ref_lse = R.dense_attention(q, k, v)
-    for merged in (R.merge_states(R.merge_states(st[0], st[1]), st[2]),
-                   R.merge_states(st[2], R.merge_states(st[1], st[0]))):
-        m, l, u = merged
+    st = [R.RowState.from_scores(R.score_matrix(q, k[a:b], sc), v[a:b]) for a, b in parts]
+    ref, ref_lse = R.definition(q, k, v)[2:]
+    for merged in (R.combine(R.combine(st[0], st[1]), st[2]),
+                   R.combine(st[2], R.combine(st[1], st[0]))):
+        m, l, u = merged.top, merged.mass, merged.acc
         assert np.max(np.abs(u / l[:, None] - ref)) < 1e-12
         assert np.max(np.abs(m + np.log(l) - ref_lse)) < 1e-12
     # the normalised-output form with natural-log normalisers
-    outs = [R.dense_attention(q, k[a:b], v[a:b]) for a, b in parts]
-    o, L = R.merge_lse(*outs[0], *outs[1])
-    o, L = R.merge_lse(o, L, *outs[2])
+    outs = [R.from_normalised(*R.definition(q, k[a:b], v[a:b])[2:]) for a, b in parts]
+    o, L = R.combine(outs[0], outs[1]).result()
+    o, L = R.combine(R.from_normalised(o, L), outs[2]).result()
     assert np.max(np.abs(o - ref)) < 1e-12 and np.max(np.abs(L - ref_lse)) < 1e-12
 
 

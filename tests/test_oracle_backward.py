@@ -10,8 +10,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.backward import attention_bwd, attention_bwd_varlen, blocked_backward
-from oracle.reference import dense_attention
+from oracle.backward import attention_bwd, attention_bwd_varlen, recomputed_backward
+from oracle.reference import blocks, definition, positions
 
 
 def _rand(shape, seed, scale=1.0):
@@ -142,30 +142,33 @@ def test_gqa_equals_repeated_heads_summed():
 
 
 @pytest.mark.parametrize("block_q,block_k", [(1, 1), (3, 4), (32, 64), (5, 2)])
-def test_blocked_recomputation_matches_definition(block_q, block_k):
+def test_recomputation_matches_definition(block_q, block_k):
     """The pages' case: five queries at the end of a nine-key sequence, causal,
     recomputed tile by tile from the saved output and log-sum-exp."""
     q, k, v, do = _rand((5, 7), 40), _rand((9, 7), 41), _rand((9, 3), 42), _rand((5, 3), 43)
     scale = 1 / math.sqrt(7)
-    o, lse = dense_attention(q, k, v, scale=scale, causal=True, q_start=4)
-    got = blocked_backward(q, k, v, o, lse, do, scale, block_q, block_k, causal=True, q_start=4)
+    o, lse = definition(q, k, v, scale=scale, causal=True, qpos=positions(5, 4))[2:]
+    got = recomputed_backward(q, k, v, o, lse, do, scale, causal=True, qpos=positions(5, 4),
+                              query_blocks=blocks(5, block_q), key_blocks=blocks(9, block_k))
     ref = attention_bwd(q[None, None], k[None, None], v[None, None], do[None, None], scale, True)
     for g, e in zip(got, ref):
         np.testing.assert_allclose(g, e[0, 0], atol=1e-12)
 
 
-def test_blocked_handles_rows_without_keys():
+def test_recomputation_handles_rows_without_keys():
     """q_start = -2: the first two queries precede every key (LSE = -inf)."""
     q, k, v, do = _rand((6, 4), 50), _rand((5, 4), 51), _rand((5, 4), 52), _rand((6, 4), 53)
-    o, lse = dense_attention(q, k, v, scale=0.5, causal=True, q_start=-2)
+    o, lse = definition(q, k, v, scale=0.5, causal=True, qpos=positions(6, -2))[2:]
     assert np.isneginf(lse[:2]).all()
-    dq, dk, dv = blocked_backward(q, k, v, o, lse, do, 0.5, 4, 2, causal=True, q_start=-2)
+    dq, dk, dv = recomputed_backward(q, k, v, o, lse, do, 0.5, causal=True, qpos=positions(6, -2),
+                                     query_blocks=blocks(6, 4), key_blocks=blocks(5, 2))
     assert np.all(np.isfinite(dq)) and np.abs(dq[:2]).max() == 0.0
     # same problem in the dense layout: Lq = 6 > Lk = 5 puts the offset at -1,
     # so compare with the matching bottom-right case instead
-    o2, lse2 = dense_attention(q, k, v, scale=0.5, causal=True, q_start=-1)
+    o2, lse2 = definition(q, k, v, scale=0.5, causal=True, qpos=positions(6, -1))[2:]
     ref = attention_bwd(q[None, None], k[None, None], v[None, None], do[None, None], 0.5, True)
-    got = blocked_backward(q, k, v, o2, lse2, do, 0.5, 4, 2, causal=True, q_start=-1)
+    got = recomputed_backward(q, k, v, o2, lse2, do, 0.5, causal=True, qpos=positions(6, -1),
+                              query_blocks=blocks(6, 4), key_blocks=blocks(5, 2))
     for g, e in zip(got, ref):
         np.testing.assert_allclose(g, e[0, 0], atol=1e-12)
 

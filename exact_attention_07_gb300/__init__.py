@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_varlen", "fa_fwd_hdim", "fa_fwd_varlen_hdi
                     "fa_test_inject_fault")
 SPLITKV_MAX_ROWS = 16  # (Hq / Hkv) * Lq limit of fa_fwd_splitkv
 NOALLOC_MAX_SEQS = 16384  # FA_NOALLOC_MAX_SEQS in include/fa_gb300.h
+VARLEN_SEQS_PER_LAUNCH = 1536  # FA_VARLEN_SEQS_PER_LAUNCH (64 for head dimensions (192, 128))
 
 
 class _Variant(ctypes.Structure):
@@ -135,10 +136,10 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _check_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int):
+def _check_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int, on_device: bool = True):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
+    if on_device and t.device.type != "cuda":
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -181,28 +182,42 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
     return out, lse
 
 
+def _check_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, out, lse):
+    """Dtypes, ranks, layouts and shapes of a packed call (q [Tq,Hq,D], k and
+    v [Tk,Hkv,D], offsets of equal length, out [Tq,Hq,D], lse [Hq,Tq]) first,
+    then that every tensor lives on a CUDA device.  Returns (Tq, Hq, D, Tk, Hkv)."""
+    named = [(q, "q", torch.bfloat16, 3), (k, "k", torch.bfloat16, 3), (v, "v", torch.bfloat16, 3),
+             (cu_seqlens_q, "cu_seqlens_q", torch.int32, 1), (cu_seqlens_k, "cu_seqlens_k", torch.int32, 1),
+             (out, "out", torch.float32, 3), (lse, "lse", torch.float32, 2)]
+    for t, n, dt, nd in named:
+        _check_tensor(t, n, dt, nd, on_device=False)
+    Tq, Hq, D = q.shape
+    Tk, Hkv, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Dk != D:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold num_seqs + 1 >= 2 offsets")
+    if tuple(out.shape) != tuple(q.shape) or tuple(lse.shape) != (Hq, Tq):
+        raise ValueError(f"out must be {tuple(q.shape)} and lse {(Hq, Tq)}, got {tuple(out.shape)} and "
+                         f"{tuple(lse.shape)}")
+    for t, n, _, _ in named:
+        if t.device.type != "cuda":
+            raise ValueError(f"{n} must be a CUDA tensor")
+    return Tq, Hq, D, Tk, Hkv
+
+
 def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
                   cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, causal: bool = False,
                   softmax_scale: float | None = None, out: torch.Tensor | None = None,
                   lse: torch.Tensor | None = None, stream=None):
     """Packed variable-length forward.  q [Tq,Hq,D], k/v [Tk,Hkv,D] bf16 CUDA,
-    cu_seqlens_* int32 CUDA [num_seqs+1].  Returns (o [Tq,Hq,D] fp32, lse [Hq,Tq] fp32)."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check_tensor(t, n, torch.bfloat16, 3)
-    _check_tensor(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
-    _check_tensor(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
-    Tq, Hq, D = q.shape
-    Tk, Hkv, Dk = k.shape
-    if tuple(v.shape) != tuple(k.shape) or Dk != D or cu_seqlens_q.numel() != cu_seqlens_k.numel():
-        raise ValueError("shape mismatch")
+    cu_seqlens_* int32 CUDA [num_seqs+1].  Returns (o [Tq,Hq,D] fp32, lse [Hq,Tq] fp32).
+    Allocates nothing on the device beyond ``out``/``lse`` when they are not given."""
     if out is None:
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     if lse is None:
-        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
-    _check_tensor(out, "out", torch.float32, 3)
-    _check_tensor(lse, "lse", torch.float32, 2)
-    if tuple(out.shape) != tuple(q.shape) or tuple(lse.shape) != (Hq, Tq):
-        raise ValueError("out/lse shape mismatch")
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    Tq, Hq, D, Tk, Hkv = _check_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, out, lse)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     lib = load_library()
@@ -293,18 +308,16 @@ def fa_fwd_varlen_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_
                           cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, out: torch.Tensor,
                           lse: torch.Tensor, causal: bool = False, softmax_scale: float | None = None,
                           stream=None):
-    """fa_fwd_varlen for callers that must not allocate device memory: the
-    schedule lives in a fixed array inside the library (at most
-    NOALLOC_MAX_SEQS sequences), and the caller provides ``out`` and ``lse``.
-    Calls that can overlap on the GPU share that array and must be ordered."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check_tensor(t, n, torch.bfloat16, 3)
-    _check_tensor(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
-    _check_tensor(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
-    _check_tensor(out, "out", torch.float32, 3)
-    _check_tensor(lse, "lse", torch.float32, 2)
-    Tq, Hq, D = q.shape
-    Tk, Hkv, _ = k.shape
+    """Packed forward for callers that cannot call cudaMalloc on the hot path
+    (a process whose device memory all belongs to its own allocator, a server
+    that must not allocate while serving): the caller provides ``out`` and
+    ``lse``, and the whole batch's schedule (at most NOALLOC_MAX_SEQS
+    sequences) goes into a fixed array inside the library, so one attention
+    launch covers it.  Calls that can overlap on the GPU share that array and
+    must be ordered.  Every shape is checked before the library is touched."""
+    Tq, Hq, D, Tk, Hkv = _check_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, out, lse)
+    if cu_seqlens_q.numel() - 1 > NOALLOC_MAX_SEQS:
+        raise ValueError(f"at most {NOALLOC_MAX_SEQS} sequences")
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     lib = load_library()

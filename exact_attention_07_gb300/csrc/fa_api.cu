@@ -404,11 +404,47 @@ extern "C" fa_status_t fa_fwd_variant(const void* q, const void* k, const void* 
     return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, D, 0, variant, softmax_scale, stream);
 }
 
+// ------------------------------------------------------------- allocation-free varlen
+
+// Scratch of fa_fwd_varlen_noalloc: the sequence schedule lives in this
+// fixed device array instead of memory obtained per call.  Every GPU that
+// loads the library holds it until the process exits.
+constexpr int kNoAllocMaxSeqs = FA_NOALLOC_MAX_SEQS;
+__device__ __align__(256) int g_noalloc_sched[2 + 3 * kNoAllocMaxSeqs];
+
 namespace {
+int* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_sched, per device
+
+// Resolves the array's device address on the current device (once per
+// device).  In host code the symbol names a host-side stand-in, so only the
+// address obtained here may be handed to a kernel.
+fa_status_t noalloc_scratch(int** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_sched) != cudaSuccess || !ptr) return FA_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<int*>(ptr);
+    }
+    *out = g_noalloc_ptr[dev];
+    return FA_OK;
+}
+}  // namespace
+
+namespace {
+// Packed forward.  The library allocates nothing: normally each launch's CTAs
+// build the schedule of up to varlen_sched_max_seqs(D, Dv) sequences in
+// shared memory, and a larger batch is split into consecutive launches of
+// that many sequences.  With `fixed_scratch` a schedule kernel writes one
+// schedule for the whole batch into the library's fixed device array
+// (g_noalloc_sched, at most FA_NOALLOC_MAX_SEQS sequences) and a single
+// attention launch reads it.
 fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse, const int* cu_seqlens_q,
                        const int* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
                        int max_seqlen_k, int Hq, int Hkv, int D, int Dv, int causal, const fa_variant_t* variant,
-                       float softmax_scale, cudaStream_t stream)
+                       float softmax_scale, cudaStream_t stream, bool fixed_scratch = false)
 {
     g_last_launches = 0;
     if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
@@ -420,10 +456,7 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
         (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
         return FA_ERR_INVALID_ARG;
     if (!hdim_supported(D, Dv)) return FA_ERR_UNSUPPORTED;
-    // upper bound of the work tiles: sum_s ceil(Lq_s / 256) <= total_q / 256 + num_seqs
-    long long ub = (long long)Hq * ((long long)total_q / kRowsPerCta + num_seqs);
-    const long long ub2 = (long long)Hq * num_seqs * ((max_seqlen_q + kRowsPerCta - 1) / kRowsPerCta);
-    if (ub2 < ub) ub = ub2;
+    // work tiles: sum_s ceil(Lq_s / 256) <= total_q / 256 + num_seqs per query head
     if ((long long)Hq * ((long long)total_q / kRowsPerCta + num_seqs) >= (1ll << 31) ||
         (long long)total_q * Hq >= (1ll << 31) * 64ll)
         return FA_ERR_INVALID_ARG;
@@ -433,9 +466,12 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
         var = prepare_variant(variant, D, softmax_scale, &p);
         if (var < 0) return (fa_status_t)(-var);
     }
+    if (fixed_scratch && num_seqs > kNoAllocMaxSeqs) return FA_ERR_INVALID_ARG;  // the fixed array holds no more
     DeviceState* ds = nullptr;
     fa_status_t st = device_state(&ds);
     if (st != FA_OK) return st;
+    int* sched_scratch = nullptr;
+    if (fixed_scratch && (st = noalloc_scratch(&sched_scratch)) != FA_OK) return st;
 
     CUtensorMap mq, mk, mv;
     const uint64_t row = (uint64_t)D * 2, vrow = (uint64_t)Dv * 2;
@@ -444,14 +480,6 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
         !encode_map(&mv, v, Dv, Hkv, total_k, vrow, vrow * Hkv, 1, 128))
         return FA_ERR_CUDA;
 
-    int* sched = nullptr;
-    const size_t ws = sizeof(int) * (2 + 3 * (size_t)num_seqs);
-    if (cudaMallocAsync(reinterpret_cast<void**>(&sched), ws, stream) != cudaSuccess) return FA_ERR_CUDA;
-    if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
-                               max_seqlen_k, Hq, 0, sched, ds->err, stream) != cudaSuccess) {
-        cudaFreeAsync(sched, stream);
-        return FA_ERR_CUDA;
-    }
     p.o = o;
     p.lse = lse;
     p.Hq = Hq;
@@ -461,17 +489,46 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
     p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, D + Dv, false);
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
-    p.sched = sched;
     p.num_seqs = num_seqs;
     p.total_q = total_q;
+    p.total_k = total_k;
+    p.max_q = max_seqlen_q;
+    p.max_k = max_seqlen_k;
     p.err = ds->err;
     p.diag = ds->diag;
-    const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
-    const cudaError_t e = variant ? dispatch_variant<true>(D, var, mq, mk, mv, p, grid, stream)
-                                  : dispatch<true>(D, causal != 0, mq, mk, mv, p, grid, stream);
-    cudaFreeAsync(sched, stream);
-    if (e != cudaSuccess) return FA_ERR_CUDA;
-    g_last_launches = 2;
+    const long long mb_per_seq = (max_seqlen_q + kRowsPerCta - 1) / kRowsPerCta;
+    auto launch = [&](int count) -> cudaError_t {
+        // grid: no more CTAs than work tiles can exist, at most one per SM
+        long long ub = (long long)Hq * ((long long)total_q / kRowsPerCta + count);
+        const long long ub2 = (long long)Hq * count * mb_per_seq;
+        if (ub2 < ub) ub = ub2;
+        const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
+        return variant ? dispatch_variant<true>(D, var, mq, mk, mv, p, grid, stream)
+                       : dispatch<true>(D, causal != 0, mq, mk, mv, p, grid, stream);
+    };
+    if (sched_scratch) {
+        if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                                   max_seqlen_k, Hq, 0, sched_scratch, ds->err, stream) != cudaSuccess)
+            return FA_ERR_CUDA;
+        g_last_launches = 1;
+        p.sched = sched_scratch;
+        p.seq_begin = 0;
+        p.seq_count = num_seqs;
+        if (launch(num_seqs) != cudaSuccess) return FA_ERR_CUDA;
+        g_last_launches = 2;
+        return FA_OK;
+    }
+    static_assert(varlen_sched_max_seqs(64, 64) == FA_VARLEN_SEQS_PER_LAUNCH &&
+                      varlen_sched_max_seqs(128, 128) == FA_VARLEN_SEQS_PER_LAUNCH,
+                  "launch size of packed batches differs from the header's");
+    const int per_launch = varlen_sched_max_seqs(D, Dv);
+    for (int b = 0; b < num_seqs; b += per_launch) {
+        p.sched = nullptr;
+        p.seq_begin = b;
+        p.seq_count = num_seqs - b < per_launch ? num_seqs - b : per_launch;
+        if (launch(p.seq_count) != cudaSuccess) return FA_ERR_CUDA;
+        ++g_last_launches;
+    }
     return FA_OK;
 }
 }  // namespace
@@ -506,95 +563,16 @@ extern "C" fa_status_t fa_fwd_varlen_variant(const void* q, const void* k, const
                       max_seqlen_k, Hq, Hkv, D, D, 0, variant, softmax_scale, stream);
 }
 
-// ------------------------------------------------------------- allocation-free varlen
-
-// Scratch of fa_fwd_varlen_noalloc: the sequence schedule lives in this
-// fixed device array instead of memory obtained per call.  Every GPU that
-// loads the library holds it until the process exits.
-constexpr int kNoAllocMaxSeqs = FA_NOALLOC_MAX_SEQS;
-__device__ __align__(256) int g_noalloc_sched[2 + 3 * kNoAllocMaxSeqs];
-
-namespace {
-int* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_sched, per device
-
-// Resolves the array's device address on the current device (once per
-// device).  In host code the symbol names a host-side stand-in, so only the
-// address obtained here may be handed to a kernel.
-fa_status_t noalloc_scratch(int** out)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_sched) != cudaSuccess || !ptr) return FA_ERR_CUDA;
-        g_noalloc_ptr[dev] = static_cast<int*>(ptr);
-    }
-    *out = g_noalloc_ptr[dev];
-    return FA_OK;
-}
-}  // namespace
-
 extern "C" fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, float* o, float* lse,
                                              const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
                                              int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
                                              int Hq, int Hkv, int D, int causal, float softmax_scale,
                                              cudaStream_t stream)
 {
-    g_last_launches = 0;
-    if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
-    if (num_seqs <= 0 || total_q <= 0 || total_k <= 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 || Hq <= 0 ||
-        Hkv <= 0 || D <= 0)
-        return FA_ERR_INVALID_ARG;
-    if (num_seqs > kNoAllocMaxSeqs) return FA_ERR_INVALID_ARG;  // the fixed scratch holds no more
-    if (Hq % Hkv != 0 || !scale_ok(softmax_scale)) return FA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-        (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
-        return FA_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-    long long ub = (long long)Hq * ((long long)total_q / kRowsPerCta + num_seqs);
-    const long long ub2 = (long long)Hq * num_seqs * ((max_seqlen_q + kRowsPerCta - 1) / kRowsPerCta);
-    if (ub2 < ub) ub = ub2;
-    if ((long long)Hq * ((long long)total_q / kRowsPerCta + num_seqs) >= (1ll << 31) ||
-        (long long)total_q * Hq >= (1ll << 31) * 64ll)
-        return FA_ERR_INVALID_ARG;
-    DeviceState* ds = nullptr;
-    fa_status_t st = device_state(&ds);
-    if (st != FA_OK) return st;
-    int* sched = nullptr;
-    st = noalloc_scratch(&sched);
-    if (st != FA_OK) return st;
-
-    CUtensorMap mq, mk, mv;
-    const uint64_t row = (uint64_t)D * 2;
-    if (!encode_map(&mq, q, D, Hq, total_q, row, row * Hq, 1, 128) ||
-        !encode_map(&mk, k, D, Hkv, total_k, row, row * Hkv, 1, 128) ||
-        !encode_map(&mv, v, D, Hkv, total_k, row, row * Hkv, 1, 128))
-        return FA_ERR_CUDA;
     // The schedule kernel writes every scratch entry the attention kernel
     // reads, so nothing left by an earlier call needs clearing.
-    if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
-                               max_seqlen_k, Hq, 0, sched, ds->err, stream) != cudaSuccess)
-        return FA_ERR_CUDA;
-    FwdParams p{};
-    p.o = o;
-    p.lse = lse;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.group = Hq / Hkv;
-    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
-    p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, 2 * D, false);
-    p.cu_q = cu_seqlens_q;
-    p.cu_k = cu_seqlens_k;
-    p.sched = sched;
-    p.num_seqs = num_seqs;
-    p.total_q = total_q;
-    p.err = ds->err;
-    p.diag = ds->diag;
-    const int grid = (int)(ub < ds->num_sms ? (ub > 0 ? ub : 1) : ds->num_sms);
-    if (dispatch<true>(D, causal != 0, mq, mk, mv, p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
-    g_last_launches = 2;
-    return FA_OK;
+    return fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                      max_seqlen_k, Hq, Hkv, D, D, causal, nullptr, softmax_scale, stream, true);
 }
 
 // ------------------------------------------------------------- split-KV decode

@@ -9,7 +9,7 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
                        const FwdParams& p, int grid, cudaStream_t stream)
 {
     auto kern = fa_fwd_sm103_kernel<D, CAUSAL, VARLEN, VAR, DV>;
-    constexpr int kSmem = FwdSmem<D, VAR, DV>::kAlloc;
+    constexpr int kSmem = fwd_smem_alloc<D, VARLEN, VAR, DV>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, kSmem, stream>>>(q, k, v, p);

@@ -94,6 +94,146 @@ struct FwdSmem {
     static constexpr uint32_t kColS = 0, kColO = 256;
 };
 
+// Schedule of a packed batch built by the CTA itself (launches without a
+// precomputed schedule): tile prefix by rank [n + 1] and rank -> sequence
+// [n], placed after every other region of the layout.  While it is being
+// built, the K/V ring (not yet loaded) serves as scratch for the sort.
+template <int D, int VAR, int DV>
+struct FwdSchedSmem {
+    using L = FwdSmem<D, VAR, DV>;
+    static constexpr int kMaxSeqs = varlen_sched_max_seqs(D, DV);
+    static constexpr int kOff = (L::kBytes + 15) / 16 * 16;
+    static constexpr int kBytes = kOff + (2 * kMaxSeqs + 1) * 4;
+    static constexpr int kAlloc = kBytes + 1024 <= L::kMaxDynamic ? kBytes + 1024 : L::kMaxDynamic;
+    static_assert(kBytes <= L::kMaxDynamic, "packed-batch schedule exceeds the per-CTA shared memory");
+    // sort scratch in the ring: 64-bit keys of the padded count, tiles per sequence, 32 warp sums
+    static constexpr int kPad = kMaxSeqs <= 64 ? 64 : (kMaxSeqs <= 2048 ? 2048 : 4096);
+    static_assert(kPad >= kMaxSeqs, "sort padding");
+    static_assert(kPad * 12 + 32 * 4 <= L::kStages * L::kTileBytes, "sort scratch exceeds the ring");
+};
+
+// Dynamic shared memory of one forward kernel instance.
+template <int D, bool VARLEN, int VAR, int DV>
+constexpr int fwd_smem_alloc()
+{
+    return VARLEN ? FwdSchedSmem<D, VAR, DV>::kAlloc : FwdSmem<D, VAR, DV>::kAlloc;
+}
+
+__device__ __forceinline__ int ld_shared_s32(uint32_t addr)
+{
+    int v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// The packed batch's schedule: the precomputed one in global memory
+// (p.sched), else the one this CTA built at shared address `ss` (tile prefix
+// by rank [n + 1], then rank -> sequence [n]).  Read through the kernel
+// parameters and a 32-bit shared address, so no pointer stays live in the
+// roles' registers.
+struct VarSchedView {
+    const FwdParams& p;
+    uint32_t ss;
+    __device__ __forceinline__ bool pre() const { return p.sched != nullptr; }
+    __device__ __forceinline__ int n() const { return pre() ? p.num_seqs : p.seq_count; }
+    __device__ __forceinline__ int prefix(int r) const
+    {
+        return pre() ? __ldg(p.sched + 1 + r) : ld_shared_s32(ss + 4u * (uint32_t)r);
+    }
+    __device__ __forceinline__ int order(int r) const
+    {
+        return pre() ? __ldg(p.sched + 2 + p.num_seqs + r) : ld_shared_s32(ss + 4u * (uint32_t)(p.seq_count + 1 + r));
+    }
+};
+
+// Builds the schedule of sequences [p.seq_begin, p.seq_begin + p.seq_count)
+// with every thread of the CTA: validates their offsets, orders them by key
+// length, longest first (FlashAttention-4: Blackwell Attention Kernel
+// Co-Design, "LPT scheduling for imbalanced grids"; ties keep the batch
+// order), and writes the exclusive prefix of work tiles (Hq * ceil(Lq / 256)
+// per sequence) in that order.  An invalid sequence, or any sequence when the
+// offsets do not start at 0 and end at the totals, is given no work and sets
+// error bit 1.  `keys` holds kPad 64-bit entries, `tiles` kPad + 32 ints.
+template <int kPad>
+__device__ __forceinline__ void build_varlen_schedule(const FwdParams& p, unsigned long long* keys, int* tiles,
+                                                      int* prefix, int* order)
+{
+    const int n = p.seq_count, tid = (int)threadIdx.x, nthr = (int)blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    int npad = 2;
+    while (npad < n) npad <<= 1;
+    const bool bad = __ldg(p.cu_q) != 0 || __ldg(p.cu_k) != 0 || __ldg(p.cu_q + p.num_seqs) != p.total_q ||
+                     __ldg(p.cu_k + p.num_seqs) != p.total_k;
+    for (int i = tid; i < npad; i += nthr) {
+        unsigned long long key = ~0ull;
+        if (i < n) {
+            const int s = p.seq_begin + i;
+            const int q0 = __ldg(p.cu_q + s), q1 = __ldg(p.cu_q + s + 1);
+            const int k0 = __ldg(p.cu_k + s), k1 = __ldg(p.cu_k + s + 1);
+            const bool ok = !bad && q0 >= 0 && q1 >= q0 && q1 <= p.total_q && q1 - q0 <= p.max_q && k0 >= 0 &&
+                            k1 >= k0 && k1 <= p.total_k && k1 - k0 <= p.max_k;
+            if (!ok && blockIdx.x == 0) atomicOr(p.err, 2);
+            const int len = (ok && q1 > q0) ? (k1 - k0) : -1;
+            tiles[i] = ok ? p.Hq * ((q1 - q0 + kRowsPerCta - 1) / kRowsPerCta) : 0;
+            // ascending order of (longest first, then batch order)
+            key = ((unsigned long long)(0x7fffffffu - (unsigned)len) << 32) | (unsigned)i;
+        }
+        keys[i] = key;
+    }
+    __syncthreads();
+    // bitonic sort of keys[0 .. npad)
+    for (int k = 2; k <= npad; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < npad; i += nthr) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const unsigned long long a = keys[i], b = keys[ixj];
+                    if ((a > b) == ((i & k) == 0)) {
+                        keys[i] = b;
+                        keys[ixj] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // rank -> sequence, and an exclusive scan of the tiles in rank order:
+    // each thread takes a run of consecutive ranks
+    const int per = (n + nthr - 1) / nthr;
+    const int r0 = min(n, tid * per), r1 = min(n, r0 + per);
+    int sum = 0;
+    for (int r = r0; r < r1; ++r) {
+        const int i = (int)(unsigned)keys[r];
+        order[r] = p.seq_begin + i;
+        sum += tiles[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    int* wsum = tiles + kPad;
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int x = lane < nwarps ? wsum[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, d);
+            if (lane >= d) x += y;
+        }
+        wsum[lane] = x;
+    }
+    __syncthreads();
+    int acc = (warp > 0 ? wsum[warp - 1] : 0) + incl - sum;
+    for (int r = r0; r < r1; ++r) {
+        prefix[r] = acc;
+        acc += tiles[(int)(unsigned)keys[r]];
+    }
+    if (tid == 0) prefix[n] = wsum[nwarps - 1];
+}
+
 struct Work {
     int hq, hkv;
     int m0;      // first query row of the CTA's 256-row block, within the sequence
@@ -112,7 +252,7 @@ struct Work {
 // The host launches a dense batch as B = 1 with B*Hq query heads over B*Hkv
 // KV heads (ALiBi excepted), so one longest-first list covers all of it.
 template <bool CAUSAL, bool VARLEN, int VAR>
-__device__ __forceinline__ Work decode_tile(const FwdParams& p, int t)
+__device__ __forceinline__ Work decode_tile(const FwdParams& p, uint32_t sched_smem, int t)
 {
     Work w;
     int rem = t, nmb;
@@ -120,17 +260,15 @@ __device__ __forceinline__ Work decode_tile(const FwdParams& p, int t)
     w.q0 = 0;
     int k0 = 0;
     if constexpr (VARLEN) {
-        const int n = p.num_seqs;
-        const int* prefix = p.sched + 1;
-        const int* order = p.sched + 2 + n;
-        int lo = 0, hi = n - 1;
-        while (lo < hi) {  // largest index whose prefix is <= t
+        const VarSchedView vs{p, sched_smem};
+        int lo = 0, hi = vs.n() - 1;
+        while (lo < hi) {  // largest rank whose prefix is <= t
             const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(prefix + mid) <= t) lo = mid;
+            if (vs.prefix(mid) <= t) lo = mid;
             else hi = mid - 1;
         }
-        const int s = __ldg(order + lo);
-        rem = t - __ldg(prefix + lo);
+        const int s = vs.order(lo);
+        rem = t - vs.prefix(lo);
         w.q0 = __ldg(p.cu_q + s);
         k0 = __ldg(p.cu_k + s);
         w.lq = __ldg(p.cu_q + s + 1) - w.q0;
@@ -406,7 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const WaitFailure wf{p.err, p.diag};
-    if ((uint32_t)(smem - smem_raw) + L::kBytes > (uint32_t)L::kAlloc) {
+    using SS = FwdSchedSmem<D, VAR, DV>;
+    constexpr int kUsed = VARLEN ? SS::kBytes : L::kBytes;
+    if ((uint32_t)(smem - smem_raw) + kUsed > (uint32_t)fwd_smem_alloc<D, VARLEN, VAR, DV>()) {
         // the dynamic window is aligned too loosely for the layout: report, touch nothing
         if (threadIdx.x == 0) atomicOr(p.err, 4);
         return;
@@ -444,11 +584,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
         tmem_relinquish();
     }
+    if (VARLEN && !p.sched) {
+        int* prefix = reinterpret_cast<int*>(smem + SS::kOff);
+        int* order = prefix + p.seq_count + 1;
+        auto* keys = reinterpret_cast<unsigned long long*>(smem + L::kKVOff);
+        build_varlen_schedule<SS::kPad>(p, keys, reinterpret_cast<int*>(keys + SS::kPad), prefix, order);
+        // the sort's generic-proxy writes to the ring precede the TMA writes into it
+        fence_proxy_async_shared();
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int num_tiles = VARLEN ? __ldg(p.sched) : p.num_tiles;
+    int num_tiles = p.num_tiles;
+    if constexpr (VARLEN) {
+        const VarSchedView vs{p, sb + SS::kOff};
+        num_tiles = vs.prefix(vs.n());
+    }
 
     if (warp < 8) {
         // ============================================================ softmax
@@ -472,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // commits every release as soon as the MMAs reading the stage are issued.
         const bool kv_releaser = kSoftmaxFreesKV && t == 1 && row == 0;
         for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
-            const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, tile);
+            const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, sb + SS::kOff, tile);
             if (w.nk == 0) continue;
             const int q_row = w.m0 + t * kBlockM + row;
             int kv_last = w.lk - 1;  // last key this row may attend
@@ -684,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o_ph[2] = {0, 0}, st_ph[2] = {0, 0};
         float* obase = reinterpret_cast<float*>(p.o);
         for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
-            const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, tile);
+            const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, sb + SS::kOff, tile);
             for (int t = 0; t < 2; ++t) {
                 const int q_row = w.m0 + t * kBlockM + row;
                 const bool valid = q_row < w.lq;
@@ -855,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return true;
                 };
                 for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
-                    const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, tile);
+                    const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, sb + SS::kOff, tile);
                     if (w.nk == 0) continue;
                     if (!load_q(w, 0, tile)) break;
                     if (!load_kv(&tmK, w, 0, tile)) break;
@@ -911,7 +1063,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (L::kTail) commit(L::kTEmpty + ts);
             };
             for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
-                const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, tile);
+                const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, sb + SS::kOff, tile);
                 if (w.nk == 0) continue;
                 const int nk = w.nk;
                 // prologue: S0(0), S1(0)

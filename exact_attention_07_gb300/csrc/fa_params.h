@@ -17,9 +17,15 @@ struct FwdParams {
     // variable-length batches
     const int* cu_q;
     const int* cu_k;
-    const int* sched;  // [0] tiles, [1..n+1] tile prefix in schedule order, [n+2..2n+1] order
-    int num_seqs;
-    int total_q;
+    // Precomputed schedule ([0] tiles, [1..n+1] tile prefix in schedule order,
+    // [n+2..2n+1] order, n = num_seqs), or null: then every CTA builds the
+    // schedule of sequences [seq_begin, seq_begin + seq_count) in its own
+    // shared memory (at most varlen_sched_max_seqs(D, DV) of them).
+    const int* sched;
+    int num_seqs;      // sequences in the whole batch
+    int seq_begin, seq_count;
+    int total_q, total_k;
+    int max_q, max_k;  // the caller's length bounds, checked per sequence
     // programmable variants (kernels instantiated with VAR > 0)
     int win_left, win_right;  // key window around the query's aligned position; < 0 = unlimited
     float cap_in;             // soft-capping: scale / cap
@@ -46,6 +52,11 @@ constexpr int kThreads = 512;
 // soft-capping, 3 = key window + ALiBi (FlashAttention from Scratch, sec. 12),
 // 4 = e4m3 inputs with per-tile scales (sec. 10.3).
 enum : int { kVarNone = 0, kVarWindow = 1, kVarSoftcap = 2, kVarAlibi = 3, kVarFp8 = 4 };
+
+// Sequences one launch of a packed batch can schedule in shared memory
+// (what the forward kernel's layout leaves free at each head dimension); the
+// host splits larger batches into launches of at most this many sequences.
+constexpr int varlen_sched_max_seqs(int D, int DV) { return D == DV ? 1536 : 64; }
 constexpr bool var_window(int v) { return v == kVarWindow || v == kVarSoftcap || v == kVarAlibi; }
 
 }  // namespace fa

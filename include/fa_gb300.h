@@ -87,11 +87,19 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, float* o, float*
  * Offsets are read on the device.  Offsets that are not non-decreasing, or a
  * sequence longer than its max_seqlen bound, latch FA_ERR_INVALID_ARG on the
  * device (reported by fa_check); such sequences produce no output.
- * Scheduling first sorts sequences by work, longest first, into a small
- * scratch buffer that this call obtains with cudaMallocAsync on `stream` and
- * releases with cudaFreeAsync on the same stream (stream-ordered, no
- * synchronisation).
+ *
+ * Scheduling (FlashAttention-4: Blackwell Attention Kernel Co-Design, "LPT
+ * scheduling for imbalanced grids": variable-length batches are ordered by
+ * work, longest first; FlashAttention from Scratch, sec. 11.5 on the tail of a
+ * persistent grid): every CTA of the launch reads the offsets, sorts the
+ * sequences by key length, longest first, and builds the tile list in its
+ * own shared memory.  The call allocates no memory and needs no workspace.
+ * A launch schedules at most FA_VARLEN_SEQS_PER_LAUNCH sequences (64 for
+ * the (192, 128) head dimensions of fa_fwd_varlen_hdim); a larger batch is
+ * processed by consecutive launches of that many sequences each, on
+ * `stream`, each ordered longest first within itself.
  */
+#define FA_VARLEN_SEQS_PER_LAUNCH 1536
 fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse,
                           const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
                           int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
@@ -99,18 +107,22 @@ fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, float* o,
                           cudaStream_t stream);
 
 /*
- * Allocation-free variant of fa_fwd_varlen (no counterpart on the pages: it
- * changes where the schedule lives, not what is computed).
+ * Variant of fa_fwd_varlen whose schedule lives in a fixed device array
+ * (no counterpart on the pages: it changes where the schedule lives, not what
+ * is computed).
  *
- * fa_fwd_varlen obtains a small schedule buffer with cudaMallocAsync on every
- * call.  Some callers cannot allow that: code being captured into a CUDA
- * graph where memory-pool calls are unwanted, processes that hand all device
- * memory to their own allocator up front, or runtimes that must not allocate
- * on the hot path.  This entry point takes the same arguments and gives the
- * same results, but keeps the schedule in a fixed array compiled into the
- * library (about 192 KiB, resident on every device that loads the library
- * until the process exits).  It calls no cudaMalloc, cudaFree or other
- * allocating routine.
+ * It is meant for callers that cannot call cudaMalloc on the hot path:
+ * processes that hand all device memory to their own allocator up front,
+ * runtimes that must not allocate while serving, or code that must not touch
+ * a memory pool.  fa_fwd_varlen allocates nothing either, but builds its
+ * schedule per CTA in shared memory and so splits batches of more than
+ * FA_VARLEN_SEQS_PER_LAUNCH sequences into several launches.  This entry
+ * point sorts the whole batch (up to FA_NOALLOC_MAX_SEQS sequences) once,
+ * with a schedule kernel, into an array compiled into the library (about
+ * 192 KiB, resident on every device that loads the library until the process
+ * exits), and runs one attention launch over it.  Same arguments and results
+ * as fa_fwd_varlen for D = 64 or 128; it calls no cudaMalloc, cudaFree or
+ * other allocating routine.
  *
  *  - num_seqs may be at most FA_NOALLOC_MAX_SEQS; larger batches return
  *    FA_ERR_INVALID_ARG before any device work.

@@ -7,6 +7,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 import exact_attention_07_gb300 as fa
 
@@ -81,6 +82,58 @@ def test_varlen_argument_validation(lib):
     assert call(cu_k=34) == INV                      # int32 offsets must be 4-byte aligned
     assert call(scale=-1.0) == INV
     assert call(D=80) == UNS
+
+
+def test_noalloc_argument_validation(lib):
+    INV, UNS = fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED
+
+    def call(q=16, cu_q=32, n=2, tq=10, tk=10, Hq=2, Hkv=2, D=128):
+        return lib.fa_fwd_varlen_noalloc(q, 16, 16, 16, 16, cu_q, 32, n, tq, tk, 8, 8, Hq, Hkv, D, 1,
+                                         ctypes.c_float(0.1), None)
+
+    assert call(q=None) == INV
+    assert call(cu_q=None) == INV
+    assert call(n=0) == INV
+    assert call(Hq=4, Hkv=3) == INV
+    assert call(D=80) == UNS
+    assert call(D=192) == UNS  # (192, 128) needs fa_fwd_varlen_hdim
+    n = fa.NOALLOC_MAX_SEQS + 1
+    assert call(n=n, tq=n, tk=n) == INV  # beyond the fixed array, rejected before any device work
+    assert lib.fa_last_launch_count() == 0
+
+
+def _packed_cpu(Tq=10, Tk=12, Hq=2, Hkv=1, D=64, n=2):
+    bf, f32 = torch.bfloat16, torch.float32
+    return dict(q=torch.zeros(Tq, Hq, D, dtype=bf), k=torch.zeros(Tk, Hkv, D, dtype=bf),
+                v=torch.zeros(Tk, Hkv, D, dtype=bf), cu_seqlens_q=torch.zeros(n + 1, dtype=torch.int32),
+                cu_seqlens_k=torch.zeros(n + 1, dtype=torch.int32), out=torch.zeros(Tq, Hq, D, dtype=f32),
+                lse=torch.zeros(Hq, Tq, dtype=f32))
+
+
+@pytest.mark.parametrize("entry", ["fa_fwd_varlen", "fa_fwd_varlen_noalloc"])
+def test_packed_wrappers_check_every_shape_before_the_device(entry):
+    """A wrong-shaped buffer is rejected with ValueError before the library is
+    touched (CPU tensors: the shape checks come before the device check)."""
+    fn = getattr(fa, entry)
+
+    def call(**over):
+        a = _packed_cpu()
+        a.update(over)
+        return fn(a["q"], a["k"], a["v"], a["cu_seqlens_q"], a["cu_seqlens_k"], 8, 8, out=a["out"], lse=a["lse"])
+
+    f32, bf = torch.float32, torch.bfloat16
+    with pytest.raises(ValueError, match="out must be"):
+        call(out=torch.zeros(9, 2, 64, dtype=f32))              # undersized O
+    with pytest.raises(ValueError, match="out must be"):
+        call(lse=torch.zeros(2, 9, dtype=f32))                  # undersized LSE
+    with pytest.raises(ValueError, match="shape mismatch"):
+        call(v=torch.zeros(11, 1, 64, dtype=bf))                # V shorter than K
+    with pytest.raises(ValueError, match="shape mismatch"):
+        call(k=torch.zeros(12, 1, 128, dtype=bf), v=torch.zeros(12, 1, 128, dtype=bf))  # Dk != D
+    with pytest.raises(ValueError, match="offsets"):
+        call(cu_seqlens_k=torch.zeros(2, dtype=torch.int32))    # fewer key offsets
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        call()                                                  # right shapes, host memory
 
 
 def test_splitkv_argument_validation(lib):

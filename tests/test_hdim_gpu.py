@@ -96,6 +96,29 @@ def test_hdim_varlen_full_compare(causal):
             f"hdim varlen causal={causal}")
 
 
+def test_hdim_varlen_split_across_launches():
+    """(192, 128) launches schedule at most 64 sequences each: 150 sequences
+    take three launches, every row compared in full."""
+    rng = np.random.default_rng(192)
+    n = 150
+    lq = rng.integers(0, 300, n).tolist()
+    lk = [x + int(rng.integers(0, 50)) for x in lq]
+    Hq, Hkv = 2, 1
+    Tq, Tk = sum(lq), sum(lk)
+    q, k, v = random_inputs((Tq, Hq, D), (Tk, Hkv, D), seed=9, shape_v=(Tk, Hkv, DV))
+    cq = torch.tensor([0] + np.cumsum(lq).tolist(), dtype=torch.int32)
+    ck = torch.tensor([0] + np.cumsum(lk).tolist(), dtype=torch.int32)
+    o = torch.full((Tq, Hq, DV), float("nan"), dtype=torch.float32, device=DEV)
+    lse = torch.full((Hq, Tq), 12345.0, dtype=torch.float32, device=DEV)
+    fa.fa_fwd_varlen_hdim(q.to(DEV), k.to(DEV), v.to(DEV), cq.to(DEV), ck.to(DEV), max(lq), max(lk),
+                          causal=True, out=o, lse=lse)
+    assert fa.fa_last_launch_count() == 3
+    fa.fa_check()
+    ref_o, ref_lse = oracle.attention_varlen(q, k, v, cq.numpy(), ck.numpy(), scale=1 / math.sqrt(D), causal=True)
+    compare(o.cpu().numpy().transpose(1, 0, 2), lse.cpu().numpy(), ref_o.transpose(1, 0, 2), ref_lse,
+            "hdim varlen split")
+
+
 def test_hdim_unsupported_pairs_raise():
     q, k, _ = random_inputs((1, 2, 64, 192), (1, 2, 64, 192), seed=1)
     v = torch.zeros((1, 2, 64, 192), dtype=torch.bfloat16)

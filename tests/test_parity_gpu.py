@@ -134,6 +134,66 @@ def test_varlen_small_full_compare(lq, lk, Hq, Hkv, D, causal):
     compare(o.transpose(1, 0, 2), lse, ref_o.transpose(1, 0, 2), ref_lse, f"varlen {lq} {lk}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_varlen_batch_split_across_launches(D):
+    """More sequences than one launch schedules: consecutive launches of
+    FA_VARLEN_SEQS_PER_LAUNCH sequences, every row still compared in full."""
+    rng = np.random.default_rng(100 + D)
+    n = fa.VARLEN_SEQS_PER_LAUNCH + 70
+    lq = rng.integers(0, 40, n).tolist()
+    lk = [x + int(rng.integers(0, 9)) for x in lq]
+    q, k, v, cq, ck, o, lse = run_varlen(lq, lk, 2, 1, D, True, seed=D)
+    assert fa.fa_last_launch_count() == 2
+    ref_o, ref_lse = oracle.attention_varlen(q, k, v, cq.numpy(), ck.numpy(), scale=1 / math.sqrt(D), causal=True)
+    compare(o.transpose(1, 0, 2), lse, ref_o.transpose(1, 0, 2), ref_lse, f"varlen split D={D}")
+
+
+_CU_MEMPOOL_ATTR_USED_MEM_HIGH = 8  # CUmemPool_attribute in cuda.h
+
+
+def _default_pool_high(reset: bool) -> int:
+    """High-water mark of the current device's stream-ordered memory pool
+    (what cudaMallocAsync draws from), read through the driver API."""
+    import ctypes
+    cu = ctypes.CDLL("libcuda.so.1")
+    dev = ctypes.c_int()
+    assert cu.cuCtxGetDevice(ctypes.byref(dev)) == 0
+    pool = ctypes.c_void_p()
+    assert cu.cuDeviceGetDefaultMemPool(ctypes.byref(pool), dev) == 0
+    val = ctypes.c_uint64(0)
+    if reset:
+        assert cu.cuMemPoolSetAttribute(pool, _CU_MEMPOOL_ATTR_USED_MEM_HIGH, ctypes.byref(val)) == 0
+    assert cu.cuMemPoolGetAttribute(pool, _CU_MEMPOOL_ATTR_USED_MEM_HIGH, ctypes.byref(val)) == 0
+    return int(val.value)
+
+
+def test_varlen_allocates_no_device_memory():
+    """fa_fwd_varlen obtains no device memory per call: the stream-ordered pool
+    stays unused, torch's allocator serves no request, and the device's free
+    memory is the same before and after the calls."""
+    lens = [300, 1, 777, 128, 64, 2000]
+    Hq, Hkv, D = 4, 2, 128
+    T = sum(lens)
+    q, k, v = (x.to(DEV) for x in random_inputs((T, Hq, D), (T, Hkv, D), seed=17))
+    cu = torch.tensor([0] + np.cumsum(lens).tolist(), dtype=torch.int32, device=DEV)
+    o = torch.empty((T, Hq, D), dtype=torch.float32, device=DEV)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=DEV)
+    fa.fa_fwd_varlen(q, k, v, cu, cu, max(lens), max(lens), causal=True, out=o, lse=lse)  # loads the kernels
+    torch.cuda.synchronize()
+    fa.fa_check()
+    assert _default_pool_high(reset=True) == 0
+    allocs = torch.cuda.memory_stats()["allocation.all.allocated"]
+    free0, _ = torch.cuda.mem_get_info()
+    for causal in (True, False, True):
+        fa.fa_fwd_varlen(q, k, v, cu, cu, max(lens), max(lens), causal=causal, out=o, lse=lse)
+    torch.cuda.synchronize()
+    fa.fa_check()
+    assert _default_pool_high(reset=False) == 0, "a stream-ordered allocation was made"
+    assert torch.cuda.memory_stats()["allocation.all.allocated"] == allocs
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+
+
 def test_varlen_invalid_offsets_latch_error():
     Hq, D = 2, 64
     q, k, v = random_inputs((300, Hq, D), (300, Hq, D), seed=3)

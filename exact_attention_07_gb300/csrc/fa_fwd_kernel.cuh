@@ -74,7 +74,8 @@ struct FwdSmem {
     static constexpr int kTFull = 4 + 2 * kStages, kTEmpty = kTFull + kTailStages;
     static constexpr int kSFull = kTFull + 2 * kTailStages, kPFull = kSFull + 2, kOFull = kSFull + 4,
                          kOEmpty = kSFull + 6, kStFull = kSFull + 8, kStEmpty = kSFull + 10,
-                         kDrain = kSFull + 12, kNumBars = kSFull + 13;
+                         kDrain = kSFull + 12, kSEmpty = kSFull + 13, kPEmpty = kSFull + 15,
+                         kNumBars = kSFull + 17;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;      // tmem base, abort flag
     static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;  // float2 [2][128]
     // epilogue staging: per epilogue warp one 32 x 32 fp32 block, rows padded
@@ -91,7 +92,15 @@ struct FwdSmem {
     static constexpr int kAlloc = kBytes + 1024 <= kMaxDynamic ? kBytes + 1024 : kMaxDynamic;
     static_assert(kBytes <= kMaxDynamic, "shared-memory layout exceeds the per-CTA limit");
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS = 0, kColO = 256;
+    // P in tensor-memory columns of its own (head dimension 64, bf16 inputs):
+    // S_t [128 t, 128 t + 128), P_t [256 + 64 t, ...), O_t [384 + 64 t, ...).
+    // The MMA warp can then compute S_t(j+1) as soon as the softmax has read
+    // S_t(j), while that softmax is still turning it into P_t(j).  Elsewhere P_t
+    // overwrites the first half of S_t and O_t sits at 256 + DV t.
+    static constexpr bool kSplitP = D == 64 && DV == 64 && !kFp8;
+    static constexpr uint32_t kColS = 0, kColP = kSplitP ? 256 : 0, kColO = kSplitP ? 384 : 256;
+    static constexpr uint32_t kPStride = kSplitP ? 64 : kBlockN;  // columns between P_0 and P_1
+    static_assert(kColO + 2 * DV <= kTmemCols, "tensor-memory layout");
 };
 
 // Schedule of a packed batch built by the CTA itself (launches without a
@@ -492,7 +501,7 @@ __device__ __forceinline__ void mma_pv(uint32_t tmem, uint32_t sb, int t, int vs
     } else {
         constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, DV, true);
         const uint64_t vd = smem_desc_sw128(sb + L::kKVOff + (uint32_t)(vs * L::kTileBytes), L::kBlk, 1024);
-        const uint32_t pa = tmem + L::kColS + (uint32_t)(t * kBlockN);
+        const uint32_t pa = tmem + L::kColP + (uint32_t)t * L::kPStride;
         if (leader) {
 #pragma unroll
             for (int kk = 0; kk < kBlockN / 16; ++kk)
@@ -562,16 +571,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::kOEmpty + t), kBlockM);
             mbar_init(bar(L::kStFull + t), kBlockM);
             mbar_init(bar(L::kStEmpty + t), kBlockM);
+            mbar_init(bar(L::kSEmpty + t), kBlockM);
+            mbar_init(bar(L::kPEmpty + t), 1);
         }
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(bar(L::kKVFull + s), 1);
-            mbar_init(bar(L::kKVEmpty + s), 1);
+            mbar_init(bar(L::kKVEmpty + s), L::kSplitP ? 2 : 1);  // split P: one arrival per Q tile
         }
         for (int s = 0; s < L::kTailStages; ++s) {
             mbar_init(bar(L::kTFull + s), 1);
             mbar_init(bar(L::kTEmpty + s), 1);
         }
-        mbar_init(bar(L::kDrain), 1);
+        mbar_init(bar(L::kDrain), L::kSplitP ? 2 : 1);  // split P: both MMA warps
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -609,9 +620,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = threadIdx.x & 127;   // query row within the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t tS = tmem + lane_base + L::kColS + (uint32_t)(t * kBlockN);
+        const uint32_t tP = tmem + lane_base + L::kColP + (uint32_t)t * L::kPStride;
         const uint32_t tO = tmem + lane_base + L::kColO + (uint32_t)(t * DV);
         const float sl2 = p.scale_log2;
         uint32_t s_ph = 0, st_ph = 1;
+        uint32_t pe_ph = 0;      // split P: phase of the P.V-done barrier
+        bool p_written = false;  // split P: a P of this group is in tensor memory
         // K/V ring slots taken before the current work tile (K(0), V(0), K(1), ...)
         uint32_t kv_seq = 0;
         // The first thread of the tile-1 group frees the K/V stages (a commit
@@ -622,7 +636,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ring (D > DV) cannot wait that long for V(j-1), and with e4m3 operands
         // the softmax, not the MMA warp, bounds the step: in both the MMA warp
         // commits every release as soon as the MMAs reading the stage are issued.
-        const bool kv_releaser = kSoftmaxFreesKV && t == 1 && row == 0;
+        // With P in columns of its own the next S is issued before this step's
+        // P.V, so V(j-1) is freed only once P1(j-1).V(j-1) has completed (the
+        // group waits for that before it overwrites P1).
+        // With P in columns of its own each Q tile has its own MMA warp, so each
+        // group's first thread frees its share (the barriers count two arrivals):
+        // K(j) once S_t(j) has completed, V(j-1) once P_t(j-1).V(j-1) has.
+        const bool kv_releaser = kSoftmaxFreesKV && (L::kSplitP || t == 1) && row == 0;
         for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
             const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, sb + SS::kOff, tile);
             if (w.nk == 0) continue;
@@ -655,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_ph ^= 1;
                 if (kv_releaser) {
                     mbar_arrive(bar(L::kKVEmpty + (int)((kv_seq + 2u * (uint32_t)j) % (uint32_t)L::kStages)));
-                    if (j > 0)
+                    if (!L::kSplitP && j > 0)
                         mbar_arrive(bar(L::kKVEmpty + (int)((kv_seq + 2u * (uint32_t)j - 1u) % (uint32_t)L::kStages)));
                 }
                 tc_fence_after_sync();
@@ -672,6 +692,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld32(tS + 32u * c, sv[c]);
                 }
                 tmem_wait_ld();
+                if constexpr (L::kSplitP) {
+                    // S is in registers: its columns may take the next S
+                    tc_fence_before_sync();
+                    mbar_arrive(bar(L::kSEmpty + t));
+                }
                 const int key0 = (j + w.kf) * kBlockN;
                 if constexpr (VAR == kVarFp8) smul = smul_q * __ldg(fp8_sk + j);
                 // score modifiers (FlashAttention from Scratch, sec. 12), in log2 units
@@ -783,8 +808,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             st_shared_v4(prow + (uint32_t)(((4 * c + u) ^ (row & 7)) << 4), pk[4 * u], pk[4 * u + 1],
                                          pk[4 * u + 2], pk[4 * u + 3]);
                     } else {
-                        // P (bf16 pairs) over the first 64 columns of S
-                        tmem_st32(tS + 32u * c, pk);
+                        if constexpr (L::kSplitP) {
+                            if (c == 0) {
+                                // the last P.V of this group has read P (and, for the
+                                // tile-1 group, V(j-1)) and left O idle
+                                if (p_written) {
+                                    if (!warp_wait(bar(L::kPEmpty + t), pe_ph, abort_flag, wf, 27 + t, tile)) goto done;
+                                    pe_ph ^= 1;
+                                    tc_fence_after_sync();
+                                    if (kv_releaser && j > 0)
+                                        mbar_arrive(bar(L::kKVEmpty +
+                                                        (int)((kv_seq + 2u * (uint32_t)j - 1u) % (uint32_t)L::kStages)));
+                                }
+                                p_written = true;
+                            }
+                            tmem_st32(tP + 32u * c, pk);
+                        } else {
+                            // P (bf16 pairs) over the first 64 columns of S
+                            tmem_st32(tS + 32u * c, pk);
+                        }
                     }
                 }
                 if constexpr (VAR == kVarFp8) fence_proxy_async_shared();  // P visible to the tensor core
@@ -802,7 +844,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // correction of the accumulator when the reference moved (O is idle
-                // here: the previous P.V completed before this S was committed)
+                // here: the previous P.V completed before this S was committed, or,
+                // with P in columns of its own, before the wait above returned)
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                     for (int c = 0; c < DV / 32; ++c) {
@@ -1026,7 +1069,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (t_armed[s] >= 0) mbar_settle(bar(L::kTFull + s), (uint32_t)t_armed[s], wf, 26);
             }
             __syncwarp();
-        } else if (warp == 13) {
+        } else if (warp == 13 || (L::kSplitP && warp == 14)) {
             // ============================================================ MMA issuer
             // The whole warp runs this loop; lane 0 issues every MMA and commit (a
             // commit tracks the MMAs of the thread that executes it).
@@ -1062,96 +1105,164 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto release_tail = [&](int ts) {
                 if constexpr (L::kTail) commit(L::kTEmpty + ts);
             };
-            for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
-                const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, sb + SS::kOff, tile);
-                if (w.nk == 0) continue;
-                const int nk = w.nk;
-                // prologue: S0(0), S1(0)
-                if (!warp_wait(bar(L::kQFull + 0), q_ph[0], abort_flag, wf, 15, tile)) break;
-                q_ph[0] ^= 1;
-                const int ks = stage;
-                if (!warp_wait(bar(L::kKVFull + ks), kv_ph, abort_flag, wf, 17, tile)) break;
-                next_stage();
-                int ts;
-                if (!take_tail(tile, ts)) break;
-                tc_fence_after_sync();
-                mma_qk<D, VAR, DV>(tm, sb, 0, ks, ts, leader);
-                issued = true;
-                commit(L::kSFull + 0);
-                if (nk == 1) commit(L::kQEmpty + 0);
-                if (!warp_wait(bar(L::kQFull + 1), q_ph[1], abort_flag, wf, 16, tile)) break;
-                q_ph[1] ^= 1;
-                tc_fence_after_sync();
-                mma_qk<D, VAR, DV>(tm, sb, 1, ks, ts, leader);
-                commit(L::kSFull + 1);
-                if constexpr (!kSoftmaxFreesKV) commit(L::kKVEmpty + ks);
-                release_tail(ts);
-                if (nk == 1) commit(L::kQEmpty + 1);
-                bool ok = true;
-                for (int j = 0; j < nk && ok; ++j) {
-                    // V(j), K(j+1) and P0(j): in the steady state all three have
-                    // completed when the warp gets here, and one combined test costs one
-                    // shared-memory round trip; otherwise they are awaited one by one
-                    const int vs = stage;
-                    const uint32_t vph = kv_ph;
-                    next_stage();
-                    int kn = -1, tn = 0;
-                    uint32_t kph = vph;
-                    if (j + 1 < nk) {
-                        kn = stage;
-                        kph = kv_ph;
-                        next_stage();
+            if constexpr (L::kSplitP) {
+                // P in columns of its own, one MMA warp per Q tile (warp 13: tile 0,
+                // warp 14: tile 1; the tensor pipe interleaves their MMAs).  Per KV
+                // step j the warp issues S_t(j+1) as soon as its softmax group has
+                // read S_t(j) (and K(j+1) has landed), then P_t(j).V(j) when P
+                // arrives, so the group's next scores are ready while it is still on
+                // the exponentials, and neither group waits for the other's MMAs.
+                // Ring slots are numbered from the start of the launch: K(j) of a
+                // work tile is kv_base + 2j, V(j) kv_base + 2j + 1.
+                const int t = warp - 13;
+                uint32_t se_ph = 0;
+                uint32_t kv_base = 0;
+                bool s_any = false;  // an S has been issued (later ones wait for the softmax to read it)
+                auto slot_wait = [&](uint32_t slot, int site, int tile) -> bool {
+                    return warp_wait(bar(L::kKVFull + (int)(slot % (uint32_t)L::kStages)),
+                                     (slot / (uint32_t)L::kStages) & 1u, abort_flag, wf, site, tile);
+                };
+                // S_t into its columns from K in ring slot kslot
+                auto issue_s = [&](uint32_t kslot, int tile) -> bool {
+                    if (s_any) {
+                        if (!warp_wait(bar(L::kSEmpty + t), se_ph, abort_flag, wf, 29 + t, tile)) return false;
+                        se_ph ^= 1;
                     }
-                    const bool all3 = j > 0 &&
-                        __all_sync(0xffffffffu, mbar_try_wait3(bar(L::kKVFull + vs), vph,
-                                                               bar(L::kKVFull + (kn >= 0 ? kn : vs)), kph,
-                                                               bar(L::kPFull + 0), p_ph[0]));
-                    if (!all3) {
-                        if (!(ok = warp_wait(bar(L::kKVFull + vs), vph, abort_flag, wf, 18, tile))) break;
-                        if (kn >= 0 && !(ok = warp_wait(bar(L::kKVFull + kn), kph, abort_flag, wf, 17, tile))) break;
-                    }
-                    if (kn >= 0 && !(ok = take_tail(tile, tn))) break;
-                    // tile 0: P0(j) . V(j), then S0(j+1)
-                    if (j == 0) {
-                        if (!(ok = warp_wait(bar(L::kOEmpty + 0), oe_ph[0], abort_flag, wf, 19, tile))) break;
-                        oe_ph[0] ^= 1;
-                    }
-                    if (!all3 && !(ok = warp_wait(bar(L::kPFull + 0), p_ph[0], abort_flag, wf, 21, tile))) break;
-                    p_ph[0] ^= 1;
+                    s_any = true;
                     tc_fence_after_sync();
-                    mma_pv<D, VAR, DV>(tm, sb, 0, vs, j > 0, leader);
-                    if (kn >= 0) {
-                        mma_qk<D, VAR, DV>(tm, sb, 0, kn, tn, leader);
-                        commit(L::kSFull + 0);
-                        if (j + 2 == nk) commit(L::kQEmpty + 0);
-                    } else {
-                        commit(L::kOFull + 0);
+                    mma_qk<D, VAR, DV>(tm, sb, t, (int)(kslot % (uint32_t)L::kStages), 0, leader);
+                    issued = true;
+                    commit(L::kSFull + t);
+                    return true;
+                };
+                for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
+                    const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, sb + SS::kOff, tile);
+                    if (w.nk == 0) continue;
+                    const int nk = w.nk;
+                    bool ok = warp_wait(bar(L::kQFull + t), q_ph[t], abort_flag, wf, 15 + t, tile) &&
+                              slot_wait(kv_base, 17, tile) && issue_s(kv_base, tile);
+                    q_ph[t] ^= 1;
+                    if (ok && nk == 1) commit(L::kQEmpty + t);
+                    for (int j = 0; j < nk && ok; ++j) {
+                        const bool last = j + 1 == nk;
+                        if (!last) {
+                            const uint32_t ks = kv_base + 2u * (uint32_t)(j + 1);
+                            if (!(ok = slot_wait(ks, 17, tile) && issue_s(ks, tile))) break;
+                            if (j + 2 == nk) commit(L::kQEmpty + t);
+                        }
+                        const uint32_t vslot = kv_base + 2u * (uint32_t)j + 1u;
+                        if (!(ok = slot_wait(vslot, 18, tile))) break;
+                        if (j == 0) {
+                            if (!(ok = warp_wait(bar(L::kOEmpty + t), oe_ph[t], abort_flag, wf, 19 + t, tile))) break;
+                            oe_ph[t] ^= 1;
+                        }
+                        if (!(ok = warp_wait(bar(L::kPFull + t), p_ph[t], abort_flag, wf, 21 + t, tile))) break;
+                        p_ph[t] ^= 1;
+                        tc_fence_after_sync();
+                        const int vs = (int)(vslot % (uint32_t)L::kStages);
+                        mma_pv<D, VAR, DV>(tm, sb, t, vs, j > 0, leader);
+                        commit(L::kPEmpty + t);
+                        if (last) {
+                            commit(L::kOFull + t);
+                            commit(L::kKVEmpty + vs);  // this tile's share of the last V
+                        }
                     }
-                    // tile 1: P1(j) . V(j), then S1(j+1)
-                    if (j == 0) {
-                        if (!(ok = warp_wait(bar(L::kOEmpty + 1), oe_ph[1], abort_flag, wf, 20, tile))) break;
-                        oe_ph[1] ^= 1;
-                    }
-                    if (!(ok = warp_wait(bar(L::kPFull + 1), p_ph[1], abort_flag, wf, 22, tile))) break;
-                    p_ph[1] ^= 1;
-                    tc_fence_after_sync();
-                    mma_pv<D, VAR, DV>(tm, sb, 1, vs, j > 0, leader);
-                    if constexpr (!kSoftmaxFreesKV) commit(L::kKVEmpty + vs);
-                    if (kn >= 0) {
-                        mma_qk<D, VAR, DV>(tm, sb, 1, kn, tn, leader);
-                        commit(L::kSFull + 1);
-                        if constexpr (!kSoftmaxFreesKV) commit(L::kKVEmpty + kn);
-                        release_tail(tn);
-                        if (j + 2 == nk) commit(L::kQEmpty + 1);
-                    } else {
-                        commit(L::kOFull + 1);
-                        if constexpr (kSoftmaxFreesKV) commit(L::kKVEmpty + vs);  // the work tile's last V
-                    }
+                    if (!ok) break;
+                    kv_base += 2u * (uint32_t)nk;
                 }
-                if (!ok) break;
+            } else {
+                for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
+                    const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, sb + SS::kOff, tile);
+                    if (w.nk == 0) continue;
+                    const int nk = w.nk;
+                    // prologue: S0(0), S1(0)
+                    if (!warp_wait(bar(L::kQFull + 0), q_ph[0], abort_flag, wf, 15, tile)) break;
+                    q_ph[0] ^= 1;
+                    const int ks = stage;
+                    if (!warp_wait(bar(L::kKVFull + ks), kv_ph, abort_flag, wf, 17, tile)) break;
+                    next_stage();
+                    int ts;
+                    if (!take_tail(tile, ts)) break;
+                    tc_fence_after_sync();
+                    mma_qk<D, VAR, DV>(tm, sb, 0, ks, ts, leader);
+                    issued = true;
+                    commit(L::kSFull + 0);
+                    if (nk == 1) commit(L::kQEmpty + 0);
+                    if (!warp_wait(bar(L::kQFull + 1), q_ph[1], abort_flag, wf, 16, tile)) break;
+                    q_ph[1] ^= 1;
+                    tc_fence_after_sync();
+                    mma_qk<D, VAR, DV>(tm, sb, 1, ks, ts, leader);
+                    commit(L::kSFull + 1);
+                    if constexpr (!kSoftmaxFreesKV) commit(L::kKVEmpty + ks);
+                    release_tail(ts);
+                    if (nk == 1) commit(L::kQEmpty + 1);
+                    bool ok = true;
+                    for (int j = 0; j < nk && ok; ++j) {
+                        // V(j), K(j+1) and P0(j): in the steady state all three have
+                        // completed when the warp gets here, and one combined test costs one
+                        // shared-memory round trip; otherwise they are awaited one by one
+                        const int vs = stage;
+                        const uint32_t vph = kv_ph;
+                        next_stage();
+                        int kn = -1, tn = 0;
+                        uint32_t kph = vph;
+                        if (j + 1 < nk) {
+                            kn = stage;
+                            kph = kv_ph;
+                            next_stage();
+                        }
+                        const bool all3 = j > 0 &&
+                            __all_sync(0xffffffffu, mbar_try_wait3(bar(L::kKVFull + vs), vph,
+                                                                   bar(L::kKVFull + (kn >= 0 ? kn : vs)), kph,
+                                                                   bar(L::kPFull + 0), p_ph[0]));
+                        if (!all3) {
+                            if (!(ok = warp_wait(bar(L::kKVFull + vs), vph, abort_flag, wf, 18, tile))) break;
+                            if (kn >= 0 && !(ok = warp_wait(bar(L::kKVFull + kn), kph, abort_flag, wf, 17, tile))) break;
+                        }
+                        if (kn >= 0 && !(ok = take_tail(tile, tn))) break;
+                        // tile 0: P0(j) . V(j), then S0(j+1)
+                        if (j == 0) {
+                            if (!(ok = warp_wait(bar(L::kOEmpty + 0), oe_ph[0], abort_flag, wf, 19, tile))) break;
+                            oe_ph[0] ^= 1;
+                        }
+                        if (!all3 && !(ok = warp_wait(bar(L::kPFull + 0), p_ph[0], abort_flag, wf, 21, tile))) break;
+                        p_ph[0] ^= 1;
+                        tc_fence_after_sync();
+                        mma_pv<D, VAR, DV>(tm, sb, 0, vs, j > 0, leader);
+                        if (kn >= 0) {
+                            mma_qk<D, VAR, DV>(tm, sb, 0, kn, tn, leader);
+                            commit(L::kSFull + 0);
+                            if (j + 2 == nk) commit(L::kQEmpty + 0);
+                        } else {
+                            commit(L::kOFull + 0);
+                        }
+                        // tile 1: P1(j) . V(j), then S1(j+1)
+                        if (j == 0) {
+                            if (!(ok = warp_wait(bar(L::kOEmpty + 1), oe_ph[1], abort_flag, wf, 20, tile))) break;
+                            oe_ph[1] ^= 1;
+                        }
+                        if (!(ok = warp_wait(bar(L::kPFull + 1), p_ph[1], abort_flag, wf, 22, tile))) break;
+                        p_ph[1] ^= 1;
+                        tc_fence_after_sync();
+                        mma_pv<D, VAR, DV>(tm, sb, 1, vs, j > 0, leader);
+                        if constexpr (!kSoftmaxFreesKV) commit(L::kKVEmpty + vs);
+                        if (kn >= 0) {
+                            mma_qk<D, VAR, DV>(tm, sb, 1, kn, tn, leader);
+                            commit(L::kSFull + 1);
+                            if constexpr (!kSoftmaxFreesKV) commit(L::kKVEmpty + kn);
+                            release_tail(tn);
+                            if (j + 2 == nk) commit(L::kQEmpty + 1);
+                        } else {
+                            commit(L::kOFull + 1);
+                            if constexpr (kSoftmaxFreesKV) commit(L::kKVEmpty + vs);  // the work tile's last V
+                        }
+                    }
+                    if (!ok) break;
+                }
             }
-            // every MMA this warp issued has completed before TMEM is released
-            if (issued) {
+            // every MMA this warp issued has completed before TMEM is released (with
+            // split P the drain counts one commit from each MMA warp)
+            if (issued || L::kSplitP) {
                 commit(L::kDrain);
                 mbar_settle(bar(L::kDrain), 0, wf, 23);
             }

@@ -50,7 +50,18 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--full-oracle", action="store_true",
+                    help="reference arm: time the oracle over the whole workload (every output row) per step")
+    ap.add_argument("--sustained-seconds", type=float, default=2.0,
+                    help="length of the extra back-to-back pass reported as 'sustained' (0 = none)")
     return ap.parse_args(argv)
+
+
+def workload_config(w, world: int) -> dict:
+    """The `config` object of a bench line; both arms print the same one."""
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk, "D": w.D, "Dv": w.Dv,
+            "causal": w.causal, "flops_per_step": w.flops(),
+            "parallelism": f"replicas{world}" if world > 1 else "single"}
 
 
 def dist_env():
@@ -200,11 +211,12 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def cpu_oracle_rate(w, inputs, seconds: float, rng_seed: int = 0):
-    """Time the fp64 oracle on sampled output rows for about `seconds`.
+def cpu_oracle_rate(w, inputs, seconds: float, rng_seed: int = 0, full: bool = False):
+    """Time the fp64 oracle on sampled output rows for about `seconds` (or,
+    with `full`, on every output row of the workload).
 
-    Returns (TFLOP/s, threads, description).  FLOPs per row follow the metric
-    (4*Lk*D, halved on average when causal).
+    Returns (TFLOP/s, threads, description, timed seconds).  FLOPs per row
+    follow the metric (4*Lk*D, halved on average when causal).
     """
     import numpy as np
 
@@ -214,6 +226,17 @@ def cpu_oracle_rate(w, inputs, seconds: float, rng_seed: int = 0):
         return _cpu_backward_rate(w, inputs, seconds)
     if w.window is not None:
         return _cpu_variant_rate(w, inputs, seconds)
+    if full:
+        if w.varlen:
+            q, k, v, cq, ck = inputs
+            t0 = time.perf_counter()
+            oracle.attention_varlen(q, k, v, cq.numpy(), ck.numpy(), scale=w.scale, causal=w.causal)
+        else:
+            q, k, v = inputs
+            t0 = time.perf_counter()
+            oracle.attention(q, k, v, scale=w.scale, causal=w.causal)
+        dt = time.perf_counter() - t0
+        return w.flops() / dt / 1e12, oracle.num_cpus(), f"the whole workload, every output row ({dt:.1f} s)", dt
     if w.varlen:
         q, k, v, cq, ck = inputs
         Tq = q.shape[0]
@@ -239,7 +262,7 @@ def cpu_oracle_rate(w, inputs, seconds: float, rng_seed: int = 0):
     t0 = time.perf_counter()
     run(rows)
     dt = time.perf_counter() - t0
-    return per_row * n / dt / 1e12, threads, f"{n} random output rows of {total_rows} ({dt:.1f} s)"
+    return per_row * n / dt / 1e12, threads, f"{n} random output rows of {total_rows} ({dt:.1f} s)", dt
 
 
 def _cpu_backward_rate(w, inputs, seconds: float):
@@ -277,7 +300,8 @@ def _cpu_backward_rate(w, inputs, seconds: float):
     dt, _ = run(n)
     n = int(min(Lq, max(n, n * seconds / max(dt, 1e-6))))
     dt, fl = run(n)
-    return fl / dt / 1e12, oracle.num_cpus(), f"backward of {what}the last {n} query rows of one head ({dt:.1f} s)"
+    return (fl / dt / 1e12, oracle.num_cpus(), f"backward of {what}the last {n} query rows of one head ({dt:.1f} s)",
+            dt)
 
 
 def _cpu_variant_rate(w, inputs, seconds: float):
@@ -302,7 +326,7 @@ def _cpu_variant_rate(w, inputs, seconds: float):
     dt, _ = run(n)
     n = int(min(w.Lq, max(1024, (n * seconds / max(dt, 1e-6)) // 1024 * 1024)))
     dt, fl = run(n)
-    return fl / dt / 1e12, oracle.num_cpus(), f"last {n} query rows of one head ({dt:.1f} s)"
+    return fl / dt / 1e12, oracle.num_cpus(), f"last {n} query rows of one head ({dt:.1f} s)", dt
 
 
 # ------------------------------------------------------------------ reference arm
@@ -314,19 +338,24 @@ def run_reference(args, w):
     import oracle
     from workloads import dense_inputs, varlen_inputs
     inputs = varlen_inputs(w) if w.varlen else dense_inputs(w)
+    # Each step times the oracle on a bounded sample of the workload (about
+    # 150 s over the whole run), or with --full-oracle on all of it.  The value
+    # is the sampled rate; ms_per_step is the time each step actually took.
     budget = 150.0 / max(1, args.steps + args.warmup)
-    rates = []
+    rates, secs = [], []
     for i in range(args.warmup + args.steps):
-        r, threads, desc = cpu_oracle_rate(w, inputs, budget, rng_seed=i)
+        r, threads, desc, dt = cpu_oracle_rate(w, inputs, budget, rng_seed=i, full=args.full_oracle)
         if i >= args.warmup:
             rates.append(r)
+            secs.append(dt)
     value = statistics.median(rates)
-    ms = w.flops() / (value * 1e12) * 1e3
+    ms = statistics.mean(secs) * 1e3
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk, "D": w.D,
-                       "Dv": w.Dv, "causal": w.causal},
+            "config": workload_config(w, world),
+            "sampled": not args.full_oracle,
+            "full_step_ms_at_this_rate": w.flops() / (value * 1e12) * 1e3,
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": f"per step: {desc}"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -516,6 +545,45 @@ def main(argv=None):
     value = rate / 1e12
     ms_per_step = secs_max / args.steps * 1e3
 
+    # ---- sustained: one more back-to-back pass of at least --sustained-seconds
+    # with its own clock record.  The timed loop above is short and runs at
+    # burst clocks; a pass of seconds settles under the power cap.
+    sustained = None
+    if args.sustained_seconds > 0:
+        n_sus = int(min(200000, max(args.steps, math.ceil(args.sustained_seconds / max(secs / args.steps, 1e-7)))))
+        sus_secs, done = 0.0, 0
+        barrier()
+        with ClockSampler(dev.index, os.path.join(out_dir, f"bench_clocks_sustained_rank{rank}.csv")) as sclk:
+            barrier()
+            while done < n_sus:
+                m = n_sus - done if flush_buf is None else min(1000, n_sus - done)
+                if flush_buf is None:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(m):
+                        step(o, lse)
+                    e1.record(stream)
+                    e1.synchronize()
+                    sus_secs += e0.elapsed_time(e1) / 1e3
+                else:  # the L2 flush between steps, as in the timed loop, outside the events
+                    evs2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                            for _ in range(m)]
+                    for e0, e1 in evs2:
+                        flush_buf.zero_()
+                        e0.record(stream)
+                        step(o, lse)
+                        e1.record(stream)
+                    evs2[-1][1].synchronize()
+                    sus_secs += sum(e0.elapsed_time(e1) for e0, e1 in evs2) / 1e3
+                done += m
+            barrier()
+        fa.fa_check()
+        sus_rate, sus_max = job_rate(sus_secs, flops_step * n_sus, world, dev)
+        sustained = {"value": sus_rate / 1e12, "unit": "TFLOP/s", "steps": n_sus, "seconds": sus_max,
+                     "ms_per_step": sus_max / n_sus * 1e3, "clocks": sclk.summary(),
+                     "note": "a second back-to-back pass of at least %.1f s after the timed loop"
+                             % args.sustained_seconds}
+
     # ---- end to end through the public API with host buffers (pinned)
     e2e = None
     if not args.no_e2e:
@@ -697,7 +765,7 @@ def main(argv=None):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, threads, desc = cpu_oracle_rate(w, host_inputs, args.cpu_seconds)
+        rate, threads, desc, _ = cpu_oracle_rate(w, host_inputs, args.cpu_seconds)
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
 
     if rank == 0:
@@ -705,9 +773,7 @@ def main(argv=None):
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "e4m3" if w.fp8 else "bf16", "data": "synthetic",
                 "step_ms": step_stats,
-                "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk,
-                           "D": w.D, "Dv": w.Dv, "causal": w.causal, "flops_per_step": flops_step,
-                           "parallelism": f"replicas{world}" if world > 1 else "single", "l2": l2_note},
+                "config": workload_config(w, world), "l2": l2_note, "sustained": sustained,
                 "frac_of_peak": value / world / peak,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps,

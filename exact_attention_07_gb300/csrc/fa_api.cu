@@ -26,10 +26,6 @@ __device__ int g_diag[4];
 namespace {
 
 constexpr int kMaxDevices = 64;
-// K/V bytes of one scheduling section: the whole L2.  Larger sections keep
-// the longest-first order global (what matters most for causal balance);
-// within a section, concurrently running CTAs walk the same few 256-row
-// blocks of every head, so their K/V stays L2-resident anyway.
 // K/V bytes per scheduling section of KV heads.  Work tiles of unequal
 // length (causal, key windows, packed batches) need the whole-L2 section so
 // that the longest-first order can balance them; equal tiles measured faster

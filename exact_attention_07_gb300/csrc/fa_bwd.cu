@@ -1008,7 +1008,7 @@ cudaError_t launch_bwd_kernel(const CUtensorMap& q, const CUtensorMap& k, const 
 {
     auto kern = fa_bwd_sm103_kernel<D, CAUSAL, VARLEN, VAR>;
     constexpr int kSmem = BwdSmem<D>::kDynamic;
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    const cudaError_t e = smem_limit_once<fa_bwd_sm103_kernel<D, CAUSAL, VARLEN, VAR>>(kSmem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kBwdThreads, kSmem, stream>>>(q, k, v, dout, dq, p);
     return cudaGetLastError();

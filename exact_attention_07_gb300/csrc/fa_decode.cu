@@ -511,8 +511,7 @@ struct DecKernel {
     static cudaError_t prepare()
     {
         static_assert(SMEM <= 232448, "shared memory of one CTA");
-        return cudaFuncSetAttribute(fa_decode_partial_kernel<D, RPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    SMEM);
+        return smem_limit_once<fa_decode_partial_kernel<D, RPT>>(SMEM);
     }
     static cudaError_t launch(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p, int grid,
                               cudaStream_t st)

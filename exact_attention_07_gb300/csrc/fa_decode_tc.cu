@@ -520,8 +520,7 @@ done:
 cudaError_t launch_decode_tc(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                              const DecodeParams& p, int grid, cudaStream_t stream)
 {
-    const cudaError_t e =
-        cudaFuncSetAttribute(fa_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kDynamic);
+    const cudaError_t e = smem_limit_once<fa_decode_tc_kernel>(TcSmem::kDynamic);
     if (e != cudaSuccess) return e;
     fa_decode_tc_kernel<<<grid, kTcThreads, TcSmem::kDynamic, stream>>>(q, k, v, p);
     return cudaGetLastError();

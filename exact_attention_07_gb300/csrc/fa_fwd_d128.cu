@@ -10,7 +10,7 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 {
     auto kern = fa_fwd_sm103_kernel<D, CAUSAL, VARLEN, VAR, DV>;
     constexpr int kSmem = fwd_smem_alloc<D, VARLEN, VAR, DV>();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = smem_limit_once<fa_fwd_sm103_kernel<D, CAUSAL, VARLEN, VAR, DV>>(kSmem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, kSmem, stream>>>(q, k, v, p);
     return cudaGetLastError();

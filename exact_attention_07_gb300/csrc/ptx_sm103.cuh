@@ -5,9 +5,31 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime_api.h>
+
+#include <atomic>
 #include <cstdint>
 
 namespace fa {
+
+// ------------------------------------------------------------------ host
+
+// Raises kernel Kern's dynamic shared-memory limit to `bytes` once per device
+// (the attribute belongs to the function on the current device), instead of
+// on every launch.
+template <auto Kern>
+inline cudaError_t smem_limit_once(int bytes)
+{
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // ------------------------------------------------------------------ misc
 

@@ -716,7 +716,7 @@ def main(argv=None):
                     "traffic": profiled_traffic(w.name, DECODE_SOURCES, "fa_decode"),
                     "peak_kind": f"{hbm_kind} HBM copy",
                     "algorithmic_bytes_per_step": w.hbm_bytes(), "splits": n_splits,
-                    "kernel": ("fa_decode_tc_kernel" if w.D == 128 and w.Hq // w.Hkv * w.Lq >= 2
+                    "kernel": ("fa_decode_tc_kernel<%d>" % w.D if w.Hq // w.Hkv * w.Lq >= 2
                                else "fa_decode_partial_kernel<%d,*>" % w.D) + " + fa_decode_merge_kernel<%d>" % w.D,
                     "timed": "whole step (both launches)"}
     elif w.fp8:

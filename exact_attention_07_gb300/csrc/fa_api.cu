@@ -602,7 +602,7 @@ fa_status_t splitkv_validate(int B, int Hq, int Hkv, int Lq, int Lk, int D)
 void splitkv_plan(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_splits, int num_sms, SplitPlan* pl)
 {
     pl->R = (Hq / Hkv) * Lq;
-    pl->tensor = D == 128 && pl->R >= 2;
+    pl->tensor = (D == 64 || D == 128) && pl->R >= 2;
     pl->rpt = decode_rows_per_thread(D, pl->R);
     const int keys = pl->tensor ? kDecTcKeys : kDecKeys;
     pl->num_tiles = (Lk + keys - 1) / keys;
@@ -714,7 +714,7 @@ extern "C" fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* 
     g_fault_next = 0;
     if (pl.tensor) {
         const int g = (int)(grid < ds->num_sms ? grid : ds->num_sms);
-        if (launch_decode_tc(mq, mk, mv, p, g, stream) != cudaSuccess) return FA_ERR_CUDA;
+        if (launch_decode_tc(D, mq, mk, mv, p, g, stream) != cudaSuccess) return FA_ERR_CUDA;
     } else if (launch_decode_partial(D, pl.rpt, mk, mv, p, (int)grid, stream) != cudaSuccess) {
         return FA_ERR_CUDA;
     }

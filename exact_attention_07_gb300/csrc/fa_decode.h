@@ -51,10 +51,11 @@ cudaError_t launch_decode_partial(int D, int rows_per_thread, const CUtensorMap&
 
 cudaError_t launch_decode_merge(int D, const DecodeParams& p, cudaStream_t stream);
 
-// Tensor-core partials (D = 128, 2 <= R <= 16): 128-key tiles, one persistent
-// CTA per SM (grid <= SM count) walking the (batch, KV head, partition) items.
+// Tensor-core partials (D = 64 or 128, 2 <= R <= 16): 128-key tiles, one
+// persistent CTA per SM (grid <= SM count) walking the (batch, KV head,
+// partition) items.
 constexpr int kDecTcKeys = 128;
-cudaError_t launch_decode_tc(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_decode_tc(int D, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                              const DecodeParams& p, int grid, cudaStream_t stream);
 
 }  // namespace fa

@@ -1,4 +1,4 @@
-// Split-KV decode partials on the fifth-generation tensor cores (sm_103a, D = 128).
+// Split-KV decode partials on the fifth-generation tensor cores (sm_103a, D = 64 and 128).
 //
 // Grouped-query decode has R = (Hq / Hkv) * Lq query rows per KV head (up to
 // 16 here).  Packing those rows into one work tile fills a matrix
@@ -9,7 +9,11 @@
 //     S^T [128 keys x 16 rows] = K_tile [128 x D] . Q^T [D x 16]
 //     O^T [D x 16 rows]       += V_tile^T [D x 128] . P^T [128 keys x 16]
 //
-// both accumulating in tensor memory.  The tensor core does the contraction
+// both accumulating in tensor memory.  With D = 64 the second product keeps
+// M = 128: the upper half of its A operand (dimensions 64..127) is a block of
+// zeros in shared memory, so tensor-memory lanes 64..127 accumulate zeros and
+// are never stored (decode is bound by streaming K and V, not by the MMA).
+// The tensor core does the contraction
 // at a small fraction of its rate, so the kernel is bound by streaming K and
 // V from HBM; the FP32-pipe variant (fa_decode.cu) runs out of issue slots
 // first once R reaches 4.
@@ -42,33 +46,38 @@ namespace fa {
 
 namespace {
 
-constexpr int kTcD = 128;              // head dimension of this kernel
 constexpr int kTcKeys = 128;           // keys per tile (the MMA's M)
 constexpr int kTcRows = 16;            // packed query rows (the MMA's N)
-constexpr int kTcSlots = 6;            // K/V ring slots (one tile of K or V each)
 constexpr int kTcThreads = 192;
-constexpr int kSlotBytes = kTcKeys * kTcD * 2;   // 32 KB
-constexpr int kHalfBytes = kSlotBytes / 2;       // one 64-dimension box
-constexpr int kQBytes = kTcRows * kTcD * 2;      // 4 KB: 16 rows, two 64-dimension boxes
+constexpr int kHalfBytes = kTcKeys * 64 * 2;     // one 64-dimension box of a K/V tile: 16 KB
+constexpr int kQBox = kTcRows * 64 * 2;          // one 64-dimension box of Q: 2 KB
 constexpr int kPBytes = kTcRows * kTcKeys * 2;   // 4 KB: P^T, two 64-key swizzle atoms
 
+// D = head dimension (64 or 128).  The ring holds 192 KB of K/V tiles either
+// way; D = 64 adds the zero block that pads the O^T MMA to M = 128.
+template <int D>
 struct TcSmem {
+    static constexpr int kBoxes = D / 64;                  // 64-dimension boxes per row
+    static constexpr int kSlotBytes = kTcKeys * D * 2;     // one K or V tile
+    static constexpr int kNumSlots = 6 * 128 / D;          // K/V ring slots
+    static constexpr int kQBytes = kTcRows * D * 2;
     static constexpr int kSlots = 0;
-    static constexpr int kQ = kSlots + kTcSlots * kSlotBytes;  // [2] Q buffers
-    static constexpr int kP = kQ + 2 * kQBytes;                // [2] P^T buffers
+    static constexpr int kZero = kSlots + kNumSlots * kSlotBytes;     // D = 64: 16 KB of zeros
+    static constexpr int kQ = kZero + (D < 128 ? kHalfBytes : 0);  // [2] Q buffers
+    static constexpr int kP = kQ + 2 * kQBytes;                      // [2] P^T buffers
     static constexpr int kRed = kP + 2 * kPBytes;              // float [2][4][16] row maxima
     static constexpr int kEpi = kRed + 2 * 4 * 16 * 4;         // float [4][32] row sums
     static constexpr int kBars = kEpi + 4 * 32 * 4;
     // barrier slots
-    static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kTcSlots;
-    static constexpr int bSFull = 4 + 2 * kTcSlots, bSEmpty = bSFull + 2, bPFull = bSFull + 4,
+    static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kNumSlots;
+    static constexpr int bSFull = 4 + 2 * kNumSlots, bSEmpty = bSFull + 2, bPFull = bSFull + 4,
                          bPEmpty = bSFull + 6, bOFull = bSFull + 8, bOEmpty = bSFull + 9,
                          bRed = bSFull + 10, bEpi = bSFull + 12, bDrain = bSFull + 13, kNumBars = bSFull + 14;
     static constexpr int kMisc = kBars + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kDynamic = kBytes + 1024;
+    static_assert(kDynamic <= 232448, "shared memory of one CTA");
 };
-static_assert(TcSmem::kDynamic <= 232448, "shared memory of one CTA");
 
 // TMEM columns: S^T double buffer, then O^T.
 constexpr uint32_t kColS = 0, kColO = 2 * kTcRows, kTmemCols = 64;
@@ -169,11 +178,13 @@ __device__ __forceinline__ TcItem tc_item(const DecodeParams& p, int it)
 
 }  // namespace
 
+template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p)
 {
-    using L = TcSmem;
+    using L = TcSmem<D>;
+    constexpr int kTcSlots = L::kNumSlots, kSlotBytes = L::kSlotBytes, kQBytes = L::kQBytes;
     constexpr float kTau = 8.0f;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -217,6 +228,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 5) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
+    }
+    if constexpr (D < 128) {
+        // the zero half of the O^T MMA's A operand, visible to the tensor core
+        uint4* z = reinterpret_cast<uint4*>(smem + L::kZero);
+        for (int i = threadIdx.x; i < kHalfBytes / 16; i += kTcThreads) z[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -353,10 +370,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const float lf_r = __shfl_sync(0xffffffffu, lsum, 16 + r);
                 if (r < p.R) {
                     const float val = l_r > 0.f ? o[r] / l_r : 0.f;
-                    if (single)
-                        p.o[(w.row0 + r) * kTcD + k] = val;
-                    else
-                        p.o_part[((long long)it * p.R + r) * kTcD + k] = val;
+                    if (k < D) {
+                        if (single)
+                            p.o[(w.row0 + r) * D + k] = val;
+                        else
+                            p.o_part[((long long)it * p.R + r) * D + k] = val;
+                    }
                     if (k == r) {
                         const float lse2 = lf_r > 0.f ? ref[r] + log2f(lf_r) : -INFINITY;
                         if (single)
@@ -385,8 +404,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive_expect_tx(bar(L::bKVFull + stage), kSlotBytes);
                     kv_armed[stage] = (int)kv_ph;
                     const uint32_t dst = sb + L::kSlots + (uint32_t)(stage * kSlotBytes);
-                    tma_load_3d(dst, map, bar(L::bKVFull + stage), 0, key0, bh);
-                    tma_load_3d(dst + kHalfBytes, map, bar(L::bKVFull + stage), 64, key0, bh);
+#pragma unroll
+                    for (int h = 0; h < L::kBoxes; ++h)
+                        tma_load_3d(dst + h * kHalfBytes, map, bar(L::bKVFull + stage), 64 * h, key0, bh);
                 }
                 if (++stage == kTcSlots) {
                     stage = 0;
@@ -402,8 +422,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_arrive_expect_tx(bar(L::bQFull + qb), kQBytes);
                 q_armed[qb] = (int)qph;
                 const uint32_t qdst = sb + L::kQ + (uint32_t)(qb * kQBytes);
-                tma_load_3d(qdst, &tmQ, bar(L::bQFull + qb), 0, (int)w.row0, 0);
-                tma_load_3d(qdst + kQBytes / 2, &tmQ, bar(L::bQFull + qb), 64, (int)w.row0, 0);
+#pragma unroll
+                for (int h = 0; h < L::kBoxes; ++h)
+                    tma_load_3d(qdst + h * kQBox, &tmQ, bar(L::bQFull + qb), 64 * h, (int)w.row0, 0);
                 bool ok = true;
                 for (int t = 0; t < w.n && ok; ++t) {
                     const int key0 = (w.t0 + t) * kTcKeys;
@@ -423,7 +444,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool leader = lane == 0;
         const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
         constexpr uint32_t kIdescS = idesc_bf16_f32(kTcKeys, kTcRows, false);
-        constexpr uint32_t kIdescPV = idesc_bf16_f32(kTcD, kTcRows, false) | (1u << 15);  // A (V^T) MN-major
+        // O^T keeps M = 128 (D = 64: the upper half of A is the zero block)
+        constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kTcRows, false) | (1u << 15);  // A (V^T) MN-major
         int stage = 0;
         uint32_t kv_ph = 0;
         uint32_t T = 0;
@@ -440,7 +462,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (first && !tc_warp_wait(bar(L::bOEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 72, it))
                 return false;
             tc_fence_after_sync();
-            const uint64_t vd = smem_desc_sw128(sb + L::kSlots + (uint32_t)(vs * kSlotBytes), kHalfBytes, 1024);
+            // A = V^T, MN-major: dimensions 64..127 are kHalfBytes further on, or
+            // (D = 64) in the zero block after the ring
+            const uint32_t vaddr = sb + L::kSlots + (uint32_t)(vs * kSlotBytes);
+            const uint32_t hi = D < 128 ? (uint32_t)L::kZero - (uint32_t)(L::kSlots + vs * kSlotBytes)
+                                        : (uint32_t)kHalfBytes;
+            const uint64_t vd = smem_desc_sw128(vaddr, hi, 1024);
             const uint64_t pd = smem_desc_sw128(sb + L::kP + bp * kPBytes, 16, 1024);
             if (leader) {
 #pragma unroll
@@ -477,9 +504,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint64_t kd = smem_desc_sw128(sb + L::kSlots + (uint32_t)(ks * kSlotBytes), 16, 1024);
                 if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < kTcD / 16; ++kk) {
+                    for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t koff = (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
-                        const uint64_t qoff = (uint64_t)(((kk >> 2) * (kQBytes / 2) + (kk & 3) * 32) >> 4);
+                        const uint64_t qoff = (uint64_t)(((kk >> 2) * kQBox + (kk & 3) * 32) >> 4);
                         mma_ss(tm + kColS + b * kTcRows, kd + koff, qd + qoff, kIdescS, kk > 0 ? 1u : 0u);
                     }
                 }
@@ -517,13 +544,21 @@ done:
     }
 }
 
-cudaError_t launch_decode_tc(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+template <int D>
+cudaError_t launch_decode_tc_dim(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                 const DecodeParams& p, int grid, cudaStream_t stream)
+{
+    const cudaError_t e = smem_limit_once<fa_decode_tc_kernel<D>>(TcSmem<D>::kDynamic);
+    if (e != cudaSuccess) return e;
+    fa_decode_tc_kernel<D><<<grid, kTcThreads, TcSmem<D>::kDynamic, stream>>>(q, k, v, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_tc(int D, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                              const DecodeParams& p, int grid, cudaStream_t stream)
 {
-    const cudaError_t e = smem_limit_once<fa_decode_tc_kernel>(TcSmem::kDynamic);
-    if (e != cudaSuccess) return e;
-    fa_decode_tc_kernel<<<grid, kTcThreads, TcSmem::kDynamic, stream>>>(q, k, v, p);
-    return cudaGetLastError();
+    return D == 64 ? launch_decode_tc_dim<64>(q, k, v, p, grid, stream)
+                   : launch_decode_tc_dim<128>(q, k, v, p, grid, stream);
 }
 
 }  // namespace fa

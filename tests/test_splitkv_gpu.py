@@ -61,6 +61,8 @@ CASES = [
     (2, 16, 4, 1, 2048, 128, False, 4, 20.0),   # very sharp softmax
     (1, 6, 2, 2, 3000, 128, True, 6, 1.0),      # 6 rows: padded row slots in the kernel
     (1, 12, 4, 1, 999, 64, False, 2, 1.0),      # 3 rows at D = 64
+    (2, 32, 8, 1, 4100, 64, True, 0, 1.0),      # GQA r = 4 at D = 64 on the tensor cores, ragged last tile
+    (1, 16, 1, 1, 3000, 64, False, 5, 20.0),    # MQA, 16 rows, sharp softmax, D = 64
     (4, 8, 8, 1, 65, 128, True, 1, 1.0),        # one partition: no merge launch
 ]
 
@@ -74,8 +76,9 @@ def test_splitkv_full_compare(B, Hq, Hkv, Lq, Lk, D, causal, splits, qm):
     assert 1 <= used <= math.ceil(Lk / 64)  # partitions hold whole tiles (64 or 128 keys)
     ref_o, ref_lse = oracle.attention(q, k, v, scale=1 / math.sqrt(D), causal=causal)
     compare(o, lse, ref_o, ref_lse, f"splitkv {B,Hq,Hkv,Lq,Lk,D,causal,splits,qm}")
-    if D == 64 or (Hq // Hkv) * Lq == 1:
-        # the FP32-pipe kernel keeps P in fp32: far inside the bf16-P tolerance
+    if (Hq // Hkv) * Lq == 1:
+        # one row per KV head runs the FP32-pipe kernel, which keeps P in fp32:
+        # far inside the bf16-P tolerance
         fin = np.isfinite(ref_lse)
         assert np.abs(o - ref_o).max() <= 1e-3
         assert np.abs(lse[fin] - ref_lse[fin]).max() <= 1e-4 if fin.any() else True
@@ -121,7 +124,7 @@ def test_workspace_too_small_is_rejected():
     assert st == fa.FA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("Hq,D", [(4, 128), (4, 64)])  # tensor-core and FP32-pipe partial kernels
+@pytest.mark.parametrize("Hq,D", [(4, 128), (4, 64), (1, 64)])  # tensor-core (D = 128, 64) and FP32-pipe kernels
 def test_timed_out_wait_is_reported_and_context_survives(Hq, D):
     """The test hook drops the first K/V tile of every CTA: the bounded wait
     runs out, the launch retires with FA_ERR_TIMEOUT, the next call works."""

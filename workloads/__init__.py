@@ -192,6 +192,8 @@ WORKLOADS.update(PROFILE_WORKLOADS)
 DECODE_WORKLOADS: dict[str, Workload] = {
     "decode_b8_h32x8_l32768_d128": Workload("decode_b8_h32x8_l32768_d128", 8, 32, 8, 1, 32768, 128, False,
                                             decode=True),
+    "decode_b8_h32x8_l32768_d64": Workload("decode_b8_h32x8_l32768_d64", 8, 32, 8, 1, 32768, 64, False,
+                                           decode=True),
 }
 WORKLOADS.update(DECODE_WORKLOADS)
 

@@ -145,6 +145,7 @@ cudaError_t dispatch_variant_dim(int var, const CUtensorMap& q, const CUtensorMa
 {
     if (var == kVarSoftcap) return launch_fwd<D, false, VARLEN, kVarSoftcap>(q, k, v, p, grid, st);
     if (var == kVarAlibi) return launch_fwd<D, false, VARLEN, kVarAlibi>(q, k, v, p, grid, st);
+    if (var == kVarCapAlibi) return launch_fwd<D, false, VARLEN, kVarCapAlibi>(q, k, v, p, grid, st);
     return launch_fwd<D, false, VARLEN, kVarWindow>(q, k, v, p, grid, st);
 }
 
@@ -165,14 +166,13 @@ int prepare_variant(const fa_variant_t* var, int D, float scale, FwdParams* p)
     if (!std::isfinite(var->softcap) || var->softcap < 0.f) return -(int)FA_ERR_INVALID_ARG;
     if (var->alibi_slopes && (reinterpret_cast<uintptr_t>(var->alibi_slopes) & 3u)) return -(int)FA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return -(int)FA_ERR_UNSUPPORTED;
-    if (var->softcap > 0.f && var->alibi_slopes) return -(int)FA_ERR_UNSUPPORTED;
     p->win_left = var->window_left < 0 ? -1 : var->window_left;
     p->win_right = var->window_right < 0 ? -1 : var->window_right;
     p->alibi = var->alibi_slopes;
     if (var->softcap > 0.f) {
         p->cap_in = scale / var->softcap;
         p->cap_out = (float)((double)var->softcap * 1.4426950408889634);
-        return kVarSoftcap;
+        return var->alibi_slopes ? kVarCapAlibi : kVarSoftcap;
     }
     return var->alibi_slopes ? kVarAlibi : kVarWindow;
 }
@@ -358,7 +358,7 @@ fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, flo
 
     p.o = o;
     p.lse = lse;
-    set_batch_heads(&p, B, Hq, Hkv, var != kVarAlibi);
+    set_batch_heads(&p, B, Hq, Hkv, !var_alibi(var));
     p.Lq = Lq;
     p.Lk = Lk;
     p.group = Hq / Hkv;
@@ -765,14 +765,13 @@ int prepare_bwd_variant(const fa_variant_t* var, int D, float scale, BwdParams* 
     if (!std::isfinite(var->softcap) || var->softcap < 0.f) return -(int)FA_ERR_INVALID_ARG;
     if (var->alibi_slopes && (reinterpret_cast<uintptr_t>(var->alibi_slopes) & 3u)) return -(int)FA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return -(int)FA_ERR_UNSUPPORTED;
-    if (var->softcap > 0.f && var->alibi_slopes) return -(int)FA_ERR_UNSUPPORTED;
     p->win_left = var->window_left < 0 ? -1 : var->window_left;
     p->win_right = var->window_right < 0 ? -1 : var->window_right;
     p->alibi = var->alibi_slopes;
     if (var->softcap > 0.f) {
         p->cap_in2 = (float)(2.0 * 1.4426950408889634 * (double)scale / (double)var->softcap);
         p->cap_out = (float)((double)var->softcap * 1.4426950408889634);
-        return kVarSoftcap;
+        return var->alibi_slopes ? kVarCapAlibi : kVarSoftcap;
     }
     return var->alibi_slopes ? kVarAlibi : kVarWindow;
 }

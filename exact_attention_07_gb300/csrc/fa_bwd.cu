@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (p.win_left >= 0 && kpos < q0 + kBwdTile - 1 + off - p.win_left) need_mask = true;
                     if (p.win_right >= 0 && kpos > q0 + off + p.win_right) need_mask = true;
                 }
-                if constexpr (VAR == kVarAlibi) alibi_l2 = __ldg(p.alibi + h) * 1.4426950408889634f;
+                if constexpr (var_alibi(VAR)) alibi_l2 = __ldg(p.alibi + h) * 1.4426950408889634f;
                 if (!bwd_warp_wait(bar(L::bQFull + qs), qph, abort_flag, wf, 79, it)) goto done;
                 if (!bwd_warp_wait(bar(L::bSFull), ph, abort_flag, wf, 80, it)) goto done;
                 tc_fence_after_sync();
@@ -659,14 +659,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float b0 = -l2[e], b1 = -l2[e + 1];
-                        if constexpr (VAR == kVarAlibi) {
-                            // s * scale - slope * |c_q - key|, in log2 units
+                        if constexpr (var_alibi(VAR)) {
+                            // s' - slope * |c_q - key|, in log2 units (s' = s * scale,
+                            // or with soft-capping the capped score below)
                             const float d0 = (float)(q0 + c * 32 + e + off - kpos);
                             b0 = fmaf(-alibi_l2, fabsf(d0), b0);
                             b1 = fmaf(-alibi_l2, fabsf(d0 + 1.f), b1);
                         }
                         float p0, p1, g0 = 1.f, g1 = 1.f;
-                        if constexpr (VAR == kVarSoftcap) {
+                        if constexpr (var_softcap(VAR)) {
                             // t = cap tanh(s scale / cap) with tanh(u) = 1 - 2 rho,
                             // rho = 1 / (1 + e^(2u)); dt/ds = 1 - tanh^2 = 4 rho (1 - rho)
                             const float rho0 = bwd_rcp_approx(1.f + ex2_approx(__uint_as_float(r[e]) * p.cap_in2));
@@ -691,7 +692,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 if (p.win_right >= 0 && kpos > q + 1 + off + p.win_right) p1 = 0.f;
                             }
                         }
-                        if constexpr (VAR == kVarSoftcap) {
+                        if constexpr (var_softcap(VAR)) {
                             pt[e / 2] = bwd_pack_bf16(p0, p1);
                             pk[cc * 16 + e / 2] = bwd_pack_bf16(p0 * g0, p1 * g1);
                         } else {
@@ -702,9 +703,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // columns (column 64ch + c holds queries 64ch + 2c, 2c + 1), which
                     // this thread has read; the other half's columns may still be
                     // being read by its warps
-                    if constexpr (VAR == kVarSoftcap) bwd_tmem_st16(lane_base + kColS + 64 * ch + 16 * cc, pt);
+                    if constexpr (var_softcap(VAR)) bwd_tmem_st16(lane_base + kColS + 64 * ch + 16 * cc, pt);
                 }
-                if constexpr (VAR != kVarSoftcap) {
+                if constexpr (!var_softcap(VAR)) {
                     uint32_t lo[16], hi[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -1059,6 +1060,9 @@ cudaError_t FA_BWD_VARIANT_FN(int var, bool varlen, const CUtensorMap& q, const 
     if (var == kVarSoftcap)
         return varlen ? launch_bwd_kernel<D, false, true, kVarSoftcap>(q, k, v, dout, dq, p, grid, stream)
                       : launch_bwd_kernel<D, false, false, kVarSoftcap>(q, k, v, dout, dq, p, grid, stream);
+    if (var == kVarCapAlibi)
+        return varlen ? launch_bwd_kernel<D, false, true, kVarCapAlibi>(q, k, v, dout, dq, p, grid, stream)
+                      : launch_bwd_kernel<D, false, false, kVarCapAlibi>(q, k, v, dout, dq, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 #endif

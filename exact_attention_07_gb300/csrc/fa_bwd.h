@@ -61,7 +61,7 @@ cudaError_t launch_bwd_pre(int D, bool varlen, const BwdParams& p, cudaStream_t 
 cudaError_t launch_bwd(int D, bool causal, bool varlen, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq, const BwdParams& p,
                        int grid, cudaStream_t stream);
-// Variants (var = kVarWindow, kVarSoftcap or kVarAlibi, no separate causal
+// Variants (var = kVarWindow, kVarSoftcap, kVarAlibi or kVarCapAlibi, no separate causal
 // flag: a causal window is (-1, 0)), head dimension 64 or 128, each in a
 // translation unit of its own.
 cudaError_t launch_bwd_variant_d64(int var, bool varlen, const CUtensorMap& q, const CUtensorMap& k,

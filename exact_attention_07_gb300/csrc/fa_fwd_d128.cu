@@ -48,6 +48,8 @@ FA_INSTANCE(FA_HEAD_DIM, false, false, kVarSoftcap)
 FA_INSTANCE(FA_HEAD_DIM, false, true, kVarSoftcap)
 FA_INSTANCE(FA_HEAD_DIM, false, false, kVarAlibi)
 FA_INSTANCE(FA_HEAD_DIM, false, true, kVarAlibi)
+FA_INSTANCE(FA_HEAD_DIM, false, false, kVarCapAlibi)
+FA_INSTANCE(FA_HEAD_DIM, false, true, kVarCapAlibi)
 #endif
 #endif
 

@@ -656,10 +656,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.win_left >= 0) kv_first = max(0, c_row - p.win_left);
             }
             float alibi_l2 = 0.f;  // ALiBi slope of this head, log2 units
-            if constexpr (VAR == kVarAlibi) alibi_l2 = __ldg(p.alibi + w.hq) * 1.4426950408889634f;
+            if constexpr (var_alibi(VAR)) alibi_l2 = __ldg(p.alibi + w.hq) * 1.4426950408889634f;
             // score multiplier inside the exponent: the score modifiers already
             // produce log2-unit scores; e4m3 scores carry the tiles' scales
-            constexpr bool kLog2Mod = VAR == kVarSoftcap || VAR == kVarAlibi;
+            constexpr bool kLog2Mod = var_softcap(VAR) || var_alibi(VAR);
             float smul = kLog2Mod ? 1.f : sl2;
             const float* fp8_sk = nullptr;
             if constexpr (VAR == kVarFp8) {
@@ -699,8 +699,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int key0 = (j + w.kf) * kBlockN;
                 if constexpr (VAR == kVarFp8) smul = smul_q * __ldg(fp8_sk + j);
-                // score modifiers (FlashAttention from Scratch, sec. 12), in log2 units
-                if constexpr (VAR == kVarSoftcap) {
+                // score modifiers (FlashAttention from Scratch, sec. 12), in log2 units:
+                // soft-capping of the scaled score, then the ALiBi distance bias
+                if constexpr (var_softcap(VAR)) {
                     // cap * tanh(s * scale / cap), tanh(u) = 1 - 2 / (1 + e^(2u))
                     const float k2 = p.cap_in * (2.f * 1.4426950408889634f);
 #pragma unroll
@@ -711,15 +712,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float th = fmaf(-2.f, rcp_approx(1.f + e2u), 1.f);
                             sv[c][i] = __float_as_uint(th * p.cap_out);
                         }
-                } else if constexpr (VAR == kVarAlibi) {
-                    // s * scale - slope * |c - key|
+                }
+                if constexpr (var_alibi(VAR)) {
+                    // s' - slope * |c - key|, s' = s * scale or the capped score
                     const float cf = (float)(c_row - key0);
+                    const float pre = var_softcap(VAR) ? 1.f : sl2;
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             sv[c][i] = __float_as_uint(fmaf(-alibi_l2, fabsf(cf - (float)(32 * c + i)),
-                                                            __uint_as_float(sv[c][i]) * sl2));
+                                                            __uint_as_float(sv[c][i]) * pre));
                 }
                 // masking: keys outside [kv_first, kv_last] (causal diagonal, key
                 // window, sequence tail) get -inf (FlashAttention from Scratch, sec. 7.3)

@@ -50,13 +50,16 @@ constexpr int kThreads = 512;
 
 // Variants of the forward kernel: 0 = plain, 1 = key window, 2 = key window +
 // soft-capping, 3 = key window + ALiBi (FlashAttention from Scratch, sec. 12),
-// 4 = e4m3 inputs with per-tile scales (sec. 10.3).
-enum : int { kVarNone = 0, kVarWindow = 1, kVarSoftcap = 2, kVarAlibi = 3, kVarFp8 = 4 };
+// 4 = e4m3 inputs with per-tile scales (sec. 10.3), 5 = key window +
+// soft-capping followed by ALiBi.
+enum : int { kVarNone = 0, kVarWindow = 1, kVarSoftcap = 2, kVarAlibi = 3, kVarFp8 = 4, kVarCapAlibi = 5 };
+constexpr bool var_softcap(int v) { return v == kVarSoftcap || v == kVarCapAlibi; }
+constexpr bool var_alibi(int v) { return v == kVarAlibi || v == kVarCapAlibi; }
 
 // Sequences one launch of a packed batch can schedule in shared memory
 // (what the forward kernel's layout leaves free at each head dimension); the
 // host splits larger batches into launches of at most this many sequences.
 constexpr int varlen_sched_max_seqs(int D, int DV) { return D == DV ? 1536 : 64; }
-constexpr bool var_window(int v) { return v == kVarWindow || v == kVarSoftcap || v == kVarAlibi; }
+constexpr bool var_window(int v) { return v == kVarWindow || var_softcap(v) || var_alibi(v); }
 
 }  // namespace fa

@@ -154,9 +154,10 @@ fa_status_t fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, f
  *   softcap > 0: the scaled score s becomes softcap * tanh(s / softcap).
  *   alibi_slopes: DEVICE fp32 [Hq] (or NULL); the score of query head h
  *     becomes s - alibi_slopes[h] * |c_i - j|.
- *   Order: scale, then the score modifier, then the window.  softcap and
- *   alibi_slopes cannot be combined (FA_ERR_UNSUPPORTED); D must be 64 or 128.
- *   LSE is the log-sum-exp of the modified scores.
+ *   Order: scale, then soft-capping, then the ALiBi bias, then the window:
+ *   with both modifiers the score is softcap * tanh(s / softcap) -
+ *   alibi_slopes[h] * |c_i - j| (the bias stays unbounded by the cap).
+ *   D must be 64 or 128.  LSE is the log-sum-exp of the modified scores.
  */
 typedef struct fa_variant {
     int window_left;
@@ -346,9 +347,9 @@ fa_status_t fa_bwd_varlen_workspace(int num_seqs, int total_q, int Hq, size_t* w
  * The gradient with respect to t is P * (dP - delta); the ALiBi bias and the
  * masks do not depend on the raw score s, so that is dS, while soft-capping
  * (t = cap * tanh(s / cap)) multiplies it by dt/ds = 1 - tanh^2(s / cap).
- * Layouts, workspace and launches as fa_bwd / fa_bwd_varlen; `variant` is a
- * HOST pointer.  D must be 64 or 128, and soft-capping with ALiBi is
- * unsupported, as in the forward: both return FA_ERR_UNSUPPORTED.
+ * With both modifiers the factor dt/ds is that of the cap alone.  Layouts,
+ * workspace and launches as fa_bwd / fa_bwd_varlen; `variant` is a HOST
+ * pointer.  D must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
  */
 fa_status_t fa_bwd_variant(const void* q, const void* k, const void* v, const float* o, const float* lse,
                            const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq,

@@ -195,7 +195,6 @@ def test_variant_argument_validation(lib):
     assert call(ctypes.byref(_Variant(-1, 0, -1.0, None))) == INV
     assert call(ctypes.byref(_Variant(-1, 0, 0.0, 18))) == INV        # misaligned slopes
     assert call(ctypes.byref(_Variant(-1, 0, 0.0, None)), D=96) == UNS   # head dimensions 64 and 128 only
-    assert call(ctypes.byref(_Variant(-1, 0, 5.0, 16))) == UNS        # soft-capping with ALiBi
     assert lib.fa_fwd_varlen_variant(16, 16, 16, 16, 16, 32, 32, 1, 10, 10, 8, 8, 2, 2, 128, None, 0.1,
                                      None) == INV
 
@@ -272,7 +271,6 @@ def test_bwd_variant_argument_validation(lib):
     assert call(ctypes.byref(_Variant(-1, 0, float("nan"), None))) == INV
     assert call(ctypes.byref(_Variant(-1, 0, 0.0, 18))) == INV        # misaligned slopes
     assert call(ctypes.byref(_Variant(-1, 0, 0.0, None)), D=96) == UNS   # head dimensions 64 and 128 only
-    assert call(ctypes.byref(_Variant(-1, 0, 5.0, 32))) == UNS        # soft-capping with ALiBi, as in the forward
     assert lib.fa_bwd_varlen_variant(16, 16, 16, 16, 16, 16, 16, 16, 16, 32, 32, 1, 10, 10, 8, 8, 2, 2, 128, None,
                                      0.1, 16, 1 << 20, None) == INV
     assert lib.fa_last_launch_count() == 0

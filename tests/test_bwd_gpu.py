@@ -198,6 +198,8 @@ BWD_VARIANT_CASES = [
     (1, 2, 2, 384, 384, (-1, -1), 5.0, False, 4.0),     # soft cap 5, scores ~ N(0, 16): tanh saturates
     (1, 4, 2, 333, 517, (-1, 0), 30.0, False, 6.0),     # soft cap 30, causal, GQA, ragged, Lq < Lk
     (2, 2, 2, 300, 300, (100, 20), 2.0, False, 3.0),    # soft cap 2 inside a two-sided window
+    (2, 4, 2, 400, 400, (-1, -1), 4.0, True, 3.0),     # soft-capping, then ALiBi
+    (1, 4, 4, 333, 517, (-1, 0), 6.0, True, 4.0),       # both modifiers, causal, ragged, Lq < Lk
 ]
 
 
@@ -205,6 +207,7 @@ BWD_VARIANT_CASES_D64 = [
     (1, 2, 1, 513, 513, (300, 0), 0.0, False, 1.0),     # window edge inside tiles, GQA
     (1, 4, 2, 333, 517, (-1, 0), 30.0, False, 6.0),     # soft cap 30, causal, GQA, ragged, Lq < Lk
     (1, 4, 4, 400, 400, (255, 0), 0.0, True, 1.0),      # ALiBi inside a causal window
+    (1, 4, 2, 400, 400, (-1, 0), 4.0, True, 3.0),       # soft-capping, then ALiBi, causal
 ]
 
 

@@ -75,7 +75,8 @@ def _brute(q, k, v, scale, window, cap, slope, Lq, Lk):
 
 
 @pytest.mark.parametrize("window,cap,slope", [((2, 1), 0.0, 0.0), ((-1, 0), 3.0, 0.0), ((4, -1), 0.0, 0.3),
-                                              ((0, 0), 0.0, 0.0), ((1, 2), 2.0, 0.0), ((-1, -1), 0.0, 0.7)])
+                                              ((0, 0), 0.0, 0.0), ((1, 2), 2.0, 0.0), ((-1, -1), 0.0, 0.7),
+                                              ((-1, 0), 3.0, 0.3), ((3, 2), 1.5, 0.5)])  # cap, then the bias
 @pytest.mark.parametrize("Lq,Lk", [(6, 6), (4, 9), (9, 4)])
 def test_brute_force(window, cap, slope, Lq, Lk):
     q, k, v = _rand((1, 2, Lq, 3), 1, 1.5), _rand((1, 1, Lk, 3), 2, 1.5), _rand((1, 1, Lk, 2), 3)
@@ -166,7 +167,8 @@ def _torch_variant_grads(q, k, v, do, scale, window, softcap, slopes):
 
 
 @pytest.mark.parametrize("window,softcap,alibi", [((5, 0), 0.0, False), ((3, 4), 0.0, False), ((-1, -1), 2.0, False),
-                                                 ((6, 0), 1.5, False), ((-1, -1), 0.0, True), ((4, 2), 0.0, True)])
+                                                 ((6, 0), 1.5, False), ((-1, -1), 0.0, True), ((4, 2), 0.0, True),
+                                                 ((-1, -1), 2.0, True), ((6, 0), 1.5, True)])
 @pytest.mark.parametrize("Lq,Lk", [(13, 13), (9, 17), (17, 9)])
 def test_variant_backward_matches_autograd(window, softcap, alibi, Lq, Lk):
     from oracle.variants import attention_variant_bwd

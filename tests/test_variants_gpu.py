@@ -41,6 +41,8 @@ CASES = [
     (1, 4, 2, 777, 777, (-1, 0), 5.0, False, 4.0),       # tight cap, causal, GQA
     (1, 4, 4, 600, 600, (-1, -1), 0.0, True, 1.0),       # ALiBi, full attention
     (2, 8, 2, 529, 529, (255, 0), 0.0, True, 1.0),       # ALiBi with a causal window, GQA
+    (2, 4, 2, 600, 600, (-1, -1), 5.0, True, 4.0),       # soft-capping, then ALiBi, full attention
+    (1, 4, 4, 777, 777, (300, 0), 8.0, True, 3.0),       # both modifiers inside a causal window
 ]
 
 
@@ -49,6 +51,7 @@ CASES_D64 = [
     (1, 2, 1, 300, 900, (64, 64), 0.0, False, 1.0),      # two-sided window, Lq < Lk
     (1, 4, 2, 777, 777, (-1, 0), 5.0, False, 4.0),       # tight cap, causal, GQA
     (2, 8, 2, 529, 529, (255, 0), 0.0, True, 1.0),       # ALiBi with a causal window, GQA
+    (1, 4, 2, 600, 600, (-1, 0), 5.0, True, 4.0),        # soft-capping, then ALiBi, causal
 ]
 
 
@@ -81,7 +84,8 @@ def test_varlen_variant(D):
     cq = torch.tensor([0] + np.cumsum(lens_q).tolist(), dtype=torch.int32)
     ck = torch.tensor([0] + np.cumsum(lens_k).tolist(), dtype=torch.int32)
     slopes = alibi(Hq)
-    for window, cap, sl in (((127, 0), 0.0, None), ((-1, 0), 10.0, None), ((200, 3), 0.0, slopes)):
+    for window, cap, sl in (((127, 0), 0.0, None), ((-1, 0), 10.0, None), ((200, 3), 0.0, slopes),
+                            ((-1, 0), 6.0, slopes)):
         o, lse = fa.fa_fwd_varlen_variant(q.to(DEV), k.to(DEV), v.to(DEV), cq.to(DEV), ck.to(DEV), max(lens_q),
                                           max(lens_k), window=window, softcap=cap,
                                           alibi_slopes=torch.from_numpy(sl).to(DEV) if sl is not None else None)

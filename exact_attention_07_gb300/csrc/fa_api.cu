@@ -207,7 +207,9 @@ bool hdim_supported(int D, int Dv) { return (D == Dv && (D == 64 || D == 128)) |
 // grids", step 4), and writes the exclusive prefix of work tiles in that
 // order.
 //   forward  (bwd = 0): a tile is 256 query rows of one query head and visits
-//            ceil(Lk/128) KV tiles: tiles = Hq * ceil(Lq/256), sorted by Lk.
+//            ceil(Lk/128) KV tiles: tiles = Hq * ceil(Lq/256), sorted by Lk;
+//            with paired heads (bwd = 2) 128 rows of two query heads:
+//            tiles = (Hq/2) * ceil(Lq/128).
 //   backward (bwd = 1): an item is 128 keys of one KV head and visits the Q
 //            tiles of the group: items = Hkv * ceil(Lk/128) when Lq > 0,
 //            sorted by Lq; also the sequences' row offsets in a workspace
@@ -240,12 +242,12 @@ __global__ void __launch_bounds__(kSchedThreads)
         const bool ok = !bad && q0 >= 0 && q1 >= q0 && q1 <= total_q && q1 - q0 <= max_q && k0 >= 0 &&
                         k1 >= k0 && k1 <= total_k && k1 - k0 <= max_k;
         if (!ok) atomicOr(err, 2);
-        if (bwd) {
+        if (bwd == 1) {
             if (n <= kSortMax) key[s] = (ok && q1 > q0 && k1 > k0) ? (q1 - q0) : -1;
             tiles[s] = (ok && q1 > q0) ? heads * ((k1 - k0 + 127) / 128) : 0;
         } else {
             if (n <= kSortMax) key[s] = (ok && q1 > q0) ? (k1 - k0) : -1;
-            tiles[s] = ok ? heads * ((q1 - q0 + 255) / 256) : 0;
+            tiles[s] = !ok ? 0 : bwd == 2 ? (heads / 2) * ((q1 - q0 + 127) / 128) : heads * ((q1 - q0 + 255) / 256);
         }
     }
     __syncthreads();
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(kSchedThreads)
         prefix[r] = acc;
         acc += tiles[order[r]];
     }
-    if (!bwd) return;
+    if (bwd != 1) return;
     // padded row offsets in the original sequence order (valid sequences only)
     __syncthreads();
     int padded = 0;
@@ -335,8 +337,10 @@ fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, flo
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
     if (!hdim_supported(D, Dv)) return FA_ERR_UNSUPPORTED;
-    const long long nmb = (Lq + kRowsPerCta - 1) / kRowsPerCta;
-    const long long tiles = (long long)B * Hq * nmb;
+    // causal GQA with an even group: work tiles of two query heads over 128 rows
+    const bool pair = causal != 0 && !variant && (Hq / Hkv) % 2 == 0;
+    const long long tiles = pair ? (long long)B * (Hq / 2) * ((Lq + kBlockM - 1) / kBlockM)
+                                 : (long long)B * Hq * ((Lq + kRowsPerCta - 1) / kRowsPerCta);
     if (tiles >= (1ll << 31) || (long long)B * Hq >= (1ll << 31) || (long long)B * Hkv >= (1ll << 31))
         return FA_ERR_INVALID_ARG;
     FwdParams p{};
@@ -365,6 +369,7 @@ fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, flo
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
     p.heads_per_section = heads_per_section(p.Hkv, Lk, D + Dv, !causal && var == kVarNone);
     p.num_tiles = (int)tiles;
+    p.pair_heads = pair ? 1 : 0;
     p.err = ds->err;
     p.diag = ds->diag;
     p.fault = g_fault_next;
@@ -483,6 +488,8 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
     p.group = Hq / Hkv;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
     p.heads_per_section = heads_per_section(Hkv, max_seqlen_k, D + Dv, false);
+    // causal GQA with an even group: work tiles of two query heads over 128 rows
+    p.pair_heads = (causal != 0 && !variant && (Hq / Hkv) % 2 == 0) ? 1 : 0;
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
     p.num_seqs = num_seqs;
@@ -504,7 +511,8 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
     };
     if (sched_scratch) {
         if (launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
-                                   max_seqlen_k, Hq, 0, sched_scratch, ds->err, stream) != cudaSuccess)
+                                   max_seqlen_k, Hq, p.pair_heads ? 2 : 0, sched_scratch, ds->err, stream) !=
+            cudaSuccess)
             return FA_ERR_CUDA;
         g_last_launches = 1;
         p.sched = sched_scratch;

@@ -183,7 +183,9 @@ __device__ __forceinline__ void build_varlen_schedule(const FwdParams& p, unsign
                             k1 >= k0 && k1 <= p.total_k && k1 - k0 <= p.max_k;
             if (!ok && blockIdx.x == 0) atomicOr(p.err, 2);
             const int len = (ok && q1 > q0) ? (k1 - k0) : -1;
-            tiles[i] = ok ? p.Hq * ((q1 - q0 + kRowsPerCta - 1) / kRowsPerCta) : 0;
+            tiles[i] = !ok ? 0
+                       : p.pair_heads ? (p.Hq >> 1) * ((q1 - q0 + kBlockM - 1) / kBlockM)
+                                      : p.Hq * ((q1 - q0 + kRowsPerCta - 1) / kRowsPerCta);
             // ascending order of (longest first, then batch order)
             key = ((unsigned long long)(0x7fffffffu - (unsigned)len) << 32) | (unsigned)i;
         }
@@ -245,7 +247,9 @@ __device__ __forceinline__ void build_varlen_schedule(const FwdParams& p, unsign
 
 struct Work {
     int hq, hkv;
-    int m0;      // first query row of the CTA's 256-row block, within the sequence
+    int m0;      // first query row of the CTA's block, within the sequence
+    int rstep;   // Q tile 1 starts rstep rows after Q tile 0 (0 or 128) ...
+    int hstep;   // ... in query head hq + hstep (1 when two heads share the rows)
     int lq, lk;  // query / key length of this problem
     int zq, zk;  // TMA coordinates: dense = head slab (b*H + h), varlen = first token
     int q0;      // varlen: first query token of the sequence
@@ -268,6 +272,11 @@ __device__ __forceinline__ Work decode_tile(const FwdParams& p, uint32_t sched_s
     w.b = 0;
     w.q0 = 0;
     int k0 = 0;
+    // Paired heads: two query heads of one KV head over the same 128 rows, so
+    // that under a causal mask both Q tiles see exactly the same keys (256 rows
+    // of one head leave the first Q tile a fully masked last KV step).
+    const bool pair = CAUSAL && p.pair_heads != 0;
+    const int tile_rows = pair ? kBlockM : kRowsPerCta;
     if constexpr (VARLEN) {
         const VarSchedView vs{p, sched_smem};
         int lo = 0, hi = vs.n() - 1;
@@ -282,26 +291,29 @@ __device__ __forceinline__ Work decode_tile(const FwdParams& p, uint32_t sched_s
         k0 = __ldg(p.cu_k + s);
         w.lq = __ldg(p.cu_q + s + 1) - w.q0;
         w.lk = __ldg(p.cu_k + s + 1) - k0;
-        nmb = (w.lq + kRowsPerCta - 1) / kRowsPerCta;
+        nmb = (w.lq + tile_rows - 1) / tile_rows;
     } else {
         w.lq = p.Lq;
         w.lk = p.Lk;
-        nmb = (p.Lq + kRowsPerCta - 1) / kRowsPerCta;
-        const int per_b = nmb * p.Hq;
+        nmb = (p.Lq + tile_rows - 1) / tile_rows;
+        const int per_b = nmb * (pair ? (p.Hq >> 1) : p.Hq);
         w.b = t / per_b;
         rem = t - w.b * per_b;
     }
     const int G = p.group, hs = p.heads_per_section;
-    const int sec_tiles = nmb * hs * G;
+    const int PG = pair ? (G >> 1) : G;  // query-head slots per KV head
+    const int sec_tiles = nmb * hs * PG;
     const int sec = rem / sec_tiles;
     const int rem2 = rem - sec * sec_tiles;
     const int hs_cur = min(hs, p.Hkv - sec * hs);
-    const int i = rem2 / (hs_cur * G);
-    const int rem3 = rem2 - i * hs_cur * G;
-    w.hkv = sec * hs + rem3 / G;
-    w.hq = w.hkv * G + rem3 % G;
+    const int i = rem2 / (hs_cur * PG);
+    const int rem3 = rem2 - i * hs_cur * PG;
+    w.hkv = sec * hs + rem3 / PG;
+    w.hq = w.hkv * G + (pair ? 2 * (rem3 % PG) : rem3 % PG);
     const int mb = CAUSAL ? (nmb - 1 - i) : i;
-    w.m0 = mb * kRowsPerCta;
+    w.m0 = mb * tile_rows;
+    w.rstep = pair ? 0 : kBlockM;
+    w.hstep = pair ? 1 : 0;
     if constexpr (VARLEN) {
         w.zq = w.q0;
         w.zk = k0;
@@ -315,7 +327,7 @@ __device__ __forceinline__ Work decode_tile(const FwdParams& p, uint32_t sched_s
     } else if (var_window(VAR)) {
         // key window [c - left, c + right] around each row's aligned position c
         const int off = w.lk - w.lq;
-        const int last_row = min(w.m0 + kRowsPerCta - 1, w.lq - 1);
+        const int last_row = min(w.m0 + tile_rows - 1, w.lq - 1);
         const int lo = p.win_left >= 0 ? max(0, w.m0 + off - p.win_left) : 0;
         const int hi = p.win_right >= 0 ? min(w.lk - 1, last_row + off + p.win_right) : w.lk - 1;
         if (hi < lo) {
@@ -327,7 +339,7 @@ __device__ __forceinline__ Work decode_tile(const FwdParams& p, uint32_t sched_s
     } else if (!CAUSAL) {
         w.nk = (w.lk + kBlockN - 1) / kBlockN;
     } else {
-        const int last_row = min(w.m0 + kRowsPerCta - 1, w.lq - 1);
+        const int last_row = min(w.m0 + tile_rows - 1, w.lq - 1);
         const int last_key = min(w.lk - 1, last_row + (w.lk - w.lq));
         w.nk = last_key < 0 ? 0 : last_key / kBlockN + 1;
     }
@@ -646,7 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
             const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, sb + SS::kOff, tile);
             if (w.nk == 0) continue;
-            const int q_row = w.m0 + t * kBlockM + row;
+            const int q_row = w.m0 + t * w.rstep + row;
+            const int hq_t = w.hq + t * w.hstep;  // query head of this Q tile
             int kv_last = w.lk - 1;  // last key this row may attend
             int kv_first = 0;        // first key this row may attend
             const int c_row = q_row + (w.lk - w.lq);  // the row's aligned position among the keys
@@ -656,14 +669,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.win_left >= 0) kv_first = max(0, c_row - p.win_left);
             }
             float alibi_l2 = 0.f;  // ALiBi slope of this head, log2 units
-            if constexpr (var_alibi(VAR)) alibi_l2 = __ldg(p.alibi + w.hq) * 1.4426950408889634f;
+            if constexpr (var_alibi(VAR)) alibi_l2 = __ldg(p.alibi + hq_t) * 1.4426950408889634f;
             // score multiplier inside the exponent: the score modifiers already
             // produce log2-unit scores; e4m3 scores carry the tiles' scales
             constexpr bool kLog2Mod = var_softcap(VAR) || var_alibi(VAR);
             float smul = kLog2Mod ? 1.f : sl2;
             const float* fp8_sk = nullptr;
             if constexpr (VAR == kVarFp8) {
-                smul = sl2 * __ldg(p.fp8_sq + ((long long)w.b * p.Hq + w.hq) * p.fp8_nq + (w.m0 + t * kBlockM) / kBlockM);
+                smul = sl2 * __ldg(p.fp8_sq + ((long long)w.b * p.Hq + hq_t) * p.fp8_nq + (w.m0 + t * w.rstep) / kBlockM);
                 fp8_sk = p.fp8_sk + ((long long)w.b * p.Hkv + w.hkv) * p.fp8_nk + w.kf;
             }
             const float smul_q = smul;
@@ -884,14 +897,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0, tile = cta_tile<kAlternate>(0); tile < num_tiles; tile = cta_tile<kAlternate>(++k)) {
             const Work w = decode_tile<CAUSAL, VARLEN, VAR>(p, sb + SS::kOff, tile);
             for (int t = 0; t < 2; ++t) {
-                const int q_row = w.m0 + t * kBlockM + row;
+                const int q_row = w.m0 + t * w.rstep + row;
+                const int hq_t = w.hq + t * w.hstep;
                 const bool valid = q_row < w.lq;
                 int64_t orow, lidx;
                 if constexpr (VARLEN) {
-                    orow = ((int64_t)(w.q0 + q_row) * p.Hq + w.hq) * DV;
-                    lidx = (int64_t)w.hq * p.total_q + w.q0 + q_row;
+                    orow = ((int64_t)(w.q0 + q_row) * p.Hq + hq_t) * DV;
+                    lidx = (int64_t)hq_t * p.total_q + w.q0 + q_row;
                 } else {
-                    lidx = ((int64_t)w.b * p.Hq + w.hq) * p.Lq + q_row;
+                    lidx = ((int64_t)w.b * p.Hq + hq_t) * p.Lq + q_row;
                     orow = lidx * DV;
                 }
                 uint4* dst = reinterpret_cast<uint4*>(obase + orow);
@@ -920,10 +934,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // 32 scattered sectors per instruction).
                     const uint32_t stage = sb + L::kEpiOff + (uint32_t)((warp & 3) * L::kEpiWarpBytes);
                     const int rsub = lane >> 3, cq = lane & 7;  // row within a group of four, 16-byte column
-                    const int wrow0 = w.m0 + t * kBlockM + 32 * (warp & 3);
+                    const int wrow0 = w.m0 + t * w.rstep + 32 * (warp & 3);
                     const int64_t rstride = VARLEN ? (int64_t)p.Hq * DV : (int64_t)DV;
-                    float* wbase = obase + (VARLEN ? ((int64_t)(w.q0 + wrow0) * p.Hq + w.hq) * DV
-                                                   : (((int64_t)w.b * p.Hq + w.hq) * p.Lq + wrow0) * DV);
+                    float* wbase = obase + (VARLEN ? ((int64_t)(w.q0 + wrow0) * p.Hq + hq_t) * DV
+                                                   : (((int64_t)w.b * p.Hq + hq_t) * p.Lq + wrow0) * DV);
 #pragma unroll 1
                     for (int c = 0; c < DV / 32; ++c) {
                         uint32_t ov[32];
@@ -987,13 +1001,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(bar(L::kQFull + t), L::kQBytes);
                     q_armed[t] = (int)q_ph[t];  // parity of the phase this copy completes
                     const uint32_t dst = sb + L::kQOff + (uint32_t)(t * L::kQBytes);
-                    const int row0 = w.m0 + t * kBlockM;
+                    const int row0 = w.m0 + t * w.rstep;
 #pragma unroll
                     for (int h = 0; h < L::kHalvesQ; ++h) {
                         if constexpr (VARLEN)
-                            tma_load_3d(dst + h * L::kBlk, &tmQ, bar(L::kQFull + t), 64 * h, w.hq, w.zq + row0);
+                            tma_load_3d(dst + h * L::kBlk, &tmQ, bar(L::kQFull + t), 64 * h, w.hq + t * w.hstep,
+                                        w.zq + row0);
                         else
-                            tma_load_3d(dst + h * L::kBlk, &tmQ, bar(L::kQFull + t), 64 * h, row0, w.zq);
+                            tma_load_3d(dst + h * L::kBlk, &tmQ, bar(L::kQFull + t), 64 * h, row0,
+                                        w.zq + t * w.hstep);
                     }
                     return true;
                 };

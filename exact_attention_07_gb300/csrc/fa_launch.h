@@ -17,8 +17,8 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 
 // Builds the schedule of a variable-length batch into `sched`
 // (see FwdParams::sched) and validates the offsets.  heads = Hq for the
-// forward (bwd = 0), Hkv for the backward (bwd = 1, which also writes the
-// padded workspace row offsets).
+// forward (bwd = 0; bwd = 2 counts paired-head tiles of 128 rows), Hkv for
+// the backward (bwd = 1, which also writes the padded workspace row offsets).
 cudaError_t launch_varlen_schedule(const int* cu_q, const int* cu_k, int num_seqs, int total_q,
                                    int total_k, int max_q, int max_k, int heads, int bwd, int* sched, int* err,
                                    cudaStream_t stream);

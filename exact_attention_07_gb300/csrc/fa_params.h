@@ -14,6 +14,9 @@ struct FwdParams {
     float scale_log2;  // softmax_scale * log2(e)
     int heads_per_section;  // KV heads per L2-sized scheduling section
     int num_tiles;          // dense: number of work tiles
+    // 1: a work tile is two query heads of one KV head over the same 128 rows
+    // (causal, even GQA groups); 0: one query head over 256 rows
+    int pair_heads;
     // variable-length batches
     const int* cu_q;
     const int* cu_k;

@@ -612,7 +612,7 @@ void splitkv_plan(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_splits,
     pl->R = (Hq / Hkv) * Lq;
     pl->tensor = (D == 64 || D == 128) && pl->R >= 2;
     pl->rpt = decode_rows_per_thread(D, pl->R);
-    const int keys = pl->tensor ? kDecTcKeys : kDecKeys;
+    const int keys = pl->tensor ? decode_tc_keys(D) : kDecKeys;
     pl->num_tiles = (Lk + keys - 1) / keys;
     const int nkt = pl->num_tiles;
     const long long bh = (long long)B * Hkv;

@@ -51,10 +51,12 @@ cudaError_t launch_decode_partial(int D, int rows_per_thread, const CUtensorMap&
 
 cudaError_t launch_decode_merge(int D, const DecodeParams& p, cudaStream_t stream);
 
-// Tensor-core partials (D = 64 or 128, 2 <= R <= 16): 128-key tiles, one
+// Tensor-core partials (D = 64 or 128, 2 <= R <= 16): tiles of 16384 / D keys
+// (32 KB of K or of V), loaded as [128 keys][64 dimensions] boxes, one
 // persistent CTA per SM (grid <= SM count) walking the (batch, KV head,
 // partition) items.
-constexpr int kDecTcKeys = 128;
+constexpr int kDecTcKeys = 128;  // keys of one TMA box
+constexpr int decode_tc_keys(int D) { return 16384 / D; }
 cudaError_t launch_decode_tc(int D, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                              const DecodeParams& p, int grid, cudaStream_t stream);
 

@@ -9,10 +9,13 @@
 //     S^T [128 keys x 16 rows] = K_tile [128 x D] . Q^T [D x 16]
 //     O^T [D x 16 rows]       += V_tile^T [D x 128] . P^T [128 keys x 16]
 //
-// both accumulating in tensor memory.  With D = 64 the second product keeps
-// M = 128: the upper half of its A operand (dimensions 64..127) is a block of
-// zeros in shared memory, so tensor-memory lanes 64..127 accumulate zeros and
-// are never stored (decode is bound by streaming K and V, not by the MMA).
+// both accumulating in tensor memory.  With D = 64 a tile holds 256 keys (two
+// 128-key halves, each an S^T MMA of its own), so that a tile carries the same
+// 64 KB of K and V as at D = 128 for about the same fixed softmax work per
+// tile, and the second product keeps M = 128: the upper half of its A operand
+// (dimensions 64..127) is a block of zeros in shared memory, so tensor-memory
+// lanes 64..127 accumulate zeros and are never stored (decode is bound by
+// streaming K and V, not by the MMA).
 // The tensor core does the contraction
 // at a small fraction of its rate, so the kernel is bound by streaming K and
 // V from HBM; the FP32-pipe variant (fa_decode.cu) runs out of issue slots
@@ -46,21 +49,25 @@ namespace fa {
 
 namespace {
 
-constexpr int kTcKeys = 128;           // keys per tile (the MMA's M)
 constexpr int kTcRows = 16;            // packed query rows (the MMA's N)
 constexpr int kTcThreads = 192;
-constexpr int kHalfBytes = kTcKeys * 64 * 2;     // one 64-dimension box of a K/V tile: 16 KB
+constexpr int kHalfBytes = 128 * 64 * 2;         // one [128 keys][64 dimensions] box: 16 KB
 constexpr int kQBox = kTcRows * 64 * 2;          // one 64-dimension box of Q: 2 KB
-constexpr int kPBytes = kTcRows * kTcKeys * 2;   // 4 KB: P^T, two 64-key swizzle atoms
+constexpr int kPAtom = kTcRows * 128;            // P^T: one 64-key swizzle atom of the 16 rows, 2 KB
 
-// D = head dimension (64 or 128).  The ring holds 192 KB of K/V tiles either
-// way; D = 64 adds the zero block that pads the O^T MMA to M = 128.
+// D = head dimension (64 or 128).  A tile is kKeys = 16384 / D keys (32 KB of
+// K or of V), in kSub halves of 128 keys (the S^T MMA's M); the ring holds six
+// tiles (five at D = 64, which adds the zero block that pads the O^T MMA to
+// M = 128).
 template <int D>
 struct TcSmem {
-    static constexpr int kBoxes = D / 64;                  // 64-dimension boxes per row
-    static constexpr int kSlotBytes = kTcKeys * D * 2;     // one K or V tile
-    static constexpr int kNumSlots = 6 * 128 / D;          // K/V ring slots
+    static constexpr int kKeys = 16384 / D;                // keys per tile
+    static constexpr int kSub = kKeys / 128;               // 128-key halves of a tile
+    static constexpr int kBoxes = D / 64;                  // 64-dimension boxes per key row
+    static constexpr int kSlotBytes = kKeys * D * 2;       // one K or V tile: 32 KB
+    static constexpr int kNumSlots = D == 64 ? 5 : 6;      // K/V ring slots (D = 64: room for the zero block)
     static constexpr int kQBytes = kTcRows * D * 2;
+    static constexpr int kPBytes = kTcRows * kKeys * 2;    // P^T of one tile: kKeys / 64 atoms
     static constexpr int kSlots = 0;
     static constexpr int kZero = kSlots + kNumSlots * kSlotBytes;     // D = 64: 16 KB of zeros
     static constexpr int kQ = kZero + (D < 128 ? kHalfBytes : 0);  // [2] Q buffers
@@ -79,8 +86,12 @@ struct TcSmem {
     static_assert(kDynamic <= 232448, "shared memory of one CTA");
 };
 
-// TMEM columns: S^T double buffer, then O^T.
-constexpr uint32_t kColS = 0, kColO = 2 * kTcRows, kTmemCols = 64;
+// TMEM columns: S^T double buffer (kSub groups of 16 columns each), then O^T.
+template <int D>
+struct TcTmem {
+    static constexpr uint32_t kColS = 0, kColO = 2 * TcSmem<D>::kSub * kTcRows;
+    static constexpr uint32_t kCols = kColO + kTcRows <= 64 ? 64 : 128;  // allocation: a power of two >= 32
+};
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 {
@@ -185,6 +196,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 {
     using L = TcSmem<D>;
     constexpr int kTcSlots = L::kNumSlots, kSlotBytes = L::kSlotBytes, kQBytes = L::kQBytes;
+    constexpr int kKeys = L::kKeys, kSub = L::kSub, kPBytes = L::kPBytes;
+    constexpr uint32_t kColS = TcTmem<D>::kColS, kColO = TcTmem<D>::kColO, kTmemCols = TcTmem<D>::kCols;
     constexpr float kTau = 8.0f;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -268,21 +281,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t b = T & 1u, ph = (T >> 1) & 1u;
                 if (!tc_warp_wait(bar(L::bSFull + b), ph, abort_flag, wf, 60, it)) goto done;
                 tc_fence_after_sync();
-                float s[kTcRows];
-                tmem_ld16(lane_base + kColS + b * kTcRows, s);
+                // this thread's keys: k + 128 u of the tile, u < kSub
+                float s[kSub][kTcRows];
+#pragma unroll
+                for (int u = 0; u < kSub; ++u)
+                    tmem_ld16(lane_base + kColS + (b * kSub + u) * kTcRows, s[u]);
                 tmem_wait_ld();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::bSEmpty + b));
-                const int key_base = (w.t0 + t) * kTcKeys;
+                const int key_base = (w.t0 + t) * kKeys;
 #pragma unroll
-                for (int r = 0; r < kTcRows; ++r) s[r] *= p.scale_log2;
-                if (key_base + kTcKeys - 1 > lim_min) {  // tile reaches masked keys
+                for (int u = 0; u < kSub; ++u)
 #pragma unroll
-                    for (int r = 0; r < kTcRows; ++r)
-                        if (key_base + k > lim[r]) s[r] = -INFINITY;
+                    for (int r = 0; r < kTcRows; ++r) s[u][r] *= p.scale_log2;
+                if (key_base + kKeys - 1 > lim_min) {  // tile reaches masked keys
+#pragma unroll
+                    for (int u = 0; u < kSub; ++u)
+#pragma unroll
+                        for (int r = 0; r < kTcRows; ++r)
+                            if (key_base + 128 * u + k > lim[r]) s[u][r] = -INFINITY;
                 }
-                // tile maximum of every row over the 128 keys
-                const float wm = transpose_reduce16<true>(s, lane);
+                // tile maximum of every row over the tile's keys
+                float sm[kTcRows];
+#pragma unroll
+                for (int r = 0; r < kTcRows; ++r) {
+                    sm[r] = s[0][r];
+#pragma unroll
+                    for (int u = 1; u < kSub; ++u) sm[r] = fmaxf(sm[r], s[u][r]);
+                }
+                const float wm = transpose_reduce16<true>(sm, lane);
                 float* rb = red + b * 64;
                 if ((lane & 1) == 0) rb[warp * 16 + (lane >> 1)] = wm;
                 mbar_arrive(bar(L::bRed + b));
@@ -303,27 +330,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 // probabilities, rounded to bf16 for the MMA; both sums
-                uint32_t pk[kTcRows / 2];
+                uint32_t pk[kSub][kTcRows / 2];
 #pragma unroll
-                for (int r = 0; r < kTcRows; r += 2) {
-                    const float p0 = ref[r] == -INFINITY ? 0.f : ex2_approx(s[r] - ref[r]);
-                    const float p1 = ref[r + 1] == -INFINITY ? 0.f : ex2_approx(s[r + 1] - ref[r + 1]);
-                    __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                    pk[r / 2] = *reinterpret_cast<uint32_t*>(&h);
-                    lf[r] = fmaf(lf[r], alpha[r], p0);
-                    lf[r + 1] = fmaf(lf[r + 1], alpha[r + 1], p1);
-                    lb[r] = fmaf(lb[r], alpha[r], __uint_as_float(pk[r / 2] << 16));
-                    lb[r + 1] = fmaf(lb[r + 1], alpha[r + 1], __uint_as_float(pk[r / 2] & 0xffff0000u));
+                for (int r = 0; r < kTcRows; ++r) {
+                    lf[r] *= alpha[r];
+                    lb[r] *= alpha[r];
                 }
+#pragma unroll
+                for (int u = 0; u < kSub; ++u)
+#pragma unroll
+                    for (int r = 0; r < kTcRows; r += 2) {
+                        const float p0 = ref[r] == -INFINITY ? 0.f : ex2_approx(s[u][r] - ref[r]);
+                        const float p1 = ref[r + 1] == -INFINITY ? 0.f : ex2_approx(s[u][r + 1] - ref[r + 1]);
+                        __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+                        pk[u][r / 2] = *reinterpret_cast<uint32_t*>(&h);
+                        lf[r] += p0;
+                        lf[r + 1] += p1;
+                        lb[r] += __uint_as_float(pk[u][r / 2] << 16);
+                        lb[r + 1] += __uint_as_float(pk[u][r / 2] & 0xffff0000u);
+                    }
                 // P^T buffer b is free once P.V of tile T - 2 has completed
                 if (!tc_warp_wait(bar(L::bPEmpty + b), ph ^ 1u, abort_flag, wf, 62, it)) goto done;
-                {
-                    const uint32_t pb = sb + L::kP + b * kPBytes + (uint32_t)((k >> 6) * (kPBytes / 2)) +
-                                        (uint32_t)((k & 7) * 2);
-                    const int chunk = (k & 63) >> 3;
+#pragma unroll
+                for (int u = 0; u < kSub; ++u) {
+                    const int key = 128 * u + k;  // key of the tile: 64-key atom key / 64
+                    const uint32_t pb = sb + L::kP + b * kPBytes + (uint32_t)((key >> 6) * kPAtom) +
+                                        (uint32_t)((key & 7) * 2);
+                    const int chunk = (key & 63) >> 3;
 #pragma unroll
                     for (int r = 0; r < kTcRows; ++r) {
-                        const uint16_t h = (r & 1) ? (uint16_t)(pk[r / 2] >> 16) : (uint16_t)(pk[r / 2] & 0xffffu);
+                        const uint16_t h =
+                            (r & 1) ? (uint16_t)(pk[u][r / 2] >> 16) : (uint16_t)(pk[u][r / 2] & 0xffffu);
                         sts16(pb + (uint32_t)(r * 128 + ((chunk ^ (r & 7)) << 4)), h);
                     }
                 }
@@ -404,9 +441,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive_expect_tx(bar(L::bKVFull + stage), kSlotBytes);
                     kv_armed[stage] = (int)kv_ph;
                     const uint32_t dst = sb + L::kSlots + (uint32_t)(stage * kSlotBytes);
+                    // two [128 keys][64 dimensions] boxes: the dimension halves
+                    // (D = 128) or the key halves (D = 64, 256 keys)
 #pragma unroll
-                    for (int h = 0; h < L::kBoxes; ++h)
-                        tma_load_3d(dst + h * kHalfBytes, map, bar(L::bKVFull + stage), 64 * h, key0, bh);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d(dst + h * kHalfBytes, map, bar(L::bKVFull + stage), L::kSub == 1 ? 64 * h : 0,
+                                    L::kSub == 1 ? key0 : key0 + 128 * h, bh);
                 }
                 if (++stage == kTcSlots) {
                     stage = 0;
@@ -427,7 +467,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tma_load_3d(qdst + h * kQBox, &tmQ, bar(L::bQFull + qb), 64 * h, (int)w.row0, 0);
                 bool ok = true;
                 for (int t = 0; t < w.n && ok; ++t) {
-                    const int key0 = (w.t0 + t) * kTcKeys;
+                    const int key0 = (w.t0 + t) * kKeys;
                     ok = load(&tmK, key0, w.bh, it) && load(&tmV, key0, w.bh, it);
                 }
                 if (!ok) break;
@@ -443,7 +483,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ============================================================ MMA issuer (warp 5)
         const bool leader = lane == 0;
         const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
-        constexpr uint32_t kIdescS = idesc_bf16_f32(kTcKeys, kTcRows, false);
+        constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTcRows, false);
         // O^T keeps M = 128 (D = 64: the upper half of A is the zero block)
         constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kTcRows, false) | (1u << 15);  // A (V^T) MN-major
         int stage = 0;
@@ -471,8 +511,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t pd = smem_desc_sw128(sb + L::kP + bp * kPBytes, 16, 1024);
             if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                    const uint64_t poff = (uint64_t)(((kk >> 2) * (kPBytes / 2) + (kk & 3) * 32) >> 4);
+                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                    const uint64_t poff = (uint64_t)(((kk >> 2) * kPAtom + (kk & 3) * 32) >> 4);
                     mma_ss(tm + kColO, vd + (uint64_t)((kk * 16 * 128) >> 4), pd + poff, kIdescPV,
                            (first && kk == 0) ? 0u : 1u);
                 }
@@ -503,12 +543,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_after_sync();
                 const uint64_t kd = smem_desc_sw128(sb + L::kSlots + (uint32_t)(ks * kSlotBytes), 16, 1024);
                 if (leader) {
+                    // S^T of each 128-key half: keys on the MMA's M, D/16 steps of K
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t koff = (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
-                        const uint64_t qoff = (uint64_t)(((kk >> 2) * kQBox + (kk & 3) * 32) >> 4);
-                        mma_ss(tm + kColS + b * kTcRows, kd + koff, qd + qoff, kIdescS, kk > 0 ? 1u : 0u);
-                    }
+                    for (int u = 0; u < kSub; ++u)
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t koff =
+                                (uint64_t)((u * kHalfBytes + (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+                            const uint64_t qoff = (uint64_t)(((kk >> 2) * kQBox + (kk & 3) * 32) >> 4);
+                            mma_ss(tm + kColS + (b * kSub + u) * kTcRows, kd + koff, qd + qoff, kIdescS,
+                                   kk > 0 ? 1u : 0u);
+                        }
                 }
                 __syncwarp();
                 issued = true;

@@ -74,6 +74,11 @@ def dist_env():
 FALLBACK_HBM_GBS = 6800.0
 
 
+def decode_rows(R):
+    """Query rows the tensor-core decode kernel's softmax carries for R packed rows."""
+    return 4 if R <= 4 else 8 if R <= 8 else 16
+
+
 def measured_hbm():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -716,7 +721,8 @@ def main(argv=None):
                     "traffic": profiled_traffic(w.name, DECODE_SOURCES, "fa_decode"),
                     "peak_kind": f"{hbm_kind} HBM copy",
                     "algorithmic_bytes_per_step": w.hbm_bytes(), "splits": n_splits,
-                    "kernel": ("fa_decode_tc_kernel<%d>" % w.D if w.Hq // w.Hkv * w.Lq >= 2
+                    "kernel": ("fa_decode_tc_kernel<%d,%d>" % (w.D, decode_rows(w.Hq // w.Hkv * w.Lq))
+                               if w.Hq // w.Hkv * w.Lq >= 2
                                else "fa_decode_partial_kernel<%d,*>" % w.D) + " + fa_decode_merge_kernel<%d>" % w.D,
                     "timed": "whole step (both launches)"}
     elif w.fp8:

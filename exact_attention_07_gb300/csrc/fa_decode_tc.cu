@@ -12,25 +12,33 @@
 // both accumulating in tensor memory.  With D = 64 a tile holds 256 keys (two
 // 128-key halves, each an S^T MMA of its own), so that a tile carries the same
 // 64 KB of K and V as at D = 128 for about the same fixed softmax work per
-// tile, and the second product keeps M = 128: the upper half of its A operand
-// (dimensions 64..127) is a block of zeros in shared memory, so tensor-memory
-// lanes 64..127 accumulate zeros and are never stored (decode is bound by
-// streaming K and V, not by the MMA).
+// tile.  The second product then takes both halves in one MMA of M = 128,
+// N = 32: A stacks V^T of the first half (dimensions on rows 0..63) over V^T
+// of the second (rows 64..127), B puts P^T of the first half in columns 0..15
+// and of the second in 16..31, and O^T is the sum of the two diagonal 64 x 16
+// quadrants of the accumulator (the other two are cross terms, never read).
+// A tile then takes 8 + 8 MMAs at either head dimension: each tcgen05.mma of
+// these small shapes costs the issuing warp about 100 cycles here, which is
+// what bounded a 256-key tile with 16 separate 16-key products.
 // The tensor core does the contraction
 // at a small fraction of its rate, so the kernel is bound by streaming K and
 // V from HBM; the FP32-pipe variant (fa_decode.cu) runs out of issue slots
 // first once R reaches 4.
 //
-// Roles (192 threads, one persistent CTA per SM, work items = (batch, KV
+// Roles (224 threads, one persistent CTA per SM, work items = (batch, KV
 // head, key partition) in a strided order):
-//   warps 0-3  softmax: thread k owns TMEM lane k -- key k of the tile for
-//              S^T, output dimension k for O^T.  Row maxima across the 128
-//              keys go through a transposing warp reduction and a four-warp
-//              exchange in shared memory; P^T is written to shared memory in
-//              the operand layout; O^T is rescaled in place when a row's
-//              reference moves; the epilogue normalises and stores.
+//   warps 0-3  softmax: thread k owns TMEM lane k -- key k of each 128-key
+//              half for S^T, output dimension k for O^T (D = 64: threads
+//              64..127 hold the second half's partial sums of dimension
+//              k - 64, added in the epilogue).  Row maxima across the keys go
+//              through a transposing warp reduction and a four-warp exchange
+//              in shared memory; P^T is written to shared memory in the
+//              operand layout; O^T is rescaled in place when a row's
+//              reference moves; the epilogue normalises and stores.  Only the
+//              first NR >= R of the 16 MMA columns are carried.
 //   warp  4    TMA producer: Q rows of the item, then K and V tiles in a ring.
-//   warp  5    MMA issuer and tensor-memory owner.
+//   warp  5    S^T MMA issuer and tensor-memory owner.
+//   warp  6    O^T MMA issuer.
 // The online-softmax state follows the dense kernel: base-2 exponentials,
 // a per-row reference r that moves only when a tile maximum exceeds it by
 // more than 8, the bf16-rounded probability sum to normalise O and the fp32
@@ -50,75 +58,105 @@ namespace fa {
 namespace {
 
 constexpr int kTcRows = 16;            // packed query rows (the MMA's N)
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;
 constexpr int kHalfBytes = 128 * 64 * 2;         // one [128 keys][64 dimensions] box: 16 KB
 constexpr int kQBox = kTcRows * 64 * 2;          // one 64-dimension box of Q: 2 KB
-constexpr int kPAtom = kTcRows * 128;            // P^T: one 64-key swizzle atom of the 16 rows, 2 KB
 
 // D = head dimension (64 or 128).  A tile is kKeys = 16384 / D keys (32 KB of
 // K or of V), in kSub halves of 128 keys (the S^T MMA's M); the ring holds six
-// tiles (five at D = 64, which adds the zero block that pads the O^T MMA to
-// M = 128).
+// tiles.  P^T is stored as 64-key swizzle atoms of kSub * 16 rows (row
+// 16 u + r: query row r of half u), so that the O^T MMA reads both halves'
+// probabilities as one operand of N = kSub * 16 columns.
 template <int D>
 struct TcSmem {
     static constexpr int kKeys = 16384 / D;                // keys per tile
     static constexpr int kSub = kKeys / 128;               // 128-key halves of a tile
     static constexpr int kBoxes = D / 64;                  // 64-dimension boxes per key row
     static constexpr int kSlotBytes = kKeys * D * 2;       // one K or V tile: 32 KB
-    static constexpr int kNumSlots = D == 64 ? 5 : 6;      // K/V ring slots (D = 64: room for the zero block)
+    static constexpr int kNumSlots = 6;                    // K/V ring slots
     static constexpr int kQBytes = kTcRows * D * 2;
-    static constexpr int kPBytes = kTcRows * kKeys * 2;    // P^T of one tile: kKeys / 64 atoms
+    static constexpr int kPAtom = kSub * kTcRows * 128;    // P^T: one 64-key atom of kSub * 16 rows
+    static constexpr int kPBytes = 2 * kPAtom;             // P^T of one tile: two atoms
     static constexpr int kSlots = 0;
-    static constexpr int kZero = kSlots + kNumSlots * kSlotBytes;     // D = 64: 16 KB of zeros
-    static constexpr int kQ = kZero + (D < 128 ? kHalfBytes : 0);  // [2] Q buffers
+    static constexpr int kQ = kSlots + kNumSlots * kSlotBytes;       // [2] Q buffers
     static constexpr int kP = kQ + 2 * kQBytes;                      // [2] P^T buffers
     static constexpr int kRed = kP + 2 * kPBytes;              // float [2][4][16] row maxima
     static constexpr int kEpi = kRed + 2 * 4 * 16 * 4;         // float [4][32] row sums
-    static constexpr int kBars = kEpi + 4 * 32 * 4;
+    static constexpr int kSum = kEpi + 4 * 32 * 4;             // D = 64: float [16][64] second-half O^T
+    static constexpr int kBars = kSum + (kSub == 2 ? kTcRows * 64 * 4 : 0);
     // barrier slots
     static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kNumSlots;
     static constexpr int bSFull = 4 + 2 * kNumSlots, bSEmpty = bSFull + 2, bPFull = bSFull + 4,
                          bPEmpty = bSFull + 6, bOFull = bSFull + 8, bOEmpty = bSFull + 9,
-                         bRed = bSFull + 10, bEpi = bSFull + 12, bDrain = bSFull + 13, kNumBars = bSFull + 14;
+                         bRed = bSFull + 10, bEpi = bSFull + 12, bDrain = bSFull + 13, kNumBars = bSFull + 15;
     static constexpr int kMisc = kBars + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kDynamic = kBytes + 1024;
     static_assert(kDynamic <= 232448, "shared memory of one CTA");
 };
 
-// TMEM columns: S^T double buffer (kSub groups of 16 columns each), then O^T.
+// TMEM columns: S^T double buffer (kSub groups of 16 columns each), then O^T
+// (kSub groups of 16: at D = 64 lanes 0..63 of the first and lanes 64..127 of
+// the second hold the two halves' partial sums).
 template <int D>
 struct TcTmem {
     static constexpr uint32_t kColS = 0, kColO = 2 * TcSmem<D>::kSub * kTcRows;
-    static constexpr uint32_t kCols = kColO + kTcRows <= 64 ? 64 : 128;  // allocation: a power of two >= 32
+    static constexpr uint32_t kCols = kColO + TcSmem<D>::kSub * kTcRows <= 64 ? 64 : 128;  // a power of two >= 32
 };
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+// tcgen05.ld / st of N = 4, 8 or 16 consecutive columns of this warp's 32 lanes.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N])
 {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
+    uint32_t r[N];
+    if constexpr (N == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(taddr)
+                     : "memory");
+    } else if constexpr (N == 8) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                       "=r"(r[7])
+                     : "r"(taddr)
+                     : "memory");
+    } else {
+        static_assert(N == 16, "4, 8 or 16 columns");
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+            "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr)
+            : "memory");
+    }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float (&v)[N])
 {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15]))
-        : "memory");
+    uint32_t r[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) r[i] = __float_as_uint(v[i]);
+    if constexpr (N == 4) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]),
+                     "r"(r[1]), "r"(r[2]), "r"(r[3])
+                     : "memory");
+    } else if constexpr (N == 8) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                     : "memory");
+    } else {
+        static_assert(N == 16, "4, 8 or 16 columns");
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+            "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+            "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+            "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+            : "memory");
+    }
 }
 
 // Generic-proxy shared-memory writes become visible to the tensor core's
@@ -140,34 +178,31 @@ __device__ __forceinline__ bool tc_warp_wait(uint32_t bar, uint32_t parity, vola
     return __all_sync(0xffffffffu, ok);
 }
 
-// Reduces 16 per-lane values (one per query row) across the warp with a
-// transposing butterfly: each exchange halves the rows a lane carries, so
-// 16 + 8 + 4 + 2 + 1 values cross lanes instead of 16 * 5.  Returns, in
-// every lane, the reduction of row (lane >> 1) over all 32 lanes.
-template <bool MAX>
-__device__ __forceinline__ float transpose_reduce16(const float (&v)[16], int lane)
+// Reduces N per-lane values (one per query row, N = 4, 8 or 16) across the
+// warp with a transposing butterfly: each exchange halves the rows a lane
+// carries, so N + N/2 + ... values cross lanes instead of N * 5.  Returns, in
+// every lane, the reduction of row lane / (32 / N) over all 32 lanes.
+template <bool MAX, int N>
+__device__ __forceinline__ float transpose_reduce(const float (&v)[N], int lane)
 {
     auto op = [](float a, float b) { return MAX ? fmaxf(a, b) : a + b; };
-    float a[8], b[4], c[2];
-    const bool h4 = lane & 16, h3 = lane & 8, h2 = lane & 4, h1 = lane & 2;
+    float c[N];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float send = h4 ? v[i] : v[i + 8], keep = h4 ? v[i + 8] : v[i];
-        a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-    }
+    for (int i = 0; i < N; ++i) c[i] = v[i];
+    int mask = 16;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float send = h3 ? a[i] : a[i + 4], keep = h3 ? a[i + 4] : a[i];
-        b[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-    }
+    for (int w = N; w > 1; w >>= 1, mask >>= 1) {
+        const bool upper = lane & mask;  // this lane keeps the upper half of the rows it carries
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = h2 ? b[i] : b[i + 2], keep = h2 ? b[i + 2] : b[i];
-        c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+        for (int i = 0; i < w / 2; ++i) {
+            const float send = upper ? c[i] : c[i + w / 2], keep = upper ? c[i + w / 2] : c[i];
+            c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, mask));
+        }
     }
-    const float send = h1 ? c[0] : c[1], keep = h1 ? c[1] : c[0];
-    float d = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-    return op(d, __shfl_xor_sync(0xffffffffu, d, 1));
+    float d = c[0];
+#pragma unroll
+    for (; mask >= 1; mask >>= 1) d = op(d, __shfl_xor_sync(0xffffffffu, d, mask));
+    return d;
 }
 
 struct TcItem {
@@ -189,16 +224,19 @@ __device__ __forceinline__ TcItem tc_item(const DecodeParams& p, int it)
 
 }  // namespace
 
-template <int D>
+// NR = query rows the softmax carries (4, 8 or 16 >= R); the MMAs keep N = 16,
+// and the rows of P^T past NR stay zero.
+template <int D, int NR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p)
 {
     using L = TcSmem<D>;
     constexpr int kTcSlots = L::kNumSlots, kSlotBytes = L::kSlotBytes, kQBytes = L::kQBytes;
-    constexpr int kKeys = L::kKeys, kSub = L::kSub, kPBytes = L::kPBytes;
+    constexpr int kKeys = L::kKeys, kSub = L::kSub, kPBytes = L::kPBytes, kPAtom = L::kPAtom;
     constexpr uint32_t kColS = TcTmem<D>::kColS, kColO = TcTmem<D>::kColO, kTmemCols = TcTmem<D>::kCols;
     constexpr float kTau = 8.0f;
+    constexpr int kLanesPerRow = 32 / NR;  // lanes that end a transposing reduction with the same row
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
@@ -230,6 +268,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(bar(L::bOEmpty), 128);
         mbar_init(bar(L::bEpi), 128);
         mbar_init(bar(L::bDrain), 1);
+        mbar_init(bar(L::bDrain + 1), 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -242,10 +281,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
-    if constexpr (D < 128) {
-        // the zero half of the O^T MMA's A operand, visible to the tensor core
-        uint4* z = reinterpret_cast<uint4*>(smem + L::kZero);
-        for (int i = threadIdx.x; i < kHalfBytes / 16; i += kTcThreads) z[i] = make_uint4(0, 0, 0, 0);
+    if constexpr (NR < kTcRows) {
+        // P^T rows NR..15 are never written: zeros for the O^T MMA
+        uint4* z = reinterpret_cast<uint4*>(smem + L::kP);
+        for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += kTcThreads) z[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     tc_fence_before_sync();
@@ -257,12 +296,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ============================================================ softmax
         const int k = threadIdx.x;  // TMEM lane: key of the tile / output dimension
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        // this thread's O^T columns: D = 64 warps 2-3 hold the second half's partial sums
+        const uint32_t col_o = kColO + (kSub == 2 && warp >= 2 ? (uint32_t)kTcRows : 0u);
         const int causal_off = p.Lk - p.Lq;
         // last key each row may see (bottom-right causal alignment, padding at Lk)
-        int lim[kTcRows];
+        int lim[NR];
         int lim_min = p.Lk - 1;
 #pragma unroll
-        for (int r = 0; r < kTcRows; ++r) {
+        for (int r = 0; r < NR; ++r) {
             lim[r] = p.causal ? min(p.Lk - 1, (r % p.Lq) + causal_off) : p.Lk - 1;
             if (r < p.R) lim_min = min(lim_min, lim[r]);
         }
@@ -270,9 +311,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int I = 0;
         for (int it = blockIdx.x; it < num_items; it += gridDim.x, ++I) {
             const TcItem w = tc_item(p, it);
-            float ref[kTcRows], lf[kTcRows], lb[kTcRows];
+            float ref[NR], lf[NR], lb[NR];
 #pragma unroll
-            for (int r = 0; r < kTcRows; ++r) {
+            for (int r = 0; r < NR; ++r) {
                 ref[r] = -INFINITY;
                 lf[r] = 0.f;
                 lb[r] = 0.f;
@@ -282,10 +323,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!tc_warp_wait(bar(L::bSFull + b), ph, abort_flag, wf, 60, it)) goto done;
                 tc_fence_after_sync();
                 // this thread's keys: k + 128 u of the tile, u < kSub
-                float s[kSub][kTcRows];
+                float s[kSub][NR];
 #pragma unroll
                 for (int u = 0; u < kSub; ++u)
-                    tmem_ld16(lane_base + kColS + (b * kSub + u) * kTcRows, s[u]);
+                    tmem_ld_cols<NR>(lane_base + kColS + (b * kSub + u) * kTcRows, s[u]);
                 tmem_wait_ld();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::bSEmpty + b));
@@ -293,34 +334,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int u = 0; u < kSub; ++u)
 #pragma unroll
-                    for (int r = 0; r < kTcRows; ++r) s[u][r] *= p.scale_log2;
+                    for (int r = 0; r < NR; ++r) s[u][r] *= p.scale_log2;
                 if (key_base + kKeys - 1 > lim_min) {  // tile reaches masked keys
 #pragma unroll
                     for (int u = 0; u < kSub; ++u)
 #pragma unroll
-                        for (int r = 0; r < kTcRows; ++r)
+                        for (int r = 0; r < NR; ++r)
                             if (key_base + 128 * u + k > lim[r]) s[u][r] = -INFINITY;
                 }
                 // tile maximum of every row over the tile's keys
-                float sm[kTcRows];
+                float sm[NR];
 #pragma unroll
-                for (int r = 0; r < kTcRows; ++r) {
+                for (int r = 0; r < NR; ++r) {
                     sm[r] = s[0][r];
 #pragma unroll
                     for (int u = 1; u < kSub; ++u) sm[r] = fmaxf(sm[r], s[u][r]);
                 }
-                const float wm = transpose_reduce16<true>(sm, lane);
+                const float wm = transpose_reduce<true>(sm, lane);
                 float* rb = red + b * 64;
-                if ((lane & 1) == 0) rb[warp * 16 + (lane >> 1)] = wm;
+                if (lane % kLanesPerRow == 0) rb[warp * 16 + lane / kLanesPerRow] = wm;
                 mbar_arrive(bar(L::bRed + b));
                 if (!tc_warp_wait(bar(L::bRed + b), ph, abort_flag, wf, 61, it)) goto done;
                 float tm_lane = -INFINITY;
-                if (lane < 16)
+                if (lane < NR)
                     tm_lane = fmaxf(fmaxf(rb[lane], rb[16 + lane]), fmaxf(rb[32 + lane], rb[48 + lane]));
-                float alpha[kTcRows];
+                float alpha[NR];
                 bool moved = false;
 #pragma unroll
-                for (int r = 0; r < kTcRows; ++r) {
+                for (int r = 0; r < NR; ++r) {
                     const float tm = __shfl_sync(0xffffffffu, tm_lane, r);
                     alpha[r] = 1.f;
                     if (tm > ref[r] + kTau) {  // also when ref is still -inf and the tile has a key
@@ -330,16 +371,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 // probabilities, rounded to bf16 for the MMA; both sums
-                uint32_t pk[kSub][kTcRows / 2];
+                uint32_t pk[kSub][NR / 2];
 #pragma unroll
-                for (int r = 0; r < kTcRows; ++r) {
+                for (int r = 0; r < NR; ++r) {
                     lf[r] *= alpha[r];
                     lb[r] *= alpha[r];
                 }
 #pragma unroll
                 for (int u = 0; u < kSub; ++u)
 #pragma unroll
-                    for (int r = 0; r < kTcRows; r += 2) {
+                    for (int r = 0; r < NR; r += 2) {
                         const float p0 = ref[r] == -INFINITY ? 0.f : ex2_approx(s[u][r] - ref[r]);
                         const float p1 = ref[r + 1] == -INFINITY ? 0.f : ex2_approx(s[u][r + 1] - ref[r + 1]);
                         __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
@@ -351,18 +392,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 // P^T buffer b is free once P.V of tile T - 2 has completed
                 if (!tc_warp_wait(bar(L::bPEmpty + b), ph ^ 1u, abort_flag, wf, 62, it)) goto done;
+                {
+                    // key k of each half: atom k / 64, operand row 16 u + r
+                    const uint32_t pb = sb + L::kP + b * kPBytes + (uint32_t)((k >> 6) * kPAtom) +
+                                        (uint32_t)((k & 7) * 2);
+                    const int chunk = (k & 63) >> 3;
 #pragma unroll
-                for (int u = 0; u < kSub; ++u) {
-                    const int key = 128 * u + k;  // key of the tile: 64-key atom key / 64
-                    const uint32_t pb = sb + L::kP + b * kPBytes + (uint32_t)((key >> 6) * kPAtom) +
-                                        (uint32_t)((key & 7) * 2);
-                    const int chunk = (key & 63) >> 3;
+                    for (int u = 0; u < kSub; ++u)
 #pragma unroll
-                    for (int r = 0; r < kTcRows; ++r) {
-                        const uint16_t h =
-                            (r & 1) ? (uint16_t)(pk[u][r / 2] >> 16) : (uint16_t)(pk[u][r / 2] & 0xffffu);
-                        sts16(pb + (uint32_t)(r * 128 + ((chunk ^ (r & 7)) << 4)), h);
-                    }
+                        for (int r = 0; r < NR; ++r) {
+                            const uint16_t h =
+                                (r & 1) ? (uint16_t)(pk[u][r / 2] >> 16) : (uint16_t)(pk[u][r / 2] & 0xffffu);
+                            sts16(pb + (uint32_t)((16 * u + r) * 128 + ((chunk ^ (r & 7)) << 4)), h);
+                        }
                 }
                 fence_proxy_async_smem();
                 if (moved && t > 0) {
@@ -370,12 +412,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t bp = (T - 1) & 1u, php = ((T - 1) >> 1) & 1u;
                     if (!tc_warp_wait(bar(L::bPEmpty + bp), php, abort_flag, wf, 63, it)) goto done;
                     tc_fence_after_sync();
-                    float o[kTcRows];
-                    tmem_ld16(lane_base + kColO, o);
+                    float o[NR];
+                    tmem_ld_cols<NR>(lane_base + col_o, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int r = 0; r < kTcRows; ++r) o[r] *= alpha[r];
-                    tmem_st16(lane_base + kColO, o);
+                    for (int r = 0; r < NR; ++r) o[r] *= alpha[r];
+                    tmem_st_cols<NR>(lane_base + col_o, o);
                     tmem_wait_st();
                 }
                 tc_fence_before_sync();
@@ -384,25 +426,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // ---- epilogue of the item: O = O^T / l_rounded, LSE = r + log2(l)
             if (!tc_warp_wait(bar(L::bOFull), (uint32_t)(I & 1), abort_flag, wf, 64, it)) goto done;
             tc_fence_after_sync();
-            float o[kTcRows];
-            tmem_ld16(lane_base + kColO, o);
+            float o[NR];
+            tmem_ld_cols<NR>(lane_base + col_o, o);
             tmem_wait_ld();
             tc_fence_before_sync();
             mbar_arrive(bar(L::bOEmpty));
+            float* osum = reinterpret_cast<float*>(smem + L::kSum);
+            if (kSub == 2 && k >= 64) {
+#pragma unroll
+                for (int r = 0; r < NR; ++r) osum[r * 64 + (k - 64)] = o[r];
+            }
             {
-                const float sb_w = transpose_reduce16<false>(lb, lane);
-                const float sf_w = transpose_reduce16<false>(lf, lane);
-                if ((lane & 1) == 0) {
-                    epi[warp * 32 + (lane >> 1)] = sb_w;
-                    epi[warp * 32 + 16 + (lane >> 1)] = sf_w;
+                const float sb_w = transpose_reduce<false>(lb, lane);
+                const float sf_w = transpose_reduce<false>(lf, lane);
+                if (lane % kLanesPerRow == 0) {
+                    epi[warp * 32 + lane / kLanesPerRow] = sb_w;
+                    epi[warp * 32 + 16 + lane / kLanesPerRow] = sf_w;
                 }
             }
             mbar_arrive(bar(L::bEpi));
             if (!tc_warp_wait(bar(L::bEpi), (uint32_t)(I & 1), abort_flag, wf, 65, it)) goto done;
             const float lsum = epi[lane] + epi[32 + lane] + epi[64 + lane] + epi[96 + lane];  // lane<16: rounded, else fp32
+            if (kSub == 2 && k < 64) {
+#pragma unroll
+                for (int r = 0; r < NR; ++r) o[r] += osum[r * 64 + k];
+            }
             const bool single = p.num_splits == 1;
 #pragma unroll
-            for (int r = 0; r < kTcRows; ++r) {
+            for (int r = 0; r < NR; ++r) {
                 const float l_r = __shfl_sync(0xffffffffu, lsum, r);
                 const float lf_r = __shfl_sync(0xffffffffu, lsum, 16 + r);
                 if (r < p.R) {
@@ -480,102 +531,102 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else {
-        // ============================================================ MMA issuer (warp 5)
+        // ============================================================ MMA issuers
+        // Warp 5 issues S^T, warp 6 the O^T update: each tcgen05.mma of these
+        // shapes takes about as long to issue as to run, and a tile needs
+        // 8 + 16 of them at D = 64.  K(T) and V(T) are loads 2T and 2T + 1 of
+        // the ring.
         const bool leader = lane == 0;
         const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
-        constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTcRows, false);
-        // O^T keeps M = 128 (D = 64: the upper half of A is the zero block)
-        constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kTcRows, false) | (1u << 15);  // A (V^T) MN-major
-        int stage = 0;
-        uint32_t kv_ph = 0;
-        uint32_t T = 0;
-        bool issued = false;
+        const bool s_warp = warp == 5;
+        auto ring = [&](uint32_t n, int& slot, uint32_t& ph) {
+            slot = (int)(n % (uint32_t)kTcSlots);
+            ph = (n / (uint32_t)kTcSlots) & 1u;
+        };
         auto commit = [&](int b) {
             if (leader) tc_commit(bar(b));
             __syncwarp();
         };
-        // O^T (+)= V^T P^T for tile Tp; V in slot vs (phase vph)
-        auto pv = [&](uint32_t Tp, int vs, uint32_t vph, bool first, int I, int it) -> bool {
-            const uint32_t bp = Tp & 1u;
-            if (!tc_warp_wait(bar(L::bKVFull + vs), vph, abort_flag, wf, 70, it)) return false;
-            if (!tc_warp_wait(bar(L::bPFull + bp), (Tp >> 1) & 1u, abort_flag, wf, 71, it)) return false;
-            if (first && !tc_warp_wait(bar(L::bOEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 72, it))
-                return false;
-            tc_fence_after_sync();
-            // A = V^T, MN-major: dimensions 64..127 are kHalfBytes further on, or
-            // (D = 64) in the zero block after the ring
-            const uint32_t vaddr = sb + L::kSlots + (uint32_t)(vs * kSlotBytes);
-            const uint32_t hi = D < 128 ? (uint32_t)L::kZero - (uint32_t)(L::kSlots + vs * kSlotBytes)
-                                        : (uint32_t)kHalfBytes;
-            const uint64_t vd = smem_desc_sw128(vaddr, hi, 1024);
-            const uint64_t pd = smem_desc_sw128(sb + L::kP + bp * kPBytes, 16, 1024);
-            if (leader) {
-#pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    const uint64_t poff = (uint64_t)(((kk >> 2) * kPAtom + (kk & 3) * 32) >> 4);
-                    mma_ss(tm + kColO, vd + (uint64_t)((kk * 16 * 128) >> 4), pd + poff, kIdescPV,
-                           (first && kk == 0) ? 0u : 1u);
-                }
-            }
-            __syncwarp();
-            commit(L::bPEmpty + bp);
-            commit(L::bKVEmpty + vs);
-            return true;
-        };
+        uint32_t T = 0;
+        bool issued = false, ok = true;
         int I = 0;
-        bool ok = true;
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++I) {
             const TcItem w = tc_item(p, it);
             const int qb = I & 1;
-            if (!tc_warp_wait(bar(L::bQFull + qb), (uint32_t)((I >> 1) & 1), abort_flag, wf, 73, it)) break;
-            const uint64_t qd = smem_desc_sw128(sb + L::kQ + (uint32_t)(qb * kQBytes), 16, 1024);
-            int vs_prev = 0;
-            uint32_t vph_prev = 0;
-            for (int t = 0; t < w.n; ++t, ++T) {
-                const int ks = stage;
-                if (!(ok = tc_warp_wait(bar(L::bKVFull + ks), kv_ph, abort_flag, wf, 74, it))) break;
-                if (++stage == kTcSlots) {
-                    stage = 0;
-                    kv_ph ^= 1u;
+            if (s_warp) {
+                constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTcRows, false);
+                if (!tc_warp_wait(bar(L::bQFull + qb), (uint32_t)((I >> 1) & 1), abort_flag, wf, 73, it)) break;
+                const uint64_t qd = smem_desc_sw128(sb + L::kQ + (uint32_t)(qb * kQBytes), 16, 1024);
+                for (int t = 0; t < w.n; ++t, ++T) {
+                    int ks;
+                    uint32_t kph;
+                    ring(2 * T, ks, kph);
+                    const uint32_t b = T & 1u;
+                    if (!(ok = tc_warp_wait(bar(L::bKVFull + ks), kph, abort_flag, wf, 74, it))) break;
+                    if (!(ok = tc_warp_wait(bar(L::bSEmpty + b), ((T >> 1) & 1u) ^ 1u, abort_flag, wf, 75, it)))
+                        break;
+                    tc_fence_after_sync();
+                    const uint64_t kd = smem_desc_sw128(sb + L::kSlots + (uint32_t)(ks * kSlotBytes), 16, 1024);
+                    if (leader) {
+                        // S^T of each 128-key half: keys on the MMA's M, D/16 steps of K
+#pragma unroll
+                        for (int u = 0; u < kSub; ++u)
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint64_t koff =
+                                    (uint64_t)((u * kHalfBytes + (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+                                const uint64_t qoff = (uint64_t)(((kk >> 2) * kQBox + (kk & 3) * 32) >> 4);
+                                mma_ss(tm + kColS + (b * kSub + u) * kTcRows, kd + koff, qd + qoff, kIdescS,
+                                       kk > 0 ? 1u : 0u);
+                            }
+                    }
+                    __syncwarp();
+                    issued = true;
+                    commit(L::bSFull + b);
+                    commit(L::bKVEmpty + ks);
+                    if (t == w.n - 1) commit(L::bQEmpty + qb);
                 }
-                const uint32_t b = T & 1u;
-                if (!(ok = tc_warp_wait(bar(L::bSEmpty + b), ((T >> 1) & 1u) ^ 1u, abort_flag, wf, 75, it))) break;
-                tc_fence_after_sync();
-                const uint64_t kd = smem_desc_sw128(sb + L::kSlots + (uint32_t)(ks * kSlotBytes), 16, 1024);
-                if (leader) {
-                    // S^T of each 128-key half: keys on the MMA's M, D/16 steps of K
+            } else {
+                // A (V^T) MN-major; N = 32 at D = 64 (both key halves)
+                constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kSub * kTcRows, false) | (1u << 15);
+                for (int t = 0; t < w.n; ++t, ++T) {
+                    int vs;
+                    uint32_t vph;
+                    ring(2 * T + 1, vs, vph);
+                    const uint32_t bp = T & 1u;
+                    if (!(ok = tc_warp_wait(bar(L::bKVFull + vs), vph, abort_flag, wf, 70, it))) break;
+                    if (!(ok = tc_warp_wait(bar(L::bPFull + bp), (T >> 1) & 1u, abort_flag, wf, 71, it))) break;
+                    if (t == 0 &&
+                        !(ok = tc_warp_wait(bar(L::bOEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 72, it)))
+                        break;
+                    tc_fence_after_sync();
+                    // A = V^T, MN-major, 16 keys (2 KB) per step; rows 64..127 are the
+                    // second box, 16 KB on: dimensions 64..127 (D = 128) or keys
+                    // 128..255 (D = 64)
+                    const uint64_t vd =
+                        smem_desc_sw128(sb + L::kSlots + (uint32_t)(vs * kSlotBytes), kHalfBytes, 1024);
+                    const uint64_t pd = smem_desc_sw128(sb + L::kP + bp * kPBytes, 16, 1024);
+                    if (leader) {
 #pragma unroll
-                    for (int u = 0; u < kSub; ++u)
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint64_t koff =
-                                (uint64_t)((u * kHalfBytes + (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
-                            const uint64_t qoff = (uint64_t)(((kk >> 2) * kQBox + (kk & 3) * 32) >> 4);
-                            mma_ss(tm + kColS + (b * kSub + u) * kTcRows, kd + koff, qd + qoff, kIdescS,
-                                   kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < kKeys / (16 * kSub); ++kk) {
+                            const uint64_t poff = (uint64_t)(((kk >> 2) * kPAtom + (kk & 3) * 32) >> 4);
+                            mma_ss(tm + kColO, vd + (uint64_t)((kk * 16 * 128) >> 4), pd + poff, kIdescPV,
+                                   (t == 0 && kk == 0) ? 0u : 1u);
                         }
+                    }
+                    __syncwarp();
+                    issued = true;
+                    commit(L::bPEmpty + bp);
+                    commit(L::bKVEmpty + vs);
                 }
-                __syncwarp();
-                issued = true;
-                commit(L::bSFull + b);
-                commit(L::bKVEmpty + ks);
-                if (t == w.n - 1) commit(L::bQEmpty + qb);
-                if (t > 0 && !(ok = pv(T - 1, vs_prev, vph_prev, t == 1, I, it))) break;
-                vs_prev = stage;  // V of this tile follows its K in the ring
-                vph_prev = kv_ph;
-                if (++stage == kTcSlots) {
-                    stage = 0;
-                    kv_ph ^= 1u;
-                }
+                if (ok) commit(L::bOFull);
             }
-            if (!ok) break;
-            if (!(ok = pv(T - 1, vs_prev, vph_prev, w.n == 1, I, it))) break;
-            commit(L::bOFull);
         }
         // every MMA this warp issued has completed before TMEM is released
         if (issued) {
-            commit(L::bDrain);
-            mbar_settle(bar(L::bDrain), 0, wf, 76);
+            const int db = L::bDrain + (s_warp ? 0 : 1);
+            commit(db);
+            mbar_settle(bar(db), 0, wf, 76);
         }
         __syncwarp();
     }
@@ -589,14 +640,23 @@ done:
     }
 }
 
+template <int D, int NR>
+cudaError_t launch_decode_tc_rows(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                  const DecodeParams& p, int grid, cudaStream_t stream)
+{
+    const cudaError_t e = smem_limit_once<fa_decode_tc_kernel<D, NR>>(TcSmem<D>::kDynamic);
+    if (e != cudaSuccess) return e;
+    fa_decode_tc_kernel<D, NR><<<grid, kTcThreads, TcSmem<D>::kDynamic, stream>>>(q, k, v, p);
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_decode_tc_dim(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const DecodeParams& p, int grid, cudaStream_t stream)
 {
-    const cudaError_t e = smem_limit_once<fa_decode_tc_kernel<D>>(TcSmem<D>::kDynamic);
-    if (e != cudaSuccess) return e;
-    fa_decode_tc_kernel<D><<<grid, kTcThreads, TcSmem<D>::kDynamic, stream>>>(q, k, v, p);
-    return cudaGetLastError();
+    if (p.R <= 4) return launch_decode_tc_rows<D, 4>(q, k, v, p, grid, stream);
+    if (p.R <= 8) return launch_decode_tc_rows<D, 8>(q, k, v, p, grid, stream);
+    return launch_decode_tc_rows<D, 16>(q, k, v, p, grid, stream);
 }
 
 cudaError_t launch_decode_tc(int D, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,

@@ -64,6 +64,8 @@ CASES = [
     (2, 32, 8, 1, 4100, 64, True, 0, 1.0),      # GQA r = 4 at D = 64 on the tensor cores, ragged last tile
     (1, 16, 1, 1, 3000, 64, False, 5, 20.0),    # MQA, 16 rows, sharp softmax, D = 64
     (4, 8, 8, 1, 65, 128, True, 1, 1.0),        # one partition: no merge launch
+    (1, 16, 2, 1, 2500, 64, True, 0, 1.0),      # 8 rows: the softmax carries exactly 8
+    (1, 10, 2, 1, 1999, 128, False, 3, 1.0),    # 5 rows in the 8-row softmax
 ]
 
 

@@ -182,9 +182,13 @@ struct BwdSmem {
     static constexpr int kTile = kBwdTile * D * 2;             // one 128-row tile of Q, K, V or dO
     static constexpr int kBoxes = kTile / kBox;                // 64-column boxes per tile
     static constexpr int kDSBytes = kBwdTile * kBwdTile * 2;   // dS^T [128 keys][128 queries] bf16
-    static constexpr int kK = 0, kV = kTile;
+    // K and V of a work item; at D = 64 in two stages, so that the next
+    // item's tiles load while the current item runs
+    static constexpr int kKVStages = D == 64 ? 2 : 1;
+    static constexpr int kK(int st) { return st * 2 * kTile; }
+    static constexpr int kV(int st) { return st * 2 * kTile + kTile; }
     static constexpr int kQStages = 3;
-    static constexpr int kQ = 2 * kTile;                       // [3] Q tiles
+    static constexpr int kQ = kKVStages * 2 * kTile;           // [3] Q tiles
     static constexpr int kDO = kQ + kQStages * kTile;          // dO tile (one stage: free after P.V)
     static constexpr int kDS = kDO + kTile;                    // dS^T
     static constexpr int kL2 = kDS + kDSBytes;                 // [3] lse2 rows (fp32 x 128), with Q
@@ -193,7 +197,9 @@ struct BwdSmem {
     static constexpr int bKVFull = 0, bKVEmpty = 1, bQFull = 2, bQEmpty = 5, bDOFull = 8, bDOEmpty = 9,
                          bDLFull = 10, bDLEmpty = 12, bSFull = 14, bPFull = 15, bDPFull = 16, bDSFull = 17,
                          bDSEmpty = 18, bDQFull = 19, bDQEmpty = 20, bDKVFull = 21, bDKVEmpty = 22, bDrain = 23,
-                         kNumBars = 24;
+                         bKV1 = 24, kNumBars = 24 + 2 * (kKVStages - 1);
+    static constexpr int bKVFullS(int st) { return st == 0 ? bKVFull : bKV1; }
+    static constexpr int bKVEmptyS(int st) { return st == 0 ? bKVEmpty : bKV1 + 1; }
     static constexpr int kMisc = kBars + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     // all the shared memory a CTA may have; the part beyond kBytes absorbs the
@@ -427,8 +433,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::bKVFull), 1);
-        mbar_init(bar(L::bKVEmpty), 1);
+        for (int i = 0; i < L::kKVStages; ++i) {
+            mbar_init(bar(L::bKVFullS(i)), 1);
+            mbar_init(bar(L::bKVEmptyS(i)), 1);
+        }
         for (int i = 0; i < L::kQStages; ++i) {
             mbar_init(bar(L::bQFull + i), 1);
             mbar_init(bar(L::bQEmpty + i), 4);  // each dQ warp, once its staged dQ boxes have been read
@@ -766,30 +774,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // ============================================================ TMA producer
         regs_decrease<64>();
         if (lane == 0) {
-            int q_armed[L::kQStages] = {-1, -1, -1}, dl_armed[2] = {-1, -1}, do_armed = -1, kv_armed = -1;
+            int q_armed[L::kQStages] = {-1, -1, -1}, dl_armed[2] = {-1, -1}, do_armed = -1, kv_armed[2] = {-1, -1};
             bool drop = p.fault == 1;  // test hook: this CTA's first K/V never arrives
             uint32_t gstep = 0;
             int I = 0;
             for (int k = 0, it = bwd_cta_item<kAlt>(0); it < num_items; it = bwd_cta_item<kAlt>(++k)) {
                 const BwdItem w = bwd_item<CAUSAL, VARLEN, VAR>(p, it);
                 const int bh_kv = w.b * p.Hkv + w.hkv;
+                const int st = I % L::kKVStages;
+                const uint32_t kvph = (uint32_t)((I / L::kKVStages) & 1);
                 // TMA coordinates: dense (x, row, head slab), packed (x, head, token)
                 auto ld_kv = [&](uint32_t dst, const CUtensorMap* map, int x) {
                     if constexpr (VARLEN)
-                        tma_load_3d(dst, map, bar(L::bKVFull), x, w.hkv, w.k0 + w.j * kBwdTile);
+                        tma_load_3d(dst, map, bar(L::bKVFullS(st)), x, w.hkv, w.k0 + w.j * kBwdTile);
                     else
-                        tma_load_3d(dst, map, bar(L::bKVFull), x, w.j * kBwdTile, bh_kv);
+                        tma_load_3d(dst, map, bar(L::bKVFullS(st)), x, w.j * kBwdTile, bh_kv);
                 };
-                if (!mbar_wait(bar(L::bKVEmpty), (uint32_t)(I & 1) ^ 1u, abort_flag, wf, 85, it)) break;
+                if (!mbar_wait(bar(L::bKVEmptyS(st)), kvph ^ 1u, abort_flag, wf, 85, it)) break;
                 if (drop) {
                     drop = false;
                 } else {
-                    mbar_arrive_expect_tx(bar(L::bKVFull), 2 * L::kTile);
-                    kv_armed = I & 1;
+                    mbar_arrive_expect_tx(bar(L::bKVFullS(st)), 2 * L::kTile);
+                    kv_armed[st] = (int)kvph;
 #pragma unroll
                     for (int bx = 0; bx < L::kBoxes; ++bx) {
-                        ld_kv(sb + L::kK + bx * kBox, &tmK, 64 * bx);
-                        ld_kv(sb + L::kV + bx * kBox, &tmV, 64 * bx);
+                        ld_kv(sb + L::kK(st) + bx * kBox, &tmK, 64 * bx);
+                        ld_kv(sb + L::kV(st) + bx * kBox, &tmV, 64 * bx);
                     }
                 }
                 bool ok = true;
@@ -828,7 +838,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ++I;
             }
             // every copy this thread started has landed before the CTA retires
-            if (kv_armed >= 0) mbar_settle(bar(L::bKVFull), (uint32_t)kv_armed, wf, 97);
+            for (int st = 0; st < L::kKVStages; ++st)
+                if (kv_armed[st] >= 0) mbar_settle(bar(L::bKVFullS(st)), (uint32_t)kv_armed[st], wf, 97);
             for (int t = 0; t < L::kQStages; ++t)
                 if (q_armed[t] >= 0) mbar_settle(bar(L::bQFull + t), (uint32_t)q_armed[t], wf, 98);
             for (int t = 0; t < 2; ++t)
@@ -852,9 +863,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         };
         auto kmaj = [](int kk) -> uint64_t { return (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4); };
         auto mnmaj = [](int kk) -> uint64_t { return (uint64_t)((kk * 16 * 128) >> 4); };
-        const uint64_t dK_kmaj = smem_desc_sw128(sb + L::kK, 16, 1024);
-        const uint64_t dK_mn = smem_desc_sw128(sb + L::kK, kHalf, 1024);
-        const uint64_t dV_kmaj = smem_desc_sw128(sb + L::kV, 16, 1024);
+        // K and V of the current item (stage set per item)
+        uint64_t dK_kmaj = 0, dK_mn = 0, dV_kmaj = 0;
         const uint64_t dS_kmaj = smem_desc_sw128(sb + L::kDS, 16, 1024);
         const uint64_t dS_mn = smem_desc_sw128(sb + L::kDS, kHalf, 1024);
         // S^T = K Q^T into the S region
@@ -874,7 +884,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool issued = false, ok = true;
         for (int k = 0, it = bwd_cta_item<kAlt>(0); it < num_items && ok; it = bwd_cta_item<kAlt>(++k)) {
             const BwdItem w = bwd_item<CAUSAL, VARLEN, VAR>(p, it);
-            if (!(ok = bwd_warp_wait(bar(L::bKVFull), (uint32_t)(I & 1), abort_flag, wf, 89, it))) break;
+            const int st = I % L::kKVStages;
+            if (!(ok = bwd_warp_wait(bar(L::bKVFullS(st)), (uint32_t)((I / L::kKVStages) & 1), abort_flag, wf, 89,
+                                     it)))
+                break;
+            dK_kmaj = smem_desc_sw128(sb + L::kK(st), 16, 1024);
+            dK_mn = smem_desc_sw128(sb + L::kK(st), kHalf, 1024);
+            dV_kmaj = smem_desc_sw128(sb + L::kV(st), 16, 1024);
             {
                 const uint32_t qs = gstep % L::kQStages, qph = (gstep / L::kQStages) & 1u;
                 if (!(ok = bwd_warp_wait(bar(L::bQFull + qs), qph, abort_flag, wf, 90, it))) break;
@@ -956,7 +972,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             if (!ok) break;
             commit(L::bDKVFull);
-            commit(L::bKVEmpty);
+            commit(L::bKVEmptyS(st));
             ++I;
         }
         if (issued) {

@@ -261,7 +261,9 @@ fa_status_t fa_fwd_fp8(const void* prepared, float* o, float* lse, int B, int Hq
  *     workspaces.
  *
  * Launches 1 kernel (one partition) or 2 (partials, then the merge).
- * Arithmetic is fp32 throughout (bf16 inputs widened exactly).
+ * Scores, softmax statistics and O accumulate in fp32; the tensor-core
+ * partials ((Hq / Hkv) * Lq >= 2, D = 64 or 128) round P to bf16 for P.V, as
+ * fa_fwd does, and the one-row kernel keeps P in fp32.
  */
 fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, float* o, float* lse,
                            int B, int Hq, int Hkv, int Lq, int Lk, int D, int causal,

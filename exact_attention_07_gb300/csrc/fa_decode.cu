@@ -463,22 +463,35 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const DecodeParams
     float wsum = 0.f;
     if (mx != -INFINITY) {
         const float* op = p.o_part + ((long long)bh * S * p.R + r) * D + lane * V;
-#pragma unroll 4
-        for (int s = 0; s < S; ++s) {
-            const float w = ex2_approx(lp[(long long)s * p.R] - mx);
-            const float* src = op + (long long)s * p.R * D;
-            if constexpr (V == 4) {
-                const float4 x = *reinterpret_cast<const float4*>(src);
-                acc[0] = fmaf(w, x.x, acc[0]);
-                acc[1] = fmaf(w, x.y, acc[1]);
-                acc[2] = fmaf(w, x.z, acc[2]);
-                acc[3] = fmaf(w, x.w, acc[3]);
-            } else {
-                const float2 x = *reinterpret_cast<const float2*>(src);
-                acc[0] = fmaf(w, x.x, acc[0]);
-                acc[1] = fmaf(w, x.y, acc[1]);
+        for (int s0 = 0; s0 < S; s0 += 8) {
+            // eight partitions' loads in flight before any is used
+            float lv[8], x[8][V];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int s = min(s0 + u, S - 1);
+                lv[u] = lp[(long long)s * p.R];
+                const float* src = op + (long long)s * p.R * D;
+                if constexpr (V == 4) {
+                    const float4 t = *reinterpret_cast<const float4*>(src);
+                    x[u][0] = t.x;
+                    x[u][1] = t.y;
+                    x[u][2] = t.z;
+                    x[u][3] = t.w;
+                } else {
+                    const float2 t = *reinterpret_cast<const float2*>(src);
+                    x[u][0] = t.x;
+                    x[u][1] = t.y;
+                }
             }
-            wsum += w;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (s0 + u < S) {  // partitions in order, as before the batching
+                    const float w = ex2_approx(lv[u] - mx);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) acc[e] = fmaf(w, x[u][e], acc[e]);
+                    wsum += w;
+                }
+            }
         }
     }
     const int b = bh / p.Hkv, hkv = bh - b * p.Hkv;

@@ -54,6 +54,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "fa_bwd.h"
 #include "ptx_sm103.cuh"
@@ -634,13 +635,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t ds = gstep & 1u, dph = (gstep >> 1) & 1u;
                 const float4* l2p = reinterpret_cast<const float4*>(smem + L::kL2 + qs * 512);
                 const float4* dlp = reinterpret_cast<const float4*>(smem + L::kDL + ds * 512);
-                // pairs above the bottom-right diagonal (or outside the key window)
-                // exist in this tile for this thread's key
-                bool need_mask = !key_ok || (CAUSAL && q0 < w.j * kBwdTile + kBwdTile - 1 - off);
+                // Queries q_lo .. q_hi see this thread's key: q >= key - (Lk - Lq)
+                // under the causal mask; with a key window, q >= key - off - right
+                // and q <= key - off + left.  A warp masks this step's scores
+                // only when one of its keys misses some row of the Q tile.
+                constexpr long long kFar = 1ll << 40;  // beyond any token index; no overflow below
+                long long q_lo = -kFar, q_hi = kFar;
+                if (CAUSAL) q_lo = (long long)kpos - off;
                 if constexpr (var_window(VAR)) {
-                    if (p.win_left >= 0 && kpos < q0 + kBwdTile - 1 + off - p.win_left) need_mask = true;
-                    if (p.win_right >= 0 && kpos > q0 + off + p.win_right) need_mask = true;
+                    if (p.win_right >= 0) q_lo = max(q_lo, (long long)kpos - off - p.win_right);
+                    if (p.win_left >= 0) q_hi = (long long)kpos - off + p.win_left;
                 }
+                if (!key_ok) q_lo = kFar;
+                const bool need_mask =
+                    __any_sync(0xffffffffu, q_lo > q0 || q_hi < (long long)q0 + kBwdTile - 1);
                 if constexpr (var_alibi(VAR)) alibi_l2 = __ldg(p.alibi + h) * 1.4426950408889634f;
                 if (!bwd_warp_wait(bar(L::bQFull + qs), qph, abort_flag, wf, 79, it)) goto done;
                 if (!bwd_warp_wait(bar(L::bSFull), ph, abort_flag, wf, 80, it)) goto done;
@@ -648,9 +656,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // bf16 pairs of queries 64ch + (2e, 2e+1): P, or with soft-capping
                 // P * (1 - tanh^2), the factor dS needs
                 uint32_t pk[32];
+                // the masked and the unmasked step are separate code paths
+                auto p_phase = [&](auto masked) {
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c = 2 * ch + cc;  // 32-query chunk of the tile
+                    // this thread's visible queries as offsets in the chunk, clamped to [-1, 32]
+                    const long long cq = (long long)q0 + c * 32;
+                    const int e_lo = (int)min(max(q_lo - cq, -1ll), 32ll);
+                    const int e_hi = (int)min(max(q_hi - cq, -1ll), 32ll);
                     uint32_t r[32];
                     tmem_ld32(lane_base + kColS + c * 32, r);
                     float l2[32];
@@ -689,16 +703,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             p0 = ex2_approx(fmaf(__uint_as_float(r[e]), p.scale_log2, b0));
                             p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), p.scale_log2, b1));
                         }
-                        if (need_mask) {
-                            const int q = q0 + c * 32 + e;
-                            if (!key_ok || (CAUSAL && kpos > q + off)) p0 = 0.f;
-                            if (!key_ok || (CAUSAL && kpos > q + 1 + off)) p1 = 0.f;
-                            if constexpr (var_window(VAR)) {
-                                if (p.win_left >= 0 && kpos < q + off - p.win_left) p0 = 0.f;
-                                if (p.win_left >= 0 && kpos < q + 1 + off - p.win_left) p1 = 0.f;
-                                if (p.win_right >= 0 && kpos > q + off + p.win_right) p0 = 0.f;
-                                if (p.win_right >= 0 && kpos > q + 1 + off + p.win_right) p1 = 0.f;
-                            }
+                        if constexpr (decltype(masked)::value) {
+                            if (e < e_lo || e > e_hi) p0 = 0.f;
+                            if (e + 1 < e_lo || e + 1 > e_hi) p1 = 0.f;
                         }
                         if constexpr (var_softcap(VAR)) {
                             pt[e / 2] = bwd_pack_bf16(p0, p1);
@@ -713,6 +720,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // being read by its warps
                     if constexpr (var_softcap(VAR)) bwd_tmem_st16(lane_base + kColS + 64 * ch + 16 * cc, pt);
                 }
+                };
+                if (need_mask)
+                    p_phase(std::true_type{});
+                else
+                    p_phase(std::false_type{});
                 if constexpr (!var_softcap(VAR)) {
                     uint32_t lo[16], hi[16];
 #pragma unroll

@@ -30,8 +30,8 @@ struct DecodeParams {
     int B, Hq, Hkv, Lq, Lk, group;
     int R;                // group * Lq query rows per KV head
     int num_splits;       // partitions of the key range per (batch, KV head)
-    int tiles_per_split;  // 64-key tiles of one partition (the last may have fewer)
-    int num_tiles;        // ceil(Lk / 64)
+    int tiles_per_split;  // key tiles of one partition (the last may have fewer)
+    int num_tiles;        // ceil(Lk / keys per tile): 64 keys (FP32 pipes), 16384 / D (tensor cores)
     int causal;
     float scale_log2;  // softmax_scale * log2(e)
     int* err;

@@ -768,6 +768,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         d[e / 2] = bwd_pack_bf16(ds0, ds1);
                     }
                     // dS^T row t, queries 32c .. 32c+31: half ch, 16-byte chunks 4(c&1) .. +3
+                    // (the A operand of dQ, read MN-major)
                     const uint32_t row = sb + L::kDS + (uint32_t)(ch * kHalf + t * 128);
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -775,7 +776,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         sts128(row + (uint32_t)((chunk ^ (t & 7)) << 4), d[4 * u], d[4 * u + 1], d[4 * u + 2],
                                d[4 * u + 3]);
                     }
+                    // and in tensor memory as the A operand of dK, laid out like P^T:
+                    // the first 32 of this half's 64 dP^T columns, already read
+                    bwd_tmem_st16(lane_base + kColDP + 64 * ch + 16 * cc, d);
                 }
+                tmem_wait_st();
                 bwd_fence_proxy_async();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::bDSFull));
@@ -877,7 +882,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         auto mnmaj = [](int kk) -> uint64_t { return (uint64_t)((kk * 16 * 128) >> 4); };
         // K and V of the current item (stage set per item)
         uint64_t dK_kmaj = 0, dK_mn = 0, dV_kmaj = 0;
-        const uint64_t dS_kmaj = smem_desc_sw128(sb + L::kDS, 16, 1024);
         const uint64_t dS_mn = smem_desc_sw128(sb + L::kDS, kHalf, 1024);
         // S^T = K Q^T into the S region
         const uint64_t dO_kmaj = smem_desc_sw128(sb + L::kDO, 16, 1024);
@@ -970,9 +974,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!(ok = bwd_warp_wait(bar(L::bDSFull), gstep & 1u, abort_flag, wf, 94, it))) break;
                 tc_fence_after_sync();
                 if (leader) {
+                    // dK += dS^T Q with A = dS^T from tensor memory (the P/dS warps' copy
+                    // in the dP^T columns), which saves its shared-memory reads
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tm + kColDK, dS_kmaj + kmaj(kk), q_mn + mnmaj(kk), kIdBmn, (s > 0 || kk > 0) ? 1u : 0u);
+                        mma_ts(tm + kColDK, tm + kColDP + (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)), q_mn + mnmaj(kk),
+                               kIdBmn, (s > 0 || kk > 0) ? 1u : 0u);
                     // dQ = dS K with the query rows on the TMEM lanes (A = dS and B = K
                     // both MN-major), so that each dQ thread holds one row
 #pragma unroll

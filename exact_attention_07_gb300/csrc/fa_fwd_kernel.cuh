@@ -863,14 +863,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // here: the previous P.V completed before this S was committed, or,
                 // with P in columns of its own, before the wait above returned)
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    // two 32-column chunks per tensor-memory round trip
 #pragma unroll 1
-                    for (int c = 0; c < DV / 32; ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(tO + 32u * c, ov);
+                    for (int c = 0; c < DV / 32; c += 2) {
+                        uint32_t ov[2][32];
+                        tmem_ld32(tO + 32u * c, ov[0]);
+                        tmem_ld32(tO + 32u * (c + 1), ov[1]);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tmem_st32(tO + 32u * c, ov);
+                        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) ov[h][i] = __float_as_uint(__uint_as_float(ov[h][i]) * alpha);
+                            tmem_st32(tO + 32u * (c + h), ov[h]);
+                        }
                     }
                 }
                 tmem_wait_st();

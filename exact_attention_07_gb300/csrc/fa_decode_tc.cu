@@ -25,20 +25,21 @@
 // V from HBM; the FP32-pipe variant (fa_decode.cu) runs out of issue slots
 // first once R reaches 4.
 //
-// Roles (224 threads, one persistent CTA per SM, work items = (batch, KV
-// head, key partition) in a strided order):
-//   warps 0-3  softmax: thread k owns TMEM lane k -- key k of each 128-key
-//              half for S^T, output dimension k for O^T (D = 64: threads
-//              64..127 hold the second half's partial sums of dimension
-//              k - 64, added in the epilogue).  Row maxima across the keys go
-//              through a transposing warp reduction and a four-warp exchange
-//              in shared memory; P^T is written to shared memory in the
-//              operand layout; O^T is rescaled in place when a row's
-//              reference moves; the epilogue normalises and stores.  Only the
-//              first NR >= R of the 16 MMA columns are carried.
-//   warp  4    TMA producer: Q rows of the item, then K and V tiles in a ring.
-//   warp  5    S^T MMA issuer and tensor-memory owner.
-//   warp  6    O^T MMA issuer.
+// Roles (one persistent CTA per SM, work items = (batch, KV head, key
+// partition) in a strided order), with G = 1 softmax warpgroup for up to 4
+// carried rows and G = 2 (each carrying half of the rows) for 8 or 16:
+//   warps 0..4G-1  softmax: in each group, thread k owns TMEM lane k -- key
+//              k of each 128-key half for S^T, output dimension k for O^T
+//              (D = 64: threads 64..127 hold the second half's partial sums
+//              of dimension k - 64, added in the epilogue).  Row maxima
+//              across the keys go through a transposing warp reduction and a
+//              four-warp exchange in shared memory; P^T is written to shared
+//              memory in the operand layout; O^T is rescaled in place when a
+//              row's reference moves; the epilogue normalises and stores.
+//              Only the first NR >= R of the 16 MMA columns are carried.
+//   warp  4G    TMA producer: Q rows of the item, then K and V tiles in a ring.
+//   warp  4G+1  S^T MMA issuer and tensor-memory owner.
+//   warp  4G+2  O^T MMA issuer.
 // The online-softmax state follows the dense kernel: base-2 exponentials,
 // a per-row reference r that moves only when a tile maximum exceeds it by
 // more than 8, the bf16-rounded probability sum to normalise O and the fp32
@@ -58,7 +59,11 @@ namespace fa {
 namespace {
 
 constexpr int kTcRows = 16;            // packed query rows (the MMA's N)
-constexpr int kTcThreads = 224;
+// Softmax warpgroups: one for up to 4 carried rows, two (rows split in
+// halves) for 8 or 16, so that a thread's per-tile work stays small.  The
+// producer and the two MMA warps follow them.
+constexpr int tc_groups(int NR) { return NR > 4 ? 2 : 1; }
+constexpr int tc_threads(int NR) { return 32 * (4 * tc_groups(NR) + 3); }
 constexpr int kHalfBytes = 128 * 64 * 2;         // one [128 keys][64 dimensions] box: 16 KB
 constexpr int kQBox = kTcRows * 64 * 2;          // one 64-dimension box of Q: 2 KB
 
@@ -80,15 +85,16 @@ struct TcSmem {
     static constexpr int kSlots = 0;
     static constexpr int kQ = kSlots + kNumSlots * kSlotBytes;       // [2] Q buffers
     static constexpr int kP = kQ + 2 * kQBytes;                      // [2] P^T buffers
-    static constexpr int kRed = kP + 2 * kPBytes;              // float [2][4][16] row maxima
-    static constexpr int kEpi = kRed + 2 * 4 * 16 * 4;         // float [4][32] row sums
-    static constexpr int kSum = kEpi + 4 * 32 * 4;             // D = 64: float [16][64] second-half O^T
+    static constexpr int kRed = kP + 2 * kPBytes;              // float [2 buffers][2 groups][4][16] row maxima
+    static constexpr int kEpi = kRed + 2 * 2 * 4 * 16 * 4;     // float [2 groups][4][32] row sums
+    static constexpr int kSum = kEpi + 2 * 4 * 32 * 4;         // D = 64: float [16][64] second-half O^T
     static constexpr int kBars = kSum + (kSub == 2 ? kTcRows * 64 * 4 : 0);
     // barrier slots
     static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kNumSlots;
     static constexpr int bSFull = 4 + 2 * kNumSlots, bSEmpty = bSFull + 2, bPFull = bSFull + 4,
                          bPEmpty = bSFull + 6, bOFull = bSFull + 8, bOEmpty = bSFull + 9,
-                         bRed = bSFull + 10, bEpi = bSFull + 12, bDrain = bSFull + 13, kNumBars = bSFull + 15;
+                         bRed = bSFull + 10, bEpi = bSFull + 14, bDrain = bSFull + 16, kNumBars = bSFull + 18;
+    // bRed + 2 * buffer + group, bEpi + group
     static constexpr int kMisc = kBars + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kDynamic = kBytes + 1024;
@@ -227,7 +233,7 @@ __device__ __forceinline__ TcItem tc_item(const DecodeParams& p, int it)
 // NR = query rows the softmax carries (4, 8 or 16 >= R); the MMAs keep N = 16,
 // and the rows of P^T past NR stay zero.
 template <int D, int NR>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(tc_threads(NR), 1)
     fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p)
 {
@@ -236,7 +242,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int kKeys = L::kKeys, kSub = L::kSub, kPBytes = L::kPBytes, kPAtom = L::kPAtom;
     constexpr uint32_t kColS = TcTmem<D>::kColS, kColO = TcTmem<D>::kColO, kTmemCols = TcTmem<D>::kCols;
     constexpr float kTau = 8.0f;
-    constexpr int kLanesPerRow = 32 / NR;  // lanes that end a transposing reduction with the same row
+    constexpr int NG = tc_groups(NR), RG = NR / NG;  // softmax groups, rows of each
+    constexpr int kLanesPerRow = 32 / RG;  // lanes that end a transposing reduction with the same row
+    constexpr int kThreads = tc_threads(NR);
+    constexpr int wProd = 4 * NG, wMmaS = 4 * NG + 1, wMmaPV = 4 * NG + 2;  // warp roles after the softmax
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
@@ -255,36 +264,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(bar(L::bQFull + i), 1);
             mbar_init(bar(L::bQEmpty + i), 1);
             mbar_init(bar(L::bSFull + i), 1);
-            mbar_init(bar(L::bSEmpty + i), 128);
-            mbar_init(bar(L::bPFull + i), 128);
+            mbar_init(bar(L::bSEmpty + i), 128 * NG);
+            mbar_init(bar(L::bPFull + i), 128 * NG);
             mbar_init(bar(L::bPEmpty + i), 1);
-            mbar_init(bar(L::bRed + i), 128);
+            mbar_init(bar(L::bRed + 2 * i), 128);
+            mbar_init(bar(L::bRed + 2 * i + 1), 128);
+            mbar_init(bar(L::bEpi + i), 128);
         }
         for (int s = 0; s < kTcSlots; ++s) {
             mbar_init(bar(L::bKVFull + s), 1);
             mbar_init(bar(L::bKVEmpty + s), 1);
         }
         mbar_init(bar(L::bOFull), 1);
-        mbar_init(bar(L::bOEmpty), 128);
-        mbar_init(bar(L::bEpi), 128);
+        mbar_init(bar(L::bOEmpty), 128 * NG);
         mbar_init(bar(L::bDrain), 1);
         mbar_init(bar(L::bDrain + 1), 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == wProd && lane == 0) {
         tma_prefetch_map(&tmQ);
         tma_prefetch_map(&tmK);
         tma_prefetch_map(&tmV);
     }
-    if (warp == 5) {
+    if (warp == wMmaS) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     if constexpr (NR < kTcRows) {
         // P^T rows NR..15 are never written: zeros for the O^T MMA
         uint4* z = reinterpret_cast<uint4*>(smem + L::kP);
-        for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += kTcThreads) z[i] = make_uint4(0, 0, 0, 0);
+        for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     tc_fence_before_sync();
@@ -292,28 +302,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 4) {
+    if (warp < 4 * NG) {
         // ============================================================ softmax
-        const int k = threadIdx.x;  // TMEM lane: key of the tile / output dimension
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        // this thread's O^T columns: D = 64 warps 2-3 hold the second half's partial sums
-        const uint32_t col_o = kColO + (kSub == 2 && warp >= 2 ? (uint32_t)kTcRows : 0u);
+        // group g carries query rows g*RG .. g*RG + RG - 1 of the 16
+        const int g = warp >> 2, wq = warp & 3;
+        const int k = 32 * wq + lane;  // TMEM lane: key of the tile / output dimension
+        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+        // this thread's O^T columns: D = 64 lanes 64..127 hold the second half's partial sums
+        const uint32_t col_o = kColO + (kSub == 2 && wq >= 2 ? (uint32_t)kTcRows : 0u) + (uint32_t)(g * RG);
+        const int row0 = g * RG;  // first query row of the group
         const int causal_off = p.Lk - p.Lq;
         // last key each row may see (bottom-right causal alignment, padding at Lk)
-        int lim[NR];
+        int lim[RG];
         int lim_min = p.Lk - 1;
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            lim[r] = p.causal ? min(p.Lk - 1, (r % p.Lq) + causal_off) : p.Lk - 1;
-            if (r < p.R) lim_min = min(lim_min, lim[r]);
+        for (int r = 0; r < RG; ++r) {
+            lim[r] = p.causal ? min(p.Lk - 1, ((row0 + r) % p.Lq) + causal_off) : p.Lk - 1;
+            if (row0 + r < p.R) lim_min = min(lim_min, lim[r]);
         }
         uint32_t T = 0;
         int I = 0;
         for (int it = blockIdx.x; it < num_items; it += gridDim.x, ++I) {
             const TcItem w = tc_item(p, it);
-            float ref[NR], lf[NR], lb[NR];
+            float ref[RG], lf[RG], lb[RG];
 #pragma unroll
-            for (int r = 0; r < NR; ++r) {
+            for (int r = 0; r < RG; ++r) {
                 ref[r] = -INFINITY;
                 lf[r] = 0.f;
                 lb[r] = 0.f;
@@ -323,10 +336,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!tc_warp_wait(bar(L::bSFull + b), ph, abort_flag, wf, 60, it)) goto done;
                 tc_fence_after_sync();
                 // this thread's keys: k + 128 u of the tile, u < kSub
-                float s[kSub][NR];
+                float s[kSub][RG];
 #pragma unroll
                 for (int u = 0; u < kSub; ++u)
-                    tmem_ld_cols<NR>(lane_base + kColS + (b * kSub + u) * kTcRows, s[u]);
+                    tmem_ld_cols<RG>(lane_base + kColS + (b * kSub + u) * kTcRows + row0, s[u]);
                 tmem_wait_ld();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::bSEmpty + b));
@@ -334,34 +347,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int u = 0; u < kSub; ++u)
 #pragma unroll
-                    for (int r = 0; r < NR; ++r) s[u][r] *= p.scale_log2;
+                    for (int r = 0; r < RG; ++r) s[u][r] *= p.scale_log2;
                 if (key_base + kKeys - 1 > lim_min) {  // tile reaches masked keys
 #pragma unroll
                     for (int u = 0; u < kSub; ++u)
 #pragma unroll
-                        for (int r = 0; r < NR; ++r)
+                        for (int r = 0; r < RG; ++r)
                             if (key_base + 128 * u + k > lim[r]) s[u][r] = -INFINITY;
                 }
                 // tile maximum of every row over the tile's keys
-                float sm[NR];
+                float sm[RG];
 #pragma unroll
-                for (int r = 0; r < NR; ++r) {
+                for (int r = 0; r < RG; ++r) {
                     sm[r] = s[0][r];
 #pragma unroll
                     for (int u = 1; u < kSub; ++u) sm[r] = fmaxf(sm[r], s[u][r]);
                 }
                 const float wm = transpose_reduce<true>(sm, lane);
-                float* rb = red + b * 64;
-                if (lane % kLanesPerRow == 0) rb[warp * 16 + lane / kLanesPerRow] = wm;
-                mbar_arrive(bar(L::bRed + b));
-                if (!tc_warp_wait(bar(L::bRed + b), ph, abort_flag, wf, 61, it)) goto done;
+                float* rb = red + (2 * b + g) * 64;
+                if (lane % kLanesPerRow == 0) rb[wq * 16 + lane / kLanesPerRow] = wm;
+                mbar_arrive(bar(L::bRed + 2 * b + g));
+                if (!tc_warp_wait(bar(L::bRed + 2 * b + g), ph, abort_flag, wf, 61, it)) goto done;
                 float tm_lane = -INFINITY;
-                if (lane < NR)
+                if (lane < RG)
                     tm_lane = fmaxf(fmaxf(rb[lane], rb[16 + lane]), fmaxf(rb[32 + lane], rb[48 + lane]));
-                float alpha[NR];
+                float alpha[RG];
                 bool moved = false;
 #pragma unroll
-                for (int r = 0; r < NR; ++r) {
+                for (int r = 0; r < RG; ++r) {
                     const float tm = __shfl_sync(0xffffffffu, tm_lane, r);
                     alpha[r] = 1.f;
                     if (tm > ref[r] + kTau) {  // also when ref is still -inf and the tile has a key
@@ -371,16 +384,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 // probabilities, rounded to bf16 for the MMA; both sums
-                uint32_t pk[kSub][NR / 2];
+                uint32_t pk[kSub][RG / 2];
 #pragma unroll
-                for (int r = 0; r < NR; ++r) {
+                for (int r = 0; r < RG; ++r) {
                     lf[r] *= alpha[r];
                     lb[r] *= alpha[r];
                 }
 #pragma unroll
                 for (int u = 0; u < kSub; ++u)
 #pragma unroll
-                    for (int r = 0; r < NR; r += 2) {
+                    for (int r = 0; r < RG; r += 2) {
                         const float p0 = ref[r] == -INFINITY ? 0.f : ex2_approx(s[u][r] - ref[r]);
                         const float p1 = ref[r + 1] == -INFINITY ? 0.f : ex2_approx(s[u][r + 1] - ref[r + 1]);
                         __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
@@ -400,10 +413,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int u = 0; u < kSub; ++u)
 #pragma unroll
-                        for (int r = 0; r < NR; ++r) {
+                        for (int r = 0; r < RG; ++r) {
                             const uint16_t h =
                                 (r & 1) ? (uint16_t)(pk[u][r / 2] >> 16) : (uint16_t)(pk[u][r / 2] & 0xffffu);
-                            sts16(pb + (uint32_t)((16 * u + r) * 128 + ((chunk ^ (r & 7)) << 4)), h);
+                            const int n = 16 * u + row0 + r;  // operand row
+                            sts16(pb + (uint32_t)(n * 128 + ((chunk ^ (n & 7)) << 4)), h);
                         }
                 }
                 fence_proxy_async_smem();
@@ -412,12 +426,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t bp = (T - 1) & 1u, php = ((T - 1) >> 1) & 1u;
                     if (!tc_warp_wait(bar(L::bPEmpty + bp), php, abort_flag, wf, 63, it)) goto done;
                     tc_fence_after_sync();
-                    float o[NR];
-                    tmem_ld_cols<NR>(lane_base + col_o, o);
+                    float o[RG];
+                    tmem_ld_cols<RG>(lane_base + col_o, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int r = 0; r < NR; ++r) o[r] *= alpha[r];
-                    tmem_st_cols<NR>(lane_base + col_o, o);
+                    for (int r = 0; r < RG; ++r) o[r] *= alpha[r];
+                    tmem_st_cols<RG>(lane_base + col_o, o);
                     tmem_wait_st();
                 }
                 tc_fence_before_sync();
@@ -426,55 +440,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // ---- epilogue of the item: O = O^T / l_rounded, LSE = r + log2(l)
             if (!tc_warp_wait(bar(L::bOFull), (uint32_t)(I & 1), abort_flag, wf, 64, it)) goto done;
             tc_fence_after_sync();
-            float o[NR];
-            tmem_ld_cols<NR>(lane_base + col_o, o);
+            float o[RG];
+            tmem_ld_cols<RG>(lane_base + col_o, o);
             tmem_wait_ld();
             tc_fence_before_sync();
             mbar_arrive(bar(L::bOEmpty));
             float* osum = reinterpret_cast<float*>(smem + L::kSum);
             if (kSub == 2 && k >= 64) {
 #pragma unroll
-                for (int r = 0; r < NR; ++r) osum[r * 64 + (k - 64)] = o[r];
+                for (int r = 0; r < RG; ++r) osum[(row0 + r) * 64 + (k - 64)] = o[r];
             }
             {
                 const float sb_w = transpose_reduce<false>(lb, lane);
                 const float sf_w = transpose_reduce<false>(lf, lane);
                 if (lane % kLanesPerRow == 0) {
-                    epi[warp * 32 + lane / kLanesPerRow] = sb_w;
-                    epi[warp * 32 + 16 + lane / kLanesPerRow] = sf_w;
+                    epi[g * 128 + wq * 32 + lane / kLanesPerRow] = sb_w;
+                    epi[g * 128 + wq * 32 + 16 + lane / kLanesPerRow] = sf_w;
                 }
             }
-            mbar_arrive(bar(L::bEpi));
-            if (!tc_warp_wait(bar(L::bEpi), (uint32_t)(I & 1), abort_flag, wf, 65, it)) goto done;
-            const float lsum = epi[lane] + epi[32 + lane] + epi[64 + lane] + epi[96 + lane];  // lane<16: rounded, else fp32
+            mbar_arrive(bar(L::bEpi + g));
+            if (!tc_warp_wait(bar(L::bEpi + g), (uint32_t)(I & 1), abort_flag, wf, 65, it)) goto done;
+            // lane < 16: the rounded sums of the group's rows, else the fp32 sums
+            const float* eg = epi + g * 128;
+            const float lsum = eg[lane] + eg[32 + lane] + eg[64 + lane] + eg[96 + lane];
             if (kSub == 2 && k < 64) {
 #pragma unroll
-                for (int r = 0; r < NR; ++r) o[r] += osum[r * 64 + k];
+                for (int r = 0; r < RG; ++r) o[r] += osum[(row0 + r) * 64 + k];
             }
             const bool single = p.num_splits == 1;
 #pragma unroll
-            for (int r = 0; r < NR; ++r) {
+            for (int r = 0; r < RG; ++r) {
                 const float l_r = __shfl_sync(0xffffffffu, lsum, r);
                 const float lf_r = __shfl_sync(0xffffffffu, lsum, 16 + r);
-                if (r < p.R) {
+                const int rr = row0 + r;  // query row of the item
+                if (rr < p.R) {
                     const float val = l_r > 0.f ? o[r] / l_r : 0.f;
                     if (k < D) {
                         if (single)
-                            p.o[(w.row0 + r) * D + k] = val;
+                            p.o[(w.row0 + rr) * D + k] = val;
                         else
-                            p.o_part[((long long)it * p.R + r) * D + k] = val;
+                            p.o_part[((long long)it * p.R + rr) * D + k] = val;
                     }
                     if (k == r) {
                         const float lse2 = lf_r > 0.f ? ref[r] + log2f(lf_r) : -INFINITY;
                         if (single)
-                            p.lse[w.row0 + r] = lse2 * 0.6931471805599453f;
+                            p.lse[w.row0 + rr] = lse2 * 0.6931471805599453f;
                         else
-                            p.l_part[(long long)it * p.R + r] = lse2;
+                            p.l_part[(long long)it * p.R + rr] = lse2;
                     }
                 }
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == wProd) {
         // ============================================================ TMA producer
         if (lane == 0) {
             int q_armed[2] = {-1, -1};
@@ -538,7 +555,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the ring.
         const bool leader = lane == 0;
         const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
-        const bool s_warp = warp == 5;
+        const bool s_warp = warp == wMmaS;
         auto ring = [&](uint32_t n, int& slot, uint32_t& ph) {
             slot = (int)(n % (uint32_t)kTcSlots);
             ph = (n / (uint32_t)kTcSlots) & 1u;
@@ -634,7 +651,7 @@ done:
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == wMmaS) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -646,7 +663,7 @@ cudaError_t launch_decode_tc_rows(const CUtensorMap& q, const CUtensorMap& k, co
 {
     const cudaError_t e = smem_limit_once<fa_decode_tc_kernel<D, NR>>(TcSmem<D>::kDynamic);
     if (e != cudaSuccess) return e;
-    fa_decode_tc_kernel<D, NR><<<grid, kTcThreads, TcSmem<D>::kDynamic, stream>>>(q, k, v, p);
+    fa_decode_tc_kernel<D, NR><<<grid, tc_threads(NR), TcSmem<D>::kDynamic, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 

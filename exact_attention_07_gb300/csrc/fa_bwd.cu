@@ -256,12 +256,6 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v)
-{
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
 
 __device__ __forceinline__ float bwd_rcp_approx(float x)
 {
@@ -677,7 +671,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         l2[4 * u + 3] = v4.w;
                     }
                     tmem_wait_ld();
-                    uint32_t pt[16];  // soft-capping: this chunk's P for TMEM
+                    [[maybe_unused]] uint32_t pt[16];  // soft-capping: this chunk's P for TMEM
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float b0 = -l2[e], b1 = -l2[e + 1];
@@ -688,7 +682,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             b0 = fmaf(-alibi_l2, fabsf(d0), b0);
                             b1 = fmaf(-alibi_l2, fabsf(d0 + 1.f), b1);
                         }
-                        float p0, p1, g0 = 1.f, g1 = 1.f;
+                        float p0, p1;
+                        [[maybe_unused]] float g0 = 1.f, g1 = 1.f;  // soft-capping: dt/ds
                         if constexpr (var_softcap(VAR)) {
                             // t = cap tanh(s scale / cap) with tanh(u) = 1 - 2 rho,
                             // rho = 1 / (1 + e^(2u)); dt/ds = 1 - tanh^2 = 4 rho (1 - rho)

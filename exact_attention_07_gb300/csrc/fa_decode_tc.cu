@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
     constexpr int kLanesPerRow = 32 / RG;  // lanes that end a transposing reduction with the same row
     constexpr int kThreads = tc_threads(NR);
     constexpr int wProd = 4 * NG, wMmaS = 4 * NG + 1, wMmaPV = 4 * NG + 2;  // warp roles after the softmax
+    static_assert(wMmaPV == kThreads / 32 - 1, "the O^T MMA warp is the last");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);

@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the tensor-memory load also returns each chunk's maximum when the
                 // raw score order is the order the row maximum needs
                 constexpr bool kHwMax = VAR == kVarNone || VAR == kVarWindow || VAR == kVarFp8;
-                float hmx[4];
+                float hmx[4] = {0.f, 0.f, 0.f, 0.f};  // set by the loads when kHwMax
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if constexpr (kHwMax)

@@ -913,14 +913,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int s = 0; s < w.steps; ++s, ++gstep) {
                 const uint32_t qs = gstep % L::kQStages;
                 const uint64_t q_mn = smem_desc_sw128(sb + L::kQ + qs * L::kTile, kHalf, 1024);
-                // dP^T = V dO^T; its columns held the previous step's dQ.  The waits of
-                // the MMA warp are tested together first (one shared-memory round trip
-                // when, as usual, the phases have completed), then one by one.
-                const bool ready1 = __all_sync(0xffffffffu, bwd_try_wait3(bar(L::bDQEmpty), (gstep & 1u) ^ 1u,
-                                                                          bar(L::bDOFull), gstep & 1u,
-                                                                          bar(L::bDOFull), gstep & 1u));
+                // dP^T = V dO^T.  At D = 128 its columns held the previous step's dQ,
+                // so it waits for the dQ read-out; at D = 64 dQ has columns of its own
+                // and only the dQ MMAs below wait for it, which takes the read-out
+                // off the step's chain.  The waits of the MMA warp are tested
+                // together first (one shared-memory round trip when, as usual, the
+                // phases have completed), then one by one.
+                constexpr bool kDQOwnCols = kColDQ != kColDP;
+                const bool ready1 = __all_sync(
+                    0xffffffffu, bwd_try_wait3(kDQOwnCols ? bar(L::bDOFull) : bar(L::bDQEmpty),
+                                               kDQOwnCols ? (gstep & 1u) : ((gstep & 1u) ^ 1u), bar(L::bDOFull),
+                                               gstep & 1u, bar(L::bDOFull), gstep & 1u));
                 if (!ready1) {
-                    if (!(ok = bwd_warp_wait(bar(L::bDQEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 91, it))) break;
+                    if (!kDQOwnCols &&
+                        !(ok = bwd_warp_wait(bar(L::bDQEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 91, it)))
+                        break;
                     if (!(ok = bwd_warp_wait(bar(L::bDOFull), gstep & 1u, abort_flag, wf, 101, it))) break;
                 }
                 tc_fence_after_sync();
@@ -968,18 +975,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // dK += dS^T Q and dQ = dS K
                 if (!(ok = bwd_warp_wait(bar(L::bDSFull), gstep & 1u, abort_flag, wf, 94, it))) break;
                 tc_fence_after_sync();
-                if (leader) {
-                    // dK += dS^T Q with A = dS^T from tensor memory (the P/dS warps' copy
-                    // in the dP^T columns), which saves its shared-memory reads
+                // dK += dS^T Q with A = dS^T from tensor memory (the P/dS warps' copy
+                // in the dP^T columns), which saves its shared-memory reads; dQ = dS K
+                // with the query rows on the TMEM lanes (A = dS and B = K both
+                // MN-major), so that each dQ thread holds one row
+                auto mma_dk = [&] {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ts(tm + kColDK, tm + kColDP + (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)), q_mn + mnmaj(kk),
                                kIdBmn, (s > 0 || kk > 0) ? 1u : 0u);
-                    // dQ = dS K with the query rows on the TMEM lanes (A = dS and B = K
-                    // both MN-major), so that each dQ thread holds one row
+                };
+                auto mma_dq = [&] {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ss(tm + kColDQ, dS_mn + mnmaj(kk), dK_mn + mnmaj(kk), kIdDQ, kk > 0);
+                };
+                if constexpr (kDQOwnCols) {
+                    if (leader) mma_dk();
+                    __syncwarp();
+                    // the previous dQ must have left its columns
+                    if (!(ok = bwd_warp_wait(bar(L::bDQEmpty), (gstep & 1u) ^ 1u, abort_flag, wf, 91, it))) break;
+                    if (leader) mma_dq();
+                } else {
+                    if (leader) {
+                        mma_dk();
+                        mma_dq();
+                    }
                 }
                 __syncwarp();
                 commit(L::bDQFull);  // the dQ warps then free dS^T and Q (stage qs)

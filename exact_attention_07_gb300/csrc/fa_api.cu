@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -177,6 +178,23 @@ int prepare_variant(const fa_variant_t* var, int D, float scale, FwdParams* p)
     return var->alibi_slopes ? kVarAlibi : kVarWindow;
 }
 
+// Key windows: whether the last 256-row block of an Lq x Lk problem sees at
+// least as many KV tiles as the first (a causal-like window), in which case
+// the kernel takes row blocks from the last, longest first (the same window
+// arithmetic as the kernel's tile decoding).
+int window_tiles_desc(const FwdParams& p, long long Lq, long long Lk)
+{
+    if (Lq <= 0 || Lk <= 0) return 0;
+    auto kv_tiles = [&](long long m0) -> long long {
+        const long long off = Lk - Lq, last_row = std::min(m0 + kRowsPerCta - 1, Lq - 1);
+        const long long lo = p.win_left >= 0 ? std::max(0ll, m0 + off - p.win_left) : 0;
+        const long long hi = p.win_right >= 0 ? std::min(Lk - 1, last_row + off + p.win_right) : Lk - 1;
+        return hi < lo ? 0 : hi / kBlockN - lo / kBlockN + 1;
+    };
+    const long long last_m0 = (Lq - 1) / kRowsPerCta * kRowsPerCta;
+    return kv_tiles(last_m0) >= kv_tiles(0) ? 1 : 0;
+}
+
 // (D, Dv) must satisfy hdim_supported()
 template <bool VARLEN>
 cudaError_t dispatch(int D, bool causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
@@ -348,6 +366,7 @@ fa_status_t fwd_dense(const void* q, const void* k, const void* v, float* o, flo
     if (variant) {
         var = prepare_variant(variant, D, softmax_scale, &p);
         if (var < 0) return (fa_status_t)(-var);
+        p.desc_tiles = window_tiles_desc(p, Lq, Lk);
     }
     DeviceState* ds = nullptr;
     fa_status_t st = device_state(&ds);
@@ -466,6 +485,7 @@ fa_status_t fwd_varlen(const void* q, const void* k, const void* v, float* o, fl
     if (variant) {
         var = prepare_variant(variant, D, softmax_scale, &p);
         if (var < 0) return (fa_status_t)(-var);
+        p.desc_tiles = window_tiles_desc(p, max_seqlen_q, max_seqlen_k);  // the longest sequence's profile
     }
     if (fixed_scratch && num_seqs > kNoAllocMaxSeqs) return FA_ERR_INVALID_ARG;  // the fixed array holds no more
     DeviceState* ds = nullptr;

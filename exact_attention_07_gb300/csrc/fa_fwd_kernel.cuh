@@ -310,7 +310,7 @@ __device__ __forceinline__ Work decode_tile(const FwdParams& p, uint32_t sched_s
     const int rem3 = rem2 - i * hs_cur * PG;
     w.hkv = sec * hs + rem3 / PG;
     w.hq = w.hkv * G + (pair ? 2 * (rem3 % PG) : rem3 % PG);
-    const int mb = CAUSAL ? (nmb - 1 - i) : i;
+    const int mb = (CAUSAL || (var_window(VAR) && p.desc_tiles)) ? (nmb - 1 - i) : i;
     w.m0 = mb * tile_rows;
     w.rstep = pair ? 0 : kBlockM;
     w.hstep = pair ? 1 : 0;

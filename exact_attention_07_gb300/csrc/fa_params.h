@@ -17,6 +17,9 @@ struct FwdParams {
     // 1: a work tile is two query heads of one KV head over the same 128 rows
     // (causal, even GQA groups); 0: one query head over 256 rows
     int pair_heads;
+    // key windows: 1 = row blocks from the last (when later blocks see at
+    // least as many keys, so that the longest tiles come first), 0 = from the first
+    int desc_tiles;
     // variable-length batches
     const int* cu_q;
     const int* cu_k;
